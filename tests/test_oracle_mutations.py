@@ -1,0 +1,51 @@
+"""Plant plausible mistakes in a copy of the oracle and check that the pins catch each one.
+
+Every mutant is compiled from ``oracle/msa_oracle.c`` with one textual change, loaded in place of
+the real oracle, and run through a few pins; at least one must fail.  This is what makes the pins
+worth trusting: a dropped term, a wrong sign or index, or a flipped tie rule cannot pass them.
+"""
+import pytest
+
+import oracle
+from tests import test_oracle_pins as pins
+
+MUTANTS = {
+    "dS sign": ("dS[a] = Ph[a] * (dP - Drow);", "dS[a] = Ph[a] * (dP + Drow);"),
+    "local block not forced": ("c[m] = INFINITY;", "c[m] = -INFINITY;"),
+    "tie rule flipped": ("return n1 < n2;", "return n1 > n2;"),
+    "KL gradient sign": ("const double dz = cz * (p_px - pbar[a]);",
+                         "const double dz = cz * (pbar[a] - p_px);"),
+    "causal cut dropped": ("j < (n + 1) * MSA_ORACLE_BLOCK && j <= t;",
+                           "j < (n + 1) * MSA_ORACLE_BLOCK;"),
+    "dKp from the wrong operand": ("acc[d] += scale * dz * qprow[d];",
+                                   "acc[d] += scale * dz * kprow[d];"),
+    "teacher not averaged": ("pbar[a] += Ph[a] / G;", "pbar[a] += Ph[a];"),
+    "scale dropped in dQ": ("dqrow[d] += scale * dS[a] * krow[d];",
+                            "dqrow[d] += dS[a] * krow[d];"),
+    "block max over a shifted block": ("for (int j = n * MSA_ORACLE_BLOCK; j < (n + 1) * MSA_ORACLE_BLOCK; ++j) {\n      double z",
+                                       "for (int j = n * MSA_ORACLE_BLOCK + 1; j < (n + 1) * MSA_ORACLE_BLOCK; ++j) {\n      double z"),
+}
+
+PINS = [
+    lambda: pins.test_selection_brute_force_properties(3, B=1, S=512),
+    lambda: pins.test_selection_ties_prefer_lower_block(),
+    lambda: pins.test_full_selection_is_dense_causal_attention(False),
+    lambda: pins.test_finite_differences_every_gradient(False, n_coords=2),
+    lambda: pins.test_kl_zero_when_student_equals_teacher(2),
+]
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = oracle.source()
+    assert src.count(old) == 1, f"mutation anchor for {name!r} not unique"
+    lib = oracle.compile_variant(src.replace(old, new), str(tmp_path / "mutant.so"))
+    caught = []
+    with oracle.use_library(lib):
+        for pin in PINS:
+            try:
+                pin()
+            except AssertionError:
+                caught.append(pin)
+    assert caught, f"no pin caught the planted mistake: {name}"
