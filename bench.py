@@ -1,0 +1,383 @@
+"""Benchmark: MSA training step (sparse forward + backward) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload msa_s64k_planted] [--no-cpu-baseline] [--no-e2e]
+
+One step = msa_forward (proxy top-k selection + sparse attention) followed by msa_backward
+(dQ, dK, dV, dQp, dKp) on one batch of the workload, inputs resident in HBM.  Prints one JSON
+line (rank 0).  N > 1 ranks (torchrun) each process their own batch: weak scaling, no data-path
+collective; the time is the max over ranks.
+
+--impl reference times the fp64 CPU oracle on the host cores over a bounded sample of the same
+workload (tokens/s extrapolated from the sample), as the slow reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from block_sparse_attention_qp_gb300 import dist, flops  # noqa: E402
+from block_sparse_attention_qp_gb300.inputs import WORKLOADS, make_inputs, workload_seed  # noqa: E402
+
+METRIC = "MSA fwd+bwd tokens/s & TFLOP/s at 64K ctx; % of GB300 dense bf16 peak"
+UNIT = "tokens/s"
+L2_BYTES = 129 * 2 ** 20
+
+
+def workload_by_name(name):
+    for i, w in enumerate(WORKLOADS):
+        if w.name == name:
+            return i + 1, w
+    raise SystemExit(f"unknown workload {name}; choose from {[w.name for w in WORKLOADS]}")
+
+
+def config_of(w, inputs_bytes):
+    return {"workload": w.name, "desc": w.describe(), "B": w.B, "S": w.S, "Hq": w.Hq,
+            "Hkv": w.Hkv, "Hp": w.Hp, "d": w.D, "top_k": w.top_k, "block": 128,
+            "planted_blocks": w.planted, "scale": w.scale,
+            "l2": f"inputs larger than L2 ({inputs_bytes / 2**20:.0f} MiB > 129 MiB); no flush"}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "of measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "of fallback"
+
+
+# ------------------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.samples = []
+        if self.proc is None:
+            return False
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append(parts)
+        return False
+
+    def summary(self):
+        if not getattr(self, "samples", None):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+        mx = [float(s[2]) for s in self.samples if s[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in self.samples for i in range(4)
+                          if s[5 + i].lower() == "active"})
+        pw = [float(s[3]) for s in self.samples if s[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "power_w_max": max(pw) if pw else None, "samples": len(self.samples)}
+
+
+# ------------------------------------------------------------------------------ oracle sample
+def oracle_sample(w, x64, idx_rows_fn, tokens, threads=None):
+    """Time the fp64 oracle on `tokens` (b, t) of workload w: their selection rows, their
+    forward rows and their exact share of every gradient.  Returns seconds."""
+    import oracle
+
+    if threads:
+        oracle.set_threads(threads)
+    B, S = w.B, w.S
+    t0 = time.perf_counter()
+    rows = np.array([(b, g, t) for (b, t) in tokens for g in range(w.Hp)], np.int32)
+    sel, _ = oracle.select(x64["qp"], x64["kp"], w.top_k, w.scale, rows=rows)
+    idx = idx_rows_fn(rows, sel)
+    frows = np.array([(b, t, h) for (b, t) in tokens for h in range(w.Hq)], np.int32)
+    oracle.forward(x64["q"], x64["k"], x64["v"], idx, w.top_k, w.scale, rows=frows, Hp=w.Hp)
+    mask = np.zeros((B, S), bool)
+    for b, t in tokens:
+        mask[b, t] = True
+    oracle.backward(x64["q"], x64["k"], x64["v"], x64["qp"], x64["kp"], x64["dout"], idx,
+                    w.top_k, w.scale, tok_mask=mask, only_masked=True)
+    return time.perf_counter() - t0
+
+
+def oracle_inputs(w, seed):
+    import oracle
+
+    x = make_inputs(w, seed)
+    return {k: oracle.f64(v) for k, v in x.items() if isinstance(v, torch.Tensor)}
+
+
+def idx_builder(w):
+    """Sparse index map holding only the sampled rows (others -1: they are not visited)."""
+    def build(rows, sel):
+        idx = np.full((w.B, w.Hp, w.S, w.top_k), -1, np.int32)
+        idx[rows[:, 0], rows[:, 1], rows[:, 2]] = sel
+        return idx
+    return build
+
+
+def sample_tokens(w, n, rng):
+    """Token positions spread over the sequence (the oracle's per-token cost grows with t)."""
+    ts = rng.choice(w.S, size=n, replace=False)
+    bs = rng.integers(0, w.B, size=n)
+    return sorted(zip(bs.tolist(), ts.tolist()))
+
+
+def run_reference(args, w, wi):
+    world, rank, _ = dist.env_world()
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    threads = oracle.threads()
+    x64 = oracle_inputs(w, workload_seed(wi))
+    rng = np.random.default_rng(0)
+    n_tok = args.ref_tokens
+    build = idx_builder(w)
+    times = []
+    for step in range(args.warmup + args.steps):
+        toks = sample_tokens(w, n_tok, rng)
+        dt = oracle_sample(w, x64, build, toks)
+        if step >= args.warmup:
+            times.append(dt)
+    sec = sum(times) / len(times)
+    value = n_tok / sec
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(w, 0),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": f"{n_tok} random tokens per step (all {w.Hp} groups, "
+                                       f"{w.Hq} heads): selection rows, forward rows and their "
+                                       f"exact share of every gradient"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------------------ our arm
+KERNEL_WORK = {
+    # kernel name -> (bound, function(workload) -> algorithmic FLOPs per launch)
+    "proxy_topk": ("tensor", lambda w: 2 * w.D * flops.n_px(w.S) * w.Hp * w.B),
+    "sparse_fwd": ("tensor", lambda w: 4 * w.D * flops.n_sel(w.S, w.top_k) * w.Hq * w.B),
+    "fused_bwd": ("tensor", lambda w: (10 * w.Hq + 6 * w.Hp) * w.D * flops.n_sel(w.S, w.top_k) * w.B),
+    "proxy_lse": ("tensor", lambda w: 2 * w.D * flops.n_sel(w.S, w.top_k) * w.Hp * w.B),
+}
+
+
+def src_hash(*files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_record(kernel, w):
+    """DRAM bytes per launch from the committed ncu summary, if it matches this kernel build."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        recs = json.load(f)
+    r = recs.get(kernel)
+    if not r or r.get("workload") != w.name:
+        return None
+    if r.get("src_hash") != src_hash(*r.get("src_files", [])):
+        return None  # kernel changed since the counters were taken
+    return r.get("dram_bytes_per_launch")
+
+
+def run_ours(args, w, wi):
+    from block_sparse_attention_qp_gb300 import binding as msa
+
+    world, rank, local = dist.init("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    msa.load_library()
+    x = make_inputs(w, dist.rank_seed(workload_seed(wi), rank))
+    names = ("q", "k", "v", "qp", "kp", "dout")
+    g = {n: x[n].to(dev) for n in names}
+    inputs_bytes = sum(g[n].numel() * 2 for n in names)
+    shape = msa.make_shape(g["q"], g["k"], g["qp"], w.top_k, w.scale)
+    ws_f = msa.workspace(shape, msa.OP_FORWARD, dev)
+    ws_b = msa.workspace(shape, msa.OP_BACKWARD, dev)
+    def full_step(src):
+        o, lse, bi = msa.msa_forward(src["q"], src["k"], src["v"], src["qp"], src["kp"], w.top_k,
+                                     w.scale, ws=ws_f)
+        grads = msa.msa_backward(src["q"], src["k"], src["v"], src["qp"], src["kp"], o, lse,
+                                 src["dout"], bi, w.top_k, w.scale, ws=ws_b)
+        return (o, bi) + tuple(grads)
+
+    for _ in range(args.warmup):
+        full_step(g)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        msa.profile_begin()
+        n0 = msa.launch_count()
+        e0.record(stream)
+        for _ in range(args.steps):
+            full_step(g)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        launches = msa.launch_count() - n0
+        prof = msa.profile_end()
+    dist.barrier()
+    sec = e0.elapsed_time(e1) / 1e3
+    sec_max = dist.max_over_ranks(sec, device=dev)
+    tok = w.B * w.S
+    value = dist.whole_job_rate(tok * args.steps, world, sec_max)
+    fl = flops.step_flops(w.B, w.S, w.Hq, w.Hp, w.top_k, w.D)
+    tflops = fl["total"] * args.steps * world / sec_max / 1e12
+    peaks, peak_src = measured_peaks()
+
+    # dominant kernel and its roofline
+    dom = max(prof.items(), key=lambda kv: kv[1][1])
+    dname, (dn, dms) = dom
+    per_launch_s = dms / dn / 1e3
+    bound, work = KERNEL_WORK.get(dname, ("tensor", None))
+    roof = None
+    if work is not None:
+        achieved = work(w) / per_launch_s / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        roof = {"kernel": dname, "bound": bound, "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic_record(dname, w),
+                "ms_per_launch": per_launch_s * 1e3,
+                "peak_note": f"dense bf16 sustained {peak_src} (kernel timed inside a long step)"}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(args, w, g, full_step, dev)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, wi, args)
+
+    if rank == 0:
+        kernels = {k: {"launches_per_step": n / args.steps, "ms_per_step": ms / args.steps}
+                   for k, (n, ms) in sorted(prof.items(), key=lambda kv: -kv[1][1])}
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": sec_max / args.steps * 1e3, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": config_of(w, inputs_bytes),
+                "tflops": tflops,
+                "frac_of_dense_bf16_peak": {
+                    "burst": tflops / world / peaks["bf16_tflops"],
+                    "sustained": tflops / world / peaks["bf16_tflops_sustained"],
+                    "note": f"sparse-counted FLOPs, {peak_src}"},
+                "flops_per_step": fl,
+                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": launches, "kernels": kernels, "clocks": clk.summary()}
+        print(json.dumps(line), flush=True)
+    dist.shutdown()
+
+
+def measure_e2e(args, w, g, full_step, dev):
+    """Same step through the public API with host buffers: pinned H2D copies of the inputs and
+    D2H copies of every result inside the timed region."""
+    names = ("q", "k", "v", "qp", "kp", "dout")
+    host = {n: g[n].to("cpu").pin_memory() for n in names}
+    dst = {n: torch.empty_like(g[n]) for n in names}
+    outs = full_step(g)
+    host_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+    d2h = sum(o.numel() * o.element_size() for o in outs)
+    steps = max(1, min(args.steps, 3))
+    stream = torch.cuda.current_stream(dev)
+
+    def one():
+        for n in names:
+            dst[n].copy_(host[n], non_blocking=True)
+        res = full_step(dst)
+        for ho, r in zip(host_out, res):
+            ho.copy_(r, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sec = e0.elapsed_time(e1) / 1e3
+    return {"value": w.B * w.S * steps / sec, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+def cpu_baseline(w, wi, args):
+    import oracle
+
+    oracle.build()
+    x64 = oracle_inputs(w, workload_seed(wi))
+    rng = np.random.default_rng(1)
+    toks = sample_tokens(w, args.ref_tokens, rng)
+    sec = oracle_sample(w, x64, idx_builder(w), toks)
+    return {"value": len(toks) / sec, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
+            "sample": f"{len(toks)} random tokens of {w.name} (all {w.Hp} groups, {w.Hq} heads): "
+                      f"selection rows, forward rows, exact share of every gradient; "
+                      f"{sec:.1f} s"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="msa_s64k_planted")
+    ap.add_argument("--ref-tokens", type=int, default=24)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        print("bench: raising --warmup to the minimum of 3", file=sys.stderr)
+        args.warmup = 3
+    wi, w = workload_by_name(args.workload)
+    if args.impl == "reference":
+        run_reference(args, w, wi)
+    else:
+        run_ours(args, w, wi)
+
+
+if __name__ == "__main__":
+    main()

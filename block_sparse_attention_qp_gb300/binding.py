@@ -1,0 +1,269 @@
+"""Thin Python binding of libmsa.so (C ABI in include/msa.h).
+
+Argument marshalling only: every step of the method runs in the CUDA library.  PyTorch supplies
+device memory (tensors and the workspace) and the current stream.  There is no fallback: if the
+library is missing or fails to load, every call raises.
+
+Entry points (same names as the C ABI):
+  msa_forward, msa_backward, msa_warmup_forward, msa_warmup_backward, msa_device_status,
+  msa_workspace_size.
+And the autograd pair mirroring the package API of Flash-MSA (``flash_msa_func`` /
+``flash_msa_warmup_func``, PyPI page "Usage"): ``msa_func`` and ``msa_warmup_func`` return
+``(attn_out, kl_loss)`` where kl_loss is a zero placeholder whose gradient drives the proxy
+heads in the backward.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmsa.so")
+
+OP_FORWARD, OP_BACKWARD, OP_WARMUP_FORWARD, OP_WARMUP_BACKWARD = 0, 1, 2, 3
+STATUS_BITS = {1: "bad block index", 2: "work list overflow", 4: "device wait timeout"}
+_SYMBOLS = ("msa_workspace_size", "msa_forward", "msa_backward", "msa_warmup_forward",
+            "msa_warmup_backward", "msa_device_status", "msa_status_string", "msa_last_error",
+            "msa_profile_begin", "msa_profile_end", "msa_launch_count")
+
+
+class MSAError(RuntimeError):
+    pass
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("S", ctypes.c_int32), ("Hq", ctypes.c_int32),
+                ("Hkv", ctypes.c_int32), ("Hp", ctypes.c_int32), ("D", ctypes.c_int32),
+                ("top_k", ctypes.c_int32), ("scale", ctypes.c_float)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libmsa.so (raises MSAError if it is missing: there is no CPU fallback)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise MSAError(f"{path} not found: build it with block_sparse_attention_qp_gb300.build")
+        lib = ctypes.CDLL(path)
+        P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        SP = ctypes.POINTER(Shape)
+        lib.msa_workspace_size.argtypes = [SP, I]
+        lib.msa_workspace_size.restype = Z
+        lib.msa_forward.argtypes = [SP, P, P, P, P, P, P, I, P, P, P, Z, P]
+        lib.msa_backward.argtypes = [SP, P, P, P, P, P, P, P, P, P, F, P, P, P, P, P, P, Z, P]
+        lib.msa_warmup_forward.argtypes = [SP, P, P, P, P, P, P, Z, P]
+        lib.msa_warmup_backward.argtypes = [SP, P, P, P, P, P, P, P, P, F, P, P, P, P, P, P, Z, P]
+        lib.msa_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint), P]
+        lib.msa_status_string.argtypes = [I]
+        lib.msa_status_string.restype = ctypes.c_char_p
+        lib.msa_last_error.restype = ctypes.c_char_p
+        for name in ("msa_forward", "msa_backward", "msa_warmup_forward", "msa_warmup_backward",
+                     "msa_device_status", "msa_profile_begin", "msa_profile_end"):
+            getattr(lib, name).restype = I
+        lib.msa_profile_end.argtypes = [ctypes.c_char_p, Z]
+        lib.msa_launch_count.restype = ctypes.c_longlong
+        _lib = lib
+        return lib
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        lib = load_library()
+        raise MSAError(f"{what}: {lib.msa_status_string(rc).decode()} "
+                       f"({lib.msa_last_error().decode()})")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _req(t, name, dtype=torch.bfloat16, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a tensor")
+    if not t.is_cuda:
+        raise MSAError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise MSAError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise MSAError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise MSAError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def make_shape(q, k, qp, top_k, scale) -> Shape:
+    B, S, Hq, D = q.shape
+    Hkv = k.shape[2]
+    Hp = qp.shape[2] if qp is not None else Hkv
+    return Shape(B, S, Hq, Hkv, Hp, D, int(top_k), float(scale))
+
+
+def msa_workspace_size(shape: Shape, op: int) -> int:
+    n = load_library().msa_workspace_size(ctypes.byref(shape), op)
+    if n == 0:
+        raise MSAError(f"unsupported shape for op {op}: "
+                       f"{load_library().msa_last_error().decode()}")
+    return int(n)
+
+
+def workspace(shape: Shape, op: int, device) -> torch.Tensor:
+    """Fresh workspace (uint8 tensor, 256-byte aligned by the CUDA caching allocator)."""
+    return torch.empty(msa_workspace_size(shape, op), dtype=torch.uint8, device=device)
+
+
+def msa_device_status(ws: torch.Tensor) -> int:
+    """Read and clear the device status word of a workspace (synchronises the stream)."""
+    flags = ctypes.c_uint(0)
+    _check(load_library().msa_device_status(_ptr(ws), ctypes.byref(flags), _stream(ws.device)),
+           "msa_device_status")
+    return int(flags.value)
+
+
+def profile_begin() -> None:
+    """Start per-kernel CUDA-event timing inside the library (measurement aid)."""
+    _check(load_library().msa_profile_begin(), "msa_profile_begin")
+
+
+def profile_end() -> dict:
+    """Stop timing; returns {kernel name: (launches, total milliseconds)}."""
+    buf = ctypes.create_string_buffer(1 << 16)
+    _check(load_library().msa_profile_end(buf, len(buf)), "msa_profile_end")
+    out = {}
+    for line in buf.value.decode().splitlines():
+        name, n, ms = line.split()
+        out[name] = (int(n), float(ms))
+    return out
+
+
+def launch_count() -> int:
+    """Kernels launched by the library since it was loaded."""
+    return int(load_library().msa_launch_count())
+
+
+def msa_forward(q, k, v, qp, kp, top_k: int, scale: float, block_idx=None, ws=None):
+    """Sparse forward.  Returns (o, lse, block_idx).  block_idx given -> used as the selection."""
+    B, S, Hq, D = q.shape
+    Hkv, Hp = k.shape[2], qp.shape[2]
+    for t, n, shp in ((q, "q", None), (k, "k", (B, S, Hkv, D)), (v, "v", (B, S, Hkv, D)),
+                      (qp, "qp", (B, S, Hp, D)), (kp, "kp", (B, S, 1, D))):
+        _req(t, n, shape=shp)
+    shape = make_shape(q, k, qp, top_k, scale)
+    given = block_idx is not None
+    if given:
+        _req(block_idx, "block_idx", torch.int32, (B, Hp, S, top_k))
+    else:
+        block_idx = torch.empty((B, Hp, S, top_k), dtype=torch.int32, device=q.device)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = workspace(shape, OP_FORWARD, q.device)
+    _check(load_library().msa_forward(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(qp),
+                                      _ptr(kp), _ptr(block_idx), int(given), _ptr(o), _ptr(lse),
+                                      _ptr(ws), ws.numel(), _stream(q.device)), "msa_forward")
+    return o, lse, block_idx
+
+
+def msa_backward(q, k, v, qp, kp, o, lse, dout, block_idx, top_k: int, scale: float,
+                 kl_grad: float = 1.0, ws=None):
+    """Sparse backward.  Returns (dq, dk, dv, dqp, dkp)."""
+    B, S, Hq, D = q.shape
+    Hp = qp.shape[2]
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (qp, "qp"), (kp, "kp"), (o, "o"), (dout, "dout")):
+        _req(t, n)
+    _req(lse, "lse", torch.float32, (B, Hq, S))
+    _req(block_idx, "block_idx", torch.int32, (B, Hp, S, top_k))
+    shape = make_shape(q, k, qp, top_k, scale)
+    grads = [torch.empty_like(x) for x in (q, k, v, qp, kp)]
+    if ws is None:
+        ws = workspace(shape, OP_BACKWARD, q.device)
+    _check(load_library().msa_backward(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(qp),
+                                       _ptr(kp), _ptr(o), _ptr(lse), _ptr(dout), _ptr(block_idx),
+                                       float(kl_grad), *map(_ptr, grads), _ptr(ws), ws.numel(),
+                                       _stream(q.device)), "msa_backward")
+    return tuple(grads)
+
+
+def msa_warmup_forward(q, k, v, scale: float, ws=None):
+    """Dense causal forward (warmup).  Returns (o, lse)."""
+    B, S, Hq, D = q.shape
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _req(t, n)
+    shape = make_shape(q, k, None, 0, scale)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = workspace(shape, OP_WARMUP_FORWARD, q.device)
+    _check(load_library().msa_warmup_forward(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v),
+                                             _ptr(o), _ptr(lse), _ptr(ws), ws.numel(),
+                                             _stream(q.device)), "msa_warmup_forward")
+    return o, lse
+
+
+def msa_warmup_backward(q, k, v, qp, kp, o, lse, dout, scale: float, kl_grad: float = 1.0,
+                        ws=None):
+    """Dense warmup backward (proxy KL over the full causal prefix).  Returns grads."""
+    B, S, Hq, D = q.shape
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (qp, "qp"), (kp, "kp"), (o, "o"), (dout, "dout")):
+        _req(t, n)
+    _req(lse, "lse", torch.float32, (B, Hq, S))
+    shape = make_shape(q, k, qp, 0, scale)
+    grads = [torch.empty_like(x) for x in (q, k, v, qp, kp)]
+    if ws is None:
+        ws = workspace(shape, OP_WARMUP_BACKWARD, q.device)
+    _check(load_library().msa_warmup_backward(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v),
+                                              _ptr(qp), _ptr(kp), _ptr(o), _ptr(lse), _ptr(dout),
+                                              float(kl_grad), *map(_ptr, grads), _ptr(ws),
+                                              ws.numel(), _stream(q.device)),
+           "msa_warmup_backward")
+    return tuple(grads)
+
+
+class _MSAFunction(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, qp, kp, q, k, v, top_k, scale, warmup):
+        qp, kp, q, k, v = (x.contiguous() for x in (qp, kp, q, k, v))
+        if warmup:
+            o, lse = msa_warmup_forward(q, k, v, scale)
+            idx = None
+        else:
+            o, lse, idx = msa_forward(q, k, v, qp, kp, top_k, scale)
+        ctx.save_for_backward(qp, kp, q, k, v, o, lse, *(() if idx is None else (idx,)))
+        ctx.top_k, ctx.scale, ctx.warmup = top_k, scale, warmup
+        kl = torch.zeros((), dtype=torch.float32, device=q.device)
+        return o, kl
+
+    @staticmethod
+    def backward(ctx, do, dkl):
+        saved = ctx.saved_tensors
+        qp, kp, q, k, v, o, lse = saved[:7]
+        kl_grad = 0.0 if dkl is None else float(dkl)
+        do = torch.zeros_like(o) if do is None else do.contiguous()
+        if ctx.warmup:
+            dq, dk, dv, dqp, dkp = msa_warmup_backward(q, k, v, qp, kp, o, lse, do, ctx.scale,
+                                                       kl_grad)
+        else:
+            dq, dk, dv, dqp, dkp = msa_backward(q, k, v, qp, kp, o, lse, do, saved[7], ctx.top_k,
+                                                ctx.scale, kl_grad)
+        return dqp, dkp, dq, dk, dv, None, None, None
+
+
+def msa_func(Q_proxy, K_proxy, Q, K, V, top_k: int, scale: float):
+    """Sparse MSA attention with the Flash-MSA call convention.  Returns (attn_out, kl_loss);
+    add kl_loss to the training loss so that backward() trains the proxy heads."""
+    return _MSAFunction.apply(Q_proxy, K_proxy, Q, K, V, int(top_k), float(scale), False)
+
+
+def msa_warmup_func(Q_proxy, K_proxy, Q, K, V, top_k: int, scale: float):
+    """Warmup mode: dense main attention, proxy trained over the full causal prefix."""
+    return _MSAFunction.apply(Q_proxy, K_proxy, Q, K, V, int(top_k), float(scale), True)

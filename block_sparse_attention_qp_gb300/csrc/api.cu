@@ -1,0 +1,507 @@
+// C ABI of libmsa.so (declared in include/msa.h): argument validation, workspace carving and
+// the launch sequence of every entry point.  All work is queued on the caller's stream.
+#include <stdio.h>
+#include <string.h>
+
+#include <atomic>
+#include <map>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/msa.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace msa {
+namespace {
+
+thread_local char g_err[512] = "";
+
+void set_err(const char* what) {
+  snprintf(g_err, sizeof(g_err), "%s", what);
+}
+
+int cuda_fail(const char* where) {
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) return MSA_OK;
+  snprintf(g_err, sizeof(g_err), "%s: %s", where, cudaGetErrorString(e));
+  return MSA_ERR_CUDA;
+}
+
+// ---- launch accounting and optional per-kernel event timing
+std::atomic<long long> g_launches{0};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+struct ProfRec {
+  const char* name;
+  cudaEvent_t a, b;
+};
+std::vector<ProfRec> g_prof;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t pooled_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// Runs `launch` (which issues exactly one kernel on st), counting it and timing it if enabled.
+template <typename F>
+void timed(const char* name, cudaStream_t st, F&& launch) {
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (!g_prof_on) {
+    launch();
+    return;
+  }
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  ProfRec r{name, pooled_event(), pooled_event()};
+  cudaEventRecord(r.a, st);
+  launch();
+  cudaEventRecord(r.b, st);
+  g_prof.push_back(r);
+}
+
+constexpr int kBwdChunkTiles = 8;  // tiles per backward item (bounds per-item work)
+constexpr size_t kAlign = 256;
+
+size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+// Workspace layout of one op.  Offsets are bytes from the workspace base; 0 size = absent.
+struct Plan {
+  size_t status = 0, totals = 0, seg_count = 0, seg_offset = 0, seg_cursor = 0, entries = 0;
+  size_t io0 = 0, io1 = 0, items0 = 0, items1 = 0;
+  size_t opart = 0, lpart = 0, lpx_part = 0, lse_px = 0, drow = 0;
+  size_t dq = 0, dk = 0, dv = 0, dqp = 0, dkp = 0;
+  size_t bytes = 0;
+  long long max0 = 0, max1 = 0;
+  ItemSpec spec0{1, 1, 1}, spec1{1, 1, 1};
+};
+
+struct Carver {
+  size_t off = 0;
+  size_t take(size_t n) {
+    const size_t at = off;
+    off += up(n);
+    return at;
+  }
+};
+
+long long dense_entries(const Dims& d) {  // sum over blocks of S - 128 n, per (b, g)
+  return (long long)d.B * d.Hp * ((long long)d.S * d.nblk - (long long)kBlock * d.nblk * (d.nblk - 1) / 2);
+}
+
+long long max_items(long long entries, const Dims& d, const ItemSpec& s) {
+  return (long long)s.halves * (entries / ((long long)s.tile_tokens * s.chunk_tiles) + d.nseg() + 1);
+}
+
+Plan make_plan(const Dims& d, int op) {
+  Plan p;
+  Carver c;
+  const long long nseg = d.nseg();
+  const long long rows_q = (long long)d.B * d.S * d.Hq;
+  const long long rows_kv = (long long)d.B * d.S * d.Hkv;
+  const long long rows_p = (long long)d.B * d.S * d.Hp;
+  const long long rows_kp = (long long)d.B * d.S;
+  const long long sparse_ent = rows_p * d.top_k;
+  const int TT = kBlock / d.G;
+  p.status = c.take(256);
+  p.totals = c.take(4 * sizeof(int));
+  if (op == MSA_OP_FORWARD || op == MSA_OP_BACKWARD) {
+    p.seg_count = c.take(nseg * sizeof(int));
+    p.seg_offset = c.take((nseg + 1) * sizeof(int));
+    p.seg_cursor = c.take(nseg * sizeof(int));
+    p.entries = c.take(sparse_ent * sizeof(int));
+  }
+  if (op == MSA_OP_FORWARD) {
+    p.spec0 = ItemSpec{TT, 1, 1};
+    p.max0 = max_items(sparse_ent, d, p.spec0);
+    p.io0 = c.take(nseg * sizeof(int));
+    p.items0 = c.take(p.max0 * sizeof(Item));
+    p.opart = c.take((size_t)rows_q * d.top_k * kD * sizeof(bf16));
+    p.lpart = c.take((size_t)rows_q * d.top_k * sizeof(float));
+  }
+  if (op == MSA_OP_BACKWARD || op == MSA_OP_WARMUP_BACKWARD) {
+    const bool dense = op == MSA_OP_WARMUP_BACKWARD;
+    const long long ent = dense ? dense_entries(d) : sparse_ent;
+    if (dense) {
+      p.spec0 = ItemSpec{TT, kBwdChunkTiles, 2};  // fused backward items
+      p.max0 = max_items(ent, d, p.spec0);
+      p.io0 = c.take(nseg * sizeof(int));
+      p.items0 = c.take(p.max0 * sizeof(Item));
+    } else {
+      p.spec0 = ItemSpec{kBlock, 1, 1};  // proxy normaliser items
+      p.spec1 = ItemSpec{TT, kBwdChunkTiles, 2};  // fused backward items
+      p.max0 = max_items(ent, d, p.spec0);
+      p.max1 = max_items(ent, d, p.spec1);
+      p.io0 = c.take(nseg * sizeof(int));
+      p.io1 = c.take(nseg * sizeof(int));
+      p.items0 = c.take(p.max0 * sizeof(Item));
+      p.items1 = c.take(p.max1 * sizeof(Item));
+      p.lpx_part = c.take((size_t)rows_p * d.top_k * sizeof(float));
+    }
+    p.lse_px = c.take((size_t)rows_p * sizeof(float));
+    p.drow = c.take((size_t)rows_q * sizeof(float));
+    p.dq = c.take((size_t)rows_q * kD * sizeof(float));
+    p.dk = c.take((size_t)rows_kv * kD * sizeof(float));
+    p.dv = c.take((size_t)rows_kv * kD * sizeof(float));
+    p.dqp = c.take((size_t)rows_p * kD * sizeof(float));
+    p.dkp = c.take((size_t)rows_kp * kD * sizeof(float));
+  }
+  p.bytes = c.off;
+  return p;
+}
+
+// Shape checks shared by every op.  Returns MSA_OK or an error code (message set).
+int check_shape(const msa_shape_t* s, int op, Dims* out) {
+  if (!s) {
+    set_err("shape is null");
+    return MSA_ERR_INVALID_ARG;
+  }
+  if (s->B < 1 || s->S < 1 || s->Hq < 1 || s->Hkv < 1 || s->Hp < 1) {
+    set_err("B, S, Hq, Hkv and Hp must be positive");
+    return MSA_ERR_INVALID_ARG;
+  }
+  if (!(s->scale > 0.f)) {
+    set_err("scale must be positive and finite");
+    return MSA_ERR_INVALID_ARG;
+  }
+  if (s->D != kD) {
+    set_err("only head dim 128 is supported");
+    return MSA_ERR_UNSUPPORTED;
+  }
+  if (s->S % kBlock != 0 || s->S > (1 << 23)) {
+    set_err("S must be a multiple of 128 and at most 2^23");
+    return MSA_ERR_UNSUPPORTED;
+  }
+  if (s->Hp != s->Hkv) {
+    set_err("proxy heads must equal KV heads (one proxy head per GQA group)");
+    return MSA_ERR_UNSUPPORTED;
+  }
+  if (s->Hq % s->Hkv != 0) {
+    set_err("Hq must be a multiple of Hkv");
+    return MSA_ERR_UNSUPPORTED;
+  }
+  const int G = s->Hq / s->Hkv;
+  const bool bwd = op == MSA_OP_BACKWARD || op == MSA_OP_WARMUP_BACKWARD;
+  if (!(G == 1 || G == 2 || G == 4 || G == 8 || G == 16) || (bwd && G == 1)) {
+    set_err("group size Hq/Hkv must be 2, 4, 8 or 16 (1 also allowed in the forward ops)");
+    return MSA_ERR_UNSUPPORTED;
+  }
+  const bool sparse = op == MSA_OP_FORWARD || op == MSA_OP_BACKWARD;
+  if (sparse && (s->top_k < 1 || s->top_k > 64)) {
+    set_err("top_k must be in [1, 64]");
+    return MSA_ERR_UNSUPPORTED;
+  }
+  const long long rows = (long long)s->B * s->S * s->Hq;
+  if (rows * kD * (sparse ? s->top_k : 1) >= (1ll << 62)) {
+    set_err("problem too large");
+    return MSA_ERR_UNSUPPORTED;
+  }
+  if ((long long)s->B * s->Hp * s->S * (sparse ? s->top_k : 1) >= (1ll << 31)) {
+    set_err("B*Hp*S*top_k must stay below 2^31");
+    return MSA_ERR_UNSUPPORTED;
+  }
+  Dims d;
+  d.B = s->B;
+  d.S = s->S;
+  d.Hq = s->Hq;
+  d.Hkv = s->Hkv;
+  d.Hp = s->Hp;
+  d.G = G;
+  d.top_k = sparse ? s->top_k : 1;
+  d.nblk = s->S / kBlock;
+  d.scale = s->scale;
+  if (op == MSA_OP_WARMUP_BACKWARD && dense_entries(d) >= (1ll << 31)) {
+    set_err("B*Hp*S*S/256 must stay below 2^31 in the warmup backward");
+    return MSA_ERR_UNSUPPORTED;
+  }
+  *out = d;
+  return MSA_OK;
+}
+
+int check_ptrs(std::initializer_list<const void*> ptrs) {
+  for (const void* p : ptrs) {
+    if (!p) {
+      set_err("a required pointer is null");
+      return MSA_ERR_INVALID_ARG;
+    }
+    if (reinterpret_cast<uintptr_t>(p) % 16 != 0) {
+      set_err("every pointer must be 16-byte aligned");
+      return MSA_ERR_INVALID_ARG;
+    }
+  }
+  return MSA_OK;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+int check_ws(const Plan& p, void* ws, size_t bytes) {
+  if (!ws || reinterpret_cast<uintptr_t>(ws) % kAlign != 0) {
+    set_err("workspace must be non-null and 256-byte aligned");
+    return MSA_ERR_INVALID_ARG;
+  }
+  if (bytes < p.bytes) {
+    snprintf(g_err, sizeof(g_err), "workspace too small: %zu < %zu bytes", bytes, p.bytes);
+    return MSA_ERR_WORKSPACE;
+  }
+  return MSA_OK;
+}
+
+// Inverted block map + item lists shared by the sparse forward and backward.
+void build_lists(const Dims& d, const Plan& p, const int32_t* idx, void* ws, int nspecs,
+                 cudaStream_t st) {
+  unsigned* status = at<unsigned>(ws, p.status);
+  int* seg_count = at<int>(ws, p.seg_count);
+  int* seg_cursor = at<int>(ws, p.seg_cursor);
+  cudaMemsetAsync(seg_count, 0, d.nseg() * sizeof(int), st);
+  cudaMemsetAsync(seg_cursor, 0, d.nseg() * sizeof(int), st);
+  timed("invert_count", st, [&] { launch_count(d, idx, seg_count, status, st); });
+  const ItemSpec specs[2] = {p.spec0, p.spec1};
+  timed("invert_scan", st, [&] {
+    launch_scan(d, false, seg_count, at<int>(ws, p.seg_offset), specs, nspecs, at<int>(ws, p.io0),
+                nspecs > 1 ? at<int>(ws, p.io1) : nullptr, at<int>(ws, p.totals), st);
+  });
+  timed("invert_fill", st, [&] { launch_fill(d, idx, at<int>(ws, p.seg_offset), seg_cursor, at<int>(ws, p.entries), status, st); });
+  timed("work_items", st, [&] {
+    launch_items(d, false, seg_count, p.spec0, at<int>(ws, p.io0), at<Item>(ws, p.items0), p.max0,
+                 status, st);
+  });
+  if (nspecs > 1)
+    timed("work_items", st, [&] {
+      launch_items(d, false, seg_count, p.spec1, at<int>(ws, p.io1), at<Item>(ws, p.items1),
+                   p.max1, status, st);
+    });
+}
+
+void zero_grads(const Dims& d, const Plan& p, void* ws, cudaStream_t st) {
+  cudaMemsetAsync(at<char>(ws, p.dq), 0, (size_t)d.B * d.S * d.Hq * kD * sizeof(float), st);
+  cudaMemsetAsync(at<char>(ws, p.dk), 0, (size_t)d.B * d.S * d.Hkv * kD * sizeof(float), st);
+  cudaMemsetAsync(at<char>(ws, p.dv), 0, (size_t)d.B * d.S * d.Hkv * kD * sizeof(float), st);
+  cudaMemsetAsync(at<char>(ws, p.dqp), 0, (size_t)d.B * d.S * d.Hp * kD * sizeof(float), st);
+  cudaMemsetAsync(at<char>(ws, p.dkp), 0, (size_t)d.B * d.S * kD * sizeof(float), st);
+}
+
+void emit_grads(const Dims& d, const Plan& p, void* ws, void* dq, void* dk, void* dv, void* dqp,
+                void* dkp, cudaStream_t st) {
+  timed("grad_convert", st, [&] { launch_convert(at<float>(ws, p.dq), dq, (long long)d.B * d.S * d.Hq * kD, st); });
+  timed("grad_convert", st, [&] { launch_convert(at<float>(ws, p.dk), dk, (long long)d.B * d.S * d.Hkv * kD, st); });
+  timed("grad_convert", st, [&] { launch_convert(at<float>(ws, p.dv), dv, (long long)d.B * d.S * d.Hkv * kD, st); });
+  timed("grad_convert", st, [&] { launch_convert(at<float>(ws, p.dqp), dqp, (long long)d.B * d.S * d.Hp * kD, st); });
+  timed("grad_convert", st, [&] { launch_convert(at<float>(ws, p.dkp), dkp, (long long)d.B * d.S * kD, st); });
+}
+
+}  // namespace
+}  // namespace msa
+
+using namespace msa;
+
+extern "C" {
+
+size_t msa_workspace_size(const msa_shape_t* shape, int op) {
+  Dims d;
+  if (op < MSA_OP_FORWARD || op > MSA_OP_WARMUP_BACKWARD) return 0;
+  if (check_shape(shape, op, &d) != MSA_OK) return 0;
+  return make_plan(d, op).bytes;
+}
+
+int msa_forward(const msa_shape_t* shape, const void* q, const void* k, const void* v,
+                const void* qp, const void* kp, int32_t* block_idx, int indices_given, void* o,
+                float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  Dims d;
+  int rc = check_shape(shape, MSA_OP_FORWARD, &d);
+  if (rc) return rc;
+  if ((rc = check_ptrs({q, k, v, block_idx, o, lse}))) return rc;
+  if (!indices_given && (rc = check_ptrs({qp, kp}))) return rc;
+  const Plan p = make_plan(d, MSA_OP_FORWARD);
+  if ((rc = check_ws(p, workspace, workspace_bytes))) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaGetLastError();
+  cudaMemsetAsync(at<char>(workspace, p.status), 0, sizeof(unsigned), st);
+  if (!indices_given)
+    timed("proxy_topk", st, [&] { launch_proxy_topk(d, qp, kp, block_idx, st); });
+  build_lists(d, p, block_idx, workspace, 1, st);
+  timed("sparse_fwd", st, [&] {
+    launch_sparse_fwd(d, q, k, v, at<int>(workspace, p.seg_offset), at<int>(workspace, p.entries),
+                      at<Item>(workspace, p.items0), at<int>(workspace, p.totals) + 1, p.max0,
+                      at<void>(workspace, p.opart), at<float>(workspace, p.lpart), st);
+  });
+  timed("fwd_combine", st, [&] {
+    launch_combine(d, block_idx, at<void>(workspace, p.opart), at<float>(workspace, p.lpart), o,
+                   lse, st);
+  });
+  return cuda_fail("msa_forward");
+}
+
+int msa_backward(const msa_shape_t* shape, const void* q, const void* k, const void* v,
+                 const void* qp, const void* kp, const void* o, const float* lse,
+                 const void* dout, const int32_t* block_idx, float kl_grad, void* dq, void* dk,
+                 void* dv, void* dqp, void* dkp, void* workspace, size_t workspace_bytes,
+                 void* stream) {
+  Dims d;
+  int rc = check_shape(shape, MSA_OP_BACKWARD, &d);
+  if (rc) return rc;
+  if ((rc = check_ptrs({q, k, v, qp, kp, o, lse, dout, block_idx, dq, dk, dv, dqp, dkp}))) return rc;
+  const Plan p = make_plan(d, MSA_OP_BACKWARD);
+  if ((rc = check_ws(p, workspace, workspace_bytes))) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaGetLastError();
+  cudaMemsetAsync(at<char>(workspace, p.status), 0, sizeof(unsigned), st);
+  zero_grads(d, p, workspace, st);
+  build_lists(d, p, block_idx, workspace, 2, st);
+  timed("bwd_rowdot", st, [&] { launch_bwd_rowdot(d, o, dout, at<float>(workspace, p.drow), st); });
+  timed("proxy_lse", st, [&] {
+    launch_proxy_lse_sparse(d, qp, kp, at<int>(workspace, p.seg_offset),
+                            at<int>(workspace, p.entries), at<Item>(workspace, p.items0),
+                            at<int>(workspace, p.totals) + 1, p.max0,
+                            at<float>(workspace, p.lpx_part), st);
+  });
+  timed("proxy_lse_combine", st, [&] {
+    launch_proxy_lse_combine(d, block_idx, at<float>(workspace, p.lpx_part),
+                             at<float>(workspace, p.lse_px), st);
+  });
+  timed("fused_bwd", st, [&] { launch_fused_bwd(d, false, q, k, v, qp, kp, dout, lse, at<float>(workspace, p.drow),
+                   at<float>(workspace, p.lse_px), kl_grad, at<int>(workspace, p.seg_offset),
+                   at<int>(workspace, p.entries), at<Item>(workspace, p.items1),
+                   at<int>(workspace, p.totals) + 2, p.max1, at<float>(workspace, p.dq),
+                   at<float>(workspace, p.dk), at<float>(workspace, p.dv),
+                   at<float>(workspace, p.dqp), at<float>(workspace, p.dkp), st); });
+  emit_grads(d, p, workspace, dq, dk, dv, dqp, dkp, st);
+  return cuda_fail("msa_backward");
+}
+
+int msa_warmup_forward(const msa_shape_t* shape, const void* q, const void* k, const void* v,
+                       void* o, float* lse, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+  Dims d;
+  int rc = check_shape(shape, MSA_OP_WARMUP_FORWARD, &d);
+  if (rc) return rc;
+  if ((rc = check_ptrs({q, k, v, o, lse}))) return rc;
+  const Plan p = make_plan(d, MSA_OP_WARMUP_FORWARD);
+  if ((rc = check_ws(p, workspace, workspace_bytes))) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaGetLastError();
+  cudaMemsetAsync(at<char>(workspace, p.status), 0, sizeof(unsigned), st);
+  timed("dense_fwd", st, [&] { launch_dense_fwd(d, q, k, v, o, lse, st); });
+  return cuda_fail("msa_warmup_forward");
+}
+
+int msa_warmup_backward(const msa_shape_t* shape, const void* q, const void* k, const void* v,
+                        const void* qp, const void* kp, const void* o, const float* lse,
+                        const void* dout, float kl_grad, void* dq, void* dk, void* dv, void* dqp,
+                        void* dkp, void* workspace, size_t workspace_bytes, void* stream) {
+  Dims d;
+  int rc = check_shape(shape, MSA_OP_WARMUP_BACKWARD, &d);
+  if (rc) return rc;
+  if ((rc = check_ptrs({q, k, v, qp, kp, o, lse, dout, dq, dk, dv, dqp, dkp}))) return rc;
+  const Plan p = make_plan(d, MSA_OP_WARMUP_BACKWARD);
+  if ((rc = check_ws(p, workspace, workspace_bytes))) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaGetLastError();
+  unsigned* status = at<unsigned>(workspace, p.status);
+  cudaMemsetAsync(status, 0, sizeof(unsigned), st);
+  zero_grads(d, p, workspace, st);
+  const ItemSpec specs[1] = {p.spec0};
+  timed("invert_scan", st, [&] {
+    launch_scan(d, true, nullptr, nullptr, specs, 1, at<int>(workspace, p.io0), nullptr,
+                at<int>(workspace, p.totals), st);
+  });
+  timed("work_items", st, [&] {
+    launch_items(d, true, nullptr, p.spec0, at<int>(workspace, p.io0),
+                 at<Item>(workspace, p.items0), p.max0, status, st);
+  });
+  timed("bwd_rowdot", st, [&] { launch_bwd_rowdot(d, o, dout, at<float>(workspace, p.drow), st); });
+  timed("proxy_lse_dense", st, [&] { launch_proxy_lse_dense(d, qp, kp, at<float>(workspace, p.lse_px), st); });
+  timed("fused_bwd_dense", st, [&] { launch_fused_bwd(d, true, q, k, v, qp, kp, dout, lse, at<float>(workspace, p.drow),
+                   at<float>(workspace, p.lse_px), kl_grad, nullptr, nullptr,
+                   at<Item>(workspace, p.items0), at<int>(workspace, p.totals) + 1, p.max0,
+                   at<float>(workspace, p.dq), at<float>(workspace, p.dk),
+                   at<float>(workspace, p.dv), at<float>(workspace, p.dqp),
+                   at<float>(workspace, p.dkp), st); });
+  emit_grads(d, p, workspace, dq, dk, dv, dqp, dkp, st);
+  return cuda_fail("msa_warmup_backward");
+}
+
+int msa_device_status(void* workspace, unsigned* flags, void* stream) {
+  if (!workspace || !flags) {
+    set_err("workspace and flags must be non-null");
+    return MSA_ERR_INVALID_ARG;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned h = 0;
+  cudaGetLastError();
+  cudaMemcpyAsync(&h, workspace, sizeof(unsigned), cudaMemcpyDeviceToHost, st);
+  cudaMemsetAsync(workspace, 0, sizeof(unsigned), st);
+  cudaStreamSynchronize(st);
+  *flags = h;
+  return cuda_fail("msa_device_status");
+}
+
+const char* msa_status_string(int status) {
+  switch (status) {
+    case MSA_OK: return "ok";
+    case MSA_ERR_INVALID_ARG: return "invalid argument";
+    case MSA_ERR_UNSUPPORTED: return "unsupported shape";
+    case MSA_ERR_WORKSPACE: return "workspace too small";
+    case MSA_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}
+
+const char* msa_last_error(void) { return g_err; }
+
+int msa_profile_begin(void) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  for (auto& r : g_prof) {
+    g_event_pool.push_back(r.a);
+    g_event_pool.push_back(r.b);
+  }
+  g_prof.clear();
+  g_prof_on = true;
+  return MSA_OK;
+}
+
+int msa_profile_end(char* buf, size_t len) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_prof_on = false;
+  std::map<std::string, std::pair<long long, double>> agg;
+  std::vector<std::string> order;
+  for (auto& r : g_prof) {
+    if (cudaEventSynchronize(r.b) != cudaSuccess) return cuda_fail("msa_profile_end");
+    float ms = 0.f;
+    cudaEventElapsedTime(&ms, r.a, r.b);
+    auto it = agg.find(r.name);
+    if (it == agg.end()) {
+      order.push_back(r.name);
+      agg[r.name] = {1, ms};
+    } else {
+      it->second.first += 1;
+      it->second.second += ms;
+    }
+    g_event_pool.push_back(r.a);
+    g_event_pool.push_back(r.b);
+  }
+  g_prof.clear();
+  std::string out;
+  char line[256];
+  for (auto& n : order) {
+    snprintf(line, sizeof(line), "%s %lld %.6f\n", n.c_str(), agg[n].first, agg[n].second);
+    out += line;
+  }
+  if (buf && len) {
+    snprintf(buf, len, "%s", out.c_str());
+  }
+  return cuda_fail("msa_profile_end");
+}
+
+long long msa_launch_count(void) { return g_launches.load(); }
+
+}  // extern "C"

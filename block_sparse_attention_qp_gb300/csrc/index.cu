@@ -1,0 +1,216 @@
+// Index inversion and work-list construction (integer, HBM/latency bound).
+//
+// The blog ("Backward") inverts the cached map  (batch, proxy head, query, slot) -> key block
+// into  (batch, proxy head, key block) -> queries that use the block, and schedules work per key
+// block so that the block's keys and values are loaded once for many queries.  Here the inverse
+// map is a CSR structure: one list per (b, g, n) of packed entries (t << 8 | slot); lists are
+// cut into fixed-size items that the attention kernels consume.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace msa {
+
+// Validity of entry s of a block_idx row: 0 <= n <= t/128, strictly ascending, and -1 only as
+// trailing padding.  Returns the block or -1 (padding or invalid); *bad is set for invalid.
+__device__ __forceinline__ int checked_block(const int32_t* row, int s, int t, int& prev,
+                                             bool& padded, bool& bad) {
+  const int n = row[s];
+  if (n < 0) {
+    if (n != -1) bad = true;
+    padded = true;
+    return -1;
+  }
+  if (padded || n <= prev || n > t / kBlock) {
+    bad = true;
+    return -1;
+  }
+  prev = n;
+  return n;
+}
+
+__global__ void count_kernel(Dims d, const int32_t* __restrict__ idx, int* __restrict__ seg_count,
+                             unsigned* status) {
+  const long long rows = (long long)d.B * d.Hp * d.S;
+  for (long long r = blockIdx.x * (long long)blockDim.x + threadIdx.x; r < rows;
+       r += (long long)gridDim.x * blockDim.x) {
+    const int t = (int)(r % d.S);
+    const long long bg = r / d.S;  // b * Hp + g
+    const int32_t* row = idx + r * d.top_k;
+    int prev = -1;
+    bool padded = false, bad = false;
+    for (int s = 0; s < d.top_k; ++s) {
+      const int n = checked_block(row, s, t, prev, padded, bad);
+      if (n >= 0) atomicAdd(seg_count + bg * d.nblk + n, 1);
+    }
+    if (bad) atomicOr(status, kStatusBadIndex);
+  }
+}
+
+__global__ void fill_kernel(Dims d, const int32_t* __restrict__ idx, const int* __restrict__ seg_offset,
+                            int* __restrict__ seg_cursor, int* __restrict__ entries) {
+  const long long rows = (long long)d.B * d.Hp * d.S;
+  for (long long r = blockIdx.x * (long long)blockDim.x + threadIdx.x; r < rows;
+       r += (long long)gridDim.x * blockDim.x) {
+    const int t = (int)(r % d.S);
+    const long long bg = r / d.S;
+    const int32_t* row = idx + r * d.top_k;
+    int prev = -1;
+    bool padded = false, bad = false;
+    for (int s = 0; s < d.top_k; ++s) {
+      const int n = checked_block(row, s, t, prev, padded, bad);
+      if (n < 0) continue;
+      const long long seg = bg * d.nblk + n;
+      const int pos = atomicAdd(seg_cursor + seg, 1);
+      entries[seg_offset[seg] + pos] = (t << 8) | s;
+    }
+  }
+}
+
+__device__ __forceinline__ long long list_len(const Dims& d, bool dense, const int* seg_count,
+                                              long long seg) {
+  if (dense) return d.S - (long long)(seg % d.nblk) * kBlock;  // tokens t >= 128 n
+  return seg_count[seg];
+}
+
+__device__ __forceinline__ long long items_of(long long c, const ItemSpec& s) {
+  const long long tiles = (c + s.tile_tokens - 1) / s.tile_tokens;
+  return (tiles + s.chunk_tiles - 1) / s.chunk_tiles * s.halves;
+}
+
+// Single-CTA exclusive scan over every list of three running sums: list lengths and the item
+// counts of up to two item specs.
+__global__ void __launch_bounds__(1024) scan_kernel(Dims d, int dense, const int* __restrict__ seg_count,
+                                                    int* __restrict__ seg_offset, ItemSpec s0, ItemSpec s1,
+                                                    int nspecs, int* __restrict__ io0,
+                                                    int* __restrict__ io1, int* __restrict__ totals) {
+  __shared__ long long sh[3][1024];
+  const long long nseg = d.nseg();
+  const int tid = threadIdx.x;
+  const long long per = (nseg + 1023) / 1024;
+  const long long lo = tid * per, hi = lo + per < nseg ? lo + per : nseg;
+  long long a = 0, b = 0, c = 0;
+  for (long long s = lo; s < hi; ++s) {
+    const long long len = list_len(d, dense, seg_count, s);
+    a += len;
+    if (nspecs > 0) b += items_of(len, s0);
+    if (nspecs > 1) c += items_of(len, s1);
+  }
+  sh[0][tid] = a;
+  sh[1][tid] = b;
+  sh[2][tid] = c;
+  __syncthreads();
+  for (int off = 1; off < 1024; off <<= 1) {  // inclusive Hillis-Steele scan
+    long long va = 0, vb = 0, vc = 0;
+    if (tid >= off) {
+      va = sh[0][tid - off];
+      vb = sh[1][tid - off];
+      vc = sh[2][tid - off];
+    }
+    __syncthreads();
+    sh[0][tid] += va;
+    sh[1][tid] += vb;
+    sh[2][tid] += vc;
+    __syncthreads();
+  }
+  long long ra = sh[0][tid] - a, rb = sh[1][tid] - b, rc = sh[2][tid] - c;  // exclusive
+  for (long long s = lo; s < hi; ++s) {
+    const long long len = list_len(d, dense, seg_count, s);
+    if (seg_offset) seg_offset[s] = (int)ra;
+    if (nspecs > 0) io0[s] = (int)rb;
+    if (nspecs > 1) io1[s] = (int)rc;
+    ra += len;
+    if (nspecs > 0) rb += items_of(len, s0);
+    if (nspecs > 1) rc += items_of(len, s1);
+  }
+  if (tid == 1023) {
+    if (seg_offset) seg_offset[nseg] = (int)sh[0][1023];
+    totals[0] = (int)sh[0][1023];
+    totals[1] = (int)sh[1][1023];
+    totals[2] = (int)sh[2][1023];
+  }
+}
+
+__global__ void items_kernel(Dims d, int dense, const int* __restrict__ seg_count, ItemSpec sp,
+                             const int* __restrict__ item_offset, Item* __restrict__ items,
+                             long long max_items, unsigned* status) {
+  const long long seg = blockIdx.x;
+  const long long len = list_len(d, dense, seg_count, seg);
+  const int per_item = sp.tile_tokens * sp.chunk_tiles;
+  const long long n_chunks = (len + per_item - 1) / per_item;
+  const long long base = item_offset[seg];
+  for (long long i = threadIdx.x; i < n_chunks * sp.halves; i += blockDim.x) {
+    const long long chunk = i / sp.halves;
+    const int half = (int)(i % sp.halves);
+    const long long pos = base + i;
+    if (pos >= max_items) {
+      atomicOr(status, kStatusBadItems);
+      continue;
+    }
+    const long long first = chunk * per_item;
+    const long long cnt = len - first < per_item ? len - first : per_item;
+    items[pos] = Item{(int)seg, (int)first, (int)cnt, half};
+  }
+}
+
+__global__ void convert_kernel(const float4* __restrict__ src, uint2* __restrict__ dst, long long n4) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4;
+       i += (long long)gridDim.x * blockDim.x) {
+    const float4 v = src[i];
+    dst[i] = make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
+  }
+}
+
+int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+static int grid_for(long long work, int threads) {
+  long long g = (work + threads - 1) / threads;
+  const long long cap = (long long)num_sms() * 16;
+  if (g > cap) g = cap;
+  return g < 1 ? 1 : (int)g;
+}
+
+void launch_count(const Dims& d, const int32_t* idx, int* seg_count, unsigned* status,
+                  cudaStream_t st) {
+  const long long rows = (long long)d.B * d.Hp * d.S;
+  count_kernel<<<grid_for(rows, 256), 256, 0, st>>>(d, idx, seg_count, status);
+}
+
+void launch_scan(const Dims& d, bool dense, const int* seg_count, int* seg_offset,
+                 const ItemSpec* specs, int nspecs, int* item_offset0, int* item_offset1,
+                 int* totals, cudaStream_t st) {
+  ItemSpec s0 = nspecs > 0 ? specs[0] : ItemSpec{1, 1, 1};
+  ItemSpec s1 = nspecs > 1 ? specs[1] : ItemSpec{1, 1, 1};
+  scan_kernel<<<1, 1024, 0, st>>>(d, dense ? 1 : 0, seg_count, seg_offset, s0, s1, nspecs,
+                                  item_offset0, item_offset1, totals);
+}
+
+void launch_fill(const Dims& d, const int32_t* idx, const int* seg_offset, int* seg_cursor,
+                 int* entries, unsigned* status, cudaStream_t st) {
+  (void)status;
+  const long long rows = (long long)d.B * d.Hp * d.S;
+  fill_kernel<<<grid_for(rows, 256), 256, 0, st>>>(d, idx, seg_offset, seg_cursor, entries);
+}
+
+void launch_items(const Dims& d, bool dense, const int* seg_count, const ItemSpec& spec,
+                  const int* item_offset, Item* items, long long max_items, unsigned* status,
+                  cudaStream_t st) {
+  items_kernel<<<(unsigned)d.nseg(), 128, 0, st>>>(d, dense ? 1 : 0, seg_count, spec, item_offset,
+                                                   items, max_items, status);
+}
+
+void launch_convert(const float* src, void* dst, long long n, cudaStream_t st) {
+  const long long n4 = n / 4;
+  convert_kernel<<<grid_for(n4, 256), 256, 0, st>>>(reinterpret_cast<const float4*>(src),
+                                                    reinterpret_cast<uint2*>(dst), n4);
+}
+
+}  // namespace msa

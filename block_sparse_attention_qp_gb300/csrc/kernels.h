@@ -1,0 +1,77 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernel files.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace msa {
+
+struct Dims {
+  int B, S, Hq, Hkv, Hp, G, top_k, nblk;
+  float scale;
+  __host__ __device__ long long nseg() const { return (long long)B * Hp * nblk; }  // (b, group, key block) lists
+};
+
+// A unit of attention work: `count` tokens of list `seg` starting at list position `first`,
+// on key-half `half` (0/1; forward-shaped kernels use 0).
+struct Item {
+  int seg, first, count, half;
+};
+
+// Shape of one work list: tiles of `tile_tokens` tokens, `chunk_tiles` tiles per item,
+// `halves` copies of every item (one per 64-key half of the block).
+struct ItemSpec {
+  int tile_tokens, chunk_tiles, halves;
+};
+
+// ---------------------------------------------------------------- index kernels (index.cu)
+// Count block references per (b, g, n) list (validating every index against its row).
+void launch_count(const Dims& d, const int32_t* idx, int* seg_count, unsigned* status,
+                  cudaStream_t st);
+// Exclusive scans: list offsets (sparse only) and item offsets for up to two item specs.
+// dense: list lengths are S - 128 n (every later token) instead of seg_count.
+void launch_scan(const Dims& d, bool dense, const int* seg_count, int* seg_offset,
+                 const ItemSpec* specs, int nspecs, int* item_offset0, int* item_offset1,
+                 int* totals, cudaStream_t st);
+// Scatter (t << 8 | slot) into the lists; order inside a list is unspecified.
+void launch_fill(const Dims& d, const int32_t* idx, const int* seg_offset, int* seg_cursor,
+                 int* entries, unsigned* status, cudaStream_t st);
+void launch_items(const Dims& d, bool dense, const int* seg_count, const ItemSpec& spec,
+                  const int* item_offset, Item* items, long long max_items, unsigned* status,
+                  cudaStream_t st);
+
+// ---------------------------------------------------------------- proxy top-k (topk.cu)
+void launch_proxy_topk(const Dims& d, const void* qp, const void* kp, int32_t* idx,
+                       cudaStream_t st);
+
+// ---------------------------------------------------------------- forward (fwd.cu)
+void launch_sparse_fwd(const Dims& d, const void* q, const void* k, const void* v,
+                       const int* seg_offset, const int* entries, const Item* items,
+                       const int* n_items, long long max_items, void* opart, float* lpart,
+                       cudaStream_t st);
+void launch_combine(const Dims& d, const int32_t* idx, const void* opart, const float* lpart,
+                    void* o, float* lse, cudaStream_t st);
+void launch_dense_fwd(const Dims& d, const void* q, const void* k, const void* v, void* o,
+                      float* lse, cudaStream_t st);
+
+// ---------------------------------------------------------------- backward (bwd.cu)
+void launch_bwd_rowdot(const Dims& d, const void* o, const void* dout, float* drow,
+                       cudaStream_t st);
+void launch_proxy_lse_sparse(const Dims& d, const void* qp, const void* kp, const int* seg_offset,
+                             const int* entries, const Item* items, const int* n_items,
+                             long long max_items, float* lpx_part, cudaStream_t st);
+void launch_proxy_lse_combine(const Dims& d, const int32_t* idx, const float* lpx_part,
+                              float* lse_px, cudaStream_t st);
+void launch_proxy_lse_dense(const Dims& d, const void* qp, const void* kp, float* lse_px,
+                            cudaStream_t st);
+void launch_fused_bwd(const Dims& d, bool dense, const void* q, const void* k, const void* v,
+                      const void* qp, const void* kp, const void* dout, const float* lse,
+                      const float* drow, const float* lse_px, float kl_grad,
+                      const int* seg_offset, const int* entries, const Item* items,
+                      const int* n_items, long long max_items, float* dq_acc, float* dk_acc,
+                      float* dv_acc, float* dqp_acc, float* dkp_acc, cudaStream_t st);
+void launch_convert(const float* src, void* dst, long long n, cudaStream_t st);
+
+int num_sms();
+
+}  // namespace msa

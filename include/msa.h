@@ -1,0 +1,161 @@
+/*
+ * msa.h -- C ABI of libmsa.so: MiniMax Sparse Attention (MSA) training on one GB300 (sm_103a).
+ *
+ * The method (Flash-MSA blog, "About MSA"; MSA forum summary, "Architecture: two-stage
+ * block-sparse attention"): causal GQA attention in which one proxy (index) query head per GQA
+ * group, scored against one shared proxy key head, picks for every query the top-k 128-token key
+ * blocks -- the query's own (local) block always among them -- and the main attention runs
+ * exactly, with softmax, over the picked blocks only.  The proxy is trained by a KL loss towards
+ * the group's mean main-attention distribution over the same tokens (blog, "KL Divergence Loss").
+ *
+ * Conventions shared by every entry point
+ *   Tensors are dense, row-major, on the current CUDA device, caller-owned:
+ *     q, o, dout, dq    [B, S, Hq,  128]  bf16
+ *     k, v, dk, dv      [B, S, Hkv, 128]  bf16
+ *     qp, dqp           [B, S, Hp,  128]  bf16   (proxy query; Hp == Hkv, head g serves group g)
+ *     kp, dkp           [B, S, 1,   128]  bf16   (one proxy key head shared by every group)
+ *     lse               [B, Hq, S]        fp32   natural-log sum of exp of the scaled scores
+ *     block_idx         [B, Hp, S, top_k] int32  selected key blocks per (b, group, token),
+ *                                                ascending, padded with -1 when fewer than
+ *                                                top_k blocks are visible
+ *   Query head h belongs to group h / (Hq / Hkv).  Key j is visible to token t iff j <= t.
+ *   Every pointer must be 16-byte aligned.  Supported: head dim 128, block 128 (blog / package
+ *   caveat 1), S % 128 == 0, Hp == Hkv (package caveat 5), Hq / Hkv in {1, 2, 4, 8, 16},
+ *   1 <= top_k <= 64.
+ *   `workspace` is caller-owned device memory of at least msa_workspace_size() bytes for the
+ *   same op and shape; the library allocates nothing.  The first 256 bytes hold a device status
+ *   word (see msa_device_status).  Calls sharing one workspace must not overlap on the GPU.
+ *   `stream` is a cudaStream_t (NULL = legacy default stream); all work is asynchronous on it.
+ *   Return value: an msa_status code.  Argument errors are detected on the host before any
+ *   launch; MSA_ERR_CUDA reports a launch or runtime error (msa_last_error() gives the text).
+ *   No entry point synchronises the device except msa_device_status.
+ */
+#ifndef MSA_H_
+#define MSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MSA_API __attribute__((visibility("default")))
+#else
+#define MSA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct msa_shape {
+  int32_t B;      /* batch */
+  int32_t S;      /* sequence length, multiple of 128 */
+  int32_t Hq;     /* main query heads */
+  int32_t Hkv;    /* main key/value heads (GQA groups) */
+  int32_t Hp;     /* proxy query heads, must equal Hkv */
+  int32_t D;      /* head dim, must be 128 */
+  int32_t top_k;  /* selected blocks per query, local block included (ignored by warmup ops) */
+  float scale;    /* softmax scale of both attentions, usually 128^-0.5 */
+} msa_shape_t;
+
+enum msa_status {
+  MSA_OK = 0,
+  MSA_ERR_INVALID_ARG = 1, /* null / misaligned pointer, non-positive size */
+  MSA_ERR_UNSUPPORTED = 2, /* D != 128, S % 128 != 0, Hp != Hkv, bad group size or top_k */
+  MSA_ERR_WORKSPACE = 3,   /* workspace too small */
+  MSA_ERR_CUDA = 4         /* CUDA launch / runtime error */
+};
+
+enum msa_op {
+  MSA_OP_FORWARD = 0,
+  MSA_OP_BACKWARD = 1,
+  MSA_OP_WARMUP_FORWARD = 2,
+  MSA_OP_WARMUP_BACKWARD = 3
+};
+
+/* Bits of the device status word. */
+#define MSA_DEVICE_BAD_INDEX 1u /* a given block index was out of range or not ascending */
+#define MSA_DEVICE_BAD_ITEMS 2u /* internal work list overflow (a library bug) */
+#define MSA_DEVICE_TIMEOUT 4u   /* a bounded device-side wait gave up */
+
+/* Bytes of workspace `op` needs for `shape` (0 if the shape is unsupported). */
+MSA_API size_t msa_workspace_size(const msa_shape_t* shape, int op);
+
+/*
+ * Sparse forward (blog, "Forward": proxy attention, then sparse main attention; package usage
+ * `flash_msa_func`).
+ *   1. unless indices_given: proxy scores Qp.Kp^T per group, causal max-pool per 128-key block,
+ *      the local block forced in, top-k with ties going to the lower block index
+ *      (blog "Proxy attention") -> block_idx (written);
+ *   2. exact softmax attention of every query head over the key blocks of its group in
+ *      block_idx (blog "Main attention"; forum summary "Architecture") -> o, lse.
+ * indices_given != 0: block_idx is an input (for instance the cached indices of an earlier
+ * call); invalid entries are skipped and flagged with MSA_DEVICE_BAD_INDEX.
+ */
+MSA_API int msa_forward(const msa_shape_t* shape, const void* q, const void* k, const void* v,
+                const void* qp, const void* kp, int32_t* block_idx, int indices_given, void* o,
+                float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Sparse backward (blog, "Backward" and "KL Divergence Loss").  From the cached block_idx it
+ * inverts the block map, recomputes the proxy normaliser over the selected tokens, and in one
+ * fused pass per (key block, group) recomputes the main and proxy probabilities and emits
+ *   dq, dk, dv  of  sum(o * dout)                     (teacher detached: no KL term here)
+ *   dqp, dkp    of  kl_grad * L_KL,  L_KL = mean over (b, t, group) of KL(teacher || student),
+ *               teacher = mean over the group's heads of the main softmax (stop-gradient),
+ *               student = softmax(scale * qp . kp) over the same tokens; the score gradient is
+ *               kl_grad / (B*S*Hp) * (p_student - p_teacher)  (blog, "KL Divergence Loss").
+ * o and lse are the outputs of msa_forward for the same inputs.  kl_grad is the incoming
+ * gradient of the (zero) KL placeholder the forward returns (package usage note), usually 1.
+ */
+MSA_API int msa_backward(const msa_shape_t* shape, const void* q, const void* k, const void* v,
+                 const void* qp, const void* kp, const void* o, const float* lse,
+                 const void* dout, const int32_t* block_idx, float kl_grad, void* dq, void* dk,
+                 void* dv, void* dqp, void* dkp, void* workspace, size_t workspace_bytes,
+                 void* stream);
+
+/*
+ * Warmup forward (blog, "Warmup kernels"): dense causal GQA attention, no proxy pass.
+ * Writes o and lse.  top_k is ignored.
+ */
+MSA_API int msa_warmup_forward(const msa_shape_t* shape, const void* q, const void* k, const void* v,
+                       void* o, float* lse, void* workspace, size_t workspace_bytes,
+                       void* stream);
+
+/*
+ * Warmup backward (blog, "Warmup kernels"): the proxy normaliser over the full causal prefix,
+ * then the fused main + proxy backward with every visible key in the key set.  Same outputs
+ * and KL definition as msa_backward.  top_k is ignored.
+ */
+MSA_API int msa_warmup_backward(const msa_shape_t* shape, const void* q, const void* k, const void* v,
+                        const void* qp, const void* kp, const void* o, const float* lse,
+                        const void* dout, float kl_grad, void* dq, void* dk, void* dv, void* dqp,
+                        void* dkp, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Reads (and clears) the device status word of `workspace` after the work queued on `stream`
+ * finishes; this synchronises `stream`.  *flags receives MSA_DEVICE_* bits (0 = clean).
+ */
+MSA_API int msa_device_status(void* workspace, unsigned* flags, void* stream);
+
+/*
+ * Measurement aids (not part of the method).  msa_profile_begin() makes every later call record
+ * a CUDA event pair around each kernel it launches, on the launch stream.  msa_profile_end()
+ * waits for those events, writes one line per kernel name -- "<name> <launches> <total_ms>\n" --
+ * into buf (NUL-terminated, truncated to len) and stops recording.  msa_launch_count() returns
+ * the number of kernels this library has launched since it was loaded.
+ */
+MSA_API int msa_profile_begin(void);
+MSA_API int msa_profile_end(char* buf, size_t len);
+MSA_API long long msa_launch_count(void);
+
+/* Static text for a status code. */
+MSA_API const char* msa_status_string(int status);
+
+/* Detail of the last error on the calling thread ("" if none). */
+MSA_API const char* msa_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MSA_H_ */

@@ -49,7 +49,7 @@ def _load():
             lib.msa_oracle_select.argtypes = [I, I, I, I, I, Dd, P, P, I, P, P, P]
             lib.msa_oracle_forward.argtypes = [I, I, I, I, I, I, I, Dd, P, P, P, P, I, P, P, P]
             lib.msa_oracle_backward.argtypes = [I, I, I, I, I, I, I, Dd, Dd, P, P, P, P, P, P, P,
-                                                P, I, I, P, P, P, P, P, P]
+                                                P, I, I, I, P, P, P, P, P, P]
             lib.msa_oracle_threads.restype = I
             lib.msa_oracle_set_threads.argtypes = [I]
             _lib = lib
@@ -174,12 +174,13 @@ def forward(q, k, v, idx, top_k: int, scale: float, rows=None, Hp=None):
 
 
 def backward(q, k, v, qp, kp, dout, idx, top_k: int, scale: float, kl_grad: float = 1.0,
-             tok_mask=None, key_window=None):
+             tok_mask=None, key_window=None, only_masked=False):
     """Steps 4-10: gradients of  sum(O*dO) + kl_grad * L_KL  and the KL value.
 
     idx=None: warmup (dense causal key sets).  tok_mask: optional bool [B,S] -- dq/dqp are only
     produced for flagged tokens.  key_window: optional (j0, j1) -- dk/dv/dkp only for keys in
-    [j0, j1).  Entries outside the sample are zero.
+    [j0, j1).  only_masked: tokens outside tok_mask contribute nothing at all (exact share of
+    the flagged tokens in every gradient).  Entries outside the sample are zero.
     Returns dict(dq, dk, dv, dqp, dkp, kl) in the input layouts (dkp [B,S,1,D]).
     """
     q, k, v, qp, kp, dout = f64(q), f64(k), f64(v), f64(qp), f64(kp), f64(dout)
@@ -200,7 +201,7 @@ def backward(q, k, v, qp, kp, dout, idx, top_k: int, scale: float, kl_grad: floa
     j0, j1 = (0, S) if key_window is None else (int(key_window[0]), int(key_window[1]))
     rc = _load().msa_oracle_backward(B, S, Hq, Hkv, Hp, D, top_k, float(scale), float(kl_grad),
                                      _p(q), _p(k), _p(v), _p(qp), _p(kp), _p(dout), _p(idx),
-                                     _p(tm), j0, j1, _p(dq), _p(dk), _p(dv), _p(dqp), _p(dkp),
+                                     _p(tm), int(bool(only_masked)), j0, j1, _p(dq), _p(dk), _p(dv), _p(dqp), _p(dkp),
                                      _p(kl))
     if rc:
         raise ValueError(f"oracle backward rejected the shape (code {rc})")

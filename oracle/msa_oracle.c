@@ -266,15 +266,17 @@ int msa_oracle_forward(int B, int S, int Hq, int Hkv, int Hp, int D, int top_k, 
  *
  * Sampling (for long sequences): dq/dqp are produced only for the tokens flagged in tok_mask
  * ([B,S] bytes, NULL = every token); dk/dv/dkp only for keys in [kj0, kj1) (other entries are
- * left untouched).  Outputs use the full layouts (dq [B,S,Hq,D], dk/dv [B,S,Hkv,D],
+ * left untouched).  With only_masked != 0 the tokens outside tok_mask are skipped entirely, which
+ * gives the exact contribution of the flagged tokens to every gradient (used to time a bounded
+ * sample of a workload).  Outputs use the full layouts (dq [B,S,Hq,D], dk/dv [B,S,Hkv,D],
  * dqp [B,S,Hp,D], dkp [B,S,D]) and must be zeroed by the caller.  kl_out receives L_KL (summed
  * over every row visited, i.e. the exact KL when nothing is sampled).  idx == NULL: warmup.
  */
 int msa_oracle_backward(int B, int S, int Hq, int Hkv, int Hp, int D, int top_k, double scale,
                         double kl_grad, const double* q, const double* k, const double* v,
                         const double* qp, const double* kp, const double* dout,
-                        const int32_t* idx, const unsigned char* tok_mask, int kj0, int kj1,
-                        double* dq, double* dk, double* dv, double* dqp, double* dkp,
+                        const int32_t* idx, const unsigned char* tok_mask, int only_masked,
+                        int kj0, int kj1, double* dq, double* dk, double* dv, double* dqp, double* dkp,
                         double* kl_out) {
   if (Hq % Hkv != 0 || Hp != Hkv) return 1;
   const int G = Hq / Hkv;
@@ -300,7 +302,7 @@ int msa_oracle_backward(int B, int S, int Hq, int Hkv, int Hp, int D, int top_k,
       double kl_acc = 0.0;
       for (int t = 0; t < S; ++t) {
         const int want_q = !tok_mask || tok_mask[(size_t)b * S + t];
-        if (!want_q && t < kj0) continue; /* its keys j <= t all lie before the window */
+        if (!want_q && (only_masked || t < kj0)) continue; /* nothing of it is in the sample */
         const int nj = key_set(b, g, t, S, Hp, top_k, idx, J);
         int touches = want_q;
         for (int a = 0; a < nj && !touches; ++a)

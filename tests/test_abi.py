@@ -1,0 +1,63 @@
+"""The C ABI library loads, exports every entry point include/msa.h declares, and rejects bad
+arguments on the host (no GPU work is issued by any call in this file)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from block_sparse_attention_qp_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names += re.findall(r"^MSA_API\s+[\w\s\*]+?\b(msa_\w+)\s*\(", text, flags=re.M)
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = build.build()
+    return binding.load_library(path)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_symbols()
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+    assert set(binding._SYMBOLS) <= set(names)
+
+
+def test_workspace_size_is_host_only(lib):
+    s = binding.Shape(1, 1024, 8, 2, 2, 128, 4, 128 ** -0.5)
+    for op in range(4):
+        assert binding.msa_workspace_size(s, op) > 0
+    bad = binding.Shape(1, 1000, 8, 2, 2, 128, 4, 0.1)  # S not a multiple of 128
+    assert lib.msa_workspace_size(ctypes.byref(bad), 0) == 0
+    assert b"multiple of 128" in lib.msa_last_error()
+    assert lib.msa_workspace_size(ctypes.byref(binding.Shape(1, 256, 8, 2, 4, 128, 4, 0.1)), 0) == 0
+    assert b"proxy heads" in lib.msa_last_error()
+    assert lib.msa_workspace_size(ctypes.byref(binding.Shape(1, 256, 8, 2, 2, 64, 4, 0.1)), 0) == 0
+    assert lib.msa_workspace_size(ctypes.byref(binding.Shape(1, 256, 8, 2, 2, 128, 65, 0.1)), 0) == 0
+
+
+def test_argument_errors_before_any_launch(lib):
+    s = binding.Shape(1, 256, 8, 2, 2, 128, 2, 0.1)
+    P = ctypes.c_void_p
+    null = P(0)
+    rc = lib.msa_forward(ctypes.byref(s), null, null, null, null, null, null, 0, null, null,
+                         null, 0, null)
+    assert rc == 1 and lib.msa_status_string(rc) == b"invalid argument"
+    odd = P(0x1008)  # not 16-byte aligned; rejected before it is ever dereferenced
+    rc = lib.msa_warmup_forward(ctypes.byref(s), odd, odd, odd, odd, odd, null, 0, null)
+    assert rc == 1 and b"aligned" in lib.msa_last_error()
+    s_bad = binding.Shape(1, 256, 8, 2, 2, 128, 2, -1.0)
+    rc = lib.msa_warmup_forward(ctypes.byref(s_bad), null, null, null, null, null, null, 0, null)
+    assert rc == 1
+    assert lib.msa_status_string(3) == b"workspace too small"

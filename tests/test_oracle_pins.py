@@ -310,3 +310,18 @@ def test_sampled_backward_matches_full():
     i_s, _ = oracle.select(x["qp"], x["kp"], 3, w.scale, rows=srows)
     for r, (b, g_, t) in enumerate(srows):
         np.testing.assert_array_equal(i_s[r], idx[b, g_, t])
+
+
+def test_token_restricted_backward_partitions_the_gradient():
+    """Contributions of disjoint token sets (only_masked) add up to the full gradients."""
+    w, x = tiny(S=512, Hq=4, Hkv=2, top_k=3, seed=29)
+    idx, _ = oracle.select(x["qp"], x["kp"], 3, w.scale)
+    args = (x["q"], x["k"], x["v"], x["qp"], x["kp"], x["dout"], idx, 3, w.scale)
+    full = oracle.backward(*args)
+    mask = np.zeros((1, 512), bool)
+    mask[0, ::3] = True
+    a = oracle.backward(*args, tok_mask=mask, only_masked=True)
+    b = oracle.backward(*args, tok_mask=~mask, only_masked=True)
+    for name in ("dq", "dk", "dv", "dqp", "dkp"):
+        np.testing.assert_allclose(a[name] + b[name], full[name], rtol=1e-12, atol=1e-15)
+    assert abs(a["kl"] + b["kl"] - full["kl"]) < 1e-12
