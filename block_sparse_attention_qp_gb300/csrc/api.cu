@@ -326,8 +326,16 @@ int msa_forward(const msa_shape_t* shape, const void* q, const void* k, const vo
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaGetLastError();
   cudaMemsetAsync(at<char>(workspace, p.status), 0, sizeof(unsigned), st);
-  if (!indices_given)
-    timed("proxy_topk", st, [&] { launch_proxy_topk(d, qp, kp, block_idx, st); });
+  if (!indices_given) {
+    bool ok = true;
+    timed("proxy_topk", st, [&] {
+      ok = launch_proxy_topk(d, qp, kp, block_idx, at<unsigned>(workspace, p.status), st);
+    });
+    if (!ok) {
+      set_err("msa_forward: could not create TMA tensor maps (cuTensorMapEncodeTiled)");
+      return MSA_ERR_CUDA;
+    }
+  }
   build_lists(d, p, block_idx, workspace, 1, st);
   timed("sparse_fwd", st, [&] {
     launch_sparse_fwd(d, q, k, v, at<int>(workspace, p.seg_offset), at<int>(workspace, p.entries),

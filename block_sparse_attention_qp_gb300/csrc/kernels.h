@@ -41,8 +41,9 @@ void launch_items(const Dims& d, bool dense, const int* seg_count, const ItemSpe
                   cudaStream_t st);
 
 // ---------------------------------------------------------------- proxy top-k (topk.cu)
-void launch_proxy_topk(const Dims& d, const void* qp, const void* kp, int32_t* idx,
-                       cudaStream_t st);
+// Returns false if the TMA tensor maps could not be created (driver entry point missing).
+bool launch_proxy_topk(const Dims& d, const void* qp, const void* kp, int32_t* idx,
+                       unsigned* status, cudaStream_t st);
 
 // ---------------------------------------------------------------- forward (fwd.cu)
 void launch_sparse_fwd(const Dims& d, const void* q, const void* k, const void* v,

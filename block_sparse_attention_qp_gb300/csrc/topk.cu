@@ -3,126 +3,219 @@
 //
 // A CTA owns the 128 tokens of query block qb for one group g.  Every key block n < qb is fully
 // visible to all of them (the local block qb is forced in and never scored), so the causal mask
-// reduces to "stream blocks 0 .. qb-1".  For each streamed block the CTA forms the 128 x 128 raw
-// score tile qp . kp (the positive scale does not change the order, so it is not applied),
-// max-pools each row over the block, and inserts the block score into that row's running list of
-// the best top_k - 1 non-local blocks.  Ties keep the earlier (lower) block: a new score enters
-// only if strictly larger than the current last entry and is placed after equal entries.
+// reduces to "stream blocks 0 .. qb-1".  For each streamed block the tensor core forms the
+// 128 x 128 raw score tile qp . kp in tensor memory (the positive scale does not change the
+// order, so it is not applied); the epilogue max-pools each row over the block and inserts the
+// block score into that row's running list of the best top_k - 1 non-local blocks, kept sorted
+// in registers.  Ties keep the lower block: a new score enters only if strictly larger than the
+// current last entry and is placed after equal entries.  No exponential is ever taken.
+//
+// Roles (256 threads): warp 0 issues the TMA loads (the query tile once, then a 4-deep ring of
+// 128-key proxy-key blocks), warp 1 issues the MMAs (one thread), warp 2 owns the tensor memory
+// (4 accumulators x 128 columns), warps 4..7 are the epilogue (thread i of warpgroup 1 owns
+// score row i = TMEM lane i).
 #include <math.h>
 
 #include "common.cuh"
 #include "kernels.h"
+#include "sm100.cuh"
+#include "tmap.h"
 
 namespace msa {
 
+namespace {
+constexpr int kStages = 4;
+constexpr int kAcc = 4;
+constexpr int kTileBytes = 128 * 128 * 2;  // one 128 x 128 bf16 tile (two SW128 panels)
+
+struct TopkSmem {
+  uint64_t q_full;
+  uint64_t kp_full[kStages], kp_empty[kStages];
+  uint64_t acc_full[kAcc], acc_empty[kAcc];
+  uint32_t tmem;
+};
+}  // namespace
+
+template <int KMAX>
 __global__ void __launch_bounds__(256, 1)
-    proxy_topk_kernel(Dims d, const bf16* __restrict__ qp, const bf16* __restrict__ kp,
-                      int32_t* __restrict__ idx) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  bf16* sQ = reinterpret_cast<bf16*>(smem);
-  bf16* sK = sQ + 128 * kLd;  // [2][128][kLd]
-  const int KL = d.top_k - 1;  // list length (non-local picks)
-  const int KLc = KL > 0 ? KL : 1;
-  float* sval = reinterpret_cast<float*>(sK + 2 * 128 * kLd);  // [128][KLc]
-  int* sidx = reinterpret_cast<int*>(sval + 128 * KLc);       // [128][KLc]
+    proxy_topk_kernel(const __grid_constant__ CUtensorMap tm_qp,
+                      const __grid_constant__ CUtensorMap tm_kp, Dims d,
+                      int32_t* __restrict__ idx, unsigned* __restrict__ status) {
+  using namespace sm100;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = align1024(smem_raw);
+  uint8_t* sQ = base;                  // 32 KB
+  uint8_t* sK = base + kTileBytes;     // kStages x 32 KB
+  TopkSmem* sh = reinterpret_cast<TopkSmem*>(sK + kStages * kTileBytes);
+
   const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
   const int nbg = d.B * d.Hp;
   const int qb = d.nblk - 1 - blockIdx.x / nbg;  // most work first
   const int bg = blockIdx.x % nbg;
   const int b = bg / d.Hp, g = bg % d.Hp;
   const int t0 = qb * kBlock;
+  const int KL = d.top_k - 1;
 
-  load_rows_async(sQ, 128, [&](int r) -> const bf16* {
-    return qp + (((size_t)b * d.S + t0 + r) * d.Hp + g) * kD;
-  }, tid, 256, qp);
-  auto load_block = [&](int n, int buf) {
-    load_rows_async(sK + buf * 128 * kLd, 128, [&](int r) -> const bf16* {
-      return kp + ((size_t)b * d.S + n * kBlock + r) * kD;
-    }, tid, 256, kp);
-  };
-  if (qb > 0) load_block(0, 0);
-  cp_async_commit();
-  for (int i = tid; i < 128 * KLc; i += 256) {
-    sval[i] = -INFINITY;
-    sidx[i] = -1;
+  if (tid == 0) {
+    mbar_init(&sh->q_full, 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&sh->kp_full[i], 1);
+      mbar_init(&sh->kp_empty[i], 1);
+    }
+    for (int i = 0; i < kAcc; ++i) {
+      mbar_init(&sh->acc_full[i], 1);
+      mbar_init(&sh->acc_empty[i], 4);
+    }
+    mbar_fence_init();
   }
+  if (warp == 2) {
+    tmem_alloc(&sh->tmem, 512);
+    tmem_relinquish();
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = sh->tmem;
+  const uint32_t sQa = static_cast<uint32_t>(__cvta_generic_to_shared(sQ));
+  const uint32_t sKa = static_cast<uint32_t>(__cvta_generic_to_shared(sK));
 
-  // Row owner: lane%4 == 0 owns row lane/4, lane%4 == 1 owns row lane/4 + 8 (of this warp).
-  const int own = lane % 4;
-  const int my_row = warp * 16 + lane / 4 + (own == 1 ? 8 : 0);
-  float kth = -INFINITY;  // current last list entry of my row (cached)
-
-#pragma unroll 1
-  for (int n = 0; n < qb; ++n) {
-    if (n + 1 < qb) {
-      load_block(n + 1, (n + 1) & 1);
-      cp_async_commit();
-      cp_async_wait_group<1>();
-    } else {
-      cp_async_wait_group<0>();
+  if (warp == 0 && lane == 0 && qb > 0) {
+    // ---- producer
+    tma_prefetch_desc(&tm_qp);
+    tma_prefetch_desc(&tm_kp);
+    mbar_expect_tx(&sh->q_full, kTileBytes);
+    tma_load_3d(sQ, &tm_qp, 0, g, b * d.S + t0, &sh->q_full);
+    tma_load_3d(sQ + kTileBytes / 2, &tm_qp, 64, g, b * d.S + t0, &sh->q_full);
+    for (int n = 0; n < qb; ++n) {
+      const int s = n % kStages;
+      if (n >= kStages) mbar_wait(&sh->kp_empty[s], ((n / kStages) - 1) & 1, status);
+      uint8_t* dst = sK + s * kTileBytes;
+      mbar_expect_tx(&sh->kp_full[s], kTileBytes);
+      tma_load_2d(dst, &tm_kp, 0, b * d.S + n * kBlock, &sh->kp_full[s]);
+      tma_load_2d(dst + kTileBytes / 2, &tm_kp, 64, b * d.S + n * kBlock, &sh->kp_full[s]);
     }
-    __syncthreads();
-    float acc[16][4];
-    zero_acc(acc);
-    warp_gemm_abt<128, 128>(acc, sQ + warp * 16 * kLd, kLd, sK + (n & 1) * 128 * kLd, kLd, lane);
-    float m0 = -INFINITY, m1 = -INFINITY;
+  } else if (warp == 1 && lane == 0 && qb > 0) {
+    // ---- MMA issuer
+    constexpr uint32_t idesc = idesc_bf16(128, 128, false, false);
+    mbar_wait(&sh->q_full, 0, status);
+    for (int n = 0; n < qb; ++n) {
+      const int s = n % kStages, a = n % kAcc;
+      mbar_wait(&sh->kp_full[s], (n / kStages) & 1, status);
+      if (n >= kAcc) mbar_wait(&sh->acc_empty[a], ((n / kAcc) - 1) & 1, status);
+      fence_after_sync();
+      const uint32_t kaddr = sKa + s * kTileBytes;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      m0 = fmaxf(m0, fmaxf(acc[j][0], acc[j][1]));
-      m1 = fmaxf(m1, fmaxf(acc[j][2], acc[j][3]));
+      for (int ks = 0; ks < 8; ++ks)
+        mma_ss(tmem + a * 128, desc_kmajor(sQa, 128, ks), desc_kmajor(kaddr, 128, ks), idesc,
+               ks > 0);
+      mma_commit(&sh->kp_empty[s]);
+      mma_commit(&sh->acc_full[a]);
     }
-    m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 1));
-    m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 2));
-    m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 1));
-    m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 2));
-    if (own < 2 && KL > 0) {
-      const float c = own == 0 ? m0 : m1;
-      if (c > kth) {
-        float* v = sval + my_row * KLc;
-        int* ix = sidx + my_row * KLc;
-        int p = KL - 1;
-        while (p > 0 && v[p - 1] < c) {
-          v[p] = v[p - 1];
-          ix[p] = ix[p - 1];
-          --p;
+  } else if (warp >= 4) {
+    // ---- epilogue: thread owns score row `row`
+    const int q4 = warp - 4;
+    const int row = q4 * 32 + lane;
+    float vals[KMAX - 1];
+    int ids[KMAX - 1];
+#pragma unroll
+    for (int p = 0; p < KMAX - 1; ++p) {
+      vals[p] = -INFINITY;
+      ids[p] = -1;
+    }
+    float kth = -INFINITY;
+    const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
+    for (int n = 0; n < qb; ++n) {
+      const int a = n % kAcc;
+      mbar_wait(&sh->acc_full[a], (n / kAcc) & 1, status);
+      fence_after_sync();
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; c += 2) {
+        uint32_t r0[32], r1[32];
+        tmem_ld32(tmem + lane_base + a * 128 + c * 32, r0);
+        tmem_ld32(tmem + lane_base + a * 128 + (c + 1) * 32, r1);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          mx = fmaxf(mx, fmaxf(__uint_as_float(r0[j]), __uint_as_float(r1[j])));
+      }
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh->acc_empty[a]);
+      if (mx > kth) {
+        // sorted insert (descending); after the insertion point every entry shifts down one
+        float cv = mx;
+        int ci = n;
+        bool ins = false;
+#pragma unroll
+        for (int p = 0; p < KMAX - 1; ++p) {
+          if (p < KL) {
+            const bool take = ins || cv > vals[p];
+            const float tv = vals[p];
+            const int ti = ids[p];
+            vals[p] = take ? cv : tv;
+            ids[p] = take ? ci : ti;
+            cv = take ? tv : cv;
+            ci = take ? ti : ci;
+            ins = take;
+            if (p == KL - 1) kth = vals[p];
+          }
         }
-        v[p] = c;
-        ix[p] = n;
-        kth = v[KL - 1];
       }
     }
-    __syncthreads();
-  }
-  __syncthreads();
-  // Emit: the picked non-local blocks in ascending order, then the local block, then -1.
-  if (tid < 128) {
-    int* ix = sidx + tid * KLc;
+    // emit: picked non-local blocks ascending, then the local block, then -1 padding
+    int sel[KMAX];
     int nv = 0;
-    for (int i = 0; i < KL; ++i)
-      if (ix[i] >= 0) ix[nv++] = ix[i];
-    for (int i = 1; i < nv; ++i) {  // insertion sort, nv <= 63
-      const int x = ix[i];
+#pragma unroll
+    for (int p = 0; p < KMAX - 1; ++p)
+      if (p < KL && ids[p] >= 0) sel[nv++] = ids[p];
+    for (int i = 1; i < nv; ++i) {
+      const int x = sel[i];
       int j = i - 1;
-      while (j >= 0 && ix[j] > x) {
-        ix[j + 1] = ix[j];
+      while (j >= 0 && sel[j] > x) {
+        sel[j + 1] = sel[j];
         --j;
       }
-      ix[j + 1] = x;
+      sel[j + 1] = x;
     }
-    int32_t* out = idx + (((size_t)b * d.Hp + g) * d.S + t0 + tid) * d.top_k;
-    for (int i = 0; i < nv; ++i) out[i] = ix[i];
-    out[nv] = qb;
-    for (int i = nv + 1; i < d.top_k; ++i) out[i] = -1;
+    int32_t* out = idx + (((size_t)b * d.Hp + g) * d.S + t0 + row) * d.top_k;
+    for (int i = 0; i < d.top_k; ++i) out[i] = i < nv ? sel[i] : (i == nv ? qb : -1);
   }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (warp == 2) tmem_dealloc(tmem, 512);
 }
 
-void launch_proxy_topk(const Dims& d, const void* qp, const void* kp, int32_t* idx,
-                       cudaStream_t st) {
-  const int KLc = d.top_k > 1 ? d.top_k - 1 : 1;
-  const size_t smem = 3 * 128 * kLd * sizeof(bf16) + 128 * KLc * (sizeof(float) + sizeof(int));
-  cudaFuncSetAttribute(proxy_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  proxy_topk_kernel<<<d.B * d.Hp * d.nblk, 256, smem, st>>>(d, (const bf16*)qp, (const bf16*)kp,
-                                                            idx);
+template <int KMAX>
+static void topk_launch(const CUtensorMap& mq, const CUtensorMap& mk, const Dims& d, int32_t* idx,
+                        unsigned* status, cudaStream_t st) {
+  const size_t smem = 1024 + (1 + kStages) * kTileBytes + sizeof(TopkSmem);
+  cudaFuncSetAttribute(proxy_topk_kernel<KMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       (int)smem);
+  proxy_topk_kernel<KMAX><<<d.B * d.Hp * d.nblk, 256, smem, st>>>(mq, mk, d, idx, status);
+}
+
+bool launch_proxy_topk(const Dims& d, const void* qp, const void* kp, int32_t* idx,
+                       unsigned* status, cudaStream_t st) {
+  CUtensorMap mq, mk;
+  const uint64_t qdims[3] = {128, (uint64_t)d.Hp, (uint64_t)d.B * d.S};
+  const uint64_t qstr[2] = {128 * 2, (uint64_t)d.Hp * 128 * 2};
+  const uint32_t qbox[3] = {64, 1, 128};
+  const uint64_t kdims[2] = {128, (uint64_t)d.B * d.S};
+  const uint64_t kstr[1] = {128 * 2};
+  const uint32_t kbox[2] = {64, 128};
+  if (!make_tmap_bf16(&mq, qp, 3, qdims, qstr, qbox)) return false;
+  if (!make_tmap_bf16(&mk, kp, 2, kdims, kstr, kbox)) return false;
+  if (d.top_k <= 8)
+    topk_launch<8>(mq, mk, d, idx, status, st);
+  else if (d.top_k <= 16)
+    topk_launch<16>(mq, mk, d, idx, status, st);
+  else if (d.top_k <= 32)
+    topk_launch<32>(mq, mk, d, idx, status, st);
+  else
+    topk_launch<64>(mq, mk, d, idx, status, st);
+  return true;
 }
 
 }  // namespace msa
