@@ -155,11 +155,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* mbar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait: gives up after ~`limit` polls and records kStatusTimeout-style failure in *err.
-// Returns false on timeout.  Every wait in this library is bounded so that a logic error can
-// never hang the GPU.
+// Bounded wait: gives up after ~`limit` polls (a fraction of a second; legitimate waits here
+// last microseconds), sets the timeout bit (4) of the device status word and returns false.
+// Every wait in this library is bounded and callers leave their loops on a timeout, so a logic
+// error can never hang the GPU.
 __device__ __forceinline__ bool mbar_wait(uint64_t* mbar, uint32_t parity, unsigned* err,
-                                          unsigned long long limit = (1ull << 26)) {
+                                          unsigned long long limit = (1ull << 22)) {
   for (unsigned long long i = 0; i < limit; ++i) {
     if (mbar_try_wait(mbar, parity)) return true;
     if (i > 64) __nanosleep(32);

@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(256, 1)
     tma_load_3d(sQ + kTileBytes / 2, &tm_qp, 64, g, b * d.S + t0, &sh->q_full);
     for (int n = 0; n < qb; ++n) {
       const int s = n % kStages;
-      if (n >= kStages) mbar_wait(&sh->kp_empty[s], ((n / kStages) - 1) & 1, status);
+      if (n >= kStages && !mbar_wait(&sh->kp_empty[s], ((n / kStages) - 1) & 1, status)) break;
       uint8_t* dst = sK + s * kTileBytes;
       mbar_expect_tx(&sh->kp_full[s], kTileBytes);
       tma_load_2d(dst, &tm_kp, 0, b * d.S + n * kBlock, &sh->kp_full[s]);
@@ -97,11 +97,11 @@ __global__ void __launch_bounds__(256, 1)
   } else if (warp == 1 && lane == 0 && qb > 0) {
     // ---- MMA issuer
     constexpr uint32_t idesc = idesc_bf16(128, 128, false, false);
-    mbar_wait(&sh->q_full, 0, status);
-    for (int n = 0; n < qb; ++n) {
+    bool ok = mbar_wait(&sh->q_full, 0, status);
+    for (int n = 0; ok && n < qb; ++n) {
       const int s = n % kStages, a = n % kAcc;
-      mbar_wait(&sh->kp_full[s], (n / kStages) & 1, status);
-      if (n >= kAcc) mbar_wait(&sh->acc_empty[a], ((n / kAcc) - 1) & 1, status);
+      if (!mbar_wait(&sh->kp_full[s], (n / kStages) & 1, status)) break;
+      if (n >= kAcc && !mbar_wait(&sh->acc_empty[a], ((n / kAcc) - 1) & 1, status)) break;
       fence_after_sync();
       const uint32_t kaddr = sKa + s * kTileBytes;
 #pragma unroll
@@ -126,7 +126,8 @@ __global__ void __launch_bounds__(256, 1)
     const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
     for (int n = 0; n < qb; ++n) {
       const int a = n % kAcc;
-      mbar_wait(&sh->acc_full[a], (n / kAcc) & 1, status);
+      __syncwarp();
+      if (!mbar_wait(&sh->acc_full[a], (n / kAcc) & 1, status)) break;
       fence_after_sync();
       float mx = -INFINITY;
 #pragma unroll
