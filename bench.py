@@ -261,6 +261,8 @@ def run_ours(args, w, wi):
         launches = msa.launch_count() - n0
         prof = msa.profile_end()
     dist.barrier()
+    # device status words (bounded waits that gave up, bad indices): must be 0 for a valid run
+    dev_status = {"fwd": msa.msa_device_status(ws_f), "bwd": msa.msa_device_status(ws_b)}
     sec = e0.elapsed_time(e1) / 1e3
     sec_max = dist.max_over_ranks(sec, device=dev)
     tok = w.B * w.S
@@ -306,7 +308,8 @@ def run_ours(args, w, wi):
                     "note": f"sparse-counted FLOPs, {peak_src}"},
                 "flops_per_step": fl,
                 "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": launches, "kernels": kernels, "clocks": clk.summary()}
+                "gpu_launches": launches, "kernels": kernels, "clocks": clk.summary(),
+                "device_status": dev_status}
         print(json.dumps(line), flush=True)
     dist.shutdown()
 

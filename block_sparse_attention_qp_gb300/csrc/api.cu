@@ -67,7 +67,6 @@ void timed(const char* name, cudaStream_t st, F&& launch) {
   g_prof.push_back(r);
 }
 
-constexpr int kBwdChunkTiles = 8;  // tiles per backward item (bounds per-item work)
 constexpr size_t kAlign = 256;
 
 size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
@@ -76,7 +75,7 @@ size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 struct Plan {
   size_t status = 0, totals = 0, seg_count = 0, seg_offset = 0, seg_cursor = 0, entries = 0;
   size_t io0 = 0, io1 = 0, items0 = 0, items1 = 0;
-  size_t opart = 0, lpart = 0, lpx_part = 0, lse_px = 0, drow = 0;
+  size_t opart = 0, lpart = 0, lpx_part = 0, lse_px = 0, drow = 0, pbar = 0;
   size_t dq = 0, dk = 0, dv = 0, dqp = 0, dkp = 0;
   size_t bytes = 0;
   long long max0 = 0, max1 = 0;
@@ -97,13 +96,28 @@ long long dense_entries(const Dims& d) {  // sum over blocks of S - 128 n, per (
 }
 
 long long max_items(long long entries, const Dims& d, const ItemSpec& s) {
-  return (long long)s.halves * (entries / ((long long)s.tile_tokens * s.chunk_tiles) + d.nseg() + 1);
+  return (long long)s.halves * (entries / ((long long)s.tile_tokens * s.chunk_tiles) + d.nlist() + 1);
+}
+
+// Sequence chunk of the backward's token lists: the dQ rows one chunk contributes for one group
+// (chunk x G heads x 128 x fp32) are kept to <= 32 MB so that they stay resident in L2 while the
+// work items of that chunk and group run.
+int bwd_chunk(const Dims& d) {
+  int c = kBlock;
+  while ((long long)c * 2 * d.G * kD * 4 <= (32ll << 20) && c * 2 <= d.S) c *= 2;
+  return c;
+}
+
+Dims with_chunk(Dims d, int chunk) {
+  d.chunk = chunk;
+  d.nchunk = (d.S + chunk - 1) / chunk;
+  return d;
 }
 
 Plan make_plan(const Dims& d, int op) {
   Plan p;
   Carver c;
-  const long long nseg = d.nseg();
+  const long long nseg = d.nlist();
   const long long rows_q = (long long)d.B * d.S * d.Hq;
   const long long rows_kv = (long long)d.B * d.S * d.Hkv;
   const long long rows_p = (long long)d.B * d.S * d.Hp;
@@ -129,14 +143,16 @@ Plan make_plan(const Dims& d, int op) {
   if (op == MSA_OP_BACKWARD || op == MSA_OP_WARMUP_BACKWARD) {
     const bool dense = op == MSA_OP_WARMUP_BACKWARD;
     const long long ent = dense ? dense_entries(d) : sparse_ent;
+    const ItemSpec fused{bwd_group_tokens(), bwd_item_tokens() / bwd_group_tokens(), 1};
     if (dense) {
-      p.spec0 = ItemSpec{TT, kBwdChunkTiles, 2};  // fused backward items
+      p.spec0 = fused;
       p.max0 = max_items(ent, d, p.spec0);
+      p.seg_offset = c.take((nseg + 1) * sizeof(int));
       p.io0 = c.take(nseg * sizeof(int));
       p.items0 = c.take(p.max0 * sizeof(Item));
     } else {
       p.spec0 = ItemSpec{kBlock, 1, 1};  // proxy normaliser items
-      p.spec1 = ItemSpec{TT, kBwdChunkTiles, 2};  // fused backward items
+      p.spec1 = fused;
       p.max0 = max_items(ent, d, p.spec0);
       p.max1 = max_items(ent, d, p.spec1);
       p.io0 = c.take(nseg * sizeof(int));
@@ -147,6 +163,7 @@ Plan make_plan(const Dims& d, int op) {
     }
     p.lse_px = c.take((size_t)rows_p * sizeof(float));
     p.drow = c.take((size_t)rows_q * sizeof(float));
+    p.pbar = c.take((size_t)ent * kBlock * sizeof(float));  // teacher rows, one per list entry
     p.dq = c.take((size_t)rows_q * kD * sizeof(float));
     p.dk = c.take((size_t)rows_kv * kD * sizeof(float));
     p.dv = c.take((size_t)rows_kv * kD * sizeof(float));
@@ -189,8 +206,8 @@ int check_shape(const msa_shape_t* s, int op, Dims* out) {
   }
   const int G = s->Hq / s->Hkv;
   const bool bwd = op == MSA_OP_BACKWARD || op == MSA_OP_WARMUP_BACKWARD;
-  if (!(G == 1 || G == 2 || G == 4 || G == 8 || G == 16) || (bwd && G == 1)) {
-    set_err("group size Hq/Hkv must be 2, 4, 8 or 16 (1 also allowed in the forward ops)");
+  if (!(G == 1 || G == 2 || G == 4 || G == 8 || G == 16) || (bwd && G < 4)) {
+    set_err("group size Hq/Hkv must be 4, 8 or 16 (1 and 2 also allowed in the forward ops)");
     return MSA_ERR_UNSUPPORTED;
   }
   const bool sparse = op == MSA_OP_FORWARD || op == MSA_OP_BACKWARD;
@@ -217,6 +234,7 @@ int check_shape(const msa_shape_t* s, int op, Dims* out) {
   d.top_k = sparse ? s->top_k : 1;
   d.nblk = s->S / kBlock;
   d.scale = s->scale;
+  d = with_chunk(d, bwd ? bwd_chunk(d) : d.S);
   if (op == MSA_OP_WARMUP_BACKWARD && dense_entries(d) >= (1ll << 31)) {
     set_err("B*Hp*S*S/256 must stay below 2^31 in the warmup backward");
     return MSA_ERR_UNSUPPORTED;
@@ -262,8 +280,8 @@ void build_lists(const Dims& d, const Plan& p, const int32_t* idx, void* ws, int
   unsigned* status = at<unsigned>(ws, p.status);
   int* seg_count = at<int>(ws, p.seg_count);
   int* seg_cursor = at<int>(ws, p.seg_cursor);
-  cudaMemsetAsync(seg_count, 0, d.nseg() * sizeof(int), st);
-  cudaMemsetAsync(seg_cursor, 0, d.nseg() * sizeof(int), st);
+  cudaMemsetAsync(seg_count, 0, d.nlist() * sizeof(int), st);
+  cudaMemsetAsync(seg_cursor, 0, d.nlist() * sizeof(int), st);
   timed("invert_count", st, [&] { launch_count(d, idx, seg_count, status, st); });
   const ItemSpec specs[2] = {p.spec0, p.spec1};
   timed("invert_scan", st, [&] {
@@ -376,12 +394,27 @@ int msa_backward(const msa_shape_t* shape, const void* q, const void* k, const v
     launch_proxy_lse_combine(d, block_idx, at<float>(workspace, p.lpx_part),
                              at<float>(workspace, p.lse_px), st);
   });
-  timed("fused_bwd", st, [&] { launch_fused_bwd(d, false, q, k, v, qp, kp, dout, lse, at<float>(workspace, p.drow),
-                   at<float>(workspace, p.lse_px), kl_grad, at<int>(workspace, p.seg_offset),
-                   at<int>(workspace, p.entries), at<Item>(workspace, p.items1),
-                   at<int>(workspace, p.totals) + 2, p.max1, at<float>(workspace, p.dq),
-                   at<float>(workspace, p.dk), at<float>(workspace, p.dv),
-                   at<float>(workspace, p.dqp), at<float>(workspace, p.dkp), st); });
+  bool ok = true;
+  timed("attn_bwd", st, [&] {
+    ok = launch_attn_bwd(d, false, q, k, v, dout, lse, at<float>(workspace, p.drow),
+                         at<int>(workspace, p.seg_offset), at<int>(workspace, p.entries),
+                         at<Item>(workspace, p.items1), at<int>(workspace, p.totals) + 2, p.max1,
+                         at<float>(workspace, p.dq), at<float>(workspace, p.dk),
+                         at<float>(workspace, p.dv), at<float>(workspace, p.pbar),
+                         at<unsigned>(workspace, p.status), st);
+  });
+  if (ok)
+    timed("proxy_bwd", st, [&] {
+      ok = launch_proxy_bwd(d, false, qp, kp, at<float>(workspace, p.lse_px),
+                            at<float>(workspace, p.pbar), kl_grad, at<int>(workspace, p.seg_offset),
+                            at<int>(workspace, p.entries), at<Item>(workspace, p.items1),
+                            at<int>(workspace, p.totals) + 2, p.max1, at<float>(workspace, p.dqp),
+                            at<float>(workspace, p.dkp), at<unsigned>(workspace, p.status), st);
+    });
+  if (!ok) {
+    set_err("msa_backward: could not create TMA tensor maps (cuTensorMapEncodeTiled)");
+    return MSA_ERR_CUDA;
+  }
   emit_grads(d, p, workspace, dq, dk, dv, dqp, dkp, st);
   return cuda_fail("msa_backward");
 }
@@ -419,8 +452,8 @@ int msa_warmup_backward(const msa_shape_t* shape, const void* q, const void* k, 
   zero_grads(d, p, workspace, st);
   const ItemSpec specs[1] = {p.spec0};
   timed("invert_scan", st, [&] {
-    launch_scan(d, true, nullptr, nullptr, specs, 1, at<int>(workspace, p.io0), nullptr,
-                at<int>(workspace, p.totals), st);
+    launch_scan(d, true, nullptr, at<int>(workspace, p.seg_offset), specs, 1,
+                at<int>(workspace, p.io0), nullptr, at<int>(workspace, p.totals), st);
   });
   timed("work_items", st, [&] {
     launch_items(d, true, nullptr, p.spec0, at<int>(workspace, p.io0),
@@ -428,12 +461,26 @@ int msa_warmup_backward(const msa_shape_t* shape, const void* q, const void* k, 
   });
   timed("bwd_rowdot", st, [&] { launch_bwd_rowdot(d, o, dout, at<float>(workspace, p.drow), st); });
   timed("proxy_lse_dense", st, [&] { launch_proxy_lse_dense(d, qp, kp, at<float>(workspace, p.lse_px), st); });
-  timed("fused_bwd_dense", st, [&] { launch_fused_bwd(d, true, q, k, v, qp, kp, dout, lse, at<float>(workspace, p.drow),
-                   at<float>(workspace, p.lse_px), kl_grad, nullptr, nullptr,
-                   at<Item>(workspace, p.items0), at<int>(workspace, p.totals) + 1, p.max0,
-                   at<float>(workspace, p.dq), at<float>(workspace, p.dk),
-                   at<float>(workspace, p.dv), at<float>(workspace, p.dqp),
-                   at<float>(workspace, p.dkp), st); });
+  bool ok = true;
+  timed("attn_bwd_dense", st, [&] {
+    ok = launch_attn_bwd(d, true, q, k, v, dout, lse, at<float>(workspace, p.drow),
+                         at<int>(workspace, p.seg_offset), nullptr, at<Item>(workspace, p.items0),
+                         at<int>(workspace, p.totals) + 1, p.max0, at<float>(workspace, p.dq),
+                         at<float>(workspace, p.dk), at<float>(workspace, p.dv),
+                         at<float>(workspace, p.pbar), status, st);
+  });
+  if (ok)
+    timed("proxy_bwd_dense", st, [&] {
+      ok = launch_proxy_bwd(d, true, qp, kp, at<float>(workspace, p.lse_px),
+                            at<float>(workspace, p.pbar), kl_grad, at<int>(workspace, p.seg_offset),
+                            nullptr, at<Item>(workspace, p.items0), at<int>(workspace, p.totals) + 1,
+                            p.max0, at<float>(workspace, p.dqp), at<float>(workspace, p.dkp),
+                            status, st);
+    });
+  if (!ok) {
+    set_err("msa_warmup_backward: could not create TMA tensor maps (cuTensorMapEncodeTiled)");
+    return MSA_ERR_CUDA;
+  }
   emit_grads(d, p, workspace, dq, dk, dv, dqp, dkp, st);
   return cuda_fail("msa_warmup_backward");
 }

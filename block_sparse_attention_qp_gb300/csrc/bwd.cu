@@ -1,26 +1,42 @@
-// Backward: D = rowsum(dO * O), and the fused main + proxy backward (blog, "Backward" and
-// "KL Divergence Loss").
+// Backward on the tcgen05 tensor cores (blog, "Backward" and "KL Divergence Loss"):
+//   rowdot_kernel     D = rowsum(dO * O)
+//   attn_bwd_kernel   main-attention gradients dQ, dK, dV and the teacher pbar
+//   proxy_bwd_kernel  proxy gradients dQp, dKp of the KL term, from pbar
 //
-// Fused pass.  A work item is one 64-key half of key block n of group g, plus a run of tokens that
-// use the block (from the inverted block map; in warmup mode every token t >= 128 n).  The item
-// keeps the half's K, V and Kp in shared memory and its dK, dV, dKp in registers while it streams
-// tiles of 128/G tokens x G query heads (128 rows).  Per tile:
-//   main   S = Q K^T, P = exp(scale S - LSE), dP = dO V^T, dS = P (dP - D)
-//          dV += P^T dO, dK += scale dS^T Q, dQ += scale dS K        (dQ: fp32 atomics)
-//   proxy  teacher  pbar = mean over the G heads of P  (detached: used as a constant)
-//          student  p_px = exp(scale qp.kp - LSE_px)   (LSE_px over the same key set)
-//          dz = kl_grad/(B S Hp) (p_px - pbar)          (the blog's closed form)
-//          dQp += scale dz Kp (fp32 atomics), dKp += scale dz^T Qp
-// dK, dV, dKp of the item are added into fp32 accumulators at the end (an item covers at most
-// chunk_tiles tiles, so busy blocks are spread over several CTAs).
+// Work items (shared by both kernels): one 128-key block n of group g and up to 512 tokens that
+// use it (from the inverted block map; in warmup mode every token t >= 128 n), all from one
+// sequence chunk.  Lists run chunk-major, so the dQ / dQp rows that concurrent items update
+// belong to one chunk of the sequence.
+//
+// attn_bwd_kernel keeps the block's K and V in shared memory and its dK, dV accumulators in tensor
+// memory while it streams tiles of 64/G tokens x G query heads (64 rows), double buffered:
+//   phase 1 (tensor core)  S^T = K Q^T,  dP^T = V dO^T                       (keys x rows, fp32)
+//   softmax (4 warps, thread = key)
+//                          P^T  = exp(scale S^T - LSE_row)       -> tensor memory (bf16)
+//                          dS^T = P^T (dP^T - D_row)             -> shared memory (bf16)
+//                          teacher pbar = mean over the token's G heads of P -> global (fp32)
+//   phase 2 (tensor core)  dV += P^T dO,  dK += dS^T Q,  dQ^T = K^T dS^T
+//   epilogue               dQ^T -> shared staging; a reducer thread adds each token's G rows
+//                          into dQ with one bulk tensor-memory-accelerator reduction
+//   item end               dK (x scale), dV -> fp32 atomics
+// proxy_bwd_kernel streams the same items in groups of 64 tokens:
+//   z^T = Kp Qp^T;  dz = kl_grad/(B S Hp) (exp(scale z - LSE_px) - pbar)   (the blog's closed
+//   form; the teacher is a constant, so no KL term reaches dQ, dK, dV)
+//   dKp += dz^T Qp (tensor memory, per item),  dQp^T = Kp^T dz^T (per group) -> fp32 atomics.
+// Causality everywhere: key j contributes to token t only when j <= t.
+//
+// Roles of attn_bwd_kernel (256 threads): warp 0 TMA loads of K/V and tensor-memory ownership,
+// warp 1 the MMA issuer, warp 2 gathers the tile's Q / dO rows with cp.async, warp 3 issues the dQ
+// bulk reductions, warps 4-7 softmax / epilogue.  Tensor memory (512 columns): SB0, SB1 (S^T,
+// then P^T), DB0, DB1 (dP^T, then dQ^T), dV, dK.
 #include <math.h>
 
 #include "common.cuh"
 #include "kernels.h"
+#include "sm100.cuh"
+#include "tmap.h"
 
 namespace msa {
-
-constexpr int kLdh = 72;  // padded row (bf16) of 64-column tiles
 
 __global__ void rowdot_kernel(Dims d, const bf16* __restrict__ o, const bf16* __restrict__ dout,
                               float* __restrict__ drow) {
@@ -45,269 +61,752 @@ __global__ void rowdot_kernel(Dims d, const bf16* __restrict__ o, const bf16* __
   }
 }
 
-struct BwdArgs {
+namespace {
+constexpr int kTR = 64;           // rows (tokens x heads) per tile
+constexpr int kPG = 64;           // tokens per proxy group
+constexpr int kItemTokens = 512;  // tokens per work item
+constexpr int kKV = 128 * 128 * 2;  // one 128 x 128 bf16 tile (two SW128 panels)
+constexpr int kRT = kTR * 128 * 2;  // one 64-row x 128 bf16 tile (two panels of 64 rows)
+constexpr int kST = 128 * 128;      // dS^T / dz^T: 128 keys x 64 bf16 (one panel)
+constexpr int kStage = kTR * 128 * 4;  // 64 rows x 128 fp32
+
+struct MainArgs {
   Dims d;
-  const bf16 *q, *k, *v, *qp, *kp, *dout;
-  const float *lse, *drow, *lse_px;
+  const bf16 *q, *dout;
+  const float *lse, *drow;
+  const int* seg_offset;
+  const int* entries;
+  const Item* items;
+  const int* n_items;
+  long long max_items;
+  float *dq, *dk, *dv, *pbar;
+  unsigned* status;
+};
+
+struct MainShared {
+  float lse2[2][kTR];  // row LSE * log2(e), per tile buffer
+  float drow[2][kTR];  // row D, per tile buffer
+  int tok[2][kTR];     // token position of each tile token (-1: none), per tile buffer
+  int epos[2][kTR];    // list entry of each tile token, per tile buffer
+  int rtok[kTR];       // token positions of the staged dQ tile
+  uint64_t kv_full, kv_empty, q_full[2], q_empty[2], s_full[2], p_full[2], ph2_full[2], s_free[2],
+      stage_ready, stage_free, acc_free;
+  uint32_t tmem;
+};
+
+struct ProxyArgs {
+  Dims d;
+  const bf16* qp;
+  const float *lse_px, *pbar;
   float cz;  // kl_grad / (B * S * Hp)
   const int* seg_offset;
   const int* entries;
   const Item* items;
   const int* n_items;
   long long max_items;
-  float *dq, *dk, *dv, *dqp, *dkp;
+  float *dqp, *dkp;
+  unsigned* status;
 };
 
-__device__ __forceinline__ void add2(float* p, float a, float b) {
-  atomicAdd(reinterpret_cast<float2*>(p), make_float2(a, b));
-}
+struct ProxyShared {
+  int tok[2][kPG];
+  float lpx2[2][kPG];
+  uint64_t kp_full, kp_empty, q_full[2], q_empty[2], meta_free[2], z_full, dz_full, fl_full, fl_free,
+      acc_free;
+  uint32_t tmem;
+};
 
+__device__ __forceinline__ void red4(float* p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"l"(p), "f"(a), "f"(b), "f"(c),
+               "f"(d)
+               : "memory");
+}
+__device__ __forceinline__ void red1(float* p, float a) {
+  asm volatile("red.global.add.f32 [%0], %1;\n" ::"l"(p), "f"(a) : "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
+}
+// 2^x with the result flushed to zero below the normal range (probabilities that small do not
+// matter here); one special-function-unit instruction.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// Bulk add of `bytes` fp32 values from shared memory into global memory (TMA reduction).
+__device__ __forceinline__ void bulk_reduce_add(float* g, uint32_t s, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;\n" ::"l"(g),
+               "r"(s), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
+__device__ __forceinline__ uint32_t par(long long k) { return (uint32_t)(k & 1); }
+
+// First token of a dense item / first entry of a sparse item.
+template <bool kDense>
+__device__ __forceinline__ long long item_base(const Dims& d, const int* seg_offset, const Item& it) {
+  if (kDense) {
+    const long long n = it.seg % d.nblk, c = it.seg / d.nseg();
+    const long long lo = (long long)c * d.chunk;
+    return (n * kBlock > lo ? n * kBlock : lo) + it.first;
+  }
+  return (long long)seg_offset[it.seg] + it.first;
+}
+}  // namespace
+
+// ==========================================================================================
 template <int G, bool kDense>
-__global__ void __launch_bounds__(256, 1) fused_bwd_kernel(BwdArgs A) {
-  constexpr int TT = 128 / G;              // tokens per tile
-  constexpr int TP = TT < 16 ? 16 : TT;    // proxy rows, padded to the 16-row product shape
+__global__ void __launch_bounds__(256, 1)
+    attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                    MainArgs A) {
+  using namespace sm100;
+  constexpr int TT = kTR / G;  // tokens per tile
   const Dims& d = A.d;
-  extern __shared__ __align__(128) uint8_t smem[];
-  bf16* sK = reinterpret_cast<bf16*>(smem);  // [64][kLd]
-  bf16* sV = sK + 64 * kLd;
-  bf16* sKp = sV + 64 * kLd;
-  bf16* sQ = sKp + 64 * kLd;                 // [128][kLd]
-  bf16* sdO = sQ + 128 * kLd;                // [128][kLd]
-  bf16* sQp = sdO + 128 * kLd;               // [TP][kLd]
-  bf16* sP = sQp + TP * kLd;                 // [128][kLdh]
-  bf16* sdS = sP + 128 * kLdh;               // [128][kLdh]
-  bf16* sdz = sdS + 128 * kLdh;              // [TP][kLdh]
-  float* sPbar = reinterpret_cast<float*>(sdz + TP * kLdh);  // [TP][64]
-  float* sLse = sPbar + TP * 64;             // [128]
-  float* sD = sLse + 128;                    // [128]
-  float* sLpx = sD + 128;                    // [TP]
-  int* sTok = reinterpret_cast<int*>(sLpx + TP);  // [TP]
+
+  extern __shared__ uint8_t smem_raw[];
+  MainShared* sh = reinterpret_cast<MainShared*>(smem_raw);
+  uint8_t* base = align1024(smem_raw + sizeof(MainShared));
+  uint8_t* sK = base;            // [128 keys][128 d]  (TMA)
+  uint8_t* sV = sK + kKV;
+  uint8_t* sQ = sV + kKV;        // [2][64 rows][128 d]  (gathered)
+  uint8_t* sdO = sQ + 2 * kRT;
+  uint8_t* sdS = sdO + 2 * kRT;  // [2] dS^T [128 keys][64 rows]
+  uint8_t* sSt = sdS + 2 * kST;  // dQ staging [64 rows][128 d] fp32
+  const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ), adO = smem_u32(sdO),
+                 adS = smem_u32(sdS), aSt = smem_u32(sSt);
+  float* stage = reinterpret_cast<float*>(sSt);
 
   const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
   const float sl2 = d.scale * kLog2e;
   long long total = *A.n_items;
   if (total > A.max_items) total = A.max_items;
 
-  for (long long it = blockIdx.x; it < total; it += gridDim.x) {
-    const Item item = A.items[it];
-    const int n = item.seg % d.nblk;
-    const int bg = item.seg / d.nblk;
-    const int b = bg / d.Hp, g = bg % d.Hp;
-    const int j0 = n * kBlock + item.half * 64;  // first key of the half
-    load_rows_async(sK, 64, [&](int r) -> const bf16* {
-      return A.k + (((size_t)b * d.S + j0 + r) * d.Hkv + g) * kD;
-    }, tid, 256, A.k);
-    load_rows_async(sV, 64, [&](int r) -> const bf16* {
-      return A.v + (((size_t)b * d.S + j0 + r) * d.Hkv + g) * kD;
-    }, tid, 256, A.v);
-    load_rows_async(sKp, 64, [&](int r) -> const bf16* {
-      return A.kp + ((size_t)b * d.S + j0 + r) * kD;
-    }, tid, 256, A.kp);
-    cp_async_commit();
-
-    // per-item accumulators: warp w owns keys 16 (w % 4) .. +15, head-dim columns 64 (w / 4) ..
-    float dv[8][4], dk[8][4], dkp[8][4];
-    zero_acc(dv);
-    zero_acc(dk);
-    zero_acc(dkp);
-    const int km0 = 16 * (warp % 4), dn0 = 64 * (warp / 4);
-
-#pragma unroll 1
-    for (int tt = 0; tt < item.count; tt += TT) {
-      const int cnt = min(TT, item.count - tt);
-      if (tid < TP) {
-        int t = -1;
-        if (tid < cnt) {
-          const int pos = item.first + tt + tid;
-          t = kDense ? n * kBlock + pos : (A.entries[A.seg_offset[item.seg] + pos] >> 8);
-        }
-        sTok[tid] = t;
-      }
-      __syncthreads();
-      load_rows_async(sQ, 128, [&](int r) -> const bf16* {
-        const int t = sTok[r / G];
-        return t < 0 ? nullptr : A.q + (((size_t)b * d.S + t) * d.Hq + g * G + r % G) * kD;
-      }, tid, 256, A.q);
-      load_rows_async(sdO, 128, [&](int r) -> const bf16* {
-        const int t = sTok[r / G];
-        return t < 0 ? nullptr : A.dout + (((size_t)b * d.S + t) * d.Hq + g * G + r % G) * kD;
-      }, tid, 256, A.dout);
-      load_rows_async(sQp, TP, [&](int r) -> const bf16* {
-        const int t = sTok[r];
-        return t < 0 ? nullptr : A.qp + (((size_t)b * d.S + t) * d.Hp + g) * kD;
-      }, tid, 256, A.qp);
-      cp_async_commit();
-      if (tid < 128) {
-        const int t = sTok[tid / G];
-        const size_t hrow = ((size_t)b * d.Hq + g * G + tid % G) * d.S;
-        sLse[tid] = t < 0 ? 0.f : A.lse[hrow + t] * kLog2e;
-        sD[tid] = t < 0 ? 0.f : A.drow[hrow + t];
-      }
-      if (tid < TP) {
-        const int t = sTok[tid];
-        sLpx[tid] = t < 0 ? 0.f : A.lse_px[((size_t)b * d.Hp + g) * d.S + t] * kLog2e;
-      }
-      cp_async_wait_all();
-      __syncthreads();
-
-      // ---- main probabilities and score gradients, warp rows 16 w .. 16 w + 15
-      const int ra = warp * 16 + lane / 4, rb = ra + 8;
-      const int ta = sTok[ra / G], tb = sTok[rb / G];
-      float s[8][4], dp[8][4];
-      zero_acc(s);
-      zero_acc(dp);
-      warp_gemm_abt<64, 128>(s, sQ + warp * 16 * kLd, kLd, sK, kLd, lane);
-      warp_gemm_abt<64, 128>(dp, sdO + warp * 16 * kLd, kLd, sV, kLd, lane);
-      const float la = sLse[ra], lb = sLse[rb], Da = sD[ra], Db = sD[rb];
-#pragma unroll
-      for (int jt = 0; jt < 8; ++jt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int j = j0 + 8 * jt + 2 * (lane % 4) + (e & 1);
-          const int t = e < 2 ? ta : tb;
-          const float p = (t >= 0 && j <= t) ? exp2f(s[jt][e] * sl2 - (e < 2 ? la : lb)) : 0.f;
-          s[jt][e] = p;
-          dp[jt][e] = p * (dp[jt][e] - (e < 2 ? Da : Db));
-        }
-      // teacher: sum the G rows of every token (rows of a token are consecutive)
-#pragma unroll
-      for (int jt = 0; jt < 8; ++jt) {
-        float x[4] = {s[jt][0], s[jt][1], s[jt][2], s[jt][3]};
-        if (G == 16) {
-          x[0] += x[2];
-          x[1] += x[3];
-        }
-#pragma unroll
-        for (int off = 4; off < 4 * (G < 8 ? G : 8); off <<= 1)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) x[e] += __shfl_xor_sync(0xffffffffu, x[e], off);
-        const int col = 8 * jt + 2 * (lane % 4);
-        if (G == 16) {
-          if (lane / 4 == 0) {
-            sPbar[warp * 64 + col] = x[0] * (1.f / G);
-            sPbar[warp * 64 + col + 1] = x[1] * (1.f / G);
-          }
-        } else if ((lane / 4) % G == 0) {
-          sPbar[(ra / G) * 64 + col] = x[0] * (1.f / G);
-          sPbar[(ra / G) * 64 + col + 1] = x[1] * (1.f / G);
-          sPbar[(rb / G) * 64 + col] = x[2] * (1.f / G);
-          sPbar[(rb / G) * 64 + col + 1] = x[3] * (1.f / G);
-        }
-      }
-#pragma unroll
-      for (int jt = 0; jt < 8; ++jt) {
-        const int col = 8 * jt + 2 * (lane % 4);
-        *reinterpret_cast<uint32_t*>(sP + ra * kLdh + col) = pack_bf16(s[jt][0], s[jt][1]);
-        *reinterpret_cast<uint32_t*>(sP + rb * kLdh + col) = pack_bf16(s[jt][2], s[jt][3]);
-        *reinterpret_cast<uint32_t*>(sdS + ra * kLdh + col) = pack_bf16(dp[jt][0], dp[jt][1]);
-        *reinterpret_cast<uint32_t*>(sdS + rb * kLdh + col) = pack_bf16(dp[jt][2], dp[jt][3]);
-      }
-      // dQ rows of this warp: scale dS K
-      {
-        uint32_t da[4][4];
-        c_to_a<64>(da, dp);
-        float dq[16][4];
-        zero_acc(dq);
-        warp_gemm_rb<128, 64>(dq, da, sK, kLd, lane);
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const int row = r == 0 ? ra : rb;
-          const int t = r == 0 ? ta : tb;
-          if (t < 0) continue;
-          float* dst = A.dq + (((size_t)b * d.S + t) * d.Hq + g * G + row % G) * kD + 2 * (lane % 4);
-#pragma unroll
-          for (int jt = 0; jt < 16; ++jt)
-            add2(dst + 8 * jt, dq[jt][2 * r] * d.scale, dq[jt][2 * r + 1] * d.scale);
-        }
-      }
-      __syncthreads();
-
-      // ---- dV += P^T dO, dK += dS^T Q  (scale applied at the end)
-      warp_gemm_atb<64, 128>(dv, sP, kLdh, km0, sdO + dn0, kLd, lane);
-      warp_gemm_atb<64, 128>(dk, sdS, kLdh, km0, sQ + dn0, kLd, lane);
-
-      // ---- student probabilities and dz (proxy rows x 64 keys, in 16 x 16 units)
-      for (int u = warp; u < (TP / 16) * 4; u += 8) {
-        const int mt = u / 4, nt = u % 4;
-        float z[2][4];
-        zero_acc(z);
-        warp_gemm_abt<16, 128>(z, sQp + mt * 16 * kLd, kLd, sKp + nt * 16 * kLd, kLd, lane);
-        const int pa_ = mt * 16 + lane / 4, pb_ = pa_ + 8;
-        const int tpa = sTok[pa_], tpb = sTok[pb_];
-#pragma unroll
-        for (int jt = 0; jt < 2; ++jt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int row = e < 2 ? pa_ : pb_;
-            const int t = e < 2 ? tpa : tpb;
-            const int col = nt * 16 + 8 * jt + 2 * (lane % 4) + (e & 1);
-            const int j = j0 + col;
-            float dz = 0.f;
-            if (t >= 0 && j <= t) {
-              const float ppx = exp2f(z[jt][e] * sl2 - sLpx[row]);
-              dz = A.cz * (ppx - sPbar[row * 64 + col]);
-            }
-            z[jt][e] = dz;
-          }
-#pragma unroll
-        for (int jt = 0; jt < 2; ++jt) {
-          const int col = nt * 16 + 8 * jt + 2 * (lane % 4);
-          *reinterpret_cast<uint32_t*>(sdz + pa_ * kLdh + col) = pack_bf16(z[jt][0], z[jt][1]);
-          *reinterpret_cast<uint32_t*>(sdz + pb_ * kLdh + col) = pack_bf16(z[jt][2], z[jt][3]);
-        }
-      }
-      __syncthreads();
-
-      // ---- dQp = scale dz Kp (fp32 atomics), dKp += dz^T Qp
-      for (int u = warp; u < (TP / 16) * 2; u += 8) {
-        const int mt = u / 2, nh = u % 2;
-        float acc[8][4];
-        zero_acc(acc);
-        warp_gemm_ab<64, 64>(acc, sdz + mt * 16 * kLdh, kLdh, sKp + nh * 64, kLd, lane);
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          const int row = mt * 16 + lane / 4 + 8 * r;
-          const int t = sTok[row];
-          if (t < 0) continue;
-          float* dst = A.dqp + (((size_t)b * d.S + t) * d.Hp + g) * kD + nh * 64 + 2 * (lane % 4);
-#pragma unroll
-          for (int jt = 0; jt < 8; ++jt)
-            add2(dst + 8 * jt, acc[jt][2 * r] * d.scale, acc[jt][2 * r + 1] * d.scale);
-        }
-      }
-      warp_gemm_atb<64, TP>(dkp, sdz, kLdh, km0, sQp + dn0, kLd, lane);
-      __syncthreads();
+  if (tid == 0) {
+    mbar_init(&sh->kv_full, 1);
+    mbar_init(&sh->kv_empty, 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&sh->q_full[x], 32);
+      mbar_init(&sh->q_empty[x], 1);
+      mbar_init(&sh->s_full[x], 1);
+      mbar_init(&sh->p_full[x], 4);
+      mbar_init(&sh->ph2_full[x], 1);
+      mbar_init(&sh->s_free[x], 4);
     }
-
-    // ---- item epilogue: dK (scaled), dV, dKp (scaled) into the fp32 accumulators
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int j = j0 + km0 + lane / 4 + 8 * r;
-      float* pk = A.dk + (((size_t)b * d.S + j) * d.Hkv + g) * kD + dn0 + 2 * (lane % 4);
-      float* pv = A.dv + (((size_t)b * d.S + j) * d.Hkv + g) * kD + dn0 + 2 * (lane % 4);
-      float* pkp = A.dkp + ((size_t)b * d.S + j) * kD + dn0 + 2 * (lane % 4);
-#pragma unroll
-      for (int jt = 0; jt < 8; ++jt) {
-        add2(pk + 8 * jt, dk[jt][2 * r] * d.scale, dk[jt][2 * r + 1] * d.scale);
-        add2(pv + 8 * jt, dv[jt][2 * r], dv[jt][2 * r + 1]);
-        add2(pkp + 8 * jt, dkp[jt][2 * r] * d.scale, dkp[jt][2 * r + 1] * d.scale);
-      }
-    }
-    __syncthreads();
+    mbar_init(&sh->stage_ready, 4);
+    mbar_init(&sh->stage_free, 1);
+    mbar_init(&sh->acc_free, 4);
+    mbar_fence_init();
   }
+  if (warp == 0) {
+    tmem_alloc(&sh->tmem, 512);
+    tmem_relinquish();
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = sh->tmem;
+  const uint32_t SB0 = tmem, DB0 = tmem + 128, RV = tmem + 256, RK = tmem + 384;
+  bool ok = true;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA: K, V per item
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      long long ni = 0;
+      for (long long it = blockIdx.x; it < total; it += gridDim.x, ++ni) {
+        const Item item = A.items[it];
+        const int n = item.seg % d.nblk;
+        const int bg = (int)((item.seg % d.nseg()) / d.nblk);
+        const int b = bg / d.Hp, g = bg % d.Hp;
+        if (ni > 0 && !mbar_wait(&sh->kv_empty, par(ni - 1), A.status)) break;
+        const int row0 = b * d.S + n * kBlock;
+        mbar_expect_tx(&sh->kv_full, 2 * kKV);
+        tma_load_3d(sK, &tm_k, 0, g, row0, &sh->kv_full);
+        tma_load_3d(sK + kKV / 2, &tm_k, 64, g, row0, &sh->kv_full);
+        tma_load_3d(sV, &tm_v, 0, g, row0, &sh->kv_full);
+        tma_load_3d(sV + kKV / 2, &tm_v, 64, g, row0, &sh->kv_full);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16(128, kTR, false, false);  // S^T, dP^T
+      constexpr uint32_t id_g = idesc_bf16(128, 128, false, true);   // dV, dK
+      constexpr uint32_t id_q = idesc_bf16(128, kTR, true, true);    // dQ^T
+      long long ni = 0, i = 0;
+      bool first_of_item = true;
+      auto phase2 = [&](long long ti) -> bool {
+        const int b = (int)(ti & 1);
+        if (!mbar_wait(&sh->p_full[b], par(ti >> 1), A.status)) return false;
+        if (first_of_item && ni > 0 && !mbar_wait(&sh->acc_free, par(ni - 1), A.status)) return false;
+        fence_after_sync();
+        const bool acc = !first_of_item;
+        first_of_item = false;
+        const uint32_t aQb = aQ + b * kRT, adOb = adO + b * kRT, adSb = adS + b * kST;
+        const uint32_t SBb = SB0 + 64 * b, DBb = DB0 + 64 * b;
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)  // dV += P^T dO  (P^T from tensor memory)
+          mma_ts(RV, SBb + ks * 8, desc_mnmajor(adOb, kTR, ks), id_g, acc || ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)  // dK += dS^T Q
+          mma_ss(RK, desc_kmajor(adSb, 128, ks), desc_mnmajor(aQb, kTR, ks), id_g, acc || ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)  // dQ^T = K^T dS^T
+          mma_ss(DBb, desc_mnmajor(aK, 128, ks), desc_mnmajor(adSb, 128, ks), id_q, ks > 0);
+        mma_commit(&sh->ph2_full[b]);
+        mma_commit(&sh->q_empty[b]);
+        return true;
+      };
+      for (long long it = blockIdx.x; ok && it < total; it += gridDim.x, ++ni) {
+        const Item item = A.items[it];
+        if (!mbar_wait(&sh->kv_full, par(ni), A.status)) { ok = false; break; }
+        first_of_item = true;
+        const int ntiles = (item.count + TT - 1) / TT;
+        for (int tl = 0; tl < ntiles; ++tl, ++i) {
+          const int b = (int)(i & 1);
+          if (!mbar_wait(&sh->q_full[b], par(i >> 1), A.status)) { ok = false; break; }
+          if (i >= 2 && !mbar_wait(&sh->s_free[b], par((i - 2) >> 1), A.status)) { ok = false; break; }
+          fence_after_sync();
+          const uint32_t aQb = aQ + b * kRT, adOb = adO + b * kRT;
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)  // S^T = K Q^T
+            mma_ss(SB0 + 64 * b, desc_kmajor(aK, 128, ks), desc_kmajor(aQb, kTR, ks), id_s, ks > 0);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)  // dP^T = V dO^T
+            mma_ss(DB0 + 64 * b, desc_kmajor(aV, 128, ks), desc_kmajor(adOb, kTR, ks), id_s, ks > 0);
+          mma_commit(&sh->s_full[b]);
+          if (tl > 0 && !phase2(i - 1)) { ok = false; break; }
+        }
+        if (!ok) break;
+        if (!phase2(i - 1)) { ok = false; break; }
+        mma_commit(&sh->kv_empty);
+      }
+    }
+  } else if (warp == 2) {
+    // ---------------------------------------------------------------- gather: Q, dO rows
+    long long i = 0;
+    for (long long it = blockIdx.x; ok && it < total; it += gridDim.x) {
+      const Item item = A.items[it];
+      const int bg = (int)((item.seg % d.nseg()) / d.nblk);
+      const int b = bg / d.Hp, g = bg % d.Hp;
+      const long long tb = item_base<kDense>(d, A.seg_offset, item);
+      const long long eb = (long long)A.seg_offset[item.seg] + item.first;
+      auto load_tokens = [&](int pos0, int valid, int (&tv)[TT]) {
+#pragma unroll
+        for (int x = 0; x < TT; ++x)
+          tv[x] = x < valid ? (kDense ? (int)(tb + pos0 + x) : (A.entries[tb + pos0 + x] >> 8)) : -1;
+      };
+      const int ntiles = (item.count + TT - 1) / TT;
+      int tv[TT];
+      load_tokens(0, min(TT, item.count), tv);
+      for (int tl = 0; tl < ntiles; ++tl, ++i) {
+        const int bb = (int)(i & 1);
+        // per-row metadata (rows lane, lane + 32), then the next tile's positions
+        float ml[2], md[2];
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const int r = lane + 32 * h2;
+          int t = -1;
+#pragma unroll
+          for (int x = 0; x < TT; ++x)
+            if (x == r / G) t = tv[x];
+          const size_t hrow = ((size_t)b * d.Hq + g * G + r % G) * d.S;
+          ml[h2] = t < 0 ? 0.f : A.lse[hrow + t] * kLog2e;
+          md[h2] = t < 0 ? 0.f : A.drow[hrow + t];
+        }
+        int tn[TT];
+        load_tokens((tl + 1) * TT, min(TT, item.count - (tl + 1) * TT), tn);
+        if (i >= 2 && !mbar_wait(&sh->q_empty[bb], par((i - 2) >> 1), A.status)) { ok = false; break; }
+        uint8_t* dQb = sQ + bb * kRT;
+        uint8_t* ddOb = sdO + bb * kRT;
+#pragma unroll
+        for (int k = 0; k < (kTR * 16) / 32; ++k) {
+          const int c = lane + 32 * k;
+          const int r = c >> 4, ch = c & 15;
+          int t = -1;
+#pragma unroll
+          for (int x = 0; x < TT; ++x)
+            if (x == r / G) t = tv[x];
+          const uint32_t off = (ch >> 3) * (kTR * 128) + sm100::sw128_chunk(r, ch & 7);
+          const size_t grow = (((size_t)b * d.S + (t < 0 ? 0 : t)) * d.Hq + g * G + r % G) * kD + ch * 8;
+          cp_async16(dQb + off, A.q + grow, t >= 0);
+          cp_async16(ddOb + off, A.dout + grow, t >= 0);
+        }
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          sh->lse2[bb][lane + 32 * h2] = ml[h2];
+          sh->drow[bb][lane + 32 * h2] = md[h2];
+        }
+#pragma unroll
+        for (int x = 0; x < TT; ++x)
+          if (lane == x) {
+            sh->tok[bb][x] = tv[x];
+            sh->epos[bb][x] = (int)(eb + tl * TT + x);
+          }
+        cp_async_wait_all();
+        fence_async_smem();
+        mbar_arrive(&sh->q_full[bb]);
+#pragma unroll
+        for (int x = 0; x < TT; ++x) tv[x] = tn[x];
+      }
+    }
+  } else if (warp == 3) {
+    // ---------------------------------------------------------------- dQ reducer
+    if (lane == 0) {
+      long long ns = 0;
+      for (long long it = blockIdx.x; ok && it < total; it += gridDim.x) {
+        const Item item = A.items[it];
+        const int bg = (int)((item.seg % d.nseg()) / d.nblk);
+        const int b = bg / d.Hp, g = bg % d.Hp;
+        const int ntiles = (item.count + TT - 1) / TT;
+        for (int tl = 0; tl < ntiles; ++tl, ++ns) {
+          if (!mbar_wait(&sh->stage_ready, par(ns), A.status)) { ok = false; break; }
+#pragma unroll 1
+          for (int x = 0; x < TT; ++x) {
+            const int t = sh->rtok[x];
+            if (t >= 0)
+              bulk_reduce_add(A.dq + (((size_t)b * d.S + t) * d.Hq + g * G) * kD,
+                              aSt + x * G * kD * 4, G * kD * 4);
+          }
+          bulk_commit();
+          bulk_wait_read0();
+          mbar_arrive(&sh->stage_free);
+        }
+      }
+      bulk_wait0();
+    }
+  } else {
+    // ---------------------------------------------------------------- softmax / epilogue
+    const int w4 = warp - 4;
+    const int kr = w4 * 32 + lane;  // key row of S^T / dP^T (TMEM lane); head-dim index of dQ^T
+    const uint32_t lb = static_cast<uint32_t>(w4 * 32) << 16;
+    long long i = 0, ns = 0;
+    int tprev[TT];
+    auto epilogue = [&](long long ti) -> bool {
+      const int bb = (int)(ti & 1);
+      __syncwarp();
+      if (!mbar_wait(&sh->ph2_full[bb], par(ti >> 1), A.status)) return false;
+      fence_after_sync();
+      uint32_t r0[32], r1[32];
+      tmem_ld32(DB0 + 64 * bb + lb, r0);
+      tmem_ld32(DB0 + 64 * bb + lb + 32, r1);
+      tmem_wait_ld();
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh->s_free[bb]);
+      if (ns > 0 && !mbar_wait(&sh->stage_free, par(ns - 1), A.status)) return false;
+#pragma unroll
+      for (int r = 0; r < 32; ++r) {
+        stage[r * kD + kr] = __uint_as_float(r0[r]) * d.scale;
+        stage[(r + 32) * kD + kr] = __uint_as_float(r1[r]) * d.scale;
+      }
+#pragma unroll
+      for (int x = 0; x < TT; ++x)
+        if (kr == x) sh->rtok[x] = tprev[x];
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh->stage_ready);
+      ++ns;
+      return true;
+    };
+    for (long long it = blockIdx.x; ok && it < total; it += gridDim.x) {
+      const Item item = A.items[it];
+      const int n = item.seg % d.nblk;
+      const int bg = (int)((item.seg % d.nseg()) / d.nblk);
+      const int b = bg / d.Hp, g = bg % d.Hp;
+      const int j = n * kBlock + kr;  // this thread's key
+      const int ntiles = (item.count + TT - 1) / TT;
+      for (int tl = 0; tl < ntiles; ++tl, ++i) {
+        const int bb = (int)(i & 1);
+        __syncwarp();
+        if (!mbar_wait(&sh->q_full[bb], par(i >> 1), A.status) ||
+            !mbar_wait(&sh->s_full[bb], par(i >> 1), A.status)) {
+          ok = false;
+          break;
+        }
+        fence_after_sync();
+        // ---- softmax of tile i
+        int tv[TT], ev[TT];
+        bool vis[TT];
+        float pb[TT];
+#pragma unroll
+        for (int x = 0; x < TT; ++x) {
+          tv[x] = sh->tok[bb][x];
+          ev[x] = sh->epos[bb][x];
+          vis[x] = tv[x] >= 0 && j <= tv[x];
+          pb[x] = 0.f;
+        }
+        uint32_t rs0[32], rs1[32], rp0[32], rp1[32];
+        const uint32_t SBb = SB0 + 64 * bb, DBb = DB0 + 64 * bb;
+        tmem_ld32(SBb + lb, rs0);
+        tmem_ld32(SBb + lb + 32, rs1);
+        tmem_ld32(DBb + lb, rp0);
+        tmem_ld32(DBb + lb + 32, rp1);
+        tmem_wait_ld();
+        const uint32_t adSb = adS + bb * kST;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t pw[16], dw[16];
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) {
+            const float4 l4 = reinterpret_cast<const float4*>(sh->lse2[bb])[c * 8 + q4];
+            const float4 d4 = reinterpret_cast<const float4*>(sh->drow[bb])[c * 8 + q4];
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+            const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+            float pv[4], dsv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int r = c * 32 + q4 * 4 + e;
+              const int x = r / G;
+              const float sv = __uint_as_float(c == 0 ? rs0[q4 * 4 + e] : rs1[q4 * 4 + e]);
+              const float dpv = __uint_as_float(c == 0 ? rp0[q4 * 4 + e] : rp1[q4 * 4 + e]);
+              const float p = vis[x] ? ex2(sv * sl2 - lv[e]) : 0.f;
+              pv[e] = p;
+              dsv[e] = p * (dpv - dv4[e]);
+              pb[x] += p;
+            }
+            pw[2 * q4] = pack_bf16(pv[0], pv[1]);
+            pw[2 * q4 + 1] = pack_bf16(pv[2], pv[3]);
+            dw[2 * q4] = pack_bf16(dsv[0], dsv[1]);
+            dw[2 * q4 + 1] = pack_bf16(dsv[2], dsv[3]);
+          }
+          tmem_st16(SBb + lb + c * 16, pw);  // P^T: row r packed into column r / 2
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            st_shared_v4(adSb + sm100::sw128_chunk(kr, c * 4 + u), dw[4 * u], dw[4 * u + 1],
+                         dw[4 * u + 2], dw[4 * u + 3]);
+        }
+        tmem_wait_st();
+        fence_async_smem();
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh->p_full[bb]);
+        // teacher: mean of the G heads' probabilities of each token, one fp32 row per list entry
+#pragma unroll
+        for (int x = 0; x < TT; ++x)
+          if (tv[x] >= 0) A.pbar[(size_t)ev[x] * kBlock + kr] = pb[x] * (1.f / G);
+        // ---- epilogue of the previous tile
+        if (tl > 0 && !epilogue(i - 1)) { ok = false; break; }
+#pragma unroll
+        for (int x = 0; x < TT; ++x) tprev[x] = tv[x];
+      }
+      if (!ok) break;
+      if (!epilogue(i - 1)) { ok = false; break; }
+      // ---- item end: dV and dK rows of this key
+      {
+        float* pv = A.dv + (((size_t)b * d.S + j) * d.Hkv + g) * kD;
+        float* pk = A.dk + (((size_t)b * d.S + j) * d.Hkv + g) * kD;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t rv[32], rk[32];
+          tmem_ld32(RV + lb + c * 32, rv);
+          tmem_ld32(RK + lb + c * 32, rk);
+          tmem_wait_ld();
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            red4(pv + c * 32 + 4 * u, __uint_as_float(rv[4 * u]), __uint_as_float(rv[4 * u + 1]),
+                 __uint_as_float(rv[4 * u + 2]), __uint_as_float(rv[4 * u + 3]));
+            red4(pk + c * 32 + 4 * u, __uint_as_float(rk[4 * u]) * d.scale,
+                 __uint_as_float(rk[4 * u + 1]) * d.scale, __uint_as_float(rk[4 * u + 2]) * d.scale,
+                 __uint_as_float(rk[4 * u + 3]) * d.scale);
+          }
+        }
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh->acc_free);
+      }
+    }
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
-template <int G, bool kDense>
-static void fused_bwd_g(const BwdArgs& a, cudaStream_t st) {
-  constexpr int TT = 128 / G;
-  constexpr int TP = TT < 16 ? 16 : TT;
-  const size_t smem = (size_t)(3 * 64 + 2 * 128 + TP) * kLd * sizeof(bf16) +
-                      (size_t)(2 * 128 + TP) * kLdh * sizeof(bf16) +
-                      (size_t)(TP * 64 + 2 * 128 + TP) * sizeof(float) + TP * sizeof(int);
-  cudaFuncSetAttribute(fused_bwd_kernel<G, kDense>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       (int)smem);
-  fused_bwd_kernel<G, kDense><<<num_sms(), 256, smem, st>>>(a);
+// ==========================================================================================
+// Proxy gradients of the KL term from the teacher pbar written by attn_bwd_kernel.
+// Roles: warp 0 TMA of the block's proxy keys + tensor memory, warp 1 MMA, warp 2 gathers the
+// group's Qp rows and pbar rows, warps 4-7 compute dz (thread = key) and read the results out.
+// Tensor memory (256 columns): Z (z^T, 64), QP (dQp^T, 64), KP (dKp accumulator, 128).
+template <bool kDense>
+__global__ void __launch_bounds__(256, 1)
+    proxy_bwd_kernel(const __grid_constant__ CUtensorMap tm_kp, ProxyArgs A) {
+  using namespace sm100;
+  const Dims& d = A.d;
+  extern __shared__ uint8_t smem_raw[];
+  ProxyShared* sh = reinterpret_cast<ProxyShared*>(smem_raw);
+  uint8_t* base = align1024(smem_raw + sizeof(ProxyShared));
+  uint8_t* sKp = base;             // [128 keys][128 d]  (TMA)
+  uint8_t* sQp = sKp + kKV;        // [2][64 tokens][128 d]
+  uint8_t* sdz = sQp + 2 * kRT;    // dz^T [128 keys][64 tokens]
+  float* sPb = reinterpret_cast<float*>(sdz + kST);  // [2][64 entries][128 keys] fp32
+  const uint32_t aKp = smem_u32(sKp), aQp = smem_u32(sQp), adz = smem_u32(sdz);
+
+  const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
+  const float sl2 = d.scale * kLog2e;
+  long long total = *A.n_items;
+  if (total > A.max_items) total = A.max_items;
+  if (tid == 0) {
+    mbar_init(&sh->kp_full, 1);
+    mbar_init(&sh->kp_empty, 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&sh->q_full[x], 32);
+      mbar_init(&sh->q_empty[x], 1);
+      mbar_init(&sh->meta_free[x], 4);
+    }
+    mbar_init(&sh->z_full, 1);
+    mbar_init(&sh->dz_full, 4);
+    mbar_init(&sh->fl_full, 1);
+    mbar_init(&sh->fl_free, 4);
+    mbar_init(&sh->acc_free, 4);
+    mbar_fence_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&sh->tmem, 256);
+    tmem_relinquish();
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = sh->tmem;
+  const uint32_t RZ = tmem, RQ = tmem + 64, RKP = tmem + 128;
+  bool ok = true;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_kp);
+      long long ni = 0;
+      for (long long it = blockIdx.x; it < total; it += gridDim.x, ++ni) {
+        const Item item = A.items[it];
+        const int n = item.seg % d.nblk;
+        const int bg = (int)((item.seg % d.nseg()) / d.nblk);
+        const int b = bg / d.Hp;
+        if (ni > 0 && !mbar_wait(&sh->kp_empty, par(ni - 1), A.status)) break;
+        mbar_expect_tx(&sh->kp_full, kKV);
+        tma_load_2d(sKp, &tm_kp, 0, b * d.S + n * kBlock, &sh->kp_full);
+        tma_load_2d(sKp + kKV / 2, &tm_kp, 64, b * d.S + n * kBlock, &sh->kp_full);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t id_z = idesc_bf16(128, kPG, false, false);
+      constexpr uint32_t id_k = idesc_bf16(128, 128, false, true);
+      constexpr uint32_t id_p = idesc_bf16(128, kPG, true, true);
+      long long ni = 0, i = 0;
+      for (long long it = blockIdx.x; ok && it < total; it += gridDim.x, ++ni) {
+        const Item item = A.items[it];
+        if (!mbar_wait(&sh->kp_full, par(ni), A.status)) { ok = false; break; }
+        const int ngroups = (item.count + kPG - 1) / kPG;
+        for (int gi = 0; gi < ngroups; ++gi, ++i) {
+          const int b = (int)(i & 1);
+          const int gcount = min(kPG, item.count - gi * kPG);
+          if (!mbar_wait(&sh->q_full[b], par(i >> 1), A.status)) { ok = false; break; }
+          if (i > 0 && !mbar_wait(&sh->fl_free, par(i - 1), A.status)) { ok = false; break; }
+          fence_after_sync();
+          const uint32_t aQb = aQp + b * kRT;
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)  // z^T = Kp Qp^T
+            mma_ss(RZ, desc_kmajor(aKp, 128, ks), desc_kmajor(aQb, kPG, ks), id_z, ks > 0);
+          mma_commit(&sh->z_full);
+          if (!mbar_wait(&sh->dz_full, par(i), A.status)) { ok = false; break; }
+          if (gi == 0 && ni > 0 && !mbar_wait(&sh->acc_free, par(ni - 1), A.status)) { ok = false; break; }
+          fence_after_sync();
+          const int kst = (gcount + 15) / 16;
+          for (int ks = 0; ks < kst; ++ks)  // dKp += dz^T Qp
+            mma_ss(RKP, desc_kmajor(adz, 128, ks), desc_mnmajor(aQb, kPG, ks), id_k, gi > 0 || ks > 0);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)  // dQp^T = Kp^T dz^T
+            mma_ss(RQ, desc_mnmajor(aKp, 128, ks), desc_mnmajor(adz, 128, ks), id_p, ks > 0);
+          mma_commit(&sh->fl_full);
+          mma_commit(&sh->q_empty[b]);
+        }
+        if (!ok) break;
+        mma_commit(&sh->kp_empty);
+      }
+    }
+  } else if (warp == 2) {
+    long long i = 0;
+    for (long long it = blockIdx.x; ok && it < total; it += gridDim.x) {
+      const Item item = A.items[it];
+      const int bg = (int)((item.seg % d.nseg()) / d.nblk);
+      const int b = bg / d.Hp, g = bg % d.Hp;
+      const long long tb = item_base<kDense>(d, A.seg_offset, item);
+      const long long eb = (long long)A.seg_offset[item.seg] + item.first;
+      const int ngroups = (item.count + kPG - 1) / kPG;
+      for (int gi = 0; gi < ngroups; ++gi, ++i) {
+        const int bb = (int)(i & 1);
+        const int gcount = min(kPG, item.count - gi * kPG);
+        int tv[2];
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const int x = lane + 32 * h2;
+          const long long pos = (long long)gi * kPG + x;
+          tv[h2] = x < gcount ? (kDense ? (int)(tb + pos) : (A.entries[tb + pos] >> 8)) : -1;
+        }
+        float lp[2];
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2)
+          lp[h2] = tv[h2] < 0 ? 0.f : A.lse_px[((size_t)b * d.Hp + g) * d.S + tv[h2]] * kLog2e;
+        if (i >= 2 && (!mbar_wait(&sh->q_empty[bb], par((i - 2) >> 1), A.status) ||
+                       !mbar_wait(&sh->meta_free[bb], par((i - 2) >> 1), A.status))) {
+          ok = false;
+          break;
+        }
+        // proxy query rows (K-major SW128), rows >= gcount zero-filled
+        uint8_t* dQb = sQp + bb * kRT;
+        for (int c = lane; c < kPG * 16; c += 32) {
+          const int r = c >> 4, ch = c & 15;
+          const int t = __shfl_sync(0xffffffffu, tv[r >= 32 ? 1 : 0], r & 31);
+          const uint32_t off = (ch >> 3) * (kPG * 128) + sm100::sw128_chunk(r, ch & 7);
+          const size_t grow = (((size_t)b * d.S + (t < 0 ? 0 : t)) * d.Hp + g) * kD + ch * 8;
+          cp_async16(dQb + off, A.qp + grow, t >= 0);
+        }
+        // teacher rows: gcount entries x 128 keys, contiguous in the pbar buffer
+        float* dPb = sPb + bb * kPG * kBlock;
+        const float* src = A.pbar + (size_t)(eb + gi * kPG) * kBlock;
+        for (int c = lane; c < gcount * 32; c += 32) cp_async16(dPb + c * 4, src + c * 4);
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          sh->tok[bb][lane + 32 * h2] = tv[h2];
+          sh->lpx2[bb][lane + 32 * h2] = lp[h2];
+        }
+        cp_async_wait_all();
+        fence_async_smem();
+        mbar_arrive(&sh->q_full[bb]);
+      }
+    }
+  } else if (warp >= 4) {
+    const int w4 = warp - 4;
+    const int kr = w4 * 32 + lane;  // key (TMEM lane of z^T, dKp); head-dim index for dQp^T
+    const uint32_t lb = static_cast<uint32_t>(w4 * 32) << 16;
+    long long i = 0;
+    for (long long it = blockIdx.x; ok && it < total; it += gridDim.x) {
+      const Item item = A.items[it];
+      const int n = item.seg % d.nblk;
+      const int bg = (int)((item.seg % d.nseg()) / d.nblk);
+      const int b = bg / d.Hp, g = bg % d.Hp;
+      const int j = n * kBlock + kr;
+      const int ngroups = (item.count + kPG - 1) / kPG;
+      for (int gi = 0; gi < ngroups; ++gi, ++i) {
+        const int bb = (int)(i & 1);
+        const int gcount = min(kPG, item.count - gi * kPG);
+        __syncwarp();
+        if (!mbar_wait(&sh->q_full[bb], par(i >> 1), A.status) ||
+            !mbar_wait(&sh->z_full, par(i), A.status)) {
+          ok = false;
+          break;
+        }
+        fence_after_sync();
+        uint32_t z0[32], z1[32];
+        tmem_ld32(RZ + lb, z0);
+        tmem_ld32(RZ + lb + 32, z1);
+        tmem_wait_ld();
+        const float* pbr = sPb + bb * kPG * kBlock;
+        uint32_t zw[kPG / 2];
+#pragma unroll
+        for (int k2 = 0; k2 < kPG / 2; ++k2) {
+          float dzv[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int k = 2 * k2 + e;
+            const int t = sh->tok[bb][k];
+            float v = 0.f;
+            if (k < gcount && t >= 0 && j <= t) {
+              const float zz = __uint_as_float(k < 32 ? z0[k] : z1[k - 32]);
+              v = A.cz * (ex2(zz * sl2 - sh->lpx2[bb][k]) - pbr[k * kBlock + kr]);
+            }
+            dzv[e] = v;
+          }
+          zw[k2] = pack_bf16(dzv[0], dzv[1]);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          st_shared_v4(adz + sm100::sw128_chunk(kr, u), zw[4 * u], zw[4 * u + 1], zw[4 * u + 2],
+                       zw[4 * u + 3]);
+        fence_async_smem();
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh->dz_full);
+        if (!mbar_wait(&sh->fl_full, par(i), A.status)) { ok = false; break; }
+        fence_after_sync();
+        uint32_t q0[32], q1[32];
+        tmem_ld32(RQ + lb, q0);
+        tmem_ld32(RQ + lb + 32, q1);
+        tmem_wait_ld();
+        const bool last = gi == ngroups - 1;
+        if (!last) {
+          fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh->fl_free);
+        }
+#pragma unroll
+        for (int k = 0; k < kPG; ++k) {  // dQp^T: TMEM lane = head-dim index kr
+          const int t = k < gcount ? sh->tok[bb][k] : -1;
+          if (t >= 0)
+            red1(A.dqp + (((size_t)b * d.S + t) * d.Hp + g) * kD + kr,
+                 __uint_as_float(k < 32 ? q0[k] : q1[k - 32]) * d.scale);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh->meta_free[bb]);  // token metadata of this buffer read
+        if (last) {  // item end: dKp rows of this key
+          float* dst = A.dkp + ((size_t)b * d.S + j) * kD;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t rk[32];
+            tmem_ld32(RKP + lb + c * 32, rk);
+            tmem_wait_ld();
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              red4(dst + c * 32 + 4 * u, __uint_as_float(rk[4 * u]) * d.scale,
+                   __uint_as_float(rk[4 * u + 1]) * d.scale, __uint_as_float(rk[4 * u + 2]) * d.scale,
+                   __uint_as_float(rk[4 * u + 3]) * d.scale);
+          }
+          fence_before_sync();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&sh->fl_free);
+            mbar_arrive(&sh->acc_free);
+          }
+        }
+      }
+    }
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (warp == 0) tmem_dealloc(tmem, 256);
 }
+
+namespace {
+template <int G, bool kDense>
+void attn_bwd_g(const CUtensorMap& mk, const CUtensorMap& mv, const MainArgs& a, cudaStream_t st) {
+  const size_t smem = sizeof(MainShared) + 1024 + 2 * (size_t)kKV + 4 * (size_t)kRT +
+                      2 * (size_t)kST + kStage;
+  cudaFuncSetAttribute(attn_bwd_kernel<G, kDense>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       (int)smem);
+  attn_bwd_kernel<G, kDense><<<num_sms(), 256, smem, st>>>(mk, mv, a);
+}
+template <bool kDense>
+void proxy_bwd_g(const CUtensorMap& mkp, const ProxyArgs& a, cudaStream_t st) {
+  const size_t smem = sizeof(ProxyShared) + 1024 + (size_t)kKV + 2 * (size_t)kRT + kST +
+                      2 * (size_t)kPG * kBlock * 4;
+  cudaFuncSetAttribute(proxy_bwd_kernel<kDense>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       (int)smem);
+  proxy_bwd_kernel<kDense><<<num_sms(), 256, smem, st>>>(mkp, a);
+}
+}  // namespace
+
+int bwd_item_tokens() { return kItemTokens; }
+int bwd_group_tokens() { return kPG; }
 
 void launch_bwd_rowdot(const Dims& d, const void* o, const void* dout, float* drow,
                        cudaStream_t st) {
@@ -317,24 +816,23 @@ void launch_bwd_rowdot(const Dims& d, const void* o, const void* dout, float* dr
   rowdot_kernel<<<(int)grid, 256, 0, st>>>(d, (const bf16*)o, (const bf16*)dout, drow);
 }
 
-void launch_fused_bwd(const Dims& d, bool dense, const void* q, const void* k, const void* v,
-                      const void* qp, const void* kp, const void* dout, const float* lse,
-                      const float* drow, const float* lse_px, float kl_grad,
-                      const int* seg_offset, const int* entries, const Item* items,
-                      const int* n_items, long long max_items, float* dq_acc, float* dk_acc,
-                      float* dv_acc, float* dqp_acc, float* dkp_acc, cudaStream_t st) {
-  BwdArgs a;
+bool launch_attn_bwd(const Dims& d, bool dense, const void* q, const void* k, const void* v,
+                     const void* dout, const float* lse, const float* drow, const int* seg_offset,
+                     const int* entries, const Item* items, const int* n_items, long long max_items,
+                     float* dq_acc, float* dk_acc, float* dv_acc, float* pbar, unsigned* status,
+                     cudaStream_t st) {
+  CUtensorMap mk, mv;
+  const uint64_t kvd[3] = {128, (uint64_t)d.Hkv, (uint64_t)d.B * d.S};
+  const uint64_t kvs[2] = {128 * 2, (uint64_t)d.Hkv * 128 * 2};
+  const uint32_t kvb[3] = {64, 1, 128};
+  if (!make_tmap_bf16(&mk, k, 3, kvd, kvs, kvb) || !make_tmap_bf16(&mv, v, 3, kvd, kvs, kvb))
+    return false;
+  MainArgs a;
   a.d = d;
   a.q = (const bf16*)q;
-  a.k = (const bf16*)k;
-  a.v = (const bf16*)v;
-  a.qp = (const bf16*)qp;
-  a.kp = (const bf16*)kp;
   a.dout = (const bf16*)dout;
   a.lse = lse;
   a.drow = drow;
-  a.lse_px = lse_px;
-  a.cz = (float)((double)kl_grad / ((double)d.B * d.S * d.Hp));
   a.seg_offset = seg_offset;
   a.entries = entries;
   a.items = items;
@@ -343,22 +841,55 @@ void launch_fused_bwd(const Dims& d, bool dense, const void* q, const void* k, c
   a.dq = dq_acc;
   a.dk = dk_acc;
   a.dv = dv_acc;
-  a.dqp = dqp_acc;
-  a.dkp = dkp_acc;
-#define MSA_BWD_CASE(GG)                           \
-  case GG:                                         \
-    if (dense)                                     \
-      fused_bwd_g<GG, true>(a, st);                \
-    else                                           \
-      fused_bwd_g<GG, false>(a, st);               \
+  a.pbar = pbar;
+  a.status = status;
+#define MSA_BWD_CASE(GG)                    \
+  case GG:                                  \
+    if (dense)                              \
+      attn_bwd_g<GG, true>(mk, mv, a, st);  \
+    else                                    \
+      attn_bwd_g<GG, false>(mk, mv, a, st); \
     break;
   switch (d.G) {
-    MSA_BWD_CASE(2)
     MSA_BWD_CASE(4)
     MSA_BWD_CASE(8)
     MSA_BWD_CASE(16)
+    default:
+      return false;
   }
 #undef MSA_BWD_CASE
+  return true;
+}
+
+bool launch_proxy_bwd(const Dims& d, bool dense, const void* qp, const void* kp,
+                      const float* lse_px, const float* pbar, float kl_grad, const int* seg_offset,
+                      const int* entries, const Item* items, const int* n_items,
+                      long long max_items, float* dqp_acc, float* dkp_acc, unsigned* status,
+                      cudaStream_t st) {
+  CUtensorMap mkp;
+  const uint64_t kpd[2] = {128, (uint64_t)d.B * d.S};
+  const uint64_t kps[1] = {128 * 2};
+  const uint32_t kpb[2] = {64, 128};
+  if (!make_tmap_bf16(&mkp, kp, 2, kpd, kps, kpb)) return false;
+  ProxyArgs a;
+  a.d = d;
+  a.qp = (const bf16*)qp;
+  a.lse_px = lse_px;
+  a.pbar = pbar;
+  a.cz = (float)((double)kl_grad / ((double)d.B * d.S * d.Hp));
+  a.seg_offset = seg_offset;
+  a.entries = entries;
+  a.items = items;
+  a.n_items = n_items;
+  a.max_items = max_items;
+  a.dqp = dqp_acc;
+  a.dkp = dkp_acc;
+  a.status = status;
+  if (dense)
+    proxy_bwd_g<true>(mkp, a, st);
+  else
+    proxy_bwd_g<false>(mkp, a, st);
+  return true;
 }
 
 }  // namespace msa

@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(256, 2)
   for (long long it = blockIdx.x; it < total; it += gridDim.x) {
     const Item item = items[it];
     const int n = item.seg % d.nblk;
-    const int bg = item.seg / d.nblk;
+    const int bg = (int)((item.seg % d.nseg()) / d.nblk);
     const int b = bg / d.Hp, g = bg % d.Hp;
     if (tid < TT) {
       int t = -1, slot = 0;
@@ -315,7 +315,7 @@ __global__ void __launch_bounds__(256, 2)
   for (long long it = blockIdx.x; it < total; it += gridDim.x) {
     const Item item = items[it];
     const int n = item.seg % d.nblk;
-    const int bg = item.seg / d.nblk;
+    const int bg = (int)((item.seg % d.nseg()) / d.nblk);
     const int b = bg / d.Hp, g = bg % d.Hp;
     if (tid < 128) {
       int t = -1, slot = 0;

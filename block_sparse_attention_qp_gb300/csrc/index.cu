@@ -3,8 +3,10 @@
 // The blog ("Backward") inverts the cached map  (batch, proxy head, query, slot) -> key block
 // into  (batch, proxy head, key block) -> queries that use the block, and schedules work per key
 // block so that the block's keys and values are loaded once for many queries.  Here the inverse
-// map is a CSR structure: one list per (b, g, n) of packed entries (t << 8 | slot); lists are
-// cut into fixed-size items that the attention kernels consume.
+// map is a CSR structure: one list per (chunk c, b, g, n) of packed entries (t << 8 | slot), where
+// chunk c holds the tokens [c * chunk, (c+1) * chunk).  Lists are numbered chunk-major, so work
+// items running at the same time touch the gradient rows of one chunk only (which then stay in
+// L2).  Lists are cut into fixed-size items that the attention kernels consume.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -40,7 +42,7 @@ __global__ void count_kernel(Dims d, const int32_t* __restrict__ idx, int* __res
     bool padded = false, bad = false;
     for (int s = 0; s < d.top_k; ++s) {
       const int n = checked_block(row, s, t, prev, padded, bad);
-      if (n >= 0) atomicAdd(seg_count + bg * d.nblk + n, 1);
+      if (n >= 0) atomicAdd(seg_count + (long long)(t / d.chunk) * d.nseg() + bg * d.nblk + n, 1);
     }
     if (bad) atomicOr(status, kStatusBadIndex);
   }
@@ -59,16 +61,29 @@ __global__ void fill_kernel(Dims d, const int32_t* __restrict__ idx, const int* 
     for (int s = 0; s < d.top_k; ++s) {
       const int n = checked_block(row, s, t, prev, padded, bad);
       if (n < 0) continue;
-      const long long seg = bg * d.nblk + n;
+      const long long seg = (long long)(t / d.chunk) * d.nseg() + bg * d.nblk + n;
       const int pos = atomicAdd(seg_cursor + seg, 1);
       entries[seg_offset[seg] + pos] = (t << 8) | s;
     }
   }
 }
 
+// Dense lists: chunk c of block n holds the tokens t >= 128 n with t in the chunk, i.e. the range
+// [max(128 n, c * chunk), min(S, (c+1) * chunk)).
+__device__ __forceinline__ long long dense_first(const Dims& d, long long seg) {
+  const long long n = seg % d.nblk, c = seg / d.nseg();
+  const long long lo = (long long)c * d.chunk;
+  return n * kBlock > lo ? n * kBlock : lo;
+}
 __device__ __forceinline__ long long list_len(const Dims& d, bool dense, const int* seg_count,
                                               long long seg) {
-  if (dense) return d.S - (long long)(seg % d.nblk) * kBlock;  // tokens t >= 128 n
+  if (dense) {
+    const long long c = seg / d.nseg();
+    long long hi = (c + 1) * (long long)d.chunk;
+    if (hi > d.S) hi = d.S;
+    const long long lo = dense_first(d, seg);
+    return hi > lo ? hi - lo : 0;
+  }
   return seg_count[seg];
 }
 
@@ -84,7 +99,7 @@ __global__ void __launch_bounds__(1024) scan_kernel(Dims d, int dense, const int
                                                     int nspecs, int* __restrict__ io0,
                                                     int* __restrict__ io1, int* __restrict__ totals) {
   __shared__ long long sh[3][1024];
-  const long long nseg = d.nseg();
+  const long long nseg = d.nlist();
   const int tid = threadIdx.x;
   const long long per = (nseg + 1023) / 1024;
   const long long lo = tid * per, hi = lo + per < nseg ? lo + per : nseg;
@@ -203,8 +218,8 @@ void launch_fill(const Dims& d, const int32_t* idx, const int* seg_offset, int* 
 void launch_items(const Dims& d, bool dense, const int* seg_count, const ItemSpec& spec,
                   const int* item_offset, Item* items, long long max_items, unsigned* status,
                   cudaStream_t st) {
-  items_kernel<<<(unsigned)d.nseg(), 128, 0, st>>>(d, dense ? 1 : 0, seg_count, spec, item_offset,
-                                                   items, max_items, status);
+  items_kernel<<<(unsigned)d.nlist(), 128, 0, st>>>(d, dense ? 1 : 0, seg_count, spec,
+                                                    item_offset, items, max_items, status);
 }
 
 void launch_convert(const float* src, void* dst, long long n, cudaStream_t st) {

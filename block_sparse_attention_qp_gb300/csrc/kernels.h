@@ -9,11 +9,14 @@ namespace msa {
 struct Dims {
   int B, S, Hq, Hkv, Hp, G, top_k, nblk;
   float scale;
-  __host__ __device__ long long nseg() const { return (long long)B * Hp * nblk; }  // (b, group, key block) lists
+  int chunk;   // token-list chunk: a list holds the tokens of one (b, g, n) in one chunk of the
+  int nchunk;  // sequence [c * chunk, (c+1) * chunk); lists are ordered chunk-major
+  __host__ __device__ long long nseg() const { return (long long)B * Hp * nblk; }  // (b, g, n)
+  __host__ __device__ long long nlist() const { return nseg() * nchunk; }           // (c, b, g, n)
 };
 
-// A unit of attention work: `count` tokens of list `seg` starting at list position `first`,
-// on key-half `half` (0/1; forward-shaped kernels use 0).
+// A unit of attention work: `count` tokens of list `seg` (= c * nseg + (b * Hp + g) * nblk + n)
+// starting at list position `first`, on key-half `half` (0/1; 0 for most kernels).
 struct Item {
   int seg, first, count, half;
 };
@@ -25,11 +28,11 @@ struct ItemSpec {
 };
 
 // ---------------------------------------------------------------- index kernels (index.cu)
-// Count block references per (b, g, n) list (validating every index against its row).
+// Count block references per (c, b, g, n) list (validating every index against its row).
 void launch_count(const Dims& d, const int32_t* idx, int* seg_count, unsigned* status,
                   cudaStream_t st);
 // Exclusive scans: list offsets (sparse only) and item offsets for up to two item specs.
-// dense: list lengths are S - 128 n (every later token) instead of seg_count.
+// dense: list lengths are the tokens t >= 128 n of the chunk instead of seg_count.
 void launch_scan(const Dims& d, bool dense, const int* seg_count, int* seg_offset,
                  const ItemSpec* specs, int nspecs, int* item_offset0, int* item_offset1,
                  int* totals, cudaStream_t st);
@@ -65,12 +68,22 @@ void launch_proxy_lse_combine(const Dims& d, const int32_t* idx, const float* lp
                               float* lse_px, cudaStream_t st);
 void launch_proxy_lse_dense(const Dims& d, const void* qp, const void* kp, float* lse_px,
                             cudaStream_t st);
-void launch_fused_bwd(const Dims& d, bool dense, const void* q, const void* k, const void* v,
-                      const void* qp, const void* kp, const void* dout, const float* lse,
-                      const float* drow, const float* lse_px, float kl_grad,
-                      const int* seg_offset, const int* entries, const Item* items,
-                      const int* n_items, long long max_items, float* dq_acc, float* dk_acc,
-                      float* dv_acc, float* dqp_acc, float* dkp_acc, cudaStream_t st);
+// Main-attention backward (dQ, dK, dV into fp32 accumulators) and the teacher pbar
+// ([list entry][128 keys] fp32).  Returns false for an unsupported group size or if the TMA
+// tensor maps cannot be created.
+bool launch_attn_bwd(const Dims& d, bool dense, const void* q, const void* k, const void* v,
+                     const void* dout, const float* lse, const float* drow, const int* seg_offset,
+                     const int* entries, const Item* items, const int* n_items, long long max_items,
+                     float* dq_acc, float* dk_acc, float* dv_acc, float* pbar, unsigned* status,
+                     cudaStream_t st);
+// Proxy gradients (dQp, dKp into fp32 accumulators) of the KL term from pbar.
+bool launch_proxy_bwd(const Dims& d, bool dense, const void* qp, const void* kp,
+                      const float* lse_px, const float* pbar, float kl_grad, const int* seg_offset,
+                      const int* entries, const Item* items, const int* n_items,
+                      long long max_items, float* dqp_acc, float* dkp_acc, unsigned* status,
+                      cudaStream_t st);
+int bwd_item_tokens();   // tokens per fused-backward work item
+int bwd_group_tokens();  // tokens per proxy-gradient flush group
 void launch_convert(const float* src, void* dst, long long n, cudaStream_t st);
 
 int num_sms();
