@@ -191,10 +191,10 @@ def backward(q, k, v, qp, kp, dout, idx, top_k: int, scale: float, kl_grad: floa
     if idx is not None:
         idx = np.ascontiguousarray(idx, dtype=np.int32)
         top_k = idx.shape[-1]
-    dq = np.zeros_like(q)
-    dk = np.zeros_like(k)
-    dv = np.zeros_like(v)
-    dqp = np.zeros_like(qp)
+    dq = np.zeros(q.shape, np.float64)  # np.zeros maps lazily-zeroed pages: sampled runs on long
+    dk = np.zeros(k.shape, np.float64)  # sequences only touch the rows they write
+    dv = np.zeros(v.shape, np.float64)
+    dqp = np.zeros(qp.shape, np.float64)
     dkp = np.zeros((B, S, D), np.float64)
     kl = np.zeros((1,), np.float64)
     tm = None if tok_mask is None else np.ascontiguousarray(tok_mask, dtype=np.uint8)
