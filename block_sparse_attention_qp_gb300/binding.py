@@ -27,7 +27,7 @@ OP_FORWARD, OP_BACKWARD, OP_WARMUP_FORWARD, OP_WARMUP_BACKWARD = 0, 1, 2, 3
 STATUS_BITS = {1: "bad block index", 2: "work list overflow", 4: "device wait timeout"}
 _SYMBOLS = ("msa_workspace_size", "msa_forward", "msa_backward", "msa_warmup_forward",
             "msa_warmup_backward", "msa_device_status", "msa_status_string", "msa_last_error",
-            "msa_profile_begin", "msa_profile_end", "msa_launch_count")
+            "msa_profile_begin", "msa_profile_end", "msa_launch_count", "msa_forward_noalloc")
 
 
 class MSAError(RuntimeError):
@@ -69,6 +69,8 @@ def load_library(path: str = LIB_PATH):
                      "msa_device_status", "msa_profile_begin", "msa_profile_end"):
             getattr(lib, name).restype = I
         lib.msa_profile_end.argtypes = [ctypes.c_char_p, Z]
+        lib.msa_forward_noalloc.argtypes = [SP, P, P, P, P, P, P, I, P, P, P]
+        lib.msa_forward_noalloc.restype = I
         lib.msa_launch_count.restype = ctypes.c_longlong
         _lib = lib
         return lib
@@ -171,6 +173,28 @@ def msa_forward(q, k, v, qp, kp, top_k: int, scale: float, block_idx=None, ws=No
     _check(load_library().msa_forward(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(qp),
                                       _ptr(kp), _ptr(block_idx), int(given), _ptr(o), _ptr(lse),
                                       _ptr(ws), ws.numel(), _stream(q.device)), "msa_forward")
+    return o, lse, block_idx
+
+
+def msa_forward_noalloc(q, k, v, qp, kp, top_k: int, scale: float, block_idx=None):
+    """msa_forward without a workspace: the library's fixed device scratch array is used instead
+    (see include/msa.h).  Returns (o, lse, block_idx)."""
+    B, S, Hq, D = q.shape
+    Hp = qp.shape[2]
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (qp, "qp"), (kp, "kp")):
+        _req(t, n)
+    shape = make_shape(q, k, qp, top_k, scale)
+    given = block_idx is not None
+    if given:
+        _req(block_idx, "block_idx", torch.int32, (B, Hp, S, top_k))
+    else:
+        block_idx = torch.empty((B, Hp, S, top_k), dtype=torch.int32, device=q.device)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq, S), dtype=torch.float32, device=q.device)
+    _check(load_library().msa_forward_noalloc(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v),
+                                              _ptr(qp), _ptr(kp), _ptr(block_idx), int(given),
+                                              _ptr(o), _ptr(lse), _stream(q.device)),
+           "msa_forward_noalloc")
     return o, lse, block_idx
 
 

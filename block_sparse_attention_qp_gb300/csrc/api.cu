@@ -318,6 +318,10 @@ void emit_grads(const Dims& d, const Plan& p, void* ws, void* dq, void* dk, void
 }
 
 }  // namespace
+
+// Sets the text msa_last_error() returns on this thread (used by entry points in other files).
+void set_api_error(const char* what) { set_err(what); }
+
 }  // namespace msa
 
 using namespace msa;

@@ -87,5 +87,6 @@ int bwd_group_tokens();  // tokens per proxy-gradient flush group
 void launch_convert(const float* src, void* dst, long long n, cudaStream_t st);
 
 int num_sms();
+void set_api_error(const char* what);
 
 }  // namespace msa

@@ -148,6 +148,24 @@ MSA_API int msa_profile_begin(void);
 MSA_API int msa_profile_end(char* buf, size_t len);
 MSA_API long long msa_launch_count(void);
 
+/*
+ * Allocation-free variant of msa_forward (the method's pages have no counterpart; this is an
+ * integration aid).  Some callers cannot allocate device memory where they call the forward --
+ * for example a C layer embedded in a framework whose allocator it cannot reach, or code running
+ * while a sequence of launches is being recorded for replay, where allocating is not allowed.
+ * This entry point needs no workspace: it uses a fixed scratch array of 64 MiB (67108864 bytes)
+ * that lives in device memory for as long as the library is loaded, one per GPU that loads it.  Arguments and results are those of msa_forward; inputs and outputs are still
+ * the caller's.  Shapes whose forward workspace exceeds the array are rejected with
+ * MSA_ERR_WORKSPACE before any launch.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress), so make that first call before any stream capture.  Every call
+ * on a device shares the one array and it keeps the last call's contents: the call re-initialises
+ * what must start at zero itself, but calls that overlap on the GPU (different streams without
+ * ordering) race on it and must be serialised by the caller.
+ */
+MSA_API int msa_forward_noalloc(const msa_shape_t* shape, const void* q, const void* k,
+                                const void* v, const void* qp, const void* kp, int32_t* block_idx,
+                                int indices_given, void* o, float* lse, void* stream);
+
 /* Static text for a status code. */
 MSA_API const char* msa_status_string(int status);
 
