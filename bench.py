@@ -193,8 +193,11 @@ def run_reference(args, w, wi):
 KERNEL_WORK = {
     # kernel name -> (bound, function(workload) -> algorithmic FLOPs per launch)
     "proxy_topk": ("tensor", lambda w: 2 * w.D * flops.n_px(w.S) * w.Hp * w.B),
-    "sparse_fwd": ("tensor", lambda w: 4 * w.D * flops.n_sel(w.S, w.top_k) * w.Hq * w.B),
-    "fused_bwd": ("tensor", lambda w: (10 * w.Hq + 6 * w.Hp) * w.D * flops.n_sel(w.S, w.top_k) * w.B),
+    "attn_fwd": ("tensor", lambda w: 4 * w.D * flops.n_sel(w.S, w.top_k) * w.Hq * w.B),
+    # main-attention backward: S, dP (2d each), dV, dK, dQ (2d each) per selected pair and head
+    "attn_bwd": ("tensor", lambda w: 10 * w.D * flops.n_sel(w.S, w.top_k) * w.Hq * w.B),
+    # proxy backward: z recompute, dKp, dQp (2d each) per selected pair and proxy head
+    "proxy_bwd": ("tensor", lambda w: 6 * w.D * flops.n_sel(w.S, w.top_k) * w.Hp * w.B),
     "proxy_lse": ("tensor", lambda w: 2 * w.D * flops.n_sel(w.S, w.top_k) * w.Hp * w.B),
 }
 
@@ -368,7 +371,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="msa_s64k_planted")
-    ap.add_argument("--ref-tokens", type=int, default=24)
+    ap.add_argument("--ref-tokens", type=int, default=384)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()

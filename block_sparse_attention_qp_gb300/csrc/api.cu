@@ -108,6 +108,15 @@ int bwd_chunk(const Dims& d) {
   return c;
 }
 
+// Sequence chunk of the forward's token lists: one chunk's query rows of one group
+// (chunk x G heads x 128 x bf16) are kept to <= 16 MB, so the up to top_k reads of every query row
+// (one per selected block) hit L2 while the items of that chunk and group run.
+int fwd_chunk(const Dims& d) {
+  int c = kBlock;
+  while ((long long)c * 2 * d.G * kD * 2 <= (16ll << 20) && c * 2 <= d.S) c *= 2;
+  return c;
+}
+
 Dims with_chunk(Dims d, int chunk) {
   d.chunk = chunk;
   d.nchunk = (d.S + chunk - 1) / chunk;
@@ -133,7 +142,7 @@ Plan make_plan(const Dims& d, int op) {
     p.entries = c.take(sparse_ent * sizeof(int));
   }
   if (op == MSA_OP_FORWARD) {
-    p.spec0 = ItemSpec{TT, 1, 1};
+    p.spec0 = ItemSpec{TT, fwd_item_tiles(), 1};
     p.max0 = max_items(sparse_ent, d, p.spec0);
     p.io0 = c.take(nseg * sizeof(int));
     p.items0 = c.take(p.max0 * sizeof(Item));
@@ -234,7 +243,7 @@ int check_shape(const msa_shape_t* s, int op, Dims* out) {
   d.top_k = sparse ? s->top_k : 1;
   d.nblk = s->S / kBlock;
   d.scale = s->scale;
-  d = with_chunk(d, bwd ? bwd_chunk(d) : d.S);
+  d = with_chunk(d, bwd ? bwd_chunk(d) : sparse ? fwd_chunk(d) : d.S);
   if (op == MSA_OP_WARMUP_BACKWARD && dense_entries(d) >= (1ll << 31)) {
     set_err("B*Hp*S*S/256 must stay below 2^31 in the warmup backward");
     return MSA_ERR_UNSUPPORTED;
@@ -359,11 +368,17 @@ int msa_forward(const msa_shape_t* shape, const void* q, const void* k, const vo
     }
   }
   build_lists(d, p, block_idx, workspace, 1, st);
-  timed("sparse_fwd", st, [&] {
-    launch_sparse_fwd(d, q, k, v, at<int>(workspace, p.seg_offset), at<int>(workspace, p.entries),
-                      at<Item>(workspace, p.items0), at<int>(workspace, p.totals) + 1, p.max0,
-                      at<void>(workspace, p.opart), at<float>(workspace, p.lpart), st);
+  bool fok = true;
+  timed("attn_fwd", st, [&] {
+    fok = launch_attn_fwd(d, q, k, v, at<int>(workspace, p.seg_offset),
+                          at<int>(workspace, p.entries), at<Item>(workspace, p.items0),
+                          at<int>(workspace, p.totals) + 1, p.max0, at<void>(workspace, p.opart),
+                          at<float>(workspace, p.lpart), at<unsigned>(workspace, p.status), st);
   });
+  if (!fok) {
+    set_err("msa_forward: could not create TMA tensor maps (cuTensorMapEncodeTiled)");
+    return MSA_ERR_CUDA;
+  }
   timed("fwd_combine", st, [&] {
     launch_combine(d, block_idx, at<void>(workspace, p.opart), at<float>(workspace, p.lpart), o,
                    lse, st);

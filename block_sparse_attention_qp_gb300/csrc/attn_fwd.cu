@@ -1,0 +1,443 @@
+// Sparse main-attention forward on the tcgen05 tensor cores (blog, "Main attention"; forum
+// summary, "GPU kernel co-design": KV-outer iteration with gathered queries and a two-phase
+// forward).
+//
+// Phase 1 (attn_fwd_kernel): a work item is one 128-key block n of group g and up to 8 tiles of
+// the tokens whose selection holds n (from the inverted block map).  A tile is 128 rows: 128/G
+// tokens x the G query heads of the group.  Per tile
+//   S = Q K^T                       (tensor core, 128 x 128 fp32 in tensor memory)
+//   P = exp(scale S - m), l = sum P  (softmax warps, thread = row; causal cut in the local block)
+//   O = P V                         (tensor core, P read from tensor memory)
+//   partial (t, h, slot) = O / l in bf16, and its log-sum-exp m + log l   (epilogue warps)
+// Phase 2 (combine_kernel in fwd.cu) merges the <= top_k partials of every (t, h).
+//
+// Roles (384 threads): warp 0 TMA loads of K/V (two stages) and tensor-memory ownership, warp 1
+// the MMA issuer, warps 2-3 gather the tile's Q rows (cp.async, two buffers), warps 4-7 softmax,
+// warps 8-11 epilogue.  Tensor memory (512 columns): S0, S1 (S, then P in place), O0, O1.
+// The MMA issuer runs S of tile i before O of tile i-1, so the tensor pipe works on one tile while
+// the softmax warps work on the next.  Every wait is bounded (see sm100::mbar_wait).
+#include <math.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "sm100.cuh"
+#include "tmap.h"
+
+namespace msa {
+namespace {
+
+constexpr int kFwdRows = 128;                  // rows (tokens x heads) per tile
+constexpr int kFwdTile = kFwdRows * 128 * 2;   // one 128-row x 128 bf16 tile (two SW128 panels)
+constexpr int kFwdItemTiles = 8;               // tiles per work item
+constexpr int kStageWarp = 32 * 128;           // epilogue staging per warp: 32 rows x 128 bytes
+
+struct FwdArgs {
+  Dims d;
+  const bf16* q;
+  const int* seg_offset;
+  const int* entries;
+  const Item* items;
+  const int* n_items;
+  long long max_items;
+  bf16* opart;
+  float* lpart;
+  unsigned* status;
+};
+
+struct FwdShared {
+  int tok[2][kFwdRows];         // token of each tile token (-1: none), per Q buffer
+  int slot[2][kFwdRows];        // its selection slot
+  long long dst[2][kFwdRows];   // partial row (t, h, slot) of each tile row (-1: none), per O buffer
+  float inv_l[2][kFwdRows];     // 1 / l of each row
+  float lse[2][kFwdRows];       // natural log-sum-exp of each row's partial
+  uint64_t kv_full[2], kv_empty[2], q_full[2], q_empty[2], meta_free[2], s_full[2], p_full[2],
+      o_full[2], o_free[2], mma_done;
+  uint32_t tmem;
+};
+
+__device__ __forceinline__ float ex2f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ uint32_t par(long long k) { return (uint32_t)(k & 1); }
+__device__ __forceinline__ void st_global_v4(void* p, uint4 v) {
+  asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+}  // namespace
+
+template <int G>
+__global__ void __launch_bounds__(384, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                    FwdArgs A) {
+  using namespace sm100;
+  constexpr int TT = kFwdRows / G;  // tokens per tile
+  const Dims& d = A.d;
+
+  extern __shared__ uint8_t smem_raw[];
+  FwdShared* sh = reinterpret_cast<FwdShared*>(smem_raw);
+  uint8_t* base = align1024(smem_raw + sizeof(FwdShared));
+  uint8_t* sK = base;                 // [2 stages][128 keys][128 d]   (TMA)
+  uint8_t* sV = sK + 2 * kFwdTile;    // [2 stages][128 keys][128 d]   (TMA)
+  uint8_t* sQ = sV + 2 * kFwdTile;    // [2][128 rows][128 d]          (gathered)
+  uint8_t* sSt = sQ + 2 * kFwdTile;   // epilogue staging, [4 warps][32 rows][128 bytes]
+  const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ), aSt = smem_u32(sSt);
+
+  const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
+  const float sl2 = d.scale * kLog2e;
+  long long total = *A.n_items;
+  if (total > A.max_items) total = A.max_items;
+
+  if (tid == 0) {
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&sh->kv_full[x], 1);
+      mbar_init(&sh->kv_empty[x], 1);
+      mbar_init(&sh->q_full[x], 64);
+      mbar_init(&sh->q_empty[x], 1);
+      mbar_init(&sh->meta_free[x], 4);
+      mbar_init(&sh->s_full[x], 1);
+      mbar_init(&sh->p_full[x], 4);
+      mbar_init(&sh->o_full[x], 1);
+      mbar_init(&sh->o_free[x], 4);
+    }
+    mbar_init(&sh->mma_done, 1);
+    mbar_fence_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&sh->tmem, 512);
+    tmem_relinquish();
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = sh->tmem;
+  const uint32_t S0 = tmem, O0 = tmem + 256;  // S_b = S0 + 128 b, O_b = O0 + 128 b
+  bool ok = true;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA: K, V per item
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      long long ni = 0;
+      for (long long it = blockIdx.x; it < total; it += gridDim.x, ++ni) {
+        const Item item = A.items[it];
+        const int n = item.seg % d.nblk;
+        const int bg = (int)((item.seg % d.nseg()) / d.nblk);
+        const int b = bg / d.Hp, g = bg % d.Hp;
+        const int s = (int)(ni & 1);
+        if (ni >= 2 && !mbar_wait(&sh->kv_empty[s], par((ni - 2) >> 1), A.status)) break;
+        const int row0 = b * d.S + n * kBlock;
+        uint8_t* k_s = sK + s * kFwdTile;
+        uint8_t* v_s = sV + s * kFwdTile;
+        mbar_expect_tx(&sh->kv_full[s], 2 * kFwdTile);
+        tma_load_3d(k_s, &tm_k, 0, g, row0, &sh->kv_full[s]);
+        tma_load_3d(k_s + kFwdTile / 2, &tm_k, 64, g, row0, &sh->kv_full[s]);
+        tma_load_3d(v_s, &tm_v, 0, g, row0, &sh->kv_full[s]);
+        tma_load_3d(v_s + kFwdTile / 2, &tm_v, 64, g, row0, &sh->kv_full[s]);
+      }
+      // no copy may still be landing in shared memory when the block exits
+      for (long long x = (ni >= 2 ? ni - 2 : 0); x < ni; ++x)
+        mbar_wait(&sh->kv_full[x & 1], par(x >> 1), A.status);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);  // S = Q K^T
+      constexpr uint32_t id_o = idesc_bf16(128, 128, false, true);   // O = P V
+      long long ni = 0, i = 0;
+      bool pending = false;
+      long long pi = 0;
+      int ps = 0;
+      bool plast = false;
+      auto mma_o = [&](long long ti, int s, bool last) -> bool {
+        const int b = (int)(ti & 1);
+        if (!mbar_wait(&sh->p_full[b], par(ti >> 1), A.status)) return false;
+        if (ti >= 2 && !mbar_wait(&sh->o_free[b], par((ti - 2) >> 1), A.status)) return false;
+        fence_after_sync();
+        const uint32_t aVs = aV + s * kFwdTile;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          mma_ts(O0 + 128 * b, S0 + 128 * b + ks * 8, desc_mnmajor(aVs, 128, ks), id_o, ks > 0);
+        mma_commit(&sh->o_full[b]);
+        if (last) mma_commit(&sh->kv_empty[s]);
+        return true;
+      };
+      for (long long it = blockIdx.x; ok && it < total; it += gridDim.x, ++ni) {
+        const Item item = A.items[it];
+        const int s = (int)(ni & 1);
+        if (!mbar_wait(&sh->kv_full[s], par(ni >> 1), A.status)) { ok = false; break; }
+        const uint32_t aKs = aK + s * kFwdTile;
+        const int ntiles = (item.count + TT - 1) / TT;
+        if (ntiles == 0) mma_commit(&sh->kv_empty[s]);  // (items are never empty)
+        for (int tl = 0; tl < ntiles; ++tl, ++i) {
+          const int b = (int)(i & 1);
+          if (!mbar_wait(&sh->q_full[b], par(i >> 1), A.status)) { ok = false; break; }
+          // S_b still holds P of tile i-2 until that tile's O product has completed
+          if (i >= 2 && !mbar_wait(&sh->o_full[b], par((i - 2) >> 1), A.status)) { ok = false; break; }
+          fence_after_sync();
+          const uint32_t aQb = aQ + b * kFwdTile;
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            mma_ss(S0 + 128 * b, desc_kmajor(aQb, 128, ks), desc_kmajor(aKs, 128, ks), id_s, ks > 0);
+          mma_commit(&sh->s_full[b]);
+          mma_commit(&sh->q_empty[b]);
+          if (pending && !mma_o(pi, ps, plast)) { ok = false; break; }
+          pending = true;
+          pi = i;
+          ps = s;
+          plast = tl == ntiles - 1;
+        }
+      }
+      if (ok && pending) mma_o(pi, ps, plast);
+      mma_commit(&sh->mma_done);
+      mbar_wait(&sh->mma_done, 0, A.status);
+    }
+  } else if (warp < 4) {
+    // ---------------------------------------------------------------- gather: Q rows
+    const int w2 = warp - 2;             // rows [64 w2, 64 w2 + 64)
+    constexpr int XT = 64 / G;           // tokens per gather warp
+    const int x0 = w2 * XT;
+    long long i = 0;
+    for (long long it = blockIdx.x; ok && it < total; it += gridDim.x) {
+      const Item item = A.items[it];
+      const int bg = (int)((item.seg % d.nseg()) / d.nblk);
+      const int b = bg / d.Hp, g = bg % d.Hp;
+      const long long eb = (long long)A.seg_offset[item.seg] + item.first;
+      const int ntiles = (item.count + TT - 1) / TT;
+      for (int tl = 0; tl < ntiles; ++tl, ++i) {
+        const int bb = (int)(i & 1);
+        if (i >= 2 && (!mbar_wait(&sh->q_empty[bb], par((i - 2) >> 1), A.status) ||
+                       !mbar_wait(&sh->meta_free[bb], par((i - 2) >> 1), A.status))) {
+          ok = false;
+          break;
+        }
+        for (int xx = lane; xx < XT; xx += 32) {
+          const int pos = tl * TT + x0 + xx;
+          const int e = pos < item.count ? A.entries[eb + pos] : -1;
+          sh->tok[bb][x0 + xx] = e < 0 ? -1 : (e >> 8);
+          sh->slot[bb][x0 + xx] = e < 0 ? 0 : (e & 255);
+        }
+        __syncwarp();
+        uint8_t* dQb = sQ + bb * kFwdTile;
+#pragma unroll 8
+        for (int k = 0; k < 32; ++k) {
+          const int c = lane + 32 * k;
+          const int r = 64 * w2 + (c >> 4), ch = c & 15;
+          const int t = sh->tok[bb][r / G];
+          const uint32_t off = (ch >> 3) * (kFwdRows * 128) + sm100::sw128_chunk(r, ch & 7);
+          const size_t grow = (((size_t)b * d.S + (t < 0 ? 0 : t)) * d.Hq + g * G + r % G) * kD + ch * 8;
+          cp_async16(dQb + off, A.q + grow, t >= 0);
+        }
+        cp_async_wait_all();
+        fence_async_smem();
+        mbar_arrive(&sh->q_full[bb]);
+      }
+    }
+  } else if (warp < 8) {
+    // ---------------------------------------------------------------- softmax
+    const int w4 = warp - 4;
+    const int r = w4 * 32 + lane;  // tile row = tensor-memory lane
+    const uint32_t lb = static_cast<uint32_t>(w4 * 32) << 16;
+    long long i = 0;
+    for (long long it = blockIdx.x; ok && it < total; it += gridDim.x) {
+      const Item item = A.items[it];
+      const int n = item.seg % d.nblk;
+      const int bg = (int)((item.seg % d.nseg()) / d.nblk);
+      const int b = bg / d.Hp, g = bg % d.Hp;
+      const int ntiles = (item.count + TT - 1) / TT;
+      for (int tl = 0; tl < ntiles; ++tl, ++i) {
+        const int bb = (int)(i & 1);
+        __syncwarp();
+        if (!mbar_wait(&sh->s_full[bb], par(i >> 1), A.status) ||
+            !mbar_wait(&sh->q_full[bb], par(i >> 1), A.status)) {
+          ok = false;
+          break;
+        }
+        fence_after_sync();
+        const int t = sh->tok[bb][r / G];
+        const int slot = sh->slot[bb][r / G];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh->meta_free[bb]);
+        // visible key columns of this row: 0 .. lim (the causal cut only bites in the local block)
+        const int lim = t < 0 ? -1 : min(kBlock - 1, t - n * kBlock);
+        const uint32_t Sb = S0 + 128 * bb + lb;
+        // pass 1: row maximum over the visible keys
+        float mx = -INFINITY;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t v0[32], v1[32];
+          tmem_ld32(Sb + h * 64, v0);
+          tmem_ld32(Sb + h * 64 + 32, v1);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            if (h * 64 + c <= lim) mx = fmaxf(mx, __uint_as_float(v0[c]));
+            if (h * 64 + 32 + c <= lim) mx = fmaxf(mx, __uint_as_float(v1[c]));
+          }
+        }
+        const float m2 = lim < 0 ? 0.f : mx * sl2;
+        // pass 2: P = 2^(S sl2 - m2) written over S as packed bf16 (column j holds keys 2j, 2j+1)
+        float l = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t v0[32], v1[32];
+          tmem_ld32(Sb + h * 64, v0);
+          tmem_ld32(Sb + h * 64 + 32, v1);
+          tmem_wait_ld();
+          uint32_t pw0[16], pw1[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const int k0 = h * 64 + 2 * c, k1 = h * 64 + 32 + 2 * c;
+            const float a0 = k0 <= lim ? ex2f(fmaf(__uint_as_float(v0[2 * c]), sl2, -m2)) : 0.f;
+            const float a1 = k0 + 1 <= lim ? ex2f(fmaf(__uint_as_float(v0[2 * c + 1]), sl2, -m2)) : 0.f;
+            const float c0 = k1 <= lim ? ex2f(fmaf(__uint_as_float(v1[2 * c]), sl2, -m2)) : 0.f;
+            const float c1 = k1 + 1 <= lim ? ex2f(fmaf(__uint_as_float(v1[2 * c + 1]), sl2, -m2)) : 0.f;
+            l += (a0 + a1) + (c0 + c1);
+            pw0[c] = pack_bf16(a0, a1);
+            pw1[c] = pack_bf16(c0, c1);
+          }
+          tmem_st16(Sb + h * 32, pw0);
+          tmem_st16(Sb + h * 32 + 16, pw1);
+        }
+        // row results for the epilogue (its buffer is free once the epilogue of tile i-2 read it)
+        if (i >= 2 && !mbar_wait(&sh->o_free[bb], par((i - 2) >> 1), A.status)) {
+          ok = false;
+          break;
+        }
+        const bool valid = t >= 0;
+        sh->dst[bb][r] = valid ? (((long long)b * d.S + t) * d.Hq + g * G + r % G) * d.top_k + slot : -1;
+        sh->inv_l[bb][r] = valid ? 1.f / l : 0.f;
+        sh->lse[bb][r] = valid ? (m2 + log2f(l)) * kLn2 : 0.f;
+        tmem_wait_st();
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh->p_full[bb]);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    const int w8 = warp - 8;
+    const int r = w8 * 32 + lane;
+    const uint32_t lb = static_cast<uint32_t>(w8 * 32) << 16;
+    const uint32_t stw = aSt + w8 * kStageWarp;  // this warp's staging: [32 rows][128 bytes]
+    long long i = 0;
+    for (long long it = blockIdx.x; ok && it < total; it += gridDim.x) {
+      const Item item = A.items[it];
+      const int ntiles = (item.count + TT - 1) / TT;
+      for (int tl = 0; tl < ntiles; ++tl, ++i) {
+        const int bb = (int)(i & 1);
+        __syncwarp();
+        if (!mbar_wait(&sh->o_full[bb], par(i >> 1), A.status) ||
+            !mbar_wait(&sh->p_full[bb], par(i >> 1), A.status)) {
+          ok = false;
+          break;
+        }
+        fence_after_sync();
+        const long long dst = sh->dst[bb][r];
+        const float sc = sh->inv_l[bb][r];
+        const float lse = sh->lse[bb][r];
+        const uint32_t Ob = O0 + 128 * bb + lb;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t v0[32], v1[32];
+          tmem_ld32(Ob + h * 64, v0);
+          tmem_ld32(Ob + h * 64 + 32, v1);
+          tmem_wait_ld();
+          if (h == 1) {
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh->o_free[bb]);
+          }
+          // this row's 64 columns -> 128 bytes of bf16 in the warp's staging (16-byte chunks
+          // XOR-swizzled by row), then 4 rows x 128 contiguous bytes per store instruction
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint32_t* src = u < 2 ? v0 : v1;
+            const int o = (u & 1) * 16;
+            const uint32_t w0 = pack_bf16(__uint_as_float(src[o + 0]) * sc, __uint_as_float(src[o + 1]) * sc);
+            const uint32_t w1 = pack_bf16(__uint_as_float(src[o + 2]) * sc, __uint_as_float(src[o + 3]) * sc);
+            const uint32_t w2 = pack_bf16(__uint_as_float(src[o + 4]) * sc, __uint_as_float(src[o + 5]) * sc);
+            const uint32_t w3 = pack_bf16(__uint_as_float(src[o + 6]) * sc, __uint_as_float(src[o + 7]) * sc);
+            const uint32_t w4_ = pack_bf16(__uint_as_float(src[o + 8]) * sc, __uint_as_float(src[o + 9]) * sc);
+            const uint32_t w5 = pack_bf16(__uint_as_float(src[o + 10]) * sc, __uint_as_float(src[o + 11]) * sc);
+            const uint32_t w6 = pack_bf16(__uint_as_float(src[o + 12]) * sc, __uint_as_float(src[o + 13]) * sc);
+            const uint32_t w7 = pack_bf16(__uint_as_float(src[o + 14]) * sc, __uint_as_float(src[o + 15]) * sc);
+            const uint32_t a0 = stw + lane * 128 + ((((2 * u) ^ lane) & 7) << 4);
+            const uint32_t a1 = stw + lane * 128 + ((((2 * u + 1) ^ lane) & 7) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(a0), "r"(w0), "r"(w1),
+                         "r"(w2), "r"(w3)
+                         : "memory");
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(a1), "r"(w4_), "r"(w5),
+                         "r"(w6), "r"(w7)
+                         : "memory");
+          }
+          __syncwarp();
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int rr = u * 4 + lane / 8, c = lane % 8;
+            const long long drr = __shfl_sync(0xffffffffu, dst, rr);
+            uint4 v;
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];\n"
+                         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                         : "r"(stw + rr * 128 + (((c ^ rr) & 7) << 4)));
+            if (drr >= 0) st_global_v4(A.opart + drr * kD + h * 64 + c * 8, v);
+          }
+          __syncwarp();
+        }
+        if (dst >= 0) A.lpart[dst] = lse;
+      }
+    }
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+template <int G>
+static void attn_fwd_g(const CUtensorMap& mk, const CUtensorMap& mv, const FwdArgs& a,
+                       cudaStream_t st) {
+  const size_t smem = sizeof(FwdShared) + 1024 + 6 * kFwdTile + 4 * kStageWarp;
+  cudaFuncSetAttribute(attn_fwd_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  attn_fwd_kernel<G><<<num_sms(), 384, smem, st>>>(mk, mv, a);
+}
+
+int fwd_item_tiles() { return kFwdItemTiles; }
+
+bool launch_attn_fwd(const Dims& d, const void* q, const void* k, const void* v,
+                     const int* seg_offset, const int* entries, const Item* items,
+                     const int* n_items, long long max_items, void* opart, float* lpart,
+                     unsigned* status, cudaStream_t st) {
+  CUtensorMap mk, mv;
+  const uint64_t kvd[3] = {128, (uint64_t)d.Hkv, (uint64_t)d.B * d.S};
+  const uint64_t kvs[2] = {128 * 2, (uint64_t)d.Hkv * 128 * 2};
+  const uint32_t kvb[3] = {64, 1, 128};
+  if (!make_tmap_bf16(&mk, k, 3, kvd, kvs, kvb) || !make_tmap_bf16(&mv, v, 3, kvd, kvs, kvb))
+    return false;
+  FwdArgs a;
+  a.d = d;
+  a.q = (const bf16*)q;
+  a.seg_offset = seg_offset;
+  a.entries = entries;
+  a.items = items;
+  a.n_items = n_items;
+  a.max_items = max_items;
+  a.opart = (bf16*)opart;
+  a.lpart = lpart;
+  a.status = status;
+  switch (d.G) {
+    case 1: attn_fwd_g<1>(mk, mv, a, st); break;
+    case 2: attn_fwd_g<2>(mk, mv, a, st); break;
+    case 4: attn_fwd_g<4>(mk, mv, a, st); break;
+    case 8: attn_fwd_g<8>(mk, mv, a, st); break;
+    case 16: attn_fwd_g<16>(mk, mv, a, st); break;
+    default: return false;
+  }
+  return true;
+}
+
+}  // namespace msa

@@ -1,13 +1,9 @@
-// Forward kernels: sparse main attention (KV-outer over the inverted block map, gathered query
-// tiles, then a combine), the dense warmup forward, and the proxy normaliser used by the
-// backward (sparse over the selected blocks, dense over the causal prefix).
-//
-// Sparse main attention (blog "Forward > Main attention"; forum summary "GPU kernel co-design":
-// KV-outer iteration with query gathering, two-phase forward).  A work item is one key block n of
-// one group g together with up to 128/G tokens that selected it; the G query heads of each token
-// fill the 128 rows of the tile, so every row of the 128 x 128 score tile is useful work.  Each
-// (token, head, slot) gets a partial result (normalised output + its log-sum-exp) and a combine
-// kernel merges the <= top_k partials of every row into O and LSE.
+// Forward kernels on CUDA cores and warp-level m16n8k16 tensor-core products:
+//   combine_kernel            second phase of the sparse forward (attn_fwd.cu writes the
+//                             per-(token, head, slot) partials it merges)
+//   dense_fwd_kernel          dense causal forward of the warmup mode
+//   proxy_lse_*_kernel        proxy normaliser used by the backward (sparse over the selected
+//                             blocks, dense over the causal prefix)
 #include <math.h>
 
 #include "common.cuh"
@@ -86,102 +82,16 @@ __device__ __forceinline__ void online_step(float (&s)[8][4], float (&m)[2], flo
 }
 
 // ------------------------------------------------------------------------------------------
-// Sparse forward: one item = (b, g, block n) and <= 128/G tokens; 8 warps x 16 rows.
-template <int G>
-__global__ void __launch_bounds__(256, 2)
-    sparse_fwd_kernel(Dims d, const bf16* __restrict__ q, const bf16* __restrict__ k,
-                      const bf16* __restrict__ v, const int* __restrict__ seg_offset,
-                      const int* __restrict__ entries, const Item* __restrict__ items,
-                      const int* __restrict__ n_items, long long max_items,
-                      bf16* __restrict__ opart, float* __restrict__ lpart) {
-  constexpr int TT = 128 / G;
-  extern __shared__ __align__(128) uint8_t smem[];
-  bf16* sQ = reinterpret_cast<bf16*>(smem);
-  bf16* sK = sQ + 128 * kLd;
-  bf16* sV = sK + 128 * kLd;
-  int* sTok = reinterpret_cast<int*>(sV + 128 * kLd);
-  int* sSlot = sTok + TT;
-  const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
-  const float sl2 = d.scale * kLog2e;
-  long long total = *n_items;
-  if (total > max_items) total = max_items;
-  for (long long it = blockIdx.x; it < total; it += gridDim.x) {
-    const Item item = items[it];
-    const int n = item.seg % d.nblk;
-    const int bg = (int)((item.seg % d.nseg()) / d.nblk);
-    const int b = bg / d.Hp, g = bg % d.Hp;
-    if (tid < TT) {
-      int t = -1, slot = 0;
-      if (tid < item.count) {
-        const int e = entries[seg_offset[item.seg] + item.first + tid];
-        t = e >> 8;
-        slot = e & 255;
-      }
-      sTok[tid] = t;
-      sSlot[tid] = slot;
-    }
-    __syncthreads();
-    load_rows_async(sQ, 128, [&](int r) -> const bf16* {
-      const int t = sTok[r / G];
-      return t < 0 ? nullptr : q + (((size_t)b * d.S + t) * d.Hq + g * G + r % G) * kD;
-    }, tid, 256, q);
-    load_rows_async(sK, 128, [&](int r) -> const bf16* {
-      return k + (((size_t)b * d.S + n * kBlock + r) * d.Hkv + g) * kD;
-    }, tid, 256, k);
-    load_rows_async(sV, 128, [&](int r) -> const bf16* {
-      return v + (((size_t)b * d.S + n * kBlock + r) * d.Hkv + g) * kD;
-    }, tid, 256, v);
-    cp_async_commit();
-    cp_async_wait_all();
-    __syncthreads();
-
-    const int ra = warp * 16 + lane / 4, rb = ra + 8;
-    int ta = sTok[ra / G], tb = sTok[rb / G];
-    const bool va = ta >= 0, vb = tb >= 0;
-    if (!va) ta = 0x7fffffff;  // padding rows: unmasked, results discarded
-    if (!vb) tb = 0x7fffffff;
-    float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
-    float o[16][4];
-    zero_acc(o);
-#pragma unroll 1
-    for (int half = 0; half < 2; ++half) {
-      float s[8][4];
-      zero_acc(s);
-      warp_gemm_abt<64, 128>(s, sQ + warp * 16 * kLd, kLd, sK + half * 64 * kLd, kLd, lane);
-      online_step<true>(s, m, l, o, sV + half * 64 * kLd, kLd, n * kBlock + half * 64, ta, tb,
-                        sl2, lane);
-    }
-    l[0] = quad_sum(l[0]);
-    l[1] = quad_sum(l[1]);
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const bool valid = r == 0 ? va : vb;
-      if (!valid) continue;
-      const int row = r == 0 ? ra : rb;
-      const int i = row / G;
-      const int t = sTok[i];
-      const int h = g * G + row % G;
-      const size_t base = (((size_t)b * d.S + t) * d.Hq + h) * d.top_k + sSlot[i];
-      const float inv = 1.f / l[r];
-      bf16* dst = opart + base * kD + 2 * (lane % 4);
-#pragma unroll
-      for (int jt = 0; jt < 16; ++jt) {
-        *reinterpret_cast<uint32_t*>(dst + 8 * jt) =
-            pack_bf16(o[jt][2 * r] * inv, o[jt][2 * r + 1] * inv);
-      }
-      if (lane % 4 == 0) lpart[base] = (m[r] + log2f(l[r])) * kLn2;
-    }
-    __syncthreads();
-  }
-}
-
-// ------------------------------------------------------------------------------------------
-// Combine: one warp per (b, t, h) merges the partials of its valid slots.
-__global__ void combine_kernel(Dims d, const int32_t* __restrict__ idx, const bf16* __restrict__ opart,
-                               const float* __restrict__ lpart, bf16* __restrict__ o,
-                               float* __restrict__ lse) {
+// Combine (second phase of the sparse forward): one warp per (b, t, h) merges the partials of
+// its valid slots,  O = sum_s w_s O_s / sum_s w_s,  w_s = exp(lse_s - max),  LSE = max + log sum.
+// Half-warps take alternate slots with 16-byte loads (8 columns per lane), so a warp keeps
+// several 512-byte reads in flight.
+__global__ void __launch_bounds__(256) combine_kernel(Dims d, const int32_t* __restrict__ idx,
+                                                      const bf16* __restrict__ opart,
+                                                      const float* __restrict__ lpart,
+                                                      bf16* __restrict__ o, float* __restrict__ lse) {
   const long long rows = (long long)d.B * d.S * d.Hq;
-  const int lane = threadIdx.x % 32;
+  const int lane = threadIdx.x % 32, half = lane >> 4, l16 = lane & 15;
   for (long long r = (blockIdx.x * (long long)blockDim.x + threadIdx.x) / 32; r < rows;
        r += (long long)gridDim.x * blockDim.x / 32) {
     const int h = (int)(r % d.Hq);
@@ -190,34 +100,48 @@ __global__ void combine_kernel(Dims d, const int32_t* __restrict__ idx, const bf
     const int g = h / d.G;
     const int32_t* row = idx + (((size_t)b * d.Hp + g) * d.S + t) * d.top_k;
     const size_t base = (size_t)r * d.top_k;
-    float mx = -INFINITY;
+    unsigned long long valid = 0;
     {
       int prev = -1;
       bool padded = false;
       for (int s = 0; s < d.top_k; ++s)
-        if (slot_valid(row, s, t, prev, padded)) mx = fmaxf(mx, lpart[base + s]);
+        if (slot_valid(row, s, t, prev, padded)) valid |= 1ull << s;
     }
-    float sum = 0.f;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    if (mx != -INFINITY) {
-      int prev = -1;
-      bool padded = false;
-      for (int s = 0; s < d.top_k; ++s) {
-        if (!slot_valid(row, s, t, prev, padded)) continue;
-        const float w = expf(lpart[base + s] - mx);
-        sum += w;
-        const uint2 pv = *reinterpret_cast<const uint2*>(opart + (base + s) * kD + lane * 4);
-        const __nv_bfloat162 p01 = *reinterpret_cast<const __nv_bfloat162*>(&pv.x);
-        const __nv_bfloat162 p23 = *reinterpret_cast<const __nv_bfloat162*>(&pv.y);
-        acc[0] += w * __low2float(p01);
-        acc[1] += w * __high2float(p01);
-        acc[2] += w * __low2float(p23);
-        acc[3] += w * __high2float(p23);
+    const float l0 = (valid >> lane) & 1 ? lpart[base + lane] : -INFINITY;
+    const float l1 = lane + 32 < d.top_k && ((valid >> (lane + 32)) & 1) ? lpart[base + lane + 32] : -INFINITY;
+    float mx = fmaxf(l0, l1);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    const float w0 = l0 == -INFINITY ? 0.f : expf(l0 - mx);
+    const float w1 = l1 == -INFINITY ? 0.f : expf(l1 - mx);
+    float sum = w0 + w1;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+    for (int s0 = 0; s0 < d.top_k; s0 += 2) {
+      const int s = s0 + half;
+      const float a = __shfl_sync(0xffffffffu, w0, s & 31);
+      const float c = __shfl_sync(0xffffffffu, w1, s & 31);
+      const float w = s < 32 ? a : c;
+      if (s < d.top_k && w > 0.f) {
+        const uint4 pv = *reinterpret_cast<const uint4*>(opart + (base + s) * kD + l16 * 8);
+        const uint32_t pw[4] = {pv.x, pv.y, pv.z, pv.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const __nv_bfloat162 p2 = *reinterpret_cast<const __nv_bfloat162*>(&pw[e]);
+          acc[2 * e] += w * __low2float(p2);
+          acc[2 * e + 1] += w * __high2float(p2);
+        }
       }
     }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], 16);
     const float inv = sum > 0.f ? 1.f / sum : 0.f;
-    *reinterpret_cast<uint2*>(o + (size_t)r * kD + lane * 4) =
-        make_uint2(pack_bf16(acc[0] * inv, acc[1] * inv), pack_bf16(acc[2] * inv, acc[3] * inv));
+    if (half == 0)
+      *reinterpret_cast<uint4*>(o + (size_t)r * kD + l16 * 8) =
+          make_uint4(pack_bf16(acc[0] * inv, acc[1] * inv), pack_bf16(acc[2] * inv, acc[3] * inv),
+                     pack_bf16(acc[4] * inv, acc[5] * inv), pack_bf16(acc[6] * inv, acc[7] * inv));
     if (lane == 0) lse[((size_t)b * d.Hq + h) * d.S + t] = sum > 0.f ? mx + logf(sum) : -INFINITY;
   }
 }
@@ -488,36 +412,11 @@ __global__ void __launch_bounds__(256, 2)
 // ------------------------------------------------------------------------------------------
 static int persistent_grid(int ctas_per_sm) { return num_sms() * ctas_per_sm; }
 
-template <int G>
-static void sparse_fwd_g(const Dims& d, const void* q, const void* k, const void* v,
-                         const int* seg_offset, const int* entries, const Item* items,
-                         const int* n_items, long long max_items, void* opart, float* lpart,
-                         cudaStream_t st) {
-  const size_t smem = 3 * 128 * kLd * sizeof(bf16) + 2 * (128 / G) * sizeof(int);
-  cudaFuncSetAttribute(sparse_fwd_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  sparse_fwd_kernel<G><<<persistent_grid(2), 256, smem, st>>>(
-      d, (const bf16*)q, (const bf16*)k, (const bf16*)v, seg_offset, entries, items, n_items,
-      max_items, (bf16*)opart, lpart);
-}
-
-void launch_sparse_fwd(const Dims& d, const void* q, const void* k, const void* v,
-                       const int* seg_offset, const int* entries, const Item* items,
-                       const int* n_items, long long max_items, void* opart, float* lpart,
-                       cudaStream_t st) {
-  switch (d.G) {
-    case 1: sparse_fwd_g<1>(d, q, k, v, seg_offset, entries, items, n_items, max_items, opart, lpart, st); break;
-    case 2: sparse_fwd_g<2>(d, q, k, v, seg_offset, entries, items, n_items, max_items, opart, lpart, st); break;
-    case 4: sparse_fwd_g<4>(d, q, k, v, seg_offset, entries, items, n_items, max_items, opart, lpart, st); break;
-    case 8: sparse_fwd_g<8>(d, q, k, v, seg_offset, entries, items, n_items, max_items, opart, lpart, st); break;
-    case 16: sparse_fwd_g<16>(d, q, k, v, seg_offset, entries, items, n_items, max_items, opart, lpart, st); break;
-  }
-}
-
 void launch_combine(const Dims& d, const int32_t* idx, const void* opart, const float* lpart,
                     void* o, float* lse, cudaStream_t st) {
   const long long rows = (long long)d.B * d.S * d.Hq;
   long long grid = (rows * 32 + 255) / 256;
-  if (grid > (long long)num_sms() * 16) grid = (long long)num_sms() * 16;
+  if (grid > (long long)num_sms() * 8) grid = (long long)num_sms() * 8;
   combine_kernel<<<(int)grid, 256, 0, st>>>(d, idx, (const bf16*)opart, lpart, (bf16*)o, lse);
 }
 

@@ -49,10 +49,15 @@ bool launch_proxy_topk(const Dims& d, const void* qp, const void* kp, int32_t* i
                        unsigned* status, cudaStream_t st);
 
 // ---------------------------------------------------------------- forward (fwd.cu)
-void launch_sparse_fwd(const Dims& d, const void* q, const void* k, const void* v,
-                       const int* seg_offset, const int* entries, const Item* items,
-                       const int* n_items, long long max_items, void* opart, float* lpart,
-                       cudaStream_t st);
+// Sparse main-attention partials (attn_fwd.cu): for every list entry (t, slot) and query head h
+// of the group, the block's normalised output (bf16, opart[(t, h, slot)][128]) and its natural
+// log-sum-exp (lpart).  Returns false for an unsupported group size or if the TMA tensor maps
+// cannot be created.
+bool launch_attn_fwd(const Dims& d, const void* q, const void* k, const void* v,
+                     const int* seg_offset, const int* entries, const Item* items,
+                     const int* n_items, long long max_items, void* opart, float* lpart,
+                     unsigned* status, cudaStream_t st);
+int fwd_item_tiles();  // 128-row tiles per sparse-forward work item
 void launch_combine(const Dims& d, const int32_t* idx, const void* opart, const float* lpart,
                     void* o, float* lse, cudaStream_t st);
 void launch_dense_fwd(const Dims& d, const void* q, const void* k, const void* v, void* o,

@@ -20,8 +20,9 @@
  *                                                top_k blocks are visible
  *   Query head h belongs to group h / (Hq / Hkv).  Key j is visible to token t iff j <= t.
  *   Every pointer must be 16-byte aligned.  Supported: head dim 128, block 128 (blog / package
- *   caveat 1), S % 128 == 0, Hp == Hkv (package caveat 5), Hq / Hkv in {1, 2, 4, 8, 16},
- *   1 <= top_k <= 64.
+ *   caveat 1), S % 128 == 0, Hp == Hkv (package caveat 5), 1 <= top_k <= 64, and a group size
+ *   Hq / Hkv in {1, 2, 4, 8, 16} for the forward ops, {4, 8, 16} for the backward ops (other
+ *   group sizes return MSA_ERR_UNSUPPORTED).
  *   `workspace` is caller-owned device memory of at least msa_workspace_size() bytes for the
  *   same op and shape; the library allocates nothing.  The first 256 bytes hold a device status
  *   word (see msa_device_status).  Calls sharing one workspace must not overlap on the GPU.
