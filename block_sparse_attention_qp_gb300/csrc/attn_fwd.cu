@@ -11,9 +11,9 @@
 //   partial (t, h, slot) = O / l in bf16, and its log-sum-exp m + log l   (epilogue warps)
 // Phase 2 (combine_kernel in fwd.cu) merges the <= top_k partials of every (t, h).
 //
-// Roles (384 threads): warp 0 TMA loads of K/V (two stages) and tensor-memory ownership, warp 1
-// the MMA issuer, warps 2-3 gather the tile's Q rows (cp.async, two buffers), warps 4-7 softmax,
-// warps 8-11 epilogue.  Tensor memory (512 columns): S0, S1 (S, then P in place), O0, O1.
+// Roles (384 threads): warp 0 TMA loads of K/V (a three-slot ring) and tensor-memory ownership,
+// warp 1 the MMA issuer, warps 2-3 gather the tile's Q rows (cp.async, three buffers), warps 4-7
+// softmax, warps 8-11 epilogue.  Tensor memory (512 columns): S0, S1 (S, then P in place), O0, O1.
 // The MMA issuer runs S of tile i before O of tile i-1, so the tensor pipe works on one tile while
 // the softmax warps work on the next.  Every wait is bounded (see sm100::mbar_wait).
 #include <math.h>
@@ -29,6 +29,8 @@ namespace {
 constexpr int kFwdRows = 128;                  // rows (tokens x heads) per tile
 constexpr int kFwdTile = kFwdRows * 128 * 2;   // one 128-row x 128 bf16 tile (two SW128 panels)
 constexpr int kFwdItemTiles = 8;               // tiles per work item
+constexpr int kRing = 3;                       // K/V ring slots (one 128 x 128 tile each)
+constexpr int kQBuf = 3;                       // gathered Q buffers
 constexpr int kStageWarp = 32 * 128;           // epilogue staging per warp: 32 rows x 128 bytes
 
 struct FwdArgs {
@@ -45,13 +47,13 @@ struct FwdArgs {
 };
 
 struct FwdShared {
-  int tok[2][kFwdRows];         // token of each tile token (-1: none), per Q buffer
-  int slot[2][kFwdRows];        // its selection slot
+  int tok[kQBuf][kFwdRows];     // token of each tile token (-1: none), per Q buffer
+  int slot[kQBuf][kFwdRows];    // its selection slot
   long long dst[2][kFwdRows];   // partial row (t, h, slot) of each tile row (-1: none), per O buffer
   float inv_l[2][kFwdRows];     // 1 / l of each row
   float lse[2][kFwdRows];       // natural log-sum-exp of each row's partial
-  uint64_t kv_full[2], kv_empty[2], q_full[2], q_empty[2], meta_free[2], s_full[2], p_full[2],
-      o_full[2], o_free[2], mma_done;
+  uint64_t kv_full[kRing], kv_empty[kRing], q_full[kQBuf], q_empty[kQBuf], meta_free[kQBuf],
+      s_full[2], p_full[2], o_full[2], o_free[2], mma_done;
   uint32_t tmem;
 };
 
@@ -65,6 +67,23 @@ __device__ __forceinline__ void st_global_v4(void* p, uint4 v) {
   asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
                "r"(v.w)
                : "memory");
+}
+// Arrive on `mbar` once every cp.async this thread issued so far has landed (counts as one of
+// the barrier's expected arrivals).
+__device__ __forceinline__ void cp_async_arrive(uint64_t* mbar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_u32(mbar))
+               : "memory");
+}
+
+// The K/V ring: loads alternate K, V, K, V, ... (load L = 2 * item + {0: K, 1: V}) over kRing
+// slots, so the next item's V can land as soon as the current item's K is no longer needed.
+struct RingPos {
+  int slot;
+  uint32_t parity;  // phase parity of this use of the slot
+  long long use;    // how many times the slot was used before
+};
+__device__ __forceinline__ RingPos ring_pos(long long load) {
+  return RingPos{(int)(load % kRing), (uint32_t)((load / kRing) & 1), load / kRing};
 }
 
 }  // namespace
@@ -80,11 +99,10 @@ __global__ void __launch_bounds__(384, 1)
   extern __shared__ uint8_t smem_raw[];
   FwdShared* sh = reinterpret_cast<FwdShared*>(smem_raw);
   uint8_t* base = align1024(smem_raw + sizeof(FwdShared));
-  uint8_t* sK = base;                 // [2 stages][128 keys][128 d]   (TMA)
-  uint8_t* sV = sK + 2 * kFwdTile;    // [2 stages][128 keys][128 d]   (TMA)
-  uint8_t* sQ = sV + 2 * kFwdTile;    // [2][128 rows][128 d]          (gathered)
-  uint8_t* sSt = sQ + 2 * kFwdTile;   // epilogue staging, [4 warps][32 rows][128 bytes]
-  const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ), aSt = smem_u32(sSt);
+  uint8_t* sR = base;                     // K/V ring: [kRing][128 keys][128 d]   (TMA)
+  uint8_t* sQ = sR + kRing * kFwdTile;    // [kQBuf][128 rows][128 d]          (gathered)
+  uint8_t* sSt = sQ + kQBuf * kFwdTile;   // epilogue staging, [4 warps][32 rows][128 bytes]
+  const uint32_t aR = smem_u32(sR), aQ = smem_u32(sQ), aSt = smem_u32(sSt);
 
   const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
   const float sl2 = d.scale * kLog2e;
@@ -92,12 +110,16 @@ __global__ void __launch_bounds__(384, 1)
   if (total > A.max_items) total = A.max_items;
 
   if (tid == 0) {
-    for (int x = 0; x < 2; ++x) {
+    for (int x = 0; x < kRing; ++x) {
       mbar_init(&sh->kv_full[x], 1);
       mbar_init(&sh->kv_empty[x], 1);
-      mbar_init(&sh->q_full[x], 64);
+    }
+    for (int x = 0; x < kQBuf; ++x) {
+      mbar_init(&sh->q_full[x], 128);  // 64 gather lanes: one plain and one cp.async arrival each
       mbar_init(&sh->q_empty[x], 1);
       mbar_init(&sh->meta_free[x], 4);
+    }
+    for (int x = 0; x < 2; ++x) {
       mbar_init(&sh->s_full[x], 1);
       mbar_init(&sh->p_full[x], 4);
       mbar_init(&sh->o_full[x], 1);
@@ -122,120 +144,174 @@ __global__ void __launch_bounds__(384, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      long long ni = 0;
-      for (long long it = blockIdx.x; it < total; it += gridDim.x, ++ni) {
+      long long nl = 0;  // loads issued
+      for (long long it = blockIdx.x; ok && it < total; it += gridDim.x) {
         const Item item = A.items[it];
         const int n = item.seg % d.nblk;
         const int bg = (int)((item.seg % d.nseg()) / d.nblk);
         const int b = bg / d.Hp, g = bg % d.Hp;
-        const int s = (int)(ni & 1);
-        if (ni >= 2 && !mbar_wait(&sh->kv_empty[s], par((ni - 2) >> 1), A.status)) break;
         const int row0 = b * d.S + n * kBlock;
-        uint8_t* k_s = sK + s * kFwdTile;
-        uint8_t* v_s = sV + s * kFwdTile;
-        mbar_expect_tx(&sh->kv_full[s], 2 * kFwdTile);
-        tma_load_3d(k_s, &tm_k, 0, g, row0, &sh->kv_full[s]);
-        tma_load_3d(k_s + kFwdTile / 2, &tm_k, 64, g, row0, &sh->kv_full[s]);
-        tma_load_3d(v_s, &tm_v, 0, g, row0, &sh->kv_full[s]);
-        tma_load_3d(v_s + kFwdTile / 2, &tm_v, 64, g, row0, &sh->kv_full[s]);
+        for (int w = 0; w < 2; ++w) {
+          const RingPos rp = ring_pos(nl);
+          if (rp.use >= 1 && !mbar_wait(&sh->kv_empty[rp.slot], rp.parity ^ 1u, A.status)) {
+            ok = false;
+            break;
+          }
+          uint8_t* dst = sR + rp.slot * kFwdTile;
+          const CUtensorMap* tm = w == 0 ? &tm_k : &tm_v;
+          mbar_expect_tx(&sh->kv_full[rp.slot], kFwdTile);
+          tma_load_3d(dst, tm, 0, g, row0, &sh->kv_full[rp.slot]);
+          tma_load_3d(dst + kFwdTile / 2, tm, 64, g, row0, &sh->kv_full[rp.slot]);
+          ++nl;
+        }
       }
       // no copy may still be landing in shared memory when the block exits
-      for (long long x = (ni >= 2 ? ni - 2 : 0); x < ni; ++x)
-        mbar_wait(&sh->kv_full[x & 1], par(x >> 1), A.status);
+      for (long long x = (nl >= kRing ? nl - kRing : 0); x < nl; ++x) {
+        const RingPos rp = ring_pos(x);
+        mbar_wait(&sh->kv_full[rp.slot], rp.parity, A.status);
+      }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);  // S = Q K^T
       constexpr uint32_t id_o = idesc_bf16(128, 128, false, true);   // O = P V
-      long long ni = 0, i = 0;
+      struct Pending {
+        long long ti;
+        RingPos v;
+        bool first, last;
+      };
+      Pending pd{};
       bool pending = false;
-      long long pi = 0;
-      int ps = 0;
-      bool plast = false;
-      auto mma_o = [&](long long ti, int s, bool last) -> bool {
-        const int b = (int)(ti & 1);
-        if (!mbar_wait(&sh->p_full[b], par(ti >> 1), A.status)) return false;
-        if (ti >= 2 && !mbar_wait(&sh->o_free[b], par((ti - 2) >> 1), A.status)) return false;
+      auto mma_o = [&](const Pending& p) -> bool {
+        const int b = (int)(p.ti & 1);
+        if (!mbar_wait(&sh->p_full[b], par(p.ti >> 1), A.status)) return false;
+        if (p.first && !mbar_wait(&sh->kv_full[p.v.slot], p.v.parity, A.status)) return false;
+        if (p.ti >= 2 && !mbar_wait(&sh->o_free[b], par((p.ti - 2) >> 1), A.status)) return false;
         fence_after_sync();
-        const uint32_t aVs = aV + s * kFwdTile;
+        const uint32_t aV = aR + p.v.slot * kFwdTile;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          mma_ts(O0 + 128 * b, S0 + 128 * b + ks * 8, desc_mnmajor(aVs, 128, ks), id_o, ks > 0);
+          mma_ts(O0 + 128 * b, S0 + 128 * b + ks * 8, desc_mnmajor(aV, 128, ks), id_o, ks > 0);
         mma_commit(&sh->o_full[b]);
-        if (last) mma_commit(&sh->kv_empty[s]);
+        if (p.last) mma_commit(&sh->kv_empty[p.v.slot]);
         return true;
       };
+      long long ni = 0, i = 0;
       for (long long it = blockIdx.x; ok && it < total; it += gridDim.x, ++ni) {
         const Item item = A.items[it];
-        const int s = (int)(ni & 1);
-        if (!mbar_wait(&sh->kv_full[s], par(ni >> 1), A.status)) { ok = false; break; }
-        const uint32_t aKs = aK + s * kFwdTile;
+        const RingPos kp = ring_pos(2 * ni), vp = ring_pos(2 * ni + 1);
+        if (!mbar_wait(&sh->kv_full[kp.slot], kp.parity, A.status)) { ok = false; break; }
+        const uint32_t aK = aR + kp.slot * kFwdTile;
         const int ntiles = (item.count + TT - 1) / TT;
-        if (ntiles == 0) mma_commit(&sh->kv_empty[s]);  // (items are never empty)
+        if (ntiles == 0) {  // (items are never empty)
+          mma_commit(&sh->kv_empty[kp.slot]);
+          if (!mbar_wait(&sh->kv_full[vp.slot], vp.parity, A.status)) { ok = false; break; }
+          mma_commit(&sh->kv_empty[vp.slot]);
+        }
         for (int tl = 0; tl < ntiles; ++tl, ++i) {
-          const int b = (int)(i & 1);
-          if (!mbar_wait(&sh->q_full[b], par(i >> 1), A.status)) { ok = false; break; }
+          const int b = (int)(i & 1), qb = (int)(i % kQBuf);
+          if (!mbar_wait(&sh->q_full[qb], par(i / kQBuf), A.status)) { ok = false; break; }
           // S_b still holds P of tile i-2 until that tile's O product has completed
           if (i >= 2 && !mbar_wait(&sh->o_full[b], par((i - 2) >> 1), A.status)) { ok = false; break; }
           fence_after_sync();
-          const uint32_t aQb = aQ + b * kFwdTile;
+          const uint32_t aQb = aQ + qb * kFwdTile;
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            mma_ss(S0 + 128 * b, desc_kmajor(aQb, 128, ks), desc_kmajor(aKs, 128, ks), id_s, ks > 0);
+            mma_ss(S0 + 128 * b, desc_kmajor(aQb, 128, ks), desc_kmajor(aK, 128, ks), id_s, ks > 0);
           mma_commit(&sh->s_full[b]);
-          mma_commit(&sh->q_empty[b]);
-          if (pending && !mma_o(pi, ps, plast)) { ok = false; break; }
+          mma_commit(&sh->q_empty[qb]);
+          if (tl == ntiles - 1) mma_commit(&sh->kv_empty[kp.slot]);
+          if (pending && !mma_o(pd)) { ok = false; break; }
           pending = true;
-          pi = i;
-          ps = s;
-          plast = tl == ntiles - 1;
+          pd = Pending{i, vp, tl == 0, tl == ntiles - 1};
         }
       }
-      if (ok && pending) mma_o(pi, ps, plast);
+      if (ok && pending) mma_o(pd);
       mma_commit(&sh->mma_done);
       mbar_wait(&sh->mma_done, 0, A.status);
     }
   } else if (warp < 4) {
     // ---------------------------------------------------------------- gather: Q rows
-    const int w2 = warp - 2;             // rows [64 w2, 64 w2 + 64)
-    constexpr int XT = 64 / G;           // tokens per gather warp
+    // Each of the two warps fills 64 rows of every tile.  The copies complete asynchronously
+    // (tracked by q_full); the warp prefetches the next tile's list entries and the next item.
+    const int w2 = warp - 2;        // rows [64 w2, 64 w2 + 64)
+    constexpr int XT = 64 / G;      // tokens per gather warp
     const int x0 = w2 * XT;
-    long long i = 0;
-    for (long long it = blockIdx.x; ok && it < total; it += gridDim.x) {
-      const Item item = A.items[it];
-      const int bg = (int)((item.seg % d.nseg()) / d.nblk);
-      const int b = bg / d.Hp, g = bg % d.Hp;
-      const long long eb = (long long)A.seg_offset[item.seg] + item.first;
-      const int ntiles = (item.count + TT - 1) / TT;
-      for (int tl = 0; tl < ntiles; ++tl, ++i) {
-        const int bb = (int)(i & 1);
-        if (i >= 2 && (!mbar_wait(&sh->q_empty[bb], par((i - 2) >> 1), A.status) ||
-                       !mbar_wait(&sh->meta_free[bb], par((i - 2) >> 1), A.status))) {
+    long long it = blockIdx.x;
+    if (it < total) {
+      Item cur = A.items[it];
+      long long ceb = (long long)A.seg_offset[cur.seg] + cur.first;
+      long long nit = it + gridDim.x;
+      Item nxt{};
+      long long neb = 0;
+      if (nit < total) {
+        nxt = A.items[nit];
+        neb = (long long)A.seg_offset[nxt.seg] + nxt.first;
+      }
+      int tl = 0;
+      int e[2];
+      auto load_e = [&](long long eb, int count, int tile) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int xx = lane + 32 * u;
+          const int pos = tile * TT + x0 + xx;
+          e[u] = (xx < XT && pos < count) ? A.entries[eb + pos] : -1;
+        }
+      };
+      load_e(ceb, cur.count, 0);
+      long long i = 0;
+      while (true) {
+        const int qb = (int)(i % kQBuf);
+        if (i >= kQBuf && (!mbar_wait_warp(&sh->q_empty[qb], par(i / kQBuf - 1), A.status) ||
+                           !mbar_wait_warp(&sh->meta_free[qb], par(i / kQBuf - 1), A.status))) {
           ok = false;
           break;
         }
-        for (int xx = lane; xx < XT; xx += 32) {
-          const int pos = tl * TT + x0 + xx;
-          const int e = pos < item.count ? A.entries[eb + pos] : -1;
-          sh->tok[bb][x0 + xx] = e < 0 ? -1 : (e >> 8);
-          sh->slot[bb][x0 + xx] = e < 0 ? 0 : (e & 255);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int xx = lane + 32 * u;
+          if (xx < XT) {
+            sh->tok[qb][x0 + xx] = e[u] < 0 ? -1 : (e[u] >> 8);
+            sh->slot[qb][x0 + xx] = e[u] < 0 ? 0 : (e[u] & 255);
+          }
         }
         __syncwarp();
-        uint8_t* dQb = sQ + bb * kFwdTile;
+        const int bg = (int)((cur.seg % d.nseg()) / d.nblk);
+        const int b = bg / d.Hp, g = bg % d.Hp;
+        uint8_t* dQb = sQ + qb * kFwdTile;
 #pragma unroll 8
         for (int k = 0; k < 32; ++k) {
           const int c = lane + 32 * k;
           const int r = 64 * w2 + (c >> 4), ch = c & 15;
-          const int t = sh->tok[bb][r / G];
+          const int t = sh->tok[qb][r / G];
           const uint32_t off = (ch >> 3) * (kFwdRows * 128) + sm100::sw128_chunk(r, ch & 7);
           const size_t grow = (((size_t)b * d.S + (t < 0 ? 0 : t)) * d.Hq + g * G + r % G) * kD + ch * 8;
           cp_async16(dQb + off, A.q + grow, t >= 0);
         }
-        cp_async_wait_all();
-        fence_async_smem();
-        mbar_arrive(&sh->q_full[bb]);
+        cp_async_arrive(&sh->q_full[qb]);
+        mbar_arrive(&sh->q_full[qb]);  // publishes tok / slot
+        ++i;
+        // advance: next tile of this item, or the first tile of the next item
+        const int ntiles = (cur.count + TT - 1) / TT;
+        if (tl + 1 < ntiles) {
+          ++tl;
+          load_e(ceb, cur.count, tl);
+        } else {
+          it = nit;
+          if (it >= total) break;
+          cur = nxt;
+          ceb = neb;
+          tl = 0;
+          load_e(ceb, cur.count, 0);
+          nit = it + gridDim.x;
+          if (nit < total) {
+            nxt = A.items[nit];
+            neb = (long long)A.seg_offset[nxt.seg] + nxt.first;
+          }
+        }
       }
+      cp_async_wait_all();  // nothing may land after the block exits
     }
   } else if (warp < 8) {
     // ---------------------------------------------------------------- softmax
@@ -250,61 +326,98 @@ __global__ void __launch_bounds__(384, 1)
       const int b = bg / d.Hp, g = bg % d.Hp;
       const int ntiles = (item.count + TT - 1) / TT;
       for (int tl = 0; tl < ntiles; ++tl, ++i) {
-        const int bb = (int)(i & 1);
+        const int bb = (int)(i & 1), qb = (int)(i % kQBuf);
         __syncwarp();
-        if (!mbar_wait(&sh->s_full[bb], par(i >> 1), A.status) ||
-            !mbar_wait(&sh->q_full[bb], par(i >> 1), A.status)) {
+        if (!mbar_wait_warp(&sh->s_full[bb], par(i >> 1), A.status) ||
+            !mbar_wait_warp(&sh->q_full[qb], par(i / kQBuf), A.status)) {
           ok = false;
           break;
         }
         fence_after_sync();
-        const int t = sh->tok[bb][r / G];
-        const int slot = sh->slot[bb][r / G];
+        const int t = sh->tok[qb][r / G];
+        const int slot = sh->slot[qb][r / G];
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sh->meta_free[bb]);
+        if (lane == 0) mbar_arrive(&sh->meta_free[qb]);
         // visible key columns of this row: 0 .. lim (the causal cut only bites in the local block)
         const int lim = t < 0 ? -1 : min(kBlock - 1, t - n * kBlock);
         const uint32_t Sb = S0 + 128 * bb + lb;
-        // pass 1: row maximum over the visible keys
-        float mx = -INFINITY;
+        float l = 0.f, m2 = 0.f;
+        // tcgen05.ld / st are warp-collective (.sync.aligned): the path must be uniform per warp
+        if (__all_sync(0xffffffffu, lim == kBlock - 1)) {
+          // ---- every key of every row of this warp visible
+          float mx = -INFINITY;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t v0[32], v1[32];
-          tmem_ld32(Sb + h * 64, v0);
-          tmem_ld32(Sb + h * 64 + 32, v1);
-          tmem_wait_ld();
+          for (int h = 0; h < 2; ++h) {
+            uint32_t v0[32], v1[32];
+            tmem_ld32(Sb + h * 64, v0);
+            tmem_ld32(Sb + h * 64 + 32, v1);
+            tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            if (h * 64 + c <= lim) mx = fmaxf(mx, __uint_as_float(v0[c]));
-            if (h * 64 + 32 + c <= lim) mx = fmaxf(mx, __uint_as_float(v1[c]));
+            for (int c = 0; c < 32; ++c)
+              mx = fmaxf(mx, fmaxf(__uint_as_float(v0[c]), __uint_as_float(v1[c])));
           }
-        }
-        const float m2 = lim < 0 ? 0.f : mx * sl2;
-        // pass 2: P = 2^(S sl2 - m2) written over S as packed bf16 (column j holds keys 2j, 2j+1)
-        float l = 0.f;
+          m2 = mx * sl2;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t v0[32], v1[32];
-          tmem_ld32(Sb + h * 64, v0);
-          tmem_ld32(Sb + h * 64 + 32, v1);
-          tmem_wait_ld();
-          uint32_t pw0[16], pw1[16];
+          for (int h = 0; h < 2; ++h) {
+            uint32_t v0[32], v1[32];
+            tmem_ld32(Sb + h * 64, v0);
+            tmem_ld32(Sb + h * 64 + 32, v1);
+            tmem_wait_ld();
+            uint32_t pw0[16], pw1[16];
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const int k0 = h * 64 + 2 * c, k1 = h * 64 + 32 + 2 * c;
-            const float a0 = k0 <= lim ? ex2f(fmaf(__uint_as_float(v0[2 * c]), sl2, -m2)) : 0.f;
-            const float a1 = k0 + 1 <= lim ? ex2f(fmaf(__uint_as_float(v0[2 * c + 1]), sl2, -m2)) : 0.f;
-            const float c0 = k1 <= lim ? ex2f(fmaf(__uint_as_float(v1[2 * c]), sl2, -m2)) : 0.f;
-            const float c1 = k1 + 1 <= lim ? ex2f(fmaf(__uint_as_float(v1[2 * c + 1]), sl2, -m2)) : 0.f;
-            l += (a0 + a1) + (c0 + c1);
-            pw0[c] = pack_bf16(a0, a1);
-            pw1[c] = pack_bf16(c0, c1);
+            for (int c = 0; c < 16; ++c) {
+              const float a0 = ex2f(fmaf(__uint_as_float(v0[2 * c]), sl2, -m2));
+              const float a1 = ex2f(fmaf(__uint_as_float(v0[2 * c + 1]), sl2, -m2));
+              const float c0 = ex2f(fmaf(__uint_as_float(v1[2 * c]), sl2, -m2));
+              const float c1 = ex2f(fmaf(__uint_as_float(v1[2 * c + 1]), sl2, -m2));
+              l += (a0 + a1) + (c0 + c1);
+              pw0[c] = pack_bf16(a0, a1);
+              pw1[c] = pack_bf16(c0, c1);
+            }
+            tmem_st16(Sb + h * 32, pw0);
+            tmem_st16(Sb + h * 32 + 16, pw1);
           }
-          tmem_st16(Sb + h * 32, pw0);
-          tmem_st16(Sb + h * 32 + 16, pw1);
+        } else {
+          // ---- some row of this warp is in its local block (keys after the token masked) or is
+          // a padding row (lim = -1)
+          float mx = -INFINITY;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t v0[32], v1[32];
+            tmem_ld32(Sb + h * 64, v0);
+            tmem_ld32(Sb + h * 64 + 32, v1);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              if (h * 64 + c <= lim) mx = fmaxf(mx, __uint_as_float(v0[c]));
+              if (h * 64 + 32 + c <= lim) mx = fmaxf(mx, __uint_as_float(v1[c]));
+            }
+          }
+          m2 = lim < 0 ? 0.f : mx * sl2;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t v0[32], v1[32];
+            tmem_ld32(Sb + h * 64, v0);
+            tmem_ld32(Sb + h * 64 + 32, v1);
+            tmem_wait_ld();
+            uint32_t pw0[16], pw1[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              const int k0 = h * 64 + 2 * c, k1 = h * 64 + 32 + 2 * c;
+              const float a0 = k0 <= lim ? ex2f(fmaf(__uint_as_float(v0[2 * c]), sl2, -m2)) : 0.f;
+              const float a1 = k0 + 1 <= lim ? ex2f(fmaf(__uint_as_float(v0[2 * c + 1]), sl2, -m2)) : 0.f;
+              const float c0 = k1 <= lim ? ex2f(fmaf(__uint_as_float(v1[2 * c]), sl2, -m2)) : 0.f;
+              const float c1 = k1 + 1 <= lim ? ex2f(fmaf(__uint_as_float(v1[2 * c + 1]), sl2, -m2)) : 0.f;
+              l += (a0 + a1) + (c0 + c1);
+              pw0[c] = pack_bf16(a0, a1);
+              pw1[c] = pack_bf16(c0, c1);
+            }
+            tmem_st16(Sb + h * 32, pw0);
+            tmem_st16(Sb + h * 32 + 16, pw1);
+          }
         }
         // row results for the epilogue (its buffer is free once the epilogue of tile i-2 read it)
-        if (i >= 2 && !mbar_wait(&sh->o_free[bb], par((i - 2) >> 1), A.status)) {
+        if (i >= 2 && !mbar_wait_warp(&sh->o_free[bb], par((i - 2) >> 1), A.status)) {
           ok = false;
           break;
         }
@@ -331,8 +444,8 @@ __global__ void __launch_bounds__(384, 1)
       for (int tl = 0; tl < ntiles; ++tl, ++i) {
         const int bb = (int)(i & 1);
         __syncwarp();
-        if (!mbar_wait(&sh->o_full[bb], par(i >> 1), A.status) ||
-            !mbar_wait(&sh->p_full[bb], par(i >> 1), A.status)) {
+        if (!mbar_wait_warp(&sh->o_full[bb], par(i >> 1), A.status) ||
+            !mbar_wait_warp(&sh->p_full[bb], par(i >> 1), A.status)) {
           ok = false;
           break;
         }
@@ -401,7 +514,7 @@ __global__ void __launch_bounds__(384, 1)
 template <int G>
 static void attn_fwd_g(const CUtensorMap& mk, const CUtensorMap& mv, const FwdArgs& a,
                        cudaStream_t st) {
-  const size_t smem = sizeof(FwdShared) + 1024 + 6 * kFwdTile + 4 * kStageWarp;
+  const size_t smem = sizeof(FwdShared) + 1024 + (kRing + kQBuf) * kFwdTile + 4 * kStageWarp;
   cudaFuncSetAttribute(attn_fwd_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   attn_fwd_kernel<G><<<num_sms(), 384, smem, st>>>(mk, mv, a);
 }

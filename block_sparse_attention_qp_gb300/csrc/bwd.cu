@@ -325,7 +325,7 @@ __global__ void __launch_bounds__(256, 1)
         }
         int tn[TT];
         load_tokens((tl + 1) * TT, min(TT, item.count - (tl + 1) * TT), tn);
-        if (i >= 2 && !mbar_wait(&sh->q_empty[bb], par((i - 2) >> 1), A.status)) { ok = false; break; }
+        if (i >= 2 && !mbar_wait_warp(&sh->q_empty[bb], par((i - 2) >> 1), A.status)) { ok = false; break; }
         uint8_t* dQb = sQ + bb * kRT;
         uint8_t* ddOb = sdO + bb * kRT;
 #pragma unroll
@@ -394,7 +394,7 @@ __global__ void __launch_bounds__(256, 1)
     auto epilogue = [&](long long ti) -> bool {
       const int bb = (int)(ti & 1);
       __syncwarp();
-      if (!mbar_wait(&sh->ph2_full[bb], par(ti >> 1), A.status)) return false;
+      if (!mbar_wait_warp(&sh->ph2_full[bb], par(ti >> 1), A.status)) return false;
       fence_after_sync();
       uint32_t r0[32], r1[32];
       tmem_ld32(DB0 + 64 * bb + lb, r0);
@@ -403,7 +403,7 @@ __global__ void __launch_bounds__(256, 1)
       fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh->s_free[bb]);
-      if (ns > 0 && !mbar_wait(&sh->stage_free, par(ns - 1), A.status)) return false;
+      if (ns > 0 && !mbar_wait_warp(&sh->stage_free, par(ns - 1), A.status)) return false;
 #pragma unroll
       for (int r = 0; r < 32; ++r) {
         stage[r * kD + kr] = __uint_as_float(r0[r]) * d.scale;
@@ -428,8 +428,8 @@ __global__ void __launch_bounds__(256, 1)
       for (int tl = 0; tl < ntiles; ++tl, ++i) {
         const int bb = (int)(i & 1);
         __syncwarp();
-        if (!mbar_wait(&sh->q_full[bb], par(i >> 1), A.status) ||
-            !mbar_wait(&sh->s_full[bb], par(i >> 1), A.status)) {
+        if (!mbar_wait_warp(&sh->q_full[bb], par(i >> 1), A.status) ||
+            !mbar_wait_warp(&sh->s_full[bb], par(i >> 1), A.status)) {
           ok = false;
           break;
         }
@@ -656,8 +656,8 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2)
           lp[h2] = tv[h2] < 0 ? 0.f : A.lse_px[((size_t)b * d.Hp + g) * d.S + tv[h2]] * kLog2e;
-        if (i >= 2 && (!mbar_wait(&sh->q_empty[bb], par((i - 2) >> 1), A.status) ||
-                       !mbar_wait(&sh->meta_free[bb], par((i - 2) >> 1), A.status))) {
+        if (i >= 2 && (!mbar_wait_warp(&sh->q_empty[bb], par((i - 2) >> 1), A.status) ||
+                       !mbar_wait_warp(&sh->meta_free[bb], par((i - 2) >> 1), A.status))) {
           ok = false;
           break;
         }
@@ -700,8 +700,8 @@ __global__ void __launch_bounds__(256, 1)
         const int bb = (int)(i & 1);
         const int gcount = min(kPG, item.count - gi * kPG);
         __syncwarp();
-        if (!mbar_wait(&sh->q_full[bb], par(i >> 1), A.status) ||
-            !mbar_wait(&sh->z_full, par(i), A.status)) {
+        if (!mbar_wait_warp(&sh->q_full[bb], par(i >> 1), A.status) ||
+            !mbar_wait_warp(&sh->z_full, par(i), A.status)) {
           ok = false;
           break;
         }
@@ -736,7 +736,7 @@ __global__ void __launch_bounds__(256, 1)
         fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh->dz_full);
-        if (!mbar_wait(&sh->fl_full, par(i), A.status)) { ok = false; break; }
+        if (!mbar_wait_warp(&sh->fl_full, par(i), A.status)) { ok = false; break; }
         fence_after_sync();
         uint32_t q0[32], q1[32];
         tmem_ld32(RQ + lb, q0);

@@ -212,6 +212,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* mbar, uint32_t parity, unsig
   return false;
 }
 
+// Warp-collective form of mbar_wait for roles in which every lane waits: the result is the AND
+// over the warp, so the lanes leave (or continue) together.  Warp-collective instructions that
+// follow (tcgen05.ld / st, __syncwarp) must never run with part of a warp.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* mbar, uint32_t parity, unsigned* err) {
+  const bool ok = mbar_wait(mbar, parity, err);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // ------------------------------------------------------------------ TMA (bulk tensor copies)
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* mbar, uint32_t bytes) {
   asm volatile("{\n.reg .b64 st;\nmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n}\n" ::"r"(

@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(256, 1)
     for (int n = 0; n < qb; ++n) {
       const int a = n % kAcc;
       __syncwarp();
-      if (!mbar_wait(&sh->acc_full[a], (n / kAcc) & 1, status)) break;
+      if (!mbar_wait_warp(&sh->acc_full[a], (n / kAcc) & 1, status)) break;
       fence_after_sync();
       float mx = -INFINITY;
 #pragma unroll
