@@ -79,7 +79,7 @@ struct Plan {
   size_t dq = 0, dk = 0, dv = 0, dqp = 0, dkp = 0;
   size_t bytes = 0;
   long long max0 = 0, max1 = 0;
-  ItemSpec spec0{1, 1, 1}, spec1{1, 1, 1};
+  ItemSpec spec0{1, 1}, spec1{1, 1};
 };
 
 struct Carver {
@@ -96,7 +96,7 @@ long long dense_entries(const Dims& d) {  // sum over blocks of S - 128 n, per (
 }
 
 long long max_items(long long entries, const Dims& d, const ItemSpec& s) {
-  return (long long)s.halves * (entries / ((long long)s.tile_tokens * s.chunk_tiles) + d.nlist() + 1);
+  return entries / ((long long)s.tile_tokens * s.chunk_tiles) + d.nlist() + 1;
 }
 
 // Sequence chunk of the backward's token lists: the dQ rows one chunk contributes for one group
@@ -142,7 +142,7 @@ Plan make_plan(const Dims& d, int op) {
     p.entries = c.take(sparse_ent * sizeof(int));
   }
   if (op == MSA_OP_FORWARD) {
-    p.spec0 = ItemSpec{TT, fwd_item_tiles(), 1};
+    p.spec0 = ItemSpec{TT, fwd_item_tiles()};
     p.max0 = max_items(sparse_ent, d, p.spec0);
     p.io0 = c.take(nseg * sizeof(int));
     p.items0 = c.take(p.max0 * sizeof(Item));
@@ -152,7 +152,7 @@ Plan make_plan(const Dims& d, int op) {
   if (op == MSA_OP_BACKWARD || op == MSA_OP_WARMUP_BACKWARD) {
     const bool dense = op == MSA_OP_WARMUP_BACKWARD;
     const long long ent = dense ? dense_entries(d) : sparse_ent;
-    const ItemSpec fused{bwd_group_tokens(), bwd_item_tokens() / bwd_group_tokens(), 1};
+    const ItemSpec fused{bwd_group_tokens(), bwd_item_tokens() / bwd_group_tokens()};
     if (dense) {
       p.spec0 = fused;
       p.max0 = max_items(ent, d, p.spec0);
@@ -160,7 +160,7 @@ Plan make_plan(const Dims& d, int op) {
       p.io0 = c.take(nseg * sizeof(int));
       p.items0 = c.take(p.max0 * sizeof(Item));
     } else {
-      p.spec0 = ItemSpec{kBlock, 1, 1};  // proxy normaliser items
+      p.spec0 = ItemSpec{kBlock, 1};  // proxy normaliser items
       p.spec1 = fused;
       p.max0 = max_items(ent, d, p.spec0);
       p.max1 = max_items(ent, d, p.spec1);
@@ -225,6 +225,10 @@ int check_shape(const msa_shape_t* s, int op, Dims* out) {
     return MSA_ERR_UNSUPPORTED;
   }
   const long long rows = (long long)s->B * s->S * s->Hq;
+  if (rows >= (1ll << 31)) {  // query rows are addressed with 32-bit TMA coordinates
+    set_err("B*S*Hq must stay below 2^31");
+    return MSA_ERR_UNSUPPORTED;
+  }
   if (rows * kD * (sparse ? s->top_k : 1) >= (1ll << 62)) {
     set_err("problem too large");
     return MSA_ERR_UNSUPPORTED;
@@ -299,12 +303,13 @@ void build_lists(const Dims& d, const Plan& p, const int32_t* idx, void* ws, int
   });
   timed("invert_fill", st, [&] { launch_fill(d, idx, at<int>(ws, p.seg_offset), seg_cursor, at<int>(ws, p.entries), status, st); });
   timed("work_items", st, [&] {
-    launch_items(d, false, seg_count, p.spec0, at<int>(ws, p.io0), at<Item>(ws, p.items0), p.max0,
-                 status, st);
+    launch_items(d, false, seg_count, at<int>(ws, p.seg_offset), p.spec0, at<int>(ws, p.io0),
+                 at<Item>(ws, p.items0), p.max0, status, st);
   });
   if (nspecs > 1)
     timed("work_items", st, [&] {
-      launch_items(d, false, seg_count, p.spec1, at<int>(ws, p.io1), at<Item>(ws, p.items1),
+      launch_items(d, false, seg_count, at<int>(ws, p.seg_offset), p.spec1, at<int>(ws, p.io1),
+                   at<Item>(ws, p.items1),
                    p.max1, status, st);
     });
 }
@@ -475,7 +480,7 @@ int msa_warmup_backward(const msa_shape_t* shape, const void* q, const void* k, 
                 at<int>(workspace, p.io0), nullptr, at<int>(workspace, p.totals), st);
   });
   timed("work_items", st, [&] {
-    launch_items(d, true, nullptr, p.spec0, at<int>(workspace, p.io0),
+    launch_items(d, true, nullptr, at<int>(workspace, p.seg_offset), p.spec0, at<int>(workspace, p.io0),
                  at<Item>(workspace, p.items0), p.max0, status, st);
   });
   timed("bwd_rowdot", st, [&] { launch_bwd_rowdot(d, o, dout, at<float>(workspace, p.drow), st); });

@@ -12,8 +12,8 @@
 // Phase 2 (combine_kernel in fwd.cu) merges the <= top_k partials of every (t, h).
 //
 // Roles (384 threads): warp 0 TMA loads of K/V (a three-slot ring) and tensor-memory ownership,
-// warp 1 the MMA issuer, warps 2-3 gather the tile's Q rows (cp.async, three buffers), warps 4-7
-// softmax, warps 8-11 epilogue.  Tensor memory (512 columns): S0, S1 (S, then P in place), O0, O1.
+// warp 1 the MMA issuer, warp 2 gathers the tile's Q rows (four-row TMA gathers, three buffers),
+// warp 3 idle, warps 4-7 softmax, warps 8-11 epilogue.  Tensor memory (512 columns): S0, S1 (S, then P in place), O0, O1.
 // The MMA issuer runs S of tile i before O of tile i-1, so the tensor pipe works on one tile while
 // the softmax warps work on the next.  Every wait is bounded (see sm100::mbar_wait).
 #include <math.h>
@@ -63,11 +63,6 @@ __device__ __forceinline__ float ex2f(float x) {
   return y;
 }
 __device__ __forceinline__ uint32_t par(long long k) { return (uint32_t)(k & 1); }
-__device__ __forceinline__ void st_global_v4(void* p, uint4 v) {
-  asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
-               "r"(v.w)
-               : "memory");
-}
 // Arrive on `mbar` once every cp.async this thread issued so far has landed (counts as one of
 // the barrier's expected arrivals).
 __device__ __forceinline__ void cp_async_arrive(uint64_t* mbar) {
@@ -91,7 +86,7 @@ __device__ __forceinline__ RingPos ring_pos(long long load) {
 template <int G>
 __global__ void __launch_bounds__(384, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                    FwdArgs A) {
+                    const __grid_constant__ CUtensorMap tm_q, FwdArgs A) {
   using namespace sm100;
   constexpr int TT = kFwdRows / G;  // tokens per tile
   const Dims& d = A.d;
@@ -115,7 +110,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&sh->kv_empty[x], 1);
     }
     for (int x = 0; x < kQBuf; ++x) {
-      mbar_init(&sh->q_full[x], 128);  // 64 gather lanes: one plain and one cp.async arrival each
+      mbar_init(&sh->q_full[x], 1);  // the gather's expect-tx arrival; the bytes complete it
       mbar_init(&sh->q_empty[x], 1);
       mbar_init(&sh->meta_free[x], 4);
     }
@@ -231,35 +226,30 @@ __global__ void __launch_bounds__(384, 1)
       mma_commit(&sh->mma_done);
       mbar_wait(&sh->mma_done, 0, A.status);
     }
-  } else if (warp < 4) {
-    // ---------------------------------------------------------------- gather: Q rows
-    // Each of the two warps fills 64 rows of every tile.  The copies complete asynchronously
-    // (tracked by q_full); the warp prefetches the next tile's list entries and the next item.
-    const int w2 = warp - 2;        // rows [64 w2, 64 w2 + 64)
-    constexpr int XT = 64 / G;      // tokens per gather warp
-    const int x0 = w2 * XT;
+  } else if (warp == 2) {
+    // ---------------------------------------------------------------- gather: Q rows (TMA)
+    // Lane j fetches rows 4j .. 4j+3 of every tile with one four-row TMA gather per 64-column
+    // panel; completion is counted in bytes on q_full.  The list entries of the next tile and the
+    // next work item are loaded one step ahead.
+    const uint64_t pol_q = l2_policy_evict_last();  // each query row is read once per selected block
+    constexpr int XL = (TT + 31) / 32;               // tile tokens per lane
     long long it = blockIdx.x;
+    if (lane == 0) tma_prefetch_desc(&tm_q);
     if (it < total) {
       Item cur = A.items[it];
-      long long ceb = (long long)A.seg_offset[cur.seg] + cur.first;
       long long nit = it + gridDim.x;
-      Item nxt{};
-      long long neb = 0;
-      if (nit < total) {
-        nxt = A.items[nit];
-        neb = (long long)A.seg_offset[nxt.seg] + nxt.first;
-      }
+      Item nxt = nit < total ? A.items[nit] : cur;
       int tl = 0;
-      int e[2];
-      auto load_e = [&](long long eb, int count, int tile) {
+      int e[XL];
+      auto load_e = [&](const Item& item, int tile) {
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int xx = lane + 32 * u;
-          const int pos = tile * TT + x0 + xx;
-          e[u] = (xx < XT && pos < count) ? A.entries[eb + pos] : -1;
+        for (int u = 0; u < XL; ++u) {
+          const int x = lane + 32 * u;
+          const int pos = tile * TT + x;
+          e[u] = (x < TT && pos < item.count) ? __ldg(A.entries + item.base + pos) : -1;
         }
       };
-      load_e(ceb, cur.count, 0);
+      load_e(cur, 0);
       long long i = 0;
       while (true) {
         const int qb = (int)(i % kQBuf);
@@ -269,50 +259,52 @@ __global__ void __launch_bounds__(384, 1)
           break;
         }
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int xx = lane + 32 * u;
-          if (xx < XT) {
-            sh->tok[qb][x0 + xx] = e[u] < 0 ? -1 : (e[u] >> 8);
-            sh->slot[qb][x0 + xx] = e[u] < 0 ? 0 : (e[u] & 255);
+        for (int u = 0; u < XL; ++u) {
+          const int x = lane + 32 * u;
+          if (x < TT) {
+            sh->tok[qb][x] = e[u] < 0 ? -1 : (e[u] >> 8);
+            sh->slot[qb][x] = e[u] < 0 ? 0 : (e[u] & 255);
           }
         }
         __syncwarp();
+        if (lane == 0) mbar_expect_tx(&sh->q_full[qb], kFwdTile);  // publishes tok / slot
+        __syncwarp();
         const int bg = (int)((cur.seg % d.nseg()) / d.nblk);
         const int b = bg / d.Hp, g = bg % d.Hp;
-        uint8_t* dQb = sQ + qb * kFwdTile;
-#pragma unroll 8
-        for (int k = 0; k < 32; ++k) {
-          const int c = lane + 32 * k;
-          const int r = 64 * w2 + (c >> 4), ch = c & 15;
+        int rows[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int r = 4 * lane + u;
           const int t = sh->tok[qb][r / G];
-          const uint32_t off = (ch >> 3) * (kFwdRows * 128) + sm100::sw128_chunk(r, ch & 7);
-          const size_t grow = (((size_t)b * d.S + (t < 0 ? 0 : t)) * d.Hq + g * G + r % G) * kD + ch * 8;
-          cp_async16(dQb + off, A.q + grow, t >= 0);
+          // a padding row reads row 0 (finite data; its results are never used)
+          rows[u] = t < 0 ? 0 : (int)(((long long)b * d.S + t) * d.Hq + g * G + r % G);
         }
-        cp_async_arrive(&sh->q_full[qb]);
-        mbar_arrive(&sh->q_full[qb]);  // publishes tok / slot
+        uint8_t* dQb = sQ + qb * kFwdTile + lane * 4 * 128;
+        tma_gather4(dQb, &tm_q, 0, rows[0], rows[1], rows[2], rows[3], &sh->q_full[qb], pol_q);
+        tma_gather4(dQb + kFwdTile / 2, &tm_q, 64, rows[0], rows[1], rows[2], rows[3],
+                    &sh->q_full[qb], pol_q);
         ++i;
         // advance: next tile of this item, or the first tile of the next item
         const int ntiles = (cur.count + TT - 1) / TT;
         if (tl + 1 < ntiles) {
           ++tl;
-          load_e(ceb, cur.count, tl);
+          load_e(cur, tl);
         } else {
           it = nit;
           if (it >= total) break;
           cur = nxt;
-          ceb = neb;
           tl = 0;
-          load_e(ceb, cur.count, 0);
+          load_e(cur, 0);
           nit = it + gridDim.x;
-          if (nit < total) {
-            nxt = A.items[nit];
-            neb = (long long)A.seg_offset[nxt.seg] + nxt.first;
-          }
+          if (nit < total) nxt = A.items[nit];
         }
       }
-      cp_async_wait_all();  // nothing may land after the block exits
+      // no copy may still be landing in shared memory when the block exits
+      for (long long x = (i >= kQBuf ? i - kQBuf : 0); x < i; ++x)
+        mbar_wait_warp(&sh->q_full[x % kQBuf], par(x / kQBuf), A.status);
     }
+  } else if (warp == 3) {
+    // idle
   } else if (warp < 8) {
     // ---------------------------------------------------------------- softmax
     const int w4 = warp - 4;
@@ -344,39 +336,34 @@ __global__ void __launch_bounds__(384, 1)
         float l = 0.f, m2 = 0.f;
         // tcgen05.ld / st are warp-collective (.sync.aligned): the path must be uniform per warp
         if (__all_sync(0xffffffffu, lim == kBlock - 1)) {
-          // ---- every key of every row of this warp visible
-          float mx = -INFINITY;
+          // ---- every key of every row of this warp visible: one tensor-memory round trip
+          uint32_t v[4][32];
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint32_t v0[32], v1[32];
-            tmem_ld32(Sb + h * 64, v0);
-            tmem_ld32(Sb + h * 64 + 32, v1);
-            tmem_wait_ld();
+          for (int q = 0; q < 4; ++q) tmem_ld32(Sb + q * 32, v[q]);
+          tmem_wait_ld();
+          float mq[4];
 #pragma unroll
-            for (int c = 0; c < 32; ++c)
-              mx = fmaxf(mx, fmaxf(__uint_as_float(v0[c]), __uint_as_float(v1[c])));
+          for (int q = 0; q < 4; ++q) {
+            mq[q] = __uint_as_float(v[q][0]);
+#pragma unroll
+            for (int c = 1; c < 32; ++c) mq[q] = fmaxf(mq[q], __uint_as_float(v[q][c]));
           }
-          m2 = mx * sl2;
+          m2 = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * sl2;
+          float la = 0.f, lc = 0.f;
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint32_t v0[32], v1[32];
-            tmem_ld32(Sb + h * 64, v0);
-            tmem_ld32(Sb + h * 64 + 32, v1);
-            tmem_wait_ld();
-            uint32_t pw0[16], pw1[16];
+          for (int q = 0; q < 4; ++q) {
+            uint32_t pw[16];
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
-              const float a0 = ex2f(fmaf(__uint_as_float(v0[2 * c]), sl2, -m2));
-              const float a1 = ex2f(fmaf(__uint_as_float(v0[2 * c + 1]), sl2, -m2));
-              const float c0 = ex2f(fmaf(__uint_as_float(v1[2 * c]), sl2, -m2));
-              const float c1 = ex2f(fmaf(__uint_as_float(v1[2 * c + 1]), sl2, -m2));
-              l += (a0 + a1) + (c0 + c1);
-              pw0[c] = pack_bf16(a0, a1);
-              pw1[c] = pack_bf16(c0, c1);
+              const float a0 = ex2f(fmaf(__uint_as_float(v[q][2 * c]), sl2, -m2));
+              const float a1 = ex2f(fmaf(__uint_as_float(v[q][2 * c + 1]), sl2, -m2));
+              la += a0;
+              lc += a1;
+              pw[c] = pack_bf16(a0, a1);
             }
-            tmem_st16(Sb + h * 32, pw0);
-            tmem_st16(Sb + h * 32 + 16, pw1);
+            tmem_st16(Sb + q * 16, pw);
           }
+          l = la + lc;
         } else {
           // ---- some row of this warp is in its local block (keys after the token masked) or is
           // a padding row (lim = -1)
@@ -437,6 +424,7 @@ __global__ void __launch_bounds__(384, 1)
     const int r = w8 * 32 + lane;
     const uint32_t lb = static_cast<uint32_t>(w8 * 32) << 16;
     const uint32_t stw = aSt + w8 * kStageWarp;  // this warp's staging: [32 rows][128 bytes]
+    const uint64_t pol_part = l2_policy_evict_first();  // partials are read once, by the combine
     long long i = 0;
     for (long long it = blockIdx.x; ok && it < total; it += gridDim.x) {
       const Item item = A.items[it];
@@ -497,7 +485,7 @@ __global__ void __launch_bounds__(384, 1)
             asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];\n"
                          : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                          : "r"(stw + rr * 128 + (((c ^ rr) & 7) << 4)));
-            if (drr >= 0) st_global_v4(A.opart + drr * kD + h * 64 + c * 8, v);
+            if (drr >= 0) st_global_v4_hint(A.opart + drr * kD + h * 64 + c * 8, v, pol_part);
           }
           __syncwarp();
         }
@@ -512,11 +500,11 @@ __global__ void __launch_bounds__(384, 1)
 }
 
 template <int G>
-static void attn_fwd_g(const CUtensorMap& mk, const CUtensorMap& mv, const FwdArgs& a,
-                       cudaStream_t st) {
+static void attn_fwd_g(const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mq,
+                       const FwdArgs& a, cudaStream_t st) {
   const size_t smem = sizeof(FwdShared) + 1024 + (kRing + kQBuf) * kFwdTile + 4 * kStageWarp;
   cudaFuncSetAttribute(attn_fwd_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  attn_fwd_kernel<G><<<num_sms(), 384, smem, st>>>(mk, mv, a);
+  attn_fwd_kernel<G><<<num_sms(), 384, smem, st>>>(mk, mv, mq, a);
 }
 
 int fwd_item_tiles() { return kFwdItemTiles; }
@@ -529,7 +517,13 @@ bool launch_attn_fwd(const Dims& d, const void* q, const void* k, const void* v,
   const uint64_t kvd[3] = {128, (uint64_t)d.Hkv, (uint64_t)d.B * d.S};
   const uint64_t kvs[2] = {128 * 2, (uint64_t)d.Hkv * 128 * 2};
   const uint32_t kvb[3] = {64, 1, 128};
-  if (!make_tmap_bf16(&mk, k, 3, kvd, kvs, kvb) || !make_tmap_bf16(&mv, v, 3, kvd, kvs, kvb))
+  // query rows for the four-row gathers: [B*S*Hq rows][128], box 64 columns x 1 row
+  CUtensorMap mq;
+  const uint64_t qd[2] = {128, (uint64_t)d.B * d.S * d.Hq};
+  const uint64_t qs[1] = {128 * 2};
+  const uint32_t qbx[2] = {64, 1};
+  if (!make_tmap_bf16(&mk, k, 3, kvd, kvs, kvb) || !make_tmap_bf16(&mv, v, 3, kvd, kvs, kvb) ||
+      !make_tmap_bf16(&mq, q, 2, qd, qs, qbx))
     return false;
   FwdArgs a;
   a.d = d;
@@ -543,11 +537,11 @@ bool launch_attn_fwd(const Dims& d, const void* q, const void* k, const void* v,
   a.lpart = lpart;
   a.status = status;
   switch (d.G) {
-    case 1: attn_fwd_g<1>(mk, mv, a, st); break;
-    case 2: attn_fwd_g<2>(mk, mv, a, st); break;
-    case 4: attn_fwd_g<4>(mk, mv, a, st); break;
-    case 8: attn_fwd_g<8>(mk, mv, a, st); break;
-    case 16: attn_fwd_g<16>(mk, mv, a, st); break;
+    case 1: attn_fwd_g<1>(mk, mv, mq, a, st); break;
+    case 2: attn_fwd_g<2>(mk, mv, mq, a, st); break;
+    case 4: attn_fwd_g<4>(mk, mv, mq, a, st); break;
+    case 8: attn_fwd_g<8>(mk, mv, mq, a, st); break;
+    case 16: attn_fwd_g<16>(mk, mv, mq, a, st); break;
     default: return false;
   }
   return true;

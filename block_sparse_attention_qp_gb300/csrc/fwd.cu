@@ -92,6 +92,7 @@ __global__ void __launch_bounds__(256) combine_kernel(Dims d, const int32_t* __r
                                                       bf16* __restrict__ o, float* __restrict__ lse) {
   const long long rows = (long long)d.B * d.S * d.Hq;
   const int lane = threadIdx.x % 32, half = lane >> 4, l16 = lane & 15;
+  const uint64_t pol = l2_policy_evict_first();  // each partial is read exactly once
   for (long long r = (blockIdx.x * (long long)blockDim.x + threadIdx.x) / 32; r < rows;
        r += (long long)gridDim.x * blockDim.x / 32) {
     const int h = (int)(r % d.Hq);
@@ -125,7 +126,7 @@ __global__ void __launch_bounds__(256) combine_kernel(Dims d, const int32_t* __r
       const float c = __shfl_sync(0xffffffffu, w1, s & 31);
       const float w = s < 32 ? a : c;
       if (s < d.top_k && w > 0.f) {
-        const uint4 pv = *reinterpret_cast<const uint4*>(opart + (base + s) * kD + l16 * 8);
+        const uint4 pv = ld_global_nc_v4_hint(opart + (base + s) * kD + l16 * 8, pol);
         const uint32_t pw[4] = {pv.x, pv.y, pv.z, pv.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {

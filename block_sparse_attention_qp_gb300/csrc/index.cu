@@ -89,7 +89,7 @@ __device__ __forceinline__ long long list_len(const Dims& d, bool dense, const i
 
 __device__ __forceinline__ long long items_of(long long c, const ItemSpec& s) {
   const long long tiles = (c + s.tile_tokens - 1) / s.tile_tokens;
-  return (tiles + s.chunk_tiles - 1) / s.chunk_tiles * s.halves;
+  return (tiles + s.chunk_tiles - 1) / s.chunk_tiles;
 }
 
 // Single-CTA exclusive scan over every list of three running sums: list lengths and the item
@@ -145,7 +145,8 @@ __global__ void __launch_bounds__(1024) scan_kernel(Dims d, int dense, const int
   }
 }
 
-__global__ void items_kernel(Dims d, int dense, const int* __restrict__ seg_count, ItemSpec sp,
+__global__ void items_kernel(Dims d, int dense, const int* __restrict__ seg_count,
+                             const int* __restrict__ seg_offset, ItemSpec sp,
                              const int* __restrict__ item_offset, Item* __restrict__ items,
                              long long max_items, unsigned* status) {
   const long long seg = blockIdx.x;
@@ -153,17 +154,16 @@ __global__ void items_kernel(Dims d, int dense, const int* __restrict__ seg_coun
   const int per_item = sp.tile_tokens * sp.chunk_tiles;
   const long long n_chunks = (len + per_item - 1) / per_item;
   const long long base = item_offset[seg];
-  for (long long i = threadIdx.x; i < n_chunks * sp.halves; i += blockDim.x) {
-    const long long chunk = i / sp.halves;
-    const int half = (int)(i % sp.halves);
+  const long long list0 = seg_offset ? seg_offset[seg] : 0;
+  for (long long i = threadIdx.x; i < n_chunks; i += blockDim.x) {
     const long long pos = base + i;
     if (pos >= max_items) {
       atomicOr(status, kStatusBadItems);
       continue;
     }
-    const long long first = chunk * per_item;
+    const long long first = i * per_item;
     const long long cnt = len - first < per_item ? len - first : per_item;
-    items[pos] = Item{(int)seg, (int)first, (int)cnt, half};
+    items[pos] = Item{(int)seg, (int)first, (int)cnt, (int)(list0 + first)};
   }
 }
 
@@ -202,8 +202,8 @@ void launch_count(const Dims& d, const int32_t* idx, int* seg_count, unsigned* s
 void launch_scan(const Dims& d, bool dense, const int* seg_count, int* seg_offset,
                  const ItemSpec* specs, int nspecs, int* item_offset0, int* item_offset1,
                  int* totals, cudaStream_t st) {
-  ItemSpec s0 = nspecs > 0 ? specs[0] : ItemSpec{1, 1, 1};
-  ItemSpec s1 = nspecs > 1 ? specs[1] : ItemSpec{1, 1, 1};
+  ItemSpec s0 = nspecs > 0 ? specs[0] : ItemSpec{1, 1};
+  ItemSpec s1 = nspecs > 1 ? specs[1] : ItemSpec{1, 1};
   scan_kernel<<<1, 1024, 0, st>>>(d, dense ? 1 : 0, seg_count, seg_offset, s0, s1, nspecs,
                                   item_offset0, item_offset1, totals);
 }
@@ -215,10 +215,10 @@ void launch_fill(const Dims& d, const int32_t* idx, const int* seg_offset, int* 
   fill_kernel<<<grid_for(rows, 256), 256, 0, st>>>(d, idx, seg_offset, seg_cursor, entries);
 }
 
-void launch_items(const Dims& d, bool dense, const int* seg_count, const ItemSpec& spec,
-                  const int* item_offset, Item* items, long long max_items, unsigned* status,
-                  cudaStream_t st) {
-  items_kernel<<<(unsigned)d.nlist(), 128, 0, st>>>(d, dense ? 1 : 0, seg_count, spec,
+void launch_items(const Dims& d, bool dense, const int* seg_count, const int* seg_offset,
+                  const ItemSpec& spec, const int* item_offset, Item* items, long long max_items,
+                  unsigned* status, cudaStream_t st) {
+  items_kernel<<<(unsigned)d.nlist(), 128, 0, st>>>(d, dense ? 1 : 0, seg_count, seg_offset, spec,
                                                     item_offset, items, max_items, status);
 }
 

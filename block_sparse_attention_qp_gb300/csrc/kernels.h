@@ -16,15 +16,15 @@ struct Dims {
 };
 
 // A unit of attention work: `count` tokens of list `seg` (= c * nseg + (b * Hp + g) * nblk + n)
-// starting at list position `first`, on key-half `half` (0/1; 0 for most kernels).
+// starting at list position `first`; `base` = the list's offset + first, i.e. the position of
+// the item's first entry in the packed entry array.
 struct Item {
-  int seg, first, count, half;
+  int seg, first, count, base;
 };
 
-// Shape of one work list: tiles of `tile_tokens` tokens, `chunk_tiles` tiles per item,
-// `halves` copies of every item (one per 64-key half of the block).
+// Shape of one work list: tiles of `tile_tokens` tokens, `chunk_tiles` tiles per item.
 struct ItemSpec {
-  int tile_tokens, chunk_tiles, halves;
+  int tile_tokens, chunk_tiles;
 };
 
 // ---------------------------------------------------------------- index kernels (index.cu)
@@ -39,9 +39,9 @@ void launch_scan(const Dims& d, bool dense, const int* seg_count, int* seg_offse
 // Scatter (t << 8 | slot) into the lists; order inside a list is unspecified.
 void launch_fill(const Dims& d, const int32_t* idx, const int* seg_offset, int* seg_cursor,
                  int* entries, unsigned* status, cudaStream_t st);
-void launch_items(const Dims& d, bool dense, const int* seg_count, const ItemSpec& spec,
-                  const int* item_offset, Item* items, long long max_items, unsigned* status,
-                  cudaStream_t st);
+void launch_items(const Dims& d, bool dense, const int* seg_count, const int* seg_offset,
+                  const ItemSpec& spec, const int* item_offset, Item* items, long long max_items,
+                  unsigned* status, cudaStream_t st);
 
 // ---------------------------------------------------------------- proxy top-k (topk.cu)
 // Returns false if the TMA tensor maps could not be created (driver entry point missing).

@@ -247,6 +247,19 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int c0,
       "r"(static_cast<uint32_t>(__cvta_generic_to_shared(mbar)))
       : "memory");
 }
+// Row gather: four rows r0..r3 (any order, any distance) of a 2D tensor whose map has a box
+// of 64 columns x 1 row; the rows land one after the other at dst (4 x 128 bytes, swizzled like
+// rows of a tile at that shared-memory address).  c0 is the column (0 or 64).
+__device__ __forceinline__ void tma_gather4(void* dst, const void* tmap, int c0, int r0, int r1,
+                                            int r2, int r3, uint64_t* mbar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;\n" ::"r"(
+          static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+      "l"(tmap), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+      "r"(static_cast<uint32_t>(__cvta_generic_to_shared(mbar))), "l"(policy)
+      : "memory");
+}
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];\n" ::"l"(tmap) : "memory");
 }
