@@ -11,9 +11,9 @@
 //   partial (t, h, slot) = O / l in bf16, and its log-sum-exp m + log l   (epilogue warps)
 // Phase 2 (combine_kernel in fwd.cu) merges the <= top_k partials of every (t, h).
 //
-// Roles (576 threads): warp 0 TMA loads of K/V (a three-slot ring) and tensor-memory ownership,
+// Roles (448 threads): warp 0 TMA loads of K/V (a three-slot ring) and tensor-memory ownership,
 // warp 1 the MMA issuer, warps 2, 3, 12, 13 gather the tile's Q rows (cp.async, three buffers),
-// warps 4-7 and 14-17 softmax (two groups, alternate tiles), warps 8-11 epilogue.  (TMA issues about one request per 70 cycles per SM,
+// warps 4-7 and 8-11 two softmax + epilogue groups that take alternate tiles.  (TMA issues about one request per 70 cycles per SM,
 // so 1 KB row boxes cannot feed a 128-row tile in time; four cp.async warps can.)  Tensor memory (512 columns): S0, S1 (S, then P in place), O0, O1.
 // The MMA issuer runs S of tile i before O of tile i-1, so the tensor pipe works on one tile while
 // the softmax warps work on the next.  Every wait is bounded (see sm100::mbar_wait).
@@ -32,7 +32,7 @@ constexpr int kFwdTile = kFwdRows * 128 * 2;   // one 128-row x 128 bf16 tile (t
 constexpr int kFwdItemTiles = 8;               // tiles per work item
 constexpr int kRing = 3;                       // K/V ring slots (one 128 x 128 tile each)
 constexpr int kQBuf = 3;                       // gathered Q buffers
-constexpr int kStageWarp = 32 * 128;           // epilogue staging per warp: 32 rows x 128 bytes
+constexpr int kStageWarp = 32 * 64;            // epilogue staging per warp: 32 rows x 64 bytes
 
 struct FwdArgs {
   Dims d;
@@ -50,9 +50,6 @@ struct FwdArgs {
 struct FwdShared {
   int tok[kQBuf][kFwdRows];     // token of each tile token (-1: none), per Q buffer
   int slot[kQBuf][kFwdRows];    // its selection slot
-  long long dst[2][kFwdRows];   // partial row (t, h, slot) of each tile row (-1: none), per O buffer
-  float inv_l[2][kFwdRows];     // 1 / l of each row
-  float lse[2][kFwdRows];       // natural log-sum-exp of each row's partial
   uint64_t kv_full[kRing], kv_empty[kRing], q_full[kQBuf], q_empty[kQBuf], meta_free[kQBuf],
       s_full[2], p_full[2], o_full[2], o_free[2], mma_done;
   uint32_t tmem;
@@ -85,7 +82,7 @@ __device__ __forceinline__ RingPos ring_pos(long long load) {
 }  // namespace
 
 template <int G>
-__global__ void __launch_bounds__(576, 1)
+__global__ void __launch_bounds__(448, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     FwdArgs A) {
   using namespace sm100;
@@ -97,7 +94,7 @@ __global__ void __launch_bounds__(576, 1)
   uint8_t* base = align1024(smem_raw + sizeof(FwdShared));
   uint8_t* sR = base;                     // K/V ring: [kRing][128 keys][128 d]   (TMA)
   uint8_t* sQ = sR + kRing * kFwdTile;    // [kQBuf][128 rows][128 d]          (gathered)
-  uint8_t* sSt = sQ + kQBuf * kFwdTile;   // epilogue staging, [4 warps][32 rows][128 bytes]
+  uint8_t* sSt = sQ + kQBuf * kFwdTile;   // epilogue staging, [8 warps][32 rows][64 bytes]
   const uint32_t aR = smem_u32(sR), aQ = smem_u32(sQ), aSt = smem_u32(sSt);
 
   const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
@@ -176,26 +173,24 @@ __global__ void __launch_bounds__(576, 1)
     // (the whole warp runs the loop and waits; lane 0 issues the MMAs and commits)
     constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);  // S = Q K^T
     constexpr uint32_t id_o = idesc_bf16(128, 128, false, true);   // O = P V
-    struct Pending {
-      long long ti;
-      RingPos v;
-      bool first, last;
-    };
-    Pending pd{};
-    bool pending = false;
-    auto mma_o = [&](const Pending& p) -> bool {
-      const int b = (int)(p.ti & 1);
-      if (!mbar_wait_warp(&sh->p_full[b], par(p.ti >> 1), A.status)) return false;
-      if (p.first && !mbar_wait_warp(&sh->kv_full[p.v.slot], p.v.parity, A.status)) return false;
-      if (p.ti >= 2 && !mbar_wait_warp(&sh->o_free[b], par((p.ti - 2) >> 1), A.status)) return false;
+    // the O product of the previous tile, issued after the next tile's S product
+    long long p_ti = -1;  // < 0: none pending
+    int p_vslot = 0;
+    uint32_t p_vpar = 0;
+    bool p_first = false, p_last = false;
+    auto mma_o = [=](long long ti, int vslot, uint32_t vpar, bool first, bool last) -> bool {
+      const int b = (int)(ti & 1);
+      if (!mbar_wait_warp(&sh->p_full[b], par(ti >> 1), A.status)) return false;
+      if (first && !mbar_wait_warp(&sh->kv_full[vslot], vpar, A.status)) return false;
+      if (ti >= 2 && !mbar_wait_warp(&sh->o_free[b], par((ti - 2) >> 1), A.status)) return false;
       fence_after_sync();
       if (lane == 0) {
-        const uint32_t aV = aR + p.v.slot * kFwdTile;
+        const uint32_t aV = aR + vslot * kFwdTile;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
           mma_ts(O0 + 128 * b, S0 + 128 * b + ks * 8, desc_mnmajor(aV, 128, ks), id_o, ks > 0);
         mma_commit(&sh->o_full[b]);
-        if (p.last) mma_commit(&sh->kv_empty[p.v.slot]);
+        if (last) mma_commit(&sh->kv_empty[vslot]);
       }
       __syncwarp();
       return true;
@@ -231,12 +226,15 @@ __global__ void __launch_bounds__(576, 1)
           if (tl == ntiles - 1) mma_commit(&sh->kv_empty[kp.slot]);
         }
         __syncwarp();
-        if (pending && !mma_o(pd)) { ok = false; break; }
-        pending = true;
-        pd = Pending{i, vp, tl == 0, tl == ntiles - 1};
+        if (p_ti >= 0 && !mma_o(p_ti, p_vslot, p_vpar, p_first, p_last)) { ok = false; break; }
+        p_ti = i;
+        p_vslot = vp.slot;
+        p_vpar = vp.parity;
+        p_first = tl == 0;
+        p_last = tl == ntiles - 1;
       }
     }
-    if (ok && pending) mma_o(pd);
+    if (ok && p_ti >= 0) mma_o(p_ti, p_vslot, p_vpar, p_first, p_last);
     if (lane == 0) mma_commit(&sh->mma_done);
     __syncwarp();
     mbar_wait_warp(&sh->mma_done, 0, A.status);
@@ -254,12 +252,11 @@ __global__ void __launch_bounds__(576, 1)
       long long nit = it + gridDim.x;
       Item nxt = nit < total ? A.items[nit] : cur;
       int tl = 0;
-      int e = -1;
-      auto load_e = [&](const Item& item, int tile) {
+      auto load_e = [=](int base, int count, int tile) -> int {
         const int pos = tile * TT + x0 + lane;
-        e = (lane < XT && (G < 64 || gw == 0) && pos < item.count) ? __ldg(A.entries + item.base + pos) : -1;
+        return (lane < XT && pos < count) ? __ldg(A.entries + base + pos) : -1;
       };
-      load_e(cur, 0);
+      int e = load_e(cur.base, cur.count, 0);
       long long i = 0;
       while (true) {
         const int qb = (int)(i % kQBuf);
@@ -293,27 +290,30 @@ __global__ void __launch_bounds__(576, 1)
         const int ntiles = (cur.count + TT - 1) / TT;
         if (tl + 1 < ntiles) {
           ++tl;
-          load_e(cur, tl);
+          e = load_e(cur.base, cur.count, tl);
         } else {
           it = nit;
           if (it >= total) break;
           cur = nxt;
           tl = 0;
-          load_e(cur, 0);
+          e = load_e(cur.base, cur.count, 0);
           nit = it + gridDim.x;
           if (nit < total) nxt = A.items[nit];
         }
       }
       cp_async_wait_all();  // nothing may land after the block exits
     }
-  } else if (warp < 8 || warp >= 14) {
-    // ---------------------------------------------------------------- softmax
-    // Two warpgroups take alternate tiles (group sg owns S buffer sg), so one group's tensor-memory
-    // round trips and barrier waits overlap the other's arithmetic.
-    const int sg = warp >= 14 ? 1 : 0;
+  } else {
+    // ---------------------------------------------------------------- softmax + epilogue
+    // Warps 4-7 and 8-11 form two groups that take alternate tiles (group sg owns S and O buffer
+    // sg): per tile the group writes P over S, and once O = P V has landed it writes the tile's
+    // partials, while the other group works on the next tile.
+    const int sg = (warp - 4) >> 2;
     const int w4 = warp % 4;       // tensor-memory lane quadrant of this warp
     const int r = w4 * 32 + lane;  // tile row = tensor-memory lane
     const uint32_t lb = static_cast<uint32_t>(w4 * 32) << 16;
+    const uint32_t stw = aSt + (warp - 4) * kStageWarp;  // this warp's staging: [32 rows][64 bytes]
+    const uint64_t pol_part = l2_policy_evict_first();    // partials are read once, by the combine
     long long i = 0;
     for (long long it = blockIdx.x; ok && it < total; it += gridDim.x) {
       const Item item = A.items[it];
@@ -344,18 +344,16 @@ __global__ void __launch_bounds__(576, 1)
           // ---- every key of every row of this warp visible
           float mx = -INFINITY;
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint32_t v0[32], v1[32];
-            tmem_ld32(Sb + h * 64, v0);
-            tmem_ld32(Sb + h * 64 + 32, v1);
+          for (int q = 0; q < 4; ++q) {
+            uint32_t v0[32];
+            tmem_ld32(Sb + q * 32, v0);
             tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < 32; ++c)
-              mx = fmaxf(mx, fmaxf(__uint_as_float(v0[c]), __uint_as_float(v1[c])));
+            for (int c = 0; c < 32; ++c) mx = fmaxf(mx, __uint_as_float(v0[c]));
           }
           m2 = mx * sl2;
           float la = 0.f, lc = 0.f;
-#pragma unroll
+#pragma unroll 1  // (a full unroll makes the compiler spill)
           for (int q = 0; q < 4; ++q) {
             uint32_t v0[32];
             tmem_ld32(Sb + q * 32, v0);
@@ -386,7 +384,7 @@ __global__ void __launch_bounds__(576, 1)
               mx = fmaxf(mx, q * 32 + c <= lim ? __uint_as_float(v0[c]) : -INFINITY);
           }
           m2 = lim < 0 ? 0.f : mx * sl2;
-#pragma unroll
+#pragma unroll 1  // (a full unroll makes the compiler spill)
           for (int q = 0; q < 4; ++q) {
             uint32_t v0[32];
             tmem_ld32(Sb + q * 32, v0);
@@ -406,85 +404,56 @@ __global__ void __launch_bounds__(576, 1)
             tmem_st16(Sb + q * 16, pw);
           }
         }
-        // row results for the epilogue (its buffer is free once the epilogue of tile i-2 read it)
-        if (i >= 2 && !mbar_wait_warp(&sh->o_free[bb], par((i - 2) >> 1), A.status)) {
-          ok = false;
-          break;
-        }
         const bool valid = t >= 0;
-        sh->dst[bb][r] = valid ? (((long long)b * d.S + t) * d.Hq + g * G + r % G) * d.top_k + slot : -1;
-        sh->inv_l[bb][r] = valid ? __fdividef(1.f, l) : 0.f;
-        sh->lse[bb][r] = valid ? (m2 + __log2f(l)) * kLn2 : 0.f;
+        const long long dst = valid ? (((long long)b * d.S + t) * d.Hq + g * G + r % G) * d.top_k + slot : -1;
+        const float sc = valid ? __fdividef(1.f, l) : 0.f;
+        const float lse = valid ? (m2 + __log2f(l)) * kLn2 : 0.f;
         tmem_wait_st();
         fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh->p_full[bb]);
-      }
-    }
-  } else {
-    // ---------------------------------------------------------------- epilogue
-    const int w8 = warp - 8;
-    const int r = w8 * 32 + lane;
-    const uint32_t lb = static_cast<uint32_t>(w8 * 32) << 16;
-    const uint32_t stw = aSt + w8 * kStageWarp;  // this warp's staging: [32 rows][128 bytes]
-    const uint64_t pol_part = l2_policy_evict_first();  // partials are read once, by the combine
-    long long i = 0;
-    for (long long it = blockIdx.x; ok && it < total; it += gridDim.x) {
-      const Item item = A.items[it];
-      const int ntiles = (item.count + TT - 1) / TT;
-      for (int tl = 0; tl < ntiles; ++tl, ++i) {
-        const int bb = (int)(i & 1);
-        __syncwarp();
-        if (!mbar_wait_warp(&sh->o_full[bb], par(i >> 1), A.status) ||
-            !mbar_wait_warp(&sh->p_full[bb], par(i >> 1), A.status)) {
+        // ---- epilogue of this tile: O / l -> bf16 partials, 32 columns at a time through the
+        // warp's staging rows (16-byte chunks rotated by row pair: conflict-free both ways),
+        // leaving as 8 rows x 64 contiguous bytes per store instruction
+        if (!mbar_wait_warp(&sh->o_full[bb], par(i >> 1), A.status)) {
           ok = false;
           break;
         }
         fence_after_sync();
-        const long long dst = sh->dst[bb][r];
-        const float sc = sh->inv_l[bb][r];
-        const float lse = sh->lse[bb][r];
         const uint32_t Ob = O0 + 128 * bb + lb;
-#pragma unroll
+#pragma unroll 1
         for (int q = 0; q < 4; ++q) {
           uint32_t v0[32];
           tmem_ld32(Ob + q * 32, v0);
           tmem_wait_ld();
-          if (q == 3) {
+          if (q == 3) {  // O_b may now be overwritten by the O product of tile i+2
             fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh->o_free[bb]);
           }
-          // 32 columns of this row -> 64 bytes of bf16 in the warp's staging row (16-byte chunks
-          // XOR-swizzled by row); each half row (64 columns) then leaves as 4 rows x 128
-          // contiguous bytes per store instruction
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const uint32_t w0 = pack_bf16(__uint_as_float(v0[8 * u + 0]) * sc, __uint_as_float(v0[8 * u + 1]) * sc);
             const uint32_t w1 = pack_bf16(__uint_as_float(v0[8 * u + 2]) * sc, __uint_as_float(v0[8 * u + 3]) * sc);
             const uint32_t w2 = pack_bf16(__uint_as_float(v0[8 * u + 4]) * sc, __uint_as_float(v0[8 * u + 5]) * sc);
             const uint32_t w3 = pack_bf16(__uint_as_float(v0[8 * u + 6]) * sc, __uint_as_float(v0[8 * u + 7]) * sc);
-            const int ch = (q & 1) * 4 + u;  // 16-byte chunk of the 128-byte half row
-            const uint32_t a0 = stw + lane * 128 + (((ch ^ lane) & 7) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(a0), "r"(w0), "r"(w1),
+            const uint32_t a = stw + lane * 64 + (((u + (lane >> 1)) & 3) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(a), "r"(w0), "r"(w1),
                          "r"(w2), "r"(w3)
                          : "memory");
           }
-          if (q & 1) {
-            const int h = q >> 1;
-            __syncwarp();
+          __syncwarp();
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              const int rr = u * 4 + lane / 8, c = lane % 8;
-              const long long drr = __shfl_sync(0xffffffffu, dst, rr);
-              uint4 v;
-              asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];\n"
-                           : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                           : "r"(stw + rr * 128 + (((c ^ rr) & 7) << 4)));
-              if (drr >= 0) st_global_v4_hint(A.opart + drr * kD + h * 64 + c * 8, v, pol_part);
-            }
-            __syncwarp();
+          for (int j = 0; j < 4; ++j) {
+            const int rr = j * 8 + lane / 4, c = lane % 4;
+            const long long drr = __shfl_sync(0xffffffffu, dst, rr);
+            uint4 v;
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];\n"
+                         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                         : "r"(stw + rr * 64 + (((c + (rr >> 1)) & 3) << 4)));
+            if (drr >= 0) st_global_v4_hint(A.opart + drr * kD + q * 32 + c * 8, v, pol_part);
           }
+          __syncwarp();
         }
         if (dst >= 0) A.lpart[dst] = lse;
       }
@@ -499,9 +468,9 @@ __global__ void __launch_bounds__(576, 1)
 template <int G>
 static void attn_fwd_g(const CUtensorMap& mk, const CUtensorMap& mv, const FwdArgs& a,
                        cudaStream_t st) {
-  const size_t smem = sizeof(FwdShared) + 1024 + (kRing + kQBuf) * kFwdTile + 4 * kStageWarp;
+  const size_t smem = sizeof(FwdShared) + 1024 + (kRing + kQBuf) * kFwdTile + 8 * kStageWarp;
   cudaFuncSetAttribute(attn_fwd_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  attn_fwd_kernel<G><<<num_sms(), 576, smem, st>>>(mk, mv, a);
+  attn_fwd_kernel<G><<<num_sms(), 448, smem, st>>>(mk, mv, a);
 }
 
 int fwd_item_tiles() { return kFwdItemTiles; }
