@@ -61,12 +61,6 @@ __device__ __forceinline__ float ex2f(float x) {
   return y;
 }
 __device__ __forceinline__ uint32_t par(long long k) { return (uint32_t)(k & 1); }
-// Arrive on `mbar` once every cp.async this thread issued so far has landed (counts as one of
-// the barrier's expected arrivals).
-__device__ __forceinline__ void cp_async_arrive(uint64_t* mbar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_u32(mbar))
-               : "memory");
-}
 
 // The K/V ring: loads alternate K, V, K, V, ... (load L = 2 * item + {0: K, 1: V}) over kRing
 // slots, so the next item's V can land as soon as the current item's K is no longer needed.

@@ -559,7 +559,8 @@ __global__ void __launch_bounds__(256, 1)
     mbar_init(&sh->kp_full, 1);
     mbar_init(&sh->kp_empty, 1);
     for (int x = 0; x < 2; ++x) {
-      mbar_init(&sh->q_full[x], 32);
+      mbar_init(&sh->q_full[x], 128);  // 2 gather warps x 32 lanes: a plain (or expect-tx) and a
+                                       // cp.async arrival each
       mbar_init(&sh->q_empty[x], 1);
       mbar_init(&sh->meta_free[x], 4);
     }
@@ -611,6 +612,8 @@ __global__ void __launch_bounds__(256, 1)
           const int gcount = min(kPG, item.count - gi * kPG);
           if (!mbar_wait(&sh->q_full[b], par(i >> 1), A.status)) { ok = false; break; }
           if (i > 0 && !mbar_wait(&sh->fl_free, par(i - 1), A.status)) { ok = false; break; }
+          // Qp rows came from other threads' cp.async (generic proxy), tracked by q_full
+          fence_async_smem();
           fence_after_sync();
           const uint32_t aQb = aQp + b * kRT;
 #pragma unroll
@@ -633,56 +636,86 @@ __global__ void __launch_bounds__(256, 1)
         mma_commit(&sh->kp_empty);
       }
     }
-  } else if (warp == 2) {
-    long long i = 0;
-    for (long long it = blockIdx.x; ok && it < total; it += gridDim.x) {
-      const Item item = A.items[it];
-      const int bg = (int)((item.seg % d.nseg()) / d.nblk);
-      const int b = bg / d.Hp, g = bg % d.Hp;
-      const long long tb = item_base<kDense>(d, A.seg_offset, item);
-      const long long eb = (long long)A.seg_offset[item.seg] + item.first;
-      const int ngroups = (item.count + kPG - 1) / kPG;
-      for (int gi = 0; gi < ngroups; ++gi, ++i) {
+  } else if (warp == 2 || warp == 3) {
+    // ---- gather: warp 2 + w fetches proxy query rows 32 w .. 32 w + 31 of each group with
+    // cp.async; lane 0 of warp 2 also copies the group's teacher rows, which are contiguous
+    // (consecutive list entries), with one bulk copy.  Completion is counted on q_full; the next
+    // group's tokens and proxy normalisers are loaded one step ahead.
+    const int w = warp - 2;
+    long long it = blockIdx.x;
+    if (it < total) {
+      Item cur = A.items[it];
+      long long nit = it + gridDim.x;
+      Item nxt = nit < total ? A.items[nit] : cur;
+      int gi = 0;
+      // token and proxy log-normaliser (x log2 e) of group row 32 w + lane of group `grp`
+      auto load_row = [=](const Item& item, int grp, float& lp) -> int {
+        const int bg = (int)((item.seg % d.nseg()) / d.nblk);
+        const int b = bg / d.Hp, g = bg % d.Hp;
+        const int x = 32 * w + lane;
+        const int pos = grp * kPG + x;
+        int t = -1;
+        if (pos < item.count)
+          t = kDense ? (int)(item_base<true>(d, nullptr, item) + pos) : (__ldg(A.entries + item.base + pos) >> 8);
+        lp = t < 0 ? 0.f : __ldg(A.lse_px + ((size_t)b * d.Hp + g) * d.S + t) * kLog2e;
+        return t;
+      };
+      float lp_next;
+      int t_next = load_row(cur, 0, lp_next);
+      long long i = 0;
+      while (true) {
         const int bb = (int)(i & 1);
-        const int gcount = min(kPG, item.count - gi * kPG);
-        int tv[2];
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          const int x = lane + 32 * h2;
-          const long long pos = (long long)gi * kPG + x;
-          tv[h2] = x < gcount ? (kDense ? (int)(tb + pos) : (A.entries[tb + pos] >> 8)) : -1;
-        }
-        float lp[2];
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2)
-          lp[h2] = tv[h2] < 0 ? 0.f : A.lse_px[((size_t)b * d.Hp + g) * d.S + tv[h2]] * kLog2e;
+        const int gcount = min(kPG, cur.count - gi * kPG);
         if (i >= 2 && (!mbar_wait_warp(&sh->q_empty[bb], par((i - 2) >> 1), A.status) ||
                        !mbar_wait_warp(&sh->meta_free[bb], par((i - 2) >> 1), A.status))) {
           ok = false;
           break;
         }
+        const int bg = (int)((cur.seg % d.nseg()) / d.nblk);
+        const int b = bg / d.Hp, g = bg % d.Hp;
+        sh->tok[bb][32 * w + lane] = t_next;
+        sh->lpx2[bb][32 * w + lane] = lp_next;
+        __syncwarp();
+        if (w == 0) {
+          if (lane == 0) {  // teacher rows: gcount entries x 128 keys, one bulk copy
+            const uint32_t bytes = (uint32_t)gcount * kBlock * 4;
+            mbar_expect_tx(&sh->q_full[bb], bytes);  // also this lane's plain arrival
+            bulk_load(sPb + bb * kPG * kBlock, A.pbar + (size_t)(cur.base + gi * kPG) * kBlock, bytes,
+                      &sh->q_full[bb]);
+          }
+        }
         // proxy query rows (K-major SW128), rows >= gcount zero-filled
         uint8_t* dQb = sQp + bb * kRT;
-        for (int c = lane; c < kPG * 16; c += 32) {
-          const int r = c >> 4, ch = c & 15;
-          const int t = __shfl_sync(0xffffffffu, tv[r >= 32 ? 1 : 0], r & 31);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const int c = lane + 32 * k;  // 16-byte chunk of this warp's 32 rows
+          const int r = 32 * w + (c >> 4), ch = c & 15;
+          const int t = sh->tok[bb][r];
           const uint32_t off = (ch >> 3) * (kPG * 128) + sm100::sw128_chunk(r, ch & 7);
           const size_t grow = (((size_t)b * d.S + (t < 0 ? 0 : t)) * d.Hp + g) * kD + ch * 8;
           cp_async16(dQb + off, A.qp + grow, t >= 0);
         }
-        // teacher rows: gcount entries x 128 keys, contiguous in the pbar buffer
-        float* dPb = sPb + bb * kPG * kBlock;
-        const float* src = A.pbar + (size_t)(eb + gi * kPG) * kBlock;
-        for (int c = lane; c < gcount * 32; c += 32) cp_async16(dPb + c * 4, src + c * 4);
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          sh->tok[bb][lane + 32 * h2] = tv[h2];
-          sh->lpx2[bb][lane + 32 * h2] = lp[h2];
+        cp_async_arrive(&sh->q_full[bb]);
+        if (!(w == 0 && lane == 0)) mbar_arrive(&sh->q_full[bb]);  // publishes tok / lpx2
+        ++i;
+        const int ngroups = (cur.count + kPG - 1) / kPG;
+        if (gi + 1 < ngroups) {
+          ++gi;
+          t_next = load_row(cur, gi, lp_next);
+        } else {
+          it = nit;
+          if (it >= total) break;
+          cur = nxt;
+          gi = 0;
+          t_next = load_row(cur, 0, lp_next);
+          nit = it + gridDim.x;
+          if (nit < total) nxt = A.items[nit];
         }
-        cp_async_wait_all();
-        fence_async_smem();
-        mbar_arrive(&sh->q_full[bb]);
       }
+      cp_async_wait_all();  // nothing may land after the block exits
+      // the last bulk copies land before the block exits
+      for (long long x = (i >= 2 ? i - 2 : 0); x < i; ++x)
+        mbar_wait_warp(&sh->q_full[x & 1], par(x >> 1), A.status);
     }
   } else if (warp >= 4) {
     const int w4 = warp - 4;

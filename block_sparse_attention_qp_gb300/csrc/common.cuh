@@ -73,6 +73,12 @@ __device__ __forceinline__ uint4 ld_global_nc_v4_hint(const void* p, uint64_t po
                : "l"(p), "l"(pol));
   return v;
 }
+// Arrive on the mbarrier at `mbar` once every cp.async this thread issued so far has landed
+// (counts as one of the barrier's expected arrivals).
+__device__ __forceinline__ void cp_async_arrive(uint64_t* mbar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_u32(mbar))
+               : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 template <int N>

@@ -260,6 +260,15 @@ __device__ __forceinline__ void tma_gather4(void* dst, const void* tmap, int c0,
       "r"(static_cast<uint32_t>(__cvta_generic_to_shared(mbar))), "l"(policy)
       : "memory");
 }
+// Plain (untiled) bulk copy global -> shared of `bytes` bytes (both addresses 16-byte aligned,
+// size a multiple of 16), completion reported to `mbar` as transaction bytes.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* mbar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+          static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+      "l"(src), "r"(bytes), "r"(static_cast<uint32_t>(__cvta_generic_to_shared(mbar)))
+      : "memory");
+}
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];\n" ::"l"(tmap) : "memory");
 }
