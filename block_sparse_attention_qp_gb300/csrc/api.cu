@@ -373,6 +373,8 @@ int msa_forward(const msa_shape_t* shape, const void* q, const void* k, const vo
     }
   }
   build_lists(d, p, block_idx, workspace, 1, st);
+  // partial log-sum-exps of slots no list entry reaches stay NaN (all-ones bytes)
+  cudaMemsetAsync(at<float>(workspace, p.lpart), 0xff, (size_t)d.B * d.S * d.Hq * d.top_k * sizeof(float), st);
   bool fok = true;
   timed("attn_fwd", st, [&] {
     fok = launch_attn_fwd(d, q, k, v, at<int>(workspace, p.seg_offset),
@@ -385,8 +387,7 @@ int msa_forward(const msa_shape_t* shape, const void* q, const void* k, const vo
     return MSA_ERR_CUDA;
   }
   timed("fwd_combine", st, [&] {
-    launch_combine(d, block_idx, at<void>(workspace, p.opart), at<float>(workspace, p.lpart), o,
-                   lse, st);
+    launch_combine(d, at<void>(workspace, p.opart), at<float>(workspace, p.lpart), o, lse, st);
   });
   return cuda_fail("msa_forward");
 }

@@ -549,6 +549,7 @@ __global__ void __launch_bounds__(256, 1)
   uint8_t* sQp = sKp + kKV;        // [2][64 tokens][128 d]
   uint8_t* sdz = sQp + 2 * kRT;    // dz^T [128 keys][64 tokens]
   float* sPb = reinterpret_cast<float*>(sdz + kST);  // [2][64 entries][128 keys] fp32
+  float* sStg = sPb + 2 * kPG * kBlock;               // dQp staging: [4 warps][64 tokens][32 d] fp32
   const uint32_t aKp = smem_u32(sKp), aQp = smem_u32(sQp), adz = smem_u32(sdz);
 
   const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
@@ -752,12 +753,10 @@ __global__ void __launch_bounds__(256, 1)
           for (int e = 0; e < 2; ++e) {
             const int k = 2 * k2 + e;
             const int t = sh->tok[bb][k];
-            float v = 0.f;
-            if (k < gcount && t >= 0 && j <= t) {
-              const float zz = __uint_as_float(k < 32 ? z0[k] : z1[k - 32]);
-              v = A.cz * (ex2(zz * sl2 - sh->lpx2[bb][k]) - pbr[k * kBlock + kr]);
-            }
-            dzv[e] = v;
+            // exponentiate unconditionally and select (no per-lane branch around the asm)
+            const float zz = __uint_as_float(k < 32 ? z0[k] : z1[k - 32]);
+            const float v = A.cz * (ex2(zz * sl2 - sh->lpx2[bb][k]) - pbr[k * kBlock + kr]);
+            dzv[e] = (k < gcount && t >= 0 && j <= t) ? v : 0.f;
           }
           zw[k2] = pack_bf16(dzv[0], dzv[1]);
         }
@@ -781,12 +780,19 @@ __global__ void __launch_bounds__(256, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&sh->fl_free);
         }
+        // dQp^T (TMEM lane = head-dim index kr) -> token-major staging -> 16-byte reductions, each
+        // instruction covering 4 tokens x 128 contiguous bytes
+        float* stg = sStg + w4 * (kPG * 32);
 #pragma unroll
-        for (int k = 0; k < kPG; ++k) {  // dQp^T: TMEM lane = head-dim index kr
+        for (int k = 0; k < kPG; ++k)
+          stg[k * 32 + lane] = __uint_as_float(k < 32 ? q0[k] : q1[k - 32]) * d.scale;
+        __syncwarp();
+#pragma unroll 4
+        for (int it2 = 0; it2 < kPG / 4; ++it2) {
+          const int k = it2 * 4 + lane / 8, c4 = lane % 8;
+          const float4 v = *reinterpret_cast<const float4*>(stg + k * 32 + 4 * c4);
           const int t = k < gcount ? sh->tok[bb][k] : -1;
-          if (t >= 0)
-            red1(A.dqp + (((size_t)b * d.S + t) * d.Hp + g) * kD + kr,
-                 __uint_as_float(k < 32 ? q0[k] : q1[k - 32]) * d.scale);
+          red_add_v4_if(t >= 0, A.dqp + (((size_t)b * d.S + (t < 0 ? 0 : t)) * d.Hp + g) * kD + w4 * 32 + 4 * c4, v);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh->meta_free[bb]);  // token metadata of this buffer read
@@ -831,7 +837,7 @@ void attn_bwd_g(const CUtensorMap& mk, const CUtensorMap& mv, const MainArgs& a,
 template <bool kDense>
 void proxy_bwd_g(const CUtensorMap& mkp, const ProxyArgs& a, cudaStream_t st) {
   const size_t smem = sizeof(ProxyShared) + 1024 + (size_t)kKV + 2 * (size_t)kRT + kST +
-                      2 * (size_t)kPG * kBlock * 4;
+                      2 * (size_t)kPG * kBlock * 4 + 4 * (size_t)kPG * 32 * 4;
   cudaFuncSetAttribute(proxy_bwd_kernel<kDense>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        (int)smem);
   proxy_bwd_kernel<kDense><<<num_sms(), 256, smem, st>>>(mkp, a);

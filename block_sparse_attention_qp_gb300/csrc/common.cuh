@@ -79,6 +79,13 @@ __device__ __forceinline__ void cp_async_arrive(uint64_t* mbar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(smem_u32(mbar))
                : "memory");
 }
+// 16-byte fp32 reduction predicated inside the instruction (no branch).
+__device__ __forceinline__ void red_add_v4_if(bool pred, float* p, float4 v) {
+  asm volatile(
+      "{\n.reg .pred q;\nsetp.ne.b32 q, %5, 0;\n@q red.global.add.v4.f32 [%0], {%1, %2, %3, %4};\n}\n" ::"l"(p),
+      "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"((int)pred)
+      : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 template <int N>

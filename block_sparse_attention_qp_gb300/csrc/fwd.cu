@@ -84,10 +84,9 @@ __device__ __forceinline__ void online_step(float (&s)[8][4], float (&m)[2], flo
 // ------------------------------------------------------------------------------------------
 // Combine (second phase of the sparse forward): one warp per (b, t, h) merges the partials of
 // its valid slots,  O = sum_s w_s O_s / sum_s w_s,  w_s = exp(lse_s - max),  LSE = max + log sum.
-// Half-warps take alternate slots with 16-byte loads (8 columns per lane), so a warp keeps
-// several 512-byte reads in flight.
-__global__ void __launch_bounds__(256) combine_kernel(Dims d, const int32_t* __restrict__ idx,
-                                                      const bf16* __restrict__ opart,
+// A slot is valid iff its partial log-sum-exp was written: the workspace holds NaN (all-ones
+// bytes) elsewhere.  Half-warps take alternate slots with 16-byte loads (8 columns per lane).
+__global__ void __launch_bounds__(256) combine_kernel(Dims d, const bf16* __restrict__ opart,
                                                       const float* __restrict__ lpart,
                                                       bf16* __restrict__ o, float* __restrict__ lse) {
   const long long rows = (long long)d.B * d.S * d.Hq;
@@ -95,21 +94,11 @@ __global__ void __launch_bounds__(256) combine_kernel(Dims d, const int32_t* __r
   const uint64_t pol = l2_policy_evict_first();  // each partial is read exactly once
   for (long long r = (blockIdx.x * (long long)blockDim.x + threadIdx.x) / 32; r < rows;
        r += (long long)gridDim.x * blockDim.x / 32) {
-    const int h = (int)(r % d.Hq);
-    const long long bt = r / d.Hq;
-    const int t = (int)(bt % d.S), b = (int)(bt / d.S);
-    const int g = h / d.G;
-    const int32_t* row = idx + (((size_t)b * d.Hp + g) * d.S + t) * d.top_k;
     const size_t base = (size_t)r * d.top_k;
-    unsigned long long valid = 0;
-    {
-      int prev = -1;
-      bool padded = false;
-      for (int s = 0; s < d.top_k; ++s)
-        if (slot_valid(row, s, t, prev, padded)) valid |= 1ull << s;
-    }
-    const float l0 = (valid >> lane) & 1 ? lpart[base + lane] : -INFINITY;
-    const float l1 = lane + 32 < d.top_k && ((valid >> (lane + 32)) & 1) ? lpart[base + lane + 32] : -INFINITY;
+    float l0 = lane < d.top_k ? lpart[base + lane] : NAN;
+    float l1 = lane + 32 < d.top_k ? lpart[base + lane + 32] : NAN;
+    l0 = l0 == l0 ? l0 : -INFINITY;  // NaN: slot not written (invalid or padding)
+    l1 = l1 == l1 ? l1 : -INFINITY;
     float mx = fmaxf(l0, l1);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
@@ -143,7 +132,12 @@ __global__ void __launch_bounds__(256) combine_kernel(Dims d, const int32_t* __r
       *reinterpret_cast<uint4*>(o + (size_t)r * kD + l16 * 8) =
           make_uint4(pack_bf16(acc[0] * inv, acc[1] * inv), pack_bf16(acc[2] * inv, acc[3] * inv),
                      pack_bf16(acc[4] * inv, acc[5] * inv), pack_bf16(acc[6] * inv, acc[7] * inv));
-    if (lane == 0) lse[((size_t)b * d.Hq + h) * d.S + t] = sum > 0.f ? mx + logf(sum) : -INFINITY;
+    if (lane == 0) {
+      const int h = (int)(r % d.Hq);
+      const long long bt = r / d.Hq;
+      const int t = (int)(bt % d.S), b = (int)(bt / d.S);
+      lse[((size_t)b * d.Hq + h) * d.S + t] = sum > 0.f ? mx + logf(sum) : -INFINITY;
+    }
   }
 }
 
@@ -413,12 +407,12 @@ __global__ void __launch_bounds__(256, 2)
 // ------------------------------------------------------------------------------------------
 static int persistent_grid(int ctas_per_sm) { return num_sms() * ctas_per_sm; }
 
-void launch_combine(const Dims& d, const int32_t* idx, const void* opart, const float* lpart,
-                    void* o, float* lse, cudaStream_t st) {
+void launch_combine(const Dims& d, const void* opart, const float* lpart, void* o, float* lse,
+                    cudaStream_t st) {
   const long long rows = (long long)d.B * d.S * d.Hq;
   long long grid = (rows * 32 + 255) / 256;
   if (grid > (long long)num_sms() * 8) grid = (long long)num_sms() * 8;
-  combine_kernel<<<(int)grid, 256, 0, st>>>(d, idx, (const bf16*)opart, lpart, (bf16*)o, lse);
+  combine_kernel<<<(int)grid, 256, 0, st>>>(d, (const bf16*)opart, lpart, (bf16*)o, lse);
 }
 
 template <int G>

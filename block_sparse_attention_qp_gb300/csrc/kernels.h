@@ -58,8 +58,10 @@ bool launch_attn_fwd(const Dims& d, const void* q, const void* k, const void* v,
                      const int* n_items, long long max_items, void* opart, float* lpart,
                      unsigned* status, cudaStream_t st);
 int fwd_item_tiles();  // 128-row tiles per sparse-forward work item
-void launch_combine(const Dims& d, const int32_t* idx, const void* opart, const float* lpart,
-                    void* o, float* lse, cudaStream_t st);
+// Merges the partials of every (b, t, h); a partial is valid iff its log-sum-exp is not NaN
+// (the caller fills lpart with NaN bytes before the partial pass).
+void launch_combine(const Dims& d, const void* opart, const float* lpart, void* o, float* lse,
+                    cudaStream_t st);
 void launch_dense_fwd(const Dims& d, const void* q, const void* k, const void* v, void* o,
                       float* lse, cudaStream_t st);
 
