@@ -111,8 +111,8 @@ struct ProxyArgs {
 struct ProxyShared {
   int tok[2][kPG];
   float lpx2[2][kPG];
-  uint64_t kp_full, kp_empty, q_full[2], q_empty[2], meta_free[2], z_full, dz_full, fl_full, fl_free,
-      acc_free;
+  uint64_t kp_full, kp_empty, q_full[2], q_empty[2], meta_free[2], z_full[2], dz_full, fl_full[2],
+      fl_free, acc_free;
   uint32_t tmem;
 };
 
@@ -534,11 +534,13 @@ __global__ void __launch_bounds__(256, 1)
 
 // ==========================================================================================
 // Proxy gradients of the KL term from the teacher pbar written by attn_bwd_kernel.
-// Roles: warp 0 TMA of the block's proxy keys + tensor memory, warp 1 MMA, warp 2 gathers the
-// group's Qp rows and pbar rows, warps 4-7 compute dz (thread = key) and read the results out.
-// Tensor memory (256 columns): Z (z^T, 64), QP (dQp^T, 64), KP (dKp accumulator, 128).
+// Roles (384 threads): warp 0 TMA of the block's proxy keys + tensor memory, warp 1 MMA, warps 2-3
+// gather the group's Qp rows and pbar rows, warps 4-7 compute dz (thread = key) and flush dKp at
+// item end, warps 8-11 flush dQp.  Tensor memory (512 columns allocated): Z0, Z1 (z^T, 64 each,
+// alternate groups), QP (dQp^T, 64), KP (dKp accumulator, 128).  dz^T is double-buffered in
+// shared memory, so the dz of one group overlaps the products and the flush of the previous one.
 template <bool kDense>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
     proxy_bwd_kernel(const __grid_constant__ CUtensorMap tm_kp, ProxyArgs A) {
   using namespace sm100;
   const Dims& d = A.d;
@@ -547,8 +549,8 @@ __global__ void __launch_bounds__(256, 1)
   uint8_t* base = align1024(smem_raw + sizeof(ProxyShared));
   uint8_t* sKp = base;             // [128 keys][128 d]  (TMA)
   uint8_t* sQp = sKp + kKV;        // [2][64 tokens][128 d]
-  uint8_t* sdz = sQp + 2 * kRT;    // dz^T [128 keys][64 tokens]
-  float* sPb = reinterpret_cast<float*>(sdz + kST);  // [2][64 entries][128 keys] fp32
+  uint8_t* sdz = sQp + 2 * kRT;    // [2] dz^T [128 keys][64 tokens]
+  float* sPb = reinterpret_cast<float*>(sdz + 2 * kST);  // [2][64 entries][128 keys] fp32
   float* sStg = sPb + 2 * kPG * kBlock;               // dQp staging: [4 warps][64 tokens][32 d] fp32
   const uint32_t aKp = smem_u32(sKp), aQp = smem_u32(sQp), adz = smem_u32(sdz);
 
@@ -563,24 +565,24 @@ __global__ void __launch_bounds__(256, 1)
       mbar_init(&sh->q_full[x], 128);  // 2 gather warps x 32 lanes: a plain (or expect-tx) and a
                                        // cp.async arrival each
       mbar_init(&sh->q_empty[x], 1);
-      mbar_init(&sh->meta_free[x], 4);
+      mbar_init(&sh->meta_free[x], 8);  // the dz and the dQp-flush warps
+      mbar_init(&sh->z_full[x], 1);
+      mbar_init(&sh->fl_full[x], 1);
     }
-    mbar_init(&sh->z_full, 1);
     mbar_init(&sh->dz_full, 4);
-    mbar_init(&sh->fl_full, 1);
     mbar_init(&sh->fl_free, 4);
     mbar_init(&sh->acc_free, 4);
     mbar_fence_init();
   }
   if (warp == 0) {
-    tmem_alloc(&sh->tmem, 256);
+    tmem_alloc(&sh->tmem, 512);
     tmem_relinquish();
   }
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = sh->tmem;
-  const uint32_t RZ = tmem, RQ = tmem + 64, RKP = tmem + 128;
+  const uint32_t RZ0 = tmem, RQ = tmem + 128, RKP = tmem + 256;  // RZ_b = RZ0 + 64 b
   bool ok = true;
 
   if (warp == 0) {
@@ -599,42 +601,54 @@ __global__ void __launch_bounds__(256, 1)
       }
     }
   } else if (warp == 1) {
+    // ---- MMA issuer: z(i) for group i, then the gradients of group i-1 (within an item)
     if (lane == 0) {
       constexpr uint32_t id_z = idesc_bf16(128, kPG, false, false);
       constexpr uint32_t id_k = idesc_bf16(128, 128, false, true);
       constexpr uint32_t id_p = idesc_bf16(128, kPG, true, true);
       long long ni = 0, i = 0;
+      // dKp += dz^T Qp and dQp^T = Kp^T dz^T for group j (gj-th of its item, gcount tokens)
+      auto grads = [&](long long j, int gj, int gcount, bool last) -> bool {
+        const int b = (int)(j & 1);
+        if (!mbar_wait(&sh->dz_full, par(j), A.status)) return false;
+        if (gj == 0 && ni > 0 && !mbar_wait(&sh->acc_free, par(ni - 1), A.status)) return false;
+        if (j > 0 && !mbar_wait(&sh->fl_free, par(j - 1), A.status)) return false;  // RQ read
+        fence_async_smem();  // dz^T was written with st.shared by the dz warps
+        fence_after_sync();
+        const uint32_t aQb = aQp + b * kRT, adzb = adz + b * kST;
+        const int kst = (gcount + 15) / 16;
+        for (int ks = 0; ks < kst; ++ks)  // dKp += dz^T Qp
+          mma_ss(RKP, desc_kmajor(adzb, 128, ks), desc_mnmajor(aQb, kPG, ks), id_k, gj > 0 || ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)  // dQp^T = Kp^T dz^T
+          mma_ss(RQ, desc_mnmajor(aKp, 128, ks), desc_mnmajor(adzb, 128, ks), id_p, ks > 0);
+        mma_commit(&sh->fl_full[b]);
+        mma_commit(&sh->q_empty[b]);
+        if (last) mma_commit(&sh->kp_empty);
+        return true;
+      };
       for (long long it = blockIdx.x; ok && it < total; it += gridDim.x, ++ni) {
         const Item item = A.items[it];
         if (!mbar_wait(&sh->kp_full, par(ni), A.status)) { ok = false; break; }
         const int ngroups = (item.count + kPG - 1) / kPG;
         for (int gi = 0; gi < ngroups; ++gi, ++i) {
           const int b = (int)(i & 1);
-          const int gcount = min(kPG, item.count - gi * kPG);
           if (!mbar_wait(&sh->q_full[b], par(i >> 1), A.status)) { ok = false; break; }
-          if (i > 0 && !mbar_wait(&sh->fl_free, par(i - 1), A.status)) { ok = false; break; }
+          // RZ_b was last read by the dz warps for group i-2; the gradients of that group, which
+          // waited for it (dz_full), were issued before this point
           // Qp rows came from other threads' cp.async (generic proxy), tracked by q_full
           fence_async_smem();
           fence_after_sync();
           const uint32_t aQb = aQp + b * kRT;
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)  // z^T = Kp Qp^T
-            mma_ss(RZ, desc_kmajor(aKp, 128, ks), desc_kmajor(aQb, kPG, ks), id_z, ks > 0);
-          mma_commit(&sh->z_full);
-          if (!mbar_wait(&sh->dz_full, par(i), A.status)) { ok = false; break; }
-          if (gi == 0 && ni > 0 && !mbar_wait(&sh->acc_free, par(ni - 1), A.status)) { ok = false; break; }
-          fence_after_sync();
-          const int kst = (gcount + 15) / 16;
-          for (int ks = 0; ks < kst; ++ks)  // dKp += dz^T Qp
-            mma_ss(RKP, desc_kmajor(adz, 128, ks), desc_mnmajor(aQb, kPG, ks), id_k, gi > 0 || ks > 0);
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks)  // dQp^T = Kp^T dz^T
-            mma_ss(RQ, desc_mnmajor(aKp, 128, ks), desc_mnmajor(adz, 128, ks), id_p, ks > 0);
-          mma_commit(&sh->fl_full);
-          mma_commit(&sh->q_empty[b]);
+            mma_ss(RZ0 + 64 * b, desc_kmajor(aKp, 128, ks), desc_kmajor(aQb, kPG, ks), id_z, ks > 0);
+          mma_commit(&sh->z_full[b]);
+          if (gi > 0 && !grads(i - 1, gi - 1, kPG, false)) { ok = false; break; }
         }
         if (!ok) break;
-        mma_commit(&sh->kp_empty);
+        if (ngroups > 0 &&
+            !grads(i - 1, ngroups - 1, item.count - (ngroups - 1) * kPG, true)) { ok = false; break; }
       }
     }
   } else if (warp == 2 || warp == 3) {
@@ -718,16 +732,17 @@ __global__ void __launch_bounds__(256, 1)
       for (long long x = (i >= 2 ? i - 2 : 0); x < i; ++x)
         mbar_wait_warp(&sh->q_full[x & 1], par(x >> 1), A.status);
     }
-  } else if (warp >= 4) {
+  } else if (warp < 8) {
+    // ---- dz (thread = key): dz^T = kl_grad/(B S Hp) (softmax(scale z) - pbar); item end: dKp
     const int w4 = warp - 4;
-    const int kr = w4 * 32 + lane;  // key (TMEM lane of z^T, dKp); head-dim index for dQp^T
+    const int kr = w4 * 32 + lane;  // key (tensor-memory lane of z^T and dKp)
     const uint32_t lb = static_cast<uint32_t>(w4 * 32) << 16;
     long long i = 0;
     for (long long it = blockIdx.x; ok && it < total; it += gridDim.x) {
       const Item item = A.items[it];
       const int n = item.seg % d.nblk;
       const int bg = (int)((item.seg % d.nseg()) / d.nblk);
-      const int b = bg / d.Hp, g = bg % d.Hp;
+      const int b = bg / d.Hp;
       const int j = n * kBlock + kr;
       const int ngroups = (item.count + kPG - 1) / kPG;
       for (int gi = 0; gi < ngroups; ++gi, ++i) {
@@ -735,14 +750,14 @@ __global__ void __launch_bounds__(256, 1)
         const int gcount = min(kPG, item.count - gi * kPG);
         __syncwarp();
         if (!mbar_wait_warp(&sh->q_full[bb], par(i >> 1), A.status) ||
-            !mbar_wait_warp(&sh->z_full, par(i), A.status)) {
+            !mbar_wait_warp(&sh->z_full[bb], par(i >> 1), A.status)) {
           ok = false;
           break;
         }
         fence_after_sync();
         uint32_t z0[32], z1[32];
-        tmem_ld32(RZ + lb, z0);
-        tmem_ld32(RZ + lb + 32, z1);
+        tmem_ld32(RZ0 + 64 * bb + lb, z0);
+        tmem_ld32(RZ0 + 64 * bb + lb + 32, z1);
         tmem_wait_ld();
         const float* pbr = sPb + bb * kPG * kBlock;
         uint32_t zw[kPG / 2];
@@ -760,46 +775,33 @@ __global__ void __launch_bounds__(256, 1)
           }
           zw[k2] = pack_bf16(dzv[0], dzv[1]);
         }
+        // dz^T buffer bb was last read by the gradient products of group i-2
+        if (i >= 2 && !mbar_wait_warp(&sh->fl_full[bb], par((i - 2) >> 1), A.status)) {
+          ok = false;
+          break;
+        }
+        const uint32_t adzb = adz + bb * kST;
 #pragma unroll
         for (int u = 0; u < 8; ++u)
-          st_shared_v4(adz + sm100::sw128_chunk(kr, u), zw[4 * u], zw[4 * u + 1], zw[4 * u + 2],
+          st_shared_v4(adzb + sm100::sw128_chunk(kr, u), zw[4 * u], zw[4 * u + 1], zw[4 * u + 2],
                        zw[4 * u + 3]);
         fence_async_smem();
         fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sh->dz_full);
-        if (!mbar_wait_warp(&sh->fl_full, par(i), A.status)) { ok = false; break; }
-        fence_after_sync();
-        uint32_t q0[32], q1[32];
-        tmem_ld32(RQ + lb, q0);
-        tmem_ld32(RQ + lb + 32, q1);
-        tmem_wait_ld();
-        const bool last = gi == ngroups - 1;
-        if (!last) {
-          fence_before_sync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sh->fl_free);
+        if (lane == 0) {
+          mbar_arrive(&sh->dz_full);        // also: RZ_bb read
+          mbar_arrive(&sh->meta_free[bb]);  // tok / lpx2 / pbar rows of this buffer read
         }
-        // dQp^T (TMEM lane = head-dim index kr) -> token-major staging -> 16-byte reductions, each
-        // instruction covering 4 tokens x 128 contiguous bytes
-        float* stg = sStg + w4 * (kPG * 32);
-#pragma unroll
-        for (int k = 0; k < kPG; ++k)
-          stg[k * 32 + lane] = __uint_as_float(k < 32 ? q0[k] : q1[k - 32]) * d.scale;
-        __syncwarp();
-#pragma unroll 4
-        for (int it2 = 0; it2 < kPG / 4; ++it2) {
-          const int k = it2 * 4 + lane / 8, c4 = lane % 8;
-          const float4 v = *reinterpret_cast<const float4*>(stg + k * 32 + 4 * c4);
-          const int t = k < gcount ? sh->tok[bb][k] : -1;
-          red_add_v4_if(t >= 0, A.dqp + (((size_t)b * d.S + (t < 0 ? 0 : t)) * d.Hp + g) * kD + w4 * 32 + 4 * c4, v);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh->meta_free[bb]);  // token metadata of this buffer read
-        if (last) {  // item end: dKp rows of this key
+        if (gi == ngroups - 1) {  // item end: dKp rows of this key, once its last product landed
+          if (!mbar_wait_warp(&sh->fl_full[bb], par(i >> 1), A.status)) {
+            ok = false;
+            break;
+          }
+          fence_after_sync();
           float* dst = A.dkp + ((size_t)b * d.S + j) * kD;
-#pragma unroll
+#pragma unroll 1
           for (int c = 0; c < 4; ++c) {
+            __syncwarp();
             uint32_t rk[32];
             tmem_ld32(RKP + lb + c * 32, rk);
             tmem_wait_ld();
@@ -811,18 +813,59 @@ __global__ void __launch_bounds__(256, 1)
           }
           fence_before_sync();
           __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(&sh->fl_free);
-            mbar_arrive(&sh->acc_free);
-          }
+          if (lane == 0) mbar_arrive(&sh->acc_free);
         }
+      }
+    }
+  } else {
+    // ---- dQp flush (warps 8-11, thread = head-dim index): dQp^T -> token-major staging ->
+    // 16-byte reductions, each instruction covering 4 tokens x 128 contiguous bytes
+    const int w4 = warp - 8;
+    const uint32_t lb = static_cast<uint32_t>(w4 * 32) << 16;
+    float* stg = sStg + w4 * (kPG * 32);
+    long long i = 0;
+    for (long long it = blockIdx.x; ok && it < total; it += gridDim.x) {
+      const Item item = A.items[it];
+      const int bg = (int)((item.seg % d.nseg()) / d.nblk);
+      const int b = bg / d.Hp, g = bg % d.Hp;
+      const int ngroups = (item.count + kPG - 1) / kPG;
+      for (int gi = 0; gi < ngroups; ++gi, ++i) {
+        const int bb = (int)(i & 1);
+        const int gcount = min(kPG, item.count - gi * kPG);
+        __syncwarp();
+        if (!mbar_wait_warp(&sh->fl_full[bb], par(i >> 1), A.status)) {
+          ok = false;
+          break;
+        }
+        fence_after_sync();
+        uint32_t q0[32], q1[32];
+        tmem_ld32(RQ + lb, q0);
+        tmem_ld32(RQ + lb + 32, q1);
+        tmem_wait_ld();
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh->fl_free);  // RQ may take the next group's dQp^T
+#pragma unroll
+        for (int k = 0; k < kPG; ++k)
+          stg[k * 32 + lane] = __uint_as_float(k < 32 ? q0[k] : q1[k - 32]) * d.scale;
+        __syncwarp();
+#pragma unroll 4
+        for (int it2 = 0; it2 < kPG / 4; ++it2) {
+          const int k = it2 * 4 + lane / 8, c4 = lane % 8;
+          const float4 v = *reinterpret_cast<const float4*>(stg + k * 32 + 4 * c4);
+          const int t = k < gcount ? sh->tok[bb][k] : -1;
+          red_add_v4_if(t >= 0,
+                        A.dqp + (((size_t)b * d.S + (t < 0 ? 0 : t)) * d.Hp + g) * kD + w4 * 32 + 4 * c4, v);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh->meta_free[bb]);  // token metadata of this buffer read
       }
     }
   }
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
-  if (warp == 0) tmem_dealloc(tmem, 256);
+  if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
 namespace {
@@ -836,11 +879,11 @@ void attn_bwd_g(const CUtensorMap& mk, const CUtensorMap& mv, const MainArgs& a,
 }
 template <bool kDense>
 void proxy_bwd_g(const CUtensorMap& mkp, const ProxyArgs& a, cudaStream_t st) {
-  const size_t smem = sizeof(ProxyShared) + 1024 + (size_t)kKV + 2 * (size_t)kRT + kST +
+  const size_t smem = sizeof(ProxyShared) + 1024 + (size_t)kKV + 2 * (size_t)kRT + 2 * (size_t)kST +
                       2 * (size_t)kPG * kBlock * 4 + 4 * (size_t)kPG * 32 * 4;
   cudaFuncSetAttribute(proxy_bwd_kernel<kDense>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        (int)smem);
-  proxy_bwd_kernel<kDense><<<num_sms(), 256, smem, st>>>(mkp, a);
+  proxy_bwd_kernel<kDense><<<num_sms(), 384, smem, st>>>(mkp, a);
 }
 }  // namespace
 
