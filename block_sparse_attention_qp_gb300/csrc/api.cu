@@ -75,7 +75,7 @@ size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 struct Plan {
   size_t status = 0, totals = 0, seg_count = 0, seg_offset = 0, seg_cursor = 0, entries = 0;
   size_t io0 = 0, io1 = 0, items0 = 0, items1 = 0;
-  size_t opart = 0, lpart = 0, lpx_part = 0, lse_px = 0, drow = 0, pbar = 0;
+  size_t opart = 0, lpart = 0, lpx_part = 0, lse_px = 0, lpxe = 0, drow = 0, pbar = 0;
   size_t dq = 0, dk = 0, dv = 0, dqp = 0, dkp = 0;
   size_t bytes = 0;
   long long max0 = 0, max1 = 0;
@@ -173,6 +173,7 @@ Plan make_plan(const Dims& d, int op) {
     p.lse_px = c.take((size_t)rows_p * sizeof(float));
     p.drow = c.take((size_t)rows_q * sizeof(float));
     p.pbar = c.take((size_t)ent * kBlock * sizeof(float));  // teacher rows, one per list entry
+    p.lpxe = c.take((size_t)ent * sizeof(float));            // proxy log-normaliser per entry
     p.dq = c.take((size_t)rows_q * kD * sizeof(float));
     p.dk = c.take((size_t)rows_kv * kD * sizeof(float));
     p.dv = c.take((size_t)rows_kv * kD * sizeof(float));
@@ -428,9 +429,14 @@ int msa_backward(const msa_shape_t* shape, const void* q, const void* k, const v
                          at<float>(workspace, p.dv), at<float>(workspace, p.pbar),
                          at<unsigned>(workspace, p.status), st);
   });
+  timed("entry_lse", st, [&] {
+    launch_entry_lse(d, false, at<int>(workspace, p.seg_count), at<int>(workspace, p.seg_offset),
+                     at<int>(workspace, p.entries), at<float>(workspace, p.lse_px),
+                     at<float>(workspace, p.lpxe), st);
+  });
   if (ok)
     timed("proxy_bwd", st, [&] {
-      ok = launch_proxy_bwd(d, false, qp, kp, at<float>(workspace, p.lse_px),
+      ok = launch_proxy_bwd(d, false, qp, kp, at<float>(workspace, p.lpxe),
                             at<float>(workspace, p.pbar), kl_grad, at<int>(workspace, p.seg_offset),
                             at<int>(workspace, p.entries), at<Item>(workspace, p.items1),
                             at<int>(workspace, p.totals) + 2, p.max1, at<float>(workspace, p.dqp),
@@ -494,9 +500,13 @@ int msa_warmup_backward(const msa_shape_t* shape, const void* q, const void* k, 
                          at<float>(workspace, p.dk), at<float>(workspace, p.dv),
                          at<float>(workspace, p.pbar), status, st);
   });
+  timed("entry_lse", st, [&] {
+    launch_entry_lse(d, true, nullptr, at<int>(workspace, p.seg_offset), nullptr,
+                     at<float>(workspace, p.lse_px), at<float>(workspace, p.lpxe), st);
+  });
   if (ok)
     timed("proxy_bwd_dense", st, [&] {
-      ok = launch_proxy_bwd(d, true, qp, kp, at<float>(workspace, p.lse_px),
+      ok = launch_proxy_bwd(d, true, qp, kp, at<float>(workspace, p.lpxe),
                             at<float>(workspace, p.pbar), kl_grad, at<int>(workspace, p.seg_offset),
                             nullptr, at<Item>(workspace, p.items0), at<int>(workspace, p.totals) + 1,
                             p.max0, at<float>(workspace, p.dqp), at<float>(workspace, p.dkp),

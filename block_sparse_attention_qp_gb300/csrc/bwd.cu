@@ -97,7 +97,7 @@ struct MainShared {
 struct ProxyArgs {
   Dims d;
   const bf16* qp;
-  const float *lse_px, *pbar;
+  const float *lpxe, *pbar;  // per list entry: LSE_px x log2 e, teacher row [128 keys]
   float cz;  // kl_grad / (B * S * Hp)
   const int* seg_offset;
   const int* entries;
@@ -108,11 +108,14 @@ struct ProxyArgs {
   unsigned* status;
 };
 
+constexpr int kQPB = 3;  // proxy query row buffers
+
 struct ProxyShared {
-  int tok[2][kPG];
+  int tok[2][kPG];     // per teacher buffer (read by the dz warps)
   float lpx2[2][kPG];
-  uint64_t kp_full, kp_empty, q_full[2], q_empty[2], meta_free[2], z_full[2], dz_full, fl_full[2],
-      fl_free, acc_free;
+  int tokq[kQPB][kPG];  // per query-row buffer (read by the dQp-flush warps)
+  uint64_t kp_full, kp_empty, qp_full[kQPB], qp_empty[kQPB], pb_full[2], meta_free[2], z_full[2],
+      dz_full, fl_full[2], fl_free, acc_free;
   uint32_t tmem;
 };
 
@@ -548,8 +551,8 @@ __global__ void __launch_bounds__(384, 1)
   ProxyShared* sh = reinterpret_cast<ProxyShared*>(smem_raw);
   uint8_t* base = align1024(smem_raw + sizeof(ProxyShared));
   uint8_t* sKp = base;             // [128 keys][128 d]  (TMA)
-  uint8_t* sQp = sKp + kKV;        // [2][64 tokens][128 d]
-  uint8_t* sdz = sQp + 2 * kRT;    // [2] dz^T [128 keys][64 tokens]
+  uint8_t* sQp = sKp + kKV;        // [kQPB][64 tokens][128 d]
+  uint8_t* sdz = sQp + kQPB * kRT;  // [2] dz^T [128 keys][64 tokens]
   float* sPb = reinterpret_cast<float*>(sdz + 2 * kST);  // [2][64 entries][128 keys] fp32
   float* sStg = sPb + 2 * kPG * kBlock;               // dQp staging: [4 warps][64 tokens][32 d] fp32
   const uint32_t aKp = smem_u32(sKp), aQp = smem_u32(sQp), adz = smem_u32(sdz);
@@ -561,11 +564,13 @@ __global__ void __launch_bounds__(384, 1)
   if (tid == 0) {
     mbar_init(&sh->kp_full, 1);
     mbar_init(&sh->kp_empty, 1);
+    for (int x = 0; x < kQPB; ++x) {
+      mbar_init(&sh->qp_full[x], 128);  // 2 gather warps x 32 lanes: a plain and a cp.async arrival
+      mbar_init(&sh->qp_empty[x], 5);   // the MMA's commit and the 4 dQp-flush warps
+    }
     for (int x = 0; x < 2; ++x) {
-      mbar_init(&sh->q_full[x], 128);  // 2 gather warps x 32 lanes: a plain (or expect-tx) and a
-                                       // cp.async arrival each
-      mbar_init(&sh->q_empty[x], 1);
-      mbar_init(&sh->meta_free[x], 8);  // the dz and the dQp-flush warps
+      mbar_init(&sh->pb_full[x], 64);  // the gather lanes (one with the bulk copy's expect-tx)
+      mbar_init(&sh->meta_free[x], 4);  // the dz warps
       mbar_init(&sh->z_full[x], 1);
       mbar_init(&sh->fl_full[x], 1);
     }
@@ -615,7 +620,7 @@ __global__ void __launch_bounds__(384, 1)
         if (j > 0 && !mbar_wait(&sh->fl_free, par(j - 1), A.status)) return false;  // RQ read
         fence_async_smem();  // dz^T was written with st.shared by the dz warps
         fence_after_sync();
-        const uint32_t aQb = aQp + b * kRT, adzb = adz + b * kST;
+        const uint32_t aQb = aQp + (int)(j % kQPB) * kRT, adzb = adz + b * kST;
         const int kst = (gcount + 15) / 16;
         for (int ks = 0; ks < kst; ++ks)  // dKp += dz^T Qp
           mma_ss(RKP, desc_kmajor(adzb, 128, ks), desc_mnmajor(aQb, kPG, ks), id_k, gj > 0 || ks > 0);
@@ -623,7 +628,7 @@ __global__ void __launch_bounds__(384, 1)
         for (int ks = 0; ks < 8; ++ks)  // dQp^T = Kp^T dz^T
           mma_ss(RQ, desc_mnmajor(aKp, 128, ks), desc_mnmajor(adzb, 128, ks), id_p, ks > 0);
         mma_commit(&sh->fl_full[b]);
-        mma_commit(&sh->q_empty[b]);
+        mma_commit(&sh->qp_empty[j % kQPB]);
         if (last) mma_commit(&sh->kp_empty);
         return true;
       };
@@ -632,14 +637,14 @@ __global__ void __launch_bounds__(384, 1)
         if (!mbar_wait(&sh->kp_full, par(ni), A.status)) { ok = false; break; }
         const int ngroups = (item.count + kPG - 1) / kPG;
         for (int gi = 0; gi < ngroups; ++gi, ++i) {
-          const int b = (int)(i & 1);
-          if (!mbar_wait(&sh->q_full[b], par(i >> 1), A.status)) { ok = false; break; }
+          const int b = (int)(i & 1), qb = (int)(i % kQPB);
+          if (!mbar_wait(&sh->qp_full[qb], par(i / kQPB), A.status)) { ok = false; break; }
           // RZ_b was last read by the dz warps for group i-2; the gradients of that group, which
           // waited for it (dz_full), were issued before this point
-          // Qp rows came from other threads' cp.async (generic proxy), tracked by q_full
+          // Qp rows came from other threads' cp.async (generic proxy), tracked by qp_full
           fence_async_smem();
           fence_after_sync();
-          const uint32_t aQb = aQp + b * kRT;
+          const uint32_t aQb = aQp + qb * kRT;
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)  // z^T = Kp Qp^T
             mma_ss(RZ0 + 64 * b, desc_kmajor(aKp, 128, ks), desc_kmajor(aQb, kPG, ks), id_z, ks > 0);
@@ -652,9 +657,10 @@ __global__ void __launch_bounds__(384, 1)
       }
     }
   } else if (warp == 2 || warp == 3) {
-    // ---- gather: warp 2 + w fetches proxy query rows 32 w .. 32 w + 31 of each group with
-    // cp.async; lane 0 of warp 2 also copies the group's teacher rows, which are contiguous
-    // (consecutive list entries), with one bulk copy.  Completion is counted on q_full; the next
+    // ---- gather: warp 2 + w handles rows 32 w .. 32 w + 31 of each group.  The group's teacher
+    // rows (consecutive list entries, so contiguous) come with one bulk copy issued by lane 0 of
+    // warp 2 as soon as the dz warps have released that buffer; the proxy query rows come with
+    // cp.async into one of three buffers, released by the MMA and the dQp-flush warps.  The next
     // group's tokens and proxy normalisers are loaded one step ahead.
     const int w = warp - 2;
     long long it = blockIdx.x;
@@ -670,48 +676,58 @@ __global__ void __launch_bounds__(384, 1)
         const int x = 32 * w + lane;
         const int pos = grp * kPG + x;
         int t = -1;
-        if (pos < item.count)
+        lp = 0.f;
+        if (pos < item.count) {  // two independent loads, both indexed by the entry
           t = kDense ? (int)(item_base<true>(d, nullptr, item) + pos) : (__ldg(A.entries + item.base + pos) >> 8);
-        lp = t < 0 ? 0.f : __ldg(A.lse_px + ((size_t)b * d.Hp + g) * d.S + t) * kLog2e;
+          lp = __ldg(A.lpxe + item.base + pos);
+        }
+        (void)b;
+        (void)g;
         return t;
       };
       float lp_next;
       int t_next = load_row(cur, 0, lp_next);
       long long i = 0;
       while (true) {
-        const int bb = (int)(i & 1);
+        const int pb = (int)(i & 1), qb = (int)(i % kQPB);
         const int gcount = min(kPG, cur.count - gi * kPG);
-        if (i >= 2 && (!mbar_wait_warp(&sh->q_empty[bb], par((i - 2) >> 1), A.status) ||
-                       !mbar_wait_warp(&sh->meta_free[bb], par((i - 2) >> 1), A.status))) {
+        // ---- teacher rows + dz metadata (buffer pb: free once the dz warps read group i-2)
+        if (i >= 2 && !mbar_wait_warp(&sh->meta_free[pb], par((i - 2) >> 1), A.status)) {
+          ok = false;
+          break;
+        }
+        sh->tok[pb][32 * w + lane] = t_next;
+        sh->lpx2[pb][32 * w + lane] = lp_next;
+        __syncwarp();
+        if (w == 0 && lane == 0) {  // gcount entries x 128 keys, one bulk copy
+          const uint32_t bytes = (uint32_t)gcount * kBlock * 4;
+          mbar_expect_tx(&sh->pb_full[pb], bytes);  // also this lane's arrival
+          bulk_load(sPb + pb * kPG * kBlock, A.pbar + (size_t)(cur.base + gi * kPG) * kBlock, bytes,
+                    &sh->pb_full[pb]);
+        } else {
+          mbar_arrive(&sh->pb_full[pb]);  // publishes tok / lpx2
+        }
+        // ---- proxy query rows (buffer qb: free once group i-3's products and flush are done)
+        if (i >= kQPB && !mbar_wait_warp(&sh->qp_empty[qb], par(i / kQPB - 1), A.status)) {
           ok = false;
           break;
         }
         const int bg = (int)((cur.seg % d.nseg()) / d.nblk);
         const int b = bg / d.Hp, g = bg % d.Hp;
-        sh->tok[bb][32 * w + lane] = t_next;
-        sh->lpx2[bb][32 * w + lane] = lp_next;
+        sh->tokq[qb][32 * w + lane] = t_next;
         __syncwarp();
-        if (w == 0) {
-          if (lane == 0) {  // teacher rows: gcount entries x 128 keys, one bulk copy
-            const uint32_t bytes = (uint32_t)gcount * kBlock * 4;
-            mbar_expect_tx(&sh->q_full[bb], bytes);  // also this lane's plain arrival
-            bulk_load(sPb + bb * kPG * kBlock, A.pbar + (size_t)(cur.base + gi * kPG) * kBlock, bytes,
-                      &sh->q_full[bb]);
-          }
-        }
-        // proxy query rows (K-major SW128), rows >= gcount zero-filled
-        uint8_t* dQb = sQp + bb * kRT;
+        uint8_t* dQb = sQp + qb * kRT;
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
+        for (int k = 0; k < 16; ++k) {  // K-major SW128 rows, rows >= gcount zero-filled
           const int c = lane + 32 * k;  // 16-byte chunk of this warp's 32 rows
           const int r = 32 * w + (c >> 4), ch = c & 15;
-          const int t = sh->tok[bb][r];
+          const int t = sh->tokq[qb][r];
           const uint32_t off = (ch >> 3) * (kPG * 128) + sm100::sw128_chunk(r, ch & 7);
           const size_t grow = (((size_t)b * d.S + (t < 0 ? 0 : t)) * d.Hp + g) * kD + ch * 8;
           cp_async16(dQb + off, A.qp + grow, t >= 0);
         }
-        cp_async_arrive(&sh->q_full[bb]);
-        if (!(w == 0 && lane == 0)) mbar_arrive(&sh->q_full[bb]);  // publishes tok / lpx2
+        cp_async_arrive(&sh->qp_full[qb]);
+        mbar_arrive(&sh->qp_full[qb]);  // publishes tokq
         ++i;
         const int ngroups = (cur.count + kPG - 1) / kPG;
         if (gi + 1 < ngroups) {
@@ -730,7 +746,7 @@ __global__ void __launch_bounds__(384, 1)
       cp_async_wait_all();  // nothing may land after the block exits
       // the last bulk copies land before the block exits
       for (long long x = (i >= 2 ? i - 2 : 0); x < i; ++x)
-        mbar_wait_warp(&sh->q_full[x & 1], par(x >> 1), A.status);
+        mbar_wait_warp(&sh->pb_full[x & 1], par(x >> 1), A.status);
     }
   } else if (warp < 8) {
     // ---- dz (thread = key): dz^T = kl_grad/(B S Hp) (softmax(scale z) - pbar); item end: dKp
@@ -749,7 +765,7 @@ __global__ void __launch_bounds__(384, 1)
         const int bb = (int)(i & 1);
         const int gcount = min(kPG, item.count - gi * kPG);
         __syncwarp();
-        if (!mbar_wait_warp(&sh->q_full[bb], par(i >> 1), A.status) ||
+        if (!mbar_wait_warp(&sh->pb_full[bb], par(i >> 1), A.status) ||
             !mbar_wait_warp(&sh->z_full[bb], par(i >> 1), A.status)) {
           ok = false;
           break;
@@ -830,10 +846,12 @@ __global__ void __launch_bounds__(384, 1)
       const int b = bg / d.Hp, g = bg % d.Hp;
       const int ngroups = (item.count + kPG - 1) / kPG;
       for (int gi = 0; gi < ngroups; ++gi, ++i) {
-        const int bb = (int)(i & 1);
+        const int bb = (int)(i & 1), qb = (int)(i % kQPB);
         const int gcount = min(kPG, item.count - gi * kPG);
         __syncwarp();
-        if (!mbar_wait_warp(&sh->fl_full[bb], par(i >> 1), A.status)) {
+        // (qp_full: acquire the gather's token list of this buffer; already complete)
+        if (!mbar_wait_warp(&sh->fl_full[bb], par(i >> 1), A.status) ||
+            !mbar_wait_warp(&sh->qp_full[qb], par(i / kQPB), A.status)) {
           ok = false;
           break;
         }
@@ -853,12 +871,12 @@ __global__ void __launch_bounds__(384, 1)
         for (int it2 = 0; it2 < kPG / 4; ++it2) {
           const int k = it2 * 4 + lane / 8, c4 = lane % 8;
           const float4 v = *reinterpret_cast<const float4*>(stg + k * 32 + 4 * c4);
-          const int t = k < gcount ? sh->tok[bb][k] : -1;
+          const int t = k < gcount ? sh->tokq[qb][k] : -1;
           red_add_v4_if(t >= 0,
                         A.dqp + (((size_t)b * d.S + (t < 0 ? 0 : t)) * d.Hp + g) * kD + w4 * 32 + 4 * c4, v);
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sh->meta_free[bb]);  // token metadata of this buffer read
+        if (lane == 0) mbar_arrive(&sh->qp_empty[qb]);  // token list of this buffer read
       }
     }
   }
@@ -879,7 +897,7 @@ void attn_bwd_g(const CUtensorMap& mk, const CUtensorMap& mv, const MainArgs& a,
 }
 template <bool kDense>
 void proxy_bwd_g(const CUtensorMap& mkp, const ProxyArgs& a, cudaStream_t st) {
-  const size_t smem = sizeof(ProxyShared) + 1024 + (size_t)kKV + 2 * (size_t)kRT + 2 * (size_t)kST +
+  const size_t smem = sizeof(ProxyShared) + 1024 + (size_t)kKV + kQPB * (size_t)kRT + 2 * (size_t)kST +
                       2 * (size_t)kPG * kBlock * 4 + 4 * (size_t)kPG * 32 * 4;
   cudaFuncSetAttribute(proxy_bwd_kernel<kDense>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        (int)smem);
@@ -944,7 +962,7 @@ bool launch_attn_bwd(const Dims& d, bool dense, const void* q, const void* k, co
 }
 
 bool launch_proxy_bwd(const Dims& d, bool dense, const void* qp, const void* kp,
-                      const float* lse_px, const float* pbar, float kl_grad, const int* seg_offset,
+                      const float* lpxe, const float* pbar, float kl_grad, const int* seg_offset,
                       const int* entries, const Item* items, const int* n_items,
                       long long max_items, float* dqp_acc, float* dkp_acc, unsigned* status,
                       cudaStream_t st) {
@@ -956,7 +974,7 @@ bool launch_proxy_bwd(const Dims& d, bool dense, const void* qp, const void* kp,
   ProxyArgs a;
   a.d = d;
   a.qp = (const bf16*)qp;
-  a.lse_px = lse_px;
+  a.lpxe = lpxe;
   a.pbar = pbar;
   a.cz = (float)((double)kl_grad / ((double)d.B * d.S * d.Hp));
   a.seg_offset = seg_offset;

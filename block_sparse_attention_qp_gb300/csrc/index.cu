@@ -167,6 +167,24 @@ __global__ void items_kernel(Dims d, int dense, const int* __restrict__ seg_coun
   }
 }
 
+// Proxy log-normaliser of every list entry, in entry order: lpxe[e] = LSE_px(b, g, t(e)) * log2 e,
+// so the proxy-gradient pass reads it with the entry, without a dependent gather.
+__global__ void entry_lse_kernel(Dims d, int dense, const int* __restrict__ seg_count,
+                                 const int* __restrict__ seg_offset, const int* __restrict__ entries,
+                                 const float* __restrict__ lse_px, float* __restrict__ lpxe) {
+  const long long seg = blockIdx.x;
+  const long long len = list_len(d, dense, seg_count, seg);
+  if (len == 0) return;
+  const long long base = seg_offset[seg];
+  const long long bg = (seg % d.nseg()) / d.nblk;  // b * Hp + g
+  const float* row = lse_px + bg * d.S;
+  const long long t0 = dense ? dense_first(d, seg) : 0;
+  for (long long k = threadIdx.x; k < len; k += blockDim.x) {
+    const long long t = dense ? t0 + k : (long long)(entries[base + k] >> 8);
+    lpxe[base + k] = row[t] * kLog2e;
+  }
+}
+
 __global__ void convert_kernel(const float4* __restrict__ src, uint2* __restrict__ dst, long long n4) {
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4;
        i += (long long)gridDim.x * blockDim.x) {
@@ -220,6 +238,12 @@ void launch_items(const Dims& d, bool dense, const int* seg_count, const int* se
                   unsigned* status, cudaStream_t st) {
   items_kernel<<<(unsigned)d.nlist(), 128, 0, st>>>(d, dense ? 1 : 0, seg_count, seg_offset, spec,
                                                     item_offset, items, max_items, status);
+}
+
+void launch_entry_lse(const Dims& d, bool dense, const int* seg_count, const int* seg_offset,
+                      const int* entries, const float* lse_px, float* lpxe, cudaStream_t st) {
+  entry_lse_kernel<<<(unsigned)d.nlist(), 128, 0, st>>>(d, dense ? 1 : 0, seg_count, seg_offset,
+                                                         entries, lse_px, lpxe);
 }
 
 void launch_convert(const float* src, void* dst, long long n, cudaStream_t st) {

@@ -43,6 +43,10 @@ void launch_items(const Dims& d, bool dense, const int* seg_count, const int* se
                   const ItemSpec& spec, const int* item_offset, Item* items, long long max_items,
                   unsigned* status, cudaStream_t st);
 
+// lpxe[e] = LSE_px of entry e's token x log2(e), in entry order (dense: the lists' implicit tokens).
+void launch_entry_lse(const Dims& d, bool dense, const int* seg_count, const int* seg_offset,
+                      const int* entries, const float* lse_px, float* lpxe, cudaStream_t st);
+
 // ---------------------------------------------------------------- proxy top-k (topk.cu)
 // Returns false if the TMA tensor maps could not be created (driver entry point missing).
 bool launch_proxy_topk(const Dims& d, const void* qp, const void* kp, int32_t* idx,
@@ -85,7 +89,7 @@ bool launch_attn_bwd(const Dims& d, bool dense, const void* q, const void* k, co
                      cudaStream_t st);
 // Proxy gradients (dQp, dKp into fp32 accumulators) of the KL term from pbar.
 bool launch_proxy_bwd(const Dims& d, bool dense, const void* qp, const void* kp,
-                      const float* lse_px, const float* pbar, float kl_grad, const int* seg_offset,
+                      const float* lpxe, const float* pbar, float kl_grad, const int* seg_offset,
                       const int* entries, const Item* items, const int* n_items,
                       long long max_items, float* dqp_acc, float* dkp_acc, unsigned* status,
                       cudaStream_t st);
