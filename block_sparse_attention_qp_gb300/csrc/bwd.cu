@@ -25,9 +25,9 @@
 //   dKp += dz^T Qp (tensor memory, per item),  dQp^T = Kp^T dz^T (per group) -> fp32 atomics.
 // Causality everywhere: key j contributes to token t only when j <= t.
 //
-// Roles of attn_bwd_kernel (256 threads): warp 0 TMA loads of K/V and tensor-memory ownership,
-// warp 1 the MMA issuer, warp 2 gathers the tile's Q / dO rows with cp.async, warp 3 issues the dQ
-// bulk reductions, warps 4-7 softmax / epilogue.  Tensor memory (512 columns): SB0, SB1 (S^T,
+// Roles of attn_bwd_kernel (352 threads): warp 0 TMA loads of K/V and tensor-memory ownership,
+// warp 1 the MMA issuer, warps 2 and 8-10 gather the tile's Q / dO rows with cp.async, warp 3
+// issues the dQ bulk reductions, warps 4-7 softmax / epilogue.  Tensor memory (512 columns): SB0, SB1 (S^T,
 // then P^T), DB0, DB1 (dP^T, then dQ^T), dV, dK.
 #include <math.h>
 
@@ -87,7 +87,6 @@ struct MainShared {
   float lse2[2][kTR];  // row LSE * log2(e), per tile buffer
   float drow[2][kTR];  // row D, per tile buffer
   int tok[2][kTR];     // token position of each tile token (-1: none), per tile buffer
-  int epos[2][kTR];    // list entry of each tile token, per tile buffer
   int rtok[kTR];       // token positions of the staged dQ tile
   uint64_t kv_full, kv_empty, q_full[2], q_empty[2], s_full[2], p_full[2], ph2_full[2], s_free[2],
       stage_ready, stage_free, acc_free;
@@ -141,10 +140,11 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 // Bulk add of `bytes` fp32 values from shared memory into global memory (TMA reduction).
-__device__ __forceinline__ void bulk_reduce_add(float* g, uint32_t s, uint32_t bytes) {
-  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;\n" ::"l"(g),
-               "r"(s), "r"(bytes)
-               : "memory");
+__device__ __forceinline__ void bulk_reduce_add(float* g, uint32_t s, uint32_t bytes, uint64_t pol) {
+  asm volatile(
+      "cp.reduce.async.bulk.global.shared::cta.bulk_group.L2::cache_hint.add.f32 [%0], [%1], %2, %3;\n" ::"l"(g),
+      "r"(s), "r"(bytes), "l"(pol)
+      : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read0() {
@@ -167,7 +167,7 @@ __device__ __forceinline__ long long item_base(const Dims& d, const int* seg_off
 
 // ==========================================================================================
 template <int G, bool kDense>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(352, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     MainArgs A) {
   using namespace sm100;
@@ -196,7 +196,7 @@ __global__ void __launch_bounds__(256, 1)
     mbar_init(&sh->kv_full, 1);
     mbar_init(&sh->kv_empty, 1);
     for (int x = 0; x < 2; ++x) {
-      mbar_init(&sh->q_full[x], 32);
+      mbar_init(&sh->q_full[x], 256);  // 4 gather warps x 32 lanes: a cp.async and a plain arrival each
       mbar_init(&sh->q_empty[x], 1);
       mbar_init(&sh->s_full[x], 1);
       mbar_init(&sh->p_full[x], 4);
@@ -277,12 +277,18 @@ __global__ void __launch_bounds__(256, 1)
         for (int tl = 0; tl < ntiles; ++tl, ++i) {
           const int b = (int)(i & 1);
           if (!mbar_wait(&sh->q_full[b], par(i >> 1), A.status)) { ok = false; break; }
-          if (i >= 2 && !mbar_wait(&sh->s_free[b], par((i - 2) >> 1), A.status)) { ok = false; break; }
+          // the Q / dO rows were written by other threads' cp.async (generic proxy) and are only
+          // tracked by the barrier: order them before the tensor core's (async proxy) reads
+          fence_async_smem();
           fence_after_sync();
           const uint32_t aQb = aQ + b * kRT, adOb = adO + b * kRT;
+          // SB_b last held P^T of tile i-2, read by that tile's phase 2, issued earlier
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)  // S^T = K Q^T
             mma_ss(SB0 + 64 * b, desc_kmajor(aK, 128, ks), desc_kmajor(aQb, kTR, ks), id_s, ks > 0);
+          // DB_b holds dQ^T of tile i-2 until the epilogue has read it out
+          if (i >= 2 && !mbar_wait(&sh->s_free[b], par((i - 2) >> 1), A.status)) { ok = false; break; }
+          fence_after_sync();
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)  // dP^T = V dO^T
             mma_ss(DB0 + 64 * b, desc_kmajor(aV, 128, ks), desc_kmajor(adOb, kTR, ks), id_s, ks > 0);
@@ -294,77 +300,85 @@ __global__ void __launch_bounds__(256, 1)
         mma_commit(&sh->kv_empty);
       }
     }
-  } else if (warp == 2) {
+  } else if (warp == 2 || warp >= 8) {
     // ---------------------------------------------------------------- gather: Q, dO rows
+    // Four warps (2, 8, 9, 10) each fill 16 of the tile's 64 rows with cp.async; completion is
+    // counted on q_full (one cp.async arrival and one plain arrival per lane), so a warp moves on
+    // to the next tile as soon as its copies are issued.
+    const uint64_t keep = l2_policy_evict_last();  // read again by the chunk's other blocks
+    const int gw = warp == 2 ? 0 : warp - 7;
+    constexpr int WT = 16 / G;  // tokens of one warp's 16 rows (G in {4, 8, 16})
+    const int r0 = 16 * gw;
+    const int hi = lane >> 4, ch = lane & 15;
     long long i = 0;
     for (long long it = blockIdx.x; ok && it < total; it += gridDim.x) {
       const Item item = A.items[it];
       const int bg = (int)((item.seg % d.nseg()) / d.nblk);
       const int b = bg / d.Hp, g = bg % d.Hp;
       const long long tb = item_base<kDense>(d, A.seg_offset, item);
-      const long long eb = (long long)A.seg_offset[item.seg] + item.first;
       auto load_tokens = [&](int pos0, int valid, int (&tv)[TT]) {
 #pragma unroll
         for (int x = 0; x < TT; ++x)
-          tv[x] = x < valid ? (kDense ? (int)(tb + pos0 + x) : (A.entries[tb + pos0 + x] >> 8)) : -1;
+          tv[x] = x < valid ? (kDense ? (int)(tb + pos0 + x) : (__ldg(A.entries + tb + pos0 + x) >> 8)) : -1;
       };
       const int ntiles = (item.count + TT - 1) / TT;
       int tv[TT];
       load_tokens(0, min(TT, item.count), tv);
       for (int tl = 0; tl < ntiles; ++tl, ++i) {
         const int bb = (int)(i & 1);
-        // per-row metadata (rows lane, lane + 32), then the next tile's positions
-        float ml[2], md[2];
+        int wt[WT];  // this warp's tokens
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          const int r = lane + 32 * h2;
-          int t = -1;
+        for (int j = 0; j < WT; ++j) {
+          wt[j] = -1;
 #pragma unroll
           for (int x = 0; x < TT; ++x)
-            if (x == r / G) t = tv[x];
-          const size_t hrow = ((size_t)b * d.Hq + g * G + r % G) * d.S;
-          ml[h2] = t < 0 ? 0.f : A.lse[hrow + t] * kLog2e;
-          md[h2] = t < 0 ? 0.f : A.drow[hrow + t];
+            if (x == r0 / G + j) wt[j] = tv[x];
         }
+        // row data of rows r0 + (lane & 15): lanes 0-15 LSE * log2 e, lanes 16-31 D
+        const int mr = r0 + ch;
+        int mt = -1;
+#pragma unroll
+        for (int j = 0; j < WT; ++j)
+          if (j == ch / G) mt = wt[j];
+        const size_t hrow = ((size_t)b * d.Hq + g * G + mr % G) * d.S;
+        const float mv = mt < 0 ? 0.f : (hi == 0 ? __ldg(A.lse + hrow + mt) * kLog2e : __ldg(A.drow + hrow + mt));
         int tn[TT];
         load_tokens((tl + 1) * TT, min(TT, item.count - (tl + 1) * TT), tn);
         if (i >= 2 && !mbar_wait_warp(&sh->q_empty[bb], par((i - 2) >> 1), A.status)) { ok = false; break; }
         uint8_t* dQb = sQ + bb * kRT;
         uint8_t* ddOb = sdO + bb * kRT;
 #pragma unroll
-        for (int k = 0; k < (kTR * 16) / 32; ++k) {
-          const int c = lane + 32 * k;
-          const int r = c >> 4, ch = c & 15;
-          int t = -1;
+        for (int k = 0; k < 8; ++k) {
+          const int rr = 2 * k + hi;  // row within the warp's 16
+          const int r = r0 + rr;
+          const int t = wt[(2 * k) / G];
+          const uint32_t off = (ch >> 3) * (kTR * 128) + sm100::sw128_chunk(r, ch & 7);
+          const size_t grow = (((size_t)b * d.S + (t < 0 ? 0 : t)) * d.Hq + g * G + rr % G) * kD + ch * 8;
+          cp_async16_hint(dQb + off, A.q + grow, t >= 0, keep);
+          cp_async16_hint(ddOb + off, A.dout + grow, t >= 0, keep);
+        }
+        if (hi == 0)
+          sh->lse2[bb][mr] = mv;
+        else
+          sh->drow[bb][mr] = mv;
+        if (gw == 0) {
 #pragma unroll
           for (int x = 0; x < TT; ++x)
-            if (x == r / G) t = tv[x];
-          const uint32_t off = (ch >> 3) * (kTR * 128) + sm100::sw128_chunk(r, ch & 7);
-          const size_t grow = (((size_t)b * d.S + (t < 0 ? 0 : t)) * d.Hq + g * G + r % G) * kD + ch * 8;
-          cp_async16(dQb + off, A.q + grow, t >= 0);
-          cp_async16(ddOb + off, A.dout + grow, t >= 0);
+            if (lane == x) {
+              sh->tok[bb][x] = tv[x];
+            }
         }
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          sh->lse2[bb][lane + 32 * h2] = ml[h2];
-          sh->drow[bb][lane + 32 * h2] = md[h2];
-        }
-#pragma unroll
-        for (int x = 0; x < TT; ++x)
-          if (lane == x) {
-            sh->tok[bb][x] = tv[x];
-            sh->epos[bb][x] = (int)(eb + tl * TT + x);
-          }
-        cp_async_wait_all();
-        fence_async_smem();
-        mbar_arrive(&sh->q_full[bb]);
+        cp_async_arrive(&sh->q_full[bb]);
+        mbar_arrive(&sh->q_full[bb]);  // publishes the row data and tok
 #pragma unroll
         for (int x = 0; x < TT; ++x) tv[x] = tn[x];
       }
     }
+    cp_async_wait_all();  // nothing may land after the block exits
   } else if (warp == 3) {
     // ---------------------------------------------------------------- dQ reducer
     if (lane == 0) {
+      const uint64_t keep = l2_policy_evict_last();  // dQ rows of the chunk: reduced into again
       long long ns = 0;
       for (long long it = blockIdx.x; ok && it < total; it += gridDim.x) {
         const Item item = A.items[it];
@@ -378,7 +392,7 @@ __global__ void __launch_bounds__(256, 1)
             const int t = sh->rtok[x];
             if (t >= 0)
               bulk_reduce_add(A.dq + (((size_t)b * d.S + t) * d.Hq + g * G) * kD,
-                              aSt + x * G * kD * 4, G * kD * 4);
+                              aSt + x * G * kD * 4, G * kD * 4, keep);
           }
           bulk_commit();
           bulk_wait_read0();
@@ -392,29 +406,28 @@ __global__ void __launch_bounds__(256, 1)
     const int w4 = warp - 4;
     const int kr = w4 * 32 + lane;  // key row of S^T / dP^T (TMEM lane); head-dim index of dQ^T
     const uint32_t lb = static_cast<uint32_t>(w4 * 32) << 16;
+    const uint64_t stream = l2_policy_evict_first();  // pbar rows: read once, by proxy_bwd
     long long i = 0, ns = 0;
-    int tprev[TT];
+    int tpv = -1;  // token of row-token kr of the previous tile (kr < TT)
     auto epilogue = [&](long long ti) -> bool {
       const int bb = (int)(ti & 1);
       __syncwarp();
       if (!mbar_wait_warp(&sh->ph2_full[bb], par(ti >> 1), A.status)) return false;
       fence_after_sync();
-      uint32_t r0[32], r1[32];
-      tmem_ld32(DB0 + 64 * bb + lb, r0);
-      tmem_ld32(DB0 + 64 * bb + lb + 32, r1);
-      tmem_wait_ld();
+      if (ns > 0 && !mbar_wait_warp(&sh->stage_free, par(ns - 1), A.status)) return false;
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        uint32_t r0[32];
+        __syncwarp();
+        tmem_ld32(DB0 + 64 * bb + lb + 32 * c, r0);
+        tmem_wait_ld();
+#pragma unroll
+        for (int r = 0; r < 32; ++r) stage[(32 * c + r) * kD + kr] = __uint_as_float(r0[r]) * d.scale;
+      }
       fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh->s_free[bb]);
-      if (ns > 0 && !mbar_wait_warp(&sh->stage_free, par(ns - 1), A.status)) return false;
-#pragma unroll
-      for (int r = 0; r < 32; ++r) {
-        stage[r * kD + kr] = __uint_as_float(r0[r]) * d.scale;
-        stage[(r + 32) * kD + kr] = __uint_as_float(r1[r]) * d.scale;
-      }
-#pragma unroll
-      for (int x = 0; x < TT; ++x)
-        if (kr == x) sh->rtok[x] = tprev[x];
+      if (kr < TT) sh->rtok[kr] = tpv;
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh->stage_ready);
@@ -427,6 +440,7 @@ __global__ void __launch_bounds__(256, 1)
       const int bg = (int)((item.seg % d.nseg()) / d.nblk);
       const int b = bg / d.Hp, g = bg % d.Hp;
       const int j = n * kBlock + kr;  // this thread's key
+      const long long eb = (long long)A.seg_offset[item.seg] + item.first;  // first list entry
       const int ntiles = (item.count + TT - 1) / TT;
       for (int tl = 0; tl < ntiles; ++tl, ++i) {
         const int bb = (int)(i & 1);
@@ -438,26 +452,24 @@ __global__ void __launch_bounds__(256, 1)
         }
         fence_after_sync();
         // ---- softmax of tile i
-        int tv[TT], ev[TT];
+        int tv[TT];
         bool vis[TT];
         float pb[TT];
 #pragma unroll
         for (int x = 0; x < TT; ++x) {
           tv[x] = sh->tok[bb][x];
-          ev[x] = sh->epos[bb][x];
           vis[x] = tv[x] >= 0 && j <= tv[x];
           pb[x] = 0.f;
         }
-        uint32_t rs0[32], rs1[32], rp0[32], rp1[32];
         const uint32_t SBb = SB0 + 64 * bb, DBb = DB0 + 64 * bb;
-        tmem_ld32(SBb + lb, rs0);
-        tmem_ld32(SBb + lb + 32, rs1);
-        tmem_ld32(DBb + lb, rp0);
-        tmem_ld32(DBb + lb + 32, rp1);
-        tmem_wait_ld();
         const uint32_t adSb = adS + bb * kST;
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+        for (int c = 0; c < 2; ++c) {  // 32 rows at a time (P^T of rows 0-31 lands in columns 0-15)
+          uint32_t rs[32], rp[32];
+          __syncwarp();
+          tmem_ld32(SBb + lb + 32 * c, rs);
+          tmem_ld32(DBb + lb + 32 * c, rp);
+          tmem_wait_ld();
           uint32_t pw[16], dw[16];
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4) {
@@ -470,8 +482,8 @@ __global__ void __launch_bounds__(256, 1)
             for (int e = 0; e < 4; ++e) {
               const int r = c * 32 + q4 * 4 + e;
               const int x = r / G;
-              const float sv = __uint_as_float(c == 0 ? rs0[q4 * 4 + e] : rs1[q4 * 4 + e]);
-              const float dpv = __uint_as_float(c == 0 ? rp0[q4 * 4 + e] : rp1[q4 * 4 + e]);
+              const float sv = __uint_as_float(rs[q4 * 4 + e]);
+              const float dpv = __uint_as_float(rp[q4 * 4 + e]);
               const float p = vis[x] ? ex2(sv * sl2 - lv[e]) : 0.f;
               pv[e] = p;
               dsv[e] = p * (dpv - dv4[e]);
@@ -496,11 +508,15 @@ __global__ void __launch_bounds__(256, 1)
         // teacher: mean of the G heads' probabilities of each token, one fp32 row per list entry
 #pragma unroll
         for (int x = 0; x < TT; ++x)
-          if (tv[x] >= 0) A.pbar[(size_t)ev[x] * kBlock + kr] = pb[x] * (1.f / G);
+          if (tv[x] >= 0)
+            st_global_f32_hint(A.pbar + (size_t)(eb + tl * TT + x) * kBlock + kr, pb[x] * (1.f / G), stream);
+        int tcur = -1;  // row-token kr of this tile, for its dQ epilogue
+#pragma unroll
+        for (int x = 0; x < TT; ++x)
+          if (kr == x) tcur = tv[x];
         // ---- epilogue of the previous tile
         if (tl > 0 && !epilogue(i - 1)) { ok = false; break; }
-#pragma unroll
-        for (int x = 0; x < TT; ++x) tprev[x] = tv[x];
+        tpv = tcur;
       }
       if (!ok) break;
       if (!epilogue(i - 1)) { ok = false; break; }
@@ -893,7 +909,7 @@ void attn_bwd_g(const CUtensorMap& mk, const CUtensorMap& mv, const MainArgs& a,
                       2 * (size_t)kST + kStage;
   cudaFuncSetAttribute(attn_bwd_kernel<G, kDense>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        (int)smem);
-  attn_bwd_kernel<G, kDense><<<num_sms(), 256, smem, st>>>(mk, mv, a);
+  attn_bwd_kernel<G, kDense><<<num_sms(), 352, smem, st>>>(mk, mv, a);
 }
 template <bool kDense>
 void proxy_bwd_g(const CUtensorMap& mkp, const ProxyArgs& a, cudaStream_t st) {

@@ -66,6 +66,9 @@ __device__ __forceinline__ void st_global_v4_hint(void* p, uint4 v, uint64_t pol
                "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
                : "memory");
 }
+__device__ __forceinline__ void st_global_f32_hint(float* p, float v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;\n" ::"l"(p), "f"(v), "l"(pol) : "memory");
+}
 __device__ __forceinline__ uint4 ld_global_nc_v4_hint(const void* p, uint64_t pol) {
   uint4 v;
   asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.b32 {%0, %1, %2, %3}, [%4], %5;\n"
