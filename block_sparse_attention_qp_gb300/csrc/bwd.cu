@@ -68,7 +68,9 @@ constexpr int kItemTokens = 512;  // tokens per work item
 constexpr int kKV = 128 * 128 * 2;  // one 128 x 128 bf16 tile (two SW128 panels)
 constexpr int kRT = kTR * 128 * 2;  // one 64-row x 128 bf16 tile (two panels of 64 rows)
 constexpr int kST = 128 * 128;      // dS^T / dz^T: 128 keys x 64 bf16 (one panel)
-constexpr int kStage = kTR * 128 * 4;  // 64 rows x 128 fp32
+constexpr int kQS = 3;               // Q / dO slots of attn_bwd_kernel
+constexpr int kSlot = 2 * kRT;         // one slot: Q rows then dO rows; later the tile's dQ staging
+static_assert(kTR * 128 * 4 == kSlot, "a tile's fp32 dQ staging fills exactly one Q / dO slot");
 
 struct MainArgs {
   Dims d;
@@ -84,12 +86,11 @@ struct MainArgs {
 };
 
 struct MainShared {
-  float lse2[2][kTR];  // row LSE * log2(e), per tile buffer
-  float drow[2][kTR];  // row D, per tile buffer
-  int tok[2][kTR];     // token position of each tile token (-1: none), per tile buffer
-  int rtok[kTR];       // token positions of the staged dQ tile
-  uint64_t kv_full, kv_empty, q_full[2], q_empty[2], s_full[2], p_full[2], ph2_full[2], s_free[2],
-      stage_ready, stage_free, acc_free;
+  float lse2[kQS][kTR];  // row LSE * log2(e), per slot
+  float drow[kQS][kTR];  // row D, per slot
+  int tok[kQS][kTR];     // token position of each tile token (-1: none), per slot
+  uint64_t kv_full, kv_empty, q_full[kQS], q_empty[kQS], stage_ready[kQS], s_full[2], p_full[2],
+      ph2_full[2], s_free[2], acc_free;
   uint32_t tmem;
 };
 
@@ -177,15 +178,11 @@ __global__ void __launch_bounds__(352, 1)
   extern __shared__ uint8_t smem_raw[];
   MainShared* sh = reinterpret_cast<MainShared*>(smem_raw);
   uint8_t* base = align1024(smem_raw + sizeof(MainShared));
-  uint8_t* sK = base;            // [128 keys][128 d]  (TMA)
+  uint8_t* sK = base;                  // [128 keys][128 d]  (TMA)
   uint8_t* sV = sK + kKV;
-  uint8_t* sQ = sV + kKV;        // [2][64 rows][128 d]  (gathered)
-  uint8_t* sdO = sQ + 2 * kRT;
-  uint8_t* sdS = sdO + 2 * kRT;  // [2] dS^T [128 keys][64 rows]
-  uint8_t* sSt = sdS + 2 * kST;  // dQ staging [64 rows][128 d] fp32
-  const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aQ = smem_u32(sQ), adO = smem_u32(sdO),
-                 adS = smem_u32(sdS), aSt = smem_u32(sSt);
-  float* stage = reinterpret_cast<float*>(sSt);
+  uint8_t* sSl = sV + kKV;             // [kQS] slots: Q [64 rows][128 d], dO [64 rows][128 d]
+  uint8_t* sdS = sSl + kQS * kSlot;    // [2] dS^T [128 keys][64 rows]
+  const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aSl = smem_u32(sSl), adS = smem_u32(sdS);
 
   const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
   const float sl2 = d.scale * kLog2e;
@@ -195,16 +192,17 @@ __global__ void __launch_bounds__(352, 1)
   if (tid == 0) {
     mbar_init(&sh->kv_full, 1);
     mbar_init(&sh->kv_empty, 1);
-    for (int x = 0; x < 2; ++x) {
+    for (int x = 0; x < kQS; ++x) {
       mbar_init(&sh->q_full[x], 256);  // 4 gather warps x 32 lanes: a cp.async and a plain arrival each
-      mbar_init(&sh->q_empty[x], 1);
+      mbar_init(&sh->q_empty[x], 1);   // the dQ reducer, once the staged dQ rows were read
+      mbar_init(&sh->stage_ready[x], 4);
+    }
+    for (int x = 0; x < 2; ++x) {
       mbar_init(&sh->s_full[x], 1);
       mbar_init(&sh->p_full[x], 4);
       mbar_init(&sh->ph2_full[x], 1);
       mbar_init(&sh->s_free[x], 4);
     }
-    mbar_init(&sh->stage_ready, 4);
-    mbar_init(&sh->stage_free, 1);
     mbar_init(&sh->acc_free, 4);
     mbar_fence_init();
   }
@@ -254,7 +252,7 @@ __global__ void __launch_bounds__(352, 1)
         fence_after_sync();
         const bool acc = !first_of_item;
         first_of_item = false;
-        const uint32_t aQb = aQ + b * kRT, adOb = adO + b * kRT, adSb = adS + b * kST;
+        const uint32_t aQb = aSl + (uint32_t)(ti % kQS) * kSlot, adOb = aQb + kRT, adSb = adS + b * kST;
         const uint32_t SBb = SB0 + 64 * b, DBb = DB0 + 64 * b;
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)  // dV += P^T dO  (P^T from tensor memory)
@@ -265,8 +263,7 @@ __global__ void __launch_bounds__(352, 1)
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)  // dQ^T = K^T dS^T
           mma_ss(DBb, desc_mnmajor(aK, 128, ks), desc_mnmajor(adSb, 128, ks), id_q, ks > 0);
-        mma_commit(&sh->ph2_full[b]);
-        mma_commit(&sh->q_empty[b]);
+        mma_commit(&sh->ph2_full[b]);  // also: the slot's Q / dO rows are no longer read
         return true;
       };
       for (long long it = blockIdx.x; ok && it < total; it += gridDim.x, ++ni) {
@@ -275,13 +272,13 @@ __global__ void __launch_bounds__(352, 1)
         first_of_item = true;
         const int ntiles = (item.count + TT - 1) / TT;
         for (int tl = 0; tl < ntiles; ++tl, ++i) {
-          const int b = (int)(i & 1);
-          if (!mbar_wait(&sh->q_full[b], par(i >> 1), A.status)) { ok = false; break; }
+          const int b = (int)(i & 1), sl = (int)(i % kQS);
+          if (!mbar_wait(&sh->q_full[sl], par(i / kQS), A.status)) { ok = false; break; }
           // the Q / dO rows were written by other threads' cp.async (generic proxy) and are only
           // tracked by the barrier: order them before the tensor core's (async proxy) reads
           fence_async_smem();
           fence_after_sync();
-          const uint32_t aQb = aQ + b * kRT, adOb = adO + b * kRT;
+          const uint32_t aQb = aSl + (uint32_t)sl * kSlot, adOb = aQb + kRT;
           // SB_b last held P^T of tile i-2, read by that tile's phase 2, issued earlier
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)  // S^T = K Q^T
@@ -325,7 +322,7 @@ __global__ void __launch_bounds__(352, 1)
       int tv[TT];
       load_tokens(0, min(TT, item.count), tv);
       for (int tl = 0; tl < ntiles; ++tl, ++i) {
-        const int bb = (int)(i & 1);
+        const int sl = (int)(i % kQS);
         int wt[WT];  // this warp's tokens
 #pragma unroll
         for (int j = 0; j < WT; ++j) {
@@ -344,9 +341,9 @@ __global__ void __launch_bounds__(352, 1)
         const float mv = mt < 0 ? 0.f : (hi == 0 ? __ldg(A.lse + hrow + mt) * kLog2e : __ldg(A.drow + hrow + mt));
         int tn[TT];
         load_tokens((tl + 1) * TT, min(TT, item.count - (tl + 1) * TT), tn);
-        if (i >= 2 && !mbar_wait_warp(&sh->q_empty[bb], par((i - 2) >> 1), A.status)) { ok = false; break; }
-        uint8_t* dQb = sQ + bb * kRT;
-        uint8_t* ddOb = sdO + bb * kRT;
+        if (i >= kQS && !mbar_wait_warp(&sh->q_empty[sl], par(i / kQS - 1), A.status)) { ok = false; break; }
+        uint8_t* dQb = sSl + sl * kSlot;
+        uint8_t* ddOb = dQb + kRT;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const int rr = 2 * k + hi;  // row within the warp's 16
@@ -358,18 +355,16 @@ __global__ void __launch_bounds__(352, 1)
           cp_async16_hint(ddOb + off, A.dout + grow, t >= 0, keep);
         }
         if (hi == 0)
-          sh->lse2[bb][mr] = mv;
+          sh->lse2[sl][mr] = mv;
         else
-          sh->drow[bb][mr] = mv;
+          sh->drow[sl][mr] = mv;
         if (gw == 0) {
 #pragma unroll
           for (int x = 0; x < TT; ++x)
-            if (lane == x) {
-              sh->tok[bb][x] = tv[x];
-            }
+            if (lane == x) sh->tok[sl][x] = tv[x];
         }
-        cp_async_arrive(&sh->q_full[bb]);
-        mbar_arrive(&sh->q_full[bb]);  // publishes the row data and tok
+        cp_async_arrive(&sh->q_full[sl]);
+        mbar_arrive(&sh->q_full[sl]);  // publishes the row data and tok
 #pragma unroll
         for (int x = 0; x < TT; ++x) tv[x] = tn[x];
       }
@@ -386,17 +381,19 @@ __global__ void __launch_bounds__(352, 1)
         const int b = bg / d.Hp, g = bg % d.Hp;
         const int ntiles = (item.count + TT - 1) / TT;
         for (int tl = 0; tl < ntiles; ++tl, ++ns) {
-          if (!mbar_wait(&sh->stage_ready, par(ns), A.status)) { ok = false; break; }
+          const int sl = (int)(ns % kQS);
+          if (!mbar_wait(&sh->stage_ready[sl], par(ns / kQS), A.status)) { ok = false; break; }
+          const uint32_t aSt = aSl + (uint32_t)sl * kSlot;  // the tile's dQ rows, staged in its slot
 #pragma unroll 1
           for (int x = 0; x < TT; ++x) {
-            const int t = sh->rtok[x];
+            const int t = sh->tok[sl][x];
             if (t >= 0)
               bulk_reduce_add(A.dq + (((size_t)b * d.S + t) * d.Hq + g * G) * kD,
                               aSt + x * G * kD * 4, G * kD * 4, keep);
           }
           bulk_commit();
           bulk_wait_read0();
-          mbar_arrive(&sh->stage_free);
+          mbar_arrive(&sh->q_empty[sl]);  // the slot may take the rows of tile ns + kQS
         }
       }
       bulk_wait0();
@@ -407,14 +404,15 @@ __global__ void __launch_bounds__(352, 1)
     const int kr = w4 * 32 + lane;  // key row of S^T / dP^T (TMEM lane); head-dim index of dQ^T
     const uint32_t lb = static_cast<uint32_t>(w4 * 32) << 16;
     const uint64_t stream = l2_policy_evict_first();  // pbar rows: read once, by proxy_bwd
-    long long i = 0, ns = 0;
-    int tpv = -1;  // token of row-token kr of the previous tile (kr < TT)
+    long long i = 0;
+    // dQ of tile ti: dQ^T (tensor memory) -> fp32 rows staged in the tile's own slot, whose Q / dO
+    // rows phase 2 has finished reading; the reducer warp then adds them to dQ
     auto epilogue = [&](long long ti) -> bool {
-      const int bb = (int)(ti & 1);
+      const int bb = (int)(ti & 1), sl = (int)(ti % kQS);
       __syncwarp();
       if (!mbar_wait_warp(&sh->ph2_full[bb], par(ti >> 1), A.status)) return false;
       fence_after_sync();
-      if (ns > 0 && !mbar_wait_warp(&sh->stage_free, par(ns - 1), A.status)) return false;
+      float* stage = reinterpret_cast<float*>(sSl + sl * kSlot);
 #pragma unroll 1
       for (int c = 0; c < 2; ++c) {
         uint32_t r0[32];
@@ -427,11 +425,9 @@ __global__ void __launch_bounds__(352, 1)
       fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh->s_free[bb]);
-      if (kr < TT) sh->rtok[kr] = tpv;
       fence_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sh->stage_ready);
-      ++ns;
+      if (lane == 0) mbar_arrive(&sh->stage_ready[sl]);
       return true;
     };
     for (long long it = blockIdx.x; ok && it < total; it += gridDim.x) {
@@ -443,9 +439,9 @@ __global__ void __launch_bounds__(352, 1)
       const long long eb = (long long)A.seg_offset[item.seg] + item.first;  // first list entry
       const int ntiles = (item.count + TT - 1) / TT;
       for (int tl = 0; tl < ntiles; ++tl, ++i) {
-        const int bb = (int)(i & 1);
+        const int bb = (int)(i & 1), sl = (int)(i % kQS);
         __syncwarp();
-        if (!mbar_wait_warp(&sh->q_full[bb], par(i >> 1), A.status) ||
+        if (!mbar_wait_warp(&sh->q_full[sl], par(i / kQS), A.status) ||
             !mbar_wait_warp(&sh->s_full[bb], par(i >> 1), A.status)) {
           ok = false;
           break;
@@ -457,7 +453,7 @@ __global__ void __launch_bounds__(352, 1)
         float pb[TT];
 #pragma unroll
         for (int x = 0; x < TT; ++x) {
-          tv[x] = sh->tok[bb][x];
+          tv[x] = sh->tok[sl][x];
           vis[x] = tv[x] >= 0 && j <= tv[x];
           pb[x] = 0.f;
         }
@@ -473,8 +469,8 @@ __global__ void __launch_bounds__(352, 1)
           uint32_t pw[16], dw[16];
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4) {
-            const float4 l4 = reinterpret_cast<const float4*>(sh->lse2[bb])[c * 8 + q4];
-            const float4 d4 = reinterpret_cast<const float4*>(sh->drow[bb])[c * 8 + q4];
+            const float4 l4 = reinterpret_cast<const float4*>(sh->lse2[sl])[c * 8 + q4];
+            const float4 d4 = reinterpret_cast<const float4*>(sh->drow[sl])[c * 8 + q4];
             const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
             const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
             float pv[4], dsv[4];
@@ -510,13 +506,8 @@ __global__ void __launch_bounds__(352, 1)
         for (int x = 0; x < TT; ++x)
           if (tv[x] >= 0)
             st_global_f32_hint(A.pbar + (size_t)(eb + tl * TT + x) * kBlock + kr, pb[x] * (1.f / G), stream);
-        int tcur = -1;  // row-token kr of this tile, for its dQ epilogue
-#pragma unroll
-        for (int x = 0; x < TT; ++x)
-          if (kr == x) tcur = tv[x];
         // ---- epilogue of the previous tile
         if (tl > 0 && !epilogue(i - 1)) { ok = false; break; }
-        tpv = tcur;
       }
       if (!ok) break;
       if (!epilogue(i - 1)) { ok = false; break; }
@@ -905,8 +896,8 @@ __global__ void __launch_bounds__(384, 1)
 namespace {
 template <int G, bool kDense>
 void attn_bwd_g(const CUtensorMap& mk, const CUtensorMap& mv, const MainArgs& a, cudaStream_t st) {
-  const size_t smem = sizeof(MainShared) + 1024 + 2 * (size_t)kKV + 4 * (size_t)kRT +
-                      2 * (size_t)kST + kStage;
+  const size_t smem = sizeof(MainShared) + 1024 + 2 * (size_t)kKV + kQS * (size_t)kSlot +
+                      2 * (size_t)kST;
   cudaFuncSetAttribute(attn_bwd_kernel<G, kDense>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        (int)smem);
   attn_bwd_kernel<G, kDense><<<num_sms(), 352, smem, st>>>(mk, mv, a);
