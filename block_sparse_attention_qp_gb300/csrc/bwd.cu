@@ -71,6 +71,7 @@ constexpr int kST = 128 * 128;      // dS^T / dz^T: 128 keys x 64 bf16 (one pane
 constexpr int kQS = 3;               // Q / dO slots of attn_bwd_kernel
 constexpr int kSlot = 2 * kRT;         // one slot: Q rows then dO rows; later the tile's dQ staging
 static_assert(kTR * 128 * 4 == kSlot, "a tile's fp32 dQ staging fills exactly one Q / dO slot");
+constexpr int kIR = 4;                 // work-item ring: item numbers handed out to the block's roles
 
 struct MainArgs {
   Dims d;
@@ -83,14 +84,16 @@ struct MainArgs {
   long long max_items;
   float *dq, *dk, *dv, *pbar;
   unsigned* status;
+  int* sched;  // work-item counter (zero at launch): blocks take items in order as they get free
 };
 
 struct MainShared {
   float lse2[kQS][kTR];  // row LSE * log2(e), per slot
   float drow[kQS][kTR];  // row D, per slot
   int tok[kQS][kTR];     // token position of each tile token (-1: none), per slot
+  int it_ring[kIR];       // item numbers taken by this block, in order (>= total: no more)
   uint64_t kv_full, kv_empty, q_full[kQS], q_empty[kQS], stage_ready[kQS], s_full[2], p_full[2],
-      ph2_full[2], s_free[2], acc_free;
+      ph2_full[2], s_free[2], acc_free, it_full[kIR], it_empty[kIR];
   uint32_t tmem;
 };
 
@@ -204,6 +207,10 @@ __global__ void __launch_bounds__(352, 1)
       mbar_init(&sh->s_free[x], 4);
     }
     mbar_init(&sh->acc_free, 4);
+    for (int x = 0; x < kIR; ++x) {
+      mbar_init(&sh->it_full[x], 1);
+      mbar_init(&sh->it_empty[x], 10);  // MMA, 4 gather warps, reducer, 4 softmax warps
+    }
     mbar_fence_init();
   }
   if (warp == 0) {
@@ -216,14 +223,46 @@ __global__ void __launch_bounds__(352, 1)
   const uint32_t tmem = sh->tmem;
   const uint32_t SB0 = tmem, DB0 = tmem + 128, RV = tmem + 256, RK = tmem + 384;
   bool ok = true;
+  // Item number ni of this block, for one thread / for a whole warp.  Items are handed out in list
+  // order to whichever block asks next, so the blocks stay within a short window of the list (the
+  // rows of one sequence chunk stay in L2) however unevenly long the items are.
+  auto take_item1 = [&](long long ni, int& v) -> bool {
+    const int x = (int)(ni % kIR);
+    if (!mbar_wait(&sh->it_full[x], par(ni / kIR), A.status)) return false;
+    v = sh->it_ring[x];
+    mbar_arrive(&sh->it_empty[x]);
+    return true;
+  };
+  auto take_itemw = [&](long long ni, int& v) -> bool {
+    const int x = (int)(ni % kIR);
+    if (!mbar_wait_warp(&sh->it_full[x], par(ni / kIR), A.status)) return false;
+    v = sh->it_ring[x];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh->it_empty[x]);
+    return true;
+  };
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA: K, V per item
     if (lane == 0) {
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
-      long long ni = 0;
-      for (long long it = blockIdx.x; it < total; it += gridDim.x, ++ni) {
+      // item numbers are published up to two items ahead of the K / V loads
+      long long pub = 0;
+      bool last = false;
+      for (long long ni = 0;; ++ni) {
+        while (!last && pub < ni + 2) {
+          const int x = (int)(pub % kIR);
+          if (pub >= kIR && !mbar_wait(&sh->it_empty[x], par(pub / kIR - 1), A.status)) break;
+          const int v = atomicAdd(A.sched, 1);
+          sh->it_ring[x] = v;
+          mbar_arrive(&sh->it_full[x]);
+          last = v >= total;
+          ++pub;
+        }
+        if (pub <= ni) break;  // a wait gave up
+        const int it = sh->it_ring[ni % kIR];
+        if (it >= total) break;
         const Item item = A.items[it];
         const int n = item.seg % d.nblk;
         const int bg = (int)((item.seg % d.nseg()) / d.nblk);
@@ -266,7 +305,10 @@ __global__ void __launch_bounds__(352, 1)
         mma_commit(&sh->ph2_full[b]);  // also: the slot's Q / dO rows are no longer read
         return true;
       };
-      for (long long it = blockIdx.x; ok && it < total; it += gridDim.x, ++ni) {
+      for (;; ++ni) {
+        int it;
+        if (!take_item1(ni, it)) { ok = false; break; }
+        if (it >= total) break;
         const Item item = A.items[it];
         if (!mbar_wait(&sh->kv_full, par(ni), A.status)) { ok = false; break; }
         first_of_item = true;
@@ -308,7 +350,10 @@ __global__ void __launch_bounds__(352, 1)
     const int r0 = 16 * gw;
     const int hi = lane >> 4, ch = lane & 15;
     long long i = 0;
-    for (long long it = blockIdx.x; ok && it < total; it += gridDim.x) {
+    for (long long ni = 0; ok; ++ni) {
+      int it;
+      if (!take_itemw(ni, it)) { ok = false; break; }
+      if (it >= total) break;
       const Item item = A.items[it];
       const int bg = (int)((item.seg % d.nseg()) / d.nblk);
       const int b = bg / d.Hp, g = bg % d.Hp;
@@ -375,7 +420,10 @@ __global__ void __launch_bounds__(352, 1)
     if (lane == 0) {
       const uint64_t keep = l2_policy_evict_last();  // dQ rows of the chunk: reduced into again
       long long ns = 0;
-      for (long long it = blockIdx.x; ok && it < total; it += gridDim.x) {
+      for (long long ni = 0; ok; ++ni) {
+        int it;
+        if (!take_item1(ni, it)) { ok = false; break; }
+        if (it >= total) break;
         const Item item = A.items[it];
         const int bg = (int)((item.seg % d.nseg()) / d.nblk);
         const int b = bg / d.Hp, g = bg % d.Hp;
@@ -430,7 +478,10 @@ __global__ void __launch_bounds__(352, 1)
       if (lane == 0) mbar_arrive(&sh->stage_ready[sl]);
       return true;
     };
-    for (long long it = blockIdx.x; ok && it < total; it += gridDim.x) {
+    for (long long ni = 0; ok; ++ni) {
+      int it;
+      if (!take_itemw(ni, it)) { ok = false; break; }
+      if (it >= total) break;
       const Item item = A.items[it];
       const int n = item.seg % d.nblk;
       const int bg = (int)((item.seg % d.nseg()) / d.nblk);
@@ -950,6 +1001,8 @@ bool launch_attn_bwd(const Dims& d, bool dense, const void* q, const void* k, co
   a.dv = dv_acc;
   a.pbar = pbar;
   a.status = status;
+  a.sched = reinterpret_cast<int*>(status + kSchedAttnBwd);
+  cudaMemsetAsync(a.sched, 0, sizeof(int), st);
 #define MSA_BWD_CASE(GG)                    \
   case GG:                                  \
     if (dense)                              \

@@ -25,6 +25,11 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr unsigned kStatusBadIndex = 1u;    // a block index out of range / not ascending
 constexpr unsigned kStatusBadItems = 2u;    // work list larger than its reserved space
 constexpr unsigned kStatusTimeout = 4u;     // a bounded device wait expired
+// Words 8.. of the workspace's status area: work-item counters of the persistent kernels, each
+// zeroed on the launch stream right before its kernel starts.
+constexpr int kSchedAttnBwd = 8;
+constexpr int kSchedProxyBwd = 9;
+constexpr int kSchedAttnFwd = 10;
 
 typedef __nv_bfloat16 bf16;
 
