@@ -33,6 +33,7 @@ constexpr int kFwdItemTiles = 8;               // tiles per work item
 constexpr int kRing = 3;                       // K/V ring slots (one 128 x 128 tile each)
 constexpr int kQBuf = 3;                       // gathered Q buffers
 constexpr int kStageWarp = 32 * 64;            // epilogue staging per warp: 32 rows x 64 bytes
+constexpr int kIR = 4;                         // work-item ring: item numbers for the block's roles
 
 struct FwdArgs {
   Dims d;
@@ -45,13 +46,15 @@ struct FwdArgs {
   bf16* opart;
   float* lpart;
   unsigned* status;
+  int* sched;  // work-item counter (zero at launch): blocks take items in order as they get free
 };
 
 struct FwdShared {
   int tok[kQBuf][kFwdRows];     // token of each tile token (-1: none), per Q buffer
   int slot[kQBuf][kFwdRows];    // its selection slot
+  int it_ring[kIR];             // item numbers taken by this block, in order (>= total: no more)
   uint64_t kv_full[kRing], kv_empty[kRing], q_full[kQBuf], q_empty[kQBuf], meta_free[kQBuf],
-      s_full[2], p_full[2], o_full[2], o_free[2], mma_done;
+      s_full[2], p_full[2], o_full[2], o_free[2], mma_done, it_full[kIR], it_empty[kIR];
   uint32_t tmem;
 };
 
@@ -113,6 +116,10 @@ __global__ void __launch_bounds__(448, 1)
       mbar_init(&sh->o_free[x], 4);
     }
     mbar_init(&sh->mma_done, 1);
+    for (int x = 0; x < kIR; ++x) {
+      mbar_init(&sh->it_full[x], 1);
+      mbar_init(&sh->it_empty[x], 13);  // MMA, 4 gather warps, 8 softmax warps
+    }
     mbar_fence_init();
   }
   if (warp == 0) {
@@ -125,6 +132,17 @@ __global__ void __launch_bounds__(448, 1)
   const uint32_t tmem = sh->tmem;
   const uint32_t S0 = tmem, O0 = tmem + 256;  // S_b = S0 + 128 b, O_b = O0 + 128 b
   bool ok = true;
+  // Item number ni of this block, for a whole warp.  Items are handed out in list order to
+  // whichever block asks next, so the blocks stay within a short window of the list (the query
+  // rows of one sequence chunk stay in L2) however unevenly long the items are.
+  auto take_item = [&](long long ni, int& v) -> bool {
+    const int x = (int)(ni % kIR);
+    if (!mbar_wait_warp(&sh->it_full[x], par(ni / kIR), A.status)) return false;
+    v = sh->it_ring[x];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh->it_empty[x]);
+    return true;
+  };
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA: K, V per item
@@ -134,7 +152,31 @@ __global__ void __launch_bounds__(448, 1)
       tma_prefetch_desc(&tm_v);
     }
     long long nl = 0;  // loads issued
-    for (long long it = blockIdx.x; ok && it < total; it += gridDim.x) {
+    // item numbers are published up to two items ahead of the K / V loads
+    long long pub = 0;
+    bool last = false;
+    for (long long ni = 0; ok; ++ni) {
+      while (!last && pub < ni + 2) {
+        const int x = (int)(pub % kIR);
+        if (pub >= kIR && !mbar_wait_warp(&sh->it_empty[x], par(pub / kIR - 1), A.status)) {
+          ok = false;
+          break;
+        }
+        int v = 0;
+        if (lane == 0) {
+          v = atomicAdd(A.sched, 1);
+          sh->it_ring[x] = v;
+          mbar_arrive(&sh->it_full[x]);
+        }
+        v = __shfl_sync(0xffffffffu, v, 0);
+        last = v >= total;
+        ++pub;
+      }
+      if (!ok) break;
+      int it = 0;
+      if (lane == 0) it = sh->it_ring[ni % kIR];
+      it = __shfl_sync(0xffffffffu, it, 0);
+      if (it >= total) break;
       const Item item = A.items[it];
       const int n = item.seg % d.nblk;
       const int bg = (int)((item.seg % d.nseg()) / d.nblk);
@@ -190,7 +232,10 @@ __global__ void __launch_bounds__(448, 1)
       return true;
     };
     long long ni = 0, i = 0;
-    for (long long it = blockIdx.x; ok && it < total; it += gridDim.x, ++ni) {
+    for (;; ++ni) {
+      int it;
+      if (!take_item(ni, it)) { ok = false; break; }
+      if (it >= total) break;
       const Item item = A.items[it];
       const RingPos kp = ring_pos(2 * ni), vp = ring_pos(2 * ni + 1);
       if (!mbar_wait_warp(&sh->kv_full[kp.slot], kp.parity, A.status)) { ok = false; break; }
@@ -240,11 +285,11 @@ __global__ void __launch_bounds__(448, 1)
     constexpr int XT = (32 + G - 1) / G;             // tokens per gather warp (G = 1: 32)
     const int x0 = gw * 32 / G;                      // first token of this warp
     const uint64_t pol_q = l2_policy_evict_last();  // each query row is read once per selected block
-    long long it = blockIdx.x;
-    if (it < total) {
+    long long gni = 0;
+    int it = 0;
+    if (!take_item(gni, it)) ok = false;
+    if (ok && it < total) {
       Item cur = A.items[it];
-      long long nit = it + gridDim.x;
-      Item nxt = nit < total ? A.items[nit] : cur;
       int tl = 0;
       auto load_e = [=](int base, int count, int tile) -> int {
         const int pos = tile * TT + x0 + lane;
@@ -286,13 +331,11 @@ __global__ void __launch_bounds__(448, 1)
           ++tl;
           e = load_e(cur.base, cur.count, tl);
         } else {
-          it = nit;
+          if (!take_item(++gni, it)) { ok = false; break; }
           if (it >= total) break;
-          cur = nxt;
+          cur = A.items[it];
           tl = 0;
           e = load_e(cur.base, cur.count, 0);
-          nit = it + gridDim.x;
-          if (nit < total) nxt = A.items[nit];
         }
       }
       cp_async_wait_all();  // nothing may land after the block exits
@@ -309,7 +352,10 @@ __global__ void __launch_bounds__(448, 1)
     const uint32_t stw = aSt + (warp - 4) * kStageWarp;  // this warp's staging: [32 rows][64 bytes]
     const uint64_t pol_part = l2_policy_evict_first();    // partials are read once, by the combine
     long long i = 0;
-    for (long long it = blockIdx.x; ok && it < total; it += gridDim.x) {
+    for (long long ni = 0; ok; ++ni) {
+      int it;
+      if (!take_item(ni, it)) { ok = false; break; }
+      if (it >= total) break;
       const Item item = A.items[it];
       const int n = item.seg % d.nblk;
       const int bg = (int)((item.seg % d.nseg()) / d.nblk);
@@ -490,6 +536,8 @@ bool launch_attn_fwd(const Dims& d, const void* q, const void* k, const void* v,
   a.opart = (bf16*)opart;
   a.lpart = lpart;
   a.status = status;
+  a.sched = reinterpret_cast<int*>(status + kSchedAttnFwd);
+  cudaMemsetAsync(a.sched, 0, sizeof(int), st);
   switch (d.G) {
     case 1: attn_fwd_g<1>(mk, mv, a, st); break;
     case 2: attn_fwd_g<2>(mk, mv, a, st); break;

@@ -109,6 +109,7 @@ struct ProxyArgs {
   long long max_items;
   float *dqp, *dkp;
   unsigned* status;
+  int* sched;  // work-item counter (zero at launch)
 };
 
 constexpr int kQPB = 3;  // proxy query row buffers
@@ -117,8 +118,9 @@ struct ProxyShared {
   int tok[2][kPG];     // per teacher buffer (read by the dz warps)
   float lpx2[2][kPG];
   int tokq[kQPB][kPG];  // per query-row buffer (read by the dQp-flush warps)
+  int it_ring[kIR];  // item numbers taken by this block, in order (>= total: no more)
   uint64_t kp_full, kp_empty, qp_full[kQPB], qp_empty[kQPB], pb_full[2], meta_free[2], z_full[2],
-      dz_full, fl_full[2], fl_free, acc_free;
+      dz_full, fl_full[2], fl_free, acc_free, it_full[kIR], it_empty[kIR];
   uint32_t tmem;
 };
 
@@ -635,6 +637,10 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(&sh->dz_full, 4);
     mbar_init(&sh->fl_free, 4);
     mbar_init(&sh->acc_free, 4);
+    for (int x = 0; x < kIR; ++x) {
+      mbar_init(&sh->it_full[x], 1);
+      mbar_init(&sh->it_empty[x], 11);  // MMA, 2 gather warps, 4 dz warps, 4 flush warps
+    }
     mbar_fence_init();
   }
   if (warp == 0) {
@@ -647,12 +653,43 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tmem = sh->tmem;
   const uint32_t RZ0 = tmem, RQ = tmem + 128, RKP = tmem + 256;  // RZ_b = RZ0 + 64 b
   bool ok = true;
+  // item number ni of this block (handed out in list order by a shared counter), for one thread /
+  // for a whole warp
+  auto take_item1 = [&](long long ni, int& v) -> bool {
+    const int x = (int)(ni % kIR);
+    if (!mbar_wait(&sh->it_full[x], par(ni / kIR), A.status)) return false;
+    v = sh->it_ring[x];
+    mbar_arrive(&sh->it_empty[x]);
+    return true;
+  };
+  auto take_itemw = [&](long long ni, int& v) -> bool {
+    const int x = (int)(ni % kIR);
+    if (!mbar_wait_warp(&sh->it_full[x], par(ni / kIR), A.status)) return false;
+    v = sh->it_ring[x];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh->it_empty[x]);
+    return true;
+  };
 
   if (warp == 0) {
     if (lane == 0) {
       tma_prefetch_desc(&tm_kp);
-      long long ni = 0;
-      for (long long it = blockIdx.x; it < total; it += gridDim.x, ++ni) {
+      // item numbers are published up to two items ahead of the proxy-key loads
+      long long pub = 0;
+      bool last = false;
+      for (long long ni = 0;; ++ni) {
+        while (!last && pub < ni + 2) {
+          const int x = (int)(pub % kIR);
+          if (pub >= kIR && !mbar_wait(&sh->it_empty[x], par(pub / kIR - 1), A.status)) break;
+          const int v = atomicAdd(A.sched, 1);
+          sh->it_ring[x] = v;
+          mbar_arrive(&sh->it_full[x]);
+          last = v >= total;
+          ++pub;
+        }
+        if (pub <= ni) break;  // a wait gave up
+        const int it = sh->it_ring[ni % kIR];
+        if (it >= total) break;
         const Item item = A.items[it];
         const int n = item.seg % d.nblk;
         const int bg = (int)((item.seg % d.nseg()) / d.nblk);
@@ -690,7 +727,10 @@ __global__ void __launch_bounds__(384, 1)
         if (last) mma_commit(&sh->kp_empty);
         return true;
       };
-      for (long long it = blockIdx.x; ok && it < total; it += gridDim.x, ++ni) {
+      for (;; ++ni) {
+        int it;
+        if (!take_item1(ni, it)) { ok = false; break; }
+        if (it >= total) break;
         const Item item = A.items[it];
         if (!mbar_wait(&sh->kp_full, par(ni), A.status)) { ok = false; break; }
         const int ngroups = (item.count + kPG - 1) / kPG;
@@ -721,11 +761,11 @@ __global__ void __launch_bounds__(384, 1)
     // cp.async into one of three buffers, released by the MMA and the dQp-flush warps.  The next
     // group's tokens and proxy normalisers are loaded one step ahead.
     const int w = warp - 2;
-    long long it = blockIdx.x;
-    if (it < total) {
+    long long gni = 0;
+    int it = 0;
+    if (!take_itemw(gni, it)) ok = false;
+    if (ok && it < total) {
       Item cur = A.items[it];
-      long long nit = it + gridDim.x;
-      Item nxt = nit < total ? A.items[nit] : cur;
       int gi = 0;
       // token and proxy log-normaliser (x log2 e) of group row 32 w + lane of group `grp`
       auto load_row = [=](const Item& item, int grp, float& lp) -> int {
@@ -792,13 +832,11 @@ __global__ void __launch_bounds__(384, 1)
           ++gi;
           t_next = load_row(cur, gi, lp_next);
         } else {
-          it = nit;
+          if (!take_itemw(++gni, it)) { ok = false; break; }
           if (it >= total) break;
-          cur = nxt;
+          cur = A.items[it];
           gi = 0;
           t_next = load_row(cur, 0, lp_next);
-          nit = it + gridDim.x;
-          if (nit < total) nxt = A.items[nit];
         }
       }
       cp_async_wait_all();  // nothing may land after the block exits
@@ -812,7 +850,10 @@ __global__ void __launch_bounds__(384, 1)
     const int kr = w4 * 32 + lane;  // key (tensor-memory lane of z^T and dKp)
     const uint32_t lb = static_cast<uint32_t>(w4 * 32) << 16;
     long long i = 0;
-    for (long long it = blockIdx.x; ok && it < total; it += gridDim.x) {
+    for (long long ni = 0; ok; ++ni) {
+      int it;
+      if (!take_itemw(ni, it)) { ok = false; break; }
+      if (it >= total) break;
       const Item item = A.items[it];
       const int n = item.seg % d.nblk;
       const int bg = (int)((item.seg % d.nseg()) / d.nblk);
@@ -898,7 +939,10 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t lb = static_cast<uint32_t>(w4 * 32) << 16;
     float* stg = sStg + w4 * (kPG * 32);
     long long i = 0;
-    for (long long it = blockIdx.x; ok && it < total; it += gridDim.x) {
+    for (long long ni = 0; ok; ++ni) {
+      int it;
+      if (!take_itemw(ni, it)) { ok = false; break; }
+      if (it >= total) break;
       const Item item = A.items[it];
       const int bg = (int)((item.seg % d.nseg()) / d.nblk);
       const int b = bg / d.Hp, g = bg % d.Hp;
@@ -1045,6 +1089,8 @@ bool launch_proxy_bwd(const Dims& d, bool dense, const void* qp, const void* kp,
   a.dqp = dqp_acc;
   a.dkp = dkp_acc;
   a.status = status;
+  a.sched = reinterpret_cast<int*>(status + kSchedProxyBwd);
+  cudaMemsetAsync(a.sched, 0, sizeof(int), st);
   if (dense)
     proxy_bwd_g<true>(mkp, a, st);
   else
