@@ -75,7 +75,7 @@ size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 struct Plan {
   size_t status = 0, totals = 0, seg_count = 0, seg_offset = 0, seg_cursor = 0, entries = 0;
   size_t io0 = 0, io1 = 0, items0 = 0, items1 = 0;
-  size_t opart = 0, lpart = 0, lpx_part = 0, lse_px = 0, lpxe = 0, drow = 0, pbar = 0;
+  size_t opart = 0, lpart = 0, lpx_part = 0, lse_px = 0, lpxe = 0, rowm = 0, emeta = 0, pbar = 0;
   size_t dq = 0, dk = 0, dv = 0, dqp = 0, dkp = 0;
   size_t bytes = 0;
   long long max0 = 0, max1 = 0;
@@ -173,9 +173,10 @@ Plan make_plan(const Dims& d, int op) {
       p.lpx_part = c.take((size_t)rows_p * d.top_k * sizeof(float));
     }
     p.lse_px = c.take((size_t)rows_p * sizeof(float));
-    p.drow = c.take((size_t)rows_q * sizeof(float));
+    p.rowm = c.take((size_t)rows_q * sizeof(float2));  // {LSE log2 e, D} per query row
     p.pbar = c.take((size_t)ent * kBlock * sizeof(float));  // teacher rows, one per list entry
     p.lpxe = c.take((size_t)ent * sizeof(float));            // proxy log-normaliser per entry
+    p.emeta = c.take((size_t)ent * d.G * sizeof(float2));    // rowm per entry and head
     p.dq = c.take((size_t)rows_q * kD * sizeof(float));
     p.dk = c.take((size_t)rows_kv * kD * sizeof(float));
     p.dv = c.take((size_t)rows_kv * kD * sizeof(float));
@@ -411,7 +412,7 @@ int msa_backward(const msa_shape_t* shape, const void* q, const void* k, const v
   cudaMemsetAsync(at<char>(workspace, p.status), 0, sizeof(unsigned), st);
   zero_grads(d, p, workspace, st);
   build_lists(d, p, block_idx, workspace, 2, st);
-  timed("bwd_rowdot", st, [&] { launch_bwd_rowdot(d, o, dout, at<float>(workspace, p.drow), st); });
+  timed("bwd_rowdot", st, [&] { launch_bwd_rowdot(d, o, dout, lse, at<float2>(workspace, p.rowm), st); });
   timed("proxy_lse", st, [&] {
     launch_proxy_lse_sparse(d, qp, kp, at<int>(workspace, p.seg_offset),
                             at<int>(workspace, p.entries), at<Item>(workspace, p.items0),
@@ -422,19 +423,20 @@ int msa_backward(const msa_shape_t* shape, const void* q, const void* k, const v
     launch_proxy_lse_combine(d, block_idx, at<float>(workspace, p.lpx_part),
                              at<float>(workspace, p.lse_px), st);
   });
+  timed("entry_meta", st, [&] {
+    launch_entry_meta(d, false, at<int>(workspace, p.seg_count), at<int>(workspace, p.seg_offset),
+                      at<int>(workspace, p.entries), at<float>(workspace, p.lse_px),
+                      at<float2>(workspace, p.rowm), at<float>(workspace, p.lpxe),
+                      at<float2>(workspace, p.emeta), st);
+  });
   bool ok = true;
   timed("attn_bwd", st, [&] {
-    ok = launch_attn_bwd(d, false, q, k, v, dout, lse, at<float>(workspace, p.drow),
+    ok = launch_attn_bwd(d, false, q, k, v, dout, at<float2>(workspace, p.emeta),
                          at<int>(workspace, p.seg_offset), at<int>(workspace, p.entries),
                          at<Item>(workspace, p.items1), at<int>(workspace, p.totals) + 2, p.max1,
                          at<float>(workspace, p.dq), at<float>(workspace, p.dk),
                          at<float>(workspace, p.dv), at<float>(workspace, p.pbar),
                          at<unsigned>(workspace, p.status), st);
-  });
-  timed("entry_lse", st, [&] {
-    launch_entry_lse(d, false, at<int>(workspace, p.seg_count), at<int>(workspace, p.seg_offset),
-                     at<int>(workspace, p.entries), at<float>(workspace, p.lse_px),
-                     at<float>(workspace, p.lpxe), st);
   });
   if (ok)
     timed("proxy_bwd", st, [&] {
@@ -492,19 +494,20 @@ int msa_warmup_backward(const msa_shape_t* shape, const void* q, const void* k, 
     launch_items(d, true, nullptr, at<int>(workspace, p.seg_offset), p.spec0, at<int>(workspace, p.io0),
                  at<Item>(workspace, p.items0), p.max0, status, st);
   });
-  timed("bwd_rowdot", st, [&] { launch_bwd_rowdot(d, o, dout, at<float>(workspace, p.drow), st); });
+  timed("bwd_rowdot", st, [&] { launch_bwd_rowdot(d, o, dout, lse, at<float2>(workspace, p.rowm), st); });
   timed("proxy_lse_dense", st, [&] { launch_proxy_lse_dense(d, qp, kp, at<float>(workspace, p.lse_px), st); });
+  timed("entry_meta", st, [&] {
+    launch_entry_meta(d, true, nullptr, at<int>(workspace, p.seg_offset), nullptr,
+                      at<float>(workspace, p.lse_px), at<float2>(workspace, p.rowm),
+                      at<float>(workspace, p.lpxe), at<float2>(workspace, p.emeta), st);
+  });
   bool ok = true;
   timed("attn_bwd_dense", st, [&] {
-    ok = launch_attn_bwd(d, true, q, k, v, dout, lse, at<float>(workspace, p.drow),
+    ok = launch_attn_bwd(d, true, q, k, v, dout, at<float2>(workspace, p.emeta),
                          at<int>(workspace, p.seg_offset), nullptr, at<Item>(workspace, p.items0),
                          at<int>(workspace, p.totals) + 1, p.max0, at<float>(workspace, p.dq),
                          at<float>(workspace, p.dk), at<float>(workspace, p.dv),
                          at<float>(workspace, p.pbar), status, st);
-  });
-  timed("entry_lse", st, [&] {
-    launch_entry_lse(d, true, nullptr, at<int>(workspace, p.seg_offset), nullptr,
-                     at<float>(workspace, p.lse_px), at<float>(workspace, p.lpxe), st);
   });
   if (ok)
     timed("proxy_bwd_dense", st, [&] {

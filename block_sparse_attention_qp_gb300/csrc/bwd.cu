@@ -38,8 +38,10 @@
 
 namespace msa {
 
+// Row data of every query row (b, t, h), token-major: rowm[(b S + t) Hq + h] = {LSE log2 e, D}
+// with D = rowsum(dO * O).
 __global__ void rowdot_kernel(Dims d, const bf16* __restrict__ o, const bf16* __restrict__ dout,
-                              float* __restrict__ drow) {
+                              const float* __restrict__ lse, float2* __restrict__ rowm) {
   const long long rows = (long long)d.B * d.S * d.Hq;
   const int lane = threadIdx.x % 32;
   for (long long r = (blockIdx.x * (long long)blockDim.x + threadIdx.x) / 32; r < rows;
@@ -56,7 +58,7 @@ __global__ void rowdot_kernel(Dims d, const bf16* __restrict__ o, const bf16* __
       const int h = (int)(r % d.Hq);
       const long long bt = r / d.Hq;
       const int t = (int)(bt % d.S), b = (int)(bt / d.S);
-      drow[((size_t)b * d.Hq + h) * d.S + t] = s;
+      rowm[r] = make_float2(lse[((size_t)b * d.Hq + h) * d.S + t] * kLog2e, s);
     }
   }
 }
@@ -76,7 +78,7 @@ constexpr int kIR = 4;                 // work-item ring: item numbers handed ou
 struct MainArgs {
   Dims d;
   const bf16 *q, *dout;
-  const float *lse, *drow;
+  const float2* emeta;  // per list entry and head: {LSE log2 e, D}
   const int* seg_offset;
   const int* entries;
   const Item* items;
@@ -345,7 +347,8 @@ __global__ void __launch_bounds__(352, 1)
     // ---------------------------------------------------------------- gather: Q, dO rows
     // Four warps (2, 8, 9, 10) each fill 16 of the tile's 64 rows with cp.async; completion is
     // counted on q_full (one cp.async arrival and one plain arrival per lane), so a warp moves on
-    // to the next tile as soon as its copies are issued.
+    // to the next tile as soon as its copies are issued.  (Q rows as per-token TMA boxes were
+    // slower: the TMA unit also carries the dQ bulk reductions.)
     const uint64_t keep = l2_policy_evict_last();  // read again by the chunk's other blocks
     const int gw = warp == 2 ? 0 : warp - 7;
     constexpr int WT = 16 / G;  // tokens of one warp's 16 rows (G in {4, 8, 16})
@@ -360,14 +363,24 @@ __global__ void __launch_bounds__(352, 1)
       const int bg = (int)((item.seg % d.nseg()) / d.nblk);
       const int b = bg / d.Hp, g = bg % d.Hp;
       const long long tb = item_base<kDense>(d, A.seg_offset, item);
+      const long long eb = (long long)A.seg_offset[item.seg] + item.first;  // first list entry
       auto load_tokens = [&](int pos0, int valid, int (&tv)[TT]) {
 #pragma unroll
         for (int x = 0; x < TT; ++x)
           tv[x] = x < valid ? (kDense ? (int)(tb + pos0 + x) : (__ldg(A.entries + tb + pos0 + x) >> 8)) : -1;
       };
+      // row data of row r0 + (lane & 15) of tile tl_ (lanes 0-15), indexed by the list entry, so
+      // it needs no token first
+      auto load_meta = [&](int tl_) -> float2 {
+        const int x = tl_ * TT + (r0 + ch) / G;
+        float2 m = make_float2(0.f, 0.f);
+        if (hi == 0 && x < item.count) m = __ldg(A.emeta + (size_t)(eb + x) * G + (r0 + ch) % G);
+        return m;
+      };
       const int ntiles = (item.count + TT - 1) / TT;
       int tv[TT];
       load_tokens(0, min(TT, item.count), tv);
+      float2 mcur = load_meta(0);
       for (int tl = 0; tl < ntiles; ++tl, ++i) {
         const int sl = (int)(i % kQS);
         int wt[WT];  // this warp's tokens
@@ -378,16 +391,10 @@ __global__ void __launch_bounds__(352, 1)
           for (int x = 0; x < TT; ++x)
             if (x == r0 / G + j) wt[j] = tv[x];
         }
-        // row data of rows r0 + (lane & 15): lanes 0-15 LSE * log2 e, lanes 16-31 D
         const int mr = r0 + ch;
-        int mt = -1;
-#pragma unroll
-        for (int j = 0; j < WT; ++j)
-          if (j == ch / G) mt = wt[j];
-        const size_t hrow = ((size_t)b * d.Hq + g * G + mr % G) * d.S;
-        const float mv = mt < 0 ? 0.f : (hi == 0 ? __ldg(A.lse + hrow + mt) * kLog2e : __ldg(A.drow + hrow + mt));
         int tn[TT];
         load_tokens((tl + 1) * TT, min(TT, item.count - (tl + 1) * TT), tn);
+        const float2 mnext = load_meta(tl + 1);
         if (i >= kQS && !mbar_wait_warp(&sh->q_empty[sl], par(i / kQS - 1), A.status)) { ok = false; break; }
         uint8_t* dQb = sSl + sl * kSlot;
         uint8_t* ddOb = dQb + kRT;
@@ -401,10 +408,10 @@ __global__ void __launch_bounds__(352, 1)
           cp_async16_hint(dQb + off, A.q + grow, t >= 0, keep);
           cp_async16_hint(ddOb + off, A.dout + grow, t >= 0, keep);
         }
-        if (hi == 0)
-          sh->lse2[sl][mr] = mv;
-        else
-          sh->drow[sl][mr] = mv;
+        if (hi == 0) {
+          sh->lse2[sl][mr] = mcur.x;
+          sh->drow[sl][mr] = mcur.y;
+        }
         if (gw == 0) {
 #pragma unroll
           for (int x = 0; x < TT; ++x)
@@ -414,6 +421,7 @@ __global__ void __launch_bounds__(352, 1)
         mbar_arrive(&sh->q_full[sl]);  // publishes the row data and tok
 #pragma unroll
         for (int x = 0; x < TT; ++x) tv[x] = tn[x];
+        mcur = mnext;
       }
     }
     cp_async_wait_all();  // nothing may land after the block exits
@@ -1010,16 +1018,16 @@ void proxy_bwd_g(const CUtensorMap& mkp, const ProxyArgs& a, cudaStream_t st) {
 int bwd_item_tokens() { return kItemTokens; }
 int bwd_group_tokens() { return kPG; }
 
-void launch_bwd_rowdot(const Dims& d, const void* o, const void* dout, float* drow,
-                       cudaStream_t st) {
+void launch_bwd_rowdot(const Dims& d, const void* o, const void* dout, const float* lse,
+                       float2* rowm, cudaStream_t st) {
   const long long rows = (long long)d.B * d.S * d.Hq;
   long long grid = (rows * 32 + 255) / 256;
   if (grid > (long long)num_sms() * 16) grid = (long long)num_sms() * 16;
-  rowdot_kernel<<<(int)grid, 256, 0, st>>>(d, (const bf16*)o, (const bf16*)dout, drow);
+  rowdot_kernel<<<(int)grid, 256, 0, st>>>(d, (const bf16*)o, (const bf16*)dout, lse, rowm);
 }
 
 bool launch_attn_bwd(const Dims& d, bool dense, const void* q, const void* k, const void* v,
-                     const void* dout, const float* lse, const float* drow, const int* seg_offset,
+                     const void* dout, const float2* emeta, const int* seg_offset,
                      const int* entries, const Item* items, const int* n_items, long long max_items,
                      float* dq_acc, float* dk_acc, float* dv_acc, float* pbar, unsigned* status,
                      cudaStream_t st) {
@@ -1033,8 +1041,7 @@ bool launch_attn_bwd(const Dims& d, bool dense, const void* q, const void* k, co
   a.d = d;
   a.q = (const bf16*)q;
   a.dout = (const bf16*)dout;
-  a.lse = lse;
-  a.drow = drow;
+  a.emeta = emeta;
   a.seg_offset = seg_offset;
   a.entries = entries;
   a.items = items;

@@ -167,21 +167,29 @@ __global__ void items_kernel(Dims d, int dense, const int* __restrict__ seg_coun
   }
 }
 
-// Proxy log-normaliser of every list entry, in entry order: lpxe[e] = LSE_px(b, g, t(e)) * log2 e,
-// so the proxy-gradient pass reads it with the entry, without a dependent gather.
-__global__ void entry_lse_kernel(Dims d, int dense, const int* __restrict__ seg_count,
-                                 const int* __restrict__ seg_offset, const int* __restrict__ entries,
-                                 const float* __restrict__ lse_px, float* __restrict__ lpxe) {
+// Row data of every list entry, in entry order, so the gradient passes read it with the entry
+// instead of through its token: lpxe[e] = LSE_px(b, g, t(e)) * log2 e and, for the G heads of the
+// group, emeta[e G + h] = {LSE(b, g G + h, t(e)) log2 e, D(b, t(e), g G + h)}.
+__global__ void entry_meta_kernel(Dims d, int dense, const int* __restrict__ seg_count,
+                                  const int* __restrict__ seg_offset, const int* __restrict__ entries,
+                                  const float* __restrict__ lse_px, const float2* __restrict__ rowm,
+                                  float* __restrict__ lpxe, float2* __restrict__ emeta) {
   const long long seg = blockIdx.x;
   const long long len = list_len(d, dense, seg_count, seg);
   if (len == 0) return;
   const long long base = seg_offset[seg];
   const long long bg = (seg % d.nseg()) / d.nblk;  // b * Hp + g
+  const long long b = bg / d.Hp, g = bg % d.Hp;
   const float* row = lse_px + bg * d.S;
   const long long t0 = dense ? dense_first(d, seg) : 0;
   for (long long k = threadIdx.x; k < len; k += blockDim.x) {
     const long long t = dense ? t0 + k : (long long)(entries[base + k] >> 8);
     lpxe[base + k] = row[t] * kLog2e;
+  }
+  for (long long x = threadIdx.x; x < len * d.G; x += blockDim.x) {
+    const long long k = x / d.G, h = x % d.G;
+    const long long t = dense ? t0 + k : (long long)(entries[base + k] >> 8);
+    emeta[base * d.G + x] = rowm[((b * d.S + t) * d.Hq + g * d.G + h)];
   }
 }
 
@@ -240,10 +248,11 @@ void launch_items(const Dims& d, bool dense, const int* seg_count, const int* se
                                                     item_offset, items, max_items, status);
 }
 
-void launch_entry_lse(const Dims& d, bool dense, const int* seg_count, const int* seg_offset,
-                      const int* entries, const float* lse_px, float* lpxe, cudaStream_t st) {
-  entry_lse_kernel<<<(unsigned)d.nlist(), 128, 0, st>>>(d, dense ? 1 : 0, seg_count, seg_offset,
-                                                         entries, lse_px, lpxe);
+void launch_entry_meta(const Dims& d, bool dense, const int* seg_count, const int* seg_offset,
+                       const int* entries, const float* lse_px, const float2* rowm, float* lpxe,
+                       float2* emeta, cudaStream_t st) {
+  entry_meta_kernel<<<(unsigned)d.nlist(), 256, 0, st>>>(d, dense ? 1 : 0, seg_count, seg_offset,
+                                                          entries, lse_px, rowm, lpxe, emeta);
 }
 
 void launch_convert(const float* src, void* dst, long long n, cudaStream_t st) {

@@ -43,9 +43,11 @@ void launch_items(const Dims& d, bool dense, const int* seg_count, const int* se
                   const ItemSpec& spec, const int* item_offset, Item* items, long long max_items,
                   unsigned* status, cudaStream_t st);
 
-// lpxe[e] = LSE_px of entry e's token x log2(e), in entry order (dense: the lists' implicit tokens).
-void launch_entry_lse(const Dims& d, bool dense, const int* seg_count, const int* seg_offset,
-                      const int* entries, const float* lse_px, float* lpxe, cudaStream_t st);
+// Row data of every list entry e (dense: the lists' implicit tokens), in entry order:
+// lpxe[e] = LSE_px of e's token x log2(e); emeta[e G + h] = rowm of e's token and head g G + h.
+void launch_entry_meta(const Dims& d, bool dense, const int* seg_count, const int* seg_offset,
+                       const int* entries, const float* lse_px, const float2* rowm, float* lpxe,
+                       float2* emeta, cudaStream_t st);
 
 // ---------------------------------------------------------------- proxy top-k (topk.cu)
 // Returns false if the TMA tensor maps could not be created (driver entry point missing).
@@ -70,8 +72,9 @@ void launch_dense_fwd(const Dims& d, const void* q, const void* k, const void* v
                       float* lse, cudaStream_t st);
 
 // ---------------------------------------------------------------- backward (bwd.cu)
-void launch_bwd_rowdot(const Dims& d, const void* o, const void* dout, float* drow,
-                       cudaStream_t st);
+// rowm[(b S + t) Hq + h] = {LSE(b, h, t) log2 e, rowsum(dO * O)(b, t, h)}
+void launch_bwd_rowdot(const Dims& d, const void* o, const void* dout, const float* lse,
+                       float2* rowm, cudaStream_t st);
 void launch_proxy_lse_sparse(const Dims& d, const void* qp, const void* kp, const int* seg_offset,
                              const int* entries, const Item* items, const int* n_items,
                              long long max_items, float* lpx_part, cudaStream_t st);
@@ -83,7 +86,7 @@ void launch_proxy_lse_dense(const Dims& d, const void* qp, const void* kp, float
 // ([list entry][128 keys] fp32).  Returns false for an unsupported group size or if the TMA
 // tensor maps cannot be created.
 bool launch_attn_bwd(const Dims& d, bool dense, const void* q, const void* k, const void* v,
-                     const void* dout, const float* lse, const float* drow, const int* seg_offset,
+                     const void* dout, const float2* emeta, const int* seg_offset,
                      const int* entries, const Item* items, const int* n_items, long long max_items,
                      float* dq_acc, float* dk_acc, float* dv_acc, float* pbar, unsigned* status,
                      cudaStream_t st);
