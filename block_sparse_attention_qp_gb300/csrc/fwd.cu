@@ -86,7 +86,7 @@ __device__ __forceinline__ void online_step(float (&s)[8][4], float (&m)[2], flo
 // its valid slots,  O = sum_s w_s O_s / sum_s w_s,  w_s = exp(lse_s - max),  LSE = max + log sum.
 // A slot is valid iff its partial log-sum-exp was written: the workspace holds NaN (all-ones
 // bytes) elsewhere.  Half-warps take alternate slots with 16-byte loads (8 columns per lane).
-__global__ void __launch_bounds__(256) combine_kernel(Dims d, const bf16* __restrict__ opart,
+__global__ void __launch_bounds__(256, 3) combine_kernel(Dims d, const bf16* __restrict__ opart,
                                                       const float* __restrict__ lpart,
                                                       bf16* __restrict__ o, float* __restrict__ lse) {
   const long long rows = (long long)d.B * d.S * d.Hq;
@@ -108,20 +108,30 @@ __global__ void __launch_bounds__(256) combine_kernel(Dims d, const bf16* __rest
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-    for (int s0 = 0; s0 < d.top_k; s0 += 2) {
-      const int s = s0 + half;
-      const float a = __shfl_sync(0xffffffffu, w0, s & 31);
-      const float c = __shfl_sync(0xffffffffu, w1, s & 31);
-      const float w = s < 32 ? a : c;
-      if (s < d.top_k && w > 0.f) {
-        const uint4 pv = ld_global_nc_v4_hint(opart + (base + s) * kD + l16 * 8, pol);
-        const uint32_t pw[4] = {pv.x, pv.y, pv.z, pv.w};
+    // 16 slots per pass: all eight 16-byte loads of a lane are issued before any is used, and
+    // they do not wait for the weights (a slot that was never written is loaded but not used)
+    for (int s0 = 0; s0 < d.top_k; s0 += 16) {
+      uint4 pv[8];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const __nv_bfloat162 p2 = *reinterpret_cast<const __nv_bfloat162*>(&pw[e]);
-          acc[2 * e] += w * __low2float(p2);
-          acc[2 * e + 1] += w * __high2float(p2);
+      for (int u = 0; u < 8; ++u) {
+        const int s = s0 + 2 * u + half;
+        pv[u] = s < d.top_k ? ld_global_nc_v4_hint(opart + (base + s) * kD + l16 * 8, pol)
+                            : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int s = s0 + 2 * u + half;
+        const float a = __shfl_sync(0xffffffffu, w0, s & 31);
+        const float c = __shfl_sync(0xffffffffu, w1, s & 31);
+        const float w = s < 32 ? a : c;
+        if (s < d.top_k && w > 0.f) {
+          const uint32_t pw[4] = {pv[u].x, pv[u].y, pv[u].z, pv[u].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const __nv_bfloat162 p2 = *reinterpret_cast<const __nv_bfloat162*>(&pw[e]);
+            acc[2 * e] += w * __low2float(p2);
+            acc[2 * e + 1] += w * __high2float(p2);
+          }
         }
       }
     }
