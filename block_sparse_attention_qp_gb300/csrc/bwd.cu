@@ -40,26 +40,48 @@ namespace msa {
 
 // Row data of every query row (b, t, h), token-major: rowm[(b S + t) Hq + h] = {LSE log2 e, D}
 // with D = rowsum(dO * O).
+__device__ __forceinline__ float dot8_bf16(uint4 a, uint4 c) {
+  const uint32_t pa[4] = {a.x, a.y, a.z, a.w}, pc[4] = {c.x, c.y, c.z, c.w};
+  float s = 0.f;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(&pa[e]);
+    const __nv_bfloat162 y = *reinterpret_cast<const __nv_bfloat162*>(&pc[e]);
+    s += __low2float(x) * __low2float(y) + __high2float(x) * __high2float(y);
+  }
+  return s;
+}
+
+// A warp takes four consecutive rows, eight lanes per row, 32 bytes of O and of dO per lane.
 __global__ void rowdot_kernel(Dims d, const bf16* __restrict__ o, const bf16* __restrict__ dout,
                               const float* __restrict__ lse, float2* __restrict__ rowm) {
   const long long rows = (long long)d.B * d.S * d.Hq;
-  const int lane = threadIdx.x % 32;
-  for (long long r = (blockIdx.x * (long long)blockDim.x + threadIdx.x) / 32; r < rows;
-       r += (long long)gridDim.x * blockDim.x / 32) {
-    const uint2 a = *reinterpret_cast<const uint2*>(o + (size_t)r * kD + lane * 4);
-    const uint2 c = *reinterpret_cast<const uint2*>(dout + (size_t)r * kD + lane * 4);
-    const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
-    const __nv_bfloat162* pc = reinterpret_cast<const __nv_bfloat162*>(&c);
-    float s = __low2float(pa[0]) * __low2float(pc[0]) + __high2float(pa[0]) * __high2float(pc[0]) +
-              __low2float(pa[1]) * __low2float(pc[1]) + __high2float(pa[1]) * __high2float(pc[1]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    if (lane == 0) {
-      const int h = (int)(r % d.Hq);
-      const long long bt = r / d.Hq;
-      const int t = (int)(bt % d.S), b = (int)(bt / d.S);
-      rowm[r] = make_float2(lse[((size_t)b * d.Hq + h) * d.S + t] * kLog2e, s);
+  const int lane = threadIdx.x % 32, q = lane >> 3, l8 = lane & 7;
+  const long long nw = (long long)gridDim.x * blockDim.x / 32;
+  for (long long w = (blockIdx.x * (long long)blockDim.x + threadIdx.x) / 32; w * 4 < rows; w += nw) {
+    const long long r = w * 4 + q;
+    const bool in = r < rows;
+    const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+    uint4 a0 = z, a1 = z, c0 = z, c1 = z;
+    float lv = 0.f;
+    if (in) {
+      const uint4* po = reinterpret_cast<const uint4*>(o + (size_t)r * kD + l8 * 16);
+      const uint4* pd = reinterpret_cast<const uint4*>(dout + (size_t)r * kD + l8 * 16);
+      a0 = po[0];
+      a1 = po[1];
+      c0 = pd[0];
+      c1 = pd[1];
+      if (l8 == 0) {
+        const int h = (int)(r % d.Hq);
+        const long long bt = r / d.Hq;
+        const int t = (int)(bt % d.S), b = (int)(bt / d.S);
+        lv = lse[((size_t)b * d.Hq + h) * d.S + t];
+      }
     }
+    float s = dot8_bf16(a0, c0) + dot8_bf16(a1, c1);
+#pragma unroll
+    for (int off = 4; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (in && l8 == 0) rowm[r] = make_float2(lv * kLog2e, s);
   }
 }
 
@@ -1021,7 +1043,7 @@ int bwd_group_tokens() { return kPG; }
 void launch_bwd_rowdot(const Dims& d, const void* o, const void* dout, const float* lse,
                        float2* rowm, cudaStream_t st) {
   const long long rows = (long long)d.B * d.S * d.Hq;
-  long long grid = (rows * 32 + 255) / 256;
+  long long grid = ((rows + 3) / 4 * 32 + 255) / 256;
   if (grid > (long long)num_sms() * 16) grid = (long long)num_sms() * 16;
   rowdot_kernel<<<(int)grid, 256, 0, st>>>(d, (const bf16*)o, (const bf16*)dout, lse, rowm);
 }
