@@ -25,7 +25,8 @@
  *   group sizes return MSA_ERR_UNSUPPORTED).
  *   `workspace` is caller-owned device memory of at least msa_workspace_size() bytes for the
  *   same op and shape; the library allocates nothing.  The first 256 bytes hold a device status
- *   word (see msa_device_status).  Calls sharing one workspace must not overlap on the GPU.
+ *   word (see msa_device_status) and the work-item counters of the persistent kernels (reset on
+ *   the stream before each launch).  Calls sharing one workspace must not overlap on the GPU.
  *   `stream` is a cudaStream_t (NULL = legacy default stream); all work is asynchronous on it.
  *   Return value: an msa_status code.  Argument errors are detected on the host before any
  *   launch; MSA_ERR_CUDA reports a launch or runtime error (msa_last_error() gives the text).
