@@ -199,6 +199,11 @@ KERNEL_WORK = {
     # proxy backward: z recompute, dKp, dQp (2d each) per selected pair and proxy head
     "proxy_bwd": ("tensor", lambda w: 6 * w.D * flops.n_sel(w.S, w.top_k) * w.Hp * w.B),
     "proxy_lse": ("tensor", lambda w: 2 * w.D * flops.n_sel(w.S, w.top_k) * w.Hp * w.B),
+    # warmup step: the same per-pair work over every causal pair
+    "dense_fwd": ("tensor", lambda w: 4 * w.D * flops.n_dense(w.S) * w.Hq * w.B),
+    "attn_bwd_dense": ("tensor", lambda w: 10 * w.D * flops.n_dense(w.S) * w.Hq * w.B),
+    "proxy_bwd_dense": ("tensor", lambda w: 6 * w.D * flops.n_dense(w.S) * w.Hp * w.B),
+    "proxy_lse_dense": ("tensor", lambda w: 2 * w.D * flops.n_dense(w.S) * w.Hp * w.B),
 }
 
 
@@ -237,9 +242,16 @@ def run_ours(args, w, wi):
     g = {n: x[n].to(dev) for n in names}
     inputs_bytes = sum(g[n].numel() * 2 for n in names)
     shape = msa.make_shape(g["q"], g["k"], g["qp"], w.top_k, w.scale)
-    ws_f = msa.workspace(shape, msa.OP_FORWARD, dev)
-    ws_b = msa.workspace(shape, msa.OP_BACKWARD, dev)
+    dense = w.top_k == 0  # the warmup step: dense causal attention, proxy KL over the prefix
+    ws_f = msa.workspace(shape, msa.OP_WARMUP_FORWARD if dense else msa.OP_FORWARD, dev)
+    ws_b = msa.workspace(shape, msa.OP_WARMUP_BACKWARD if dense else msa.OP_BACKWARD, dev)
+
     def full_step(src):
+        if dense:
+            o, lse = msa.msa_warmup_forward(src["q"], src["k"], src["v"], w.scale, ws=ws_f)
+            grads = msa.msa_warmup_backward(src["q"], src["k"], src["v"], src["qp"], src["kp"], o,
+                                            lse, src["dout"], w.scale, ws=ws_b)
+            return (o,) + tuple(grads)
         o, lse, bi = msa.msa_forward(src["q"], src["k"], src["v"], src["qp"], src["kp"], w.top_k,
                                      w.scale, ws=ws_f)
         grads = msa.msa_backward(src["q"], src["k"], src["v"], src["qp"], src["kp"], o, lse,
