@@ -1,23 +1,24 @@
 // Backward on the tcgen05 tensor cores (blog, "Backward" and "KL Divergence Loss"):
-//   rowdot_kernel     D = rowsum(dO * O)
+//   rowdot_kernel     row data {LSE log2 e, D = rowsum(dO * O)} of every query row
 //   attn_bwd_kernel   main-attention gradients dQ, dK, dV and the teacher pbar
 //   proxy_bwd_kernel  proxy gradients dQp, dKp of the KL term, from pbar
 //
 // Work items (shared by both kernels): one 128-key block n of group g and up to 512 tokens that
 // use it (from the inverted block map; in warmup mode every token t >= 128 n), all from one
-// sequence chunk.  Lists run chunk-major, so the dQ / dQp rows that concurrent items update
-// belong to one chunk of the sequence.
+// sequence chunk.  Lists run chunk-major and blocks take items in list order from a shared
+// counter, so the dQ / dQp rows that concurrent items update belong to one chunk of the sequence.
 //
 // attn_bwd_kernel keeps the block's K and V in shared memory and its dK, dV accumulators in tensor
-// memory while it streams tiles of 64/G tokens x G query heads (64 rows), double buffered:
+// memory while it streams tiles of 64/G tokens x G query heads (64 rows) through three Q / dO
+// slots (S^T and dP^T double buffered in tensor memory):
 //   phase 1 (tensor core)  S^T = K Q^T,  dP^T = V dO^T                       (keys x rows, fp32)
 //   softmax (4 warps, thread = key)
 //                          P^T  = exp(scale S^T - LSE_row)       -> tensor memory (bf16)
 //                          dS^T = P^T (dP^T - D_row)             -> shared memory (bf16)
 //                          teacher pbar = mean over the token's G heads of P -> global (fp32)
 //   phase 2 (tensor core)  dV += P^T dO,  dK += dS^T Q,  dQ^T = K^T dS^T
-//   epilogue               dQ^T -> shared staging; a reducer thread adds each token's G rows
-//                          into dQ with one bulk tensor-memory-accelerator reduction
+//   epilogue               dQ^T -> fp32 rows staged in the tile's own slot; a reducer thread adds
+//                          each token's G rows into dQ with one bulk TMA reduction
 //   item end               dK (x scale), dV -> fp32 atomics
 // proxy_bwd_kernel streams the same items in groups of 64 tokens:
 //   z^T = Kp Qp^T;  dz = kl_grad/(B S Hp) (exp(scale z - LSE_px) - pbar)   (the blog's closed
@@ -25,10 +26,10 @@
 //   dKp += dz^T Qp (tensor memory, per item),  dQp^T = Kp^T dz^T (per group) -> fp32 atomics.
 // Causality everywhere: key j contributes to token t only when j <= t.
 //
-// Roles of attn_bwd_kernel (352 threads): warp 0 TMA loads of K/V and tensor-memory ownership,
-// warp 1 the MMA issuer, warps 2 and 8-10 gather the tile's Q / dO rows with cp.async, warp 3
-// issues the dQ bulk reductions, warps 4-7 softmax / epilogue.  Tensor memory (512 columns): SB0, SB1 (S^T,
-// then P^T), DB0, DB1 (dP^T, then dQ^T), dV, dK.
+// Roles of attn_bwd_kernel (352 threads): warp 0 TMA loads of K/V, the block's work-item numbers
+// and tensor-memory ownership, warp 1 the MMA issuer, warps 2 and 8-10 gather the tile's Q / dO
+// rows with cp.async, warp 3 issues the dQ bulk reductions, warps 4-7 softmax / epilogue.  Tensor
+// memory (512 columns): SB0, SB1 (S^T, then P^T), DB0, DB1 (dP^T, then dQ^T), dV, dK.
 #include <math.h>
 
 #include "common.cuh"
