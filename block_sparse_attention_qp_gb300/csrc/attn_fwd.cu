@@ -3,18 +3,21 @@
 // forward).
 //
 // Phase 1 (attn_fwd_kernel): a work item is one 128-key block n of group g and up to 8 tiles of
-// the tokens whose selection holds n (from the inverted block map).  A tile is 128 rows: 128/G
-// tokens x the G query heads of the group.  Per tile
+// the tokens whose selection holds n (from the inverted block map); blocks take items in list
+// order from a shared counter.  A tile is 128 rows: 128/G tokens x the G query heads of the
+// group.  Per tile
 //   S = Q K^T                       (tensor core, 128 x 128 fp32 in tensor memory)
 //   P = exp(scale S - m), l = sum P  (softmax warps, thread = row; causal cut in the local block)
 //   O = P V                         (tensor core, P read from tensor memory)
 //   partial (t, h, slot) = O / l in bf16, and its log-sum-exp m + log l   (epilogue warps)
 // Phase 2 (combine_kernel in fwd.cu) merges the <= top_k partials of every (t, h).
 //
-// Roles (448 threads): warp 0 TMA loads of K/V (a three-slot ring) and tensor-memory ownership,
-// warp 1 the MMA issuer, warps 2, 3, 12, 13 gather the tile's Q rows (cp.async, three buffers),
-// warps 4-7 and 8-11 two softmax + epilogue groups that take alternate tiles.  (TMA issues about one request per 70 cycles per SM,
-// so 1 KB row boxes cannot feed a 128-row tile in time; four cp.async warps can.)  Tensor memory (512 columns): S0, S1 (S, then P in place), O0, O1.
+// Roles (448 threads): warp 0 TMA loads of K/V (a three-slot ring), the block's work-item numbers
+// and tensor-memory ownership, warp 1 the MMA issuer, warps 2, 3, 12, 13 gather the tile's Q rows
+// (cp.async, three buffers), warps 4-7 and 8-11 two softmax + epilogue groups that take alternate
+// tiles.  (TMA issues about one request per 70 cycles per SM, so 1 KB row boxes cannot feed a
+// 128-row tile in time; four cp.async warps can.)  Tensor memory (512 columns): S0, S1 (S, then P
+// in place), O0, O1.
 // The MMA issuer runs S of tile i before O of tile i-1, so the tensor pipe works on one tile while
 // the softmax warps work on the next.  Every wait is bounded (see sm100::mbar_wait).
 #include <math.h>
