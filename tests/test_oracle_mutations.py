@@ -24,6 +24,18 @@ MUTANTS = {
                             "dqrow[d] += dS[a] * krow[d];"),
     "block max over a shifted block": ("for (int j = n * MSA_ORACLE_BLOCK; j < (n + 1) * MSA_ORACLE_BLOCK; ++j) {\n      double z",
                                        "for (int j = n * MSA_ORACLE_BLOCK + 1; j < (n + 1) * MSA_ORACLE_BLOCK; ++j) {\n      double z"),
+    "dV from dS instead of P": ("dvrow[d] += Ph[a] * dorow[d];", "dvrow[d] += dS[a] * dorow[d];"),
+    "scale dropped in dK": ("dkrow[d] += scale * dS[a] * qrow[d];", "dkrow[d] += dS[a] * qrow[d];"),
+    "row term D dropped": ("const double Drow = dot(dorow, o, D);",
+                           "const double Drow = 0.0 * dot(dorow, o, D);"),
+    "student not normalised": ("const double lse_px = zmx + log(zsum);", "const double lse_px = zmx;"),
+    "query head mapped to the wrong group": ("const int g = h / G;", "const int g = h % Hkv;"),
+    "scale dropped in dQp": ("dqprow[d] += scale * dz * kprow[d];", "dqprow[d] += dz * kprow[d];"),
+    "KL mean not over proxy heads": ("if (kl_out) *kl_out = kl / ((double)B * S * Hp);",
+                                     "if (kl_out) *kl_out = kl / ((double)B * S);"),
+    "padding with block 0": ("for (; w < top_k; ++w) out[w] = -1;", "for (; w < top_k; ++w) out[w] = 0;"),
+    "one block too few": ("const int K = top_k < m + 1 ? top_k : m + 1;",
+                          "const int K = top_k - 1 < m + 1 ? top_k - 1 : m + 1;"),
 }
 
 PINS = [
