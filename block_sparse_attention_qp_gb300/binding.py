@@ -72,6 +72,8 @@ def load_library(path: str = LIB_PATH):
         lib.msa_forward_noalloc.argtypes = [SP, P, P, P, P, P, P, I, P, P, P]
         lib.msa_forward_noalloc.restype = I
         lib.msa_launch_count.restype = ctypes.c_longlong
+        lib.msa_selftest_wait_timeout.argtypes = [P, ctypes.c_uint, P]
+        lib.msa_selftest_wait_timeout.restype = I
         _lib = lib
         return lib
 
@@ -130,6 +132,13 @@ def msa_device_status(ws: torch.Tensor) -> int:
     _check(load_library().msa_device_status(_ptr(ws), ctypes.byref(flags), _stream(ws.device)),
            "msa_device_status")
     return int(flags.value)
+
+
+def selftest_wait_timeout(ws: torch.Tensor, limit_us: int = 1000) -> None:
+    """Run the library's bounded-wait self-test on ws's device (see msa_selftest_wait_timeout);
+    the timeout shows up in msa_device_status(ws)."""
+    _check(load_library().msa_selftest_wait_timeout(_ptr(ws), int(limit_us), _stream(ws.device)),
+           "msa_selftest_wait_timeout")
 
 
 def profile_begin() -> None:

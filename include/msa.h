@@ -168,6 +168,16 @@ MSA_API int msa_forward_noalloc(const msa_shape_t* shape, const void* q, const v
                                 const void* v, const void* qp, const void* kp, int32_t* block_idx,
                                 int indices_given, void* o, float* lse, void* stream);
 
+/*
+ * Failure-detection self-test (not part of the method).  Launches one block on `stream` whose
+ * thread waits on a shared-memory mbarrier that nothing arrives at, through the same bounded wait
+ * every kernel of the library uses; after limit_us microseconds (1 .. 1000000) the wait gives up
+ * and sets MSA_DEVICE_TIMEOUT in the status word of `workspace` (any workspace of this library, or
+ * 256 zeroed, 16-byte aligned device bytes).  Read it with msa_device_status.  Returns
+ * MSA_ERR_INVALID_ARG for a null or misaligned workspace or a limit out of range.
+ */
+MSA_API int msa_selftest_wait_timeout(void* workspace, unsigned limit_us, void* stream);
+
 /* Static text for a status code. */
 MSA_API const char* msa_status_string(int status);
 
