@@ -27,7 +27,8 @@ OP_FORWARD, OP_BACKWARD, OP_WARMUP_FORWARD, OP_WARMUP_BACKWARD = 0, 1, 2, 3
 STATUS_BITS = {1: "bad block index", 2: "work list overflow", 4: "device wait timeout"}
 _SYMBOLS = ("msa_workspace_size", "msa_forward", "msa_backward", "msa_warmup_forward",
             "msa_warmup_backward", "msa_device_status", "msa_status_string", "msa_last_error",
-            "msa_profile_begin", "msa_profile_end", "msa_launch_count", "msa_forward_noalloc")
+            "msa_profile_begin", "msa_profile_end", "msa_launch_count", "msa_forward_noalloc",
+            "msa_selftest_wait_timeout")
 
 
 class MSAError(RuntimeError):

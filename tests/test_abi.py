@@ -61,3 +61,13 @@ def test_argument_errors_before_any_launch(lib):
     rc = lib.msa_warmup_forward(ctypes.byref(s_bad), null, null, null, null, null, null, 0, null)
     assert rc == 1
     assert lib.msa_status_string(3) == b"workspace too small"
+
+
+def test_selftest_rejects_bad_arguments_on_the_host(lib):
+    P = ctypes.c_void_p
+    assert lib.msa_selftest_wait_timeout(P(0), 1000, P(0)) == 1
+    assert lib.msa_selftest_wait_timeout(P(0x1008), 1000, P(0)) == 1  # misaligned, never touched
+    assert b"aligned" in lib.msa_last_error()
+    assert lib.msa_selftest_wait_timeout(P(0x1000), 0, P(0)) == 1  # limit out of range
+    assert lib.msa_selftest_wait_timeout(P(0x1000), 2_000_000, P(0)) == 1
+    assert b"limit_us" in lib.msa_last_error()
