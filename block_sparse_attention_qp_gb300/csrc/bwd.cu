@@ -154,9 +154,6 @@ __device__ __forceinline__ void red4(float* p, float a, float b, float c, float 
                "f"(d)
                : "memory");
 }
-__device__ __forceinline__ void red1(float* p, float a) {
-  asm volatile("red.global.add.f32 [%0], %1;\n" ::"l"(p), "f"(a) : "memory");
-}
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(a), "r"(b), "r"(c),
