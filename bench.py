@@ -43,7 +43,13 @@ def workload_by_name(name):
     raise SystemExit(f"unknown workload {name}; choose from {[w.name for w in WORKLOADS]}")
 
 
-def config_of(w, inputs_bytes):
+def input_bytes(w):
+    """Bytes of the step's bf16 inputs q, k, v, qp, kp, dout."""
+    return w.B * w.S * (2 * w.Hq + 2 * w.Hkv + w.Hp + 1) * w.D * 2
+
+
+def config_of(w):
+    inputs_bytes = input_bytes(w)
     return {"workload": w.name, "desc": w.describe(), "B": w.B, "S": w.S, "Hq": w.Hq,
             "Hkv": w.Hkv, "Hp": w.Hp, "d": w.D, "top_k": w.top_k, "block": 128,
             "planted_blocks": w.planted, "scale": w.scale,
@@ -179,8 +185,9 @@ def run_reference(args, w, wi):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": config_of(w, 0),
+            "config": config_of(w),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "cpu_model": cpu_model(),
                              "sample": f"{n_tok} random tokens per step (all {w.Hp} groups, "
                                        f"{w.Hq} heads): selection rows, forward rows and their "
                                        f"exact share of every gradient"},
@@ -240,7 +247,6 @@ def run_ours(args, w, wi):
     x = make_inputs(w, dist.rank_seed(workload_seed(wi), rank))
     names = ("q", "k", "v", "qp", "kp", "dout")
     g = {n: x[n].to(dev) for n in names}
-    inputs_bytes = sum(g[n].numel() * 2 for n in names)
     shape = msa.make_shape(g["q"], g["k"], g["qp"], w.top_k, w.scale)
     dense = w.top_k == 0  # the warmup step: dense causal attention, proxy KL over the prefix
     ws_f = msa.workspace(shape, msa.OP_WARMUP_FORWARD if dense else msa.OP_FORWARD, dev)
@@ -315,7 +321,7 @@ def run_ours(args, w, wi):
                 "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": sec_max / args.steps * 1e3, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-                "config": config_of(w, inputs_bytes),
+                "config": config_of(w),
                 "tflops": tflops,
                 "frac_of_dense_bf16_peak": {
                     "burst": tflops / world / peaks["bf16_tflops"],
@@ -388,6 +394,46 @@ def measure_e2e(args, w, g, full_step, dev):
             "overlap": "copies on two streams, overlapped with the neighbouring steps' compute"}
 
 
+def cpu_model():
+    """Host CPU model name (lscpu, else /proc/cpuinfo), for the baseline record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() == "Model name":
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def oracle_full_step_single_thread():
+    """The oracle on the whole of the smallest workload (msa_s1k: every selection row, every
+    forward row, every gradient) on one host thread.  Returns (seconds, tokens)."""
+    import oracle
+
+    wi, w1 = workload_by_name("msa_s1k")
+    x64 = oracle_inputs(w1, workload_seed(wi))
+    saved = oracle.threads()
+    oracle.set_threads(1)
+    try:
+        t0 = time.perf_counter()
+        idx, _ = oracle.select(x64["qp"], x64["kp"], w1.top_k, w1.scale)
+        oracle.forward(x64["q"], x64["k"], x64["v"], idx, w1.top_k, w1.scale)
+        oracle.backward(x64["q"], x64["k"], x64["v"], x64["qp"], x64["kp"], x64["dout"], idx,
+                        w1.top_k, w1.scale)
+        sec = time.perf_counter() - t0
+    finally:
+        oracle.set_threads(saved)
+    return sec, w1.B * w1.S
+
+
 def cpu_baseline(w, wi, args):
     import oracle
 
@@ -396,10 +442,14 @@ def cpu_baseline(w, wi, args):
     rng = np.random.default_rng(1)
     toks = sample_tokens(w, args.ref_tokens, rng)
     sec = oracle_sample(w, x64, idx_builder(w), toks)
+    st_sec, st_tok = oracle_full_step_single_thread()
     return {"value": len(toks) / sec, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
+            "cpu_model": cpu_model(),
             "sample": f"{len(toks)} random tokens of {w.name} (all {w.Hp} groups, {w.Hq} heads): "
                       f"selection rows, forward rows, exact share of every gradient; "
-                      f"{sec:.1f} s"}
+                      f"{sec:.1f} s",
+            "single_thread_msa_s1k": {"value": st_tok / st_sec, "unit": UNIT, "sec": st_sec,
+                                      "cores": 1, "sample": "the whole msa_s1k step"}}
 
 
 def main():

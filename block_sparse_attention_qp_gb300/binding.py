@@ -28,7 +28,7 @@ STATUS_BITS = {1: "bad block index", 2: "work list overflow", 4: "device wait ti
 _SYMBOLS = ("msa_workspace_size", "msa_forward", "msa_backward", "msa_warmup_forward",
             "msa_warmup_backward", "msa_device_status", "msa_status_string", "msa_last_error",
             "msa_profile_begin", "msa_profile_end", "msa_launch_count", "msa_forward_noalloc",
-            "msa_selftest_wait_timeout")
+            "msa_forward_noalloc_status", "msa_selftest_wait_timeout")
 
 
 class MSAError(RuntimeError):
@@ -72,6 +72,8 @@ def load_library(path: str = LIB_PATH):
         lib.msa_profile_end.argtypes = [ctypes.c_char_p, Z]
         lib.msa_forward_noalloc.argtypes = [SP, P, P, P, P, P, P, I, P, P, P]
         lib.msa_forward_noalloc.restype = I
+        lib.msa_forward_noalloc_status.argtypes = [ctypes.POINTER(ctypes.c_uint), P]
+        lib.msa_forward_noalloc_status.restype = I
         lib.msa_launch_count.restype = ctypes.c_longlong
         lib.msa_selftest_wait_timeout.argtypes = [P, ctypes.c_uint, P]
         lib.msa_selftest_wait_timeout.restype = I
@@ -206,6 +208,15 @@ def msa_forward_noalloc(q, k, v, qp, kp, top_k: int, scale: float, block_idx=Non
                                               _ptr(o), _ptr(lse), _stream(q.device)),
            "msa_forward_noalloc")
     return o, lse, block_idx
+
+
+def msa_forward_noalloc_status(device=None) -> int:
+    """Read and clear the status word of the fixed scratch array msa_forward_noalloc uses on the
+    current device (synchronises the current stream)."""
+    flags = ctypes.c_uint(0)
+    _check(load_library().msa_forward_noalloc_status(ctypes.byref(flags), _stream(device)),
+           "msa_forward_noalloc_status")
+    return int(flags.value)
 
 
 def msa_backward(q, k, v, qp, kp, o, lse, dout, block_idx, top_k: int, scale: float,

@@ -200,6 +200,11 @@ __global__ void __launch_bounds__(352, 1)
                     MainArgs A) {
   using namespace sm100;
   constexpr int TT = kTR / G;  // tokens per tile
+  // With 16 heads per group, up to 16 x (tokens) rows add into each key's dV; P rounded once to
+  // bf16 for dV = P^T dO then costs up to ~2e-2 on the largest entries.  P^T is then written as
+  // its bf16 value plus the bf16 residual P - bf16(P) (columns 32-63 of the same buffer) and dV
+  // takes both: dV += P_hi^T dO + P_lo^T dO (P to ~16 significant bits; four more MMAs a tile).
+  constexpr bool kSplitP = G >= 16;
   const Dims& d = A.d;
 
   extern __shared__ uint8_t smem_raw[];
@@ -320,6 +325,11 @@ __global__ void __launch_bounds__(352, 1)
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)  // dV += P^T dO  (P^T from tensor memory)
           mma_ts(RV, SBb + ks * 8, desc_mnmajor(adOb, kTR, ks), id_g, acc || ks > 0);
+        if constexpr (kSplitP) {
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)  // dV += P_lo^T dO  (the bf16 residual of P)
+            mma_ts(RV, SBb + 32 + ks * 8, desc_mnmajor(adOb, kTR, ks), id_g, true);
+        }
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)  // dK += dS^T Q
           mma_ss(RK, desc_kmajor(adSb, 128, ks), desc_mnmajor(aQb, kTR, ks), id_g, acc || ks > 0);
@@ -540,6 +550,9 @@ __global__ void __launch_bounds__(352, 1)
         }
         const uint32_t SBb = SB0 + 64 * bb, DBb = DB0 + 64 * bb;
         const uint32_t adSb = adS + bb * kST;
+        // kSplitP: the bf16 residual P - bf16(P) of rows 0-31, written to columns 32-47 only once
+        // the S^T values of rows 32-63 in those columns have been read
+        uint32_t lw0[kSplitP ? 16 : 1];
 #pragma unroll
         for (int c = 0; c < 2; ++c) {  // 32 rows at a time (P^T of rows 0-31 lands in columns 0-15)
           uint32_t rs[32], rp[32];
@@ -548,6 +561,7 @@ __global__ void __launch_bounds__(352, 1)
           tmem_ld32(DBb + lb + 32 * c, rp);
           tmem_wait_ld();
           uint32_t pw[16], dw[16];
+          uint32_t lw[kSplitP ? 16 : 1];
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4) {
             const float4 l4 = reinterpret_cast<const float4*>(sh->lse2[sl])[c * 8 + q4];
@@ -570,8 +584,24 @@ __global__ void __launch_bounds__(352, 1)
             pw[2 * q4 + 1] = pack_bf16(pv[2], pv[3]);
             dw[2 * q4] = pack_bf16(dsv[0], dsv[1]);
             dw[2 * q4 + 1] = pack_bf16(dsv[2], dsv[3]);
+            if constexpr (kSplitP) {
+#pragma unroll
+              for (int h2 = 0; h2 < 2; ++h2) {
+                const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&pw[2 * q4 + h2]);
+                lw[2 * q4 + h2] = pack_bf16(pv[2 * h2] - __low2float(hi), pv[2 * h2 + 1] - __high2float(hi));
+              }
+            }
           }
           tmem_st16(SBb + lb + c * 16, pw);  // P^T: row r packed into column r / 2
+          if constexpr (kSplitP) {
+            if (c == 0) {
+#pragma unroll
+              for (int u = 0; u < 16; ++u) lw0[u] = lw[u];
+            } else {  // every S^T column of this warp's lanes has been read: residuals to 32-63
+              tmem_st16(SBb + lb + 32, lw0);
+              tmem_st16(SBb + lb + 48, lw);
+            }
+          }
 #pragma unroll
           for (int u = 0; u < 4; ++u)
             st_shared_v4(adSb + sm100::sw128_chunk(kr, c * 4 + u), dw[4 * u], dw[4 * u + 1],

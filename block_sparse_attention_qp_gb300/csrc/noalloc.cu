@@ -70,4 +70,19 @@ int msa_forward_noalloc(const msa_shape_t* shape, const void* q, const void* k, 
                      msa::kMaxScratch, stream);
 }
 
+int msa_forward_noalloc_status(unsigned* flags, void* stream) {
+  if (!flags) {
+    msa::set_api_error("msa_forward_noalloc_status: flags must be non-null");
+    return MSA_ERR_INVALID_ARG;
+  }
+  void* scratch = nullptr;
+  const int rc = msa::scratch_for_current_device(&scratch);
+  if (rc != MSA_OK) {
+    msa::set_api_error("msa_forward_noalloc_status: cudaGetSymbolAddress of the scratch array failed");
+    return rc;
+  }
+  // the status word is the first word of the array, as of any workspace
+  return msa_device_status(scratch, flags, stream);
+}
+
 }  // extern "C"

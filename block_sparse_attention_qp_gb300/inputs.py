@@ -98,3 +98,62 @@ def make_inputs(w: Workload, seed: int, device="cpu"):
            for name, t in dict(q=q, k=k, v=v, qp=qp, kp=kp, dout=dout).items()}
     out["planted"] = planted
     return out
+
+
+def random_selection(B: int, Hp: int, S: int, top_k: int, seed: int, exclude: int = -1):
+    """A seeded random valid block map [B, Hp, S, top_k] int32 (numpy): every row holds its local
+    block t // 128 plus min(top_k, m + 1) - 1 distinct earlier blocks drawn uniformly (never
+    ``exclude``), ascending, padded with -1.  It stands in for a selection where a test needs the
+    gradient passes driven by an index map that both sides know without running the selection
+    (the map is a plain input of the backward)."""
+    import numpy as np
+
+    rng = np.random.default_rng(seed)
+    nblk = S // BLOCK
+    k1 = top_k - 1
+    out = np.full((B, Hp, S, top_k), -1, np.int32)
+    t = np.arange(S)
+    m = t // BLOCK
+    step = max(1, (1 << 24) // max(nblk, 1))  # rows per draw: bounded host memory
+    for b in range(B):
+        for g in range(Hp):
+            for r0 in range(0, S, step):
+                r1 = min(S, r0 + step)
+                mm = m[r0:r1]
+                keys = rng.random((r1 - r0, nblk), dtype=np.float32)
+                blk = np.arange(nblk)
+                bad = (blk[None, :] >= mm[:, None]) | (blk[None, :] == exclude)
+                keys[bad] = np.inf
+                if k1 > 0:
+                    pick = np.argpartition(keys, min(k1, nblk - 1), axis=1)[:, :k1] if nblk > k1 \
+                        else np.argsort(keys, axis=1)[:, :k1]
+                    ok = np.take_along_axis(keys, pick, axis=1) < np.inf
+                    pick = np.where(ok, pick, nblk + 1)  # not enough visible blocks: padding
+                else:
+                    pick = np.zeros((r1 - r0, 0), np.int64)
+                rows = np.concatenate([pick, mm[:, None]], axis=1)
+                rows.sort(axis=1)
+                rows[rows > nblk] = -1
+                # padding (-1) sorted first: move it to the end of the row
+                valid = rows >= 0
+                order = np.argsort(~valid, axis=1, kind="stable")
+                out[b, g, r0:r1] = np.take_along_axis(rows, order, axis=1)
+    return out
+
+
+def force_block(idx, rows, n: int):
+    """Put block ``n`` into the given rows (b, g, t) of a map from random_selection in place of
+    the row's first non-local block (each row must have t // 128 > n and no block n yet), keeping
+    the row ascending.  Returns the map (modified in place)."""
+    import numpy as np
+
+    for b, g, t in rows:
+        row = idx[b, g, t]
+        m = t // BLOCK
+        assert m > n and n not in row, (b, g, t)
+        first = int(np.nonzero((row >= 0) & (row != m))[0][0])
+        row[first] = n
+        valid = np.sort(row[row >= 0])
+        row[:] = -1
+        row[:len(valid)] = valid
+    return idx

@@ -169,6 +169,17 @@ MSA_API int msa_forward_noalloc(const msa_shape_t* shape, const void* q, const v
                                 int indices_given, void* o, float* lse, void* stream);
 
 /*
+ * Device status word of the fixed scratch array that msa_forward_noalloc uses on the current
+ * device: same bits and behaviour as msa_device_status (reads and clears the word once the work
+ * queued on `stream` has finished; synchronises `stream`).  Callers of msa_forward_noalloc have no
+ * workspace pointer to pass to msa_device_status, so this is how they learn that given block
+ * indices were skipped as invalid (MSA_DEVICE_BAD_INDEX) or that a bounded wait gave up.  Every
+ * call of msa_forward_noalloc on a device clears the word before it launches, so read it after
+ * each call whose result matters.
+ */
+MSA_API int msa_forward_noalloc_status(unsigned* flags, void* stream);
+
+/*
  * Failure-detection self-test (not part of the method).  Launches one block on `stream` whose
  * thread waits on a shared-memory mbarrier that nothing arrives at, through the same bounded wait
  * every kernel of the library uses; after limit_us microseconds (1 .. 1000000) the wait gives up

@@ -33,19 +33,30 @@ def ulp_bf16(x):
     return np.where(a > 0, np.exp2(e - 7), 0.0)
 
 
+# Every comparison made in this session: (name, rel L2, raw max abs, max abs beyond the
+# allowance, entries whose raw error exceeds the max-abs bound and pass only through the
+# half-ulp allowance, entries compared).  tests/conftest.py prints a summary at the end.
+RECORDS = []
+
+
 def close(name, got, want, rel=REL_L2, atol=MAX_ABS, ulps=0.5):
+    """Asserts the parity bound; returns (rel L2, raw max abs, entries that needed the
+    allowance) and records the comparison in RECORDS."""
     got, want = as64(got), as64(want)
     assert got.shape == want.shape, (name, got.shape, want.shape)
     assert np.isfinite(got).all(), f"{name}: non-finite values"
     diff = got - want
     den = np.linalg.norm(want)
     r = np.linalg.norm(diff) / den if den > 0 else np.linalg.norm(diff)
-    m = np.abs(diff).max() if diff.size else 0.0
-    beyond = (np.abs(diff) - ulps * ulp_bf16(want)).max() if diff.size else 0.0
+    ad = np.abs(diff)
+    m = ad.max() if diff.size else 0.0
+    beyond = (ad - ulps * ulp_bf16(want)).max() if diff.size else 0.0
+    n_allow = int((ad > atol).sum())
+    RECORDS.append((name, float(r), float(m), float(beyond), n_allow, int(diff.size)))
     assert r <= rel and beyond <= atol, (
         f"{name}: rel L2 {r:.3e} (<= {rel}), max abs beyond {ulps} bf16 ulp {beyond:.3e} "
-        f"(<= {atol}), raw max abs {m:.3e}")
-    return r, m
+        f"(<= {atol}), raw max abs {m:.3e}, {n_allow} of {diff.size} entries above {atol} raw")
+    return r, m, n_allow
 
 
 def compare_selection(gpu_idx, ora_idx, gap):

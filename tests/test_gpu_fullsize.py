@@ -122,3 +122,66 @@ def test_fullsize_warmup_sampled():
     close("dk", dk[:, win], ref["dk"][:, win])
     close("dv", dv[:, win], ref["dv"][:, win])
     close("dkp", dkp[:, win], ref["dkp"][:, win])
+
+
+def test_fullsize_multichunk_key_window():
+    """dK / dV / dKp of a mid-sequence key block that tokens of every backward chunk reach, at
+    the 64K workload's full size and launch configuration.
+
+    The backward splits each key block's token list by sequence chunk (16384 tokens at 64K with
+    8 heads per group) and items of different chunks add their dK / dV / dKp into the same rows
+    at different times.  The last-window check above cannot see that (only the last block's
+    tokens reach the last keys).  Here both sides run on one seeded random index map
+    (random_selection, the same input for both) in which block FOCUS is put into the selection of
+    tokens from all four chunks -- 600 of them in one chunk for group 0, so that list spans two
+    work items -- and of nobody else but the block's own tokens.  The oracle then computes every
+    contribution to that block exactly (it visits every row whose key set touches the window)."""
+    from block_sparse_attention_qp_gb300.inputs import force_block, random_selection
+
+    wi, w = [(i + 1, x) for i, x in enumerate(WORKLOADS) if x.name == "msa_s64k_planted"][0]
+    FOCUS = 100  # keys 12800 .. 12927, in the first chunk
+    x = make_inputs(w, workload_seed(wi))
+    idx = random_selection(w.B, w.Hp, w.S, w.top_k, seed=4321, exclude=FOCUS)
+    rng = np.random.default_rng(99)
+    chunk = 16384
+    forced = []
+    for g in range(w.Hp):
+        for c in range(w.S // chunk):
+            lo = max(c * chunk, (FOCUS + 1) * 128)
+            n = 600 if (g == 0 and c == 1) else 20
+            for t in rng.choice(np.arange(lo, (c + 1) * chunk), size=n, replace=False):
+                forced.append((0, g, int(t)))
+    force_block(idx, forced, FOCUS)
+    g_ = {k: v.to(DEV) for k, v in x.items() if isinstance(v, torch.Tensor)}
+    idx_d = torch.from_numpy(idx).to(DEV)
+    o, lse, _ = msa.msa_forward(g_["q"], g_["k"], g_["v"], g_["qp"], g_["kp"], w.top_k, w.scale,
+                                block_idx=idx_d)
+    wsb = msa.workspace(msa.make_shape(g_["q"], g_["k"], g_["qp"], w.top_k, w.scale),
+                        msa.OP_BACKWARD, DEV)
+    dq, dk, dv, dqp, dkp = msa.msa_backward(g_["q"], g_["k"], g_["v"], g_["qp"], g_["kp"], o,
+                                            lse, g_["dout"], idx_d, w.top_k, w.scale, ws=wsb)
+    assert msa.msa_device_status(wsb) == 0
+    del wsb
+    torch.cuda.synchronize()
+    # every token whose key set touches the block: the forced ones and the block's own tokens
+    touch = {t for _, _, t in forced} | set(range(FOCUS * 128, (FOCUS + 1) * 128))
+    toks = {0: touch}
+    q64, do64, qp64 = (_f64_rows(x[n], toks) for n in ("q", "dout", "qp"))
+    k64, v64, kp64 = oracle.f64(x["k"]), oracle.f64(x["v"]), oracle.f64(x["kp"])
+    sample = sorted(rng.choice(sorted(touch), size=24, replace=False).tolist())
+    mask = np.zeros((w.B, w.S), bool)
+    mask[0, sample] = True
+    j0, j1 = FOCUS * 128, (FOCUS + 1) * 128
+    ref = oracle.backward(q64, k64, v64, qp64, kp64, do64, idx, w.top_k, w.scale,
+                          tok_mask=mask, key_window=(j0, j1))
+    print(f"{len(forced)} forced rows over {w.S // chunk} chunks, {len(touch)} tokens reach "
+          f"keys {j0}..{j1 - 1}")
+    close("dk window", dk[:, j0:j1], ref["dk"][:, j0:j1])
+    close("dv window", dv[:, j0:j1], ref["dv"][:, j0:j1])
+    close("dkp window", dkp[:, j0:j1], ref["dkp"][:, j0:j1])
+    close("dq sample", dq[0, sample], ref["dq"][0, sample])
+    close("dqp sample", dqp[0, sample], ref["dqp"][0, sample])
+    frows = np.array([(0, t, h) for t in sample for h in range(w.Hq)], np.int32)
+    o_ref, lse_ref = oracle.forward(q64, k64, v64, idx, w.top_k, w.scale, rows=frows, Hp=w.Hp)
+    close("O sample", o[frows[:, 0], frows[:, 1], frows[:, 2]], o_ref)
+    close("LSE sample", lse[frows[:, 0], frows[:, 2], frows[:, 1]], lse_ref)

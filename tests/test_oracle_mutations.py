@@ -36,11 +36,19 @@ MUTANTS = {
     "padding with block 0": ("for (; w < top_k; ++w) out[w] = -1;", "for (; w < top_k; ++w) out[w] = 0;"),
     "one block too few": ("const int K = top_k < m + 1 ? top_k : m + 1;",
                           "const int K = top_k - 1 < m + 1 ? top_k - 1 : m + 1;"),
+    "near-tie gap always zero": ("*gap = den > 0.0 ? (lo_sel - hi_uns) / den : 0.0;",
+                                 "*gap = 0.0;"),
+    "near-tie gap from the highest selected score": (
+        "if (c[n] < lo_sel) lo_sel = c[n];",
+        "if (lo_sel == INFINITY || c[n] > lo_sel) lo_sel = c[n];"),
+    "near-tie gap not relative": ("*gap = den > 0.0 ? (lo_sel - hi_uns) / den : 0.0;",
+                                  "*gap = lo_sel - hi_uns;"),
 }
 
 PINS = [
     lambda: pins.test_selection_brute_force_properties(3, B=1, S=512),
     lambda: pins.test_selection_ties_prefer_lower_block(),
+    lambda: [pins.test_selection_gap_closed_form(c) for c in sorted(pins.GAP_CASES)],
     lambda: pins.test_full_selection_is_dense_causal_attention(False),
     lambda: pins.test_finite_differences_every_gradient(False, n_coords=2),
     lambda: pins.test_kl_zero_when_student_equals_teacher(2),

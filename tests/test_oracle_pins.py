@@ -112,6 +112,86 @@ def test_selection_ties_prefer_lower_block():
             assert gap[0, gg, t] == 0.0
 
 
+def _uniform_block_keys(vecs, S):
+    """Proxy keys whose 128 rows in block n all equal vecs[n]: block n's score is then exactly
+    scale * qp . vecs[n] (no max over differing keys)."""
+    kp = torch.zeros(1, S, 1, 128)
+    for n, v in enumerate(vecs):
+        kp[0, n * 128:(n + 1) * 128, 0, :] = v
+    return kp.to(torch.bfloat16)
+
+
+def _e(i, a=1.0):
+    v = torch.zeros(128)
+    v[i] = a
+    return v
+
+
+GAP_CASES = {
+    # name: (proxy query row, block key vectors, top_k, {query block m: expected gap})
+    # qp = e0 + e1 and block n = e0 + d_n e1 give block scores scale * (1 + d_n), all exact in
+    # bf16 and fp64; the near-tie gap is (lowest selected - highest unselected non-local score)
+    # / max(|lowest selected|, |highest unselected|).
+    "positive": (_e(0) + _e(1),
+                 [_e(0) + _e(1, 2.0 ** -9), _e(0), _e(0) + _e(1, 2.0 ** -11), _e(0, 0.5),
+                  _e(0) + _e(1, 2.0 ** -7)],
+                 3,
+                 {5: (2.0 ** -9 - 2.0 ** -11) / (1 + 2.0 ** -9),   # picks 4, 0; best left out: 2
+                  4: 2.0 ** -11 / (1 + 2.0 ** -11),               # picks 0, 2; best left out: 1
+                  3: 2.0 ** -11 / (1 + 2.0 ** -11),
+                  2: math.inf, 1: math.inf, 0: math.inf}),      # nothing visible left out
+    # the same keys against -qp: every score changes sign, the order reverses
+    "negative": (-(_e(0) + _e(1)),
+                 [_e(0) + _e(1, 2.0 ** -9), _e(0), _e(0) + _e(1, 2.0 ** -11), _e(0, 0.5),
+                  _e(0) + _e(1, 2.0 ** -7)],
+                 3,
+                 {5: 2.0 ** -11 / (1 + 2.0 ** -11),   # picks 3 (-0.5), 1 (-1); left out: 2
+                  4: 2.0 ** -11 / (1 + 2.0 ** -11),   # visible 0-3: same picks and left-out
+                  3: (2.0 ** -9 - 2.0 ** -11) / (1 + 2.0 ** -9)}),  # picks 1, 2; left out: 0
+    # one non-local pick: +1/4 chosen over -1/4 and -1 -> gap (1/4 + 1/4) / (1/4) = 2
+    "mixed sign": (_e(0) + _e(1), [_e(0, 0.25), _e(0, -0.25), _e(0, -1.0)], 2,
+                   {3: 2.0, 2: 2.0, 1: math.inf}),
+}
+
+
+@pytest.mark.parametrize("case", sorted(GAP_CASES))
+def test_selection_gap_closed_form(case):
+    """The near-tie gap the parity rule excuses mismatches by, on block scores known exactly."""
+    qrow, vecs, top_k, want = GAP_CASES[case]
+    S = 768
+    kp = _uniform_block_keys(vecs, S)
+    qp = qrow.to(torch.bfloat16).expand(1, S, 2, 128).contiguous()
+    scale = 128 ** -0.5
+    idx, gap = oracle.select(qp, kp, top_k, scale)
+    for m, g in want.items():
+        for t in (128 * m, 128 * m + 77, 128 * m + 127):
+            for gg in range(2):
+                if math.isinf(g):
+                    assert math.isinf(gap[0, gg, t]), (case, m, gap[0, gg, t])
+                else:
+                    assert abs(gap[0, gg, t] - g) <= 1e-12 * abs(g), (case, m, gap[0, gg, t], g)
+
+
+def test_selection_gap_brute_force_random():
+    """Gap on random and planted inputs against block scores from a library matmul."""
+    for seed, planted in ((31, 0), (37, 4)):
+        w, x = tiny(S=1024, top_k=4, seed=seed, planted=planted)
+        idx, gap = oracle.select(x["qp"], x["kp"], 4, w.scale)
+        c = block_scores_np(x["qp"], x["kp"], w.scale)
+        for g in range(2):
+            for t in range(0, 1024, 13):
+                m = t // 128
+                sel = [int(n) for n in idx[0, g, t] if 0 <= n < m]
+                rest = [n for n in range(m) if n not in sel]
+                if not sel or not rest:
+                    assert math.isinf(gap[0, g, t])
+                    continue
+                lo = min(c[0, g, t, n] for n in sel)
+                hi = max(c[0, g, t, n] for n in rest)
+                want = (lo - hi) / max(abs(lo), abs(hi))
+                assert want >= 0 and abs(gap[0, g, t] - want) <= 1e-9 * max(1.0, want)
+
+
 def test_selection_k_covers_everything():
     w, x = tiny(S=640, top_k=5, seed=9)
     idx, gap = oracle.select(x["qp"], x["kp"], 5, w.scale)

@@ -59,3 +59,52 @@ def test_noalloc_rejects_shapes_beyond_the_fixed_array():
                                  null, None)
     assert rc == 3  # MSA_ERR_WORKSPACE
     assert b"scratch" in lib.msa_last_error()
+
+
+def _fresh_forward(w, g, idx=None):
+    """msa_forward on a workspace of its own (the comparison for the fixed-array calls)."""
+    return msa.msa_forward(g["q"], g["k"], g["v"], g["qp"], g["kp"], w.top_k, w.scale,
+                           block_idx=idx)
+
+
+def test_noalloc_shapes_in_turn_leave_no_stale_state():
+    """A larger call, then a smaller one with other head counts and top_k, then the first shape
+    again: each must match msa_forward on a fresh workspace, so nothing a call leaves in the
+    shared array (longer lists, more work items) leaks into the next."""
+    lib = msa.load_library()
+    cases = [Workload("big", B=1, S=1024, Hq=8, Hkv=2, Hp=2, top_k=4),
+             Workload("small", B=1, S=512, Hq=16, Hkv=4, Hp=4, top_k=2),
+             Workload("big", B=1, S=1024, Hq=8, Hkv=2, Hp=2, top_k=4)]
+    for n, w in enumerate(cases):
+        x = make_inputs(w, 900 + n)
+        g = {k: v.to(DEV) for k, v in x.items() if isinstance(v, torch.Tensor)}
+        o_ref, lse_ref, idx_ref = _fresh_forward(w, g)
+        shape = msa.make_shape(g["q"], g["k"], g["qp"], w.top_k, w.scale)
+        idx = torch.full_like(idx_ref, -7)
+        o, lse = torch.empty_like(o_ref), torch.empty_like(lse_ref)
+        assert _call_noalloc(lib, shape, g, w.top_k, idx, 0, o, lse) == 0, lib.msa_last_error()
+        assert msa.msa_forward_noalloc_status() == 0
+        assert torch.equal(idx, idx_ref), w.name
+        close("O " + w.name, o, o_ref.float(), rel=1e-5, atol=2e-3, ulps=1.0)
+        close("LSE " + w.name, lse, lse_ref, rel=1e-6, atol=1e-5, ulps=0.0)
+
+
+def test_noalloc_reports_bad_given_indices():
+    """Given indices that are out of range are skipped and flagged; callers of the fixed-array
+    forward read the flag with msa_forward_noalloc_status (they have no workspace pointer)."""
+    lib = msa.load_library()
+    w = Workload("badidx", B=1, S=512, Hq=8, Hkv=2, Hp=2, top_k=3)
+    g = {k: v.to(DEV) for k, v in make_inputs(w, 77).items() if isinstance(v, torch.Tensor)}
+    _, _, idx = _fresh_forward(w, g)
+    bad = idx.clone()
+    bad[0, 0, 300, 0] = 99  # beyond the token's local block
+    shape = msa.make_shape(g["q"], g["k"], g["qp"], w.top_k, w.scale)
+    o = torch.empty(g["q"].shape, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((1, 8, 512), dtype=torch.float32, device=DEV)
+    assert _call_noalloc(lib, shape, g, w.top_k, bad, 1, o, lse) == 0
+    assert msa.msa_forward_noalloc_status() & 1
+    assert torch.isfinite(o.float()).all()
+    assert msa.msa_forward_noalloc_status() == 0  # the read clears the word
+    # a clean call after the bad one reports nothing
+    assert _call_noalloc(lib, shape, g, w.top_k, idx.clone(), 1, o, lse) == 0
+    assert msa.msa_forward_noalloc_status() == 0
