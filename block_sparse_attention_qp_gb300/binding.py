@@ -59,9 +59,10 @@ def load_library(path: str = LIB_PATH):
         lib.msa_workspace_size.argtypes = [SP, I]
         lib.msa_workspace_size.restype = Z
         lib.msa_forward.argtypes = [SP, P, P, P, P, P, P, I, P, P, P, Z, P]
-        lib.msa_backward.argtypes = [SP, P, P, P, P, P, P, P, P, P, F, P, P, P, P, P, P, Z, P]
+        lib.msa_backward.argtypes = [SP, P, P, P, P, P, P, P, P, P, F, P, P, P, P, P, P, P, Z, P]
         lib.msa_warmup_forward.argtypes = [SP, P, P, P, P, P, P, Z, P]
-        lib.msa_warmup_backward.argtypes = [SP, P, P, P, P, P, P, P, P, F, P, P, P, P, P, P, Z, P]
+        lib.msa_warmup_backward.argtypes = [SP, P, P, P, P, P, P, P, P, F, P, P, P, P, P, P, P, Z,
+                                            P]
         lib.msa_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint), P]
         lib.msa_status_string.argtypes = [I]
         lib.msa_status_string.restype = ctypes.c_char_p
@@ -220,8 +221,9 @@ def msa_forward_noalloc_status(device=None) -> int:
 
 
 def msa_backward(q, k, v, qp, kp, o, lse, dout, block_idx, top_k: int, scale: float,
-                 kl_grad: float = 1.0, ws=None):
-    """Sparse backward.  Returns (dq, dk, dv, dqp, dkp)."""
+                 kl_grad: float = 1.0, ws=None, return_kl: bool = False):
+    """Sparse backward.  Returns (dq, dk, dv, dqp, dkp), plus the KL value L_KL as a 0-d fp32
+    CUDA tensor when return_kl (computed on the device; no host synchronisation)."""
     B, S, Hq, D = q.shape
     Hp = qp.shape[2]
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (qp, "qp"), (kp, "kp"), (o, "o"), (dout, "dout")):
@@ -230,13 +232,14 @@ def msa_backward(q, k, v, qp, kp, o, lse, dout, block_idx, top_k: int, scale: fl
     _req(block_idx, "block_idx", torch.int32, (B, Hp, S, top_k))
     shape = make_shape(q, k, qp, top_k, scale)
     grads = [torch.empty_like(x) for x in (q, k, v, qp, kp)]
+    kl = torch.empty((), dtype=torch.float32, device=q.device) if return_kl else None
     if ws is None:
         ws = workspace(shape, OP_BACKWARD, q.device)
     _check(load_library().msa_backward(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(qp),
                                        _ptr(kp), _ptr(o), _ptr(lse), _ptr(dout), _ptr(block_idx),
-                                       float(kl_grad), *map(_ptr, grads), _ptr(ws), ws.numel(),
-                                       _stream(q.device)), "msa_backward")
-    return tuple(grads)
+                                       float(kl_grad), *map(_ptr, grads), _ptr(kl), _ptr(ws),
+                                       ws.numel(), _stream(q.device)), "msa_backward")
+    return tuple(grads) + ((kl,) if return_kl else ())
 
 
 def msa_warmup_forward(q, k, v, scale: float, ws=None):
@@ -256,22 +259,24 @@ def msa_warmup_forward(q, k, v, scale: float, ws=None):
 
 
 def msa_warmup_backward(q, k, v, qp, kp, o, lse, dout, scale: float, kl_grad: float = 1.0,
-                        ws=None):
-    """Dense warmup backward (proxy KL over the full causal prefix).  Returns grads."""
+                        ws=None, return_kl: bool = False):
+    """Dense warmup backward (proxy KL over the full causal prefix).  Returns grads (and the KL
+    value as a 0-d fp32 CUDA tensor when return_kl)."""
     B, S, Hq, D = q.shape
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (qp, "qp"), (kp, "kp"), (o, "o"), (dout, "dout")):
         _req(t, n)
     _req(lse, "lse", torch.float32, (B, Hq, S))
     shape = make_shape(q, k, qp, 0, scale)
     grads = [torch.empty_like(x) for x in (q, k, v, qp, kp)]
+    kl = torch.empty((), dtype=torch.float32, device=q.device) if return_kl else None
     if ws is None:
         ws = workspace(shape, OP_WARMUP_BACKWARD, q.device)
     _check(load_library().msa_warmup_backward(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v),
                                               _ptr(qp), _ptr(kp), _ptr(o), _ptr(lse), _ptr(dout),
-                                              float(kl_grad), *map(_ptr, grads), _ptr(ws),
-                                              ws.numel(), _stream(q.device)),
+                                              float(kl_grad), *map(_ptr, grads), _ptr(kl),
+                                              _ptr(ws), ws.numel(), _stream(q.device)),
            "msa_warmup_backward")
-    return tuple(grads)
+    return tuple(grads) + ((kl,) if return_kl else ())
 
 
 class _MSAFunction(torch.autograd.Function):

@@ -162,7 +162,7 @@ Plan make_plan(const Dims& d, int op) {
       p.io0 = c.take(nseg * sizeof(int));
       p.items0 = c.take(p.max0 * sizeof(Item));
     } else {
-      p.spec0 = ItemSpec{kBlock, 1};  // proxy normaliser items
+      p.spec0 = ItemSpec{kBlock, fwd_item_tiles()};  // proxy normaliser items (128-token tiles)
       p.spec1 = fused;
       p.max0 = max_items(ent, d, p.spec0);
       p.max1 = max_items(ent, d, p.spec1);
@@ -174,7 +174,7 @@ Plan make_plan(const Dims& d, int op) {
     }
     p.lse_px = c.take((size_t)rows_p * sizeof(float));
     p.rowm = c.take((size_t)rows_q * sizeof(float2));  // {LSE log2 e, D} per query row
-    p.pbar = c.take((size_t)ent * kBlock * sizeof(float));  // teacher rows, one per list entry
+    p.pbar = c.take((size_t)ent * kBlock * sizeof(uint16_t));  // teacher rows (fp16), one per entry
     p.lpxe = c.take((size_t)ent * sizeof(float));            // proxy log-normaliser per entry
     p.emeta = c.take((size_t)ent * d.G * sizeof(float2));    // rowm per entry and head
     p.dq = c.take((size_t)rows_q * kD * sizeof(float));
@@ -277,6 +277,21 @@ int check_ptrs(std::initializer_list<const void*> ptrs) {
 template <typename T>
 T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+int check_kl(const float* kl_out) {
+  if (reinterpret_cast<uintptr_t>(kl_out) % 4 != 0) {
+    set_err("kl_out must be 4-byte aligned");
+    return MSA_ERR_INVALID_ARG;
+  }
+  return MSA_OK;
+}
+
+// The KL accumulator: a double at byte 128 of the workspace's status area, zeroed on the stream.
+double* kl_accumulator(void* ws, const Plan& p, cudaStream_t st) {
+  double* acc = at<double>(ws, p.status + 128);
+  cudaMemsetAsync(acc, 0, sizeof(double), st);
+  return acc;
 }
 
 int check_ws(const Plan& p, void* ws, size_t bytes) {
@@ -399,12 +414,13 @@ int msa_forward(const msa_shape_t* shape, const void* q, const void* k, const vo
 int msa_backward(const msa_shape_t* shape, const void* q, const void* k, const void* v,
                  const void* qp, const void* kp, const void* o, const float* lse,
                  const void* dout, const int32_t* block_idx, float kl_grad, void* dq, void* dk,
-                 void* dv, void* dqp, void* dkp, void* workspace, size_t workspace_bytes,
-                 void* stream) {
+                 void* dv, void* dqp, void* dkp, float* kl_out, void* workspace,
+                 size_t workspace_bytes, void* stream) {
   Dims d;
   int rc = check_shape(shape, MSA_OP_BACKWARD, &d);
   if (rc) return rc;
   if ((rc = check_ptrs({q, k, v, qp, kp, o, lse, dout, block_idx, dq, dk, dv, dqp, dkp}))) return rc;
+  if (kl_out && (rc = check_kl(kl_out))) return rc;
   const Plan p = make_plan(d, MSA_OP_BACKWARD);
   if ((rc = check_ws(p, workspace, workspace_bytes))) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -413,15 +429,23 @@ int msa_backward(const msa_shape_t* shape, const void* q, const void* k, const v
   zero_grads(d, p, workspace, st);
   build_lists(d, p, block_idx, workspace, 2, st);
   timed("bwd_rowdot", st, [&] { launch_bwd_rowdot(d, o, dout, lse, at<float2>(workspace, p.rowm), st); });
+  // partial normalisers of slots no list entry reaches stay NaN (all-ones bytes)
+  cudaMemsetAsync(at<float>(workspace, p.lpx_part), 0xff,
+                  (size_t)d.B * d.S * d.Hp * d.top_k * sizeof(float), st);
+  bool lok = true;
   timed("proxy_lse", st, [&] {
-    launch_proxy_lse_sparse(d, qp, kp, at<int>(workspace, p.seg_offset),
-                            at<int>(workspace, p.entries), at<Item>(workspace, p.items0),
-                            at<int>(workspace, p.totals) + 1, p.max0,
-                            at<float>(workspace, p.lpx_part), st);
+    lok = launch_proxy_lse_sparse(d, qp, kp, at<int>(workspace, p.seg_offset),
+                                  at<int>(workspace, p.entries), at<Item>(workspace, p.items0),
+                                  at<int>(workspace, p.totals) + 1, p.max0,
+                                  at<float>(workspace, p.lpx_part), at<unsigned>(workspace, p.status),
+                                  st);
   });
+  if (!lok) {
+    set_err("msa_backward: could not create TMA tensor maps (cuTensorMapEncodeTiled)");
+    return MSA_ERR_CUDA;
+  }
   timed("proxy_lse_combine", st, [&] {
-    launch_proxy_lse_combine(d, block_idx, at<float>(workspace, p.lpx_part),
-                             at<float>(workspace, p.lse_px), st);
+    launch_proxy_lse_combine(d, at<float>(workspace, p.lpx_part), at<float>(workspace, p.lse_px), st);
   });
   timed("entry_meta", st, [&] {
     launch_entry_meta(d, false, at<int>(workspace, p.seg_count), at<int>(workspace, p.seg_offset),
@@ -435,21 +459,24 @@ int msa_backward(const msa_shape_t* shape, const void* q, const void* k, const v
                          at<int>(workspace, p.seg_offset), at<int>(workspace, p.entries),
                          at<Item>(workspace, p.items1), at<int>(workspace, p.totals) + 2, p.max1,
                          at<float>(workspace, p.dq), at<float>(workspace, p.dk),
-                         at<float>(workspace, p.dv), at<float>(workspace, p.pbar),
+                         at<float>(workspace, p.dv), at<void>(workspace, p.pbar),
                          at<unsigned>(workspace, p.status), st);
   });
+  double* kl_acc = kl_out ? kl_accumulator(workspace, p, st) : nullptr;
   if (ok)
     timed("proxy_bwd", st, [&] {
       ok = launch_proxy_bwd(d, false, qp, kp, at<float>(workspace, p.lpxe),
-                            at<float>(workspace, p.pbar), kl_grad, at<int>(workspace, p.seg_offset),
+                            at<void>(workspace, p.pbar), kl_grad, at<int>(workspace, p.seg_offset),
                             at<int>(workspace, p.entries), at<Item>(workspace, p.items1),
                             at<int>(workspace, p.totals) + 2, p.max1, at<float>(workspace, p.dqp),
-                            at<float>(workspace, p.dkp), at<unsigned>(workspace, p.status), st);
+                            at<float>(workspace, p.dkp), kl_acc, at<unsigned>(workspace, p.status),
+                            st);
     });
   if (!ok) {
     set_err("msa_backward: could not create TMA tensor maps (cuTensorMapEncodeTiled)");
     return MSA_ERR_CUDA;
   }
+  if (kl_out) timed("kl_finalize", st, [&] { launch_kl_finalize(d, kl_acc, kl_out, st); });
   emit_grads(d, p, workspace, dq, dk, dv, dqp, dkp, st);
   return cuda_fail("msa_backward");
 }
@@ -466,18 +493,27 @@ int msa_warmup_forward(const msa_shape_t* shape, const void* q, const void* k, c
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaGetLastError();
   cudaMemsetAsync(at<char>(workspace, p.status), 0, sizeof(unsigned), st);
-  timed("dense_fwd", st, [&] { launch_dense_fwd(d, q, k, v, o, lse, st); });
+  bool ok = true;
+  timed("dense_fwd", st, [&] {
+    ok = launch_dense_fwd(d, q, k, v, o, lse, at<unsigned>(workspace, p.status), st);
+  });
+  if (!ok) {
+    set_err("msa_warmup_forward: could not create TMA tensor maps (cuTensorMapEncodeTiled)");
+    return MSA_ERR_CUDA;
+  }
   return cuda_fail("msa_warmup_forward");
 }
 
 int msa_warmup_backward(const msa_shape_t* shape, const void* q, const void* k, const void* v,
                         const void* qp, const void* kp, const void* o, const float* lse,
                         const void* dout, float kl_grad, void* dq, void* dk, void* dv, void* dqp,
-                        void* dkp, void* workspace, size_t workspace_bytes, void* stream) {
+                        void* dkp, float* kl_out, void* workspace, size_t workspace_bytes,
+                        void* stream) {
   Dims d;
   int rc = check_shape(shape, MSA_OP_WARMUP_BACKWARD, &d);
   if (rc) return rc;
   if ((rc = check_ptrs({q, k, v, qp, kp, o, lse, dout, dq, dk, dv, dqp, dkp}))) return rc;
+  if (kl_out && (rc = check_kl(kl_out))) return rc;
   const Plan p = make_plan(d, MSA_OP_WARMUP_BACKWARD);
   if ((rc = check_ws(p, workspace, workspace_bytes))) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -495,7 +531,14 @@ int msa_warmup_backward(const msa_shape_t* shape, const void* q, const void* k, 
                  at<Item>(workspace, p.items0), p.max0, status, st);
   });
   timed("bwd_rowdot", st, [&] { launch_bwd_rowdot(d, o, dout, lse, at<float2>(workspace, p.rowm), st); });
-  timed("proxy_lse_dense", st, [&] { launch_proxy_lse_dense(d, qp, kp, at<float>(workspace, p.lse_px), st); });
+  bool lok = true;
+  timed("proxy_lse_dense", st, [&] {
+    lok = launch_proxy_lse_dense(d, qp, kp, at<float>(workspace, p.lse_px), status, st);
+  });
+  if (!lok) {
+    set_err("msa_warmup_backward: could not create TMA tensor maps (cuTensorMapEncodeTiled)");
+    return MSA_ERR_CUDA;
+  }
   timed("entry_meta", st, [&] {
     launch_entry_meta(d, true, nullptr, at<int>(workspace, p.seg_offset), nullptr,
                       at<float>(workspace, p.lse_px), at<float2>(workspace, p.rowm),
@@ -507,20 +550,22 @@ int msa_warmup_backward(const msa_shape_t* shape, const void* q, const void* k, 
                          at<int>(workspace, p.seg_offset), nullptr, at<Item>(workspace, p.items0),
                          at<int>(workspace, p.totals) + 1, p.max0, at<float>(workspace, p.dq),
                          at<float>(workspace, p.dk), at<float>(workspace, p.dv),
-                         at<float>(workspace, p.pbar), status, st);
+                         at<void>(workspace, p.pbar), status, st);
   });
+  double* kl_acc = kl_out ? kl_accumulator(workspace, p, st) : nullptr;
   if (ok)
     timed("proxy_bwd_dense", st, [&] {
       ok = launch_proxy_bwd(d, true, qp, kp, at<float>(workspace, p.lpxe),
-                            at<float>(workspace, p.pbar), kl_grad, at<int>(workspace, p.seg_offset),
+                            at<void>(workspace, p.pbar), kl_grad, at<int>(workspace, p.seg_offset),
                             nullptr, at<Item>(workspace, p.items0), at<int>(workspace, p.totals) + 1,
                             p.max0, at<float>(workspace, p.dqp), at<float>(workspace, p.dkp),
-                            status, st);
+                            kl_acc, status, st);
     });
   if (!ok) {
     set_err("msa_warmup_backward: could not create TMA tensor maps (cuTensorMapEncodeTiled)");
     return MSA_ERR_CUDA;
   }
+  if (kl_out) timed("kl_finalize", st, [&] { launch_kl_finalize(d, kl_acc, kl_out, st); });
   emit_grads(d, p, workspace, dq, dk, dv, dqp, dkp, st);
   return cuda_fail("msa_warmup_backward");
 }

@@ -20,6 +20,12 @@
 // in place), O0, O1.
 // The MMA issuer runs S of tile i before O of tile i-1, so the tensor pipe works on one tile while
 // the softmax warps work on the next.  Every wait is bounded (see sm100::mbar_wait).
+//
+// kProxy = true runs the same pipeline as the sparse proxy normaliser of the backward (blog,
+// "Proxy attention" and "Backward": the student's log-sum-exp over the selected tokens is
+// recomputed there, not kept from the forward): rows are tokens (G = 1) of proxy head g, the ring
+// holds only proxy-key blocks, each tile runs S = Qp Kp^T alone (no V, no O), and the softmax
+// warps write the natural log-sum-exp of scale * S over each (token, slot)'s visible keys.
 #include <math.h>
 
 #include "common.cuh"
@@ -81,12 +87,13 @@ __device__ __forceinline__ RingPos ring_pos(long long load) {
 
 }  // namespace
 
-template <int G>
+template <int G, bool kProxy>
 __global__ void __launch_bounds__(448, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     FwdArgs A) {
   using namespace sm100;
   constexpr int TT = kFwdRows / G;  // tokens per tile
+  constexpr int kLoads = kProxy ? 1 : 2;  // ring loads per item: K (or Kp) and V
   const Dims& d = A.d;
 
   extern __shared__ uint8_t smem_raw[];
@@ -185,7 +192,8 @@ __global__ void __launch_bounds__(448, 1)
       const int bg = (int)((item.seg % d.nseg()) / d.nblk);
       const int b = bg / d.Hp, g = bg % d.Hp;
       const int row0 = b * d.S + n * kBlock;
-      for (int w = 0; w < 2; ++w) {
+      const int kvh = kProxy ? 0 : g;  // the proxy key head is shared by every group
+      for (int w = 0; w < kLoads; ++w) {
         const RingPos rp = ring_pos(nl);
         if (rp.use >= 1 && !mbar_wait_warp(&sh->kv_empty[rp.slot], rp.parity ^ 1u, A.status)) {
           ok = false;
@@ -195,8 +203,8 @@ __global__ void __launch_bounds__(448, 1)
           uint8_t* dst = sR + rp.slot * kFwdTile;
           const CUtensorMap* tm = w == 0 ? &tm_k : &tm_v;
           mbar_expect_tx(&sh->kv_full[rp.slot], kFwdTile);
-          tma_load_3d(dst, tm, 0, g, row0, &sh->kv_full[rp.slot]);
-          tma_load_3d(dst + kFwdTile / 2, tm, 64, g, row0, &sh->kv_full[rp.slot]);
+          tma_load_3d(dst, tm, 0, kvh, row0, &sh->kv_full[rp.slot]);
+          tma_load_3d(dst + kFwdTile / 2, tm, 64, kvh, row0, &sh->kv_full[rp.slot]);
         }
         __syncwarp();
         ++nl;
@@ -240,20 +248,24 @@ __global__ void __launch_bounds__(448, 1)
       if (!take_item(ni, it)) { ok = false; break; }
       if (it >= total) break;
       const Item item = A.items[it];
-      const RingPos kp = ring_pos(2 * ni), vp = ring_pos(2 * ni + 1);
+      const RingPos kp = ring_pos(kLoads * ni), vp = ring_pos(kLoads * ni + 1);
       if (!mbar_wait_warp(&sh->kv_full[kp.slot], kp.parity, A.status)) { ok = false; break; }
       const uint32_t aK = aR + kp.slot * kFwdTile;
       const int ntiles = (item.count + TT - 1) / TT;
       if (ntiles == 0) {  // (items are never empty)
         if (lane == 0) mma_commit(&sh->kv_empty[kp.slot]);
-        if (!mbar_wait_warp(&sh->kv_full[vp.slot], vp.parity, A.status)) { ok = false; break; }
-        if (lane == 0) mma_commit(&sh->kv_empty[vp.slot]);
+        if (!kProxy) {
+          if (!mbar_wait_warp(&sh->kv_full[vp.slot], vp.parity, A.status)) { ok = false; break; }
+          if (lane == 0) mma_commit(&sh->kv_empty[vp.slot]);
+        }
       }
       for (int tl = 0; tl < ntiles; ++tl, ++i) {
         const int b = (int)(i & 1), qb = (int)(i % kQBuf);
         if (!mbar_wait_warp(&sh->q_full[qb], par(i / kQBuf), A.status)) { ok = false; break; }
-        // S_b still holds P of tile i-2 until that tile's O product has completed
-        if (i >= 2 && !mbar_wait_warp(&sh->o_full[b], par((i - 2) >> 1), A.status)) { ok = false; break; }
+        // S_b still holds P of tile i-2 until that tile's O product has completed (proxy mode: until
+        // the softmax warps have read S of tile i-2)
+        if (i >= 2 && !mbar_wait_warp(kProxy ? &sh->p_full[b] : &sh->o_full[b], par((i - 2) >> 1),
+                                      A.status)) { ok = false; break; }
         // the Q rows were written by other threads' cp.async (generic proxy) and only tracked by
         // the barrier: order them before the tensor core's (async proxy) reads
         fence_async_smem();
@@ -268,6 +280,7 @@ __global__ void __launch_bounds__(448, 1)
           if (tl == ntiles - 1) mma_commit(&sh->kv_empty[kp.slot]);
         }
         __syncwarp();
+        if (kProxy) continue;
         if (p_ti >= 0 && !mma_o(p_ti, p_vslot, p_vpar, p_first, p_last)) { ok = false; break; }
         p_ti = i;
         p_vslot = vp.slot;
@@ -276,7 +289,7 @@ __global__ void __launch_bounds__(448, 1)
         p_last = tl == ntiles - 1;
       }
     }
-    if (ok && p_ti >= 0) mma_o(p_ti, p_vslot, p_vpar, p_first, p_last);
+    if (!kProxy && ok && p_ti >= 0) mma_o(p_ti, p_vslot, p_vpar, p_first, p_last);
     if (lane == 0) mma_commit(&sh->mma_done);
     __syncwarp();
     mbar_wait_warp(&sh->mma_done, 0, A.status);
@@ -410,7 +423,7 @@ __global__ void __launch_bounds__(448, 1)
               lc += a1;
               pw[c] = pack_bf16(a0, a1);
             }
-            tmem_st16(Sb + q * 16, pw);
+            if constexpr (!kProxy) tmem_st16(Sb + q * 16, pw);
           }
           l = la + lc;
         } else {
@@ -444,7 +457,7 @@ __global__ void __launch_bounds__(448, 1)
               l += a0 + a1;
               pw[c] = pack_bf16(a0, a1);
             }
-            tmem_st16(Sb + q * 16, pw);
+            if constexpr (!kProxy) tmem_st16(Sb + q * 16, pw);
           }
         }
         const bool valid = t >= 0;
@@ -454,7 +467,11 @@ __global__ void __launch_bounds__(448, 1)
         tmem_wait_st();
         fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sh->p_full[bb]);
+        if (lane == 0) mbar_arrive(&sh->p_full[bb]);  // proxy mode: S_b read
+        if constexpr (kProxy) {  // the partial log-sum-exp is all the proxy normaliser needs
+          if (valid) A.lpart[dst] = lse;
+          continue;
+        }
         // ---- epilogue of this tile: O / l -> bf16 partials, 32 columns at a time through the
         // warp's staging rows (16-byte chunks rotated by row pair: conflict-free both ways),
         // leaving as 8 rows x 64 contiguous bytes per store instruction
@@ -508,12 +525,13 @@ __global__ void __launch_bounds__(448, 1)
   if (warp == 0) tmem_dealloc(tmem, 512);
 }
 
-template <int G>
+template <int G, bool kProxy>
 static void attn_fwd_g(const CUtensorMap& mk, const CUtensorMap& mv, const FwdArgs& a,
                        cudaStream_t st) {
   const size_t smem = sizeof(FwdShared) + 1024 + (kRing + kQBuf) * kFwdTile + 8 * kStageWarp;
-  cudaFuncSetAttribute(attn_fwd_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  attn_fwd_kernel<G><<<num_sms(), 448, smem, st>>>(mk, mv, a);
+  cudaFuncSetAttribute(attn_fwd_kernel<G, kProxy>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       (int)smem);
+  attn_fwd_kernel<G, kProxy><<<num_sms(), 448, smem, st>>>(mk, mv, a);
 }
 
 int fwd_item_tiles() { return kFwdItemTiles; }
@@ -542,13 +560,41 @@ bool launch_attn_fwd(const Dims& d, const void* q, const void* k, const void* v,
   a.sched = reinterpret_cast<int*>(status + kSchedAttnFwd);
   cudaMemsetAsync(a.sched, 0, sizeof(int), st);
   switch (d.G) {
-    case 1: attn_fwd_g<1>(mk, mv, a, st); break;
-    case 2: attn_fwd_g<2>(mk, mv, a, st); break;
-    case 4: attn_fwd_g<4>(mk, mv, a, st); break;
-    case 8: attn_fwd_g<8>(mk, mv, a, st); break;
-    case 16: attn_fwd_g<16>(mk, mv, a, st); break;
+    case 1: attn_fwd_g<1, false>(mk, mv, a, st); break;
+    case 2: attn_fwd_g<2, false>(mk, mv, a, st); break;
+    case 4: attn_fwd_g<4, false>(mk, mv, a, st); break;
+    case 8: attn_fwd_g<8, false>(mk, mv, a, st); break;
+    case 16: attn_fwd_g<16, false>(mk, mv, a, st); break;
     default: return false;
   }
+  return true;
+}
+
+bool launch_proxy_lse_sparse(const Dims& d, const void* qp, const void* kp, const int* seg_offset,
+                             const int* entries, const Item* items, const int* n_items,
+                             long long max_items, float* lpx_part, unsigned* status,
+                             cudaStream_t st) {
+  CUtensorMap mk;
+  const uint64_t kd[3] = {128, 1, (uint64_t)d.B * d.S};
+  const uint64_t ks[2] = {128 * 2, 128 * 2};
+  const uint32_t kb[3] = {64, 1, 128};
+  if (!make_tmap_bf16(&mk, kp, 3, kd, ks, kb)) return false;
+  FwdArgs a;
+  a.d = d;
+  a.d.Hq = d.Hp;  // rows are the proxy heads' query rows: one per (token, group)
+  a.d.G = 1;
+  a.q = (const bf16*)qp;
+  a.seg_offset = seg_offset;
+  a.entries = entries;
+  a.items = items;
+  a.n_items = n_items;
+  a.max_items = max_items;
+  a.opart = nullptr;
+  a.lpart = lpx_part;
+  a.status = status;
+  a.sched = reinterpret_cast<int*>(status + kSchedProxyLse);
+  cudaMemsetAsync(a.sched, 0, sizeof(int), st);
+  attn_fwd_g<1, true>(mk, mk, a, st);
   return true;
 }
 

@@ -15,7 +15,7 @@
 //   softmax (4 warps, thread = key)
 //                          P^T  = exp(scale S^T - LSE_row)       -> tensor memory (bf16)
 //                          dS^T = P^T (dP^T - D_row)             -> shared memory (bf16)
-//                          teacher pbar = mean over the token's G heads of P -> global (fp32)
+//                          teacher pbar = mean over the token's G heads of P -> global (fp16)
 //   phase 2 (tensor core)  dV += P^T dO,  dK += dS^T Q,  dQ^T = K^T dS^T
 //   epilogue               dQ^T -> fp32 rows staged in the tile's own slot; a reducer thread adds
 //                          each token's G rows into dQ with one bulk TMA reduction
@@ -30,6 +30,7 @@
 // and tensor-memory ownership, warp 1 the MMA issuer, warps 2 and 8-10 gather the tile's Q / dO
 // rows with cp.async, warp 3 issues the dQ bulk reductions, warps 4-7 softmax / epilogue.  Tensor
 // memory (512 columns): SB0, SB1 (S^T, then P^T), DB0, DB1 (dP^T, then dQ^T), dV, dK.
+#include <cuda_fp16.h>
 #include <math.h>
 
 #include "common.cuh"
@@ -107,7 +108,8 @@ struct MainArgs {
   const Item* items;
   const int* n_items;
   long long max_items;
-  float *dq, *dk, *dv, *pbar;
+  float *dq, *dk, *dv;
+  __half* pbar;  // teacher rows [list entry][128 keys]: probabilities in [0, 1], fp16
   unsigned* status;
   int* sched;  // work-item counter (zero at launch): blocks take items in order as they get free
 };
@@ -125,7 +127,8 @@ struct MainShared {
 struct ProxyArgs {
   Dims d;
   const bf16* qp;
-  const float *lpxe, *pbar;  // per list entry: LSE_px x log2 e, teacher row [128 keys]
+  const float* lpxe;   // per list entry: LSE_px x log2 e
+  const __half* pbar;  // per list entry: teacher row [128 keys] (fp16)
   float cz;  // kl_grad / (B * S * Hp)
   const int* seg_offset;
   const int* entries;
@@ -133,18 +136,20 @@ struct ProxyArgs {
   const int* n_items;
   long long max_items;
   float *dqp, *dkp;
+  double* kl_acc;  // kKL: sum of pbar (ln pbar - ln p_student) over the visited pairs
   unsigned* status;
   int* sched;  // work-item counter (zero at launch)
 };
 
 constexpr int kQPB = 3;  // proxy query row buffers
+constexpr int kNPB = 4;  // teacher row buffers (64 entries x 128 keys fp16 each)
 
 struct ProxyShared {
-  int tok[2][kPG];     // per teacher buffer (read by the dz warps)
-  float lpx2[2][kPG];
+  int tok[kNPB][kPG];     // per teacher buffer (read by the dz warps)
+  float lpx2[kNPB][kPG];
   int tokq[kQPB][kPG];  // per query-row buffer (read by the dQp-flush warps)
   int it_ring[kIR];  // item numbers taken by this block, in order (>= total: no more)
-  uint64_t kp_full, kp_empty, qp_full[kQPB], qp_empty[kQPB], pb_full[2], meta_free[2], z_full[2],
+  uint64_t kp_full, kp_empty, qp_full[kQPB], qp_empty[kQPB], pb_full[kNPB], meta_free[kNPB], z_full[2],
       dz_full, fl_full[2], fl_free, acc_free, it_full[kIR], it_empty[kIR];
   uint32_t tmem;
 };
@@ -152,6 +157,11 @@ struct ProxyShared {
 __device__ __forceinline__ void red4(float* p, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"l"(p), "f"(a), "f"(b), "f"(c),
                "f"(d)
+               : "memory");
+}
+__device__ __forceinline__ void st_global_h_hint(__half* p, float v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.b16 [%0], %1, %2;\n" ::"l"(p),
+               "h"(__half_as_ushort(__float2half_rn(v))), "l"(pol)
                : "memory");
 }
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
@@ -200,10 +210,12 @@ __global__ void __launch_bounds__(352, 1)
                     MainArgs A) {
   using namespace sm100;
   constexpr int TT = kTR / G;  // tokens per tile
-  // With 16 heads per group, up to 16 x (tokens) rows add into each key's dV; P rounded once to
-  // bf16 for dV = P^T dO then costs up to ~2e-2 on the largest entries.  P^T is then written as
-  // its bf16 value plus the bf16 residual P - bf16(P) (columns 32-63 of the same buffer) and dV
-  // takes both: dV += P_hi^T dO + P_lo^T dO (P to ~16 significant bits; four more MMAs a tile).
+  // With 16 heads per group, up to 16 x (tokens) rows add into each key's dV and dK; P and dS
+  // rounded once to bf16 for dV = P^T dO and dK = dS^T Q then cost up to ~2e-2 on the largest
+  // entries.  So P^T is written as its bf16 value plus the bf16 residual P - bf16(P) (columns 32-63
+  // of the same buffer), dS^T's residual goes to the dP^T buffer (its columns are read just before,
+  // and dQ^T overwrites them only after the dK products, in issue order), and dV, dK take both
+  // parts (to ~16 significant bits; eight more MMAs a tile).
   constexpr bool kSplitP = G >= 16;
   const Dims& d = A.d;
 
@@ -333,6 +345,11 @@ __global__ void __launch_bounds__(352, 1)
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)  // dK += dS^T Q
           mma_ss(RK, desc_kmajor(adSb, 128, ks), desc_mnmajor(aQb, kTR, ks), id_g, acc || ks > 0);
+        if constexpr (kSplitP) {
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)  // dK += dS_lo^T Q  (the bf16 residual, from DB_b)
+            mma_ts(RK, DBb + ks * 8, desc_mnmajor(aQb, kTR, ks), id_g, true);
+        }
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)  // dQ^T = K^T dS^T
           mma_ss(DBb, desc_mnmajor(aK, 128, ks), desc_mnmajor(adSb, 128, ks), id_q, ks > 0);
@@ -561,7 +578,7 @@ __global__ void __launch_bounds__(352, 1)
           tmem_ld32(DBb + lb + 32 * c, rp);
           tmem_wait_ld();
           uint32_t pw[16], dw[16];
-          uint32_t lw[kSplitP ? 16 : 1];
+          uint32_t lw[kSplitP ? 16 : 1], dlw[kSplitP ? 16 : 1];
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4) {
             const float4 l4 = reinterpret_cast<const float4*>(sh->lse2[sl])[c * 8 + q4];
@@ -589,11 +606,15 @@ __global__ void __launch_bounds__(352, 1)
               for (int h2 = 0; h2 < 2; ++h2) {
                 const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&pw[2 * q4 + h2]);
                 lw[2 * q4 + h2] = pack_bf16(pv[2 * h2] - __low2float(hi), pv[2 * h2 + 1] - __high2float(hi));
+                const __nv_bfloat162 dh = *reinterpret_cast<const __nv_bfloat162*>(&dw[2 * q4 + h2]);
+                dlw[2 * q4 + h2] = pack_bf16(dsv[2 * h2] - __low2float(dh), dsv[2 * h2 + 1] - __high2float(dh));
               }
             }
           }
           tmem_st16(SBb + lb + c * 16, pw);  // P^T: row r packed into column r / 2
           if constexpr (kSplitP) {
+            // dS^T residual of these 32 rows over dP^T columns 16 c .. 16 c + 15, already read
+            tmem_st16(DBb + lb + c * 16, dlw);
             if (c == 0) {
 #pragma unroll
               for (int u = 0; u < 16; ++u) lw0[u] = lw[u];
@@ -616,7 +637,7 @@ __global__ void __launch_bounds__(352, 1)
 #pragma unroll
         for (int x = 0; x < TT; ++x)
           if (tv[x] >= 0)
-            st_global_f32_hint(A.pbar + (size_t)(eb + tl * TT + x) * kBlock + kr, pb[x] * (1.f / G), stream);
+            st_global_h_hint(A.pbar + (size_t)(eb + tl * TT + x) * kBlock + kr, pb[x] * (1.f / G), stream);
         // ---- epilogue of the previous tile
         if (tl > 0 && !epilogue(i - 1)) { ok = false; break; }
       }
@@ -660,7 +681,7 @@ __global__ void __launch_bounds__(352, 1)
 // item end, warps 8-11 flush dQp.  Tensor memory (512 columns allocated): Z0, Z1 (z^T, 64 each,
 // alternate groups), QP (dQp^T, 64), KP (dKp accumulator, 128).  dz^T is double-buffered in
 // shared memory, so the dz of one group overlaps the products and the flush of the previous one.
-template <bool kDense>
+template <bool kDense, bool kKL>
 __global__ void __launch_bounds__(384, 1)
     proxy_bwd_kernel(const __grid_constant__ CUtensorMap tm_kp, ProxyArgs A) {
   using namespace sm100;
@@ -671,8 +692,8 @@ __global__ void __launch_bounds__(384, 1)
   uint8_t* sKp = base;             // [128 keys][128 d]  (TMA)
   uint8_t* sQp = sKp + kKV;        // [kQPB][64 tokens][128 d]
   uint8_t* sdz = sQp + kQPB * kRT;  // [2] dz^T [128 keys][64 tokens]
-  float* sPb = reinterpret_cast<float*>(sdz + 2 * kST);  // [2][64 entries][128 keys] fp32
-  float* sStg = sPb + 2 * kPG * kBlock;               // dQp staging: [4 warps][64 tokens][32 d] fp32
+  __half* sPb = reinterpret_cast<__half*>(sdz + 2 * kST);  // [kNPB][64 entries][128 keys] fp16
+  float* sStg = reinterpret_cast<float*>(sPb + kNPB * kPG * kBlock);  // dQp staging: [4 warps][64 tokens][32 d]
   const uint32_t aKp = smem_u32(sKp), aQp = smem_u32(sQp), adz = smem_u32(sdz);
 
   const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
@@ -687,10 +708,12 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&sh->qp_empty[x], 5);   // the MMA's commit and the 4 dQp-flush warps
     }
     for (int x = 0; x < 2; ++x) {
-      mbar_init(&sh->pb_full[x], 64);  // the gather lanes (one with the bulk copy's expect-tx)
-      mbar_init(&sh->meta_free[x], 4);  // the dz warps
       mbar_init(&sh->z_full[x], 1);
       mbar_init(&sh->fl_full[x], 1);
+    }
+    for (int x = 0; x < kNPB; ++x) {
+      mbar_init(&sh->pb_full[x], 64);   // the gather lanes (one with the bulk copy's expect-tx)
+      mbar_init(&sh->meta_free[x], 4);  // the dz warps
     }
     mbar_init(&sh->dz_full, 4);
     mbar_init(&sh->fl_free, 4);
@@ -845,10 +868,10 @@ __global__ void __launch_bounds__(384, 1)
       int t_next = load_row(cur, 0, lp_next);
       long long i = 0;
       while (true) {
-        const int pb = (int)(i & 1), qb = (int)(i % kQPB);
+        const int pb = (int)(i % kNPB), qb = (int)(i % kQPB);
         const int gcount = min(kPG, cur.count - gi * kPG);
-        // ---- teacher rows + dz metadata (buffer pb: free once the dz warps read group i-2)
-        if (i >= 2 && !mbar_wait_warp(&sh->meta_free[pb], par((i - 2) >> 1), A.status)) {
+        // ---- teacher rows + dz metadata (buffer pb: free once the dz warps read group i-kNPB)
+        if (i >= kNPB && !mbar_wait_warp(&sh->meta_free[pb], par(i / kNPB - 1), A.status)) {
           ok = false;
           break;
         }
@@ -856,7 +879,7 @@ __global__ void __launch_bounds__(384, 1)
         sh->lpx2[pb][32 * w + lane] = lp_next;
         __syncwarp();
         if (w == 0 && lane == 0) {  // gcount entries x 128 keys, one bulk copy
-          const uint32_t bytes = (uint32_t)gcount * kBlock * 4;
+          const uint32_t bytes = (uint32_t)gcount * kBlock * 2;
           mbar_expect_tx(&sh->pb_full[pb], bytes);  // also this lane's arrival
           bulk_load(sPb + pb * kPG * kBlock, A.pbar + (size_t)(cur.base + gi * kPG) * kBlock, bytes,
                     &sh->pb_full[pb]);
@@ -899,14 +922,15 @@ __global__ void __launch_bounds__(384, 1)
       }
       cp_async_wait_all();  // nothing may land after the block exits
       // the last bulk copies land before the block exits
-      for (long long x = (i >= 2 ? i - 2 : 0); x < i; ++x)
-        mbar_wait_warp(&sh->pb_full[x & 1], par(x >> 1), A.status);
+      for (long long x = (i >= kNPB ? i - kNPB : 0); x < i; ++x)
+        mbar_wait_warp(&sh->pb_full[x % kNPB], par(x / kNPB), A.status);
     }
   } else if (warp < 8) {
     // ---- dz (thread = key): dz^T = kl_grad/(B S Hp) (softmax(scale z) - pbar); item end: dKp
     const int w4 = warp - 4;
     const int kr = w4 * 32 + lane;  // key (tensor-memory lane of z^T and dKp)
     const uint32_t lb = static_cast<uint32_t>(w4 * 32) << 16;
+    float kl = 0.f;  // kKL: this thread's share of sum pbar (ln pbar - ln p_student)
     long long i = 0;
     for (long long ni = 0; ok; ++ni) {
       int it;
@@ -919,10 +943,10 @@ __global__ void __launch_bounds__(384, 1)
       const int j = n * kBlock + kr;
       const int ngroups = (item.count + kPG - 1) / kPG;
       for (int gi = 0; gi < ngroups; ++gi, ++i) {
-        const int bb = (int)(i & 1);
+        const int bb = (int)(i & 1), pbi = (int)(i % kNPB);
         const int gcount = min(kPG, item.count - gi * kPG);
         __syncwarp();
-        if (!mbar_wait_warp(&sh->pb_full[bb], par(i >> 1), A.status) ||
+        if (!mbar_wait_warp(&sh->pb_full[pbi], par(i / kNPB), A.status) ||
             !mbar_wait_warp(&sh->z_full[bb], par(i >> 1), A.status)) {
           ok = false;
           break;
@@ -932,7 +956,7 @@ __global__ void __launch_bounds__(384, 1)
         tmem_ld32(RZ0 + 64 * bb + lb, z0);
         tmem_ld32(RZ0 + 64 * bb + lb + 32, z1);
         tmem_wait_ld();
-        const float* pbr = sPb + bb * kPG * kBlock;
+        const __half* pbr = sPb + pbi * kPG * kBlock;
         uint32_t zw[kPG / 2];
 #pragma unroll
         for (int k2 = 0; k2 < kPG / 2; ++k2) {
@@ -940,11 +964,15 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int k = 2 * k2 + e;
-            const int t = sh->tok[bb][k];
+            const int t = sh->tok[pbi][k];
             // exponentiate unconditionally and select (no per-lane branch around the asm)
             const float zz = __uint_as_float(k < 32 ? z0[k] : z1[k - 32]);
-            const float v = A.cz * (ex2(zz * sl2 - sh->lpx2[bb][k]) - pbr[k * kBlock + kr]);
-            dzv[e] = (k < gcount && t >= 0 && j <= t) ? v : 0.f;
+            const float lz = zz * sl2 - sh->lpx2[pbi][k];  // log2 of the student probability
+            const float pb = __half2float(pbr[k * kBlock + kr]);
+            const float v = A.cz * (ex2(lz) - pb);
+            const bool vis = k < gcount && t >= 0 && j <= t;
+            dzv[e] = vis ? v : 0.f;
+            if constexpr (kKL) kl += (vis && pb > 0.f) ? pb * (__logf(pb) - lz * kLn2) : 0.f;
           }
           zw[k2] = pack_bf16(dzv[0], dzv[1]);
         }
@@ -963,7 +991,7 @@ __global__ void __launch_bounds__(384, 1)
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&sh->dz_full);        // also: RZ_bb read
-          mbar_arrive(&sh->meta_free[bb]);  // tok / lpx2 / pbar rows of this buffer read
+          mbar_arrive(&sh->meta_free[pbi]);  // tok / lpx2 / pbar rows of this buffer read
         }
         if (gi == ngroups - 1) {  // item end: dKp rows of this key, once its last product landed
           if (!mbar_wait_warp(&sh->fl_full[bb], par(i >> 1), A.status)) {
@@ -989,6 +1017,11 @@ __global__ void __launch_bounds__(384, 1)
           if (lane == 0) mbar_arrive(&sh->acc_free);
         }
       }
+    }
+    if constexpr (kKL) {
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) kl += __shfl_xor_sync(0xffffffffu, kl, off);
+      if (lane == 0) atomicAdd(A.kl_acc, (double)kl);
     }
   } else {
     // ---- dQp flush (warps 8-11, thread = head-dim index): dQp^T -> token-major staging ->
@@ -1055,13 +1088,17 @@ void attn_bwd_g(const CUtensorMap& mk, const CUtensorMap& mv, const MainArgs& a,
                        (int)smem);
   attn_bwd_kernel<G, kDense><<<num_sms(), 352, smem, st>>>(mk, mv, a);
 }
-template <bool kDense>
+template <bool kDense, bool kKL>
 void proxy_bwd_g(const CUtensorMap& mkp, const ProxyArgs& a, cudaStream_t st) {
   const size_t smem = sizeof(ProxyShared) + 1024 + (size_t)kKV + kQPB * (size_t)kRT + 2 * (size_t)kST +
-                      2 * (size_t)kPG * kBlock * 4 + 4 * (size_t)kPG * 32 * 4;
-  cudaFuncSetAttribute(proxy_bwd_kernel<kDense>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                      kNPB * (size_t)kPG * kBlock * 2 + 4 * (size_t)kPG * 32 * 4;
+  cudaFuncSetAttribute(proxy_bwd_kernel<kDense, kKL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        (int)smem);
-  proxy_bwd_kernel<kDense><<<num_sms(), 384, smem, st>>>(mkp, a);
+  proxy_bwd_kernel<kDense, kKL><<<num_sms(), 384, smem, st>>>(mkp, a);
+}
+
+__global__ void kl_finalize_kernel(const double* acc, float* out, double inv) {
+  out[0] = (float)(acc[0] * inv);
 }
 }  // namespace
 
@@ -1079,7 +1116,7 @@ void launch_bwd_rowdot(const Dims& d, const void* o, const void* dout, const flo
 bool launch_attn_bwd(const Dims& d, bool dense, const void* q, const void* k, const void* v,
                      const void* dout, const float2* emeta, const int* seg_offset,
                      const int* entries, const Item* items, const int* n_items, long long max_items,
-                     float* dq_acc, float* dk_acc, float* dv_acc, float* pbar, unsigned* status,
+                     float* dq_acc, float* dk_acc, float* dv_acc, void* pbar, unsigned* status,
                      cudaStream_t st) {
   CUtensorMap mk, mv;
   const uint64_t kvd[3] = {128, (uint64_t)d.Hkv, (uint64_t)d.B * d.S};
@@ -1100,7 +1137,7 @@ bool launch_attn_bwd(const Dims& d, bool dense, const void* q, const void* k, co
   a.dq = dq_acc;
   a.dk = dk_acc;
   a.dv = dv_acc;
-  a.pbar = pbar;
+  a.pbar = static_cast<__half*>(pbar);
   a.status = status;
   a.sched = reinterpret_cast<int*>(status + kSchedAttnBwd);
   cudaMemsetAsync(a.sched, 0, sizeof(int), st);
@@ -1123,10 +1160,10 @@ bool launch_attn_bwd(const Dims& d, bool dense, const void* q, const void* k, co
 }
 
 bool launch_proxy_bwd(const Dims& d, bool dense, const void* qp, const void* kp,
-                      const float* lpxe, const float* pbar, float kl_grad, const int* seg_offset,
+                      const float* lpxe, const void* pbar, float kl_grad, const int* seg_offset,
                       const int* entries, const Item* items, const int* n_items,
-                      long long max_items, float* dqp_acc, float* dkp_acc, unsigned* status,
-                      cudaStream_t st) {
+                      long long max_items, float* dqp_acc, float* dkp_acc, double* kl_acc,
+                      unsigned* status, cudaStream_t st) {
   CUtensorMap mkp;
   const uint64_t kpd[2] = {128, (uint64_t)d.B * d.S};
   const uint64_t kps[1] = {128 * 2};
@@ -1136,7 +1173,7 @@ bool launch_proxy_bwd(const Dims& d, bool dense, const void* qp, const void* kp,
   a.d = d;
   a.qp = (const bf16*)qp;
   a.lpxe = lpxe;
-  a.pbar = pbar;
+  a.pbar = static_cast<const __half*>(pbar);
   a.cz = (float)((double)kl_grad / ((double)d.B * d.S * d.Hp));
   a.seg_offset = seg_offset;
   a.entries = entries;
@@ -1145,14 +1182,19 @@ bool launch_proxy_bwd(const Dims& d, bool dense, const void* qp, const void* kp,
   a.max_items = max_items;
   a.dqp = dqp_acc;
   a.dkp = dkp_acc;
+  a.kl_acc = kl_acc;
   a.status = status;
   a.sched = reinterpret_cast<int*>(status + kSchedProxyBwd);
   cudaMemsetAsync(a.sched, 0, sizeof(int), st);
   if (dense)
-    proxy_bwd_g<true>(mkp, a, st);
+    kl_acc ? proxy_bwd_g<true, true>(mkp, a, st) : proxy_bwd_g<true, false>(mkp, a, st);
   else
-    proxy_bwd_g<false>(mkp, a, st);
+    kl_acc ? proxy_bwd_g<false, true>(mkp, a, st) : proxy_bwd_g<false, false>(mkp, a, st);
   return true;
+}
+
+void launch_kl_finalize(const Dims& d, const double* kl_acc, float* kl_out, cudaStream_t st) {
+  kl_finalize_kernel<<<1, 1, 0, st>>>(kl_acc, kl_out, 1.0 / ((double)d.B * d.S * d.Hp));
 }
 
 }  // namespace msa

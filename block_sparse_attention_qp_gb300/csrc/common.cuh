@@ -1,13 +1,6 @@
-// Shared device helpers for the MSA kernels (sm_103a).
-//
-// Tile conventions used by every attention-shaped kernel here:
-//   * head dim D = 128 and key block = 128 tokens (the method's only supported shapes);
-//   * bf16 tiles in shared memory are row-major with a padded row of kLd elements (272 bytes),
-//     which keeps 8-row ldmatrix accesses free of bank conflicts;
-//   * warp-level products use the m16n8k16 bf16 tensor-core instruction with fp32 accumulate;
-//     an accumulator "acc[N/8][4]" holds a 16 x N fp32 tile in the instruction's C layout:
-//     acc[j][0..1] -> row lane/4,     columns 8j + 2(lane%4) + {0,1}
-//     acc[j][2..3] -> row lane/4 + 8, same columns.
+// Shared device helpers for the MSA kernels (sm_103a): constants of the method, the device status
+// word, asynchronous copies with L2 cache hints, and bf16 packing.  Every contraction of the
+// library runs on the tcgen05 tensor cores (sm100.cuh); nothing here issues warp-level MMAs.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -17,7 +10,6 @@ namespace msa {
 
 constexpr int kBlock = 128;  // key block of the method
 constexpr int kD = 128;      // head dim
-constexpr int kLd = kD + 8;  // padded bf16 row in shared memory
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -30,6 +22,8 @@ constexpr unsigned kStatusTimeout = 4u;     // a bounded device wait expired
 constexpr int kSchedAttnBwd = 8;
 constexpr int kSchedProxyBwd = 9;
 constexpr int kSchedAttnFwd = 10;
+constexpr int kSchedProxyLse = 11;
+constexpr int kSchedDenseFwd = 12;
 
 typedef __nv_bfloat16 bf16;
 
@@ -101,131 +95,9 @@ __device__ __forceinline__ void cp_async_wait_group() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
 }
 
-__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(smem_u32(p)));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(smem_u32(p)));
-}
-
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                         uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};\n"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
-}
-
-template <int NT>
-__device__ __forceinline__ void zero_acc(float (&acc)[NT][4]) {
-#pragma unroll
-  for (int j = 0; j < NT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-}
-
-// acc (16 x N) += A (16 x K, smem row-major, lda) * Bt^T, Bt is [N][K] row-major (ldb).
-template <int N, int K>
-__device__ __forceinline__ void warp_gemm_abt(float (&acc)[N / 8][4], const bf16* a, int lda,
-                                              const bf16* bt, int ldb, int lane) {
-#pragma unroll
-  for (int kk = 0; kk < K; kk += 16) {
-    uint32_t af[4];
-    ldsm_x4(af, a + (lane % 16) * lda + kk + (lane / 16) * 8);
-#pragma unroll
-    for (int nn = 0; nn < N; nn += 16) {
-      uint32_t bfr[4];
-      ldsm_x4(bfr, bt + (nn + (lane % 8) + (lane / 16) * 8) * ldb + kk + ((lane / 8) % 2) * 8);
-      mma16816(acc[nn / 8], af, bfr[0], bfr[1]);
-      mma16816(acc[nn / 8 + 1], af, bfr[2], bfr[3]);
-    }
-  }
-}
-
-// acc (16 x N) += A (16 x K, smem row-major, lda) * B, B is [K][N] row-major (ldb).
-template <int N, int K>
-__device__ __forceinline__ void warp_gemm_ab(float (&acc)[N / 8][4], const bf16* a, int lda,
-                                             const bf16* b, int ldb, int lane) {
-#pragma unroll
-  for (int kk = 0; kk < K; kk += 16) {
-    uint32_t af[4];
-    ldsm_x4(af, a + (lane % 16) * lda + kk + (lane / 16) * 8);
-#pragma unroll
-    for (int nn = 0; nn < N; nn += 16) {
-      uint32_t bfr[4];
-      ldsm_x4_t(bfr, b + (kk + (lane % 8) + ((lane / 8) % 2) * 8) * ldb + nn + (lane / 16) * 8);
-      mma16816(acc[nn / 8], af, bfr[0], bfr[1]);
-      mma16816(acc[nn / 8 + 1], af, bfr[2], bfr[3]);
-    }
-  }
-}
-
-// acc (16 x N) += A * B with A given as register fragments af[K/16][4] (from a C-layout tile),
-// B is [K][N] row-major in smem (ldb).
-template <int N, int K>
-__device__ __forceinline__ void warp_gemm_rb(float (&acc)[N / 8][4], const uint32_t (&af)[K / 16][4],
-                                             const bf16* b, int ldb, int lane) {
-#pragma unroll
-  for (int kk = 0; kk < K; kk += 16) {
-#pragma unroll
-    for (int nn = 0; nn < N; nn += 16) {
-      uint32_t bfr[4];
-      ldsm_x4_t(bfr, b + (kk + (lane % 8) + ((lane / 8) % 2) * 8) * ldb + nn + (lane / 16) * 8);
-      mma16816(acc[nn / 8], af[kk / 16], bfr[0], bfr[1]);
-      mma16816(acc[nn / 8 + 1], af[kk / 16], bfr[2], bfr[3]);
-    }
-  }
-}
-
-// acc (16 x N) += X^T (rows m0..m0+15 of X^T) * B, X is [K][M] row-major (ldx), B is [K][N]
-// row-major (ldb).  Used for dV = P^T dO, dK = dS^T Q, dKp = dz^T Qp.
-template <int N, int K>
-__device__ __forceinline__ void warp_gemm_atb(float (&acc)[N / 8][4], const bf16* x, int ldx,
-                                              int m0, const bf16* b, int ldb, int lane) {
-#pragma unroll
-  for (int kk = 0; kk < K; kk += 16) {
-    uint32_t af[4];
-    ldsm_x4_t(af, x + (kk + (lane % 8) + (lane / 16) * 8) * ldx + m0 + ((lane / 8) % 2) * 8);
-#pragma unroll
-    for (int nn = 0; nn < N; nn += 16) {
-      uint32_t bfr[4];
-      ldsm_x4_t(bfr, b + (kk + (lane % 8) + ((lane / 8) % 2) * 8) * ldb + nn + (lane / 16) * 8);
-      mma16816(acc[nn / 8], af, bfr[0], bfr[1]);
-      mma16816(acc[nn / 8 + 1], af, bfr[2], bfr[3]);
-    }
-  }
-}
-
-// Convert a 16 x K fp32 C-layout tile into A-operand fragments (bf16) for a following product.
-template <int K>
-__device__ __forceinline__ void c_to_a(uint32_t (&af)[K / 16][4], const float (&c)[K / 8][4]) {
-#pragma unroll
-  for (int j = 0; j < K / 16; ++j) {
-    af[j][0] = pack_bf16(c[2 * j][0], c[2 * j][1]);
-    af[j][1] = pack_bf16(c[2 * j][2], c[2 * j][3]);
-    af[j][2] = pack_bf16(c[2 * j + 1][0], c[2 * j + 1][1]);
-    af[j][3] = pack_bf16(c[2 * j + 1][2], c[2 * j + 1][3]);
-  }
-}
-
-// Load `rows` rows of 128 bf16 from global rows given by a per-row pointer function into a
-// padded smem tile; rows with a null pointer are zero-filled.
-template <typename RowPtr>
-__device__ __forceinline__ void load_rows_async(bf16* s, int rows, RowPtr rowptr, int tid,
-                                                int nthreads, const void* any_valid) {
-  for (int c = tid; c < rows * 16; c += nthreads) {
-    const int r = c >> 4, ch = c & 15;
-    const bf16* g = rowptr(r);
-    cp_async16(s + r * kLd + ch * 8, g ? (const void*)(g + ch * 8) : any_valid, g != nullptr);
-  }
 }
 
 }  // namespace msa

@@ -53,6 +53,9 @@ void launch_entry_meta(const Dims& d, bool dense, const int* seg_count, const in
 // Returns false if the TMA tensor maps could not be created (driver entry point missing).
 bool launch_proxy_topk(const Dims& d, const void* qp, const void* kp, int32_t* idx,
                        unsigned* status, cudaStream_t st);
+// Dense proxy normaliser (warmup): lse_px[(b Hp + g) S + t] = log sum_{j <= t} exp(scale qp.kp).
+bool launch_proxy_lse_dense(const Dims& d, const void* qp, const void* kp, float* lse_px,
+                            unsigned* status, cudaStream_t st);
 
 // ---------------------------------------------------------------- forward (fwd.cu)
 // Sparse main-attention partials (attn_fwd.cu): for every list entry (t, slot) and query head h
@@ -68,34 +71,43 @@ int fwd_item_tiles();  // 128-row tiles per sparse-forward work item
 // (the caller fills lpart with NaN bytes before the partial pass).
 void launch_combine(const Dims& d, const void* opart, const float* lpart, void* o, float* lse,
                     cudaStream_t st);
-void launch_dense_fwd(const Dims& d, const void* q, const void* k, const void* v, void* o,
-                      float* lse, cudaStream_t st);
+// Dense causal forward of the warmup mode (dense_fwd.cu).  Returns false for an unsupported group
+// size or if the TMA tensor maps cannot be created.
+bool launch_dense_fwd(const Dims& d, const void* q, const void* k, const void* v, void* o,
+                      float* lse, unsigned* status, cudaStream_t st);
 
 // ---------------------------------------------------------------- backward (bwd.cu)
 // rowm[(b S + t) Hq + h] = {LSE(b, h, t) log2 e, rowsum(dO * O)(b, t, h)}
 void launch_bwd_rowdot(const Dims& d, const void* o, const void* dout, const float* lse,
                        float2* rowm, cudaStream_t st);
-void launch_proxy_lse_sparse(const Dims& d, const void* qp, const void* kp, const int* seg_offset,
+// Sparse proxy normaliser, first pass (attn_fwd.cu, proxy mode): lpx_part[((b S + t) Hp + g) top_k
+// + slot] = log-sum-exp of scale qp.kp over the visible keys of that slot's block; slots no list
+// entry reaches are left as they were (the caller fills lpx_part with NaN bytes first).
+bool launch_proxy_lse_sparse(const Dims& d, const void* qp, const void* kp, const int* seg_offset,
                              const int* entries, const Item* items, const int* n_items,
-                             long long max_items, float* lpx_part, cudaStream_t st);
-void launch_proxy_lse_combine(const Dims& d, const int32_t* idx, const float* lpx_part,
-                              float* lse_px, cudaStream_t st);
-void launch_proxy_lse_dense(const Dims& d, const void* qp, const void* kp, float* lse_px,
-                            cudaStream_t st);
+                             long long max_items, float* lpx_part, unsigned* status,
+                             cudaStream_t st);
+// Second pass: lse_px[(b Hp + g) S + t] from the written (non-NaN) partials of each row.
+void launch_proxy_lse_combine(const Dims& d, const float* lpx_part, float* lse_px, cudaStream_t st);
+
 // Main-attention backward (dQ, dK, dV into fp32 accumulators) and the teacher pbar
-// ([list entry][128 keys] fp32).  Returns false for an unsupported group size or if the TMA
+// ([list entry][128 keys] fp16).  Returns false for an unsupported group size or if the TMA
 // tensor maps cannot be created.
 bool launch_attn_bwd(const Dims& d, bool dense, const void* q, const void* k, const void* v,
                      const void* dout, const float2* emeta, const int* seg_offset,
                      const int* entries, const Item* items, const int* n_items, long long max_items,
-                     float* dq_acc, float* dk_acc, float* dv_acc, float* pbar, unsigned* status,
+                     float* dq_acc, float* dk_acc, float* dv_acc, void* pbar, unsigned* status,
                      cudaStream_t st);
-// Proxy gradients (dQp, dKp into fp32 accumulators) of the KL term from pbar.
+// Proxy gradients (dQp, dKp into fp32 accumulators) of the KL term from pbar.  kl_acc: NULL, or
+// a zeroed double that receives sum over the visited (token, key) pairs of
+// pbar (ln pbar - ln p_student), i.e. B S Hp times the KL value.
 bool launch_proxy_bwd(const Dims& d, bool dense, const void* qp, const void* kp,
-                      const float* lpxe, const float* pbar, float kl_grad, const int* seg_offset,
+                      const float* lpxe, const void* pbar, float kl_grad, const int* seg_offset,
                       const int* entries, const Item* items, const int* n_items,
-                      long long max_items, float* dqp_acc, float* dkp_acc, unsigned* status,
-                      cudaStream_t st);
+                      long long max_items, float* dqp_acc, float* dkp_acc, double* kl_acc,
+                      unsigned* status, cudaStream_t st);
+// kl_out[0] = kl_acc[0] / (B S Hp)  (one thread)
+void launch_kl_finalize(const Dims& d, const double* kl_acc, float* kl_out, cudaStream_t st);
 int bwd_item_tokens();   // tokens per fused-backward work item
 int bwd_group_tokens();  // tokens per proxy-gradient flush group
 void launch_convert(const float* src, void* dst, long long n, cudaStream_t st);

@@ -14,6 +14,12 @@
 // 128-key proxy-key blocks), warp 1 issues the MMAs (one thread), warp 2 owns the tensor memory
 // (4 accumulators x 128 columns), warps 4..7 are the epilogue (thread i of warpgroup 1 owns
 // score row i = TMEM lane i).
+//
+// The same pipeline with kLse = true is the dense proxy normaliser of the warmup backward (blog,
+// "Warmup kernels": the indexer's log-sum-exp over the full causal prefix): blocks 0 .. qb, the
+// local block included with its causal cut (key j visible to token t iff j <= t), and an epilogue
+// that keeps per row a running maximum and sum of exponentials of scale * qp . kp and writes
+// LSE_px[b, g, t] = log sum_{j <= t} exp(scale * qp_t . kp_j).
 #include <math.h>
 
 #include "common.cuh"
@@ -24,6 +30,12 @@
 namespace msa {
 
 namespace {
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 constexpr int kStages = 4;
 constexpr int kAcc = 4;
 constexpr int kTileBytes = 128 * 128 * 2;  // one 128 x 128 bf16 tile (two SW128 panels)
@@ -36,11 +48,12 @@ struct TopkSmem {
 };
 }  // namespace
 
-template <int KMAX>
+template <int KMAX, bool kLse>
 __global__ void __launch_bounds__(256, 1)
     proxy_topk_kernel(const __grid_constant__ CUtensorMap tm_qp,
                       const __grid_constant__ CUtensorMap tm_kp, Dims d,
-                      int32_t* __restrict__ idx, unsigned* __restrict__ status) {
+                      int32_t* __restrict__ idx, float* __restrict__ lse_out,
+                      unsigned* __restrict__ status) {
   using namespace sm100;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = align1024(smem_raw);
@@ -55,6 +68,7 @@ __global__ void __launch_bounds__(256, 1)
   const int b = bg / d.Hp, g = bg % d.Hp;
   const int t0 = qb * kBlock;
   const int KL = d.top_k - 1;
+  const int nb = kLse ? qb + 1 : qb;  // key blocks streamed
 
   if (tid == 0) {
     mbar_init(&sh->q_full, 1);
@@ -79,14 +93,14 @@ __global__ void __launch_bounds__(256, 1)
   const uint32_t sQa = static_cast<uint32_t>(__cvta_generic_to_shared(sQ));
   const uint32_t sKa = static_cast<uint32_t>(__cvta_generic_to_shared(sK));
 
-  if (warp == 0 && lane == 0 && qb > 0) {
+  if (warp == 0 && lane == 0 && nb > 0) {
     // ---- producer
     tma_prefetch_desc(&tm_qp);
     tma_prefetch_desc(&tm_kp);
     mbar_expect_tx(&sh->q_full, kTileBytes);
     tma_load_3d(sQ, &tm_qp, 0, g, b * d.S + t0, &sh->q_full);
     tma_load_3d(sQ + kTileBytes / 2, &tm_qp, 64, g, b * d.S + t0, &sh->q_full);
-    for (int n = 0; n < qb; ++n) {
+    for (int n = 0; n < nb; ++n) {
       const int s = n % kStages;
       if (n >= kStages && !mbar_wait(&sh->kp_empty[s], ((n / kStages) - 1) & 1, status)) break;
       uint8_t* dst = sK + s * kTileBytes;
@@ -94,11 +108,11 @@ __global__ void __launch_bounds__(256, 1)
       tma_load_2d(dst, &tm_kp, 0, b * d.S + n * kBlock, &sh->kp_full[s]);
       tma_load_2d(dst + kTileBytes / 2, &tm_kp, 64, b * d.S + n * kBlock, &sh->kp_full[s]);
     }
-  } else if (warp == 1 && lane == 0 && qb > 0) {
+  } else if (warp == 1 && lane == 0 && nb > 0) {
     // ---- MMA issuer
     constexpr uint32_t idesc = idesc_bf16(128, 128, false, false);
     bool ok = mbar_wait(&sh->q_full, 0, status);
-    for (int n = 0; ok && n < qb; ++n) {
+    for (int n = 0; ok && n < nb; ++n) {
       const int s = n % kStages, a = n % kAcc;
       if (!mbar_wait(&sh->kp_full[s], (n / kStages) & 1, status)) break;
       if (n >= kAcc && !mbar_wait(&sh->acc_empty[a], ((n / kAcc) - 1) & 1, status)) break;
@@ -111,6 +125,59 @@ __global__ void __launch_bounds__(256, 1)
       mma_commit(&sh->kp_empty[s]);
       mma_commit(&sh->acc_full[a]);
     }
+  } else if (warp >= 4 && kLse) {
+    // ---- normaliser epilogue: thread owns score row `row` (token t0 + row)
+    const int q4 = warp - 4;
+    const int row = q4 * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
+    const float sl2 = d.scale * kLog2e;
+    float m = -INFINITY, l = 0.f;  // running max of the raw scores, sum of exp2(sl2 (z - m))
+    for (int n = 0; n < nb; ++n) {
+      const int a = n % kAcc;
+      const int lim = n == qb ? row : kBlock - 1;  // visible columns 0 .. lim
+      __syncwarp();
+      if (!mbar_wait_warp(&sh->acc_full[a], (n / kAcc) & 1, status)) break;
+      fence_after_sync();
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; c += 2) {
+        uint32_t r0[32], r1[32];
+        tmem_ld32(tmem + lane_base + a * 128 + c * 32, r0);
+        tmem_ld32(tmem + lane_base + a * 128 + (c + 1) * 32, r1);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          mx = fmaxf(mx, c * 32 + j <= lim ? __uint_as_float(r0[j]) : -INFINITY);
+          mx = fmaxf(mx, (c + 1) * 32 + j <= lim ? __uint_as_float(r1[j]) : -INFINITY);
+        }
+      }
+      if (mx > m) {  // column 0 is always visible, so mx is finite
+        l *= ex2_approx((m - mx) * sl2);  // m = -inf: l = 0 anyway
+        m = mx;
+      }
+      const float mb = m * sl2;
+      float la = 0.f, lc = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; c += 2) {
+        uint32_t r0[32], r1[32];
+        tmem_ld32(tmem + lane_base + a * 128 + c * 32, r0);
+        tmem_ld32(tmem + lane_base + a * 128 + (c + 1) * 32, r1);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          // exponentiate unconditionally, then select: no per-lane branches
+          const float e0 = ex2_approx(fmaf(__uint_as_float(r0[j]), sl2, -mb));
+          const float e1 = ex2_approx(fmaf(__uint_as_float(r1[j]), sl2, -mb));
+          la += c * 32 + j <= lim ? e0 : 0.f;
+          lc += (c + 1) * 32 + j <= lim ? e1 : 0.f;
+        }
+      }
+      l += la + lc;
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh->acc_empty[a]);
+    }
+    lse_out[((size_t)b * d.Hp + g) * d.S + t0 + row] = (m * sl2 + __log2f(l)) * kLn2;
   } else if (warp >= 4) {
     // ---- epilogue: thread owns score row `row`
     const int q4 = warp - 4;
@@ -188,34 +255,45 @@ __global__ void __launch_bounds__(256, 1)
   if (warp == 2) tmem_dealloc(tmem, 512);
 }
 
-template <int KMAX>
+template <int KMAX, bool kLse>
 static void topk_launch(const CUtensorMap& mq, const CUtensorMap& mk, const Dims& d, int32_t* idx,
-                        unsigned* status, cudaStream_t st) {
+                        float* lse, unsigned* status, cudaStream_t st) {
   const size_t smem = 1024 + (1 + kStages) * kTileBytes + sizeof(TopkSmem);
-  cudaFuncSetAttribute(proxy_topk_kernel<KMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaFuncSetAttribute(proxy_topk_kernel<KMAX, kLse>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        (int)smem);
-  proxy_topk_kernel<KMAX><<<d.B * d.Hp * d.nblk, 256, smem, st>>>(mq, mk, d, idx, status);
+  proxy_topk_kernel<KMAX, kLse><<<d.B * d.Hp * d.nblk, 256, smem, st>>>(mq, mk, d, idx, lse, status);
 }
 
-bool launch_proxy_topk(const Dims& d, const void* qp, const void* kp, int32_t* idx,
-                       unsigned* status, cudaStream_t st) {
-  CUtensorMap mq, mk;
+static bool proxy_maps(const Dims& d, const void* qp, const void* kp, CUtensorMap* mq, CUtensorMap* mk) {
   const uint64_t qdims[3] = {128, (uint64_t)d.Hp, (uint64_t)d.B * d.S};
   const uint64_t qstr[2] = {128 * 2, (uint64_t)d.Hp * 128 * 2};
   const uint32_t qbox[3] = {64, 1, 128};
   const uint64_t kdims[2] = {128, (uint64_t)d.B * d.S};
   const uint64_t kstr[1] = {128 * 2};
   const uint32_t kbox[2] = {64, 128};
-  if (!make_tmap_bf16(&mq, qp, 3, qdims, qstr, qbox)) return false;
-  if (!make_tmap_bf16(&mk, kp, 2, kdims, kstr, kbox)) return false;
+  return make_tmap_bf16(mq, qp, 3, qdims, qstr, qbox) && make_tmap_bf16(mk, kp, 2, kdims, kstr, kbox);
+}
+
+bool launch_proxy_topk(const Dims& d, const void* qp, const void* kp, int32_t* idx,
+                       unsigned* status, cudaStream_t st) {
+  CUtensorMap mq, mk;
+  if (!proxy_maps(d, qp, kp, &mq, &mk)) return false;
   if (d.top_k <= 8)
-    topk_launch<8>(mq, mk, d, idx, status, st);
+    topk_launch<8, false>(mq, mk, d, idx, nullptr, status, st);
   else if (d.top_k <= 16)
-    topk_launch<16>(mq, mk, d, idx, status, st);
+    topk_launch<16, false>(mq, mk, d, idx, nullptr, status, st);
   else if (d.top_k <= 32)
-    topk_launch<32>(mq, mk, d, idx, status, st);
+    topk_launch<32, false>(mq, mk, d, idx, nullptr, status, st);
   else
-    topk_launch<64>(mq, mk, d, idx, status, st);
+    topk_launch<64, false>(mq, mk, d, idx, nullptr, status, st);
+  return true;
+}
+
+bool launch_proxy_lse_dense(const Dims& d, const void* qp, const void* kp, float* lse_px,
+                            unsigned* status, cudaStream_t st) {
+  CUtensorMap mq, mk;
+  if (!proxy_maps(d, qp, kp, &mq, &mk)) return false;
+  topk_launch<2, true>(mq, mk, d, nullptr, lse_px, status, st);
   return true;
 }
 

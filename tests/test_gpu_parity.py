@@ -42,8 +42,8 @@ def run_sparse(w: Workload, seed: int, kl_grad=1.0):
                              w.top_k, w.scale)
         return n_bad, n_exc
     wsb = msa.workspace(msa.make_shape(g["q"], g["k"], g["qp"], w.top_k, w.scale), msa.OP_BACKWARD, DEV)
-    grads = msa.msa_backward(g["q"], g["k"], g["v"], g["qp"], g["kp"], o, lse, g["dout"], idx_t,
-                             w.top_k, w.scale, kl_grad=kl_grad, ws=wsb)
+    *grads, kl = msa.msa_backward(g["q"], g["k"], g["v"], g["qp"], g["kp"], o, lse, g["dout"],
+                                  idx_t, w.top_k, w.scale, kl_grad=kl_grad, ws=wsb, return_kl=True)
     assert msa.msa_device_status(wsb) == 0, "a bounded device wait gave up"
     torch.cuda.synchronize()
     o_ref, lse_ref = oracle.forward(x["q"], x["k"], x["v"], oidx, w.top_k, w.scale)
@@ -53,7 +53,14 @@ def run_sparse(w: Workload, seed: int, kl_grad=1.0):
     close("LSE", lse, lse_ref)
     for name, gt in zip(("dq", "dk", "dv", "dqp", "dkp"), grads):
         close(name, gt, ref[name])
+    check_kl(kl, ref["kl"])
     return n_bad, n_exc
+
+
+def check_kl(kl, want, rel=5e-3):
+    """The KL value the backward materialises on request, against the oracle's L_KL."""
+    got = float(kl)
+    assert want > 0 and abs(got - want) <= rel * want, f"KL {got:.6e} vs oracle {want:.6e}"
 
 
 SMALL = [
@@ -93,8 +100,8 @@ def test_warmup_small(case):
     x = make_inputs(w, 300 + S)
     g = to_dev(x)
     o, lse = msa.msa_warmup_forward(g["q"], g["k"], g["v"], w.scale)
-    grads = msa.msa_warmup_backward(g["q"], g["k"], g["v"], g["qp"], g["kp"], o, lse, g["dout"],
-                                    w.scale, kl_grad=1.0)
+    *grads, kl = msa.msa_warmup_backward(g["q"], g["k"], g["v"], g["qp"], g["kp"], o, lse,
+                                         g["dout"], w.scale, kl_grad=1.0, return_kl=True)
     torch.cuda.synchronize()
     o_ref, lse_ref = oracle.forward(x["q"], x["k"], x["v"], None, 1, w.scale)
     ref = oracle.backward(x["q"], x["k"], x["v"], x["qp"], x["kp"], x["dout"], None, 1, w.scale)
@@ -102,6 +109,7 @@ def test_warmup_small(case):
     close("LSE", lse, lse_ref)
     for name_, gt in zip(("dq", "dk", "dv", "dqp", "dkp"), grads):
         close(name_, gt, ref[name_])
+    check_kl(kl, ref["kl"])
 
 
 def test_dense_forward_group_one():
@@ -140,6 +148,21 @@ def test_cfg2_full_parity():
     w = WORKLOADS[1]
     n_bad, n_exc = run_sparse(w, workload_seed(2))
     print(f"workload 2: {n_bad} selection rows differ, all near ties ({n_exc})")
+
+
+def test_kl_value_does_not_change_the_gradients():
+    """Asking for the KL value leaves every gradient bit-identical up to fp32 summation order
+    (the value is computed beside the proxy gradients, not from them)."""
+    w = Workload("klv", B=1, S=1024, Hq=8, Hkv=2, Hp=2, top_k=4)
+    g = to_dev(make_inputs(w, 61))
+    o, lse, idx = msa.msa_forward(g["q"], g["k"], g["v"], g["qp"], g["kp"], w.top_k, w.scale)
+    a = msa.msa_backward(g["q"], g["k"], g["v"], g["qp"], g["kp"], o, lse, g["dout"], idx,
+                         w.top_k, w.scale)
+    *b, kl = msa.msa_backward(g["q"], g["k"], g["v"], g["qp"], g["kp"], o, lse, g["dout"], idx,
+                              w.top_k, w.scale, return_kl=True)
+    for name, x, y in zip(("dq", "dk", "dv", "dqp", "dkp"), a, b):
+        close(name, x, y.float(), rel=1e-5, atol=1e-3, ulps=1.0)
+    assert float(kl) > 0
 
 
 def test_bad_indices_are_flagged_not_faulted():
@@ -189,3 +212,22 @@ def test_autograd_function_matches_direct_calls():
     close("O", out, o.float(), rel=1e-5, atol=2e-3, ulps=1.0)  # equal up to fp32 summation order
     for name, r in zip(("q", "k", "v", "qp", "kp"), ref):
         close("d" + name, leaves[name].grad, r.float(), rel=1e-2, ulps=1.5)
+
+
+@pytest.mark.parametrize("G,S", [(2, 768), (4, 1280), (8, 896)])
+def test_warmup_forward_growing_row_maxima(G, S):
+    """Dense forward on inputs whose score scale grows along the sequence (key rows scaled by
+    1 + t/128, queries by 3): later key blocks keep raising the row maxima by far more than the
+    kernel's lazy-rescale threshold, so O and l are rescaled many times per row."""
+    Hkv = 2
+    w = Workload("grow", B=1, S=S, Hq=G * Hkv, Hkv=Hkv, Hp=Hkv, top_k=0)
+    x = make_inputs(w, 500 + S + G)
+    ramp = (1.0 + torch.arange(S, dtype=torch.float32) / 128.0).view(1, S, 1, 1)
+    x["k"] = (x["k"].float() * ramp).to(torch.bfloat16)
+    x["q"] = (x["q"].float() * 3.0).to(torch.bfloat16)
+    g = to_dev(x)
+    o, lse = msa.msa_warmup_forward(g["q"], g["k"], g["v"], w.scale)
+    torch.cuda.synchronize()
+    o_ref, lse_ref = oracle.forward(x["q"], x["k"], x["v"], None, 1, w.scale)
+    close("O", o, o_ref)
+    close("LSE", lse, lse_ref, rel=1e-5, atol=1e-3, ulps=0.0)
