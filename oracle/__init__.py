@@ -147,16 +147,19 @@ def select(qp, kp, top_k: int, scale: float, rows=None):
 def forward(q, k, v, idx, top_k: int, scale: float, rows=None, Hp=None):
     """Steps 4-5 (key set and main attention).  idx=None: warmup (dense causal).
 
-    q [B,S,Hq,D], k/v [B,S,Hkv,D], idx int32 [B,Hp,S,top_k].  rows: optional [n,3] (b, t, h).
+    q [B,S,Hq,D], k/v [B,S,Hkv,D], idx int32 [B,Hp,S,top_k] (query head h uses the selection of
+    proxy head h / (Hq/Hp) and the keys of KV head h / (Hq/Hkv)).  rows: optional [n,3] (b, t, h).
     Returns (o, lse): o [B,S,Hq,D], lse [B,Hq,S] (or [n,D], [n]).
     """
     q, k, v = f64(q), f64(k), f64(v)
     B, S, Hq, D = q.shape
     Hkv = k.shape[2]
-    Hp = Hkv if Hp is None else Hp
     if idx is not None:
         idx = np.ascontiguousarray(idx, dtype=np.int32)
         top_k = idx.shape[-1]
+        if Hp is None:
+            Hp = idx.shape[1]  # the map's proxy heads
+    Hp = Hkv if Hp is None else Hp
     if rows is None:
         o = np.empty((B, S, Hq, D), np.float64)
         lse = np.empty((B, Hq, S), np.float64)

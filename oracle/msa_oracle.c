@@ -12,16 +12,17 @@
  *   (MSA): Turning Theoretical Sparse Attention Gains into Real GPU Speedups", sections
  *   "Architecture: two-stage block-sparse attention" and "Training stability".
  *
- *   For batch b, group g (= proxy head g = KV head g), token t, local block m = t / 128:
+ *   For batch b, proxy head g (one MSA group), token t, local block m = t / 128:
  *   1. proxy scores   z[t,j] = scale * <Qp[b,t,g], Kp[b,j]>       (one shared proxy key head)
  *   2. block scores   c[n] = max over the 128 keys of block n of z, for every block n < m;
  *                     the local block m is forced to +infinity ("set the local KV block to inf")
  *   3. selection      the first K = min(top_k, m+1) blocks under (c descending, n ascending);
  *                     emitted in ascending block order, padded with -1
  *   4. key set        J = union of the selected blocks, cut causally at t (j <= t)
- *   5. main attention softmax(scale * <Q[b,t,h], K[b,j,g]>) over J for every query head h of
- *                     group g (h / G == g), O = sum P V, LSE = log sum exp
- *   6. teacher        pbar = mean over the G heads of the main probabilities (stop-gradient);
+ *   5. main attention softmax(scale * <Q[b,t,h], K[b,j,h/G]>) over J for every query head h of
+ *                     proxy head g (h / Gp == g, Gp = Hq/Hp), O = sum P V, LSE = log sum exp;
+ *                     keys and values come from h's own KV head h / G (G = Hq/Hkv)
+ *   6. teacher        pbar = mean over the Gp heads of the main probabilities (stop-gradient);
  *      student        p_px = softmax over J of z
  *   7. KL             L_KL = 1/(B*S*Hp) * sum over (b,t,g) of KL(pbar || p_px)
  *   8. main gradients textbook softmax-attention backward of  L = sum(O * dO) + kl_grad * L_KL;
@@ -29,6 +30,12 @@
  *   9. proxy grads    dz = kl_grad/(B*S*Hp) * (p_px - pbar)   (the blog's closed form)
  *                     dQp = scale * sum_j dz_j Kp_j ; dKp_j += scale * dz_j Qp
  *  10. warmup         same as 5-9 with J = [0, t] and no selection.
+ *
+ * Head mapping (blog, "Note about scheduler requiring proxy heads >= KV heads"; package caveat 5):
+ * the MSA group is the proxy head.  With Hp == Hkv it is one GQA group; with Hp < Hkv one proxy
+ * head selects for Hkv/Hp whole GQA groups (the inverted mapping the blog's kernels do not
+ * schedule) and its teacher averages all their Hq/Hp query heads; with Hp > Hkv a GQA group is
+ * split among Hp/Hkv proxy heads.  Query heads of proxy head g are g*Gp .. g*Gp + Gp - 1.
  *
  * Plain loops, no blocking and no fusion beyond the steps above.  Every array is contiguous:
  *   q    [B,S,Hq,D]   k, v [B,S,Hkv,D]   qp [B,S,Hp,D]   kp [B,S,D]   dout [B,S,Hq,D]
@@ -224,10 +231,16 @@ static double attend_row(int b, int t, int h, int S, int Hq, int Hkv, int D, dou
  * Forward for every (b,t,h) (rows == NULL: o_out [B,S,Hq,D], lse_out [B,Hq,S]) or for nrows
  * given triples (b, t, h) (o_out [nrows,D], lse_out [nrows]).  idx == NULL: warmup (dense).
  */
+/* Head counts the mapping above accepts. */
+static int heads_ok(int Hq, int Hkv, int Hp) {
+  if (Hq <= 0 || Hkv <= 0 || Hp <= 0 || Hq % Hkv != 0 || Hq % Hp != 0) return 0;
+  return Hp % Hkv == 0 || Hkv % Hp == 0;
+}
+
 int msa_oracle_forward(int B, int S, int Hq, int Hkv, int Hp, int D, int top_k, double scale,
                        const double* q, const double* k, const double* v, const int32_t* idx,
                        int nrows, const int32_t* rows, double* o_out, double* lse_out) {
-  if (Hq % Hkv != 0 || Hp != Hkv) return 1;
+  if (!heads_ok(Hq, Hkv, Hp)) return 1;
   const long total = rows ? nrows : (long)B * S * Hq;
   const int maxJ = idx ? (top_k * MSA_ORACLE_BLOCK < S ? top_k * MSA_ORACLE_BLOCK : S) : S;
 #pragma omp parallel
@@ -246,7 +259,7 @@ int msa_oracle_forward(int B, int S, int Hq, int Hkv, int Hp, int D, int top_k, 
         t = (int)((r / Hq) % S);
         h = (int)(r % Hq);
       }
-      const int g = h / (Hq / Hkv);
+      const int g = h / (Hq / Hp); /* the proxy head whose selection h uses */
       int nj = key_set(b, g, t, S, Hp, top_k, idx, J);
       double lse = attend_row(b, t, h, S, Hq, Hkv, D, scale, q, k, v, J, nj, P,
                               o_out + (rows ? (size_t)r * D : at4(b, t, h, S, Hq, D)));
@@ -278,10 +291,16 @@ int msa_oracle_backward(int B, int S, int Hq, int Hkv, int Hp, int D, int top_k,
                         const int32_t* idx, const unsigned char* tok_mask, int only_masked,
                         int kj0, int kj1, double* dq, double* dk, double* dv, double* dqp, double* dkp,
                         double* kl_out) {
-  if (Hq % Hkv != 0 || Hp != Hkv) return 1;
-  const int G = Hq / Hkv;
+  if (!heads_ok(Hq, Hkv, Hp)) return 1;
+  const int G = Hq / Hkv;  /* query heads per KV head */
+  const int Gp = Hq / Hp;  /* query heads per proxy head (the teacher's average) */
+  /* Work unit of one thread: (b, c) with c the coarser of the two groupings, so that every
+   * gradient row a unit writes (dq, dk, dv, dqp) belongs to it alone: a proxy head (Hp <= Hkv)
+   * with its whole KV heads, or a KV head (Hp > Hkv) with the proxy heads that split it. */
+  const int Hu = Hp < Hkv ? Hp : Hkv;
+  const int per_unit = Hp / Hu;  /* proxy heads per unit */
   const double cz = kl_grad / ((double)B * S * Hp); /* step 9 factor: mean over (b,t,g) */
-  const int npairs = B * Hp;
+  const int npairs = B * Hu;
   const int nwin = kj1 > kj0 ? kj1 - kj0 : 0;
   const int maxJ = idx ? (top_k * MSA_ORACLE_BLOCK < S ? top_k * MSA_ORACLE_BLOCK : S) : S;
   double* dkp_part = (double*)calloc((size_t)npairs * (size_t)nwin * D + 1, sizeof(double));
@@ -290,16 +309,18 @@ int msa_oracle_backward(int B, int S, int Hq, int Hkv, int Hp, int D, int top_k,
 #pragma omp parallel
   {
     int32_t* J = (int32_t*)malloc(sizeof(int32_t) * (size_t)maxJ);
-    double* P = (double*)malloc(sizeof(double) * (size_t)maxJ * G); /* P[h_local][a]   */
+    double* P = (double*)malloc(sizeof(double) * (size_t)maxJ * Gp); /* P[h_local][a]  */
     double* dS = (double*)malloc(sizeof(double) * (size_t)maxJ);    /* one head at a time */
     double* pbar = (double*)malloc(sizeof(double) * (size_t)maxJ);
     double* z = (double*)malloc(sizeof(double) * (size_t)maxJ);
     double* o = (double*)malloc(sizeof(double) * (size_t)D);
 #pragma omp for schedule(dynamic, 1)
     for (int pr = 0; pr < npairs; ++pr) {
-      const int b = pr / Hp, g = pr % Hp;
+      const int b = pr / Hu;
       double* my_dkp = dkp_part + (size_t)pr * nwin * D; /* rows kj0 .. kj1-1 */
       double kl_acc = 0.0;
+      for (int gi = 0; gi < per_unit; ++gi) {
+      const int g = (pr % Hu) * per_unit + gi; /* proxy head */
       for (int t = 0; t < S; ++t) {
         const int want_q = !tok_mask || tok_mask[(size_t)b * S + t];
         if (!want_q && (only_masked || t < kj0)) continue; /* nothing of it is in the sample */
@@ -310,21 +331,22 @@ int msa_oracle_backward(int B, int S, int Hq, int Hkv, int Hp, int D, int top_k,
         if (!touches) continue;
         /* step 5 + main backward, head by head */
         for (int a = 0; a < nj; ++a) pbar[a] = 0.0;
-        for (int hl = 0; hl < G; ++hl) {
-          const int h = g * G + hl;
+        for (int hl = 0; hl < Gp; ++hl) {
+          const int h = g * Gp + hl;
+          const int kvh = h / G; /* the KV head of query head h */
           double* Ph = P + (size_t)hl * maxJ;
           attend_row(b, t, h, S, Hq, Hkv, D, scale, q, k, v, J, nj, Ph, o);
           const double* dorow = dout + at4(b, t, h, S, Hq, D);
           const double Drow = dot(dorow, o, D); /* D = rowsum(dO * O) */
           for (int a = 0; a < nj; ++a) {
-            double dP = dot(dorow, v + at4(b, J[a], g, S, Hkv, D), D);
+            double dP = dot(dorow, v + at4(b, J[a], kvh, S, Hkv, D), D);
             dS[a] = Ph[a] * (dP - Drow);
-            pbar[a] += Ph[a] / G;
+            pbar[a] += Ph[a] / Gp;
           }
           if (want_q) {
             double* dqrow = dq + at4(b, t, h, S, Hq, D);
             for (int a = 0; a < nj; ++a) {
-              const double* krow = k + at4(b, J[a], g, S, Hkv, D);
+              const double* krow = k + at4(b, J[a], kvh, S, Hkv, D);
               for (int d = 0; d < D; ++d) dqrow[d] += scale * dS[a] * krow[d];
             }
           }
@@ -332,8 +354,8 @@ int msa_oracle_backward(int B, int S, int Hq, int Hkv, int Hp, int D, int top_k,
           for (int a = 0; a < nj; ++a) {
             const int j = J[a];
             if (j < kj0 || j >= kj1) continue;
-            double* dkrow = dk + at4(b, j, g, S, Hkv, D);
-            double* dvrow = dv + at4(b, j, g, S, Hkv, D);
+            double* dkrow = dk + at4(b, j, kvh, S, Hkv, D);
+            double* dvrow = dv + at4(b, j, kvh, S, Hkv, D);
             for (int d = 0; d < D; ++d) {
               dkrow[d] += scale * dS[a] * qrow[d];
               dvrow[d] += Ph[a] * dorow[d];
@@ -366,6 +388,7 @@ int msa_oracle_backward(int B, int S, int Hq, int Hkv, int Hp, int D, int top_k,
           }
         }
       }
+      }
       kl_part[pr] = kl_acc;
     }
     free(J);
@@ -378,7 +401,7 @@ int msa_oracle_backward(int B, int S, int Hq, int Hkv, int Hp, int D, int top_k,
   /* dKp: the proxy key head is shared by every group, so sum the per-(b,g) parts */
   double kl = 0.0;
   for (int pr = 0; pr < npairs; ++pr) {
-    const int b = pr / Hp;
+    const int b = pr / Hu;
     kl += kl_part[pr];
     for (int j = kj0; j < kj1; ++j)
       for (int d = 0; d < D; ++d)

@@ -53,19 +53,20 @@ def eager_msa(q, k, v, qp, kp, dout, idx, scale, kl_grad=1.0, warmup=False):
     q, k, v, qp, kp = (x.detach().clone().requires_grad_(True) for x in (q, k, v, qp, kp))
     B, S, Hq, D = q.shape
     Hkv, Hp = k.shape[2], qp.shape[2]
-    G = Hq // Hkv
+    G, Gp = Hq // Hkv, Hq // Hp  # query heads per KV head / per proxy head (MSA group)
     mask = key_mask(idx, S, warmup=warmup, Hp=Hp, B=B)  # [B,Hp,S,S]
-    head_group = torch.arange(Hq) // G
-    mask_h = mask[:, head_group]  # [B,Hq,S,S]
-    k_h = k[:, :, head_group, :]
-    v_h = v[:, :, head_group, :]
+    kv_of = torch.arange(Hq) // G      # query head -> KV head
+    proxy_of = torch.arange(Hq) // Gp  # query head -> proxy head whose selection it uses
+    mask_h = mask[:, proxy_of]  # [B,Hq,S,S]
+    k_h = k[:, :, kv_of, :]
+    v_h = v[:, :, kv_of, :]
     s = scale * torch.einsum("bthd,bjhd->bhtj", q, k_h)
     s = s.masked_fill(~mask_h, float("-inf"))
     lse = torch.logsumexp(s, dim=-1)  # [B,Hq,S]
     p = torch.softmax(s, dim=-1)
     o = torch.einsum("bhtj,bjhd->bthd", p, v_h)
-    # teacher: mean over the G heads of each group, stop-gradient
-    pbar = p.detach().reshape(B, Hp, G, S, S).mean(2)
+    # teacher: mean over the Gp query heads of each proxy head, stop-gradient
+    pbar = p.detach().reshape(B, Hp, Gp, S, S).mean(2)
     z = scale * torch.einsum("bthd,bjd->bhtj", qp, kp[:, :, 0, :])
     z = z.masked_fill(~mask, float("-inf"))
     logp_px = torch.log_softmax(z, dim=-1)

@@ -19,7 +19,10 @@ MUTANTS = {
                            "j < (n + 1) * MSA_ORACLE_BLOCK;"),
     "dKp from the wrong operand": ("acc[d] += scale * dz * qprow[d];",
                                    "acc[d] += scale * dz * kprow[d];"),
-    "teacher not averaged": ("pbar[a] += Ph[a] / G;", "pbar[a] += Ph[a];"),
+    "teacher not averaged": ("pbar[a] += Ph[a] / Gp;", "pbar[a] += Ph[a];"),
+    "teacher averaged over the KV group": ("pbar[a] += Ph[a] / Gp;", "pbar[a] += Ph[a] / G;"),
+    "keys of the proxy head's first KV head": ("const int kvh = h / G; /* the KV head of query head h */",
+                                               "const int kvh = (h / Gp) * Hkv / Hp;"),
     "scale dropped in dQ": ("dqrow[d] += scale * dS[a] * krow[d];",
                             "dqrow[d] += dS[a] * krow[d];"),
     "block max over a shifted block": ("for (int j = n * MSA_ORACLE_BLOCK; j < (n + 1) * MSA_ORACLE_BLOCK; ++j) {\n      double z",
@@ -52,6 +55,8 @@ PINS = [
     lambda: pins.test_full_selection_is_dense_causal_attention(False),
     lambda: pins.test_finite_differences_every_gradient(False, n_coords=2),
     lambda: pins.test_kl_zero_when_student_equals_teacher(2),
+    lambda: pins.test_eager_second_implementation((1, 384, 8, 4, 2, 2), False),
+    lambda: pins.test_finite_differences_general_mapping(4, 1, 2, n_coords=2),
 ]
 
 

@@ -29,8 +29,9 @@ from tests.eager_msa import eager_msa, eager_select
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
 
-def tiny(S=512, Hq=4, Hkv=2, top_k=3, D=128, seed=7, planted=0, B=1):
-    w = Workload("tiny", B=B, S=S, Hq=Hq, Hkv=Hkv, Hp=Hkv, top_k=top_k, planted=planted, D=D)
+def tiny(S=512, Hq=4, Hkv=2, top_k=3, D=128, seed=7, planted=0, B=1, Hp=None):
+    w = Workload("tiny", B=B, S=S, Hq=Hq, Hkv=Hkv, Hp=Hkv if Hp is None else Hp, top_k=top_k,
+                 planted=planted, D=D)
     return w, make_inputs(w, seed)
 
 
@@ -261,8 +262,8 @@ def test_warmup_equals_sparse_with_every_block():
 # ----------------------------------------------------------------------------- finite differences
 
 
-def _fd_case():
-    w, x = tiny(S=384, Hq=4, Hkv=2, top_k=2, D=16, seed=13)
+def _fd_case(Hq=4, Hkv=2, Hp=None):
+    w, x = tiny(S=384, Hq=Hq, Hkv=Hkv, top_k=2, D=16, seed=13, Hp=Hp)
     idx, _ = oracle.select(x["qp"], x["kp"], 2, w.scale)
     arrs = {n: oracle.f64(x[n]) for n in ("q", "k", "v", "qp", "kp", "dout")}
     return w, idx, arrs
@@ -279,8 +280,8 @@ def _kl(w, idx, a, warmup=False):
 
 
 @pytest.mark.parametrize("warmup", [False, True])
-def test_finite_differences_every_gradient(warmup, n_coords=6):
-    w, idx, a = _fd_case()
+def test_finite_differences_every_gradient(warmup, n_coords=6, heads=None):
+    w, idx, a = _fd_case(*(heads or ()))
     kl_grad = 0.75
     use_idx = None if warmup else idx
     g = oracle.backward(a["q"], a["k"], a["v"], a["qp"], a["kp"], a["dout"], use_idx, w.top_k,
@@ -310,6 +311,14 @@ def test_finite_differences_every_gradient(warmup, n_coords=6):
             assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)) + 1e-9, (name, pos, fd, an)
 
 
+@pytest.mark.parametrize("Hq,Hkv,Hp", [(4, 1, 2), (8, 4, 2), (8, 2, 1), (4, 2, 4)])
+def test_finite_differences_general_mapping(Hq, Hkv, Hp, n_coords=4):
+    """Every gradient against central differences when proxy heads and KV heads differ in
+    number (teacher over the proxy head's Hq/Hp query heads; keys of each head's own KV head)."""
+    for warmup in (False, True):
+        test_finite_differences_every_gradient(warmup, n_coords=n_coords, heads=(Hq, Hkv, Hp))
+
+
 # ----------------------------------------------------------------------------- KL properties
 
 
@@ -323,6 +332,20 @@ def test_kl_nonnegative_and_zero_gradient_sum():
     kp[:] = kp[0, 0]
     g2 = oracle.backward(x["q"], x["k"], x["v"], x["qp"], kp, x["dout"], idx, 3, w.scale)
     assert np.abs(g2["dqp"]).max() < 1e-15
+
+
+def test_kl_zero_when_proxy_head_spans_several_kv_heads():
+    """Hp < Hkv: every query head of proxy head g equals Qp[g] and every key head equals Kp, so
+    each head's softmax is the student and so is their mean over the Hkv/Hp GQA groups."""
+    Hq, Hkv, Hp = 8, 4, 2
+    w, x = tiny(S=512, Hq=Hq, Hkv=Hkv, Hp=Hp, seed=41)
+    qp, kp = x["qp"], x["kp"]
+    q = qp.repeat_interleave(Hq // Hp, dim=2)
+    k = kp.expand(-1, -1, Hkv, -1).contiguous()
+    idx, _ = oracle.select(qp, kp, 3, w.scale)
+    g = oracle.backward(q, k, x["v"], qp, kp, x["dout"], idx, 3, w.scale)
+    assert abs(g["kl"]) < 1e-13
+    assert np.abs(g["dqp"]).max() < 1e-15 and np.abs(g["dkp"]).max() < 1e-15
 
 
 @pytest.mark.parametrize("G", [1, 2])
@@ -341,11 +364,18 @@ def test_kl_zero_when_student_equals_teacher(G):
 # ----------------------------------------------------------------------------- second implementation
 
 
+# (B, S, Hq, Hkv, Hp, top_k): Hp == Hkv, then proxy heads fewer than KV heads (one proxy head
+# selects for several GQA groups) and more (a GQA group split among proxy heads)
+EAGER_SHAPES = [(1, 384, 4, 2, 2, 2), (2, 512, 4, 1, 1, 3), (1, 640, 6, 3, 3, 4),
+                (1, 384, 8, 4, 2, 2), (1, 512, 8, 4, 1, 3), (2, 384, 8, 1, 2, 2),
+                (1, 512, 8, 2, 4, 3)]
+
+
 @pytest.mark.parametrize("warmup", [False, True])
-@pytest.mark.parametrize("shape", [(1, 384, 4, 2, 2), (2, 512, 4, 1, 3), (1, 640, 6, 3, 4)])
+@pytest.mark.parametrize("shape", EAGER_SHAPES)
 def test_eager_second_implementation(shape, warmup):
-    B, S, Hq, Hkv, top_k = shape
-    w, x = tiny(S=S, Hq=Hq, Hkv=Hkv, top_k=top_k, D=32, seed=S + Hq, B=B, planted=0)
+    B, S, Hq, Hkv, Hp, top_k = shape
+    w, x = tiny(S=S, Hq=Hq, Hkv=Hkv, top_k=top_k, D=32, seed=S + Hq, B=B, planted=0, Hp=Hp)
     d = {n: x[n].double() for n in ("q", "k", "v", "qp", "kp", "dout")}
     idx, _ = oracle.select(x["qp"], x["kp"], top_k, w.scale)
     if not warmup:
