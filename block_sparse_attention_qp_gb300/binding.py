@@ -23,12 +23,13 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmsa.so")
 
-OP_FORWARD, OP_BACKWARD, OP_WARMUP_FORWARD, OP_WARMUP_BACKWARD = 0, 1, 2, 3
-STATUS_BITS = {1: "bad block index", 2: "work list overflow", 4: "device wait timeout"}
+OP_FORWARD, OP_BACKWARD, OP_WARMUP_FORWARD, OP_WARMUP_BACKWARD, OP_DECODE = 0, 1, 2, 3, 4
+STATUS_BITS = {1: "bad block index", 2: "work list overflow", 4: "device wait timeout",
+               8: "internal layout check"}
 _SYMBOLS = ("msa_workspace_size", "msa_forward", "msa_backward", "msa_warmup_forward",
             "msa_warmup_backward", "msa_device_status", "msa_status_string", "msa_last_error",
             "msa_profile_begin", "msa_profile_end", "msa_launch_count", "msa_forward_noalloc",
-            "msa_forward_noalloc_status", "msa_selftest_wait_timeout")
+            "msa_forward_noalloc_status", "msa_selftest_wait_timeout", "msa_decode")
 
 
 class MSAError(RuntimeError):
@@ -64,6 +65,8 @@ def load_library(path: str = LIB_PATH):
         lib.msa_warmup_backward.argtypes = [SP, P, P, P, P, P, P, P, P, F, P, P, P, P, P, P, P, Z,
                                             P]
         lib.msa_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint), P]
+        lib.msa_decode.argtypes = [SP, P, P, P, P, P, P, P, P, P, P, Z, P]
+        lib.msa_decode.restype = I
         lib.msa_status_string.argtypes = [I]
         lib.msa_status_string.restype = ctypes.c_char_p
         lib.msa_last_error.restype = ctypes.c_char_p
@@ -240,6 +243,30 @@ def msa_backward(q, k, v, qp, kp, o, lse, dout, block_idx, top_k: int, scale: fl
                                        float(kl_grad), *map(_ptr, grads), _ptr(kl), _ptr(ws),
                                        ws.numel(), _stream(q.device)), "msa_backward")
     return tuple(grads) + ((kl,) if return_kl else ())
+
+
+def msa_decode(q, qp, k_cache, v_cache, kp_cache, seq_len, top_k: int, scale: float, ws=None):
+    """Decode step: q [B, Hq, D], qp [B, Hp, D] (the new tokens), caches k/v [B, S, Hkv, D] and
+    kp [B, S, 1, D] (or [B, S, D]) already holding the new tokens at seq_len - 1, seq_len [B] int32
+    on the device.  Returns (o [B, Hq, D], lse [B, Hq], block_idx [B, Hp, top_k])."""
+    B, Hq, D = q.shape
+    S, Hkv = k_cache.shape[1], k_cache.shape[2]
+    Hp = qp.shape[1]
+    for t, n in ((q, "q"), (qp, "qp"), (k_cache, "k_cache"), (v_cache, "v_cache"),
+                 (kp_cache, "kp_cache")):
+        _req(t, n)
+    _req(seq_len, "seq_len", torch.int32, (B,))
+    shape = Shape(B, S, Hq, Hkv, Hp, D, int(top_k), float(scale))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    idx = torch.empty((B, Hp, top_k), dtype=torch.int32, device=q.device)
+    if ws is None:
+        ws = workspace(shape, OP_DECODE, q.device)
+    _check(load_library().msa_decode(ctypes.byref(shape), _ptr(q), _ptr(qp), _ptr(k_cache),
+                                     _ptr(v_cache), _ptr(kp_cache), _ptr(seq_len), _ptr(idx),
+                                     _ptr(o), _ptr(lse), _ptr(ws), ws.numel(), _stream(q.device)),
+           "msa_decode")
+    return o, lse, idx
 
 
 def msa_warmup_forward(q, k, v, scale: float, ws=None):

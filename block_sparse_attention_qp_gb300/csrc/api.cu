@@ -76,7 +76,7 @@ struct Plan {
   size_t status = 0, totals = 0, seg_count = 0, seg_offset = 0, seg_cursor = 0, entries = 0;
   size_t io0 = 0, io1 = 0, items0 = 0, items1 = 0;
   size_t opart = 0, lpart = 0, lpx_part = 0, lse_px = 0, lpxe = 0, rowm = 0, emeta = 0, pbar = 0;
-  size_t dq = 0, dk = 0, dv = 0, dqp = 0, dkp = 0;
+  size_t dq = 0, dk = 0, dv = 0, dqp = 0, dkp = 0, scores = 0;
   size_t bytes = 0;
   long long max0 = 0, max1 = 0;
   ItemSpec spec0{1, 1}, spec1{1, 1};
@@ -96,26 +96,26 @@ long long dense_entries(const Dims& d) {  // sum over blocks of S - 128 n, per (
 }
 
 long long max_items(long long entries, const Dims& d, const ItemSpec& s) {
-  return entries / ((long long)s.tile_tokens * s.chunk_tiles) + d.nlist() + 1;
+  return (entries / ((long long)s.tile_tokens * s.chunk_tiles) + d.nlist()) * s.nsub + 1;
 }
 
-// Sequence chunk of the backward's token lists: the dQ rows one chunk contributes for one group
-// (chunk x G heads x 128 x fp32) are kept to <= 64 MB, so that most of them stay resident in L2
+// Sequence chunk of the backward's token lists: the dQ rows one chunk contributes for one proxy
+// head (chunk x Gp heads x 128 x fp32) are kept to <= 64 MB, so that most of them stay resident in L2
 // while the work items of that chunk and group run.  Smaller chunks cut the lists into more,
 // shorter items (more partly filled tiles and K / V loads); on GB300 at S = 64K, G = 8 the step
 // was fastest at 64 MB among 8, 16, 32 and 64 MB.
 int bwd_chunk(const Dims& d) {
   int c = kBlock;
-  while ((long long)c * 2 * d.G * kD * 4 <= (64ll << 20) && c * 2 <= d.S) c *= 2;
+  while ((long long)c * 2 * d.Gp() * kD * 4 <= (64ll << 20) && c * 2 <= d.S) c *= 2;
   return c;
 }
 
-// Sequence chunk of the forward's token lists: one chunk's query rows of one group
-// (chunk x G heads x 128 x bf16) are kept to <= 16 MB, so the up to top_k reads of every query row
+// Sequence chunk of the forward's token lists: one chunk's query rows of one proxy head
+// (chunk x Gp heads x 128 x bf16) are kept to <= 16 MB, so the up to top_k reads of every query row
 // (one per selected block) hit L2 while the items of that chunk and group run.
 int fwd_chunk(const Dims& d) {
   int c = kBlock;
-  while ((long long)c * 2 * d.G * kD * 2 <= (16ll << 20) && c * 2 <= d.S) c *= 2;
+  while ((long long)c * 2 * d.Gp() * kD * 2 <= (16ll << 20) && c * 2 <= d.S) c *= 2;
   return c;
 }
 
@@ -144,7 +144,7 @@ Plan make_plan(const Dims& d, int op) {
     p.entries = c.take(sparse_ent * sizeof(int));
   }
   if (op == MSA_OP_FORWARD) {
-    p.spec0 = ItemSpec{TT, fwd_item_tiles()};
+    p.spec0 = ItemSpec{TT, fwd_item_tiles(), d.R};
     p.max0 = max_items(sparse_ent, d, p.spec0);
     p.io0 = c.take(nseg * sizeof(int));
     p.items0 = c.take(p.max0 * sizeof(Item));
@@ -154,7 +154,8 @@ Plan make_plan(const Dims& d, int op) {
   if (op == MSA_OP_BACKWARD || op == MSA_OP_WARMUP_BACKWARD) {
     const bool dense = op == MSA_OP_WARMUP_BACKWARD;
     const long long ent = dense ? dense_entries(d) : sparse_ent;
-    const ItemSpec fused{bwd_group_tokens(), bwd_item_tokens() / bwd_group_tokens()};
+    // one item per attention group (the proxy gradient kernel takes those with sub == 0)
+    const ItemSpec fused{bwd_group_tokens(), bwd_item_tokens() / bwd_group_tokens(), d.R};
     if (dense) {
       p.spec0 = fused;
       p.max0 = max_items(ent, d, p.spec0);
@@ -162,7 +163,7 @@ Plan make_plan(const Dims& d, int op) {
       p.io0 = c.take(nseg * sizeof(int));
       p.items0 = c.take(p.max0 * sizeof(Item));
     } else {
-      p.spec0 = ItemSpec{kBlock, fwd_item_tiles()};  // proxy normaliser items (128-token tiles)
+      p.spec0 = ItemSpec{kBlock, fwd_item_tiles(), 1};  // proxy normaliser items (128-token tiles)
       p.spec1 = fused;
       p.max0 = max_items(ent, d, p.spec0);
       p.max1 = max_items(ent, d, p.spec1);
@@ -176,13 +177,14 @@ Plan make_plan(const Dims& d, int op) {
     p.rowm = c.take((size_t)rows_q * sizeof(float2));  // {LSE log2 e, D} per query row
     p.pbar = c.take((size_t)ent * kBlock * sizeof(uint16_t));  // teacher rows (fp16), one per entry
     p.lpxe = c.take((size_t)ent * sizeof(float));            // proxy log-normaliser per entry
-    p.emeta = c.take((size_t)ent * d.G * sizeof(float2));    // rowm per entry and head
+    p.emeta = c.take((size_t)ent * d.Gp() * sizeof(float2));  // rowm per entry and query head
     p.dq = c.take((size_t)rows_q * kD * sizeof(float));
     p.dk = c.take((size_t)rows_kv * kD * sizeof(float));
     p.dv = c.take((size_t)rows_kv * kD * sizeof(float));
     p.dqp = c.take((size_t)rows_p * kD * sizeof(float));
     p.dkp = c.take((size_t)rows_kp * kD * sizeof(float));
   }
+  if (op == MSA_OP_DECODE) p.scores = c.take((size_t)d.B * d.Hp * d.nblk * sizeof(float));
   p.bytes = c.off;
   return p;
 }
@@ -209,21 +211,25 @@ int check_shape(const msa_shape_t* s, int op, Dims* out) {
     set_err("S must be a multiple of 128 and at most 2^23");
     return MSA_ERR_UNSUPPORTED;
   }
-  if (s->Hp != s->Hkv) {
-    set_err("proxy heads must equal KV heads (one proxy head per GQA group)");
+  if (s->Hq % s->Hkv != 0 || s->Hq % s->Hp != 0 || (s->Hp % s->Hkv != 0 && s->Hkv % s->Hp != 0)) {
+    set_err("proxy heads: Hq must be a multiple of Hkv and of Hp, and one of Hp, Hkv a multiple "
+            "of the other");
     return MSA_ERR_UNSUPPORTED;
   }
-  if (s->Hq % s->Hkv != 0) {
-    set_err("Hq must be a multiple of Hkv");
-    return MSA_ERR_UNSUPPORTED;
-  }
-  const int G = s->Hq / s->Hkv;
+  // heads per attention group: the query heads that share one selection row and one KV head
+  // (the warmup forward has no selection: its groups are the GQA groups)
+  const int G = op == MSA_OP_WARMUP_FORWARD ? s->Hq / s->Hkv : s->Hq / (s->Hp > s->Hkv ? s->Hp : s->Hkv);
   const bool bwd = op == MSA_OP_BACKWARD || op == MSA_OP_WARMUP_BACKWARD;
   if (!(G == 1 || G == 2 || G == 4 || G == 8 || G == 16) || (bwd && G < 4)) {
-    set_err("group size Hq/Hkv must be 4, 8 or 16 (1 and 2 also allowed in the forward ops)");
+    set_err("heads per attention group, Hq / max(Hp, Hkv), must be 4, 8 or 16 (1 and 2 also "
+            "allowed in the forward ops)");
     return MSA_ERR_UNSUPPORTED;
   }
-  const bool sparse = op == MSA_OP_FORWARD || op == MSA_OP_BACKWARD;
+  const bool sparse = op == MSA_OP_FORWARD || op == MSA_OP_BACKWARD || op == MSA_OP_DECODE;
+  if (op == MSA_OP_DECODE && s->Hp > 32) {
+    set_err("the decode step supports at most 32 proxy heads");
+    return MSA_ERR_UNSUPPORTED;
+  }
   if (sparse && (s->top_k < 1 || s->top_k > 64)) {
     set_err("top_k must be in [1, 64]");
     return MSA_ERR_UNSUPPORTED;
@@ -248,6 +254,7 @@ int check_shape(const msa_shape_t* s, int op, Dims* out) {
   d.Hkv = s->Hkv;
   d.Hp = s->Hp;
   d.G = G;
+  d.R = op == MSA_OP_WARMUP_FORWARD || s->Hkv <= s->Hp ? 1 : s->Hkv / s->Hp;
   d.top_k = sparse ? s->top_k : 1;
   d.nblk = s->S / kBlock;
   d.scale = s->scale;
@@ -363,7 +370,7 @@ extern "C" {
 
 size_t msa_workspace_size(const msa_shape_t* shape, int op) {
   Dims d;
-  if (op < MSA_OP_FORWARD || op > MSA_OP_WARMUP_BACKWARD) return 0;
+  if (op < MSA_OP_FORWARD || op > MSA_OP_DECODE) return 0;
   if (check_shape(shape, op, &d) != MSA_OK) return 0;
   return make_plan(d, op).bytes;
 }
@@ -453,6 +460,8 @@ int msa_backward(const msa_shape_t* shape, const void* q, const void* k, const v
                       at<float2>(workspace, p.rowm), at<float>(workspace, p.lpxe),
                       at<float2>(workspace, p.emeta), st);
   });
+  if (d.R > 1)  // teacher rows accumulated over the proxy head's attention groups
+    cudaMemsetAsync(at<char>(workspace, p.pbar), 0, (size_t)d.B * d.S * d.Hp * d.top_k * kBlock * 2, st);
   bool ok = true;
   timed("attn_bwd", st, [&] {
     ok = launch_attn_bwd(d, false, q, k, v, dout, at<float2>(workspace, p.emeta),
@@ -544,6 +553,8 @@ int msa_warmup_backward(const msa_shape_t* shape, const void* q, const void* k, 
                       at<float>(workspace, p.lse_px), at<float2>(workspace, p.rowm),
                       at<float>(workspace, p.lpxe), at<float2>(workspace, p.emeta), st);
   });
+  if (d.R > 1)  // teacher rows accumulated over the proxy head's attention groups
+    cudaMemsetAsync(at<char>(workspace, p.pbar), 0, (size_t)dense_entries(d) * kBlock * 2, st);
   bool ok = true;
   timed("attn_bwd_dense", st, [&] {
     ok = launch_attn_bwd(d, true, q, k, v, dout, at<float2>(workspace, p.emeta),
@@ -568,6 +579,26 @@ int msa_warmup_backward(const msa_shape_t* shape, const void* q, const void* k, 
   if (kl_out) timed("kl_finalize", st, [&] { launch_kl_finalize(d, kl_acc, kl_out, st); });
   emit_grads(d, p, workspace, dq, dk, dv, dqp, dkp, st);
   return cuda_fail("msa_warmup_backward");
+}
+
+int msa_decode(const msa_shape_t* shape, const void* q, const void* qp, const void* k_cache,
+               const void* v_cache, const void* kp_cache, const int32_t* seq_len,
+               int32_t* block_idx, void* o, float* lse, void* workspace, size_t workspace_bytes,
+               void* stream) {
+  Dims d;
+  int rc = check_shape(shape, MSA_OP_DECODE, &d);
+  if (rc) return rc;
+  if ((rc = check_ptrs({q, qp, k_cache, v_cache, kp_cache, seq_len, block_idx, o, lse}))) return rc;
+  const Plan p = make_plan(d, MSA_OP_DECODE);
+  if ((rc = check_ws(p, workspace, workspace_bytes))) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaGetLastError();
+  unsigned* status = at<unsigned>(workspace, p.status);
+  cudaMemsetAsync(status, 0, sizeof(unsigned), st);
+  g_launches.fetch_add(3, std::memory_order_relaxed);  // scores, selection, attention
+  launch_decode(d, q, qp, k_cache, v_cache, kp_cache, seq_len, block_idx, o, lse,
+                at<float>(workspace, p.scores), status, st);
+  return cuda_fail("msa_decode");
 }
 
 int msa_device_status(void* workspace, unsigned* flags, void* stream) {

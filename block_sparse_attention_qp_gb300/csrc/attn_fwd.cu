@@ -74,6 +74,26 @@ __device__ __forceinline__ float ex2f(float x) {
 }
 __device__ __forceinline__ uint32_t par(long long k) { return (uint32_t)(k & 1); }
 
+// Maximum of the first lim + 1 (<= 32) of 32 fp32 values held as bits, -inf if lim < 0; a
+// depth-5 tree, overwriting v.
+__device__ __forceinline__ float tree_max32(uint32_t (&v)[32], int lim) {
+#pragma unroll
+  for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(c <= lim ? __uint_as_float(v[c]) : -INFINITY);
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1)
+#pragma unroll
+    for (int c = 0; c < w; ++c) v[c] = __float_as_uint(fmaxf(__uint_as_float(v[c]), __uint_as_float(v[c + w])));
+  return __uint_as_float(v[0]);
+}
+// Sum of 32 fp32 values held as bits, as a depth-5 tree, overwriting v.
+__device__ __forceinline__ float tree_sum32(uint32_t (&v)[32]) {
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1)
+#pragma unroll
+    for (int c = 0; c < w; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) + __uint_as_float(v[c + w]));
+  return __uint_as_float(v[0]);
+}
+
 // The K/V ring: loads alternate K, V, K, V, ... (load L = 2 * item + {0: K, 1: V}) over kRing
 // slots, so the next item's V can land as soon as the current item's K is no longer needed.
 struct RingPos {
@@ -190,9 +210,10 @@ __global__ void __launch_bounds__(448, 1)
       const Item item = A.items[it];
       const int n = item.seg % d.nblk;
       const int bg = (int)((item.seg % d.nseg()) / d.nblk);
-      const int b = bg / d.Hp, g = bg % d.Hp;
+      const int b = bg / d.Hp, g = bg % d.Hp;  // g: proxy head (selection row)
       const int row0 = b * d.S + n * kBlock;
-      const int kvh = kProxy ? 0 : g;  // the proxy key head is shared by every group
+      // KV head of the item's attention group; the proxy key head is shared by every group
+      const int kvh = kProxy ? 0 : d.kv_of(g * d.R + item.sub);
       for (int w = 0; w < kLoads; ++w) {
         const RingPos rp = ring_pos(nl);
         if (rp.use >= 1 && !mbar_wait_warp(&sh->kv_empty[rp.slot], rp.parity ^ 1u, A.status)) {
@@ -327,7 +348,7 @@ __global__ void __launch_bounds__(448, 1)
         }
         __syncwarp();
         const int bg = (int)((cur.seg % d.nseg()) / d.nblk);
-        const int b = bg / d.Hp, g = bg % d.Hp;
+        const int b = bg / d.Hp, a = (bg % d.Hp) * d.R + cur.sub;  // attention group
         uint8_t* dQb = sQ + qb * kFwdTile;
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
@@ -335,7 +356,7 @@ __global__ void __launch_bounds__(448, 1)
           const int r = 32 * gw + (c >> 4), ch = c & 15;
           const int t = sh->tok[qb][r / G];
           const uint32_t off = (ch >> 3) * (kFwdRows * 128) + sm100::sw128_chunk(r, ch & 7);
-          const size_t grow = (((size_t)b * d.S + (t < 0 ? 0 : t)) * d.Hq + g * G + r % G) * kD + ch * 8;
+          const size_t grow = (((size_t)b * d.S + (t < 0 ? 0 : t)) * d.Hq + a * G + r % G) * kD + ch * 8;
           cp_async16_hint(dQb + off, A.q + grow, t >= 0, pol_q);
         }
         cp_async_arrive(&sh->q_full[qb]);
@@ -375,7 +396,7 @@ __global__ void __launch_bounds__(448, 1)
       const Item item = A.items[it];
       const int n = item.seg % d.nblk;
       const int bg = (int)((item.seg % d.nseg()) / d.nblk);
-      const int b = bg / d.Hp, g = bg % d.Hp;
+      const int b = bg / d.Hp, a = (bg % d.Hp) * d.R + item.sub;  // attention group
       const int ntiles = (item.count + TT - 1) / TT;
       for (int tl = 0; tl < ntiles; ++tl, ++i) {
         const int bb = (int)(i & 1), qb = (int)(i % kQBuf);
@@ -398,17 +419,17 @@ __global__ void __launch_bounds__(448, 1)
         // tcgen05.ld / st are warp-collective (.sync.aligned): the path must be uniform per warp
         if (__all_sync(0xffffffffu, lim == kBlock - 1)) {
           // ---- every key of every row of this warp visible
+          // (each 32-column chunk is reduced as a tree in place: a running max or sum over all
+          // 128 columns would be a 128-step dependency chain)
           float mx = -INFINITY;
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             uint32_t v0[32];
             tmem_ld32(Sb + q * 32, v0);
             tmem_wait_ld();
-#pragma unroll
-            for (int c = 0; c < 32; ++c) mx = fmaxf(mx, __uint_as_float(v0[c]));
+            mx = fmaxf(mx, tree_max32(v0, 31));
           }
           m2 = mx * sl2;
-          float la = 0.f, lc = 0.f;
 #pragma unroll 1  // (a full unroll makes the compiler spill)
           for (int q = 0; q < 4; ++q) {
             uint32_t v0[32];
@@ -419,13 +440,13 @@ __global__ void __launch_bounds__(448, 1)
             for (int c = 0; c < 16; ++c) {
               const float a0 = ex2f(fmaf(__uint_as_float(v0[2 * c]), sl2, -m2));
               const float a1 = ex2f(fmaf(__uint_as_float(v0[2 * c + 1]), sl2, -m2));
-              la += a0;
-              lc += a1;
               pw[c] = pack_bf16(a0, a1);
+              v0[2 * c] = __float_as_uint(a0);
+              v0[2 * c + 1] = __float_as_uint(a1);
             }
             if constexpr (!kProxy) tmem_st16(Sb + q * 16, pw);
+            l += tree_sum32(v0);
           }
-          l = la + lc;
         } else {
           // ---- some row of this warp is in its local block (keys after the token masked) or is
           // a padding row (lim = -1)
@@ -435,9 +456,7 @@ __global__ void __launch_bounds__(448, 1)
             uint32_t v0[32];
             tmem_ld32(Sb + q * 32, v0);
             tmem_wait_ld();
-#pragma unroll
-            for (int c = 0; c < 32; ++c)
-              mx = fmaxf(mx, q * 32 + c <= lim ? __uint_as_float(v0[c]) : -INFINITY);
+            mx = fmaxf(mx, tree_max32(v0, lim - q * 32));
           }
           m2 = lim < 0 ? 0.f : mx * sl2;
 #pragma unroll 1  // (a full unroll makes the compiler spill)
@@ -454,14 +473,16 @@ __global__ void __launch_bounds__(448, 1)
               float a1 = ex2f(fmaf(__uint_as_float(v0[2 * c + 1]), sl2, -m2));
               a0 = k0 <= lim ? a0 : 0.f;
               a1 = k0 + 1 <= lim ? a1 : 0.f;
-              l += a0 + a1;
               pw[c] = pack_bf16(a0, a1);
+              v0[2 * c] = __float_as_uint(a0);
+              v0[2 * c + 1] = __float_as_uint(a1);
             }
             if constexpr (!kProxy) tmem_st16(Sb + q * 16, pw);
+            l += tree_sum32(v0);
           }
         }
         const bool valid = t >= 0;
-        const long long dst = valid ? (((long long)b * d.S + t) * d.Hq + g * G + r % G) * d.top_k + slot : -1;
+        const long long dst = valid ? (((long long)b * d.S + t) * d.Hq + a * G + r % G) * d.top_k + slot : -1;
         const float sc = valid ? __fdividef(1.f, l) : 0.f;
         const float lse = valid ? (m2 + __log2f(l)) * kLn2 : 0.f;
         tmem_wait_st();
@@ -583,6 +604,7 @@ bool launch_proxy_lse_sparse(const Dims& d, const void* qp, const void* kp, cons
   a.d = d;
   a.d.Hq = d.Hp;  // rows are the proxy heads' query rows: one per (token, group)
   a.d.G = 1;
+  a.d.R = 1;
   a.q = (const bf16*)qp;
   a.seg_offset = seg_offset;
   a.entries = entries;

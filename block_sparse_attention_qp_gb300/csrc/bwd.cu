@@ -164,6 +164,10 @@ __device__ __forceinline__ void st_global_h_hint(__half* p, float v, uint64_t po
                "h"(__half_as_ushort(__float2half_rn(v))), "l"(pol)
                : "memory");
 }
+__device__ __forceinline__ void red_add_h(__half* p, float v) {
+  asm volatile("red.global.add.noftz.f16 [%0], %1;\n" ::"l"(p), "h"(__half_as_ushort(__float2half_rn(v)))
+               : "memory");
+}
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(a), "r"(b), "r"(c),
@@ -307,14 +311,14 @@ __global__ void __launch_bounds__(352, 1)
         const Item item = A.items[it];
         const int n = item.seg % d.nblk;
         const int bg = (int)((item.seg % d.nseg()) / d.nblk);
-        const int b = bg / d.Hp, g = bg % d.Hp;
+        const int b = bg / d.Hp, kvh = d.kv_of((bg % d.Hp) * d.R + item.sub);
         if (ni > 0 && !mbar_wait(&sh->kv_empty, par(ni - 1), A.status)) break;
         const int row0 = b * d.S + n * kBlock;
         mbar_expect_tx(&sh->kv_full, 2 * kKV);
-        tma_load_3d(sK, &tm_k, 0, g, row0, &sh->kv_full);
-        tma_load_3d(sK + kKV / 2, &tm_k, 64, g, row0, &sh->kv_full);
-        tma_load_3d(sV, &tm_v, 0, g, row0, &sh->kv_full);
-        tma_load_3d(sV + kKV / 2, &tm_v, 64, g, row0, &sh->kv_full);
+        tma_load_3d(sK, &tm_k, 0, kvh, row0, &sh->kv_full);
+        tma_load_3d(sK + kKV / 2, &tm_k, 64, kvh, row0, &sh->kv_full);
+        tma_load_3d(sV, &tm_v, 0, kvh, row0, &sh->kv_full);
+        tma_load_3d(sV + kKV / 2, &tm_v, 64, kvh, row0, &sh->kv_full);
       }
     }
   } else if (warp == 1) {
@@ -408,7 +412,8 @@ __global__ void __launch_bounds__(352, 1)
       if (it >= total) break;
       const Item item = A.items[it];
       const int bg = (int)((item.seg % d.nseg()) / d.nblk);
-      const int b = bg / d.Hp, g = bg % d.Hp;
+      const int b = bg / d.Hp, a = (bg % d.Hp) * d.R + item.sub;  // attention group
+      const int gp = d.Gp();  // row data per entry: the proxy head's Gp query heads
       const long long tb = item_base<kDense>(d, A.seg_offset, item);
       const long long eb = (long long)A.seg_offset[item.seg] + item.first;  // first list entry
       auto load_tokens = [&](int pos0, int valid, int (&tv)[TT]) {
@@ -421,7 +426,8 @@ __global__ void __launch_bounds__(352, 1)
       auto load_meta = [&](int tl_) -> float2 {
         const int x = tl_ * TT + (r0 + ch) / G;
         float2 m = make_float2(0.f, 0.f);
-        if (hi == 0 && x < item.count) m = __ldg(A.emeta + (size_t)(eb + x) * G + (r0 + ch) % G);
+        if (hi == 0 && x < item.count)
+          m = __ldg(A.emeta + (size_t)(eb + x) * gp + item.sub * G + (r0 + ch) % G);
         return m;
       };
       const int ntiles = (item.count + TT - 1) / TT;
@@ -451,7 +457,7 @@ __global__ void __launch_bounds__(352, 1)
           const int r = r0 + rr;
           const int t = wt[(2 * k) / G];
           const uint32_t off = (ch >> 3) * (kTR * 128) + sm100::sw128_chunk(r, ch & 7);
-          const size_t grow = (((size_t)b * d.S + (t < 0 ? 0 : t)) * d.Hq + g * G + rr % G) * kD + ch * 8;
+          const size_t grow = (((size_t)b * d.S + (t < 0 ? 0 : t)) * d.Hq + a * G + rr % G) * kD + ch * 8;
           cp_async16_hint(dQb + off, A.q + grow, t >= 0, keep);
           cp_async16_hint(ddOb + off, A.dout + grow, t >= 0, keep);
         }
@@ -483,7 +489,7 @@ __global__ void __launch_bounds__(352, 1)
         if (it >= total) break;
         const Item item = A.items[it];
         const int bg = (int)((item.seg % d.nseg()) / d.nblk);
-        const int b = bg / d.Hp, g = bg % d.Hp;
+        const int b = bg / d.Hp, a = (bg % d.Hp) * d.R + item.sub;  // attention group
         const int ntiles = (item.count + TT - 1) / TT;
         for (int tl = 0; tl < ntiles; ++tl, ++ns) {
           const int sl = (int)(ns % kQS);
@@ -493,7 +499,7 @@ __global__ void __launch_bounds__(352, 1)
           for (int x = 0; x < TT; ++x) {
             const int t = sh->tok[sl][x];
             if (t >= 0)
-              bulk_reduce_add(A.dq + (((size_t)b * d.S + t) * d.Hq + g * G) * kD,
+              bulk_reduce_add(A.dq + (((size_t)b * d.S + t) * d.Hq + a * G) * kD,
                               aSt + x * G * kD * 4, G * kD * 4, keep);
           }
           bulk_commit();
@@ -542,7 +548,7 @@ __global__ void __launch_bounds__(352, 1)
       const Item item = A.items[it];
       const int n = item.seg % d.nblk;
       const int bg = (int)((item.seg % d.nseg()) / d.nblk);
-      const int b = bg / d.Hp, g = bg % d.Hp;
+      const int b = bg / d.Hp, kvh = d.kv_of((bg % d.Hp) * d.R + item.sub);
       const int j = n * kBlock + kr;  // this thread's key
       const long long eb = (long long)A.seg_offset[item.seg] + item.first;  // first list entry
       const int ntiles = (item.count + TT - 1) / TT;
@@ -633,11 +639,17 @@ __global__ void __launch_bounds__(352, 1)
         fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh->p_full[bb]);
-        // teacher: mean of the G heads' probabilities of each token, one fp32 row per list entry
+        // teacher: mean of the proxy head's G R query heads' probabilities of each token, one fp16
+        // row per list entry; with R > 1 attention groups per proxy head each adds its share
 #pragma unroll
         for (int x = 0; x < TT; ++x)
-          if (tv[x] >= 0)
-            st_global_h_hint(A.pbar + (size_t)(eb + tl * TT + x) * kBlock + kr, pb[x] * (1.f / G), stream);
+          if (tv[x] >= 0) {
+            __half* dst = A.pbar + (size_t)(eb + tl * TT + x) * kBlock + kr;
+            if (d.R == 1)
+              st_global_h_hint(dst, pb[x] * (1.f / G), stream);
+            else
+              red_add_h(dst, pb[x] * (1.f / (G * d.R)));
+          }
         // ---- epilogue of the previous tile
         if (tl > 0 && !epilogue(i - 1)) { ok = false; break; }
       }
@@ -645,8 +657,8 @@ __global__ void __launch_bounds__(352, 1)
       if (!epilogue(i - 1)) { ok = false; break; }
       // ---- item end: dV and dK rows of this key
       {
-        float* pv = A.dv + (((size_t)b * d.S + j) * d.Hkv + g) * kD;
-        float* pk = A.dk + (((size_t)b * d.S + j) * d.Hkv + g) * kD;
+        float* pv = A.dv + (((size_t)b * d.S + j) * d.Hkv + kvh) * kD;
+        float* pk = A.dk + (((size_t)b * d.S + j) * d.Hkv + kvh) * kD;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t rv[32], rk[32];
@@ -762,7 +774,10 @@ __global__ void __launch_bounds__(384, 1)
         while (!last && pub < ni + 2) {
           const int x = (int)(pub % kIR);
           if (pub >= kIR && !mbar_wait(&sh->it_empty[x], par(pub / kIR - 1), A.status)) break;
-          const int v = atomicAdd(A.sched, 1);
+          // the work items repeat each run of tokens for the proxy head's R attention groups;
+          // the proxy gradients need each run once
+          int v = atomicAdd(A.sched, 1);
+          while (v < total && A.items[v].sub != 0) v = atomicAdd(A.sched, 1);
           sh->it_ring[x] = v;
           mbar_arrive(&sh->it_full[x]);
           last = v >= total;
@@ -1141,21 +1156,19 @@ bool launch_attn_bwd(const Dims& d, bool dense, const void* q, const void* k, co
   a.status = status;
   a.sched = reinterpret_cast<int*>(status + kSchedAttnBwd);
   cudaMemsetAsync(a.sched, 0, sizeof(int), st);
-#define MSA_BWD_CASE(GG)                    \
-  case GG:                                  \
-    if (dense)                              \
-      attn_bwd_g<GG, true>(mk, mv, a, st);  \
-    else                                    \
-      attn_bwd_g<GG, false>(mk, mv, a, st); \
-    break;
   switch (d.G) {
-    MSA_BWD_CASE(4)
-    MSA_BWD_CASE(8)
-    MSA_BWD_CASE(16)
+    case 4:
+      dense ? attn_bwd_g<4, true>(mk, mv, a, st) : attn_bwd_g<4, false>(mk, mv, a, st);
+      break;
+    case 8:
+      dense ? attn_bwd_g<8, true>(mk, mv, a, st) : attn_bwd_g<8, false>(mk, mv, a, st);
+      break;
+    case 16:
+      dense ? attn_bwd_g<16, true>(mk, mv, a, st) : attn_bwd_g<16, false>(mk, mv, a, st);
+      break;
     default:
       return false;
   }
-#undef MSA_BWD_CASE
   return true;
 }
 

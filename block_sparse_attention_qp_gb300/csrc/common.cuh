@@ -17,6 +17,7 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr unsigned kStatusBadIndex = 1u;    // a block index out of range / not ascending
 constexpr unsigned kStatusBadItems = 2u;    // work list larger than its reserved space
 constexpr unsigned kStatusTimeout = 4u;     // a bounded device wait expired
+constexpr unsigned kStatusInternal = 8u;    // a kernel's internal check failed (library bug)
 // Words 8.. of the workspace's status area: work-item counters of the persistent kernels, each
 // zeroed on the launch stream right before its kernel starts.
 constexpr int kSchedAttnBwd = 8;

@@ -89,7 +89,7 @@ __device__ __forceinline__ long long list_len(const Dims& d, bool dense, const i
 
 __device__ __forceinline__ long long items_of(long long c, const ItemSpec& s) {
   const long long tiles = (c + s.tile_tokens - 1) / s.tile_tokens;
-  return (tiles + s.chunk_tiles - 1) / s.chunk_tiles;
+  return (tiles + s.chunk_tiles - 1) / s.chunk_tiles * s.nsub;
 }
 
 // Single-CTA exclusive scan over every list of three running sums: list lengths and the item
@@ -152,24 +152,25 @@ __global__ void items_kernel(Dims d, int dense, const int* __restrict__ seg_coun
   const long long seg = blockIdx.x;
   const long long len = list_len(d, dense, seg_count, seg);
   const int per_item = sp.tile_tokens * sp.chunk_tiles;
-  const long long n_chunks = (len + per_item - 1) / per_item;
+  const long long n_items = (len + per_item - 1) / per_item * sp.nsub;
   const long long base = item_offset[seg];
   const long long list0 = seg_offset ? seg_offset[seg] : 0;
-  for (long long i = threadIdx.x; i < n_chunks; i += blockDim.x) {
+  for (long long i = threadIdx.x; i < n_items; i += blockDim.x) {
     const long long pos = base + i;
     if (pos >= max_items) {
       atomicOr(status, kStatusBadItems);
       continue;
     }
-    const long long first = i * per_item;
-    const long long cnt = len - first < per_item ? len - first : per_item;
-    items[pos] = Item{(int)seg, (int)first, (int)cnt, (int)(list0 + first)};
+    const long long first = i / sp.nsub * per_item;  // the attention groups of a run of tokens
+    const long long cnt = len - first < per_item ? len - first : per_item;  // are consecutive
+    items[pos] = Item{(int)seg, (int)first, (int)cnt, (int)(list0 + first), (int)(i % sp.nsub)};
   }
 }
 
 // Row data of every list entry, in entry order, so the gradient passes read it with the entry
-// instead of through its token: lpxe[e] = LSE_px(b, g, t(e)) * log2 e and, for the G heads of the
-// group, emeta[e G + h] = {LSE(b, g G + h, t(e)) log2 e, D(b, t(e), g G + h)}.
+// instead of through its token: lpxe[e] = LSE_px(b, p, t(e)) * log2 e and, for the Gp = Hq / Hp
+// query heads of proxy head p, emeta[e Gp + h] = {LSE(b, p Gp + h, t(e)) log2 e,
+// D(b, t(e), p Gp + h)}.
 __global__ void entry_meta_kernel(Dims d, int dense, const int* __restrict__ seg_count,
                                   const int* __restrict__ seg_offset, const int* __restrict__ entries,
                                   const float* __restrict__ lse_px, const float2* __restrict__ rowm,
@@ -186,10 +187,11 @@ __global__ void entry_meta_kernel(Dims d, int dense, const int* __restrict__ seg
     const long long t = dense ? t0 + k : (long long)(entries[base + k] >> 8);
     lpxe[base + k] = row[t] * kLog2e;
   }
-  for (long long x = threadIdx.x; x < len * d.G; x += blockDim.x) {
-    const long long k = x / d.G, h = x % d.G;
+  const int gp = d.Gp();
+  for (long long x = threadIdx.x; x < len * gp; x += blockDim.x) {
+    const long long k = x / gp, h = x % gp;
     const long long t = dense ? t0 + k : (long long)(entries[base + k] >> 8);
-    emeta[base * d.G + x] = rowm[((b * d.S + t) * d.Hq + g * d.G + h)];
+    emeta[base * gp + x] = rowm[((b * d.S + t) * d.Hq + g * gp + h)];
   }
 }
 
@@ -228,8 +230,8 @@ void launch_count(const Dims& d, const int32_t* idx, int* seg_count, unsigned* s
 void launch_scan(const Dims& d, bool dense, const int* seg_count, int* seg_offset,
                  const ItemSpec* specs, int nspecs, int* item_offset0, int* item_offset1,
                  int* totals, cudaStream_t st) {
-  ItemSpec s0 = nspecs > 0 ? specs[0] : ItemSpec{1, 1};
-  ItemSpec s1 = nspecs > 1 ? specs[1] : ItemSpec{1, 1};
+  ItemSpec s0 = nspecs > 0 ? specs[0] : ItemSpec{1, 1, 1};
+  ItemSpec s1 = nspecs > 1 ? specs[1] : ItemSpec{1, 1, 1};
   scan_kernel<<<1, 1024, 0, st>>>(d, dense ? 1 : 0, seg_count, seg_offset, s0, s1, nspecs,
                                   item_offset0, item_offset1, totals);
 }

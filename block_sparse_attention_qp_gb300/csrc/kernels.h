@@ -6,25 +6,33 @@
 
 namespace msa {
 
+// Head mapping (the MSA group is the proxy head): proxy head p selects key blocks for its Hq / Hp
+// query heads.  An attention group is a set of G query heads that share one selection row and
+// one KV head: G = Hq / max(Hp, Hkv), and proxy head p has R = max(1, Hkv / Hp) of them,
+// a = p R + r (r < R), on KV head kv_of(a).  Hp == Hkv: a = p = the GQA group, R = 1.
 struct Dims {
   int B, S, Hq, Hkv, Hp, G, top_k, nblk;
   float scale;
-  int chunk;   // token-list chunk: a list holds the tokens of one (b, g, n) in one chunk of the
+  int chunk;   // token-list chunk: a list holds the tokens of one (b, p, n) in one chunk of the
   int nchunk;  // sequence [c * chunk, (c+1) * chunk); lists are ordered chunk-major
-  __host__ __device__ long long nseg() const { return (long long)B * Hp * nblk; }  // (b, g, n)
-  __host__ __device__ long long nlist() const { return nseg() * nchunk; }           // (c, b, g, n)
+  int R = 1;   // attention groups per proxy head
+  __host__ __device__ long long nseg() const { return (long long)B * Hp * nblk; }  // (b, p, n)
+  __host__ __device__ long long nlist() const { return nseg() * nchunk; }           // (c, b, p, n)
+  __host__ __device__ int kv_of(int a) const { return a / (Hp * R / Hkv); }
+  __host__ __device__ int Gp() const { return G * R; }  // query heads per proxy head
 };
 
-// A unit of attention work: `count` tokens of list `seg` (= c * nseg + (b * Hp + g) * nblk + n)
-// starting at list position `first`; `base` = the list's offset + first, i.e. the position of
-// the item's first entry in the packed entry array.
+// A unit of attention work: `count` tokens of list `seg` (= c * nseg + (b * Hp + p) * nblk + n)
+// starting at list position `first`, for attention group p R + sub; `base` = the list's offset +
+// first, i.e. the position of the item's first entry in the packed entry array.
 struct Item {
-  int seg, first, count, base;
+  int seg, first, count, base, sub;
 };
 
-// Shape of one work list: tiles of `tile_tokens` tokens, `chunk_tiles` tiles per item.
+// Shape of one work list: tiles of `tile_tokens` tokens, `chunk_tiles` tiles per item, and
+// `nsub` items (attention groups r = 0 .. nsub-1) for each such run of tokens.
 struct ItemSpec {
-  int tile_tokens, chunk_tiles;
+  int tile_tokens, chunk_tiles, nsub;
 };
 
 // ---------------------------------------------------------------- index kernels (index.cu)
@@ -111,6 +119,14 @@ void launch_kl_finalize(const Dims& d, const double* kl_acc, float* kl_out, cuda
 int bwd_item_tokens();   // tokens per fused-backward work item
 int bwd_group_tokens();  // tokens per proxy-gradient flush group
 void launch_convert(const float* src, void* dst, long long n, cudaStream_t st);
+
+// ---------------------------------------------------------------- decode (decode.cu)
+// One new token per sequence against its cache: proxy block scores (scores [B, Hp, nblk] fp32),
+// selection (block_idx [B, Hp, top_k]) and sparse attention (o [B, Hq, 128], lse [B, Hq]).
+void launch_decode(const Dims& d, const void* q, const void* qp, const void* k_cache,
+                   const void* v_cache, const void* kp_cache, const int32_t* seq_len,
+                   int32_t* block_idx, void* o, float* lse, float* scores, unsigned* status,
+                   cudaStream_t st);
 
 int num_sms();
 void set_api_error(const char* what);

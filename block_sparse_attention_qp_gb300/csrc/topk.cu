@@ -138,7 +138,9 @@ __global__ void __launch_bounds__(256, 1)
       __syncwarp();
       if (!mbar_wait_warp(&sh->acc_full[a], (n / kAcc) & 1, status)) break;
       fence_after_sync();
-      float mx = -INFINITY;
+      float m8[8];  // independent running maxima (no long dependency chain)
+#pragma unroll
+      for (int u = 0; u < 8; ++u) m8[u] = -INFINITY;
 #pragma unroll
       for (int c = 0; c < 4; c += 2) {
         uint32_t r0[32], r1[32];
@@ -146,17 +148,18 @@ __global__ void __launch_bounds__(256, 1)
         tmem_ld32(tmem + lane_base + a * 128 + (c + 1) * 32, r1);
         tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          mx = fmaxf(mx, c * 32 + j <= lim ? __uint_as_float(r0[j]) : -INFINITY);
-          mx = fmaxf(mx, (c + 1) * 32 + j <= lim ? __uint_as_float(r1[j]) : -INFINITY);
-        }
+        for (int j = 0; j < 32; ++j)
+          m8[j & 7] = fmaxf(m8[j & 7], fmaxf(c * 32 + j <= lim ? __uint_as_float(r0[j]) : -INFINITY,
+                                             (c + 1) * 32 + j <= lim ? __uint_as_float(r1[j]) : -INFINITY));
       }
+      const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       if (mx > m) {  // column 0 is always visible, so mx is finite
         l *= ex2_approx((m - mx) * sl2);  // m = -inf: l = 0 anyway
         m = mx;
       }
       const float mb = m * sl2;
-      float la = 0.f, lc = 0.f;
+      float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < 4; c += 2) {
         uint32_t r0[32], r1[32];
@@ -168,11 +171,10 @@ __global__ void __launch_bounds__(256, 1)
           // exponentiate unconditionally, then select: no per-lane branches
           const float e0 = ex2_approx(fmaf(__uint_as_float(r0[j]), sl2, -mb));
           const float e1 = ex2_approx(fmaf(__uint_as_float(r1[j]), sl2, -mb));
-          la += c * 32 + j <= lim ? e0 : 0.f;
-          lc += (c + 1) * 32 + j <= lim ? e1 : 0.f;
+          s8[j & 7] += (c * 32 + j <= lim ? e0 : 0.f) + ((c + 1) * 32 + j <= lim ? e1 : 0.f);
         }
       }
-      l += la + lc;
+      l += ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
       fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh->acc_empty[a]);
@@ -196,7 +198,10 @@ __global__ void __launch_bounds__(256, 1)
       __syncwarp();
       if (!mbar_wait_warp(&sh->acc_full[a], (n / kAcc) & 1, status)) break;
       fence_after_sync();
-      float mx = -INFINITY;
+      // eight independent running maxima: a single one would be a 128-step dependency chain
+      float m8[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) m8[u] = -INFINITY;
 #pragma unroll
       for (int c = 0; c < 4; c += 2) {
         uint32_t r0[32], r1[32];
@@ -205,8 +210,10 @@ __global__ void __launch_bounds__(256, 1)
         tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-          mx = fmaxf(mx, fmaxf(__uint_as_float(r0[j]), __uint_as_float(r1[j])));
+          m8[j & 7] = fmaxf(m8[j & 7], fmaxf(__uint_as_float(r0[j]), __uint_as_float(r1[j])));
       }
+      const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh->acc_empty[a]);

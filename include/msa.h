@@ -71,13 +71,15 @@ enum msa_op {
   MSA_OP_FORWARD = 0,
   MSA_OP_BACKWARD = 1,
   MSA_OP_WARMUP_FORWARD = 2,
-  MSA_OP_WARMUP_BACKWARD = 3
+  MSA_OP_WARMUP_BACKWARD = 3,
+  MSA_OP_DECODE = 4
 };
 
 /* Bits of the device status word. */
 #define MSA_DEVICE_BAD_INDEX 1u /* a given block index was out of range or not ascending */
 #define MSA_DEVICE_BAD_ITEMS 2u /* internal work list overflow (a library bug) */
 #define MSA_DEVICE_TIMEOUT 4u   /* a bounded device-side wait gave up */
+#define MSA_DEVICE_INTERNAL 8u  /* a kernel's internal layout check failed (a library bug) */
 
 /* Bytes of workspace `op` needs for `shape` (0 if the shape is unsupported). */
 MSA_API size_t msa_workspace_size(const msa_shape_t* shape, int op);
@@ -139,6 +141,27 @@ MSA_API int msa_warmup_backward(const msa_shape_t* shape, const void* q, const v
                         const void* dout, float kl_grad, void* dq, void* dk, void* dv, void* dqp,
                         void* dkp, float* kl_out, void* workspace, size_t workspace_bytes,
                         void* stream);
+
+/*
+ * Decode step of MSA inference (forum summary, "GPU kernel co-design", deployment setting
+ * B = 128, k = 16; the prefill is msa_forward).  One new token per sequence b, at position
+ * t_b = seq_len[b] - 1 of its caches, whose K, V and proxy key rows must already hold it:
+ *   q         [B, Hq, 128]  bf16   the new tokens' queries
+ *   qp        [B, Hp, 128]  bf16   their proxy queries
+ *   k_cache, v_cache [B, S, Hkv, 128] bf16, kp_cache [B, S, 128] bf16: caches of capacity S
+ *             (shape->S, a multiple of 128); rows after t_b are never read
+ *   seq_len   [B] int32 device array, 1 <= seq_len[b] <= S (other values: the row is skipped and
+ *             MSA_DEVICE_BAD_INDEX set)
+ * Writes block_idx [B, Hp, top_k] (the selection of the new token: the local block t_b / 128 and
+ * the best top_k - 1 earlier blocks by raw proxy score, ties to the lower block, ascending, -1
+ * padded), o [B, Hq, 128] bf16 and lse [B, Hq] fp32 -- the same values as row t_b of msa_forward
+ * on the whole sequence.  Head mapping and limits as for msa_forward, with Hp <= 32.  Workspace:
+ * msa_workspace_size(shape, MSA_OP_DECODE).
+ */
+MSA_API int msa_decode(const msa_shape_t* shape, const void* q, const void* qp,
+                       const void* k_cache, const void* v_cache, const void* kp_cache,
+                       const int32_t* seq_len, int32_t* block_idx, void* o, float* lse,
+                       void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Reads (and clears) the device status word of `workspace` after the work queued on `stream`

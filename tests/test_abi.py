@@ -41,8 +41,16 @@ def test_workspace_size_is_host_only(lib):
     bad = binding.Shape(1, 1000, 8, 2, 2, 128, 4, 0.1)  # S not a multiple of 128
     assert lib.msa_workspace_size(ctypes.byref(bad), 0) == 0
     assert b"multiple of 128" in lib.msa_last_error()
-    assert lib.msa_workspace_size(ctypes.byref(binding.Shape(1, 256, 8, 2, 4, 128, 4, 0.1)), 0) == 0
+    # proxy heads that do not divide the query heads, or that neither divide nor are divided by
+    # the KV heads, are rejected; Hp < Hkv and Hp > Hkv mappings are accepted
+    assert lib.msa_workspace_size(ctypes.byref(binding.Shape(1, 256, 8, 2, 3, 128, 4, 0.1)), 0) == 0
     assert b"proxy heads" in lib.msa_last_error()
+    assert lib.msa_workspace_size(ctypes.byref(binding.Shape(1, 256, 24, 6, 4, 128, 4, 0.1)), 0) == 0
+    assert binding.msa_workspace_size(binding.Shape(1, 256, 16, 4, 2, 128, 4, 0.1), 1) > 0
+    assert binding.msa_workspace_size(binding.Shape(1, 256, 16, 2, 4, 128, 4, 0.1), 1) > 0
+    # heads per attention group Hq / max(Hp, Hkv) = 2: forward only
+    assert binding.msa_workspace_size(binding.Shape(1, 256, 8, 2, 4, 128, 4, 0.1), 0) > 0
+    assert lib.msa_workspace_size(ctypes.byref(binding.Shape(1, 256, 8, 2, 4, 128, 4, 0.1)), 1) == 0
     assert lib.msa_workspace_size(ctypes.byref(binding.Shape(1, 256, 8, 2, 2, 64, 4, 0.1)), 0) == 0
     assert lib.msa_workspace_size(ctypes.byref(binding.Shape(1, 256, 8, 2, 2, 128, 65, 0.1)), 0) == 0
 
@@ -61,6 +69,19 @@ def test_argument_errors_before_any_launch(lib):
     rc = lib.msa_warmup_forward(ctypes.byref(s_bad), null, null, null, null, null, null, 0, null)
     assert rc == 1
     assert lib.msa_status_string(3) == b"workspace too small"
+
+
+def test_decode_host_checks(lib):
+    s = binding.Shape(128, 65536, 64, 8, 8, 128, 16, 128 ** -0.5)
+    assert binding.msa_workspace_size(s, binding.OP_DECODE) > 0
+    P = ctypes.c_void_p
+    null = P(0)
+    rc = lib.msa_decode(ctypes.byref(s), null, null, null, null, null, null, null, null, null,
+                        null, 0, null)
+    assert rc == 1  # null pointers, before any launch
+    many = binding.Shape(1, 256, 64, 1, 64, 128, 4, 0.1)  # 64 proxy heads: too many for decode
+    assert lib.msa_workspace_size(ctypes.byref(many), binding.OP_DECODE) == 0
+    assert b"32 proxy heads" in lib.msa_last_error()
 
 
 def test_selftest_rejects_bad_arguments_on_the_host(lib):

@@ -33,7 +33,7 @@ def run_sparse(w: Workload, seed: int, kl_grad=1.0):
     o, lse, _ = msa.msa_forward(g["q"], g["k"], g["v"], g["qp"], g["kp"], w.top_k, w.scale,
                                 block_idx=idx_t, ws=ws)
     assert msa.msa_device_status(ws) == 0
-    if w.Hq // w.Hkv < 4:  # the backward supports group sizes 4, 8 and 16
+    if w.Hq // max(w.Hp, w.Hkv) < 4:  # the backward supports 4, 8 and 16 heads per attention group
         o_ref, lse_ref = oracle.forward(x["q"], x["k"], x["v"], oidx, w.top_k, w.scale)
         close("O", o, o_ref)
         close("LSE", lse, lse_ref)
@@ -82,6 +82,37 @@ SMALL = [
 def test_sparse_small(name, B, S, Hq, Hkv, k, planted):
     w = Workload(name, B=B, S=S, Hq=Hq, Hkv=Hkv, Hp=Hkv, top_k=k, planted=planted)
     run_sparse(w, seed=100 + S + Hq)
+
+
+MAPPINGS = [
+    # name, B, S, Hq, Hkv, Hp, top_k: one proxy head selecting for several GQA groups (Hp < Hkv,
+    # the inverted mapping), and GQA groups split among proxy heads (Hp > Hkv)
+    ("hp_lt_hkv_r2", 1, 1024, 16, 4, 2, 4),
+    ("hp_lt_hkv_r4_b2", 2, 640, 16, 4, 1, 3),
+    ("hp_gt_hkv", 1, 1024, 16, 2, 4, 4),
+    ("hp_gt_hkv_fwd_only", 1, 768, 8, 2, 4, 3),
+]
+
+
+@pytest.mark.parametrize("name,B,S,Hq,Hkv,Hp,k", MAPPINGS, ids=[c[0] for c in MAPPINGS])
+def test_sparse_proxy_kv_head_mappings(name, B, S, Hq, Hkv, Hp, k):
+    w = Workload(name, B=B, S=S, Hq=Hq, Hkv=Hkv, Hp=Hp, top_k=k)
+    run_sparse(w, seed=700 + S + Hq + Hp)
+
+
+@pytest.mark.parametrize("B,S,Hq,Hkv,Hp", [(1, 768, 16, 4, 2), (1, 640, 16, 2, 4)])
+def test_warmup_proxy_kv_head_mappings(B, S, Hq, Hkv, Hp):
+    w = Workload("wmap", B=B, S=S, Hq=Hq, Hkv=Hkv, Hp=Hp, top_k=0)
+    x = make_inputs(w, 800 + S + Hp)
+    g = to_dev(x)
+    o, lse = msa.msa_warmup_forward(g["q"], g["k"], g["v"], w.scale)
+    *grads, kl = msa.msa_warmup_backward(g["q"], g["k"], g["v"], g["qp"], g["kp"], o, lse,
+                                         g["dout"], w.scale, return_kl=True)
+    torch.cuda.synchronize()
+    ref = oracle.backward(x["q"], x["k"], x["v"], x["qp"], x["kp"], x["dout"], None, 1, w.scale)
+    for name_, gt in zip(("dq", "dk", "dv", "dqp", "dkp"), grads):
+        close(name_, gt, ref[name_])
+    check_kl(kl, ref["kl"])
 
 
 def test_sparse_kl_grad_scales_proxy_only():
@@ -151,8 +182,9 @@ def test_cfg2_full_parity():
 
 
 def test_kl_value_does_not_change_the_gradients():
-    """Asking for the KL value leaves every gradient bit-identical up to fp32 summation order
-    (the value is computed beside the proxy gradients, not from them)."""
+    """Asking for the KL value leaves every gradient unchanged up to fp32 summation order (the
+    gradient accumulators take reductions in whatever order blocks finish; measured 1.7e-5 rel
+    between two runs), since the value is computed beside the proxy gradients, not from them."""
     w = Workload("klv", B=1, S=1024, Hq=8, Hkv=2, Hp=2, top_k=4)
     g = to_dev(make_inputs(w, 61))
     o, lse, idx = msa.msa_forward(g["q"], g["k"], g["v"], g["qp"], g["kp"], w.top_k, w.scale)
@@ -161,7 +193,7 @@ def test_kl_value_does_not_change_the_gradients():
     *b, kl = msa.msa_backward(g["q"], g["k"], g["v"], g["qp"], g["kp"], o, lse, g["dout"], idx,
                               w.top_k, w.scale, return_kl=True)
     for name, x, y in zip(("dq", "dk", "dv", "dqp", "dkp"), a, b):
-        close(name, x, y.float(), rel=1e-5, atol=1e-3, ulps=1.0)
+        close(name, x, y.float(), rel=1e-4, atol=2e-3, ulps=1.0)
     assert float(kl) > 0
 
 
