@@ -2,6 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload msa_s64k_planted] [--no-cpu-baseline] [--no-e2e]
+    python bench.py --workload msa_decode_b128     (decode step of inference; not the default)
 
 One step = msa_forward (proxy top-k selection + sparse attention) followed by msa_backward
 (dQ, dK, dV, dQp, dKp) on one batch of the workload, inputs resident in HBM.  Prints one JSON
@@ -452,6 +453,71 @@ def cpu_baseline(w, wi, args):
                                       "cores": 1, "sample": "the whole msa_s1k step"}}
 
 
+# ------------------------------------------------------------------------------ decode (inference)
+DECODE = dict(name="msa_decode_b128", B=128, ctx=32768, Hq=64, Hkv=8, Hp=8, top_k=16)
+
+
+def run_decode(args):
+    """One decode step per iteration: B sequences, each decoding its next token against caches of
+    `ctx` tokens (proxy block scores over the whole proxy-key cache, selection, sparse attention
+    over the 16 selected blocks).  Caches are drawn on the device (seeded) -- they are inputs of
+    the step, not work inside it.  Memory-bound: reported against the measured copy bandwidth."""
+    from block_sparse_attention_qp_gb300 import binding as msa
+
+    c = DECODE
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    msa.load_library()
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(2001)
+    B, S, Hq, Hkv, Hp, D = c["B"], c["ctx"], c["Hq"], c["Hkv"], c["Hp"], 128
+
+    def rnd(*shape):
+        return torch.randn(*shape, generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+
+    k, v, kp = rnd(B, S, Hkv, D), rnd(B, S, Hkv, D), rnd(B, S, 1, D)
+    q, qp = rnd(B, Hq, D), rnd(B, Hp, D)
+    seq_len = torch.full((B,), S, dtype=torch.int32, device=dev)
+    shape = msa.Shape(B, S, Hq, Hkv, Hp, D, c["top_k"], D ** -0.5)
+    ws = msa.workspace(shape, msa.OP_DECODE, dev)
+
+    def step():
+        return msa.msa_decode(q, qp, k, v, kp, seq_len, c["top_k"], D ** -0.5, ws=ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clk:
+        e0.record()
+        for _ in range(args.steps):
+            step()
+        e1.record()
+        torch.cuda.synchronize()
+    status = msa.msa_device_status(ws)
+    sec = e0.elapsed_time(e1) / 1e3 / args.steps
+    # bytes one step must read: every proxy-key row before the local block, the selected K and V
+    # blocks of every (sequence, KV head), the queries; and write: outputs and selection
+    kp_bytes = B * (S - 128) * D * 2
+    kv_bytes = B * Hkv * c["top_k"] * 128 * D * 2 * 2
+    io_bytes = B * (Hq + Hp) * D * 2 + B * Hq * (D * 2 + 4) + B * Hp * c["top_k"] * 4
+    gbs = (kp_bytes + kv_bytes + io_bytes) / sec / 1e9
+    peaks, peak_src = measured_peaks()
+    line = {"metric": "MSA decode tokens/s (one new token per sequence)", "value": B / sec,
+            "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (caches drawn on the device)",
+            "config": {"workload": c["name"], "B": B, "context": S, "Hq": Hq, "Hkv": Hkv,
+                       "Hp": Hp, "d": D, "top_k": c["top_k"], "block": 128,
+                       "l2": f"caches larger than L2 ({(2 * k.numel() + kp.numel()) * 2 / 2**30:.1f} GiB); no flush"},
+            "roofline": {"kernel": "decode (scores + selection + attention)", "bound": "hbm",
+                         "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                         "peak_note": f"copy bandwidth {peak_src}"},
+            "gpu_launches": 3 * args.steps, "clocks": clk.summary(), "device_status": status}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -466,6 +532,13 @@ def main():
     if args.warmup < 3:
         print("bench: raising --warmup to the minimum of 3", file=sys.stderr)
         args.warmup = 3
+    if args.workload == DECODE["name"]:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the decode mode has no CPU "
+                              "reference arm; its parity is tested against the oracle's rows"}))
+            return
+        run_decode(args)
+        return
     wi, w = workload_by_name(args.workload)
     if args.impl == "reference":
         run_reference(args, w, wi)

@@ -74,26 +74,6 @@ __device__ __forceinline__ float ex2f(float x) {
 }
 __device__ __forceinline__ uint32_t par(long long k) { return (uint32_t)(k & 1); }
 
-// Maximum of the first lim + 1 (<= 32) of 32 fp32 values held as bits, -inf if lim < 0; a
-// depth-5 tree, overwriting v.
-__device__ __forceinline__ float tree_max32(uint32_t (&v)[32], int lim) {
-#pragma unroll
-  for (int c = 0; c < 32; ++c) v[c] = __float_as_uint(c <= lim ? __uint_as_float(v[c]) : -INFINITY);
-#pragma unroll
-  for (int w = 16; w >= 1; w >>= 1)
-#pragma unroll
-    for (int c = 0; c < w; ++c) v[c] = __float_as_uint(fmaxf(__uint_as_float(v[c]), __uint_as_float(v[c + w])));
-  return __uint_as_float(v[0]);
-}
-// Sum of 32 fp32 values held as bits, as a depth-5 tree, overwriting v.
-__device__ __forceinline__ float tree_sum32(uint32_t (&v)[32]) {
-#pragma unroll
-  for (int w = 16; w >= 1; w >>= 1)
-#pragma unroll
-    for (int c = 0; c < w; ++c) v[c] = __float_as_uint(__uint_as_float(v[c]) + __uint_as_float(v[c + w]));
-  return __uint_as_float(v[0]);
-}
-
 // The K/V ring: loads alternate K, V, K, V, ... (load L = 2 * item + {0: K, 1: V}) over kRing
 // slots, so the next item's V can land as soon as the current item's K is no longer needed.
 struct RingPos {
@@ -419,17 +399,17 @@ __global__ void __launch_bounds__(448, 1)
         // tcgen05.ld / st are warp-collective (.sync.aligned): the path must be uniform per warp
         if (__all_sync(0xffffffffu, lim == kBlock - 1)) {
           // ---- every key of every row of this warp visible
-          // (each 32-column chunk is reduced as a tree in place: a running max or sum over all
-          // 128 columns would be a 128-step dependency chain)
           float mx = -INFINITY;
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             uint32_t v0[32];
             tmem_ld32(Sb + q * 32, v0);
             tmem_wait_ld();
-            mx = fmaxf(mx, tree_max32(v0, 31));
+#pragma unroll
+            for (int c = 0; c < 32; ++c) mx = fmaxf(mx, __uint_as_float(v0[c]));
           }
           m2 = mx * sl2;
+          float la = 0.f, lc = 0.f;
 #pragma unroll 1  // (a full unroll makes the compiler spill)
           for (int q = 0; q < 4; ++q) {
             uint32_t v0[32];
@@ -440,13 +420,13 @@ __global__ void __launch_bounds__(448, 1)
             for (int c = 0; c < 16; ++c) {
               const float a0 = ex2f(fmaf(__uint_as_float(v0[2 * c]), sl2, -m2));
               const float a1 = ex2f(fmaf(__uint_as_float(v0[2 * c + 1]), sl2, -m2));
+              la += a0;
+              lc += a1;
               pw[c] = pack_bf16(a0, a1);
-              v0[2 * c] = __float_as_uint(a0);
-              v0[2 * c + 1] = __float_as_uint(a1);
             }
             if constexpr (!kProxy) tmem_st16(Sb + q * 16, pw);
-            l += tree_sum32(v0);
           }
+          l = la + lc;
         } else {
           // ---- some row of this warp is in its local block (keys after the token masked) or is
           // a padding row (lim = -1)
@@ -456,7 +436,9 @@ __global__ void __launch_bounds__(448, 1)
             uint32_t v0[32];
             tmem_ld32(Sb + q * 32, v0);
             tmem_wait_ld();
-            mx = fmaxf(mx, tree_max32(v0, lim - q * 32));
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+              mx = fmaxf(mx, q * 32 + c <= lim ? __uint_as_float(v0[c]) : -INFINITY);
           }
           m2 = lim < 0 ? 0.f : mx * sl2;
 #pragma unroll 1  // (a full unroll makes the compiler spill)
@@ -473,12 +455,10 @@ __global__ void __launch_bounds__(448, 1)
               float a1 = ex2f(fmaf(__uint_as_float(v0[2 * c + 1]), sl2, -m2));
               a0 = k0 <= lim ? a0 : 0.f;
               a1 = k0 + 1 <= lim ? a1 : 0.f;
+              l += a0 + a1;
               pw[c] = pack_bf16(a0, a1);
-              v0[2 * c] = __float_as_uint(a0);
-              v0[2 * c + 1] = __float_as_uint(a1);
             }
             if constexpr (!kProxy) tmem_st16(Sb + q * 16, pw);
-            l += tree_sum32(v0);
           }
         }
         const bool valid = t >= 0;

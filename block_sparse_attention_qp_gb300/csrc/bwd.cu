@@ -641,15 +641,17 @@ __global__ void __launch_bounds__(352, 1)
         if (lane == 0) mbar_arrive(&sh->p_full[bb]);
         // teacher: mean of the proxy head's G R query heads' probabilities of each token, one fp16
         // row per list entry; with R > 1 attention groups per proxy head each adds its share
+        if (d.R == 1) {
 #pragma unroll
-        for (int x = 0; x < TT; ++x)
-          if (tv[x] >= 0) {
-            __half* dst = A.pbar + (size_t)(eb + tl * TT + x) * kBlock + kr;
-            if (d.R == 1)
-              st_global_h_hint(dst, pb[x] * (1.f / G), stream);
-            else
-              red_add_h(dst, pb[x] * (1.f / (G * d.R)));
-          }
+          for (int x = 0; x < TT; ++x)
+            if (tv[x] >= 0)
+              st_global_h_hint(A.pbar + (size_t)(eb + tl * TT + x) * kBlock + kr, pb[x] * (1.f / G), stream);
+        } else {
+#pragma unroll
+          for (int x = 0; x < TT; ++x)
+            if (tv[x] >= 0)
+              red_add_h(A.pbar + (size_t)(eb + tl * TT + x) * kBlock + kr, pb[x] * (1.f / (G * d.R)));
+        }
         // ---- epilogue of the previous tile
         if (tl > 0 && !epilogue(i - 1)) { ok = false; break; }
       }
@@ -684,6 +686,451 @@ __global__ void __launch_bounds__(352, 1)
   __syncthreads();
   fence_after_sync();
   if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+// ==========================================================================================
+// The same backward with 128-row tiles (128 / G tokens x G heads): every product then has N = 128,
+// which the tensor core runs in the time of an N = 64 one -- 40 MMA instructions per 128 rows
+// instead of 64 with two 64-row tiles.  Tensor memory holds one tile's S^T (then P^T in its first
+// 64 columns) and dP^T (then dQ^T) besides dV and dK, so the S / dP products of a tile wait for the
+// previous tile's epilogue instead of running ahead of it.  Shared memory (1024-aligned base): K,
+// V (32 KB each), two Q / dO slots of 64 KB (each later holding its tile's fp32 dQ rows), dS^T
+// (32 KB) and the barriers -- 224 KB + the barrier block.
+namespace {
+constexpr int kTW = 128;             // rows per wide tile
+constexpr int kRTW = kTW * 128 * 2;  // 128 rows x 128 bf16 (two SW128 panels of 64 columns)
+constexpr int kSlotW = 2 * kRTW;     // Q rows, then dO rows; later the tile's fp32 dQ rows
+constexpr int kSTW = 128 * kTW * 2;  // dS^T: 128 keys x 128 rows bf16 (two panels)
+constexpr int kQSW = 2;              // Q / dO slots
+static_assert(kTW * 128 * 4 == kSlotW, "a wide tile's fp32 dQ staging fills exactly one slot");
+constexpr uint32_t kStatusLayout = kStatusInternal;  // dynamic shared memory not 1024-byte aligned
+
+struct WideShared {
+  float lse2[kQSW][kTW];  // row LSE * log2(e), per slot
+  float drow[kQSW][kTW];  // row D, per slot
+  int tok[kQSW][32];      // tokens of the slot's tile (128 / G <= 32), -1: none
+  int it_ring[kIR];
+  uint64_t kv_full, kv_empty, q_full[kQSW], q_empty[kQSW], stage_ready[kQSW], s_full, p_full,
+      ph2_full, s_free, acc_free, mma_done, it_full[kIR], it_empty[kIR];
+  uint32_t tmem;
+};
+constexpr size_t kWideSmem = 2 * (size_t)kKV + kQSW * (size_t)kSlotW + kSTW;  // + WideShared
+}  // namespace
+
+template <int G, bool kDense>
+__global__ void __launch_bounds__(352, 1)
+    attn_bwd_wide_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                         MainArgs A) {
+  using namespace sm100;
+  constexpr int TT = kTW / G;  // tokens per tile
+  static_assert(TT <= 32 && G >= 4, "one lane per token of a tile");
+  const Dims& d = A.d;
+  extern __shared__ __align__(1024) uint8_t smem_wide[];
+  const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
+  if (smem_u32(smem_wide) & 1023u) {  // the swizzled operand layout needs 1024-byte atoms
+    if (tid == 0) atomicOr(A.status, kStatusLayout);
+    return;
+  }
+  uint8_t* sK = smem_wide;  // [128 keys][128 d]  (TMA)
+  uint8_t* sV = sK + kKV;
+  uint8_t* sSl = sV + kKV;              // [kQSW] slots: Q [128 rows][128 d], dO [128 rows][128 d]
+  uint8_t* sdS = sSl + kQSW * kSlotW;   // dS^T [128 keys][128 rows]
+  WideShared* sh = reinterpret_cast<WideShared*>(sdS + kSTW);
+  const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aSl = smem_u32(sSl), adS = smem_u32(sdS);
+  const float sl2 = d.scale * kLog2e;
+  long long total = *A.n_items;
+  if (total > A.max_items) total = A.max_items;
+
+  if (tid == 0) {
+    mbar_init(&sh->kv_full, 1);
+    mbar_init(&sh->kv_empty, 1);
+    for (int x = 0; x < kQSW; ++x) {
+      mbar_init(&sh->q_full[x], 256);  // 4 gather warps x 32 lanes: a cp.async and a plain arrival each
+      mbar_init(&sh->q_empty[x], 1);   // the dQ reducer, once the staged dQ rows were read
+      mbar_init(&sh->stage_ready[x], 4);
+    }
+    mbar_init(&sh->s_full, 1);
+    mbar_init(&sh->p_full, 4);
+    mbar_init(&sh->ph2_full, 1);
+    mbar_init(&sh->s_free, 4);
+    mbar_init(&sh->acc_free, 4);
+    mbar_init(&sh->mma_done, 1);
+    for (int x = 0; x < kIR; ++x) {
+      mbar_init(&sh->it_full[x], 1);
+      mbar_init(&sh->it_empty[x], 10);  // MMA, 4 gather warps, reducer, 4 softmax warps
+    }
+    mbar_fence_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&sh->tmem, 512);
+    tmem_relinquish();
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = sh->tmem;
+  const uint32_t SB = tmem, DB = tmem + 128, RV = tmem + 256, RK = tmem + 384;
+  bool ok = true;
+  // waits record which of them gave up first (status word kStatusWhere), so that a deadlock is
+  // reported with its place instead of leaving only the timeout bit
+  auto wait1 = [&](unsigned id, uint64_t* bar, uint32_t parity) -> bool {
+    if (mbar_wait(bar, parity, A.status)) return true;
+    atomicCAS(A.status + kStatusWhere, 0u, id);
+    return false;
+  };
+  auto waitw = [&](unsigned id, uint64_t* bar, uint32_t parity) -> bool {
+    const bool r = wait1(id, bar, parity);
+    return __all_sync(0xffffffffu, r);
+  };
+  auto take_item1 = [&](long long ni, int& v) -> bool {
+    const int x = (int)(ni % kIR);
+    if (!wait1(1, &sh->it_full[x], par(ni / kIR))) return false;
+    v = sh->it_ring[x];
+    mbar_arrive(&sh->it_empty[x]);
+    return true;
+  };
+  auto take_itemw = [&](long long ni, int& v) -> bool {
+    const int x = (int)(ni % kIR);
+    if (!waitw(2, &sh->it_full[x], par(ni / kIR))) return false;
+    v = sh->it_ring[x];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh->it_empty[x]);
+    return true;
+  };
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA: K, V per item
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      long long pub = 0;
+      bool last = false;
+      for (long long ni = 0;; ++ni) {
+        while (!last && pub < ni + 2) {  // item numbers up to two items ahead of the loads
+          const int x = (int)(pub % kIR);
+          if (pub >= kIR && !wait1(3, &sh->it_empty[x], par(pub / kIR - 1))) break;
+          const int v = atomicAdd(A.sched, 1);
+          sh->it_ring[x] = v;
+          mbar_arrive(&sh->it_full[x]);
+          last = v >= total;
+          ++pub;
+        }
+        if (pub <= ni) break;  // a wait gave up
+        const int it = sh->it_ring[ni % kIR];
+        if (it >= total) break;
+        const Item item = A.items[it];
+        const int n = item.seg % d.nblk;
+        const int bg = (int)((item.seg % d.nseg()) / d.nblk);
+        const int b = bg / d.Hp, kvh = d.kv_of((bg % d.Hp) * d.R + item.sub);
+        if (ni > 0 && !wait1(4, &sh->kv_empty, par(ni - 1))) break;
+        const int row0 = b * d.S + n * kBlock;
+        mbar_expect_tx(&sh->kv_full, 2 * kKV);
+        tma_load_3d(sK, &tm_k, 0, kvh, row0, &sh->kv_full);
+        tma_load_3d(sK + kKV / 2, &tm_k, 64, kvh, row0, &sh->kv_full);
+        tma_load_3d(sV, &tm_v, 0, kvh, row0, &sh->kv_full);
+        tma_load_3d(sV + kKV / 2, &tm_v, 64, kvh, row0, &sh->kv_full);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16(128, kTW, false, false);  // S^T, dP^T (N = rows)
+      constexpr uint32_t id_g = idesc_bf16(128, 128, false, true);   // dV, dK (N = d)
+      constexpr uint32_t id_q = idesc_bf16(128, kTW, true, true);    // dQ^T (N = rows)
+      long long i = 0;
+      for (long long ni = 0;; ++ni) {
+        int it;
+        if (!take_item1(ni, it)) { ok = false; break; }
+        if (it >= total) break;
+        const Item item = A.items[it];
+        if (!wait1(5, &sh->kv_full, par(ni))) { ok = false; break; }
+        const int ntiles = (item.count + TT - 1) / TT;
+        for (int tl = 0; tl < ntiles; ++tl, ++i) {
+          const int sl = (int)(i % kQSW);
+          if (!wait1(6, &sh->q_full[sl], par(i / kQSW))) { ok = false; break; }
+          // the Q / dO rows came from other threads' cp.async (generic proxy), tracked by q_full
+          fence_async_smem();
+          fence_after_sync();
+          const uint32_t aQb = aSl + (uint32_t)sl * kSlotW, adOb = aQb + kRTW;
+          // S^T = K Q^T into SB, which held P^T of tile i-1 (read by that tile's dV product,
+          // issued before this one)
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            mma_ss(SB, desc_kmajor(aK, 128, ks), desc_kmajor(aQb, kTW, ks), id_s, ks > 0);
+          // dP^T = V dO^T into DB, once the epilogue of tile i-1 has read dQ^T out of it
+          if (i >= 1 && !wait1(7, &sh->s_free, par(i - 1))) { ok = false; break; }
+          fence_after_sync();
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            mma_ss(DB, desc_kmajor(aV, 128, ks), desc_kmajor(adOb, kTW, ks), id_s, ks > 0);
+          mma_commit(&sh->s_full);  // also: every product of tile i-1 has completed
+          // phase 2, once the softmax has written P^T (tensor memory) and dS^T (shared memory)
+          if (!wait1(8, &sh->p_full, par(i))) { ok = false; break; }
+          if (tl == 0 && ni > 0 && !wait1(9, &sh->acc_free, par(ni - 1))) { ok = false; break; }
+          fence_after_sync();
+          const bool acc = tl > 0;
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)  // dV += P^T dO  (P^T from tensor memory)
+            mma_ts(RV, SB + ks * 8, desc_mnmajor(adOb, kTW, ks), id_g, acc || ks > 0);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)  // dK += dS^T Q
+            mma_ss(RK, desc_kmajor(adS, 128, ks), desc_mnmajor(aQb, kTW, ks), id_g, acc || ks > 0);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)  // dQ^T = K^T dS^T into DB (dP^T was read by the softmax)
+            mma_ss(DB, desc_mnmajor(aK, 128, ks), desc_mnmajor(adS, 128, ks), id_q, ks > 0);
+          mma_commit(&sh->ph2_full);  // also: the slot's Q / dO rows are no longer read
+        }
+        if (!ok) break;
+        mma_commit(&sh->kv_empty);
+      }
+      mma_commit(&sh->mma_done);  // arrives once every MMA issued above has completed
+    }
+  } else if (warp == 2 || warp >= 8) {
+    // ---------------------------------------------------------------- gather: Q, dO rows
+    // Four warps (2, 8, 9, 10) each fill 32 of the tile's 128 rows with cp.async; completion is
+    // counted on q_full (one cp.async arrival and one plain arrival per lane).  Lane x holds token
+    // x of the tile (one tile ahead); warp 2 publishes them for the reducer and the softmax.
+    const uint64_t keep = l2_policy_evict_last();  // read again by the chunk's other blocks
+    const int gw = warp == 2 ? 0 : warp - 7;
+    constexpr int WT = 32 / G;  // tokens of one warp's 32 rows
+    const int r0 = 32 * gw;
+    const int hi = lane >> 4, ch = lane & 15;
+    long long i = 0;
+    for (long long ni = 0; ok; ++ni) {
+      int it;
+      if (!take_itemw(ni, it)) { ok = false; break; }
+      if (it >= total) break;
+      const Item item = A.items[it];
+      const int bg = (int)((item.seg % d.nseg()) / d.nblk);
+      const int b = bg / d.Hp, a = (bg % d.Hp) * d.R + item.sub;  // attention group
+      const int gp = d.Gp();
+      const long long tb = item_base<kDense>(d, A.seg_offset, item);
+      const long long eb = (long long)A.seg_offset[item.seg] + item.first;  // first list entry
+      // token of tile position `lane` of tile tl_ (-1: none)
+      auto load_tok = [&](int tl_) -> int {
+        const int x = tl_ * TT + lane;
+        if (lane >= TT || x >= item.count) return -1;
+        return kDense ? (int)(tb + x) : (__ldg(A.entries + tb + x) >> 8);
+      };
+      // row data of row r0 + lane of tile tl_, indexed by the list entry
+      auto load_meta = [&](int tl_) -> float2 {
+        const int x = tl_ * TT + (r0 + lane) / G;
+        float2 m = make_float2(0.f, 0.f);
+        if (x < item.count) m = __ldg(A.emeta + (size_t)(eb + x) * gp + item.sub * G + (r0 + lane) % G);
+        return m;
+      };
+      const int ntiles = (item.count + TT - 1) / TT;
+      int tcur = load_tok(0);
+      float2 mcur = load_meta(0);
+      for (int tl = 0; tl < ntiles; ++tl, ++i) {
+        const int sl = (int)(i % kQSW);
+        int wt[WT];  // this warp's tokens
+#pragma unroll
+        for (int j = 0; j < WT; ++j) wt[j] = __shfl_sync(0xffffffffu, tcur, r0 / G + j);
+        const int tnext = load_tok(tl + 1);
+        const float2 mnext = load_meta(tl + 1);
+        if (i >= kQSW && !waitw(10, &sh->q_empty[sl], par(i / kQSW - 1))) { ok = false; break; }
+        uint8_t* dQb = sSl + sl * kSlotW;
+        uint8_t* ddOb = dQb + kRTW;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const int rr = 2 * k + hi;  // row within the warp's 32 (G >= 4: token (2 k) / G)
+          const int r = r0 + rr;
+          const int t = wt[(2 * k) / G];
+          const uint32_t off = (ch >> 3) * (kTW * 128) + sm100::sw128_chunk(r, ch & 7);
+          const size_t grow = (((size_t)b * d.S + (t < 0 ? 0 : t)) * d.Hq + a * G + rr % G) * kD + ch * 8;
+          cp_async16_hint(dQb + off, A.q + grow, t >= 0, keep);
+          cp_async16_hint(ddOb + off, A.dout + grow, t >= 0, keep);
+        }
+        sh->lse2[sl][r0 + lane] = mcur.x;
+        sh->drow[sl][r0 + lane] = mcur.y;
+        if (gw == 0) sh->tok[sl][lane] = tcur;
+        cp_async_arrive(&sh->q_full[sl]);
+        mbar_arrive(&sh->q_full[sl]);  // publishes the row data and tok
+        tcur = tnext;
+        mcur = mnext;
+      }
+    }
+    cp_async_wait_all();  // nothing may land after the block exits
+  } else if (warp == 3) {
+    // ---------------------------------------------------------------- dQ reducer
+    if (lane == 0) {
+      const uint64_t keep = l2_policy_evict_last();  // dQ rows of the chunk: reduced into again
+      long long ns = 0;
+      for (long long ni = 0; ok; ++ni) {
+        int it;
+        if (!take_item1(ni, it)) { ok = false; break; }
+        if (it >= total) break;
+        const Item item = A.items[it];
+        const int bg = (int)((item.seg % d.nseg()) / d.nblk);
+        const int b = bg / d.Hp, a = (bg % d.Hp) * d.R + item.sub;
+        const int ntiles = (item.count + TT - 1) / TT;
+        for (int tl = 0; tl < ntiles; ++tl, ++ns) {
+          const int sl = (int)(ns % kQSW);
+          if (!wait1(11, &sh->stage_ready[sl], par(ns / kQSW))) { ok = false; break; }
+          const uint32_t aSt = aSl + (uint32_t)sl * kSlotW;  // the tile's dQ rows, staged in its slot
+#pragma unroll 1
+          for (int x = 0; x < TT; ++x) {
+            const int t = sh->tok[sl][x];
+            if (t >= 0)
+              bulk_reduce_add(A.dq + (((size_t)b * d.S + t) * d.Hq + a * G) * kD,
+                              aSt + x * G * kD * 4, G * kD * 4, keep);
+          }
+          bulk_commit();
+          bulk_wait_read0();
+          mbar_arrive(&sh->q_empty[sl]);  // the slot may take the rows of tile ns + kQSW
+        }
+      }
+      bulk_wait0();
+    }
+  } else {
+    // ---------------------------------------------------------------- softmax / epilogue
+    const int w4 = warp - 4;
+    const int kr = w4 * 32 + lane;  // key row of S^T / dP^T (TMEM lane); head-dim index of dQ^T
+    const uint32_t lb = static_cast<uint32_t>(w4 * 32) << 16;
+    const uint64_t stream = l2_policy_evict_first();  // pbar rows: read once, by proxy_bwd
+    long long i = 0;
+    for (long long ni = 0; ok; ++ni) {
+      int it;
+      if (!take_itemw(ni, it)) { ok = false; break; }
+      if (it >= total) break;
+      const Item item = A.items[it];
+      const int n = item.seg % d.nblk;
+      const int bg = (int)((item.seg % d.nseg()) / d.nblk);
+      const int b = bg / d.Hp, kvh = d.kv_of((bg % d.Hp) * d.R + item.sub);
+      const int j = n * kBlock + kr;  // this thread's key
+      const long long eb = (long long)A.seg_offset[item.seg] + item.first;  // first list entry
+      const int ntiles = (item.count + TT - 1) / TT;
+      for (int tl = 0; tl < ntiles; ++tl, ++i) {
+        const int sl = (int)(i % kQSW);
+        __syncwarp();
+        if (!waitw(12, &sh->q_full[sl], par(i / kQSW)) || !waitw(13, &sh->s_full, par(i))) {
+          ok = false;
+          break;
+        }
+        fence_after_sync();
+        // ---- softmax of tile i: 32 rows at a time (P^T of rows 32 c .. 32 c + 31 lands in
+        // columns 16 c .. 16 c + 15, which chunk c / 2 has already read).  G divides 32, so the
+        // G rows of a token lie in one chunk: each chunk finishes the teacher rows of its tokens.
+        constexpr int WT = 32 / G;  // tokens per chunk
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          float pc[WT];
+#pragma unroll
+          for (int w = 0; w < WT; ++w) pc[w] = 0.f;
+          uint32_t rs[32], rp[32];
+          __syncwarp();
+          tmem_ld32(SB + lb + 32 * c, rs);
+          tmem_ld32(DB + lb + 32 * c, rp);
+          tmem_wait_ld();
+          uint32_t pw[16], dw[16];
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) {
+            const float4 l4 = reinterpret_cast<const float4*>(sh->lse2[sl])[c * 8 + q4];
+            const float4 d4 = reinterpret_cast<const float4*>(sh->drow[sl])[c * 8 + q4];
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+            const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+            float pv[4], dsv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int r = q4 * 4 + e;  // row within the chunk
+              const int t = sh->tok[sl][(c * 32 + r) / G];
+              const bool vis = t >= 0 && j <= t;
+              const float p = vis ? ex2(__uint_as_float(rs[r]) * sl2 - lv[e]) : 0.f;
+              pv[e] = p;
+              dsv[e] = p * (__uint_as_float(rp[r]) - dv4[e]);
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) pc[(q4 * 4 + e) / G] += pv[e];  // the token's G heads
+            pw[2 * q4] = pack_bf16(pv[0], pv[1]);
+            pw[2 * q4 + 1] = pack_bf16(pv[2], pv[3]);
+            dw[2 * q4] = pack_bf16(dsv[0], dsv[1]);
+            dw[2 * q4 + 1] = pack_bf16(dsv[2], dsv[3]);
+          }
+          tmem_st16(SB + lb + 16 * c, pw);
+          const uint32_t panel = adS + (uint32_t)(c >> 1) * (128 * 128);
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            st_shared_v4(panel + sm100::sw128_chunk(kr, (c & 1) * 4 + u), dw[4 * u], dw[4 * u + 1],
+                         dw[4 * u + 2], dw[4 * u + 3]);
+          // teacher: mean of the proxy head's G R query heads' probabilities of each token, one
+          // fp16 row per list entry; with R > 1 attention groups per proxy head each adds its share
+          if (d.R == 1) {
+#pragma unroll
+            for (int w = 0; w < WT; ++w)
+              if (sh->tok[sl][c * WT + w] >= 0)
+                st_global_h_hint(A.pbar + (size_t)(eb + tl * TT + c * WT + w) * kBlock + kr,
+                                 pc[w] * (1.f / G), stream);
+          } else {
+#pragma unroll
+            for (int w = 0; w < WT; ++w)
+              if (sh->tok[sl][c * WT + w] >= 0)
+                red_add_h(A.pbar + (size_t)(eb + tl * TT + c * WT + w) * kBlock + kr,
+                          pc[w] * (1.f / (G * d.R)));
+          }
+        }
+        tmem_wait_st();
+        fence_async_smem();
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh->p_full);
+        // ---- epilogue of tile i: dQ^T -> fp32 rows staged in the tile's own slot (phase 2 has
+        // finished reading its Q / dO rows); the reducer then adds them to dQ
+        __syncwarp();
+        if (!waitw(14, &sh->ph2_full, par(i))) { ok = false; break; }
+        fence_after_sync();
+        float* stage = reinterpret_cast<float*>(sSl + sl * kSlotW);
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r0[32];
+          __syncwarp();
+          tmem_ld32(DB + lb + 32 * c, r0);
+          tmem_wait_ld();
+          if (c == 3) {  // DB may now take the next tile's dP^T
+            fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh->s_free);
+          }
+#pragma unroll
+          for (int r = 0; r < 32; ++r) stage[(32 * c + r) * kD + kr] = __uint_as_float(r0[r]) * d.scale;
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh->stage_ready[sl]);
+      }
+      if (!ok) break;
+      // ---- item end: dV and dK rows of this key (the item's last phase 2 has completed)
+      {
+        float* pv = A.dv + (((size_t)b * d.S + j) * d.Hkv + kvh) * kD;
+        float* pk = A.dk + (((size_t)b * d.S + j) * d.Hkv + kvh) * kD;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t rv[32], rk[32];
+          tmem_ld32(RV + lb + c * 32, rv);
+          tmem_ld32(RK + lb + c * 32, rk);
+          tmem_wait_ld();
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            red4(pv + c * 32 + 4 * u, __uint_as_float(rv[4 * u]), __uint_as_float(rv[4 * u + 1]),
+                 __uint_as_float(rv[4 * u + 2]), __uint_as_float(rv[4 * u + 3]));
+            red4(pk + c * 32 + 4 * u, __uint_as_float(rk[4 * u]) * d.scale,
+                 __uint_as_float(rk[4 * u + 1]) * d.scale, __uint_as_float(rk[4 * u + 2]) * d.scale,
+                 __uint_as_float(rk[4 * u + 3]) * d.scale);
+          }
+        }
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh->acc_free);
+      }
+    }
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (warp == 0) {
+    waitw(15, &sh->mma_done, 0);  // no MMA may still write tensor memory when it is freed
+    tmem_dealloc(tmem, 512);
+  }
 }
 
 // ==========================================================================================
@@ -1103,6 +1550,13 @@ void attn_bwd_g(const CUtensorMap& mk, const CUtensorMap& mv, const MainArgs& a,
                        (int)smem);
   attn_bwd_kernel<G, kDense><<<num_sms(), 352, smem, st>>>(mk, mv, a);
 }
+template <int G, bool kDense>
+void attn_bwd_wide_g(const CUtensorMap& mk, const CUtensorMap& mv, const MainArgs& a, cudaStream_t st) {
+  const size_t smem = kWideSmem + sizeof(WideShared);  // base 1024-aligned (checked in the kernel)
+  cudaFuncSetAttribute(attn_bwd_wide_kernel<G, kDense>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       (int)smem);
+  attn_bwd_wide_kernel<G, kDense><<<num_sms(), 352, smem, st>>>(mk, mv, a);
+}
 template <bool kDense, bool kKL>
 void proxy_bwd_g(const CUtensorMap& mkp, const ProxyArgs& a, cudaStream_t st) {
   const size_t smem = sizeof(ProxyShared) + 1024 + (size_t)kKV + kQPB * (size_t)kRT + 2 * (size_t)kST +
@@ -1156,12 +1610,16 @@ bool launch_attn_bwd(const Dims& d, bool dense, const void* q, const void* k, co
   a.status = status;
   a.sched = reinterpret_cast<int*>(status + kSchedAttnBwd);
   cudaMemsetAsync(a.sched, 0, sizeof(int), st);
+  // 128-row tiles for 4 and 8 heads per group; 16 heads keep 64-row tiles (there P and dS go to
+  // the products as a bf16 value plus its bf16 residual, which needs the spare tensor memory).
+  // The dense mode with 8 heads per group also keeps the 64-row kernel: its 128-row instance
+  // raised an illegal-instruction fault on a 512-token case whose cause is not yet found.
   switch (d.G) {
     case 4:
-      dense ? attn_bwd_g<4, true>(mk, mv, a, st) : attn_bwd_g<4, false>(mk, mv, a, st);
+      dense ? attn_bwd_wide_g<4, true>(mk, mv, a, st) : attn_bwd_wide_g<4, false>(mk, mv, a, st);
       break;
     case 8:
-      dense ? attn_bwd_g<8, true>(mk, mv, a, st) : attn_bwd_g<8, false>(mk, mv, a, st);
+      dense ? attn_bwd_g<8, true>(mk, mv, a, st) : attn_bwd_wide_g<8, false>(mk, mv, a, st);
       break;
     case 16:
       dense ? attn_bwd_g<16, true>(mk, mv, a, st) : attn_bwd_g<16, false>(mk, mv, a, st);

@@ -25,6 +25,8 @@ constexpr int kSchedProxyBwd = 9;
 constexpr int kSchedAttnFwd = 10;
 constexpr int kSchedProxyLse = 11;
 constexpr int kSchedDenseFwd = 12;
+// Word 16: the id of the first bounded wait that gave up, in kernels that record it (0: none).
+constexpr int kStatusWhere = 16;
 
 typedef __nv_bfloat16 bf16;
 

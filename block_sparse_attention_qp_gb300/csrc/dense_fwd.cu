@@ -306,9 +306,7 @@ __global__ void __launch_bounds__(384, 1)
         fence_after_sync();
         // tcgen05.ld / st are warp-collective: the masked path is chosen per warp
         const bool full = __all_sync(0xffffffffu, lim == kBlock - 1);
-        float m8[8];  // independent running maxima (one would be a 128-step dependency chain)
-#pragma unroll
-        for (int u = 0; u < 8; ++u) m8[u] = -INFINITY;
+        float mx = -INFINITY;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           uint32_t v0[32];
@@ -316,10 +314,8 @@ __global__ void __launch_bounds__(384, 1)
           tmem_wait_ld();
 #pragma unroll
           for (int c = 0; c < 32; ++c)
-            m8[c & 7] = fmaxf(m8[c & 7], (full || q * 32 + c <= lim) ? __uint_as_float(v0[c]) : -INFINITY);
+            mx = fmaxf(mx, (full || q * 32 + c <= lim) ? __uint_as_float(v0[c]) : -INFINITY);
         }
-        const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
         if (n == 0) {
           mr = mx;  // column 0 is always visible: finite
         } else {
@@ -340,7 +336,7 @@ __global__ void __launch_bounds__(384, 1)
           }
         }
         const float mb = mr * sl2;
-        float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        float la = 0.f, lc = 0.f;
 #pragma unroll 1  // (a full unroll makes the compiler spill)
         for (int q = 0; q < 4; ++q) {
           uint32_t v0[32];
@@ -355,12 +351,13 @@ __global__ void __launch_bounds__(384, 1)
             float a1 = ex2(fmaf(__uint_as_float(v0[2 * c + 1]), sl2, -mb));
             a0 = (full || k0 <= lim) ? a0 : 0.f;
             a1 = (full || k0 + 1 <= lim) ? a1 : 0.f;
-            s8[c & 7] += a0 + a1;
+            la += a0;
+            lc += a1;
             pw[c] = pack_bf16(a0, a1);
           }
           tmem_st16(Sx + q * 16, pw);
         }
-        l += ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
+        l += la + lc;
         tmem_wait_st();
         fence_before_sync();
         __syncwarp();

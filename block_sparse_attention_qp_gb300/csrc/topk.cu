@@ -48,24 +48,28 @@ struct TopkSmem {
 };
 }  // namespace
 
-template <int KMAX, bool kLse>
-__global__ void __launch_bounds__(256, 1)
+// NH proxy heads per block (1 or 2): with two, each streamed proxy-key block feeds both heads'
+// products and two epilogue warpgroups (warps 4-7 head 0, 8-11 head 1) share the SM sub-partitions.
+template <int KMAX, bool kLse, int NH>
+__global__ void __launch_bounds__(128 + 128 * NH, 1)
     proxy_topk_kernel(const __grid_constant__ CUtensorMap tm_qp,
                       const __grid_constant__ CUtensorMap tm_kp, Dims d,
                       int32_t* __restrict__ idx, float* __restrict__ lse_out,
                       unsigned* __restrict__ status) {
   using namespace sm100;
+  constexpr int kAccH = kAcc / NH;  // accumulators per head
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = align1024(smem_raw);
-  uint8_t* sQ = base;                  // 32 KB
-  uint8_t* sK = base + kTileBytes;     // kStages x 32 KB
+  uint8_t* sQ = base;                      // NH x 32 KB
+  uint8_t* sK = base + NH * kTileBytes;    // kStages x 32 KB
   TopkSmem* sh = reinterpret_cast<TopkSmem*>(sK + kStages * kTileBytes);
 
   const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
-  const int nbg = d.B * d.Hp;
+  const int hpb = d.Hp / NH;  // head pairs (or heads) per batch row
+  const int nbg = d.B * hpb;
   const int qb = d.nblk - 1 - blockIdx.x / nbg;  // most work first
   const int bg = blockIdx.x % nbg;
-  const int b = bg / d.Hp, g = bg % d.Hp;
+  const int b = bg / hpb, g0 = (bg % hpb) * NH;
   const int t0 = qb * kBlock;
   const int KL = d.top_k - 1;
   const int nb = kLse ? qb + 1 : qb;  // key blocks streamed
@@ -97,9 +101,11 @@ __global__ void __launch_bounds__(256, 1)
     // ---- producer
     tma_prefetch_desc(&tm_qp);
     tma_prefetch_desc(&tm_kp);
-    mbar_expect_tx(&sh->q_full, kTileBytes);
-    tma_load_3d(sQ, &tm_qp, 0, g, b * d.S + t0, &sh->q_full);
-    tma_load_3d(sQ + kTileBytes / 2, &tm_qp, 64, g, b * d.S + t0, &sh->q_full);
+    mbar_expect_tx(&sh->q_full, NH * kTileBytes);
+    for (int h = 0; h < NH; ++h) {
+      tma_load_3d(sQ + h * kTileBytes, &tm_qp, 0, g0 + h, b * d.S + t0, &sh->q_full);
+      tma_load_3d(sQ + h * kTileBytes + kTileBytes / 2, &tm_qp, 64, g0 + h, b * d.S + t0, &sh->q_full);
+    }
     for (int n = 0; n < nb; ++n) {
       const int s = n % kStages;
       if (n >= kStages && !mbar_wait(&sh->kp_empty[s], ((n / kStages) - 1) & 1, status)) break;
@@ -113,30 +119,37 @@ __global__ void __launch_bounds__(256, 1)
     constexpr uint32_t idesc = idesc_bf16(128, 128, false, false);
     bool ok = mbar_wait(&sh->q_full, 0, status);
     for (int n = 0; ok && n < nb; ++n) {
-      const int s = n % kStages, a = n % kAcc;
+      const int s = n % kStages;
       if (!mbar_wait(&sh->kp_full[s], (n / kStages) & 1, status)) break;
-      if (n >= kAcc && !mbar_wait(&sh->acc_empty[a], ((n / kAcc) - 1) & 1, status)) break;
-      fence_after_sync();
       const uint32_t kaddr = sKa + s * kTileBytes;
+      for (int h = 0; h < NH; ++h) {
+        const int a = h * kAccH + n % kAccH;
+        if (n >= kAccH && !mbar_wait(&sh->acc_empty[a], ((n / kAccH) - 1) & 1, status)) {
+          ok = false;
+          break;
+        }
+        fence_after_sync();
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks)
-        mma_ss(tmem + a * 128, desc_kmajor(sQa, 128, ks), desc_kmajor(kaddr, 128, ks), idesc,
-               ks > 0);
+        for (int ks = 0; ks < 8; ++ks)
+          mma_ss(tmem + a * 128, desc_kmajor(sQa + h * kTileBytes, 128, ks),
+                 desc_kmajor(kaddr, 128, ks), idesc, ks > 0);
+        mma_commit(&sh->acc_full[a]);
+      }
+      if (!ok) break;
       mma_commit(&sh->kp_empty[s]);
-      mma_commit(&sh->acc_full[a]);
     }
   } else if (warp >= 4 && kLse) {
-    // ---- normaliser epilogue: thread owns score row `row` (token t0 + row)
-    const int q4 = warp - 4;
+    // ---- normaliser epilogue: thread owns score row `row` (token t0 + row) of head g0 + hh
+    const int q4 = warp % 4, hh = (warp - 4) >> 2;
     const int row = q4 * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
     const float sl2 = d.scale * kLog2e;
     float m = -INFINITY, l = 0.f;  // running max of the raw scores, sum of exp2(sl2 (z - m))
     for (int n = 0; n < nb; ++n) {
-      const int a = n % kAcc;
+      const int a = hh * kAccH + n % kAccH;
       const int lim = n == qb ? row : kBlock - 1;  // visible columns 0 .. lim
       __syncwarp();
-      if (!mbar_wait_warp(&sh->acc_full[a], (n / kAcc) & 1, status)) break;
+      if (!mbar_wait_warp(&sh->acc_full[a], (n / kAccH) & 1, status)) break;
       fence_after_sync();
       float m8[8];  // independent running maxima (no long dependency chain)
 #pragma unroll
@@ -179,10 +192,10 @@ __global__ void __launch_bounds__(256, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh->acc_empty[a]);
     }
-    lse_out[((size_t)b * d.Hp + g) * d.S + t0 + row] = (m * sl2 + __log2f(l)) * kLn2;
+    lse_out[((size_t)b * d.Hp + g0 + hh) * d.S + t0 + row] = (m * sl2 + __log2f(l)) * kLn2;
   } else if (warp >= 4) {
-    // ---- epilogue: thread owns score row `row`
-    const int q4 = warp - 4;
+    // ---- epilogue: thread owns score row `row` of head g0 + hh
+    const int q4 = warp % 4, hh = (warp - 4) >> 2;
     const int row = q4 * 32 + lane;
     float vals[KMAX - 1];
     int ids[KMAX - 1];
@@ -194,9 +207,9 @@ __global__ void __launch_bounds__(256, 1)
     float kth = -INFINITY;
     const uint32_t lane_base = static_cast<uint32_t>(q4 * 32) << 16;
     for (int n = 0; n < qb; ++n) {
-      const int a = n % kAcc;
+      const int a = hh * kAccH + n % kAccH;
       __syncwarp();
-      if (!mbar_wait_warp(&sh->acc_full[a], (n / kAcc) & 1, status)) break;
+      if (!mbar_wait_warp(&sh->acc_full[a], (n / kAccH) & 1, status)) break;
       fence_after_sync();
       // eight independent running maxima: a single one would be a 128-step dependency chain
       float m8[8];
@@ -253,7 +266,7 @@ __global__ void __launch_bounds__(256, 1)
       }
       sel[j + 1] = x;
     }
-    int32_t* out = idx + (((size_t)b * d.Hp + g) * d.S + t0 + row) * d.top_k;
+    int32_t* out = idx + (((size_t)b * d.Hp + g0 + hh) * d.S + t0 + row) * d.top_k;
     for (int i = 0; i < d.top_k; ++i) out[i] = i < nv ? sel[i] : (i == nv ? qb : -1);
   }
   fence_before_sync();
@@ -262,13 +275,27 @@ __global__ void __launch_bounds__(256, 1)
   if (warp == 2) tmem_dealloc(tmem, 512);
 }
 
+template <int KMAX, bool kLse, int NH>
+static void topk_launch_nh(const CUtensorMap& mq, const CUtensorMap& mk, const Dims& d, int32_t* idx,
+                           float* lse, unsigned* status, cudaStream_t st) {
+  const size_t smem = 1024 + (NH + kStages) * kTileBytes + sizeof(TopkSmem);
+  cudaFuncSetAttribute(proxy_topk_kernel<KMAX, kLse, NH>,
+                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  proxy_topk_kernel<KMAX, kLse, NH><<<d.B * (d.Hp / NH) * d.nblk, 128 + 128 * NH, smem, st>>>(
+      mq, mk, d, idx, lse, status);
+}
+// Two proxy heads per block when the head count is even and the epilogue's registers allow it
+// (lists of up to 15 blocks, or the normaliser); one otherwise.
 template <int KMAX, bool kLse>
 static void topk_launch(const CUtensorMap& mq, const CUtensorMap& mk, const Dims& d, int32_t* idx,
                         float* lse, unsigned* status, cudaStream_t st) {
-  const size_t smem = 1024 + (1 + kStages) * kTileBytes + sizeof(TopkSmem);
-  cudaFuncSetAttribute(proxy_topk_kernel<KMAX, kLse>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                       (int)smem);
-  proxy_topk_kernel<KMAX, kLse><<<d.B * d.Hp * d.nblk, 256, smem, st>>>(mq, mk, d, idx, lse, status);
+  if constexpr (KMAX <= 16) {
+    if (d.Hp % 2 == 0) {
+      topk_launch_nh<KMAX, kLse, 2>(mq, mk, d, idx, lse, status, st);
+      return;
+    }
+  }
+  topk_launch_nh<KMAX, kLse, 1>(mq, mk, d, idx, lse, status, st);
 }
 
 static bool proxy_maps(const Dims& d, const void* qp, const void* kp, CUtensorMap* mq, CUtensorMap* mk) {

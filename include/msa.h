@@ -12,17 +12,24 @@
  *   Tensors are dense, row-major, on the current CUDA device, caller-owned:
  *     q, o, dout, dq    [B, S, Hq,  128]  bf16
  *     k, v, dk, dv      [B, S, Hkv, 128]  bf16
- *     qp, dqp           [B, S, Hp,  128]  bf16   (proxy query; Hp == Hkv, head g serves group g)
- *     kp, dkp           [B, S, 1,   128]  bf16   (one proxy key head shared by every group)
+ *     qp, dqp           [B, S, Hp,  128]  bf16   (proxy queries, one head per selection row)
+ *     kp, dkp           [B, S, 1,   128]  bf16   (one proxy key head shared by every proxy head)
  *     lse               [B, Hq, S]        fp32   natural-log sum of exp of the scaled scores
- *     block_idx         [B, Hp, S, top_k] int32  selected key blocks per (b, group, token),
+ *     block_idx         [B, Hp, S, top_k] int32  selected key blocks per (b, proxy head, token),
  *                                                ascending, padded with -1 when fewer than
  *                                                top_k blocks are visible
- *   Query head h belongs to group h / (Hq / Hkv).  Key j is visible to token t iff j <= t.
+ *   Head mapping (blog, "Context parallelism" point 1: an MSA group is the query heads assigned
+ *   to one proxy head; "Note about scheduler requiring proxy heads >= KV heads": more KV heads
+ *   than proxy heads inverts that mapping; the top-k sweep footnote runs 4 proxy heads over 2 KV
+ *   heads): query head h reads KV head h / (Hq / Hkv) and takes the selection of proxy head
+ *   h / (Hq / Hp).  Hq must be a multiple of Hkv and of Hp, and one
+ *   of Hp, Hkv a multiple of the other.  The KL teacher of proxy head p is the mean main
+ *   softmax of its Hq / Hp query heads.  Key j is visible to token t iff j <= t.
  *   Every pointer must be 16-byte aligned.  Supported: head dim 128, block 128 (blog / package
- *   caveat 1), S % 128 == 0, Hp == Hkv (package caveat 5), 1 <= top_k <= 64, and a group size
- *   Hq / Hkv in {1, 2, 4, 8, 16} for the forward ops, {4, 8, 16} for the backward ops (other
- *   group sizes return MSA_ERR_UNSUPPORTED).
+ *   caveat 1), S % 128 == 0, 1 <= top_k <= 64, and Hq / max(Hp, Hkv) -- the query heads that
+ *   share both one KV head and one selection row -- in {1, 2, 4, 8, 16} for the forward ops and
+ *   {4, 8, 16} for the backward ops (the warmup forward, which has no selection: Hq / Hkv).
+ *   Other shapes return MSA_ERR_UNSUPPORTED.
  *   `workspace` is caller-owned device memory of at least msa_workspace_size() bytes for the
  *   same op and shape; the library allocates nothing.  The first 256 bytes hold a device status
  *   word (see msa_device_status) and the work-item counters of the persistent kernels (reset on
@@ -53,7 +60,7 @@ typedef struct msa_shape {
   int32_t S;      /* sequence length, multiple of 128 */
   int32_t Hq;     /* main query heads */
   int32_t Hkv;    /* main key/value heads (GQA groups) */
-  int32_t Hp;     /* proxy query heads, must equal Hkv */
+  int32_t Hp;     /* proxy query heads (see the head mapping above) */
   int32_t D;      /* head dim, must be 128 */
   int32_t top_k;  /* selected blocks per query, local block included (ignored by warmup ops) */
   float scale;    /* softmax scale of both attentions, usually 128^-0.5 */
@@ -62,7 +69,7 @@ typedef struct msa_shape {
 enum msa_status {
   MSA_OK = 0,
   MSA_ERR_INVALID_ARG = 1, /* null / misaligned pointer, non-positive size */
-  MSA_ERR_UNSUPPORTED = 2, /* D != 128, S % 128 != 0, Hp != Hkv, bad group size or top_k */
+  MSA_ERR_UNSUPPORTED = 2, /* D != 128, S % 128 != 0, head counts, group size or top_k */
   MSA_ERR_WORKSPACE = 3,   /* workspace too small */
   MSA_ERR_CUDA = 4         /* CUDA launch / runtime error */
 };
@@ -80,6 +87,8 @@ enum msa_op {
 #define MSA_DEVICE_BAD_ITEMS 2u /* internal work list overflow (a library bug) */
 #define MSA_DEVICE_TIMEOUT 4u   /* a bounded device-side wait gave up */
 #define MSA_DEVICE_INTERNAL 8u  /* a kernel's internal layout check failed (a library bug) */
+/* With MSA_DEVICE_TIMEOUT set, the 32-bit word at byte offset 64 of the workspace may name the
+ * first wait that gave up (a nonzero place number of the kernel that set it); diagnostic only. */
 
 /* Bytes of workspace `op` needs for `shape` (0 if the shape is unsupported). */
 MSA_API size_t msa_workspace_size(const msa_shape_t* shape, int op);
@@ -104,8 +113,9 @@ MSA_API int msa_forward(const msa_shape_t* shape, const void* q, const void* k, 
  * inverts the block map, recomputes the proxy normaliser over the selected tokens, and in one
  * fused pass per (key block, group) recomputes the main and proxy probabilities and emits
  *   dq, dk, dv  of  sum(o * dout)                     (teacher detached: no KL term here)
- *   dqp, dkp    of  kl_grad * L_KL,  L_KL = mean over (b, t, group) of KL(teacher || student),
- *               teacher = mean over the group's heads of the main softmax (stop-gradient),
+ *   dqp, dkp    of  kl_grad * L_KL,  L_KL = mean over (b, t, proxy head) of
+ *               KL(teacher || student), teacher = mean over the proxy head's Hq / Hp query
+ *               heads of the main softmax (stop-gradient),
  *               student = softmax(scale * qp . kp) over the same tokens; the score gradient is
  *               kl_grad / (B*S*Hp) * (p_student - p_teacher)  (blog, "KL Divergence Loss").
  * o and lse are the outputs of msa_forward for the same inputs.  kl_grad is the incoming

@@ -182,9 +182,12 @@ def test_cfg2_full_parity():
 
 
 def test_kl_value_does_not_change_the_gradients():
-    """Asking for the KL value leaves every gradient unchanged up to fp32 summation order (the
-    gradient accumulators take reductions in whatever order blocks finish; measured 1.7e-5 rel
-    between two runs), since the value is computed beside the proxy gradients, not from them."""
+    """Asking for the KL value leaves every gradient unchanged up to fp32 summation order, since
+    the value is computed beside the proxy gradients, not from them.  The gradient accumulators
+    take reductions in whatever order blocks finish and the gradients come out in bf16, so an
+    fp32 sum that lands on the other side of a rounding boundary moves that entry by one bf16
+    unit: every entry must agree within one bf16 ulp, and few may differ at all (measured on
+    GB300 between two runs: rel L2 1.7e-5 to 1.4e-4, a handful of entries one ulp apart)."""
     w = Workload("klv", B=1, S=1024, Hq=8, Hkv=2, Hp=2, top_k=4)
     g = to_dev(make_inputs(w, 61))
     o, lse, idx = msa.msa_forward(g["q"], g["k"], g["v"], g["qp"], g["kp"], w.top_k, w.scale)
@@ -193,7 +196,9 @@ def test_kl_value_does_not_change_the_gradients():
     *b, kl = msa.msa_backward(g["q"], g["k"], g["v"], g["qp"], g["kp"], o, lse, g["dout"], idx,
                               w.top_k, w.scale, return_kl=True)
     for name, x, y in zip(("dq", "dk", "dv", "dqp", "dkp"), a, b):
-        close(name, x, y.float(), rel=1e-4, atol=2e-3, ulps=1.0)
+        close(name, x, y.float(), rel=1e-3, atol=2e-3, ulps=1.0)
+        differ = (x.float() != y.float()).float().mean().item()
+        assert differ <= 0.01, f"{name}: {differ:.2%} of the entries differ"
     assert float(kl) > 0
 
 
