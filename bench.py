@@ -76,12 +76,27 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
 
+    def _query(self, loop_ms=None):
+        cmd = ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+               "--format=csv,noheader,nounits"]
+        return cmd + (["-lms", str(loop_ms)] if loop_ms else [])
+
+    @staticmethod
+    def _parse(text):
+        rows = []
+        for line in text.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        return rows
+
     def __enter__(self):
+        self.when = "during the timed region"
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "50"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.proc = subprocess.Popen(self._query(50), stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            # the sampler is live once its first line is out (that line predates the region)
+            self.proc.stdout.readline()
         except OSError:
             self.proc = None
         return self
@@ -96,10 +111,14 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        for line in out.splitlines():
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) >= 9:
-                self.samples.append(parts)
+        self.samples = self._parse(out)
+        if not self.samples:  # region shorter than one sampling interval: read once right after
+            try:
+                one = subprocess.run(self._query(), capture_output=True, text=True, timeout=10)
+                self.samples = self._parse(one.stdout)
+                self.when = "right after the timed region (shorter than one 50 ms sample)"
+            except (OSError, subprocess.TimeoutExpired):
+                pass
         return False
 
     def summary(self):
@@ -113,7 +132,8 @@ class ClockSampler:
         pw = [float(s[3]) for s in self.samples if s[3].replace(".", "").isdigit()]
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "power_w_max": max(pw) if pw else None, "samples": len(self.samples)}
+                "power_w_max": max(pw) if pw else None, "samples": len(self.samples),
+                "sampled": self.when}
 
 
 # ------------------------------------------------------------------------------ oracle sample

@@ -133,6 +133,7 @@ __global__ void __launch_bounds__(448, 1)
     mbar_fence_init();
   }
   if (warp == 0) {
+    __syncwarp();  // lane 0 initialised the barriers alone; the allocation is warp-collective
     tmem_alloc(&sh->tmem, 512);
     tmem_relinquish();
   }
@@ -441,6 +442,10 @@ __global__ void __launch_bounds__(448, 1)
               mx = fmaxf(mx, q * 32 + c <= lim ? __uint_as_float(v0[c]) : -INFINITY);
           }
           m2 = lim < 0 ? 0.f : mx * sl2;
+          // the row sum adds in the same order as on the unmasked path (masked keys add an exact
+          // 0), so a row's result does not depend on which rows share its warp -- and so not on
+          // the order in which the list building placed the tokens
+          float la = 0.f, lc = 0.f;
 #pragma unroll 1  // (a full unroll makes the compiler spill)
           for (int q = 0; q < 4; ++q) {
             uint32_t v0[32];
@@ -455,11 +460,13 @@ __global__ void __launch_bounds__(448, 1)
               float a1 = ex2f(fmaf(__uint_as_float(v0[2 * c + 1]), sl2, -m2));
               a0 = k0 <= lim ? a0 : 0.f;
               a1 = k0 + 1 <= lim ? a1 : 0.f;
-              l += a0 + a1;
+              la += a0;
+              lc += a1;
               pw[c] = pack_bf16(a0, a1);
             }
             if constexpr (!kProxy) tmem_st16(Sb + q * 16, pw);
           }
+          l = la + lc;
         }
         const bool valid = t >= 0;
         const long long dst = valid ? (((long long)b * d.S + t) * d.Hq + a * G + r % G) * d.top_k + slot : -1;

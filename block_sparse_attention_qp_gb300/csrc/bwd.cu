@@ -259,6 +259,7 @@ __global__ void __launch_bounds__(352, 1)
     mbar_fence_init();
   }
   if (warp == 0) {
+    __syncwarp();  // lane 0 initialised the barriers alone; the allocation is warp-collective
     tmem_alloc(&sh->tmem, 512);
     tmem_relinquish();
   }
@@ -691,17 +692,23 @@ __global__ void __launch_bounds__(352, 1)
 // ==========================================================================================
 // The same backward with 128-row tiles (128 / G tokens x G heads): every product then has N = 128,
 // which the tensor core runs in the time of an N = 64 one -- 40 MMA instructions per 128 rows
-// instead of 64 with two 64-row tiles.  Tensor memory holds one tile's S^T (then P^T in its first
-// 64 columns) and dP^T (then dQ^T) besides dV and dK, so the S / dP products of a tile wait for the
-// previous tile's epilogue instead of running ahead of it.  Shared memory (1024-aligned base): K,
-// V (32 KB each), two Q / dO slots of 64 KB (each later holding its tile's fp32 dQ rows), dS^T
-// (32 KB) and the barriers -- 224 KB + the barrier block.
+// instead of 64 with two 64-row tiles.  Tensor memory holds one tile's S^T (then P^T) and dP^T
+// (then dQ^T) besides dV and dK, so the S / dP products of a tile wait for the previous tile's
+// epilogue instead of running ahead of it; the tensor core idles while the softmax runs.  To keep
+// that gap short the softmax and epilogue of a tile are split over eight warps: two per
+// tensor-memory lane quarter, one for the tile's rows 0-63 and one for rows 64-127.  Shared memory
+// (1024-aligned base): K, V (32 KB each), two Q / dO slots of 64 KB (each later holding its tile's
+// fp32 dQ rows), dS^T (32 KB) and the barriers -- 224 KB + the barrier block.
+// Roles (16 warps): 0 TMA of K / V, 1 MMA issue, 3 dQ reducer, 4-11 softmax / epilogue, 12-15
+// gather of the Q / dO rows; warp 2 has no role.
 namespace {
 constexpr int kTW = 128;             // rows per wide tile
 constexpr int kRTW = kTW * 128 * 2;  // 128 rows x 128 bf16 (two SW128 panels of 64 columns)
 constexpr int kSlotW = 2 * kRTW;     // Q rows, then dO rows; later the tile's fp32 dQ rows
 constexpr int kSTW = 128 * kTW * 2;  // dS^T: 128 keys x 128 rows bf16 (two panels)
 constexpr int kQSW = 2;              // Q / dO slots
+constexpr int kWideThreads = 512;    // 16 warps
+constexpr int kSoftW = 8;            // softmax / epilogue warps
 static_assert(kTW * 128 * 4 == kSlotW, "a wide tile's fp32 dQ staging fills exactly one slot");
 constexpr uint32_t kStatusLayout = kStatusInternal;  // dynamic shared memory not 1024-byte aligned
 
@@ -718,7 +725,7 @@ constexpr size_t kWideSmem = 2 * (size_t)kKV + kQSW * (size_t)kSlotW + kSTW;  //
 }  // namespace
 
 template <int G, bool kDense>
-__global__ void __launch_bounds__(352, 1)
+__global__ void __launch_bounds__(kWideThreads, 1)
     attn_bwd_wide_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                          MainArgs A) {
   using namespace sm100;
@@ -747,21 +754,22 @@ __global__ void __launch_bounds__(352, 1)
     for (int x = 0; x < kQSW; ++x) {
       mbar_init(&sh->q_full[x], 256);  // 4 gather warps x 32 lanes: a cp.async and a plain arrival each
       mbar_init(&sh->q_empty[x], 1);   // the dQ reducer, once the staged dQ rows were read
-      mbar_init(&sh->stage_ready[x], 4);
+      mbar_init(&sh->stage_ready[x], kSoftW);
     }
     mbar_init(&sh->s_full, 1);
-    mbar_init(&sh->p_full, 4);
+    mbar_init(&sh->p_full, kSoftW);
     mbar_init(&sh->ph2_full, 1);
-    mbar_init(&sh->s_free, 4);
-    mbar_init(&sh->acc_free, 4);
+    mbar_init(&sh->s_free, kSoftW);
+    mbar_init(&sh->acc_free, kSoftW);
     mbar_init(&sh->mma_done, 1);
     for (int x = 0; x < kIR; ++x) {
       mbar_init(&sh->it_full[x], 1);
-      mbar_init(&sh->it_empty[x], 10);  // MMA, 4 gather warps, reducer, 4 softmax warps
+      mbar_init(&sh->it_empty[x], 6 + kSoftW);  // MMA, 4 gather warps, reducer, softmax warps
     }
     mbar_fence_init();
   }
   if (warp == 0) {
+    __syncwarp();  // lane 0 initialised the barriers alone; the allocation is warp-collective
     tmem_alloc(&sh->tmem, 512);
     tmem_relinquish();
   }
@@ -870,8 +878,10 @@ __global__ void __launch_bounds__(352, 1)
           fence_after_sync();
           const bool acc = tl > 0;
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks)  // dV += P^T dO  (P^T from tensor memory)
-            mma_ts(RV, SB + ks * 8, desc_mnmajor(adOb, kTW, ks), id_g, acc || ks > 0);
+          for (int ks = 0; ks < 8; ++ks)  // dV += P^T dO  (P^T from tensor memory: rows 0-63 in
+            // columns 0-31, rows 64-127 in columns 64-95)
+            mma_ts(RV, SB + ks * 8 + (ks >= 4 ? 32 : 0), desc_mnmajor(adOb, kTW, ks), id_g,
+                   acc || ks > 0);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)  // dK += dS^T Q
             mma_ss(RK, desc_kmajor(adS, 128, ks), desc_mnmajor(aQb, kTW, ks), id_g, acc || ks > 0);
@@ -885,13 +895,13 @@ __global__ void __launch_bounds__(352, 1)
       }
       mma_commit(&sh->mma_done);  // arrives once every MMA issued above has completed
     }
-  } else if (warp == 2 || warp >= 8) {
+  } else if (warp >= 12) {
     // ---------------------------------------------------------------- gather: Q, dO rows
-    // Four warps (2, 8, 9, 10) each fill 32 of the tile's 128 rows with cp.async; completion is
-    // counted on q_full (one cp.async arrival and one plain arrival per lane).  Lane x holds token
-    // x of the tile (one tile ahead); warp 2 publishes them for the reducer and the softmax.
+    // Four warps (12-15) each fill 32 of the tile's 128 rows with cp.async; completion is counted
+    // on q_full (one cp.async arrival and one plain arrival per lane).  Lane x holds token x of the
+    // tile (one tile ahead); warp 12 publishes them for the reducer and the softmax.
     const uint64_t keep = l2_policy_evict_last();  // read again by the chunk's other blocks
-    const int gw = warp == 2 ? 0 : warp - 7;
+    const int gw = warp - 12;
     constexpr int WT = 32 / G;  // tokens of one warp's 32 rows
     const int r0 = 32 * gw;
     const int hi = lane >> 4, ch = lane & 15;
@@ -983,11 +993,14 @@ __global__ void __launch_bounds__(352, 1)
       }
       bulk_wait0();
     }
-  } else {
+  } else if (warp >= 4) {
     // ---------------------------------------------------------------- softmax / epilogue
-    const int w4 = warp - 4;
-    const int kr = w4 * 32 + lane;  // key row of S^T / dP^T (TMEM lane); head-dim index of dQ^T
-    const uint32_t lb = static_cast<uint32_t>(w4 * 32) << 16;
+    // Warps 4-7 take the tile's rows 0-63 (chunks 0, 1 of 32 rows) and the item's dV, warps 8-11
+    // rows 64-127 (chunks 2, 3) and dK; warp w reads tensor-memory lanes 32 (w % 4) onwards.
+    const int hf = (warp - 4) >> 2;  // half of the tile
+    const int quad = warp & 3;
+    const int kr = quad * 32 + lane;  // key row of S^T / dP^T (TMEM lane); head-dim index of dQ^T
+    const uint32_t lb = static_cast<uint32_t>(quad * 32) << 16;
     const uint64_t stream = l2_policy_evict_first();  // pbar rows: read once, by proxy_bwd
     long long i = 0;
     for (long long ni = 0; ok; ++ni) {
@@ -1010,49 +1023,57 @@ __global__ void __launch_bounds__(352, 1)
         }
         fence_after_sync();
         // ---- softmax of tile i: 32 rows at a time (P^T of rows 32 c .. 32 c + 31 lands in
-        // columns 16 c .. 16 c + 15, which chunk c / 2 has already read).  G divides 32, so the
-        // G rows of a token lie in one chunk: each chunk finishes the teacher rows of its tokens.
+        // columns 16 c + 32 hf .. + 15, which this half's first chunk has already read).  G divides
+        // 32, so the G rows of a token lie in one chunk: each chunk finishes the teacher rows of
+        // its tokens.
         constexpr int WT = 32 / G;  // tokens per chunk
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 2 * hf; c < 2 * hf + 2; ++c) {
           float pc[WT];
+          bool vis[WT];  // this thread's key is visible to the chunk's token w
 #pragma unroll
-          for (int w = 0; w < WT; ++w) pc[w] = 0.f;
-          uint32_t rs[32], rp[32];
-          __syncwarp();
-          tmem_ld32(SB + lb + 32 * c, rs);
-          tmem_ld32(DB + lb + 32 * c, rp);
-          tmem_wait_ld();
-          uint32_t pw[16], dw[16];
-#pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4) {
-            const float4 l4 = reinterpret_cast<const float4*>(sh->lse2[sl])[c * 8 + q4];
-            const float4 d4 = reinterpret_cast<const float4*>(sh->drow[sl])[c * 8 + q4];
-            const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-            const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-            float pv[4], dsv[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int r = q4 * 4 + e;  // row within the chunk
-              const int t = sh->tok[sl][(c * 32 + r) / G];
-              const bool vis = t >= 0 && j <= t;
-              const float p = vis ? ex2(__uint_as_float(rs[r]) * sl2 - lv[e]) : 0.f;
-              pv[e] = p;
-              dsv[e] = p * (__uint_as_float(rp[r]) - dv4[e]);
-            }
-#pragma unroll
-            for (int e = 0; e < 4; ++e) pc[(q4 * 4 + e) / G] += pv[e];  // the token's G heads
-            pw[2 * q4] = pack_bf16(pv[0], pv[1]);
-            pw[2 * q4 + 1] = pack_bf16(pv[2], pv[3]);
-            dw[2 * q4] = pack_bf16(dsv[0], dsv[1]);
-            dw[2 * q4 + 1] = pack_bf16(dsv[2], dsv[3]);
+          for (int w = 0; w < WT; ++w) {
+            const int t = sh->tok[sl][c * WT + w];
+            vis[w] = t >= 0 && j <= t;
+            pc[w] = 0.f;
           }
-          tmem_st16(SB + lb + 16 * c, pw);
           const uint32_t panel = adS + (uint32_t)(c >> 1) * (128 * 128);
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            st_shared_v4(panel + sm100::sw128_chunk(kr, (c & 1) * 4 + u), dw[4 * u], dw[4 * u + 1],
-                         dw[4 * u + 2], dw[4 * u + 3]);
+          for (int hh = 0; hh < 2; ++hh) {  // 16 rows at a time (fewer live registers)
+            uint32_t rs[16], rp[16], pw[8], dw[8];
+            __syncwarp();
+            tmem_ld16(SB + lb + 32 * c + 16 * hh, rs);
+            tmem_ld16(DB + lb + 32 * c + 16 * hh, rp);
+            tmem_wait_ld();
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+              const int q4 = hh * 4 + qq;
+              const float4 l4 = reinterpret_cast<const float4*>(sh->lse2[sl])[c * 8 + q4];
+              const float4 d4 = reinterpret_cast<const float4*>(sh->drow[sl])[c * 8 + q4];
+              const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+              const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+              float pv[4], dsv[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int r = qq * 4 + e;  // row within the 16
+                const float p = vis[(q4 * 4 + e) / G] ? ex2(__uint_as_float(rs[r]) * sl2 - lv[e]) : 0.f;
+                pv[e] = p;
+                dsv[e] = p * (__uint_as_float(rp[r]) - dv4[e]);
+              }
+#pragma unroll
+              for (int e = 0; e < 4; ++e) pc[(q4 * 4 + e) / G] += pv[e];  // the token's G heads
+              pw[2 * qq] = pack_bf16(pv[0], pv[1]);
+              pw[2 * qq + 1] = pack_bf16(pv[2], pv[3]);
+              dw[2 * qq] = pack_bf16(dsv[0], dsv[1]);
+              dw[2 * qq + 1] = pack_bf16(dsv[2], dsv[3]);
+            }
+            // P^T of these 16 rows: 8 columns of bf16 pairs, over columns this half has read
+            tmem_st8(SB + lb + 16 * c + 32 * hf + 8 * hh, pw);
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+              st_shared_v4(panel + sm100::sw128_chunk(kr, (c & 1) * 4 + 2 * hh + u), dw[4 * u],
+                           dw[4 * u + 1], dw[4 * u + 2], dw[4 * u + 3]);
+          }
           // teacher: mean of the proxy head's G R query heads' probabilities of each token, one
           // fp16 row per list entry; with R > 1 attention groups per proxy head each adds its share
           if (d.R == 1) {
@@ -1069,6 +1090,7 @@ __global__ void __launch_bounds__(352, 1)
                           pc[w] * (1.f / (G * d.R)));
           }
         }
+        __syncwarp();
         tmem_wait_st();
         fence_async_smem();
         fence_before_sync();
@@ -1081,12 +1103,12 @@ __global__ void __launch_bounds__(352, 1)
         fence_after_sync();
         float* stage = reinterpret_cast<float*>(sSl + sl * kSlotW);
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 2 * hf; c < 2 * hf + 2; ++c) {
           uint32_t r0[32];
           __syncwarp();
           tmem_ld32(DB + lb + 32 * c, r0);
           tmem_wait_ld();
-          if (c == 3) {  // DB may now take the next tile's dP^T
+          if (c == 2 * hf + 1) {  // DB may now take the next tile's dP^T
             fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh->s_free);
@@ -1099,24 +1121,23 @@ __global__ void __launch_bounds__(352, 1)
         if (lane == 0) mbar_arrive(&sh->stage_ready[sl]);
       }
       if (!ok) break;
-      // ---- item end: dV and dK rows of this key (the item's last phase 2 has completed)
+      // ---- item end: dV (rows-0-63 warps) or dK (rows-64-127 warps) row of this key (the
+      // item's last phase 2 has completed)
       {
-        float* pv = A.dv + (((size_t)b * d.S + j) * d.Hkv + kvh) * kD;
-        float* pk = A.dk + (((size_t)b * d.S + j) * d.Hkv + kvh) * kD;
-#pragma unroll
+        float* dst = (hf == 0 ? A.dv : A.dk) + (((size_t)b * d.S + j) * d.Hkv + kvh) * kD;
+        const uint32_t acc_t = hf == 0 ? RV : RK;
+        const float mul = hf == 0 ? 1.f : d.scale;
+        __syncwarp();
+#pragma unroll 1
         for (int c = 0; c < 4; ++c) {
-          uint32_t rv[32], rk[32];
-          tmem_ld32(RV + lb + c * 32, rv);
-          tmem_ld32(RK + lb + c * 32, rk);
+          uint32_t rv[32];
+          tmem_ld32(acc_t + lb + c * 32, rv);
           tmem_wait_ld();
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            red4(pv + c * 32 + 4 * u, __uint_as_float(rv[4 * u]), __uint_as_float(rv[4 * u + 1]),
-                 __uint_as_float(rv[4 * u + 2]), __uint_as_float(rv[4 * u + 3]));
-            red4(pk + c * 32 + 4 * u, __uint_as_float(rk[4 * u]) * d.scale,
-                 __uint_as_float(rk[4 * u + 1]) * d.scale, __uint_as_float(rk[4 * u + 2]) * d.scale,
-                 __uint_as_float(rk[4 * u + 3]) * d.scale);
-          }
+          for (int u = 0; u < 8; ++u)
+            red4(dst + c * 32 + 4 * u, __uint_as_float(rv[4 * u]) * mul,
+                 __uint_as_float(rv[4 * u + 1]) * mul, __uint_as_float(rv[4 * u + 2]) * mul,
+                 __uint_as_float(rv[4 * u + 3]) * mul);
         }
         fence_before_sync();
         __syncwarp();
@@ -1184,6 +1205,7 @@ __global__ void __launch_bounds__(384, 1)
     mbar_fence_init();
   }
   if (warp == 0) {
+    __syncwarp();  // lane 0 initialised the barriers alone; the allocation is warp-collective
     tmem_alloc(&sh->tmem, 512);
     tmem_relinquish();
   }
@@ -1555,7 +1577,7 @@ void attn_bwd_wide_g(const CUtensorMap& mk, const CUtensorMap& mv, const MainArg
   const size_t smem = kWideSmem + sizeof(WideShared);  // base 1024-aligned (checked in the kernel)
   cudaFuncSetAttribute(attn_bwd_wide_kernel<G, kDense>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        (int)smem);
-  attn_bwd_wide_kernel<G, kDense><<<num_sms(), 352, smem, st>>>(mk, mv, a);
+  attn_bwd_wide_kernel<G, kDense><<<num_sms(), kWideThreads, smem, st>>>(mk, mv, a);
 }
 template <bool kDense, bool kKL>
 void proxy_bwd_g(const CUtensorMap& mkp, const ProxyArgs& a, cudaStream_t st) {

@@ -119,6 +119,7 @@ __global__ void __launch_bounds__(384, 1)
     mbar_fence_init();
   }
   if (warp == 0) {
+    __syncwarp();  // lane 0 initialised the barriers alone; the allocation is warp-collective
     tmem_alloc(&sh->tmem, 512);
     tmem_relinquish();
   }

@@ -181,6 +181,20 @@ def test_cfg2_full_parity():
     print(f"workload 2: {n_bad} selection rows differ, all near ties ({n_exc})")
 
 
+def test_forward_is_bitwise_repeatable():
+    """The list building places tokens with atomic cursors, so a token's tile partners differ from
+    run to run; the forward's per-row arithmetic must not depend on them (same summation order on
+    the masked and the unmasked softmax path), so two runs give identical bits."""
+    w = Workload("det", B=2, S=1536, Hq=16, Hkv=4, Hp=4, top_k=5)
+    g = to_dev(make_inputs(w, 77))
+    runs = [msa.msa_forward(g["q"], g["k"], g["v"], g["qp"], g["kp"], w.top_k, w.scale)
+            for _ in range(3)]
+    for o, lse, idx in runs[1:]:
+        assert torch.equal(idx, runs[0][2])
+        assert torch.equal(o, runs[0][0])
+        assert torch.equal(lse, runs[0][1])
+
+
 def test_kl_value_does_not_change_the_gradients():
     """Asking for the KL value leaves every gradient unchanged up to fp32 summation order, since
     the value is computed beside the proxy gradients, not from them.  The gradient accumulators
