@@ -100,13 +100,13 @@ long long max_items(long long entries, const Dims& d, const ItemSpec& s) {
 }
 
 // Sequence chunk of the backward's token lists: the dQ rows one chunk contributes for one proxy
-// head (chunk x Gp heads x 128 x fp32) are kept to <= 64 MB, so that most of them stay resident in L2
-// while the work items of that chunk and group run.  Smaller chunks cut the lists into more,
-// shorter items (more partly filled tiles and K / V loads); on GB300 at S = 64K, G = 8 the step
-// was fastest at 64 MB among 8, 16, 32 and 64 MB.
+// head (chunk x Gp heads x 128 x fp32) are kept to <= 32 MB, so that most of them (and the chunk's
+// Q and dO rows) stay resident in L2 while the work items of that chunk and group run.  Smaller
+// chunks cut the lists into more, shorter items (more partly filled tiles and K / V loads); on
+// GB300 at S = 64K, G = 8 the backward was fastest at 32 MB among 16, 32, 64 and 128 MB.
 int bwd_chunk(const Dims& d) {
   int c = kBlock;
-  while ((long long)c * 2 * d.Gp() * kD * 4 <= (64ll << 20) && c * 2 <= d.S) c *= 2;
+  while ((long long)c * 2 * d.Gp() * kD * 4 <= (32ll << 20) && c * 2 <= d.S) c *= 2;
   return c;
 }
 

@@ -400,17 +400,22 @@ __global__ void __launch_bounds__(448, 1)
         // tcgen05.ld / st are warp-collective (.sync.aligned): the path must be uniform per warp
         if (__all_sync(0xffffffffu, lim == kBlock - 1)) {
           // ---- every key of every row of this warp visible
-          float mx = -INFINITY;
+          float mxa = -INFINITY, mxb = -INFINITY;  // two chains of three-input maxima
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             uint32_t v0[32];
             tmem_ld32(Sb + q * 32, v0);
             tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < 32; ++c) mx = fmaxf(mx, __uint_as_float(v0[c]));
+            for (int c = 0; c < 8; ++c) {
+              mxa = fmax3(mxa, __uint_as_float(v0[4 * c]), __uint_as_float(v0[4 * c + 1]));
+              mxb = fmax3(mxb, __uint_as_float(v0[4 * c + 2]), __uint_as_float(v0[4 * c + 3]));
+            }
           }
-          m2 = mx * sl2;
-          float la = 0.f, lc = 0.f;
+          m2 = fmaxf(mxa, mxb) * sl2;
+          // even and odd keys summed in two fp32 chains (la, lc) by packed adds
+          float2 lac = make_float2(0.f, 0.f);
+          const float2 sl2x2 = make_float2(sl2, sl2), nm2 = make_float2(-m2, -m2);
 #pragma unroll 1  // (a full unroll makes the compiler spill)
           for (int q = 0; q < 4; ++q) {
             uint32_t v0[32];
@@ -419,15 +424,15 @@ __global__ void __launch_bounds__(448, 1)
             uint32_t pw[16];
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
-              const float a0 = ex2f(fmaf(__uint_as_float(v0[2 * c]), sl2, -m2));
-              const float a1 = ex2f(fmaf(__uint_as_float(v0[2 * c + 1]), sl2, -m2));
-              la += a0;
-              lc += a1;
+              const float2 x = ffma2(make_float2(__uint_as_float(v0[2 * c]), __uint_as_float(v0[2 * c + 1])),
+                                     sl2x2, nm2);
+              const float a0 = ex2f(x.x), a1 = ex2f(x.y);
+              lac = fadd2(lac, make_float2(a0, a1));
               pw[c] = pack_bf16(a0, a1);
             }
             if constexpr (!kProxy) tmem_st16(Sb + q * 16, pw);
           }
-          l = la + lc;
+          l = lac.x + lac.y;
         } else {
           // ---- some row of this warp is in its local block (keys after the token masked) or is
           // a padding row (lim = -1)
@@ -445,7 +450,8 @@ __global__ void __launch_bounds__(448, 1)
           // the row sum adds in the same order as on the unmasked path (masked keys add an exact
           // 0), so a row's result does not depend on which rows share its warp -- and so not on
           // the order in which the list building placed the tokens
-          float la = 0.f, lc = 0.f;
+          float2 lac = make_float2(0.f, 0.f);
+          const float2 sl2x2 = make_float2(sl2, sl2), nm2 = make_float2(-m2, -m2);
 #pragma unroll 1  // (a full unroll makes the compiler spill)
           for (int q = 0; q < 4; ++q) {
             uint32_t v0[32];
@@ -456,17 +462,17 @@ __global__ void __launch_bounds__(448, 1)
             for (int c = 0; c < 16; ++c) {
               const int k0 = q * 32 + 2 * c;
               // exponentiate unconditionally, then select: no per-lane branches
-              float a0 = ex2f(fmaf(__uint_as_float(v0[2 * c]), sl2, -m2));
-              float a1 = ex2f(fmaf(__uint_as_float(v0[2 * c + 1]), sl2, -m2));
+              const float2 x = ffma2(make_float2(__uint_as_float(v0[2 * c]), __uint_as_float(v0[2 * c + 1])),
+                                     sl2x2, nm2);
+              float a0 = ex2f(x.x), a1 = ex2f(x.y);
               a0 = k0 <= lim ? a0 : 0.f;
               a1 = k0 + 1 <= lim ? a1 : 0.f;
-              la += a0;
-              lc += a1;
+              lac = fadd2(lac, make_float2(a0, a1));
               pw[c] = pack_bf16(a0, a1);
             }
             if constexpr (!kProxy) tmem_st16(Sb + q * 16, pw);
           }
-          l = la + lc;
+          l = lac.x + lac.y;
         }
         const bool valid = t >= 0;
         const long long dst = valid ? (((long long)b * d.S + t) * d.Hq + a * G + r % G) * d.top_k + slot : -1;
@@ -499,12 +505,17 @@ __global__ void __launch_bounds__(448, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh->o_free[bb]);
           }
+          const float2 sc2 = make_float2(sc, sc);
+          auto scaled = [&](int c) -> uint32_t {  // O columns c, c+1 times 1 / l, as bf16 pair
+            const float2 o2 = fmul2(make_float2(__uint_as_float(v0[c]), __uint_as_float(v0[c + 1])), sc2);
+            return pack_bf16(o2.x, o2.y);
+          };
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const uint32_t w0 = pack_bf16(__uint_as_float(v0[8 * u + 0]) * sc, __uint_as_float(v0[8 * u + 1]) * sc);
-            const uint32_t w1 = pack_bf16(__uint_as_float(v0[8 * u + 2]) * sc, __uint_as_float(v0[8 * u + 3]) * sc);
-            const uint32_t w2 = pack_bf16(__uint_as_float(v0[8 * u + 4]) * sc, __uint_as_float(v0[8 * u + 5]) * sc);
-            const uint32_t w3 = pack_bf16(__uint_as_float(v0[8 * u + 6]) * sc, __uint_as_float(v0[8 * u + 7]) * sc);
+            const uint32_t w0 = scaled(8 * u + 0);
+            const uint32_t w1 = scaled(8 * u + 2);
+            const uint32_t w2 = scaled(8 * u + 4);
+            const uint32_t w3 = scaled(8 * u + 6);
             const uint32_t a = stw + lane * 64 + (((u + (lane >> 1)) & 3) << 4);
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(a), "r"(w0), "r"(w1),
                          "r"(w2), "r"(w3)

@@ -145,8 +145,8 @@ constexpr int kQPB = 3;  // proxy query row buffers
 constexpr int kNPB = 4;  // teacher row buffers (64 entries x 128 keys fp16 each)
 
 struct ProxyShared {
-  int tok[kNPB][kPG];     // per teacher buffer (read by the dz warps)
-  float lpx2[kNPB][kPG];
+  alignas(16) int tok[kNPB][kPG];  // per teacher buffer (read by the dz warps, 4 at a time)
+  alignas(16) float lpx2[kNPB][kPG];
   int tokq[kQPB][kPG];  // per query-row buffer (read by the dQp-flush warps)
   int it_ring[kIR];  // item numbers taken by this block, in order (>= total: no more)
   uint64_t kp_full, kp_empty, qp_full[kQPB], qp_empty[kQPB], pb_full[kNPB], meta_free[kNPB], z_full[2],
@@ -713,8 +713,8 @@ static_assert(kTW * 128 * 4 == kSlotW, "a wide tile's fp32 dQ staging fills exac
 constexpr uint32_t kStatusLayout = kStatusInternal;  // dynamic shared memory not 1024-byte aligned
 
 struct WideShared {
-  float lse2[kQSW][kTW];  // row LSE * log2(e), per slot
-  float drow[kQSW][kTW];  // row D, per slot
+  float nlse2[kQSW][kTW];  // -(row LSE * log2(e)), per slot
+  float ndrow[kQSW][kTW];  // -(row D), per slot
   int tok[kQSW][32];      // tokens of the slot's tile (128 / G <= 32), -1: none
   int it_ring[kIR];
   uint64_t kv_full, kv_empty, q_full[kQSW], q_empty[kQSW], stage_ready[kQSW], s_full, p_full,
@@ -952,8 +952,8 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           cp_async16_hint(dQb + off, A.q + grow, t >= 0, keep);
           cp_async16_hint(ddOb + off, A.dout + grow, t >= 0, keep);
         }
-        sh->lse2[sl][r0 + lane] = mcur.x;
-        sh->drow[sl][r0 + lane] = mcur.y;
+        sh->nlse2[sl][r0 + lane] = -mcur.x;
+        sh->ndrow[sl][r0 + lane] = -mcur.y;
         if (gw == 0) sh->tok[sl][lane] = tcur;
         cp_async_arrive(&sh->q_full[sl]);
         mbar_arrive(&sh->q_full[sl]);  // publishes the row data and tok
@@ -1038,6 +1038,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             pc[w] = 0.f;
           }
           const uint32_t panel = adS + (uint32_t)(c >> 1) * (128 * 128);
+          const float2 sl2x2 = make_float2(sl2, sl2);
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {  // 16 rows at a time (fewer live registers)
             uint32_t rs[16], rp[16], pw[8], dw[8];
@@ -1048,17 +1049,23 @@ __global__ void __launch_bounds__(kWideThreads, 1)
 #pragma unroll
             for (int qq = 0; qq < 4; ++qq) {
               const int q4 = hh * 4 + qq;
-              const float4 l4 = reinterpret_cast<const float4*>(sh->lse2[sl])[c * 8 + q4];
-              const float4 d4 = reinterpret_cast<const float4*>(sh->drow[sl])[c * 8 + q4];
-              const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-              const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+              const float4 l4 = reinterpret_cast<const float4*>(sh->nlse2[sl])[c * 8 + q4];
+              const float4 d4 = reinterpret_cast<const float4*>(sh->ndrow[sl])[c * 8 + q4];
+              const float nl[4] = {l4.x, l4.y, l4.z, l4.w};
+              const float nd[4] = {d4.x, d4.y, d4.z, d4.w};
               float pv[4], dsv[4];
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int r = qq * 4 + e;  // row within the 16
-                const float p = vis[(q4 * 4 + e) / G] ? ex2(__uint_as_float(rs[r]) * sl2 - lv[e]) : 0.f;
-                pv[e] = p;
-                dsv[e] = p * (__uint_as_float(rp[r]) - dv4[e]);
+              for (int e = 0; e < 4; e += 2) {  // two rows per packed instruction
+                const int r = qq * 4 + e;      // row within the 16
+                const float2 x = ffma2(make_float2(__uint_as_float(rs[r]), __uint_as_float(rs[r + 1])),
+                                       sl2x2, make_float2(nl[e], nl[e + 1]));
+                pv[e] = vis[(q4 * 4 + e) / G] ? ex2(x.x) : 0.f;
+                pv[e + 1] = vis[(q4 * 4 + e + 1) / G] ? ex2(x.y) : 0.f;
+                const float2 ds = fmul2(make_float2(pv[e], pv[e + 1]),
+                                        fadd2(make_float2(__uint_as_float(rp[r]), __uint_as_float(rp[r + 1])),
+                                              make_float2(nd[e], nd[e + 1])));
+                dsv[e] = ds.x;
+                dsv[e + 1] = ds.y;
               }
 #pragma unroll
               for (int e = 0; e < 4; ++e) pc[(q4 * 4 + e) / G] += pv[e];  // the token's G heads
@@ -1435,41 +1442,51 @@ __global__ void __launch_bounds__(384, 1)
           ok = false;
           break;
         }
-        fence_after_sync();
-        uint32_t z0[32], z1[32];
-        tmem_ld32(RZ0 + 64 * bb + lb, z0);
-        tmem_ld32(RZ0 + 64 * bb + lb + 32, z1);
-        tmem_wait_ld();
-        const __half* pbr = sPb + pbi * kPG * kBlock;
-        uint32_t zw[kPG / 2];
-#pragma unroll
-        for (int k2 = 0; k2 < kPG / 2; ++k2) {
-          float dzv[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int k = 2 * k2 + e;
-            const int t = sh->tok[pbi][k];
-            // exponentiate unconditionally and select (no per-lane branch around the asm)
-            const float zz = __uint_as_float(k < 32 ? z0[k] : z1[k - 32]);
-            const float lz = zz * sl2 - sh->lpx2[pbi][k];  // log2 of the student probability
-            const float pb = __half2float(pbr[k * kBlock + kr]);
-            const float v = A.cz * (ex2(lz) - pb);
-            const bool vis = k < gcount && t >= 0 && j <= t;
-            dzv[e] = vis ? v : 0.f;
-            if constexpr (kKL) kl += (vis && pb > 0.f) ? pb * (__logf(pb) - lz * kLn2) : 0.f;
-          }
-          zw[k2] = pack_bf16(dzv[0], dzv[1]);
-        }
-        // dz^T buffer bb was last read by the gradient products of group i-2
+        // dz^T buffer bb was last read by the gradient products of group i-2, which ran on the
+        // tensor core before z of this group (already complete: z_full)
         if (i >= 2 && !mbar_wait_warp(&sh->fl_full[bb], par((i - 2) >> 1), A.status)) {
           ok = false;
           break;
         }
+        fence_after_sync();
+        const __half* pbr = sPb + pbi * kPG * kBlock;
         const uint32_t adzb = adz + bb * kST;
+        const float2 sl2x2 = make_float2(sl2, sl2), cz2 = make_float2(A.cz, A.cz);
+#pragma unroll 1
+        for (int h16 = 0; h16 < kPG / 16; ++h16) {  // 16 tokens (two 16-byte chunks of dz^T) at a time
+          uint32_t zr[16], zw[8];
+          __syncwarp();
+          tmem_ld16(RZ0 + 64 * bb + lb + 16 * h16, zr);
+          tmem_wait_ld();
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          st_shared_v4(adzb + sm100::sw128_chunk(kr, u), zw[4 * u], zw[4 * u + 1], zw[4 * u + 2],
-                       zw[4 * u + 3]);
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const int kb = 16 * h16 + 4 * k4;
+            const int4 t4 = *reinterpret_cast<const int4*>(&sh->tok[pbi][kb]);
+            const float4 l4 = *reinterpret_cast<const float4*>(&sh->lpx2[pbi][kb]);
+            const int tv[4] = {t4.x, t4.y, t4.z, t4.w};
+            const float nl[4] = {-l4.x, -l4.y, -l4.z, -l4.w};
+#pragma unroll
+            for (int pp = 0; pp < 2; ++pp) {
+              const int k = kb + 2 * pp;
+              // log2 of the student probabilities; exponentiate unconditionally and select
+              const float2 lz = ffma2(make_float2(__uint_as_float(zr[4 * k4 + 2 * pp]),
+                                                  __uint_as_float(zr[4 * k4 + 2 * pp + 1])),
+                                      sl2x2, make_float2(nl[2 * pp], nl[2 * pp + 1]));
+              const float pb0 = __half2float(pbr[k * kBlock + kr]);
+              const float pb1 = __half2float(pbr[(k + 1) * kBlock + kr]);
+              const float2 v = fmul2(cz2, fadd2(make_float2(ex2(lz.x), ex2(lz.y)), make_float2(-pb0, -pb1)));
+              const bool vis0 = k < gcount && tv[2 * pp] >= 0 && j <= tv[2 * pp];
+              const bool vis1 = k + 1 < gcount && tv[2 * pp + 1] >= 0 && j <= tv[2 * pp + 1];
+              zw[2 * k4 + pp] = pack_bf16(vis0 ? v.x : 0.f, vis1 ? v.y : 0.f);
+              if constexpr (kKL) {
+                kl += (vis0 && pb0 > 0.f) ? pb0 * (__logf(pb0) - lz.x * kLn2) : 0.f;
+                kl += (vis1 && pb1 > 0.f) ? pb1 * (__logf(pb1) - lz.y * kLn2) : 0.f;
+              }
+            }
+          }
+          st_shared_v4(adzb + sm100::sw128_chunk(kr, 2 * h16), zw[0], zw[1], zw[2], zw[3]);
+          st_shared_v4(adzb + sm100::sw128_chunk(kr, 2 * h16 + 1), zw[4], zw[5], zw[6], zw[7]);
+        }
         fence_async_smem();
         fence_before_sync();
         __syncwarp();

@@ -53,13 +53,16 @@ class Workload:
                 f"{mode}{extra}")
 
 
-# The five workloads of the method's training benchmark (index = workload number - 1).
+# The five workloads of the method's training benchmark, then a profiling case (index =
+# workload number - 1).
 WORKLOADS = [
     Workload("msa_s1k", B=1, S=1024, Hq=8, Hkv=2, Hp=2, top_k=4),
     Workload("msa_s8k_planted", B=2, S=8192, Hq=32, Hkv=8, Hp=8, top_k=16, planted=4),
     Workload("msa_s64k_planted", B=1, S=65536, Hq=64, Hkv=8, Hp=8, top_k=16, planted=4),
     Workload("msa_warmup_s32k", B=1, S=32768, Hq=32, Hkv=8, Hp=8, top_k=0),
     Workload("msa_s1m", B=1, S=1048576, Hq=16, Hkv=4, Hp=4, top_k=16),
+    # the 64K workload's heads at 8K tokens: the small case its kernels are profiled on
+    Workload("msa_s8k_g8_planted", B=1, S=8192, Hq=64, Hkv=8, Hp=8, top_k=16, planted=4),
 ]
 
 
