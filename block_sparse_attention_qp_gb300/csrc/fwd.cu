@@ -28,6 +28,15 @@ __global__ void __launch_bounds__(256, 3) combine_kernel(Dims d, const bf16* __r
     const size_t base = (size_t)r * d.top_k;
     float l0 = lane < d.top_k ? lpart[base + lane] : NAN;
     float l1 = lane + 32 < d.top_k ? lpart[base + lane + 32] : NAN;
+    // the first 16 slots' partials are requested together with the log-sum-exps, before the
+    // weights are known (one memory round trip per row, not two)
+    uint4 pv0[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int s = 2 * u + half;
+      pv0[u] = s < d.top_k ? ld_global_nc_v4_hint(opart + (base + s) * kD + l16 * 8, pol)
+                           : make_uint4(0u, 0u, 0u, 0u);
+    }
     l0 = l0 == l0 ? l0 : -INFINITY;  // NaN: slot not written (invalid or padding)
     l1 = l1 == l1 ? l1 : -INFINITY;
     float mx = fmaxf(l0, l1);
@@ -39,16 +48,7 @@ __global__ void __launch_bounds__(256, 3) combine_kernel(Dims d, const bf16* __r
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    // 16 slots per pass: all eight 16-byte loads of a lane are issued before any is used, and
-    // they do not wait for the weights (a slot that was never written is loaded but not used)
-    for (int s0 = 0; s0 < d.top_k; s0 += 16) {
-      uint4 pv[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int s = s0 + 2 * u + half;
-        pv[u] = s < d.top_k ? ld_global_nc_v4_hint(opart + (base + s) * kD + l16 * 8, pol)
-                            : make_uint4(0u, 0u, 0u, 0u);
-      }
+    auto accumulate = [&](int s0, const uint4 (&pv)[8]) {
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int s = s0 + 2 * u + half;
@@ -65,6 +65,19 @@ __global__ void __launch_bounds__(256, 3) combine_kernel(Dims d, const bf16* __r
           }
         }
       }
+    };
+    accumulate(0, pv0);
+    // further passes of 16 slots (top_k > 16): all eight 16-byte loads of a lane are issued
+    // before any is used (a slot that was never written is loaded but not used)
+    for (int s0 = 16; s0 < d.top_k; s0 += 16) {
+      uint4 pv[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int s = s0 + 2 * u + half;
+        pv[u] = s < d.top_k ? ld_global_nc_v4_hint(opart + (base + s) * kD + l16 * 8, pol)
+                            : make_uint4(0u, 0u, 0u, 0u);
+      }
+      accumulate(s0, pv);
     }
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], 16);
