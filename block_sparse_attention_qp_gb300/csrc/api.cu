@@ -102,11 +102,18 @@ long long max_items(long long entries, const Dims& d, const ItemSpec& s) {
 // Sequence chunk of the backward's token lists: the dQ rows one chunk contributes for one proxy
 // head (chunk x Gp heads x 128 x fp32) are kept to <= 32 MB, so that most of them (and the chunk's
 // Q and dO rows) stay resident in L2 while the work items of that chunk and group run.  Smaller
-// chunks cut the lists into more, shorter items (more partly filled tiles and K / V loads); on
-// GB300 at S = 64K, G = 8 the backward was fastest at 32 MB among 16, 32, 64 and 128 MB.
-int bwd_chunk(const Dims& d) {
+// chunks cut the lists into more, shorter items (more partly filled tiles and K / V loads): on
+// GB300 at S = 64K, G = 8 (about 256 entries per sparse list at 32 MB) the backward was fastest at
+// 32 MB among 16, 32, 64 and 128 MB, while at S = 1M, G = 4 (32 entries per list at 32 MB) 64 MB
+// was 28 % faster.  So sparse lists shorter than 128 entries on average (a list of one chunk,
+// proxy head and block holds about chunk x top_k x 128 / S entries) double the chunk, up to 64 MB.
+int bwd_chunk(const Dims& d, bool sparse) {
   int c = kBlock;
   while ((long long)c * 2 * d.Gp() * kD * 4 <= (32ll << 20) && c * 2 <= d.S) c *= 2;
+  if (sparse)
+    while ((long long)c * d.top_k * kBlock < 128ll * d.S && c * 2 <= d.S &&
+           (long long)c * 2 * d.Gp() * kD * 4 <= (64ll << 20))
+      c *= 2;
   return c;
 }
 
@@ -258,7 +265,7 @@ int check_shape(const msa_shape_t* s, int op, Dims* out) {
   d.top_k = sparse ? s->top_k : 1;
   d.nblk = s->S / kBlock;
   d.scale = s->scale;
-  d = with_chunk(d, bwd ? bwd_chunk(d) : sparse ? fwd_chunk(d) : d.S);
+  d = with_chunk(d, bwd ? bwd_chunk(d, sparse) : sparse ? fwd_chunk(d) : d.S);
   if (op == MSA_OP_WARMUP_BACKWARD && dense_entries(d) >= (1ll << 31)) {
     set_err("B*Hp*S*S/256 must stay below 2^31 in the warmup backward");
     return MSA_ERR_UNSUPPORTED;

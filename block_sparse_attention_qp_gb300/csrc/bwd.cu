@@ -714,7 +714,7 @@ constexpr uint32_t kStatusLayout = kStatusInternal;  // dynamic shared memory no
 
 struct WideShared {
   float nlse2[kQSW][kTW];  // -(row LSE * log2(e)), per slot
-  float ndrow[kQSW][kTW];  // -(row D), per slot
+  float ndrow[kQSW][kTW];  // -(row D) * scale, per slot
   int tok[kQSW][32];      // tokens of the slot's tile (128 / G <= 32), -1: none
   int it_ring[kIR];
   uint64_t kv_full, kv_empty, q_full[kQSW], q_empty[kQSW], stage_ready[kQSW], s_full, p_full,
@@ -953,7 +953,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           cp_async16_hint(ddOb + off, A.dout + grow, t >= 0, keep);
         }
         sh->nlse2[sl][r0 + lane] = -mcur.x;
-        sh->ndrow[sl][r0 + lane] = -mcur.y;
+        sh->ndrow[sl][r0 + lane] = -mcur.y * d.scale;
         if (gw == 0) sh->tok[sl][lane] = tcur;
         cp_async_arrive(&sh->q_full[sl]);
         mbar_arrive(&sh->q_full[sl]);  // publishes the row data and tok
@@ -1038,7 +1038,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
             pc[w] = 0.f;
           }
           const uint32_t panel = adS + (uint32_t)(c >> 1) * (128 * 128);
-          const float2 sl2x2 = make_float2(sl2, sl2);
+          const float2 sl2x2 = make_float2(sl2, sl2), sc2 = make_float2(d.scale, d.scale);
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {  // 16 rows at a time (fewer live registers)
             uint32_t rs[16], rp[16], pw[8], dw[8];
@@ -1061,9 +1061,10 @@ __global__ void __launch_bounds__(kWideThreads, 1)
                                        sl2x2, make_float2(nl[e], nl[e + 1]));
                 pv[e] = vis[(q4 * 4 + e) / G] ? ex2(x.x) : 0.f;
                 pv[e + 1] = vis[(q4 * 4 + e + 1) / G] ? ex2(x.y) : 0.f;
+                // dS = scale P (dP - D): the softmax scale of dK and dQ is folded in here
                 const float2 ds = fmul2(make_float2(pv[e], pv[e + 1]),
-                                        fadd2(make_float2(__uint_as_float(rp[r]), __uint_as_float(rp[r + 1])),
-                                              make_float2(nd[e], nd[e + 1])));
+                                        ffma2(make_float2(__uint_as_float(rp[r]), __uint_as_float(rp[r + 1])),
+                                              sc2, make_float2(nd[e], nd[e + 1])));
                 dsv[e] = ds.x;
                 dsv[e + 1] = ds.y;
               }
@@ -1109,19 +1110,21 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         if (!waitw(14, &sh->ph2_full, par(i))) { ok = false; break; }
         fence_after_sync();
         float* stage = reinterpret_cast<float*>(sSl + sl * kSlotW);
-#pragma unroll 1
-        for (int c = 2 * hf; c < 2 * hf + 2; ++c) {
-          uint32_t r0[32];
+        {
+          // both chunks of this half out of DB first, so that DB is free for the next tile's dP^T
+          // before the rows are staged
+          uint32_t r0[32], r1[32];
           __syncwarp();
-          tmem_ld32(DB + lb + 32 * c, r0);
+          tmem_ld32(DB + lb + 64 * hf, r0);
+          tmem_ld32(DB + lb + 64 * hf + 32, r1);
           tmem_wait_ld();
-          if (c == 2 * hf + 1) {  // DB may now take the next tile's dP^T
-            fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sh->s_free);
-          }
+          fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh->s_free);
 #pragma unroll
-          for (int r = 0; r < 32; ++r) stage[(32 * c + r) * kD + kr] = __uint_as_float(r0[r]) * d.scale;
+          for (int r = 0; r < 32; ++r) stage[(64 * hf + r) * kD + kr] = __uint_as_float(r0[r]);
+#pragma unroll
+          for (int r = 0; r < 32; ++r) stage[(64 * hf + 32 + r) * kD + kr] = __uint_as_float(r1[r]);
         }
         fence_async_smem();
         __syncwarp();
@@ -1133,7 +1136,6 @@ __global__ void __launch_bounds__(kWideThreads, 1)
       {
         float* dst = (hf == 0 ? A.dv : A.dk) + (((size_t)b * d.S + j) * d.Hkv + kvh) * kD;
         const uint32_t acc_t = hf == 0 ? RV : RK;
-        const float mul = hf == 0 ? 1.f : d.scale;
         __syncwarp();
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
@@ -1142,9 +1144,8 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           tmem_wait_ld();
 #pragma unroll
           for (int u = 0; u < 8; ++u)
-            red4(dst + c * 32 + 4 * u, __uint_as_float(rv[4 * u]) * mul,
-                 __uint_as_float(rv[4 * u + 1]) * mul, __uint_as_float(rv[4 * u + 2]) * mul,
-                 __uint_as_float(rv[4 * u + 3]) * mul);
+            red4(dst + c * 32 + 4 * u, __uint_as_float(rv[4 * u]), __uint_as_float(rv[4 * u + 1]),
+                 __uint_as_float(rv[4 * u + 2]), __uint_as_float(rv[4 * u + 3]));
         }
         fence_before_sync();
         __syncwarp();
