@@ -394,7 +394,7 @@ int msa_forward(const msa_shape_t* shape, const void* q, const void* k, const vo
   if ((rc = check_ws(p, workspace, workspace_bytes))) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaGetLastError();
-  cudaMemsetAsync(at<char>(workspace, p.status), 0, sizeof(unsigned), st);
+  cudaMemsetAsync(at<char>(workspace, p.status), 0, 32 * sizeof(unsigned), st);  // status, counters, wait place
   if (!indices_given) {
     bool ok = true;
     timed("proxy_topk", st, [&] {
@@ -439,7 +439,7 @@ int msa_backward(const msa_shape_t* shape, const void* q, const void* k, const v
   if ((rc = check_ws(p, workspace, workspace_bytes))) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaGetLastError();
-  cudaMemsetAsync(at<char>(workspace, p.status), 0, sizeof(unsigned), st);
+  cudaMemsetAsync(at<char>(workspace, p.status), 0, 32 * sizeof(unsigned), st);  // status, counters, wait place
   zero_grads(d, p, workspace, st);
   build_lists(d, p, block_idx, workspace, 2, st);
   timed("bwd_rowdot", st, [&] { launch_bwd_rowdot(d, o, dout, lse, at<float2>(workspace, p.rowm), st); });
@@ -508,7 +508,7 @@ int msa_warmup_forward(const msa_shape_t* shape, const void* q, const void* k, c
   if ((rc = check_ws(p, workspace, workspace_bytes))) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaGetLastError();
-  cudaMemsetAsync(at<char>(workspace, p.status), 0, sizeof(unsigned), st);
+  cudaMemsetAsync(at<char>(workspace, p.status), 0, 32 * sizeof(unsigned), st);  // status, counters, wait place
   bool ok = true;
   timed("dense_fwd", st, [&] {
     ok = launch_dense_fwd(d, q, k, v, o, lse, at<unsigned>(workspace, p.status), st);
@@ -535,7 +535,7 @@ int msa_warmup_backward(const msa_shape_t* shape, const void* q, const void* k, 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaGetLastError();
   unsigned* status = at<unsigned>(workspace, p.status);
-  cudaMemsetAsync(status, 0, sizeof(unsigned), st);
+  cudaMemsetAsync(status, 0, 32 * sizeof(unsigned), st);  // status, counters, wait place
   zero_grads(d, p, workspace, st);
   const ItemSpec specs[1] = {p.spec0};
   timed("invert_scan", st, [&] {
@@ -601,7 +601,7 @@ int msa_decode(const msa_shape_t* shape, const void* q, const void* qp, const vo
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaGetLastError();
   unsigned* status = at<unsigned>(workspace, p.status);
-  cudaMemsetAsync(status, 0, sizeof(unsigned), st);
+  cudaMemsetAsync(status, 0, 32 * sizeof(unsigned), st);  // status, counters, wait place
   g_launches.fetch_add(3, std::memory_order_relaxed);  // scores, selection, attention
   launch_decode(d, q, qp, k_cache, v_cache, kp_cache, seq_len, block_idx, o, lse,
                 at<float>(workspace, p.scores), status, st);

@@ -187,8 +187,13 @@ def test_forward_is_bitwise_repeatable():
     the masked and the unmasked softmax path), so two runs give identical bits."""
     w = Workload("det", B=2, S=1536, Hq=16, Hkv=4, Hp=4, top_k=5)
     g = to_dev(make_inputs(w, 77))
-    runs = [msa.msa_forward(g["q"], g["k"], g["v"], g["qp"], g["kp"], w.top_k, w.scale)
-            for _ in range(3)]
+    shape = msa.make_shape(g["q"], g["k"], g["qp"], w.top_k, w.scale)
+    runs = []
+    for _ in range(3):
+        ws = msa.workspace(shape, msa.OP_FORWARD, DEV)
+        runs.append(msa.msa_forward(g["q"], g["k"], g["v"], g["qp"], g["kp"], w.top_k, w.scale,
+                                    ws=ws))
+        assert msa.msa_device_status(ws) == 0  # no bounded wait gave up
     for o, lse, idx in runs[1:]:
         assert torch.equal(idx, runs[0][2])
         assert torch.equal(o, runs[0][0])
