@@ -60,10 +60,11 @@ def load_library(path: str = LIB_PATH):
         lib.msa_workspace_size.argtypes = [SP, I]
         lib.msa_workspace_size.restype = Z
         lib.msa_forward.argtypes = [SP, P, P, P, P, P, P, I, P, P, P, Z, P]
-        lib.msa_backward.argtypes = [SP, P, P, P, P, P, P, P, P, P, F, P, P, P, P, P, P, P, Z, P]
+        lib.msa_backward.argtypes = [SP, P, P, P, P, P, P, P, P, P, F, P, P, P, P, P, P, P, P, Z,
+                                     P]
         lib.msa_warmup_forward.argtypes = [SP, P, P, P, P, P, P, Z, P]
-        lib.msa_warmup_backward.argtypes = [SP, P, P, P, P, P, P, P, P, F, P, P, P, P, P, P, P, Z,
-                                            P]
+        lib.msa_warmup_backward.argtypes = [SP, P, P, P, P, P, P, P, P, F, P, P, P, P, P, P, P, P,
+                                            Z, P]
         lib.msa_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint), P]
         lib.msa_decode.argtypes = [SP, P, P, P, P, P, P, P, P, P, P, Z, P]
         lib.msa_decode.restype = I
@@ -131,6 +132,44 @@ def msa_workspace_size(shape: Shape, op: int) -> int:
 def workspace(shape: Shape, op: int, device) -> torch.Tensor:
     """Fresh workspace (uint8 tensor, 256-byte aligned by the CUDA caching allocator)."""
     return torch.empty(msa_workspace_size(shape, op), dtype=torch.uint8, device=device)
+
+
+_WS_CACHE: dict = {}
+
+
+def cached_workspace(shape: Shape, op: int, device) -> torch.Tensor:
+    """Workspace kept per (device, current stream) and reused by later calls on that stream: the
+    stream orders each call after the previous one, and no call leaves state in it that a later
+    call reads.  Grows (never shrinks) to the largest size asked for; clear_workspace_cache()
+    releases it."""
+    device = torch.device(device)
+    key = (device.index if device.index is not None else torch.cuda.current_device(),
+           torch.cuda.current_stream(device).cuda_stream)
+    need = msa_workspace_size(shape, op)
+    ws = _WS_CACHE.get(key)
+    if ws is None or ws.numel() < need:
+        _WS_CACHE.pop(key, None)
+        ws = torch.empty(need, dtype=torch.uint8, device=device)
+        _WS_CACHE[key] = ws
+    return ws
+
+
+def clear_workspace_cache() -> None:
+    _WS_CACHE.clear()
+
+
+def _kl_grad_args(kl_grad, device):
+    """(host value, device pointer) for the library's kl_grad / kl_grad_dev pair: a number is
+    passed by value; a one-element fp32 tensor on the device is read by the kernel, so the host
+    never waits for it."""
+    if isinstance(kl_grad, torch.Tensor):
+        if kl_grad.numel() != 1:
+            raise MSAError(f"kl_grad must have one element, got shape {tuple(kl_grad.shape)}")
+        if kl_grad.device != torch.device(device):
+            raise MSAError(f"kl_grad is on {kl_grad.device}, the inputs on {device}")
+        t = kl_grad.detach().reshape(()).to(torch.float32).contiguous()
+        return 0.0, t
+    return float(kl_grad), None
 
 
 def msa_device_status(ws: torch.Tensor) -> int:
@@ -224,9 +263,10 @@ def msa_forward_noalloc_status(device=None) -> int:
 
 
 def msa_backward(q, k, v, qp, kp, o, lse, dout, block_idx, top_k: int, scale: float,
-                 kl_grad: float = 1.0, ws=None, return_kl: bool = False):
+                 kl_grad=1.0, ws=None, return_kl: bool = False):
     """Sparse backward.  Returns (dq, dk, dv, dqp, dkp), plus the KL value L_KL as a 0-d fp32
-    CUDA tensor when return_kl (computed on the device; no host synchronisation)."""
+    CUDA tensor when return_kl (computed on the device; no host synchronisation).  kl_grad: a
+    number, or a one-element tensor on the device (read by the kernel)."""
     B, S, Hq, D = q.shape
     Hp = qp.shape[2]
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (qp, "qp"), (kp, "kp"), (o, "o"), (dout, "dout")):
@@ -236,11 +276,12 @@ def msa_backward(q, k, v, qp, kp, o, lse, dout, block_idx, top_k: int, scale: fl
     shape = make_shape(q, k, qp, top_k, scale)
     grads = [torch.empty_like(x) for x in (q, k, v, qp, kp)]
     kl = torch.empty((), dtype=torch.float32, device=q.device) if return_kl else None
+    klg, klg_dev = _kl_grad_args(kl_grad, q.device)
     if ws is None:
         ws = workspace(shape, OP_BACKWARD, q.device)
     _check(load_library().msa_backward(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(qp),
                                        _ptr(kp), _ptr(o), _ptr(lse), _ptr(dout), _ptr(block_idx),
-                                       float(kl_grad), *map(_ptr, grads), _ptr(kl), _ptr(ws),
+                                       klg, _ptr(klg_dev), *map(_ptr, grads), _ptr(kl), _ptr(ws),
                                        ws.numel(), _stream(q.device)), "msa_backward")
     return tuple(grads) + ((kl,) if return_kl else ())
 
@@ -285,10 +326,10 @@ def msa_warmup_forward(q, k, v, scale: float, ws=None):
     return o, lse
 
 
-def msa_warmup_backward(q, k, v, qp, kp, o, lse, dout, scale: float, kl_grad: float = 1.0,
+def msa_warmup_backward(q, k, v, qp, kp, o, lse, dout, scale: float, kl_grad=1.0,
                         ws=None, return_kl: bool = False):
     """Dense warmup backward (proxy KL over the full causal prefix).  Returns grads (and the KL
-    value as a 0-d fp32 CUDA tensor when return_kl)."""
+    value as a 0-d fp32 CUDA tensor when return_kl).  kl_grad as in msa_backward."""
     B, S, Hq, D = q.shape
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (qp, "qp"), (kp, "kp"), (o, "o"), (dout, "dout")):
         _req(t, n)
@@ -296,11 +337,12 @@ def msa_warmup_backward(q, k, v, qp, kp, o, lse, dout, scale: float, kl_grad: fl
     shape = make_shape(q, k, qp, 0, scale)
     grads = [torch.empty_like(x) for x in (q, k, v, qp, kp)]
     kl = torch.empty((), dtype=torch.float32, device=q.device) if return_kl else None
+    klg, klg_dev = _kl_grad_args(kl_grad, q.device)
     if ws is None:
         ws = workspace(shape, OP_WARMUP_BACKWARD, q.device)
     _check(load_library().msa_warmup_backward(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v),
                                               _ptr(qp), _ptr(kp), _ptr(o), _ptr(lse), _ptr(dout),
-                                              float(kl_grad), *map(_ptr, grads), _ptr(kl),
+                                              klg, _ptr(klg_dev), *map(_ptr, grads), _ptr(kl),
                                               _ptr(ws), ws.numel(), _stream(q.device)),
            "msa_warmup_backward")
     return tuple(grads) + ((kl,) if return_kl else ())
@@ -311,10 +353,14 @@ class _MSAFunction(torch.autograd.Function):
     def forward(ctx, qp, kp, q, k, v, top_k, scale, warmup):
         qp, kp, q, k, v = (x.contiguous() for x in (qp, kp, q, k, v))
         if warmup:
-            o, lse = msa_warmup_forward(q, k, v, scale)
+            o, lse = msa_warmup_forward(
+                q, k, v, scale,
+                ws=cached_workspace(make_shape(q, k, None, 0, scale), OP_WARMUP_FORWARD, q.device))
             idx = None
         else:
-            o, lse, idx = msa_forward(q, k, v, qp, kp, top_k, scale)
+            o, lse, idx = msa_forward(
+                q, k, v, qp, kp, top_k, scale,
+                ws=cached_workspace(make_shape(q, k, qp, top_k, scale), OP_FORWARD, q.device))
         ctx.save_for_backward(qp, kp, q, k, v, o, lse, *(() if idx is None else (idx,)))
         ctx.top_k, ctx.scale, ctx.warmup = top_k, scale, warmup
         kl = torch.zeros((), dtype=torch.float32, device=q.device)
@@ -324,14 +370,17 @@ class _MSAFunction(torch.autograd.Function):
     def backward(ctx, do, dkl):
         saved = ctx.saved_tensors
         qp, kp, q, k, v, o, lse = saved[:7]
-        kl_grad = 0.0 if dkl is None else float(dkl)
+        kl_grad = 0.0 if dkl is None else dkl  # a device tensor: read by the kernel, no sync
         do = torch.zeros_like(o) if do is None else do.contiguous()
         if ctx.warmup:
+            ws = cached_workspace(make_shape(q, k, qp, 0, ctx.scale), OP_WARMUP_BACKWARD, q.device)
             dq, dk, dv, dqp, dkp = msa_warmup_backward(q, k, v, qp, kp, o, lse, do, ctx.scale,
-                                                       kl_grad)
+                                                       kl_grad, ws=ws)
         else:
+            ws = cached_workspace(make_shape(q, k, qp, ctx.top_k, ctx.scale), OP_BACKWARD,
+                                  q.device)
             dq, dk, dv, dqp, dkp = msa_backward(q, k, v, qp, kp, o, lse, do, saved[7], ctx.top_k,
-                                                ctx.scale, kl_grad)
+                                                ctx.scale, kl_grad, ws=ws)
         return dqp, dkp, dq, dk, dv, None, None, None
 
 

@@ -102,8 +102,9 @@ def cp_forward(q, k, v, qp, kp, top_k: int, scale: float, group=None, local_forw
                    scale=scale)
 
 
-def cp_backward(state, dout, kl_grad: float = 1.0, group=None, local_backward=None):
-    """Backward on sequence shards: dout [B, S/N, Hq, D] -> (dq, dk, dv, dqp, dkp) shards."""
+def cp_backward(state, dout, kl_grad=1.0, group=None, local_backward=None):
+    """Backward on sequence shards: dout [B, S/N, Hq, D] -> (dq, dk, dv, dqp, dkp) shards.
+    kl_grad: a number or a one-element tensor (kept on its device)."""
     n, _ = _world(group)
     bwd = local_backward or _default_backward
     douth = seq_to_head(dout, group)
@@ -125,7 +126,7 @@ class _CPFunction(torch.autograd.Function):
 
     @staticmethod
     def backward(ctx, do, dkl):
-        kl_grad = 0.0 if dkl is None else float(dkl)
+        kl_grad = 0.0 if dkl is None else dkl  # stays on the device: no host sync
         shape, dtype, device = ctx.o_meta
         do = torch.zeros(shape, dtype=dtype, device=device) if do is None else do.contiguous()
         dq, dk, dv, dqp, dkp = cp_backward(ctx.state, do, kl_grad, ctx.group)

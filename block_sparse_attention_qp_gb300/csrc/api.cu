@@ -293,9 +293,10 @@ T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
 }
 
-int check_kl(const float* kl_out) {
-  if (reinterpret_cast<uintptr_t>(kl_out) % 4 != 0) {
-    set_err("kl_out must be 4-byte aligned");
+// msg names the argument: a float pointer that must be 4-byte aligned.
+int check_kl(const float* ptr, const char* msg) {
+  if (reinterpret_cast<uintptr_t>(ptr) % 4 != 0) {
+    set_err(msg);
     return MSA_ERR_INVALID_ARG;
   }
   return MSA_OK;
@@ -427,14 +428,15 @@ int msa_forward(const msa_shape_t* shape, const void* q, const void* k, const vo
 
 int msa_backward(const msa_shape_t* shape, const void* q, const void* k, const void* v,
                  const void* qp, const void* kp, const void* o, const float* lse,
-                 const void* dout, const int32_t* block_idx, float kl_grad, void* dq, void* dk,
-                 void* dv, void* dqp, void* dkp, float* kl_out, void* workspace,
-                 size_t workspace_bytes, void* stream) {
+                 const void* dout, const int32_t* block_idx, float kl_grad,
+                 const float* kl_grad_dev, void* dq, void* dk, void* dv, void* dqp, void* dkp,
+                 float* kl_out, void* workspace, size_t workspace_bytes, void* stream) {
   Dims d;
   int rc = check_shape(shape, MSA_OP_BACKWARD, &d);
   if (rc) return rc;
   if ((rc = check_ptrs({q, k, v, qp, kp, o, lse, dout, block_idx, dq, dk, dv, dqp, dkp}))) return rc;
-  if (kl_out && (rc = check_kl(kl_out))) return rc;
+  if (kl_out && (rc = check_kl(kl_out, "kl_out must be 4-byte aligned"))) return rc;
+  if (kl_grad_dev && (rc = check_kl(kl_grad_dev, "kl_grad_dev must be 4-byte aligned"))) return rc;
   const Plan p = make_plan(d, MSA_OP_BACKWARD);
   if ((rc = check_ws(p, workspace, workspace_bytes))) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -482,7 +484,8 @@ int msa_backward(const msa_shape_t* shape, const void* q, const void* k, const v
   if (ok)
     timed("proxy_bwd", st, [&] {
       ok = launch_proxy_bwd(d, false, qp, kp, at<float>(workspace, p.lpxe),
-                            at<void>(workspace, p.pbar), kl_grad, at<int>(workspace, p.seg_offset),
+                            at<void>(workspace, p.pbar), kl_grad, kl_grad_dev,
+                            at<int>(workspace, p.seg_offset),
                             at<int>(workspace, p.entries), at<Item>(workspace, p.items1),
                             at<int>(workspace, p.totals) + 2, p.max1, at<float>(workspace, p.dqp),
                             at<float>(workspace, p.dkp), kl_acc, at<unsigned>(workspace, p.status),
@@ -522,14 +525,15 @@ int msa_warmup_forward(const msa_shape_t* shape, const void* q, const void* k, c
 
 int msa_warmup_backward(const msa_shape_t* shape, const void* q, const void* k, const void* v,
                         const void* qp, const void* kp, const void* o, const float* lse,
-                        const void* dout, float kl_grad, void* dq, void* dk, void* dv, void* dqp,
-                        void* dkp, float* kl_out, void* workspace, size_t workspace_bytes,
-                        void* stream) {
+                        const void* dout, float kl_grad, const float* kl_grad_dev, void* dq,
+                        void* dk, void* dv, void* dqp, void* dkp, float* kl_out, void* workspace,
+                        size_t workspace_bytes, void* stream) {
   Dims d;
   int rc = check_shape(shape, MSA_OP_WARMUP_BACKWARD, &d);
   if (rc) return rc;
   if ((rc = check_ptrs({q, k, v, qp, kp, o, lse, dout, dq, dk, dv, dqp, dkp}))) return rc;
-  if (kl_out && (rc = check_kl(kl_out))) return rc;
+  if (kl_out && (rc = check_kl(kl_out, "kl_out must be 4-byte aligned"))) return rc;
+  if (kl_grad_dev && (rc = check_kl(kl_grad_dev, "kl_grad_dev must be 4-byte aligned"))) return rc;
   const Plan p = make_plan(d, MSA_OP_WARMUP_BACKWARD);
   if ((rc = check_ws(p, workspace, workspace_bytes))) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -574,7 +578,8 @@ int msa_warmup_backward(const msa_shape_t* shape, const void* q, const void* k, 
   if (ok)
     timed("proxy_bwd_dense", st, [&] {
       ok = launch_proxy_bwd(d, true, qp, kp, at<float>(workspace, p.lpxe),
-                            at<void>(workspace, p.pbar), kl_grad, at<int>(workspace, p.seg_offset),
+                            at<void>(workspace, p.pbar), kl_grad, kl_grad_dev,
+                            at<int>(workspace, p.seg_offset),
                             nullptr, at<Item>(workspace, p.items0), at<int>(workspace, p.totals) + 1,
                             p.max0, at<float>(workspace, p.dqp), at<float>(workspace, p.dkp),
                             kl_acc, status, st);

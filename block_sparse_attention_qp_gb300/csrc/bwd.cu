@@ -129,7 +129,8 @@ struct ProxyArgs {
   const bf16* qp;
   const float* lpxe;   // per list entry: LSE_px x log2 e
   const __half* pbar;  // per list entry: teacher row [128 keys] (fp16)
-  float cz;  // kl_grad / (B * S * Hp)
+  float cz;          // kl_grad / (B * S * Hp), or 1 / (B * S * Hp) when czp is set
+  const float* czp;  // NULL, or the device-resident kl_grad that multiplies cz
   const int* seg_offset;
   const int* entries;
   const Item* items;
@@ -1186,6 +1187,7 @@ __global__ void __launch_bounds__(384, 1)
 
   const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
   const float sl2 = d.scale * kLog2e;
+  const float cz = A.czp ? A.cz * __ldg(A.czp) : A.cz;
   long long total = *A.n_items;
   if (total > A.max_items) total = A.max_items;
   if (tid == 0) {
@@ -1452,7 +1454,7 @@ __global__ void __launch_bounds__(384, 1)
         fence_after_sync();
         const __half* pbr = sPb + pbi * kPG * kBlock;
         const uint32_t adzb = adz + bb * kST;
-        const float2 sl2x2 = make_float2(sl2, sl2), cz2 = make_float2(A.cz, A.cz);
+        const float2 sl2x2 = make_float2(sl2, sl2), cz2 = make_float2(cz, cz);
 #pragma unroll 1
         for (int h16 = 0; h16 < kPG / 16; ++h16) {  // 16 tokens (two 16-byte chunks of dz^T) at a time
           uint32_t zr[16], zw[8];
@@ -1671,7 +1673,8 @@ bool launch_attn_bwd(const Dims& d, bool dense, const void* q, const void* k, co
 }
 
 bool launch_proxy_bwd(const Dims& d, bool dense, const void* qp, const void* kp,
-                      const float* lpxe, const void* pbar, float kl_grad, const int* seg_offset,
+                      const float* lpxe, const void* pbar, float kl_grad,
+                      const float* kl_grad_dev, const int* seg_offset,
                       const int* entries, const Item* items, const int* n_items,
                       long long max_items, float* dqp_acc, float* dkp_acc, double* kl_acc,
                       unsigned* status, cudaStream_t st) {
@@ -1685,7 +1688,9 @@ bool launch_proxy_bwd(const Dims& d, bool dense, const void* qp, const void* kp,
   a.qp = (const bf16*)qp;
   a.lpxe = lpxe;
   a.pbar = static_cast<const __half*>(pbar);
-  a.cz = (float)((double)kl_grad / ((double)d.B * d.S * d.Hp));
+  const double inv_n = 1.0 / ((double)d.B * d.S * d.Hp);
+  a.cz = (float)(kl_grad_dev ? inv_n : (double)kl_grad * inv_n);
+  a.czp = kl_grad_dev;
   a.seg_offset = seg_offset;
   a.entries = entries;
   a.items = items;

@@ -106,11 +106,13 @@ bool launch_attn_bwd(const Dims& d, bool dense, const void* q, const void* k, co
                      const int* entries, const Item* items, const int* n_items, long long max_items,
                      float* dq_acc, float* dk_acc, float* dv_acc, void* pbar, unsigned* status,
                      cudaStream_t st);
-// Proxy gradients (dQp, dKp into fp32 accumulators) of the KL term from pbar.  kl_acc: NULL, or
+// Proxy gradients (dQp, dKp into fp32 accumulators) of the KL term from pbar, scaled by kl_grad,
+// or by *kl_grad_dev (read on the device) when that is not NULL.  kl_acc: NULL, or
 // a zeroed double that receives sum over the visited (token, key) pairs of
 // pbar (ln pbar - ln p_student), i.e. B S Hp times the KL value.
 bool launch_proxy_bwd(const Dims& d, bool dense, const void* qp, const void* kp,
-                      const float* lpxe, const void* pbar, float kl_grad, const int* seg_offset,
+                      const float* lpxe, const void* pbar, float kl_grad,
+                      const float* kl_grad_dev, const int* seg_offset,
                       const int* entries, const Item* items, const int* n_items,
                       long long max_items, float* dqp_acc, float* dkp_acc, double* kl_acc,
                       unsigned* status, cudaStream_t st);

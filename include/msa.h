@@ -120,6 +120,9 @@ MSA_API int msa_forward(const msa_shape_t* shape, const void* q, const void* k, 
  *               kl_grad / (B*S*Hp) * (p_student - p_teacher)  (blog, "KL Divergence Loss").
  * o and lse are the outputs of msa_forward for the same inputs.  kl_grad is the incoming
  * gradient of the (zero) KL placeholder the forward returns (package usage note), usually 1.
+ * kl_grad_dev: NULL, or a device pointer to one float that is used instead of kl_grad, read by
+ * the kernel (an autograd backward can pass the placeholder's incoming gradient tensor without a
+ * host synchronisation).
  * kl_out: NULL, or a device pointer to one float that receives the KL value L_KL itself (not
  * scaled by kl_grad).  The gradients never need it (blog, "KL Divergence Loss": the proxy
  * gradient is p_student - p_teacher), so it is computed only on request -- for logging every n
@@ -129,9 +132,9 @@ MSA_API int msa_forward(const msa_shape_t* shape, const void* q, const void* k, 
  */
 MSA_API int msa_backward(const msa_shape_t* shape, const void* q, const void* k, const void* v,
                  const void* qp, const void* kp, const void* o, const float* lse,
-                 const void* dout, const int32_t* block_idx, float kl_grad, void* dq, void* dk,
-                 void* dv, void* dqp, void* dkp, float* kl_out, void* workspace,
-                 size_t workspace_bytes, void* stream);
+                 const void* dout, const int32_t* block_idx, float kl_grad,
+                 const float* kl_grad_dev, void* dq, void* dk, void* dv, void* dqp, void* dkp,
+                 float* kl_out, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Warmup forward (blog, "Warmup kernels"): dense causal GQA attention, no proxy pass.
@@ -144,13 +147,13 @@ MSA_API int msa_warmup_forward(const msa_shape_t* shape, const void* q, const vo
 /*
  * Warmup backward (blog, "Warmup kernels"): the proxy normaliser over the full causal prefix,
  * then the fused main + proxy backward with every visible key in the key set.  Same outputs
- * (kl_out included) and KL definition as msa_backward.  top_k is ignored.
+ * (kl_grad_dev and kl_out included) and KL definition as msa_backward.  top_k is ignored.
  */
 MSA_API int msa_warmup_backward(const msa_shape_t* shape, const void* q, const void* k, const void* v,
                         const void* qp, const void* kp, const void* o, const float* lse,
-                        const void* dout, float kl_grad, void* dq, void* dk, void* dv, void* dqp,
-                        void* dkp, float* kl_out, void* workspace, size_t workspace_bytes,
-                        void* stream);
+                        const void* dout, float kl_grad, const float* kl_grad_dev, void* dq,
+                        void* dk, void* dv, void* dqp, void* dkp, float* kl_out, void* workspace,
+                        size_t workspace_bytes, void* stream);
 
 /*
  * Decode step of MSA inference (forum summary, "GPU kernel co-design", deployment setting

@@ -92,3 +92,36 @@ def test_selftest_rejects_bad_arguments_on_the_host(lib):
     assert lib.msa_selftest_wait_timeout(P(0x1000), 0, P(0)) == 1  # limit out of range
     assert lib.msa_selftest_wait_timeout(P(0x1000), 2_000_000, P(0)) == 1
     assert b"limit_us" in lib.msa_last_error()
+
+
+def declared_arity():
+    """Parameter count of every msa_* prototype in include/."""
+    out = {}
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            for name, params in re.findall(r"^MSA_API\s+[\w\s\*]+?\b(msa_\w+)\s*\(([^)]*)\)",
+                                           text, flags=re.M):
+                params = params.strip()
+                out[name] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_argument_lists_match_the_header(lib):
+    for name, n in declared_arity().items():
+        argtypes = getattr(lib, name).argtypes
+        if argtypes is not None:
+            assert len(argtypes) == n, f"{name}: header has {n} parameters, binding {len(argtypes)}"
+
+
+def test_backward_rejects_a_misaligned_kl_grad_pointer(lib):
+    s = binding.Shape(1, 256, 8, 2, 2, 128, 2, 0.1)
+    P = ctypes.c_void_p
+    a = P(0x10000)  # aligned and never dereferenced: the call fails on the host first
+    odd = P(0x10002)
+    rc = lib.msa_backward(ctypes.byref(s), a, a, a, a, a, a, a, a, a, 1.0, odd, a, a, a, a, a,
+                          P(0), a, 1 << 30, P(0))
+    assert rc == 1 and b"kl_grad_dev" in lib.msa_last_error()
+    rc = lib.msa_warmup_backward(ctypes.byref(s), a, a, a, a, a, a, a, a, 1.0, odd, a, a, a, a, a,
+                                 P(0), a, 1 << 30, P(0))
+    assert rc == 1 and b"kl_grad_dev" in lib.msa_last_error()

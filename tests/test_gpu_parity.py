@@ -260,7 +260,7 @@ def test_autograd_function_matches_direct_calls():
     g = to_dev(make_inputs(w, 11))
     leaves = {n: g[n].clone().requires_grad_(True) for n in ("qp", "kp", "q", "k", "v")}
     out, kl = msa.msa_func(leaves["qp"], leaves["kp"], leaves["q"], leaves["k"], leaves["v"], 3, w.scale)
-    assert float(kl) == 0.0
+    assert float(kl.detach()) == 0.0
     ((out.float() * g["dout"].float()).sum() + 1.5 * kl).backward()
     o, lse, idx = msa.msa_forward(g["q"], g["k"], g["v"], g["qp"], g["kp"], 3, w.scale)
     ref = msa.msa_backward(g["q"], g["k"], g["v"], g["qp"], g["kp"], o, lse, g["dout"], idx, 3,
@@ -268,6 +268,55 @@ def test_autograd_function_matches_direct_calls():
     close("O", out, o.float(), rel=1e-5, atol=2e-3, ulps=1.0)  # equal up to fp32 summation order
     for name, r in zip(("q", "k", "v", "qp", "kp"), ref):
         close("d" + name, leaves[name].grad, r.float(), rel=1e-2, ulps=1.5)
+
+
+def test_kl_grad_from_a_device_tensor_matches_the_host_value():
+    w = Workload("klgd", B=1, S=512, Hq=8, Hkv=2, Hp=2, top_k=3)
+    g = to_dev(make_inputs(w, 12))
+    o, lse, idx = msa.msa_forward(g["q"], g["k"], g["v"], g["qp"], g["kp"], 3, w.scale)
+    host = msa.msa_backward(g["q"], g["k"], g["v"], g["qp"], g["kp"], o, lse, g["dout"], idx, 3,
+                            w.scale, kl_grad=0.625)
+    dev = msa.msa_backward(g["q"], g["k"], g["v"], g["qp"], g["kp"], o, lse, g["dout"], idx, 3,
+                           w.scale, kl_grad=torch.tensor(0.625, device=DEV))
+    # equal up to the order of the fp32 reductions into the gradients (and 0.625/N against
+    # 0.625*(1/N) in the proxy ones): at most a bf16 ulp apart
+    for name, a, b in zip(("dq", "dk", "dv", "dqp", "dkp"), host, dev):
+        close(name, b, a.float(), rel=1e-3, atol=1e-6, ulps=1.0)
+    wh = msa.msa_warmup_backward(g["q"], g["k"], g["v"], g["qp"], g["kp"], o, lse, g["dout"],
+                                 w.scale, kl_grad=0.0)
+    wd = msa.msa_warmup_backward(g["q"], g["k"], g["v"], g["qp"], g["kp"], o, lse, g["dout"],
+                                 w.scale, kl_grad=torch.zeros((), device=DEV))
+    for name, a, b in zip(("dq", "dk", "dv", "dqp", "dkp"), wh, wd):
+        close("warmup " + name, b, a.float(), rel=1e-3, atol=1e-6, ulps=1.0)
+    assert float(host[3].abs().max()) > 0  # kl_grad 0.625: the proxy gradients are live
+    assert float(wd[3].abs().max()) == 0 and float(wd[4].abs().max()) == 0  # kl_grad 0 on the device
+
+
+def test_autograd_backward_never_waits_on_the_host_and_reuses_its_workspace():
+    """The placeholder's incoming gradient stays on the device (torch raises on a synchronising
+    call in sync-debug "error" mode), and a second, larger call on the same stream grows the
+    cached workspace and still matches the direct calls."""
+    msa.clear_workspace_cache()
+    for S, seed in ((512, 21), (1024, 22), (512, 23)):
+        w = Workload("agc", B=1, S=S, Hq=8, Hkv=2, Hp=2, top_k=3)
+        g = to_dev(make_inputs(w, seed))
+        leaves = {n: g[n].clone().requires_grad_(True) for n in ("qp", "kp", "q", "k", "v")}
+        out, kl = msa.msa_func(leaves["qp"], leaves["kp"], leaves["q"], leaves["k"], leaves["v"],
+                               3, w.scale)
+        loss = (out.float() * g["dout"].float()).sum() + 0.5 * kl
+        torch.cuda.set_sync_debug_mode("error")
+        try:
+            loss.backward()
+        finally:
+            torch.cuda.set_sync_debug_mode("default")
+        o, lse, idx = msa.msa_forward(g["q"], g["k"], g["v"], g["qp"], g["kp"], 3, w.scale)
+        ref = msa.msa_backward(g["q"], g["k"], g["v"], g["qp"], g["kp"], o, lse, g["dout"], idx,
+                               3, w.scale, kl_grad=0.5)
+        close("O", out, o.float(), rel=1e-5, atol=2e-3, ulps=1.0)
+        for name, r in zip(("q", "k", "v", "qp", "kp"), ref):
+            close("d" + name, leaves[name].grad, r.float(), rel=1e-2, ulps=1.5)
+    assert len(msa._WS_CACHE) == 1
+    msa.clear_workspace_cache()
 
 
 @pytest.mark.parametrize("G,S", [(2, 768), (4, 1280), (8, 896)])
