@@ -1,5 +1,7 @@
 // C ABI of libmsa.so (declared in include/msa.h): argument validation, workspace carving and
-// the launch sequence of every entry point.  All work is queued on the caller's stream.
+// the launch sequence of every entry point.  All work is ordered on the caller's stream; the
+// backward runs two pieces of independent HBM-bound work on a side stream that it forks from and
+// joins back into the caller's stream (see Branch).
 #include <stdio.h>
 #include <string.h>
 
@@ -66,6 +68,68 @@ void timed(const char* name, cudaStream_t st, F&& launch) {
   cudaEventRecord(r.b, st);
   g_prof.push_back(r);
 }
+
+// ---- a second stream for work that does not depend on the work queued beside it
+// One per host thread and device, made on first use and kept for the life of the process.
+struct Side {
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork_ev = nullptr, join_ev = nullptr;
+  bool ready = false, failed = false;
+};
+
+Side* side_stream() {
+  constexpr int kMaxDev = 64;
+  thread_local Side sides[kMaxDev];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  Side& x = sides[dev];
+  if (!x.ready && !x.failed) {
+    if (cudaStreamCreateWithFlags(&x.s, cudaStreamNonBlocking) == cudaSuccess &&
+        cudaEventCreateWithFlags(&x.fork_ev, cudaEventDisableTiming) == cudaSuccess &&
+        cudaEventCreateWithFlags(&x.join_ev, cudaEventDisableTiming) == cudaSuccess) {
+      x.ready = true;
+    } else {
+      x.failed = true;
+      cudaGetLastError();
+    }
+  }
+  return x.ready ? &x : nullptr;
+}
+
+// A branch off the caller's stream: on construction the side stream waits for everything queued
+// on the caller's stream so far; work queued on aux() then runs beside what the caller's stream
+// does next, until join() (or the destructor, on every return path) puts the caller's stream
+// behind it.  A call therefore stays ordered as a whole on the caller's stream, and a CUDA graph
+// capture of it stays closed.  At most one branch is open at a time per host thread.  Without a
+// side stream (its creation failed) aux() is the caller's stream and the work runs in order.
+class Branch {
+ public:
+  explicit Branch(cudaStream_t main) : main_(main), side_(side_stream()) {
+    if (side_) {
+      cudaEventRecord(side_->fork_ev, main_);
+      cudaStreamWaitEvent(side_->s, side_->fork_ev, 0);
+    }
+  }
+  Branch(const Branch&) = delete;
+  Branch& operator=(const Branch&) = delete;
+  ~Branch() { join(); }
+  cudaStream_t aux() const { return side_ ? side_->s : main_; }
+  void join() {
+    if (side_ && !joined_) {
+      cudaEventRecord(side_->join_ev, side_->s);
+      cudaStreamWaitEvent(main_, side_->join_ev, 0);
+    }
+    joined_ = true;
+  }
+
+ private:
+  cudaStream_t main_;
+  Side* side_;
+  bool joined_ = false;
+};
 
 constexpr size_t kAlign = 256;
 
@@ -356,11 +420,15 @@ void zero_grads(const Dims& d, const Plan& p, void* ws, cudaStream_t st) {
   cudaMemsetAsync(at<char>(ws, p.dkp), 0, (size_t)d.B * d.S * kD * sizeof(float), st);
 }
 
-void emit_grads(const Dims& d, const Plan& p, void* ws, void* dq, void* dk, void* dv, void* dqp,
-                void* dkp, cudaStream_t st) {
+// The bf16 gradients from their fp32 accumulators: the main-attention ones (dQ, dK, dV) ...
+void emit_main_grads(const Dims& d, const Plan& p, void* ws, void* dq, void* dk, void* dv,
+                     cudaStream_t st) {
   timed("grad_convert", st, [&] { launch_convert(at<float>(ws, p.dq), dq, (long long)d.B * d.S * d.Hq * kD, st); });
   timed("grad_convert", st, [&] { launch_convert(at<float>(ws, p.dk), dk, (long long)d.B * d.S * d.Hkv * kD, st); });
   timed("grad_convert", st, [&] { launch_convert(at<float>(ws, p.dv), dv, (long long)d.B * d.S * d.Hkv * kD, st); });
+}
+// ... and the proxy ones (dQp, dKp)
+void emit_proxy_grads(const Dims& d, const Plan& p, void* ws, void* dqp, void* dkp, cudaStream_t st) {
   timed("grad_convert", st, [&] { launch_convert(at<float>(ws, p.dqp), dqp, (long long)d.B * d.S * d.Hp * kD, st); });
   timed("grad_convert", st, [&] { launch_convert(at<float>(ws, p.dkp), dkp, (long long)d.B * d.S * kD, st); });
 }
@@ -442,9 +510,14 @@ int msa_backward(const msa_shape_t* shape, const void* q, const void* k, const v
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaGetLastError();
   cudaMemsetAsync(at<char>(workspace, p.status), 0, 32 * sizeof(unsigned), st);  // status, counters, wait place
-  zero_grads(d, p, workspace, st);
+  // beside the list building and the proxy normaliser: zeroing the gradient accumulators and
+  // the row data D (both HBM-bound)
+  Branch pre(st);
+  zero_grads(d, p, workspace, pre.aux());
+  timed("bwd_rowdot", pre.aux(), [&] {
+    launch_bwd_rowdot(d, o, dout, lse, at<float2>(workspace, p.rowm), pre.aux());
+  });
   build_lists(d, p, block_idx, workspace, 2, st);
-  timed("bwd_rowdot", st, [&] { launch_bwd_rowdot(d, o, dout, lse, at<float2>(workspace, p.rowm), st); });
   // partial normalisers of slots no list entry reaches stay NaN (all-ones bytes)
   cudaMemsetAsync(at<float>(workspace, p.lpx_part), 0xff,
                   (size_t)d.B * d.S * d.Hp * d.top_k * sizeof(float), st);
@@ -463,6 +536,7 @@ int msa_backward(const msa_shape_t* shape, const void* q, const void* k, const v
   timed("proxy_lse_combine", st, [&] {
     launch_proxy_lse_combine(d, at<float>(workspace, p.lpx_part), at<float>(workspace, p.lse_px), st);
   });
+  pre.join();
   timed("entry_meta", st, [&] {
     launch_entry_meta(d, false, at<int>(workspace, p.seg_count), at<int>(workspace, p.seg_offset),
                       at<int>(workspace, p.entries), at<float>(workspace, p.lse_px),
@@ -480,6 +554,9 @@ int msa_backward(const msa_shape_t* shape, const void* q, const void* k, const v
                          at<float>(workspace, p.dv), at<void>(workspace, p.pbar),
                          at<unsigned>(workspace, p.status), st);
   });
+  // dQ, dK, dV are final: their conversion runs beside the proxy backward
+  Branch post(st);
+  if (ok) emit_main_grads(d, p, workspace, dq, dk, dv, post.aux());
   double* kl_acc = kl_out ? kl_accumulator(workspace, p, st) : nullptr;
   if (ok)
     timed("proxy_bwd", st, [&] {
@@ -496,7 +573,8 @@ int msa_backward(const msa_shape_t* shape, const void* q, const void* k, const v
     return MSA_ERR_CUDA;
   }
   if (kl_out) timed("kl_finalize", st, [&] { launch_kl_finalize(d, kl_acc, kl_out, st); });
-  emit_grads(d, p, workspace, dq, dk, dv, dqp, dkp, st);
+  emit_proxy_grads(d, p, workspace, dqp, dkp, st);
+  post.join();
   return cuda_fail("msa_backward");
 }
 
@@ -540,7 +618,11 @@ int msa_warmup_backward(const msa_shape_t* shape, const void* q, const void* k, 
   cudaGetLastError();
   unsigned* status = at<unsigned>(workspace, p.status);
   cudaMemsetAsync(status, 0, 32 * sizeof(unsigned), st);  // status, counters, wait place
-  zero_grads(d, p, workspace, st);
+  Branch pre(st);  // as in msa_backward
+  zero_grads(d, p, workspace, pre.aux());
+  timed("bwd_rowdot", pre.aux(), [&] {
+    launch_bwd_rowdot(d, o, dout, lse, at<float2>(workspace, p.rowm), pre.aux());
+  });
   const ItemSpec specs[1] = {p.spec0};
   timed("invert_scan", st, [&] {
     launch_scan(d, true, nullptr, at<int>(workspace, p.seg_offset), specs, 1,
@@ -550,7 +632,6 @@ int msa_warmup_backward(const msa_shape_t* shape, const void* q, const void* k, 
     launch_items(d, true, nullptr, at<int>(workspace, p.seg_offset), p.spec0, at<int>(workspace, p.io0),
                  at<Item>(workspace, p.items0), p.max0, status, st);
   });
-  timed("bwd_rowdot", st, [&] { launch_bwd_rowdot(d, o, dout, lse, at<float2>(workspace, p.rowm), st); });
   bool lok = true;
   timed("proxy_lse_dense", st, [&] {
     lok = launch_proxy_lse_dense(d, qp, kp, at<float>(workspace, p.lse_px), status, st);
@@ -559,6 +640,7 @@ int msa_warmup_backward(const msa_shape_t* shape, const void* q, const void* k, 
     set_err("msa_warmup_backward: could not create TMA tensor maps (cuTensorMapEncodeTiled)");
     return MSA_ERR_CUDA;
   }
+  pre.join();
   timed("entry_meta", st, [&] {
     launch_entry_meta(d, true, nullptr, at<int>(workspace, p.seg_offset), nullptr,
                       at<float>(workspace, p.lse_px), at<float2>(workspace, p.rowm),
@@ -574,6 +656,8 @@ int msa_warmup_backward(const msa_shape_t* shape, const void* q, const void* k, 
                          at<float>(workspace, p.dk), at<float>(workspace, p.dv),
                          at<void>(workspace, p.pbar), status, st);
   });
+  Branch post(st);
+  if (ok) emit_main_grads(d, p, workspace, dq, dk, dv, post.aux());
   double* kl_acc = kl_out ? kl_accumulator(workspace, p, st) : nullptr;
   if (ok)
     timed("proxy_bwd_dense", st, [&] {
@@ -589,7 +673,8 @@ int msa_warmup_backward(const msa_shape_t* shape, const void* q, const void* k, 
     return MSA_ERR_CUDA;
   }
   if (kl_out) timed("kl_finalize", st, [&] { launch_kl_finalize(d, kl_acc, kl_out, st); });
-  emit_grads(d, p, workspace, dq, dk, dv, dqp, dkp, st);
+  emit_proxy_grads(d, p, workspace, dqp, dkp, st);
+  post.join();
   return cuda_fail("msa_warmup_backward");
 }
 

@@ -31,10 +31,15 @@
  *   {4, 8, 16} for the backward ops (the warmup forward, which has no selection: Hq / Hkv).
  *   Other shapes return MSA_ERR_UNSUPPORTED.
  *   `workspace` is caller-owned device memory of at least msa_workspace_size() bytes for the
- *   same op and shape; the library allocates nothing.  The first 256 bytes hold a device status
+ *   same op and shape; the library allocates no device memory.  The first 256 bytes hold a device status
  *   word (see msa_device_status) and the work-item counters of the persistent kernels (reset on
  *   the stream before each launch).  Calls sharing one workspace must not overlap on the GPU.
- *   `stream` is a cudaStream_t (NULL = legacy default stream); all work is asynchronous on it.
+ *   `stream` is a cudaStream_t (NULL = legacy default stream); all work is asynchronous and
+ *   ordered on it.  The backward ops run two independent memory-bound steps (zeroing of their
+ *   accumulators with the row data D; the bf16 conversion of dQ, dK, dV) on a side stream that the
+ *   library creates once per host thread and device, forked from `stream` with an event and
+ *   joined back into it before the call returns: the call's work still completes in `stream`'s
+ *   order, and a CUDA graph capture of the call stays closed.
  *   Return value: an msa_status code.  Argument errors are detected on the host before any
  *   launch; MSA_ERR_CUDA reports a launch or runtime error (msa_last_error() gives the text).
  *   No entry point synchronises the device except msa_device_status.

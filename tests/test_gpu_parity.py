@@ -279,15 +279,15 @@ def test_kl_grad_from_a_device_tensor_matches_the_host_value():
     dev = msa.msa_backward(g["q"], g["k"], g["v"], g["qp"], g["kp"], o, lse, g["dout"], idx, 3,
                            w.scale, kl_grad=torch.tensor(0.625, device=DEV))
     # equal up to the order of the fp32 reductions into the gradients (and 0.625/N against
-    # 0.625*(1/N) in the proxy ones): at most a bf16 ulp apart
+    # 0.625*(1/N) in the proxy ones): a bf16 ulp apart, or 1e-4 where a sum nearly cancels
     for name, a, b in zip(("dq", "dk", "dv", "dqp", "dkp"), host, dev):
-        close(name, b, a.float(), rel=1e-3, atol=1e-6, ulps=1.0)
+        close(name, b, a.float(), rel=1e-3, atol=1e-4, ulps=1.0)
     wh = msa.msa_warmup_backward(g["q"], g["k"], g["v"], g["qp"], g["kp"], o, lse, g["dout"],
                                  w.scale, kl_grad=0.0)
     wd = msa.msa_warmup_backward(g["q"], g["k"], g["v"], g["qp"], g["kp"], o, lse, g["dout"],
                                  w.scale, kl_grad=torch.zeros((), device=DEV))
     for name, a, b in zip(("dq", "dk", "dv", "dqp", "dkp"), wh, wd):
-        close("warmup " + name, b, a.float(), rel=1e-3, atol=1e-6, ulps=1.0)
+        close("warmup " + name, b, a.float(), rel=1e-3, atol=1e-4, ulps=1.0)
     assert float(host[3].abs().max()) > 0  # kl_grad 0.625: the proxy gradients are live
     assert float(wd[3].abs().max()) == 0 and float(wd[4].abs().max()) == 0  # kl_grad 0 on the device
 
@@ -336,3 +336,40 @@ def test_warmup_forward_growing_row_maxima(G, S):
     o_ref, lse_ref = oracle.forward(x["q"], x["k"], x["v"], None, 1, w.scale)
     close("O", o, o_ref)
     close("LSE", lse, lse_ref, rel=1e-5, atol=1e-3, ulps=0.0)
+
+
+def test_training_step_replays_from_a_cuda_graph():
+    """One forward + backward captured in a CUDA graph (the backward forks onto the library's side
+    stream and joins back inside the capture) replays to the eager results."""
+    w = Workload("graph", B=1, S=1024, Hq=16, Hkv=2, Hp=2, top_k=4)
+    g = to_dev(make_inputs(w, 31))
+    shape = msa.make_shape(g["q"], g["k"], g["qp"], w.top_k, w.scale)
+    wsf = msa.workspace(shape, msa.OP_FORWARD, DEV)
+    wsb = msa.workspace(shape, msa.OP_BACKWARD, DEV)
+
+    def step():
+        o, lse, idx = msa.msa_forward(g["q"], g["k"], g["v"], g["qp"], g["kp"], w.top_k, w.scale,
+                                      ws=wsf)
+        grads = msa.msa_backward(g["q"], g["k"], g["v"], g["qp"], g["kp"], o, lse, g["dout"], idx,
+                                 w.top_k, w.scale, ws=wsb)
+        return (o, lse, idx) + tuple(grads)
+
+    eager = step()
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()  # warm-up on a non-default stream, as graph capture wants
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        captured = step()
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert msa.msa_device_status(wsf) == 0 and msa.msa_device_status(wsb) == 0
+    assert torch.equal(captured[2], eager[2])                  # selection
+    assert torch.equal(captured[0], eager[0]) and torch.equal(captured[1], eager[1])  # O, LSE
+    for name, a, b in zip(("dq", "dk", "dv", "dqp", "dkp"), captured[3:], eager[3:]):
+        close(name, a, b.float(), rel=1e-3, atol=1e-4, ulps=1.0)  # fp32 reduction order only
