@@ -878,16 +878,20 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           if (tl == 0 && ni > 0 && !wait1(9, &sh->acc_free, par(ni - 1))) { ok = false; break; }
           fence_after_sync();
           const bool acc = tl > 0;
+          // dK += dS^T Q and dV += P^T dO with dS^T and P^T read from tensor memory (rows 0-63 in
+          // columns 0-31 of DB / SB, rows 64-127 in columns 64-95), which spares the shared-memory
+          // path a 32 KB operand per tile; dK first, so that the dV products separate its reads
+          // of DB from the dQ^T product that overwrites DB
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks)  // dV += P^T dO  (P^T from tensor memory: rows 0-63 in
-            // columns 0-31, rows 64-127 in columns 64-95)
+          for (int ks = 0; ks < 8; ++ks)
+            mma_ts(RK, DB + ks * 8 + (ks >= 4 ? 32 : 0), desc_mnmajor(aQb, kTW, ks), id_g,
+                   acc || ks > 0);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
             mma_ts(RV, SB + ks * 8 + (ks >= 4 ? 32 : 0), desc_mnmajor(adOb, kTW, ks), id_g,
                    acc || ks > 0);
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks)  // dK += dS^T Q
-            mma_ss(RK, desc_kmajor(adS, 128, ks), desc_mnmajor(aQb, kTW, ks), id_g, acc || ks > 0);
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks)  // dQ^T = K^T dS^T into DB (dP^T was read by the softmax)
+          for (int ks = 0; ks < 8; ++ks)  // dQ^T = K^T dS^T into DB (B operand: dS^T in shared memory)
             mma_ss(DB, desc_mnmajor(aK, 128, ks), desc_mnmajor(adS, 128, ks), id_q, ks > 0);
           mma_commit(&sh->ph2_full);  // also: the slot's Q / dO rows are no longer read
         }
@@ -1076,8 +1080,10 @@ __global__ void __launch_bounds__(kWideThreads, 1)
               dw[2 * qq] = pack_bf16(dsv[0], dsv[1]);
               dw[2 * qq + 1] = pack_bf16(dsv[2], dsv[3]);
             }
-            // P^T of these 16 rows: 8 columns of bf16 pairs, over columns this half has read
+            // P^T and dS^T of these 16 rows: 8 columns of bf16 pairs each, over columns of S^T
+            // and dP^T this half has read (dS^T also goes to shared memory for dQ^T below)
             tmem_st8(SB + lb + 16 * c + 32 * hf + 8 * hh, pw);
+            tmem_st8(DB + lb + 16 * c + 32 * hf + 8 * hh, dw);
 #pragma unroll
             for (int u = 0; u < 2; ++u)
               st_shared_v4(panel + sm100::sw128_chunk(kr, (c & 1) * 4 + 2 * hh + u), dw[4 * u],
