@@ -128,22 +128,23 @@ def test_fullsize_multichunk_key_window():
     """dK / dV / dKp of a mid-sequence key block that tokens of every backward chunk reach, at
     the 64K workload's full size and launch configuration.
 
-    The backward splits each key block's token list by sequence chunk (16384 tokens at 64K with
-    8 heads per group) and items of different chunks add their dK / dV / dKp into the same rows
+    The backward splits each key block's token list by sequence chunk (8192 tokens at 64K with
+    8 heads per group: 32 MB of fp32 dQ rows per proxy head) and items of different chunks add
+    their dK / dV / dKp into the same rows
     at different times.  The last-window check above cannot see that (only the last block's
     tokens reach the last keys).  Here both sides run on one seeded random index map
     (random_selection, the same input for both) in which block FOCUS is put into the selection of
-    tokens from all four chunks -- 600 of them in one chunk for group 0, so that list spans two
+    tokens from all eight chunks -- 600 of them in one chunk for group 0, so that list spans two
     work items -- and of nobody else but the block's own tokens.  The oracle then computes every
     contribution to that block exactly (it visits every row whose key set touches the window)."""
     from block_sparse_attention_qp_gb300.inputs import force_block, random_selection
 
     wi, w = [(i + 1, x) for i, x in enumerate(WORKLOADS) if x.name == "msa_s64k_planted"][0]
-    FOCUS = 100  # keys 12800 .. 12927, in the first chunk
+    FOCUS = 50  # keys 6400 .. 6527, in the first chunk
     x = make_inputs(w, workload_seed(wi))
     idx = random_selection(w.B, w.Hp, w.S, w.top_k, seed=4321, exclude=FOCUS)
     rng = np.random.default_rng(99)
-    chunk = 16384
+    chunk = 8192
     forced = []
     for g in range(w.Hp):
         for c in range(w.S // chunk):
