@@ -53,10 +53,11 @@ cudaEvent_t pooled_event() {
   return e;
 }
 
-// Runs `launch` (which issues exactly one kernel on st), counting it and timing it if enabled.
+// Runs `launch` (which issues `kernels` kernels on st, one unless stated), counting them and
+// timing them together if enabled.
 template <typename F>
-void timed(const char* name, cudaStream_t st, F&& launch) {
-  g_launches.fetch_add(1, std::memory_order_relaxed);
+void timed(const char* name, cudaStream_t st, F&& launch, int kernels = 1) {
+  g_launches.fetch_add(kernels, std::memory_order_relaxed);
   if (!g_prof_on) {
     launch();
     return;
@@ -140,7 +141,7 @@ struct Plan {
   size_t status = 0, totals = 0, seg_count = 0, seg_offset = 0, seg_cursor = 0, entries = 0;
   size_t io0 = 0, io1 = 0, items0 = 0, items1 = 0;
   size_t opart = 0, lpart = 0, lpx_part = 0, lse_px = 0, lpxe = 0, rowm = 0, emeta = 0, pbar = 0;
-  size_t dq = 0, dk = 0, dv = 0, dqp = 0, dkp = 0, scores = 0;
+  size_t dq = 0, dk = 0, dv = 0, dqp = 0, dkp = 0, scores = 0, scan = 0;
   size_t bytes = 0;
   long long max0 = 0, max1 = 0;
   ItemSpec spec0{1, 1}, spec1{1, 1};
@@ -208,6 +209,8 @@ Plan make_plan(const Dims& d, int op) {
   const int TT = kBlock / d.G;
   p.status = c.take(256);
   p.totals = c.take(4 * sizeof(int));
+  if (op == MSA_OP_FORWARD || op == MSA_OP_BACKWARD || op == MSA_OP_WARMUP_BACKWARD)
+    p.scan = c.take(scan_tiles(nseg) * 3 * sizeof(long long));
   if (op == MSA_OP_FORWARD || op == MSA_OP_BACKWARD) {
     p.seg_count = c.take(nseg * sizeof(int));
     p.seg_offset = c.take((nseg + 1) * sizeof(int));
@@ -397,8 +400,9 @@ void build_lists(const Dims& d, const Plan& p, const int32_t* idx, void* ws, int
   const ItemSpec specs[2] = {p.spec0, p.spec1};
   timed("invert_scan", st, [&] {
     launch_scan(d, false, seg_count, at<int>(ws, p.seg_offset), specs, nspecs, at<int>(ws, p.io0),
-                nspecs > 1 ? at<int>(ws, p.io1) : nullptr, at<int>(ws, p.totals), st);
-  });
+                nspecs > 1 ? at<int>(ws, p.io1) : nullptr, at<int>(ws, p.totals),
+                at<long long>(ws, p.scan), st);
+  }, scan_kernels(d.nlist()));
   timed("invert_fill", st, [&] { launch_fill(d, idx, at<int>(ws, p.seg_offset), seg_cursor, at<int>(ws, p.entries), status, st); });
   timed("work_items", st, [&] {
     launch_items(d, false, seg_count, at<int>(ws, p.seg_offset), p.spec0, at<int>(ws, p.io0),
@@ -626,8 +630,9 @@ int msa_warmup_backward(const msa_shape_t* shape, const void* q, const void* k, 
   const ItemSpec specs[1] = {p.spec0};
   timed("invert_scan", st, [&] {
     launch_scan(d, true, nullptr, at<int>(workspace, p.seg_offset), specs, 1,
-                at<int>(workspace, p.io0), nullptr, at<int>(workspace, p.totals), st);
-  });
+                at<int>(workspace, p.io0), nullptr, at<int>(workspace, p.totals),
+                at<long long>(workspace, p.scan), st);
+  }, scan_kernels(d.nlist()));
   timed("work_items", st, [&] {
     launch_items(d, true, nullptr, at<int>(workspace, p.seg_offset), p.spec0, at<int>(workspace, p.io0),
                  at<Item>(workspace, p.items0), p.max0, status, st);

@@ -87,34 +87,41 @@ __device__ __forceinline__ long long list_len(const Dims& d, bool dense, const i
   return seg_count[seg];
 }
 
-__device__ __forceinline__ long long items_of(long long c, const ItemSpec& s) {
-  const long long tiles = (c + s.tile_tokens - 1) / s.tile_tokens;
+// Work items of a list of c entries (c <= S < 2^31: 32-bit arithmetic, whose division is several
+// times cheaper than the 64-bit one in the single-block scan)
+__device__ __forceinline__ int items_of(int c, const ItemSpec& s) {
+  const int tiles = (c + s.tile_tokens - 1) / s.tile_tokens;
   return (tiles + s.chunk_tiles - 1) / s.chunk_tiles * s.nsub;
 }
 
-// Single-CTA exclusive scan over every list of three running sums: list lengths and the item
-// counts of up to two item specs.
-__global__ void __launch_bounds__(1024) scan_kernel(Dims d, int dense, const int* __restrict__ seg_count,
-                                                    int* __restrict__ seg_offset, ItemSpec s0, ItemSpec s1,
-                                                    int nspecs, int* __restrict__ io0,
-                                                    int* __restrict__ io1, int* __restrict__ totals) {
-  __shared__ long long sh[3][1024];
-  const long long nseg = d.nlist();
+// Exclusive scans over every list of three running sums (list lengths and the item counts of up
+// to two item specs), in three passes: per-tile sums (a tile = kScanTile consecutive lists, 8
+// per thread), an exclusive scan of the tile sums (one block), and the per-list offsets of
+// each tile from its tile's offset.  The lists number up to a few million (one per sequence
+// chunk, batch, proxy head and key block), so the work is spread over every SM.
+constexpr int kScanThreads = 1024, kScanPer = 8, kScanTile = kScanThreads * kScanPer;
+
+struct Sums3 {
+  long long a, b, c;
+};
+
+__device__ __forceinline__ Sums3 list_sums(const Dims& d, bool dense, const int* seg_count,
+                                           long long s, int nspecs, const ItemSpec& s0,
+                                           const ItemSpec& s1) {
+  const long long len = list_len(d, dense, seg_count, s);
+  return Sums3{len, nspecs > 0 ? (long long)items_of((int)len, s0) : 0,
+               nspecs > 1 ? (long long)items_of((int)len, s1) : 0};
+}
+
+// Exclusive scan of v over the block's kScanThreads threads; *total receives the block's sum.
+__device__ Sums3 block_exclusive_scan(Sums3 v, Sums3* total) {
+  __shared__ long long sh[3][kScanThreads];
   const int tid = threadIdx.x;
-  const long long per = (nseg + 1023) / 1024;
-  const long long lo = tid * per, hi = lo + per < nseg ? lo + per : nseg;
-  long long a = 0, b = 0, c = 0;
-  for (long long s = lo; s < hi; ++s) {
-    const long long len = list_len(d, dense, seg_count, s);
-    a += len;
-    if (nspecs > 0) b += items_of(len, s0);
-    if (nspecs > 1) c += items_of(len, s1);
-  }
-  sh[0][tid] = a;
-  sh[1][tid] = b;
-  sh[2][tid] = c;
+  sh[0][tid] = v.a;
+  sh[1][tid] = v.b;
+  sh[2][tid] = v.c;
   __syncthreads();
-  for (int off = 1; off < 1024; off <<= 1) {  // inclusive Hillis-Steele scan
+  for (int off = 1; off < kScanThreads; off <<= 1) {  // inclusive Hillis-Steele scan
     long long va = 0, vb = 0, vc = 0;
     if (tid >= off) {
       va = sh[0][tid - off];
@@ -127,43 +134,152 @@ __global__ void __launch_bounds__(1024) scan_kernel(Dims d, int dense, const int
     sh[2][tid] += vc;
     __syncthreads();
   }
-  long long ra = sh[0][tid] - a, rb = sh[1][tid] - b, rc = sh[2][tid] - c;  // exclusive
-  for (long long s = lo; s < hi; ++s) {
-    const long long len = list_len(d, dense, seg_count, s);
+  const Sums3 r{sh[0][tid] - v.a, sh[1][tid] - v.b, sh[2][tid] - v.c};
+  *total = Sums3{sh[0][kScanThreads - 1], sh[1][kScanThreads - 1], sh[2][kScanThreads - 1]};
+  __syncthreads();  // sh may be reused by the caller's next scan
+  return r;
+}
+
+__device__ __forceinline__ Sums3 thread_sums(const Dims& d, bool dense, const int* seg_count,
+                                             long long lo, long long nseg, int nspecs,
+                                             const ItemSpec& s0, const ItemSpec& s1) {
+  Sums3 v{0, 0, 0};
+  for (int k = 0; k < kScanPer; ++k) {
+    if (lo + k >= nseg) break;
+    const Sums3 x = list_sums(d, dense, seg_count, lo + k, nspecs, s0, s1);
+    v.a += x.a;
+    v.b += x.b;
+    v.c += x.c;
+  }
+  return v;
+}
+
+// The same scan in one block, tile after tile with a running carry: for up to kScanSingle
+// tiles, where the three dependent launches would cost more than the work.
+constexpr int kScanSingle = 8;
+__global__ void __launch_bounds__(kScanThreads) scan_single_kernel(Dims d, int dense, const int* __restrict__ seg_count,
+                                                                   int* __restrict__ seg_offset, ItemSpec s0,
+                                                                   ItemSpec s1, int nspecs, int* __restrict__ io0,
+                                                                   int* __restrict__ io1, int* __restrict__ totals) {
+  const long long nseg = d.nlist();
+  Sums3 carry{0, 0, 0};
+  for (long long base = 0; base < nseg; base += kScanTile) {
+    const long long lo = base + (long long)threadIdx.x * kScanPer;
+    Sums3 tot;
+    const Sums3 ex = block_exclusive_scan(thread_sums(d, dense, seg_count, lo, nseg, nspecs, s0, s1), &tot);
+    long long ra = carry.a + ex.a, rb = carry.b + ex.b, rc = carry.c + ex.c;
+    for (int k = 0; k < kScanPer; ++k) {
+      const long long s = lo + k;
+      if (s >= nseg) break;
+      const Sums3 x = list_sums(d, dense, seg_count, s, nspecs, s0, s1);
+      if (seg_offset) seg_offset[s] = (int)ra;
+      if (nspecs > 0) io0[s] = (int)rb;
+      if (nspecs > 1) io1[s] = (int)rc;
+      ra += x.a;
+      rb += x.b;
+      rc += x.c;
+    }
+    carry.a += tot.a;
+    carry.b += tot.b;
+    carry.c += tot.c;
+  }
+  if (threadIdx.x == 0) {
+    if (seg_offset) seg_offset[nseg] = (int)carry.a;
+    totals[0] = (int)carry.a;
+    totals[1] = (int)carry.b;
+    totals[2] = (int)carry.c;
+  }
+}
+
+// pass 1: tile_sums[3 t + {0, 1, 2}] = the sums of tile t
+__global__ void __launch_bounds__(kScanThreads) scan_tiles_kernel(Dims d, int dense, const int* __restrict__ seg_count,
+                                                                  ItemSpec s0, ItemSpec s1, int nspecs,
+                                                                  long long* __restrict__ tile_sums) {
+  const long long nseg = d.nlist();
+  const long long lo = blockIdx.x * (long long)kScanTile + (long long)threadIdx.x * kScanPer;
+  Sums3 tot;
+  block_exclusive_scan(thread_sums(d, dense, seg_count, lo, nseg, nspecs, s0, s1), &tot);
+  if (threadIdx.x == 0) {
+    tile_sums[3 * blockIdx.x + 0] = tot.a;
+    tile_sums[3 * blockIdx.x + 1] = tot.b;
+    tile_sums[3 * blockIdx.x + 2] = tot.c;
+  }
+}
+
+// pass 2 (one block): exclusive scan of the tile sums in place; totals = the grand sums
+__global__ void __launch_bounds__(kScanThreads) scan_tops_kernel(long long* __restrict__ tile_sums, int ntiles,
+                                                                 int* __restrict__ totals) {
+  Sums3 carry{0, 0, 0};
+  for (int base = 0; base < ntiles; base += kScanThreads) {
+    const int t = base + (int)threadIdx.x;
+    Sums3 v{0, 0, 0};
+    if (t < ntiles) v = Sums3{tile_sums[3 * t], tile_sums[3 * t + 1], tile_sums[3 * t + 2]};
+    Sums3 tot;
+    const Sums3 ex = block_exclusive_scan(v, &tot);
+    if (t < ntiles) {
+      tile_sums[3 * t] = carry.a + ex.a;
+      tile_sums[3 * t + 1] = carry.b + ex.b;
+      tile_sums[3 * t + 2] = carry.c + ex.c;
+    }
+    carry.a += tot.a;
+    carry.b += tot.b;
+    carry.c += tot.c;
+  }
+  if (threadIdx.x == 0) {
+    totals[0] = (int)carry.a;
+    totals[1] = (int)carry.b;
+    totals[2] = (int)carry.c;
+  }
+}
+
+// pass 3: per-list offsets (seg_offset[nseg] = the total list length)
+__global__ void __launch_bounds__(kScanThreads) scan_write_kernel(Dims d, int dense, const int* __restrict__ seg_count,
+                                                                  int* __restrict__ seg_offset, ItemSpec s0,
+                                                                  ItemSpec s1, int nspecs, int* __restrict__ io0,
+                                                                  int* __restrict__ io1,
+                                                                  const long long* __restrict__ tile_offsets,
+                                                                  const int* __restrict__ totals) {
+  const long long nseg = d.nlist();
+  const long long lo = blockIdx.x * (long long)kScanTile + (long long)threadIdx.x * kScanPer;
+  Sums3 tot;
+  const Sums3 ex = block_exclusive_scan(thread_sums(d, dense, seg_count, lo, nseg, nspecs, s0, s1), &tot);
+  long long ra = tile_offsets[3 * blockIdx.x] + ex.a, rb = tile_offsets[3 * blockIdx.x + 1] + ex.b,
+            rc = tile_offsets[3 * blockIdx.x + 2] + ex.c;
+  for (int k = 0; k < kScanPer; ++k) {
+    const long long s = lo + k;
+    if (s >= nseg) break;
+    const Sums3 x = list_sums(d, dense, seg_count, s, nspecs, s0, s1);
     if (seg_offset) seg_offset[s] = (int)ra;
     if (nspecs > 0) io0[s] = (int)rb;
     if (nspecs > 1) io1[s] = (int)rc;
-    ra += len;
-    if (nspecs > 0) rb += items_of(len, s0);
-    if (nspecs > 1) rc += items_of(len, s1);
+    ra += x.a;
+    rb += x.b;
+    rc += x.c;
   }
-  if (tid == 1023) {
-    if (seg_offset) seg_offset[nseg] = (int)sh[0][1023];
-    totals[0] = (int)sh[0][1023];
-    totals[1] = (int)sh[1][1023];
-    totals[2] = (int)sh[2][1023];
-  }
+  if (seg_offset && blockIdx.x == 0 && threadIdx.x == 0) seg_offset[nseg] = totals[0];
 }
 
 __global__ void items_kernel(Dims d, int dense, const int* __restrict__ seg_count,
                              const int* __restrict__ seg_offset, ItemSpec sp,
                              const int* __restrict__ item_offset, Item* __restrict__ items,
                              long long max_items, unsigned* status) {
-  const long long seg = blockIdx.x;
-  const long long len = list_len(d, dense, seg_count, seg);
+  const long long nseg = d.nlist();
   const int per_item = sp.tile_tokens * sp.chunk_tiles;
-  const long long n_items = (len + per_item - 1) / per_item * sp.nsub;
-  const long long base = item_offset[seg];
-  const long long list0 = seg_offset ? seg_offset[seg] : 0;
-  for (long long i = threadIdx.x; i < n_items; i += blockDim.x) {
-    const long long pos = base + i;
-    if (pos >= max_items) {
-      atomicOr(status, kStatusBadItems);
-      continue;
+  for (long long seg = blockIdx.x; seg < nseg; seg += gridDim.x) {  // a block per list in turn
+    const int len = (int)list_len(d, dense, seg_count, seg);
+    const int n_items = (len + per_item - 1) / per_item * sp.nsub;
+    const long long base = item_offset[seg];
+    const long long list0 = seg_offset ? seg_offset[seg] : 0;
+    for (int i = threadIdx.x; i < n_items; i += blockDim.x) {
+      const long long pos = base + i;
+      if (pos >= max_items) {
+        atomicOr(status, kStatusBadItems);
+        continue;
+      }
+      const int first = i / sp.nsub * per_item;  // the attention groups of a run of tokens
+      const int cnt = len - first < per_item ? len - first : per_item;  // are consecutive
+      items[pos] = Item{(int)seg, first, cnt, (int)(list0 + first), i % sp.nsub};
     }
-    const long long first = i / sp.nsub * per_item;  // the attention groups of a run of tokens
-    const long long cnt = len - first < per_item ? len - first : per_item;  // are consecutive
-    items[pos] = Item{(int)seg, (int)first, (int)cnt, (int)(list0 + first), (int)(i % sp.nsub)};
   }
 }
 
@@ -175,21 +291,24 @@ __global__ void entry_meta_kernel(Dims d, int dense, const int* __restrict__ seg
                                   const int* __restrict__ seg_offset, const int* __restrict__ entries,
                                   const float* __restrict__ lse_px, const float2* __restrict__ rowm,
                                   float* __restrict__ lpxe, float2* __restrict__ emeta) {
+  // one block per list: the lists' lengths vary by orders of magnitude (a block every token
+  // selects against a rarely chosen one), which the block scheduler balances
   const long long seg = blockIdx.x;
-  const long long len = list_len(d, dense, seg_count, seg);
+  const int len = (int)list_len(d, dense, seg_count, seg);
   if (len == 0) return;
   const long long base = seg_offset[seg];
   const long long bg = (seg % d.nseg()) / d.nblk;  // b * Hp + g
   const long long b = bg / d.Hp, g = bg % d.Hp;
   const float* row = lse_px + bg * d.S;
   const long long t0 = dense ? dense_first(d, seg) : 0;
-  for (long long k = threadIdx.x; k < len; k += blockDim.x) {
+  for (int k = threadIdx.x; k < len; k += blockDim.x) {
     const long long t = dense ? t0 + k : (long long)(entries[base + k] >> 8);
     lpxe[base + k] = row[t] * kLog2e;
   }
   const int gp = d.Gp();
-  for (long long x = threadIdx.x; x < len * gp; x += blockDim.x) {
-    const long long k = x / gp, h = x % gp;
+  const int n = len * gp;  // < 2^31: 32-bit index arithmetic
+  for (int x = threadIdx.x; x < n; x += blockDim.x) {
+    const int k = x / gp, h = x - k * gp;
     const long long t = dense ? t0 + k : (long long)(entries[base + k] >> 8);
     emeta[base * gp + x] = rowm[((b * d.S + t) * d.Hq + g * gp + h)];
   }
@@ -227,13 +346,27 @@ void launch_count(const Dims& d, const int32_t* idx, int* seg_count, unsigned* s
   count_kernel<<<grid_for(rows, 256), 256, 0, st>>>(d, idx, seg_count, status);
 }
 
+long long scan_tiles(long long nlists) { return (nlists + kScanTile - 1) / kScanTile; }
+
+int scan_kernels(long long nlists) { return scan_tiles(nlists) <= kScanSingle ? 1 : 3; }
+
 void launch_scan(const Dims& d, bool dense, const int* seg_count, int* seg_offset,
                  const ItemSpec* specs, int nspecs, int* item_offset0, int* item_offset1,
-                 int* totals, cudaStream_t st) {
+                 int* totals, long long* tile_tmp, cudaStream_t st) {
   ItemSpec s0 = nspecs > 0 ? specs[0] : ItemSpec{1, 1, 1};
   ItemSpec s1 = nspecs > 1 ? specs[1] : ItemSpec{1, 1, 1};
-  scan_kernel<<<1, 1024, 0, st>>>(d, dense ? 1 : 0, seg_count, seg_offset, s0, s1, nspecs,
-                                  item_offset0, item_offset1, totals);
+  const int ntiles = (int)scan_tiles(d.nlist());
+  if (ntiles <= kScanSingle) {
+    scan_single_kernel<<<1, kScanThreads, 0, st>>>(d, dense ? 1 : 0, seg_count, seg_offset, s0, s1,
+                                                   nspecs, item_offset0, item_offset1, totals);
+    return;
+  }
+  scan_tiles_kernel<<<ntiles, kScanThreads, 0, st>>>(d, dense ? 1 : 0, seg_count, s0, s1, nspecs,
+                                                     tile_tmp);
+  scan_tops_kernel<<<1, kScanThreads, 0, st>>>(tile_tmp, ntiles, totals);
+  scan_write_kernel<<<ntiles, kScanThreads, 0, st>>>(d, dense ? 1 : 0, seg_count, seg_offset, s0,
+                                                     s1, nspecs, item_offset0, item_offset1,
+                                                     tile_tmp, totals);
 }
 
 void launch_fill(const Dims& d, const int32_t* idx, const int* seg_offset, int* seg_cursor,
@@ -246,8 +379,8 @@ void launch_fill(const Dims& d, const int32_t* idx, const int* seg_offset, int* 
 void launch_items(const Dims& d, bool dense, const int* seg_count, const int* seg_offset,
                   const ItemSpec& spec, const int* item_offset, Item* items, long long max_items,
                   unsigned* status, cudaStream_t st) {
-  items_kernel<<<(unsigned)d.nlist(), 128, 0, st>>>(d, dense ? 1 : 0, seg_count, seg_offset, spec,
-                                                    item_offset, items, max_items, status);
+  items_kernel<<<grid_for(d.nlist(), 1), 128, 0, st>>>(d, dense ? 1 : 0, seg_count, seg_offset,
+                                                       spec, item_offset, items, max_items, status);
 }
 
 void launch_entry_meta(const Dims& d, bool dense, const int* seg_count, const int* seg_offset,

@@ -41,9 +41,13 @@ void launch_count(const Dims& d, const int32_t* idx, int* seg_count, unsigned* s
                   cudaStream_t st);
 // Exclusive scans: list offsets (sparse only) and item offsets for up to two item specs.
 // dense: list lengths are the tokens t >= 128 n of the chunk instead of seg_count.
+// tile_tmp: scan_tiles(d.nlist()) x 3 long longs of scratch.  scan_kernels: how many kernels
+// one scan launches (one block for few lists, three passes over every SM otherwise).
+long long scan_tiles(long long nlists);
+int scan_kernels(long long nlists);
 void launch_scan(const Dims& d, bool dense, const int* seg_count, int* seg_offset,
                  const ItemSpec* specs, int nspecs, int* item_offset0, int* item_offset1,
-                 int* totals, cudaStream_t st);
+                 int* totals, long long* tile_tmp, cudaStream_t st);
 // Scatter (t << 8 | slot) into the lists; order inside a list is unspecified.
 void launch_fill(const Dims& d, const int32_t* idx, const int* seg_offset, int* seg_cursor,
                  int* entries, unsigned* status, cudaStream_t st);

@@ -125,3 +125,17 @@ def test_backward_rejects_a_misaligned_kl_grad_pointer(lib):
     rc = lib.msa_warmup_backward(ctypes.byref(s), a, a, a, a, a, a, a, a, 1.0, odd, a, a, a, a, a,
                                  P(0), a, 1 << 30, P(0))
     assert rc == 1 and b"kl_grad_dev" in lib.msa_last_error()
+
+
+def test_kl_grad_argument_marshalling():
+    """kl_grad goes to the library by value when it is a number and as a device pointer (read by
+    the kernel, no host synchronisation) when it is a one-element tensor on the inputs' device."""
+    import torch
+
+    assert binding._kl_grad_args(0.5, "cpu") == (0.5, None)
+    v, t = binding._kl_grad_args(torch.tensor([2.0], dtype=torch.float64), "cpu")
+    assert v == 0.0 and t.dtype == torch.float32 and t.shape == () and float(t) == 2.0
+    with pytest.raises(binding.MSAError, match="one element"):
+        binding._kl_grad_args(torch.ones(2), "cpu")
+    with pytest.raises(binding.MSAError, match="is on"):
+        binding._kl_grad_args(torch.ones(()), "meta")
