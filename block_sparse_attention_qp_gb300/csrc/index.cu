@@ -68,6 +68,75 @@ __global__ void fill_kernel(Dims d, const int32_t* __restrict__ idx, const int* 
   }
 }
 
+// The same two steps with the counting done in shared memory first, for key-block counts up to
+// kHistBlocks: a block takes the 128 rows of one (b, g) and one sequence chunk (S and the chunk
+// are multiples of 128), so all its entries fall in the lists of one (c, b, g), and many tokens
+// share a block (their local block, blocks most of them select).  The block adds each non-zero
+// count to the global list once -- one global atomic per (block, key block) instead of one per
+// entry -- and, when filling, reserves each list's range once and places its entries from
+// shared cursors.
+constexpr int kHistRows = 128, kHistBlocks = 2048;
+
+__global__ void __launch_bounds__(kHistRows) count_hist_kernel(Dims d, const int32_t* __restrict__ idx,
+                                                               int* __restrict__ seg_count, unsigned* status) {
+  __shared__ int hist[kHistBlocks];
+  const long long r = (long long)blockIdx.x * kHistRows + threadIdx.x;
+  const long long r0 = (long long)blockIdx.x * kHistRows;
+  const int t0 = (int)(r0 % d.S), t = (int)(r % d.S);
+  const long long bg = r0 / d.S;
+  const int nmax = min(d.nblk, (t0 + kHistRows - 1) / kBlock + 1);  // blocks these tokens may use
+  for (int i = threadIdx.x; i < nmax; i += kHistRows) hist[i] = 0;
+  __syncthreads();
+  const int32_t* row = idx + r * d.top_k;
+  int prev = -1;
+  bool padded = false, bad = false;
+  for (int s = 0; s < d.top_k; ++s) {
+    const int n = checked_block(row, s, t, prev, padded, bad);
+    if (n >= 0) atomicAdd(&hist[n], 1);
+  }
+  if (bad) atomicOr(status, kStatusBadIndex);
+  __syncthreads();
+  int* dst = seg_count + (long long)(t0 / d.chunk) * d.nseg() + bg * d.nblk;
+  for (int i = threadIdx.x; i < nmax; i += kHistRows)
+    if (hist[i]) atomicAdd(dst + i, hist[i]);
+}
+
+__global__ void __launch_bounds__(kHistRows) fill_hist_kernel(Dims d, const int32_t* __restrict__ idx,
+                                                              const int* __restrict__ seg_offset,
+                                                              int* __restrict__ seg_cursor, int* __restrict__ entries) {
+  __shared__ int base[kHistBlocks], cur[kHistBlocks];
+  const long long r = (long long)blockIdx.x * kHistRows + threadIdx.x;
+  const long long r0 = (long long)blockIdx.x * kHistRows;
+  const int t0 = (int)(r0 % d.S), t = (int)(r % d.S);
+  const long long bg = r0 / d.S;
+  const int nmax = min(d.nblk, (t0 + kHistRows - 1) / kBlock + 1);
+  for (int i = threadIdx.x; i < nmax; i += kHistRows) {
+    base[i] = 0;
+    cur[i] = 0;
+  }
+  __syncthreads();
+  const int32_t* row = idx + r * d.top_k;
+  {
+    int prev = -1;
+    bool padded = false, bad = false;
+    for (int s = 0; s < d.top_k; ++s) {
+      const int n = checked_block(row, s, t, prev, padded, bad);
+      if (n >= 0) atomicAdd(&base[n], 1);  // count
+    }
+  }
+  __syncthreads();
+  const long long seg0 = (long long)(t0 / d.chunk) * d.nseg() + bg * d.nblk;
+  for (int i = threadIdx.x; i < nmax; i += kHistRows)  // reserve each list's range: count -> start
+    if (base[i]) base[i] = seg_offset[seg0 + i] + atomicAdd(seg_cursor + seg0 + i, base[i]);
+  __syncthreads();
+  int prev = -1;
+  bool padded = false, bad = false;
+  for (int s = 0; s < d.top_k; ++s) {
+    const int n = checked_block(row, s, t, prev, padded, bad);
+    if (n >= 0) entries[base[n] + atomicAdd(&cur[n], 1)] = (t << 8) | s;
+  }
+}
+
 // Dense lists: chunk c of block n holds the tokens t >= 128 n with t in the chunk, i.e. the range
 // [max(128 n, c * chunk), min(S, (c+1) * chunk)).
 __device__ __forceinline__ long long dense_first(const Dims& d, long long seg) {
@@ -343,7 +412,10 @@ static int grid_for(long long work, int threads) {
 void launch_count(const Dims& d, const int32_t* idx, int* seg_count, unsigned* status,
                   cudaStream_t st) {
   const long long rows = (long long)d.B * d.Hp * d.S;
-  count_kernel<<<grid_for(rows, 256), 256, 0, st>>>(d, idx, seg_count, status);
+  if (d.nblk <= kHistBlocks)
+    count_hist_kernel<<<(unsigned)(rows / kHistRows), kHistRows, 0, st>>>(d, idx, seg_count, status);
+  else
+    count_kernel<<<grid_for(rows, 256), 256, 0, st>>>(d, idx, seg_count, status);
 }
 
 long long scan_tiles(long long nlists) { return (nlists + kScanTile - 1) / kScanTile; }
@@ -373,7 +445,11 @@ void launch_fill(const Dims& d, const int32_t* idx, const int* seg_offset, int* 
                  int* entries, unsigned* status, cudaStream_t st) {
   (void)status;
   const long long rows = (long long)d.B * d.Hp * d.S;
-  fill_kernel<<<grid_for(rows, 256), 256, 0, st>>>(d, idx, seg_offset, seg_cursor, entries);
+  if (d.nblk <= kHistBlocks)
+    fill_hist_kernel<<<(unsigned)(rows / kHistRows), kHistRows, 0, st>>>(d, idx, seg_offset,
+                                                                         seg_cursor, entries);
+  else
+    fill_kernel<<<grid_for(rows, 256), 256, 0, st>>>(d, idx, seg_offset, seg_cursor, entries);
 }
 
 void launch_items(const Dims& d, bool dense, const int* seg_count, const int* seg_offset,
