@@ -694,7 +694,7 @@ __global__ void __launch_bounds__(352, 1)
 // The same backward with 128-row tiles (128 / G tokens x G heads): every product then has N = 128,
 // which the tensor core runs in the time of an N = 64 one -- 40 MMA instructions per 128 rows
 // instead of 64 with two 64-row tiles.  Tensor memory holds one tile's S^T (then P^T) and dP^T
-// (then dQ^T) besides dV and dK, so the S / dP products of a tile wait for the previous tile's
+// (then dS^T, then dQ^T) besides dV and dK, so the S / dP products of a tile wait for the previous tile's
 // epilogue instead of running ahead of it; the tensor core idles while the softmax runs.  To keep
 // that gap short the softmax and epilogue of a tile are split over eight warps: two per
 // tensor-memory lane quarter, one for the tile's rows 0-63 and one for rows 64-127.  Shared memory
@@ -873,7 +873,8 @@ __global__ void __launch_bounds__(kWideThreads, 1)
           for (int ks = 0; ks < 8; ++ks)
             mma_ss(DB, desc_kmajor(aV, 128, ks), desc_kmajor(adOb, kTW, ks), id_s, ks > 0);
           mma_commit(&sh->s_full);  // also: every product of tile i-1 has completed
-          // phase 2, once the softmax has written P^T (tensor memory) and dS^T (shared memory)
+          // phase 2, once the softmax has written P^T (tensor memory) and dS^T (tensor memory for
+          // dK, shared memory for dQ^T)
           if (!wait1(8, &sh->p_full, par(i))) { ok = false; break; }
           if (tl == 0 && ni > 0 && !wait1(9, &sh->acc_free, par(ni - 1))) { ok = false; break; }
           fence_after_sync();
