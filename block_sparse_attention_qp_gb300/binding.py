@@ -15,6 +15,7 @@ heads in the backward.
 from __future__ import annotations
 
 import ctypes
+import functools
 import os
 import threading
 
@@ -97,6 +98,25 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+def _on_tensor_device(fn):
+    """Runs fn with the CUDA device of its first tensor argument current, so that the library
+    launches on the device that holds the data (with that device's current stream); every other
+    tensor argument must be on the same device."""
+    @functools.wraps(fn)
+    def wrapper(*args, **kwargs):
+        tensors = [a for a in list(args) + list(kwargs.values()) if isinstance(a, torch.Tensor)]
+        if not tensors or not tensors[0].is_cuda:
+            return fn(*args, **kwargs)
+        dev = tensors[0].device
+        for t in tensors[1:]:
+            if t.device != dev:
+                raise MSAError(f"{fn.__name__}: tensors on {dev} and {t.device}; all arguments "
+                               "must be on one device")
+        with torch.cuda.device(dev):
+            return fn(*args, **kwargs)
+    return wrapper
+
+
 def _stream(device):
     return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
 
@@ -172,6 +192,7 @@ def _kl_grad_args(kl_grad, device):
     return float(kl_grad), None
 
 
+@_on_tensor_device
 def msa_device_status(ws: torch.Tensor) -> int:
     """Read and clear the device status word of a workspace (synchronises the stream)."""
     flags = ctypes.c_uint(0)
@@ -180,6 +201,7 @@ def msa_device_status(ws: torch.Tensor) -> int:
     return int(flags.value)
 
 
+@_on_tensor_device
 def selftest_wait_timeout(ws: torch.Tensor, limit_us: int = 1000) -> None:
     """Run the library's bounded-wait self-test on ws's device (see msa_selftest_wait_timeout);
     the timeout shows up in msa_device_status(ws)."""
@@ -208,6 +230,7 @@ def launch_count() -> int:
     return int(load_library().msa_launch_count())
 
 
+@_on_tensor_device
 def msa_forward(q, k, v, qp, kp, top_k: int, scale: float, block_idx=None, ws=None):
     """Sparse forward.  Returns (o, lse, block_idx).  block_idx given -> used as the selection."""
     B, S, Hq, D = q.shape
@@ -231,6 +254,7 @@ def msa_forward(q, k, v, qp, kp, top_k: int, scale: float, block_idx=None, ws=No
     return o, lse, block_idx
 
 
+@_on_tensor_device
 def msa_forward_noalloc(q, k, v, qp, kp, top_k: int, scale: float, block_idx=None):
     """msa_forward without a workspace: the library's fixed device scratch array is used instead
     (see include/msa.h).  Returns (o, lse, block_idx)."""
@@ -262,6 +286,7 @@ def msa_forward_noalloc_status(device=None) -> int:
     return int(flags.value)
 
 
+@_on_tensor_device
 def msa_backward(q, k, v, qp, kp, o, lse, dout, block_idx, top_k: int, scale: float,
                  kl_grad=1.0, ws=None, return_kl: bool = False):
     """Sparse backward.  Returns (dq, dk, dv, dqp, dkp), plus the KL value L_KL as a 0-d fp32
@@ -286,6 +311,7 @@ def msa_backward(q, k, v, qp, kp, o, lse, dout, block_idx, top_k: int, scale: fl
     return tuple(grads) + ((kl,) if return_kl else ())
 
 
+@_on_tensor_device
 def msa_decode(q, qp, k_cache, v_cache, kp_cache, seq_len, top_k: int, scale: float, ws=None):
     """Decode step: q [B, Hq, D], qp [B, Hp, D] (the new tokens), caches k/v [B, S, Hkv, D] and
     kp [B, S, 1, D] (or [B, S, D]) already holding the new tokens at seq_len - 1, seq_len [B] int32
@@ -310,6 +336,7 @@ def msa_decode(q, qp, k_cache, v_cache, kp_cache, seq_len, top_k: int, scale: fl
     return o, lse, idx
 
 
+@_on_tensor_device
 def msa_warmup_forward(q, k, v, scale: float, ws=None):
     """Dense causal forward (warmup).  Returns (o, lse)."""
     B, S, Hq, D = q.shape
@@ -326,6 +353,7 @@ def msa_warmup_forward(q, k, v, scale: float, ws=None):
     return o, lse
 
 
+@_on_tensor_device
 def msa_warmup_backward(q, k, v, qp, kp, o, lse, dout, scale: float, kl_grad=1.0,
                         ws=None, return_kl: bool = False):
     """Dense warmup backward (proxy KL over the full causal prefix).  Returns grads (and the KL

@@ -253,6 +253,8 @@ def test_host_validation_errors():
     with pytest.raises(msa.MSAError, match="workspace"):
         msa.msa_forward(g["q"], g["k"], g["v"], g["qp"], g["kp"], 2, w.scale, ws=small)
     assert msa.msa_workspace_size(shape, msa.OP_FORWARD) > 0
+    with pytest.raises(msa.MSAError, match="one device"):  # every argument on the data's device
+        msa.msa_forward(g["q"], g["k"].cpu(), g["v"], g["qp"], g["kp"], 2, w.scale)
 
 
 def test_autograd_function_matches_direct_calls():
