@@ -516,6 +516,14 @@ def run_decode(args):
         torch.cuda.synchronize()
     status = msa.msa_device_status(ws)
     sec = e0.elapsed_time(e1) / 1e3 / args.steps
+    # per-kernel CUDA-event times, from a separate loop after the timed region
+    msa.profile_begin()
+    for _ in range(args.steps):
+        step()
+    torch.cuda.synchronize()
+    prof = msa.profile_end()
+    kernels = {k: {"launches_per_step": c / args.steps, "ms_per_step": ms / args.steps}
+               for k, (c, ms) in sorted(prof.items(), key=lambda kv: -kv[1][1])}
     # bytes one step must read: every proxy-key row before the local block, the selected K and V
     # blocks of every (sequence, KV head), the queries; and write: outputs and selection
     kp_bytes = B * (S - 128) * D * 2
@@ -534,7 +542,8 @@ def run_decode(args):
                          "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": gbs / peaks["hbm_gbs"], "traffic": None,
                          "peak_note": f"copy bandwidth {peak_src}"},
-            "gpu_launches": 3 * args.steps, "clocks": clk.summary(), "device_status": status}
+            "gpu_launches": 3 * args.steps, "clocks": clk.summary(), "device_status": status,
+            "kernels": kernels}
     print(json.dumps(line), flush=True)
 
 

@@ -697,9 +697,19 @@ int msa_decode(const msa_shape_t* shape, const void* q, const void* qp, const vo
   cudaGetLastError();
   unsigned* status = at<unsigned>(workspace, p.status);
   cudaMemsetAsync(status, 0, 32 * sizeof(unsigned), st);  // status, counters, wait place
-  g_launches.fetch_add(3, std::memory_order_relaxed);  // scores, selection, attention
-  launch_decode(d, q, qp, k_cache, v_cache, kp_cache, seq_len, block_idx, o, lse,
-                at<float>(workspace, p.scores), status, st);
+  float* scores = at<float>(workspace, p.scores);
+  bool ok = true;
+  timed("decode_scores", st, [&] {
+    ok = launch_decode_scores(d, qp, kp_cache, seq_len, scores, status, st);
+  });
+  if (!ok) {
+    set_err("msa_decode: could not create TMA tensor maps (cuTensorMapEncodeTiled)");
+    return MSA_ERR_CUDA;
+  }
+  timed("decode_select", st, [&] { launch_decode_select(d, scores, seq_len, block_idx, st); });
+  timed("decode_attn", st, [&] {
+    launch_decode_attn(d, q, k_cache, v_cache, seq_len, block_idx, o, lse, st);
+  });
   return cuda_fail("msa_decode");
 }
 

@@ -18,6 +18,8 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "sm100.cuh"
+#include "tmap.h"
 
 namespace msa {
 namespace {
@@ -29,57 +31,125 @@ __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 
 
 }  // namespace
 
-// grid (ceil(nblk / kScoreBlocks), B), 128 threads (thread = key of the block); NP >= Hp.
-constexpr int kScoreBlocks = 4;
+// grid (ceil(nblk / kScoreBlocks), B), 128 threads.  Per CTA: kScoreBlocks consecutive key blocks
+// of sequence b, loaded by TMA (the proxy-key cache rows of a block are contiguous: 32 KB), and one
+// tcgen05 product per block, S^T = Kp_block Qp^T (M = 128 keys, N = NP >= Hp proxy heads, the
+// rows beyond Hp zero), into tensor memory; thread = key then reads its NP scores and the warps
+// reduce each head's maximum over the block.  The products are exact bf16 x bf16 in fp32, summed
+// in the tensor core's order, as in the training selection kernel.
+constexpr int kScoreBlocks = 3;  // 3 x 32 KB of proxy keys in flight per CTA, two CTAs per SM
+constexpr int kKpBlock = kBlock * kD * 2;
+template <int NP>
+struct ScoreShared {
+  uint64_t kv_full[kScoreBlocks], s_full[kScoreBlocks], mma_done;
+  uint32_t tmem;
+  float wmax[kScoreBlocks][4][NP];  // per block, warp and head: the warp's maximum
+};
 template <int NP>
 __global__ void __launch_bounds__(128)
-    decode_scores_kernel(Dims d, const bf16* __restrict__ qp, const bf16* __restrict__ kp_cache,
+    decode_scores_kernel(const __grid_constant__ CUtensorMap tm_kp, Dims d, const bf16* __restrict__ qp,
                          const int32_t* __restrict__ seq_len, float* __restrict__ scores,
                          unsigned* status) {
-  extern __shared__ float sq[];  // [Hp][128] proxy queries, then [4 warps][Hp] block maxima
-  float* wmax = sq + d.Hp * kD;
+  using namespace sm100;
+  extern __shared__ uint8_t smem_raw[];
+  ScoreShared<NP>* sh = reinterpret_cast<ScoreShared<NP>*>(smem_raw);
+  uint8_t* sK = align1024(smem_raw + sizeof(ScoreShared<NP>));  // [kScoreBlocks][128 keys][128 d]
+  uint8_t* sQ = sK + kScoreBlocks * kKpBlock;                    // [NP rows][128 d], K-major
   const int b = blockIdx.y, tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
   const int len = seq_len[b];
   if (len < 1 || len > d.S) {
     if (tid == 0) atomicOr(status, kStatusBadIndex);
     return;
   }
-  const int m = (len - 1) / kBlock;  // local block of the new token
-  for (int x = tid; x < d.Hp * kD; x += blockDim.x) sq[x] = __bfloat162float(qp[(size_t)b * d.Hp * kD + x]);
-  __syncthreads();
-  for (int n = blockIdx.x * kScoreBlocks; n < min(m, (int)(blockIdx.x + 1) * kScoreBlocks); ++n) {
-    const uint4* row = reinterpret_cast<const uint4*>(kp_cache + ((size_t)b * d.S + n * kBlock + tid) * kD);
-    float acc[NP];
-#pragma unroll
-    for (int p = 0; p < NP; ++p) acc[p] = 0.f;
-#pragma unroll 4
-    for (int c = 0; c < 16; ++c) {
-      const uint4 w = __ldg(row + c);
-      const float x[8] = {bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y),
-                          bf_lo(w.z), bf_hi(w.z), bf_lo(w.w), bf_hi(w.w)};
-#pragma unroll
-      for (int p = 0; p < NP; ++p) {
-        if (p < d.Hp) {
-          const float* qv = sq + p * kD + c * 8;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) acc[p] = fmaf(qv[e], x[e], acc[p]);
-        }
-      }
+  const int m = (len - 1) / kBlock;  // local block of the new token (forced, never scored)
+  const int n0 = blockIdx.x * kScoreBlocks;
+  const int nb = min(kScoreBlocks, m - n0);  // blocks of this CTA before the local one
+  if (nb <= 0) return;
+  if (tid == 0) {
+    for (int x = 0; x < kScoreBlocks; ++x) {
+      mbar_init(&sh->kv_full[x], 1);
+      mbar_init(&sh->s_full[x], 1);
     }
+    mbar_init(&sh->mma_done, 1);
+    mbar_fence_init();
+  }
+  if (warp == 0) {
+    __syncwarp();  // lane 0 initialised the barriers alone; the allocation is warp-collective
+    tmem_alloc(&sh->tmem, 128);
+    tmem_relinquish();
+  }
+  // the proxy queries as the B operand: SW128 K-major rows, rows Hp .. NP-1 zero
+  for (int x = tid; x < NP * 16; x += 128) {
+    const int r = x >> 4, ch = x & 15;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (r < d.Hp) v = *reinterpret_cast<const uint4*>(qp + ((size_t)b * d.Hp + r) * kD + ch * 8);
+    *reinterpret_cast<uint4*>(sQ + (ch >> 3) * (NP * 128) + sw128_chunk(r, ch & 7)) = v;
+  }
+  fence_async_smem();  // generic-proxy writes before the tensor core's reads
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = sh->tmem;
+  if (tid == 0) {
+    tma_prefetch_desc(&tm_kp);
+    for (int x = 0; x < nb; ++x) {
+      const int row = b * d.S + (n0 + x) * kBlock;
+      mbar_expect_tx(&sh->kv_full[x], kKpBlock);
+      tma_load_2d(sK + x * kKpBlock, &tm_kp, 0, row, &sh->kv_full[x]);
+      tma_load_2d(sK + x * kKpBlock + kKpBlock / 2, &tm_kp, 64, row, &sh->kv_full[x]);
+    }
+    constexpr uint32_t id = idesc_bf16(128, NP, false, false);
+    const uint32_t aQ = smem_u32(sQ);
+    for (int x = 0; x < nb; ++x) {
+      if (!mbar_wait(&sh->kv_full[x], 0, status)) break;
+      fence_after_sync();
+      const uint32_t aK = smem_u32(sK + x * kKpBlock);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks)
+        mma_ss(tmem + x * NP, desc_kmajor(aK, 128, ks), desc_kmajor(aQ, NP, ks), id, ks > 0);
+      mma_commit(&sh->s_full[x]);
+    }
+    mma_commit(&sh->mma_done);  // arrives once every product issued above has completed
+  }
+  __syncwarp();
+  // thread = key (tensor-memory lane 32 warp + lane): its NP head scores, then each head's
+  // maximum over the warp's 32 keys
+  const uint32_t lrow = static_cast<uint32_t>(warp * 32) << 16;
+  bool ok = true;
+  for (int x = 0; x < nb; ++x) {
+    if (!mbar_wait_warp(&sh->s_full[x], 0, status)) {
+      ok = false;
+      break;
+    }
+    fence_after_sync();
+    uint32_t v[NP];
+    if constexpr (NP == 16) tmem_ld16(tmem + lrow + x * NP, v);
+    else tmem_ld32(tmem + lrow + x * NP, v);
+    tmem_wait_ld();
 #pragma unroll
     for (int p = 0; p < NP; ++p) {
       if (p < d.Hp) {
-        float v = acc[p];
+        float mx = __uint_as_float(v[p]);
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
-        if (lane == 0) wmax[warp * d.Hp + p] = v;
+        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        if (lane == 0) sh->wmax[x][warp][p] = mx;
       }
     }
-    __syncthreads();
-    if (tid < d.Hp)
-      scores[((size_t)b * d.Hp + tid) * d.nblk + n] =
-          fmaxf(fmaxf(wmax[tid], wmax[d.Hp + tid]), fmaxf(wmax[2 * d.Hp + tid], wmax[3 * d.Hp + tid]));
-    __syncthreads();
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (ok && tid < d.Hp)
+    for (int x = 0; x < nb; ++x)
+      scores[((size_t)b * d.Hp + tid) * d.nblk + n0 + x] =
+          fmaxf(fmaxf(sh->wmax[x][0][tid], sh->wmax[x][1][tid]),
+                fmaxf(sh->wmax[x][2][tid], sh->wmax[x][3][tid]));
+  if (warp == 0) {
+    // no product may still write tensor memory, and no copy may still land in shared memory,
+    // when the block exits
+    mbar_wait_warp(&sh->mma_done, 0, status);
+    for (int x = 0; x < nb; ++x) mbar_wait_warp(&sh->kv_full[x], 0, status);
+    tmem_dealloc(tmem, 128);
   }
 }
 
@@ -260,21 +330,31 @@ __global__ void __launch_bounds__(32 * G)
   if (lane == 0) lse[(size_t)b * d.Hq + h] = l > 0.f ? (mr + log2f(l)) * kLn2 : -INFINITY;
 }
 
-void launch_decode(const Dims& d, const void* q, const void* qp, const void* k_cache,
-                   const void* v_cache, const void* kp_cache, const int32_t* seq_len,
-                   int32_t* block_idx, void* o, float* lse, float* scores, unsigned* status,
-                   cudaStream_t st) {
+bool launch_decode_scores(const Dims& d, const void* qp, const void* kp_cache,
+                          const int32_t* seq_len, float* scores, unsigned* status,
+                          cudaStream_t st) {
+  CUtensorMap mkp;  // the proxy-key cache as rows of 128: box = one 64-column panel of a block
+  const uint64_t kpd[2] = {128, (uint64_t)d.B * d.S};
+  const uint64_t kps[1] = {128 * 2};
+  const uint32_t kpb[2] = {64, 128};
+  if (!make_tmap_bf16(&mkp, kp_cache, 2, kpd, kps, kpb)) return false;
   const dim3 g1((d.nblk + kScoreBlocks - 1) / kScoreBlocks, d.B);
-  const size_t sm1 = (size_t)(d.Hp * kD + 4 * d.Hp) * sizeof(float);
-#define MSA_SC(NP) decode_scores_kernel<NP><<<g1, 128, sm1, st>>>(d, (const bf16*)qp, \
-                           (const bf16*)kp_cache, seq_len, scores, status)
-  if (d.Hp <= 1) MSA_SC(1);
-  else if (d.Hp <= 2) MSA_SC(2);
-  else if (d.Hp <= 4) MSA_SC(4);
-  else if (d.Hp <= 8) MSA_SC(8);
-  else if (d.Hp <= 16) MSA_SC(16);
-  else MSA_SC(32);
+#define MSA_SC(NP)                                                                               \
+  {                                                                                              \
+    const size_t sm = sizeof(ScoreShared<NP>) + 1024 + kScoreBlocks * (size_t)kKpBlock + NP * 256; \
+    cudaFuncSetAttribute(decode_scores_kernel<NP>, cudaFuncAttributeMaxDynamicSharedMemorySize,   \
+                         (int)sm);                                                               \
+    decode_scores_kernel<NP><<<g1, 128, sm, st>>>(mkp, d, (const bf16*)qp, seq_len, scores,      \
+                                                  status);                                       \
+  }
+  if (d.Hp <= 16) MSA_SC(16)
+  else MSA_SC(32)
 #undef MSA_SC
+  return true;
+}
+
+void launch_decode_select(const Dims& d, const float* scores, const int32_t* seq_len,
+                          int32_t* block_idx, cudaStream_t st) {
   const long long rows = (long long)d.B * d.Hp;
   const int g2 = (int)((rows * 32 + 127) / 128);
   if (d.top_k <= 8)
@@ -285,6 +365,11 @@ void launch_decode(const Dims& d, const void* q, const void* qp, const void* k_c
     decode_select_kernel<32><<<g2, 128, 0, st>>>(d, scores, seq_len, block_idx);
   else
     decode_select_kernel<64><<<g2, 128, 0, st>>>(d, scores, seq_len, block_idx);
+}
+
+void launch_decode_attn(const Dims& d, const void* q, const void* k_cache, const void* v_cache,
+                        const int32_t* seq_len, const int32_t* block_idx, void* o, float* lse,
+                        cudaStream_t st) {
   const int g3 = d.B * d.Hp * d.R;
   const size_t sm3 = 2 * (size_t)kBlock * kRow * sizeof(bf16) + (size_t)d.G * kBlock * sizeof(float);
 #define MSA_DEC_CASE(GG)                                                                        \

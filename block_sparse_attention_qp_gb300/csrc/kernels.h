@@ -127,12 +127,17 @@ int bwd_group_tokens();  // tokens per proxy-gradient flush group
 void launch_convert(const float* src, void* dst, long long n, cudaStream_t st);
 
 // ---------------------------------------------------------------- decode (decode.cu)
-// One new token per sequence against its cache: proxy block scores (scores [B, Hp, nblk] fp32),
-// selection (block_idx [B, Hp, top_k]) and sparse attention (o [B, Hq, 128], lse [B, Hq]).
-void launch_decode(const Dims& d, const void* q, const void* qp, const void* k_cache,
-                   const void* v_cache, const void* kp_cache, const int32_t* seq_len,
-                   int32_t* block_idx, void* o, float* lse, float* scores, unsigned* status,
-                   cudaStream_t st);
+// One new token per sequence against its cache, in three launches: proxy block scores (scores
+// [B, Hp, nblk] fp32), selection (block_idx [B, Hp, top_k]) and sparse attention (o [B, Hq, 128],
+// lse [B, Hq]).
+bool launch_decode_scores(const Dims& d, const void* qp, const void* kp_cache,
+                          const int32_t* seq_len, float* scores, unsigned* status,
+                          cudaStream_t st);  // false: the tensor map could not be made
+void launch_decode_select(const Dims& d, const float* scores, const int32_t* seq_len,
+                          int32_t* block_idx, cudaStream_t st);
+void launch_decode_attn(const Dims& d, const void* q, const void* k_cache, const void* v_cache,
+                        const int32_t* seq_len, const int32_t* block_idx, void* o, float* lse,
+                        cudaStream_t st);
 
 int num_sms();
 void set_api_error(const char* what);
