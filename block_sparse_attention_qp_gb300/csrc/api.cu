@@ -708,8 +708,12 @@ int msa_decode(const msa_shape_t* shape, const void* q, const void* qp, const vo
   }
   timed("decode_select", st, [&] { launch_decode_select(d, scores, seq_len, block_idx, st); });
   timed("decode_attn", st, [&] {
-    launch_decode_attn(d, q, k_cache, v_cache, seq_len, block_idx, o, lse, st);
+    ok = launch_decode_attn(d, q, k_cache, v_cache, seq_len, block_idx, o, lse, status, st);
   });
+  if (!ok) {
+    set_err("msa_decode: could not create TMA tensor maps (cuTensorMapEncodeTiled)");
+    return MSA_ERR_CUDA;
+  }
   return cuda_fail("msa_decode");
 }
 

@@ -3,17 +3,15 @@
 // "Proxy attention" and "Main attention" define the two stages).  One new token per sequence b,
 // at position t_b = seq_len[b] - 1 of its cache (its own K, V and proxy key already written there):
 //   1. decode_scores_kernel: c[b, p, n] = max over the 128 keys j of block n of qp[b, p] . kp[b, j]
-//      for every block n < t_b / 128 (the local block is forced and never scored).  One thread per
-//      key streams the proxy-key cache once for all Hp proxy heads.
+//      for every block n < t_b / 128 (the local block is forced and never scored): proxy-key
+//      blocks by TMA, one tcgen05 product per block (keys x proxy heads), block maxima by warps.
 //   2. decode_select_kernel: one warp per (b, p) keeps each lane's best top_k - 1 blocks sorted in
 //      registers, then merges the lanes by repeated warp arg-max (ties to the lower block), adds the
 //      local block and writes the selection ascending, padded with -1.
-//   3. decode_attn_kernel: one block per (b, attention group a), one warp per query head: each
-//      selected K / V block is staged in shared memory (rows padded to 272 bytes, so 16-byte reads
-//      of eight rows hit distinct banks), the warp's lanes score 4 keys each, online softmax across
-//      blocks, and the lanes accumulate O over 4 head-dim columns each.
+//   3. decode_attn_kernel: one block per (b, attention group a): the selected K / V blocks by TMA
+//      (two stages), S^T and O^T of each block on the tensor core, online softmax across blocks.
 // The whole step reads the proxy-key cache once and the selected K / V blocks once: it is bound by
-// memory traffic, so it runs on CUDA cores.
+// memory traffic; the tensor core keeps the arithmetic off its critical path.
 #include <math.h>
 
 #include "common.cuh"
@@ -22,14 +20,6 @@
 #include "tmap.h"
 
 namespace msa {
-namespace {
-
-constexpr int kRow = kD + 8;  // padded bf16 row of a staged K / V block (272 bytes)
-
-__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
-}  // namespace
 
 // grid (ceil(nblk / kScoreBlocks), B), 128 threads.  Per CTA: kScoreBlocks consecutive key blocks
 // of sequence b, loaded by TMA (the proxy-key cache rows of a block are contiguous: 32 KB), and one
@@ -236,98 +226,234 @@ __global__ void __launch_bounds__(128)
   }
 }
 
-// One block per (b, attention group a), G warps (warp = query head a G + w).
-template <int G>
-__global__ void __launch_bounds__(32 * G)
-    decode_attn_kernel(Dims d, const bf16* __restrict__ q, const bf16* __restrict__ k_cache,
-                       const bf16* __restrict__ v_cache, const int32_t* __restrict__ seq_len,
+// One block per (b, attention group a): the group's G <= 16 query heads against its selected
+// blocks of the caches, on the tensor core.  Per selected block n (K and V by TMA, two stages):
+//   S^T = K_n Q^T         (M = 128 keys, N = 16: the G heads, the rest zero)   -> tensor memory
+//   thread = key: the block's maximum of each head, P = exp2(scale log2(e) S - m), row sums;
+//   P (bf16, [16 heads][128 keys]) -> shared memory
+//   O_n^T = V_n^T P^T     (M = 128 head dims, N = 16)                         -> tensor memory
+//   thread = head dim: O += O_n^T rescaled online (flash decoding over the selected blocks).
+// Warps 0-3 softmax / accumulate, warp 4 TMA, warp 5 MMA issue.  Every wait is bounded.
+constexpr int kAttnThreads = 192;
+constexpr int kNH = 16;                   // MMA N: heads of the group, padded
+constexpr int kKVTile = kBlock * kD * 2;  // one 128 x 128 bf16 tile (32 KB)
+struct AttnShared {
+  uint64_t kv_full[2], kv_empty[2], s_full, p_full, o_full, mma_done;
+  uint32_t tmem;
+  int nsel;
+  int sel[64];            // the valid selected blocks, in order
+  float wred[4][kNH];     // per warp and head: block maximum, then block sum
+};
+__global__ void __launch_bounds__(kAttnThreads)
+    decode_attn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                       Dims d, const bf16* __restrict__ q, const int32_t* __restrict__ seq_len,
                        const int32_t* __restrict__ block_idx, bf16* __restrict__ o,
-                       float* __restrict__ lse) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  bf16* sK = reinterpret_cast<bf16*>(smem);  // [128 keys][kRow]
-  bf16* sV = sK + kBlock * kRow;             // [128 keys][kRow]
-  float* sP = reinterpret_cast<float*>(sV + kBlock * kRow);  // [G][128] probabilities
-  const int tid = threadIdx.x, lane = tid % 32, w = tid / 32;
-  const int Ha = d.Hp * d.R;
+                       float* __restrict__ lse, unsigned* status) {
+  using namespace sm100;
+  extern __shared__ uint8_t smem_raw[];
+  AttnShared* sh = reinterpret_cast<AttnShared*>(smem_raw);
+  uint8_t* sK = align1024(smem_raw + sizeof(AttnShared));  // [2 stages][128 keys][128 d]
+  uint8_t* sV = sK + 2 * kKVTile;                           // [2 stages][128 keys][128 d]
+  uint8_t* sQ = sV + 2 * kKVTile;                           // [16 heads][128 d], K-major
+  uint8_t* sP = sQ + kNH * kD * 2;                          // [16 heads][128 keys], K-major
+  const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
+  const int G = d.G, Ha = d.Hp * d.R;
   const int b = blockIdx.x / Ha, a = blockIdx.x % Ha;
-  const int p = a / d.R, kvh = d.kv_of(a), h = a * G + w;
+  const int p = a / d.R, kvh = d.kv_of(a);
   const int len = seq_len[b];
   if (len < 1 || len > d.S) return;  // flagged by decode_scores_kernel
   const int t = len - 1;
-  const float sl2 = d.scale * kLog2e;
-  // this lane's query slice: dims 4 lane .. 4 lane + 3 (for the scores, the warp reduces)
-  float qv[4];
-  {
-    const uint2 u = *reinterpret_cast<const uint2*>(q + ((size_t)b * d.Hq + h) * kD + 4 * lane);
-    qv[0] = bf_lo(u.x);
-    qv[1] = bf_hi(u.x);
-    qv[2] = bf_lo(u.y);
-    qv[3] = bf_hi(u.y);
-  }
-  float mr = -INFINITY, l = 0.f, oacc[4] = {0.f, 0.f, 0.f, 0.f};
-  const int32_t* sel = block_idx + ((size_t)b * d.Hp + p) * d.top_k;
-  for (int s = 0; s < d.top_k; ++s) {
-    const int n = sel[s];
-    if (n < 0 || n > t / kBlock) continue;  // padding (or an invalid index: skipped)
-    __syncthreads();  // the previous block's tiles are no longer read
-    for (int x = tid; x < kBlock * 16; x += blockDim.x) {  // 16-byte chunks of 128 rows
-      const int r = x >> 4, ch = x & 15;
-      const size_t g = (((size_t)b * d.S + n * kBlock + r) * d.Hkv + kvh) * kD + ch * 8;
-      cp_async16(sK + r * kRow + ch * 8, k_cache + g);
-      cp_async16(sV + r * kRow + ch * 8, v_cache + g);
+  if (tid == 0) {
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&sh->kv_full[x], 1);
+      mbar_init(&sh->kv_empty[x], 1);
     }
-    cp_async_commit();
-    cp_async_wait_all();
-    __syncthreads();
-    const int lim = min(kBlock - 1, t - n * kBlock);  // visible keys 0 .. lim
-    // scores: for each key, the warp's lanes hold 4 dims each and reduce across the warp;
-    // lane j keeps the scores of keys j, j + 32, j + 64, j + 96
-    float sc[4];
+    mbar_init(&sh->s_full, 1);
+    mbar_init(&sh->p_full, 1);
+    mbar_init(&sh->o_full, 1);
+    mbar_init(&sh->mma_done, 1);
+    mbar_fence_init();
+    const int32_t* sel = block_idx + ((size_t)b * d.Hp + p) * d.top_k;
+    int c = 0;
+    for (int s = 0; s < d.top_k; ++s) {
+      const int n = sel[s];
+      if (n >= 0 && n <= t / kBlock) sh->sel[c++] = n;  // padding (or an invalid index) skipped
+    }
+    sh->nsel = c;
+  }
+  if (warp == 0) {
+    __syncwarp();
+    tmem_alloc(&sh->tmem, 64);  // S^T: columns 0-15, O^T: 32-47
+    tmem_relinquish();
+  }
+  // Q rows of the group's heads (rows >= G zero) and P zero-initialised, as SW128 K-major tiles
+  for (int x = tid; x < kNH * 16; x += kAttnThreads) {
+    const int r = x >> 4, ch = x & 15;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (r < G) v = *reinterpret_cast<const uint4*>(q + ((size_t)b * d.Hq + a * G + r) * kD + ch * 8);
+    *reinterpret_cast<uint4*>(sQ + (ch >> 3) * (kNH * 128) + sm100::sw128_chunk(r, ch & 7)) = v;
+    *reinterpret_cast<uint4*>(sP + (ch >> 3) * (kNH * 128) + sm100::sw128_chunk(r, ch & 7)) =
+        make_uint4(0u, 0u, 0u, 0u);
+  }
+  fence_async_smem();
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = sh->tmem, tS = tmem, tO = tmem + 32;
+  const int nsel = sh->nsel;
+  if (warp == 4) {
+    // ---- TMA: K and V of selected block i into stage i & 1
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      for (int i = 0; i < nsel; ++i) {
+        const int st = i & 1;
+        if (i >= 2 && !mbar_wait(&sh->kv_empty[st], ((i - 2) >> 1) & 1, status)) break;
+        const int row = b * d.S + sh->sel[i] * kBlock;
+        mbar_expect_tx(&sh->kv_full[st], 2 * kKVTile);
+        tma_load_3d(sK + st * kKVTile, &tm_k, 0, kvh, row, &sh->kv_full[st]);
+        tma_load_3d(sK + st * kKVTile + kKVTile / 2, &tm_k, 64, kvh, row, &sh->kv_full[st]);
+        tma_load_3d(sV + st * kKVTile, &tm_v, 0, kvh, row, &sh->kv_full[st]);
+        tma_load_3d(sV + st * kKVTile + kKVTile / 2, &tm_v, 64, kvh, row, &sh->kv_full[st]);
+      }
+      // no copy may still be landing in shared memory when the block exits
+      for (int i = nsel >= 2 ? nsel - 2 : 0; i < nsel; ++i)
+        mbar_wait(&sh->kv_full[i & 1], (i >> 1) & 1, status);
+    }
+  } else if (warp == 5) {
+    // ---- MMA issue: S^T of block i + 1 goes in behind O^T of block i
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16(128, kNH, false, false);  // S^T = K Q^T
+      constexpr uint32_t id_o = idesc_bf16(128, kNH, true, false);   // O^T = V^T P^T
+      const uint32_t aQ = smem_u32(sQ), aP = smem_u32(sP);
+      auto issue_s = [&](int i) -> bool {
+        if (!mbar_wait(&sh->kv_full[i & 1], (i >> 1) & 1, status)) return false;
+        fence_after_sync();
+        const uint32_t aK = smem_u32(sK + (i & 1) * kKVTile);
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      sc[kk] = -INFINITY;
-#pragma unroll 4
-      for (int j2 = 0; j2 < 32; ++j2) {
-        const int j = kk * 32 + j2;
-        const uint2 u = *reinterpret_cast<const uint2*>(sK + j * kRow + 4 * lane);
-        float v = qv[0] * bf_lo(u.x) + qv[1] * bf_hi(u.x) + qv[2] * bf_lo(u.y) + qv[3] * bf_hi(u.y);
+        for (int ks = 0; ks < 8; ++ks)
+          mma_ss(tS, desc_kmajor(aK, 128, ks), desc_kmajor(aQ, kNH, ks), id_s, ks > 0);
+        mma_commit(&sh->s_full);
+        return true;
+      };
+      bool ok = nsel > 0 && issue_s(0);
+      for (int i = 0; ok && i < nsel; ++i) {
+        // the softmax has read S^T of block i and written its P (shared memory)
+        if (!mbar_wait(&sh->p_full, i & 1, status)) break;
+        fence_after_sync();
+        const uint32_t aV = smem_u32(sV + (i & 1) * kKVTile);
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-        if (j2 == lane) sc[kk] = j <= lim ? v * sl2 : -INFINITY;
+        for (int ks = 0; ks < 8; ++ks)
+          mma_ss(tO, desc_mnmajor(aV, 128, ks), desc_kmajor(aP, kNH, ks), id_o, ks > 0);
+        mma_commit(&sh->o_full);
+        mma_commit(&sh->kv_empty[i & 1]);  // K and V of this stage are no longer read
+        if (i + 1 < nsel) ok = issue_s(i + 1);
+      }
+      mma_commit(&sh->mma_done);
+    }
+  } else {
+    // ---- softmax (thread = key) and accumulation (thread = head dimension), per block
+    const int kr = tid;  // key row of S^T, head dimension of O^T (tensor-memory lane)
+    const uint32_t lrow = static_cast<uint32_t>(warp * 32) << 16;
+    const float sl2 = d.scale * kLog2e;
+    float mrun[kNH], l[kNH], oacc[kNH];
+#pragma unroll
+    for (int h = 0; h < kNH; ++h) {
+      mrun[h] = -INFINITY;
+      l[h] = 0.f;
+      oacc[h] = 0.f;
+    }
+    // The four warps pass the same named barriers in every block whatever happens: a wait that
+    // gives up only clears `ok` (warp-uniform), which skips the later waits and tensor-memory
+    // reads, so no warp can be left at a barrier.
+    bool ok = true;
+    for (int i = 0; i < nsel; ++i) {
+      const int n = sh->sel[i];
+      const int lim = min(kBlock - 1, t - n * kBlock);  // visible keys 0 .. lim
+      if (ok) ok = mbar_wait_warp(&sh->s_full, i & 1, status);
+      fence_after_sync();
+      uint32_t v[kNH];
+#pragma unroll
+      for (int h = 0; h < kNH; ++h) v[h] = 0u;
+      if (ok) {
+        tmem_ld16(tS + lrow, v);
+        tmem_wait_ld();
+      }
+      float sc[kNH];
+#pragma unroll
+      for (int h = 0; h < kNH; ++h) {
+        sc[h] = kr <= lim ? __uint_as_float(v[h]) * sl2 : -INFINITY;
+        float mx = sc[h];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        if (lane == 0) sh->wred[warp][h] = mx;
+      }
+      fence_before_sync();
+      bar_sync(1, 128);
+      fence_after_sync();
+      float mnew[kNH], alpha[kNH];
+#pragma unroll
+      for (int h = 0; h < kNH; ++h) {
+        const float bm = fmaxf(fmaxf(sh->wred[0][h], sh->wred[1][h]), fmaxf(sh->wred[2][h], sh->wred[3][h]));
+        mnew[h] = fmaxf(mrun[h], bm);  // key 0 of every selected block is visible: finite
+        alpha[h] = exp2f(mrun[h] - mnew[h]);  // 0 on the first block
+        mrun[h] = mnew[h];
+      }
+      bar_sync(1, 128);  // every warp has read the maxima before they are overwritten by sums
+      // P of this key for every head, bf16, into row h of the K-major P tile (heads >= G stay 0)
+      const uint32_t prow = (uint32_t)(kr >> 6) * (kNH * 128);
+#pragma unroll
+      for (int h = 0; h < kNH; ++h) {
+        const float pv = h < G ? exp2f(sc[h] - mnew[h]) : 0.f;  // masked keys: exp2(-inf) = 0
+        *reinterpret_cast<bf16*>(sP + prow + sm100::sw128_offset(h, kr & 63)) = __float2bfloat16_rn(pv);
+        float sum = pv;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+        if (lane == 0) sh->wred[warp][h] = sum;
+      }
+      fence_async_smem();  // P (generic-proxy stores) before the tensor core's reads
+      fence_before_sync();
+      bar_sync(1, 128);
+      fence_after_sync();
+      if (tid == 0) mbar_arrive(&sh->p_full);  // S^T read, P written
+#pragma unroll
+      for (int h = 0; h < kNH; ++h)
+        l[h] = l[h] * alpha[h] + (sh->wred[0][h] + sh->wred[1][h] + sh->wred[2][h] + sh->wred[3][h]);
+      // O += O_n^T, the running sum rescaled (thread = head dimension kr)
+      if (ok) ok = mbar_wait_warp(&sh->o_full, i & 1, status);
+      fence_after_sync();
+      uint32_t ov[kNH];
+#pragma unroll
+      for (int h = 0; h < kNH; ++h) ov[h] = 0u;
+      if (ok) {
+        tmem_ld16(tO + lrow, ov);
+        tmem_wait_ld();
+      }
+#pragma unroll
+      for (int h = 0; h < kNH; ++h) oacc[h] = oacc[h] * alpha[h] + __uint_as_float(ov[h]);
+      fence_before_sync();
+      bar_sync(1, 128);  // everyone has read O^T and the sums before the next block reuses them
+      fence_after_sync();
+    }
+    if (ok) {
+#pragma unroll
+      for (int h = 0; h < kNH; ++h) {
+        if (h < G) {
+          const float inv = l[h] > 0.f ? 1.f / l[h] : 0.f;
+          o[((size_t)b * d.Hq + a * G + h) * kD + kr] = __float2bfloat16_rn(oacc[h] * inv);
+          if (kr == 0)
+            lse[(size_t)b * d.Hq + a * G + h] = l[h] > 0.f ? (mrun[h] + log2f(l[h])) * kLn2 : -INFINITY;
+        }
       }
     }
-    float bm = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, off));
-    const float mn = fmaxf(mr, bm);  // key 0 of the local block is always visible: finite
-    const float alpha = exp2f(mr - mn);  // mr = -inf on the first block: 0
-    float ps = 0.f;
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-      const float pv = exp2f(sc[kk] - mn);
-      sP[w * kBlock + kk * 32 + lane] = pv;
-      ps += pv;
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
-    l = l * alpha + ps;
-    mr = mn;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) oacc[e] *= alpha;
-    __syncwarp();
-    for (int j = 0; j <= lim; ++j) {  // O += P V over this lane's 4 columns
-      const float pv = sP[w * kBlock + j];
-      const uint2 u = *reinterpret_cast<const uint2*>(sV + j * kRow + 4 * lane);
-      oacc[0] = fmaf(pv, bf_lo(u.x), oacc[0]);
-      oacc[1] = fmaf(pv, bf_hi(u.x), oacc[1]);
-      oacc[2] = fmaf(pv, bf_lo(u.y), oacc[2]);
-      oacc[3] = fmaf(pv, bf_hi(u.y), oacc[3]);
-    }
   }
-  const float inv = l > 0.f ? 1.f / l : 0.f;
-  *reinterpret_cast<uint2*>(o + ((size_t)b * d.Hq + h) * kD + 4 * lane) =
-      make_uint2(pack_bf16(oacc[0] * inv, oacc[1] * inv), pack_bf16(oacc[2] * inv, oacc[3] * inv));
-  if (lane == 0) lse[(size_t)b * d.Hq + h] = l > 0.f ? (mr + log2f(l)) * kLn2 : -INFINITY;
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (warp == 0) {
+    mbar_wait_warp(&sh->mma_done, 0, status);  // no product may still write tensor memory
+    tmem_dealloc(tmem, 64);
+  }
 }
 
 bool launch_decode_scores(const Dims& d, const void* qp, const void* kp_cache,
@@ -367,27 +493,20 @@ void launch_decode_select(const Dims& d, const float* scores, const int32_t* seq
     decode_select_kernel<64><<<g2, 128, 0, st>>>(d, scores, seq_len, block_idx);
 }
 
-void launch_decode_attn(const Dims& d, const void* q, const void* k_cache, const void* v_cache,
+bool launch_decode_attn(const Dims& d, const void* q, const void* k_cache, const void* v_cache,
                         const int32_t* seq_len, const int32_t* block_idx, void* o, float* lse,
-                        cudaStream_t st) {
-  const int g3 = d.B * d.Hp * d.R;
-  const size_t sm3 = 2 * (size_t)kBlock * kRow * sizeof(bf16) + (size_t)d.G * kBlock * sizeof(float);
-#define MSA_DEC_CASE(GG)                                                                        \
-  case GG:                                                                                      \
-    cudaFuncSetAttribute(decode_attn_kernel<GG>, cudaFuncAttributeMaxDynamicSharedMemorySize,   \
-                         (int)sm3);                                                             \
-    decode_attn_kernel<GG><<<g3, 32 * GG, sm3, st>>>(d, (const bf16*)q, (const bf16*)k_cache,   \
-                                                     (const bf16*)v_cache, seq_len, block_idx,  \
-                                                     (bf16*)o, lse);                            \
-    break;
-  switch (d.G) {
-    MSA_DEC_CASE(1)
-    MSA_DEC_CASE(2)
-    MSA_DEC_CASE(4)
-    MSA_DEC_CASE(8)
-    MSA_DEC_CASE(16)
-  }
-#undef MSA_DEC_CASE
+                        unsigned* status, cudaStream_t st) {
+  CUtensorMap mk, mv;  // the caches as [B S][Hkv][128]: box = one 64-column panel of a block
+  const uint64_t kvd[3] = {128, (uint64_t)d.Hkv, (uint64_t)d.B * d.S};
+  const uint64_t kvs[2] = {128 * 2, (uint64_t)d.Hkv * 128 * 2};
+  const uint32_t kvb[3] = {64, 1, 128};
+  if (!make_tmap_bf16(&mk, k_cache, 3, kvd, kvs, kvb) || !make_tmap_bf16(&mv, v_cache, 3, kvd, kvs, kvb))
+    return false;
+  const size_t sm = sizeof(AttnShared) + 1024 + 4 * (size_t)kKVTile + 2 * (size_t)kNH * kD * 2;
+  cudaFuncSetAttribute(decode_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  decode_attn_kernel<<<d.B * d.Hp * d.R, kAttnThreads, sm, st>>>(mk, mv, d, (const bf16*)q, seq_len,
+                                                                 block_idx, (bf16*)o, lse, status);
+  return true;
 }
 
 }  // namespace msa

@@ -135,9 +135,9 @@ bool launch_decode_scores(const Dims& d, const void* qp, const void* kp_cache,
                           cudaStream_t st);  // false: the tensor map could not be made
 void launch_decode_select(const Dims& d, const float* scores, const int32_t* seq_len,
                           int32_t* block_idx, cudaStream_t st);
-void launch_decode_attn(const Dims& d, const void* q, const void* k_cache, const void* v_cache,
+bool launch_decode_attn(const Dims& d, const void* q, const void* k_cache, const void* v_cache,
                         const int32_t* seq_len, const int32_t* block_idx, void* o, float* lse,
-                        cudaStream_t st);
+                        unsigned* status, cudaStream_t st);  // false: no tensor map
 
 int num_sms();
 void set_api_error(const char* what);
