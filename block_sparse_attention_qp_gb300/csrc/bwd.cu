@@ -189,6 +189,15 @@ __device__ __forceinline__ void bulk_reduce_add(float* g, uint32_t s, uint32_t b
       "r"(s), "r"(bytes), "l"(pol)
       : "memory");
 }
+// TMA tensor reduction: adds the fp32 box staged at shared address s into the tensor at
+// coordinates (c0, c1, c2); out-of-range elements of the box are skipped.
+__device__ __forceinline__ void tma_reduce_add_3d(const void* tmap, int c0, int c1, int c2, uint32_t s) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2, %3}], [%4];\n" ::"l"(
+          tmap),
+      "r"(c0), "r"(c1), "r"(c2), "r"(s)
+      : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read0() {
   asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
@@ -1179,7 +1188,8 @@ __global__ void __launch_bounds__(kWideThreads, 1)
 // shared memory, so the dz of one group overlaps the products and the flush of the previous one.
 template <bool kDense, bool kKL>
 __global__ void __launch_bounds__(384, 1)
-    proxy_bwd_kernel(const __grid_constant__ CUtensorMap tm_kp, ProxyArgs A) {
+    proxy_bwd_kernel(const __grid_constant__ CUtensorMap tm_kp, const __grid_constant__ CUtensorMap tm_qp,
+                     const __grid_constant__ CUtensorMap tm_dqp, ProxyArgs A) {
   using namespace sm100;
   const Dims& d = A.d;
   extern __shared__ uint8_t smem_raw[];
@@ -1397,17 +1407,31 @@ __global__ void __launch_bounds__(384, 1)
         sh->tokq[qb][32 * w + lane] = t_next;
         __syncwarp();
         uint8_t* dQb = sQp + qb * kRT;
+        if constexpr (kDense) {
+          // a dense group's tokens are consecutive (t_next of row 0 is the first): its proxy query
+          // rows come with two TMA boxes of 64 rows, one per 64-column panel (rows beyond the
+          // group's tokens load other rows -- their dz is zero -- or the fill value past the end)
+          if (w == 0 && lane == 0) {
+            mbar_expect_tx(&sh->qp_full[qb], kPG * kD * 2);  // also this lane's first arrival
+            tma_load_3d(dQb, &tm_qp, 0, g, b * d.S + t_next, &sh->qp_full[qb]);
+            tma_load_3d(dQb + kPG * 128, &tm_qp, 64, g, b * d.S + t_next, &sh->qp_full[qb]);
+          } else {
+            mbar_arrive(&sh->qp_full[qb]);
+          }
+          mbar_arrive(&sh->qp_full[qb]);  // publishes tokq
+        } else {
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {  // K-major SW128 rows, rows >= gcount zero-filled
-          const int c = lane + 32 * k;  // 16-byte chunk of this warp's 32 rows
-          const int r = 32 * w + (c >> 4), ch = c & 15;
-          const int t = sh->tokq[qb][r];
-          const uint32_t off = (ch >> 3) * (kPG * 128) + sm100::sw128_chunk(r, ch & 7);
-          const size_t grow = (((size_t)b * d.S + (t < 0 ? 0 : t)) * d.Hp + g) * kD + ch * 8;
-          cp_async16(dQb + off, A.qp + grow, t >= 0);
+          for (int k = 0; k < 16; ++k) {  // K-major SW128 rows, rows >= gcount zero-filled
+            const int c = lane + 32 * k;  // 16-byte chunk of this warp's 32 rows
+            const int r = 32 * w + (c >> 4), ch = c & 15;
+            const int t = sh->tokq[qb][r];
+            const uint32_t off = (ch >> 3) * (kPG * 128) + sm100::sw128_chunk(r, ch & 7);
+            const size_t grow = (((size_t)b * d.S + (t < 0 ? 0 : t)) * d.Hp + g) * kD + ch * 8;
+            cp_async16(dQb + off, A.qp + grow, t >= 0);
+          }
+          cp_async_arrive(&sh->qp_full[qb]);
+          mbar_arrive(&sh->qp_full[qb]);  // publishes tokq
         }
-        cp_async_arrive(&sh->qp_full[qb]);
-        mbar_arrive(&sh->qp_full[qb]);  // publishes tokq
         ++i;
         const int ngroups = (cur.count + kPG - 1) / kPG;
         if (gi + 1 < ngroups) {
@@ -1571,17 +1595,33 @@ __global__ void __launch_bounds__(384, 1)
         for (int k = 0; k < kPG; ++k)
           stg[k * 32 + lane] = __uint_as_float(k < 32 ? q0[k] : q1[k - 32]) * d.scale;
         __syncwarp();
+        if constexpr (kDense) {
+          // consecutive tokens: one TMA tensor reduction adds this warp's 64 tokens x 32 columns
+          // (the rows beyond the group's tokens hold exact zeros: their dz is zero)
+          fence_async_smem();  // the staging rows (generic-proxy stores) before the TMA reads them
+          __syncwarp();
+          if (lane == 0) {
+            tma_reduce_add_3d(&tm_dqp, 32 * w4, g, b * d.S + sh->tokq[qb][0], smem_u32(stg));
+            bulk_commit();
+            bulk_wait_read0();  // the staging rows may be overwritten by the next group
+          }
+          __syncwarp();
+        } else {
 #pragma unroll 4
-        for (int it2 = 0; it2 < kPG / 4; ++it2) {
-          const int k = it2 * 4 + lane / 8, c4 = lane % 8;
-          const float4 v = *reinterpret_cast<const float4*>(stg + k * 32 + 4 * c4);
-          const int t = k < gcount ? sh->tokq[qb][k] : -1;
-          red_add_v4_if(t >= 0,
-                        A.dqp + (((size_t)b * d.S + (t < 0 ? 0 : t)) * d.Hp + g) * kD + w4 * 32 + 4 * c4, v);
+          for (int it2 = 0; it2 < kPG / 4; ++it2) {
+            const int k = it2 * 4 + lane / 8, c4 = lane % 8;
+            const float4 v = *reinterpret_cast<const float4*>(stg + k * 32 + 4 * c4);
+            const int t = k < gcount ? sh->tokq[qb][k] : -1;
+            red_add_v4_if(t >= 0,
+                          A.dqp + (((size_t)b * d.S + (t < 0 ? 0 : t)) * d.Hp + g) * kD + w4 * 32 + 4 * c4, v);
+          }
+          __syncwarp();
         }
-        __syncwarp();
         if (lane == 0) mbar_arrive(&sh->qp_empty[qb]);  // token list of this buffer read
       }
+    }
+    if constexpr (kDense) {
+      if (lane == 0) bulk_wait0();  // every reduction has landed before the block exits
     }
   }
   fence_before_sync();
@@ -1607,12 +1647,13 @@ void attn_bwd_wide_g(const CUtensorMap& mk, const CUtensorMap& mv, const MainArg
   attn_bwd_wide_kernel<G, kDense><<<num_sms(), kWideThreads, smem, st>>>(mk, mv, a);
 }
 template <bool kDense, bool kKL>
-void proxy_bwd_g(const CUtensorMap& mkp, const ProxyArgs& a, cudaStream_t st) {
+void proxy_bwd_g(const CUtensorMap& mkp, const CUtensorMap& mqp, const CUtensorMap& mdqp,
+                 const ProxyArgs& a, cudaStream_t st) {
   const size_t smem = sizeof(ProxyShared) + 1024 + (size_t)kKV + kQPB * (size_t)kRT + 2 * (size_t)kST +
                       kNPB * (size_t)kPG * kBlock * 2 + 4 * (size_t)kPG * 32 * 4;
   cudaFuncSetAttribute(proxy_bwd_kernel<kDense, kKL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        (int)smem);
-  proxy_bwd_kernel<kDense, kKL><<<num_sms(), 384, smem, st>>>(mkp, a);
+  proxy_bwd_kernel<kDense, kKL><<<num_sms(), 384, smem, st>>>(mkp, mqp, mdqp, a);
 }
 
 __global__ void kl_finalize_kernel(const double* acc, float* out, double inv) {
@@ -1690,6 +1731,17 @@ bool launch_proxy_bwd(const Dims& d, bool dense, const void* qp, const void* kp,
   const uint64_t kps[1] = {128 * 2};
   const uint32_t kpb[2] = {64, 128};
   if (!make_tmap_bf16(&mkp, kp, 2, kpd, kps, kpb)) return false;
+  // dense groups (consecutive tokens): their proxy query rows and dQp rows as [B S][Hp][128]
+  CUtensorMap mqp = mkp, mdqp = mkp;  // (unused by the sparse kernel)
+  if (dense) {
+    const uint64_t qd[3] = {128, (uint64_t)d.Hp, (uint64_t)d.B * d.S};
+    const uint64_t qs[2] = {128 * 2, (uint64_t)d.Hp * 128 * 2};
+    const uint32_t qb[3] = {64, 1, (uint32_t)kPG};
+    const uint64_t fs[2] = {128 * 4, (uint64_t)d.Hp * 128 * 4};
+    const uint32_t fb[3] = {32, 1, (uint32_t)kPG};
+    if (!make_tmap_bf16(&mqp, qp, 3, qd, qs, qb) || !make_tmap_f32(&mdqp, dqp_acc, qd, fs, fb))
+      return false;
+  }
   ProxyArgs a;
   a.d = d;
   a.qp = (const bf16*)qp;
@@ -1710,9 +1762,9 @@ bool launch_proxy_bwd(const Dims& d, bool dense, const void* qp, const void* kp,
   a.sched = reinterpret_cast<int*>(status + kSchedProxyBwd);
   cudaMemsetAsync(a.sched, 0, sizeof(int), st);
   if (dense)
-    kl_acc ? proxy_bwd_g<true, true>(mkp, a, st) : proxy_bwd_g<true, false>(mkp, a, st);
+    kl_acc ? proxy_bwd_g<true, true>(mkp, mqp, mdqp, a, st) : proxy_bwd_g<true, false>(mkp, mqp, mdqp, a, st);
   else
-    kl_acc ? proxy_bwd_g<false, true>(mkp, a, st) : proxy_bwd_g<false, false>(mkp, a, st);
+    kl_acc ? proxy_bwd_g<false, true>(mkp, mqp, mdqp, a, st) : proxy_bwd_g<false, false>(mkp, mqp, mdqp, a, st);
   return true;
 }
 

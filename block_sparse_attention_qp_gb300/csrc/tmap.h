@@ -36,4 +36,19 @@ inline bool make_tmap_bf16(CUtensorMap* m, const void* base, int rank, const uin
   return r == CUDA_SUCCESS;
 }
 
+// Tensor of fp32 rows of 128 elements, unswizzled (for TMA reductions from row-major staging):
+// dims (128, d1, d2) with byte strides s1, s2; box (b0, b1, b2).
+inline bool make_tmap_f32(CUtensorMap* m, const void* base, const uint64_t* dims,
+                          const uint64_t* strides_bytes, const uint32_t* box) {
+  auto enc = tmap_encoder();
+  if (!enc) return false;
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base),
+                         (const cuuint64_t*)dims, (const cuuint64_t*)strides_bytes,
+                         (const cuuint32_t*)box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace msa
