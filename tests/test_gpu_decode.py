@@ -56,6 +56,9 @@ def _check_against_oracle(w, lens, seed):
     ("g4_k16", 4, 4096, 16, 4, 4, 16, [4096, 2000, 300, 3333]),
     ("hp_lt_hkv", 5, 1536, 16, 4, 2, 6, [1536, 1, 640, 641, 1000]),
     ("hp_gt_hkv_g2", 3, 768, 8, 2, 4, 3, [768, 129, 500]),
+    ("g16", 3, 640, 32, 2, 2, 4, [640, 200, 129]),      # 16 heads per group: the MMA's full N
+    ("g1", 3, 512, 4, 4, 4, 3, [512, 128, 300]),        # one head per group
+    ("hp32", 2, 384, 64, 32, 32, 3, [384, 250]),        # 32 proxy heads: the N = 32 score product
 ])
 def test_decode_matches_oracle_rows(name, B, S, Hq, Hkv, Hp, k, lens):
     w = Workload(name, B=B, S=S, Hq=Hq, Hkv=Hkv, Hp=Hp, top_k=k)
