@@ -145,6 +145,7 @@ struct Plan {
   size_t bytes = 0;
   long long max0 = 0, max1 = 0;
   ItemSpec spec0{1, 1}, spec1{1, 1};
+  int pass_chunks = 1;  // forward: sequence chunks per pass of the partial outputs
 };
 
 struct Carver {
@@ -197,7 +198,24 @@ Dims with_chunk(Dims d, int chunk) {
   return d;
 }
 
-Plan make_plan(const Dims& d, int op) {
+// The sparse forward's partial outputs (bf16 O and fp32 log-sum-exp per token, head and slot)
+// are produced and merged in passes over consecutive sequence chunks, so that they need not be
+// held for the whole sequence at once: by default a pass holds at most kFwdPartialBudget bytes of
+// them (one chunk at least).
+constexpr size_t kFwdPartialBudget = 8ull << 30;
+
+int pass_tokens(const Dims& d, int pass_chunks) {
+  const long long t = (long long)pass_chunks * d.chunk;
+  return (int)(t < d.S ? t : d.S);
+}
+
+int default_pass_chunks(const Dims& d) {
+  const size_t per_chunk = (size_t)d.B * d.chunk * d.Hq * d.top_k * (kD * sizeof(bf16) + sizeof(float));
+  const long long fit = (long long)(kFwdPartialBudget / per_chunk);
+  return (int)(fit < 1 ? 1 : fit > d.nchunk ? d.nchunk : fit);
+}
+
+Plan make_plan(const Dims& d, int op, int pass_chunks = 0) {
   Plan p;
   Carver c;
   const long long nseg = d.nlist();
@@ -222,8 +240,10 @@ Plan make_plan(const Dims& d, int op) {
     p.max0 = max_items(sparse_ent, d, p.spec0);
     p.io0 = c.take(nseg * sizeof(int));
     p.items0 = c.take(p.max0 * sizeof(Item));
-    p.opart = c.take((size_t)rows_q * d.top_k * kD * sizeof(bf16));
-    p.lpart = c.take((size_t)rows_q * d.top_k * sizeof(float));
+    p.pass_chunks = pass_chunks > 0 ? pass_chunks : default_pass_chunks(d);
+    const long long rows_pass = (long long)d.B * pass_tokens(d, p.pass_chunks) * d.Hq;
+    p.opart = c.take((size_t)rows_pass * d.top_k * kD * sizeof(bf16));
+    p.lpart = c.take((size_t)rows_pass * d.top_k * sizeof(float));
   }
   if (op == MSA_OP_BACKWARD || op == MSA_OP_WARMUP_BACKWARD) {
     const bool dense = op == MSA_OP_WARMUP_BACKWARD;
@@ -463,7 +483,17 @@ int msa_forward(const msa_shape_t* shape, const void* q, const void* k, const vo
   if (rc) return rc;
   if ((rc = check_ptrs({q, k, v, block_idx, o, lse}))) return rc;
   if (!indices_given && (rc = check_ptrs({qp, kp}))) return rc;
-  const Plan p = make_plan(d, MSA_OP_FORWARD);
+  // chunks per pass: the default, or as many as the given workspace holds (more or fewer)
+  Plan p = make_plan(d, MSA_OP_FORWARD);
+  {
+    int pc = p.pass_chunks;
+    if (workspace_bytes >= p.bytes) {
+      while (pc < d.nchunk && make_plan(d, MSA_OP_FORWARD, pc + 1).bytes <= workspace_bytes) ++pc;
+    } else {
+      while (pc > 1 && make_plan(d, MSA_OP_FORWARD, pc).bytes > workspace_bytes) --pc;
+    }
+    if (pc != p.pass_chunks) p = make_plan(d, MSA_OP_FORWARD, pc);
+  }
   if ((rc = check_ws(p, workspace, workspace_bytes))) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaGetLastError();
@@ -479,22 +509,34 @@ int msa_forward(const msa_shape_t* shape, const void* q, const void* k, const vo
     }
   }
   build_lists(d, p, block_idx, workspace, 1, st);
-  // partial log-sum-exps of slots no list entry reaches stay NaN (all-ones bytes)
-  cudaMemsetAsync(at<float>(workspace, p.lpart), 0xff, (size_t)d.B * d.S * d.Hq * d.top_k * sizeof(float), st);
-  bool fok = true;
-  timed("attn_fwd", st, [&] {
-    fok = launch_attn_fwd(d, q, k, v, at<int>(workspace, p.seg_offset),
-                          at<int>(workspace, p.entries), at<Item>(workspace, p.items0),
-                          at<int>(workspace, p.totals) + 1, p.max0, at<void>(workspace, p.opart),
-                          at<float>(workspace, p.lpart), at<unsigned>(workspace, p.status), st);
-  });
-  if (!fok) {
-    set_err("msa_forward: could not create TMA tensor maps (cuTensorMapEncodeTiled)");
-    return MSA_ERR_CUDA;
+  // passes over consecutive sequence chunks: the items of chunks [c0, c1) are the items
+  // [io0[c0 nseg], io0[c1 nseg]) of the chunk-major list, their partials indexed from c0 chunk
+  const int pc = p.pass_chunks, tp = pass_tokens(d, pc);
+  const int* io0 = at<int>(workspace, p.io0);
+  for (int c0 = 0; c0 < d.nchunk; c0 += pc) {
+    const int c1 = c0 + pc < d.nchunk ? c0 + pc : d.nchunk;
+    const int t0 = c0 * d.chunk, tn = pass_tokens(d, c1) - t0;
+    // partial log-sum-exps of slots no list entry reaches stay NaN (all-ones bytes)
+    cudaMemsetAsync(at<float>(workspace, p.lpart), 0xff, (size_t)d.B * tp * d.Hq * d.top_k * sizeof(float), st);
+    bool fok = true;
+    timed("attn_fwd", st, [&] {
+      fok = launch_attn_fwd(d, q, k, v, at<int>(workspace, p.seg_offset),
+                            at<int>(workspace, p.entries), at<Item>(workspace, p.items0),
+                            at<int>(workspace, p.totals) + 1, p.max0,
+                            c0 > 0 ? io0 + (long long)c0 * d.nseg() : nullptr,
+                            c1 < d.nchunk ? io0 + (long long)c1 * d.nseg() : nullptr, t0, tp,
+                            at<void>(workspace, p.opart), at<float>(workspace, p.lpart),
+                            at<unsigned>(workspace, p.status), st);
+    });
+    if (!fok) {
+      set_err("msa_forward: could not create TMA tensor maps (cuTensorMapEncodeTiled)");
+      return MSA_ERR_CUDA;
+    }
+    timed("fwd_combine", st, [&] {
+      launch_combine(d, at<void>(workspace, p.opart), at<float>(workspace, p.lpart), o, lse, t0,
+                     tn, tp, st);
+    });
   }
-  timed("fwd_combine", st, [&] {
-    launch_combine(d, at<void>(workspace, p.opart), at<float>(workspace, p.lpart), o, lse, st);
-  });
   return cuda_fail("msa_forward");
 }
 

@@ -56,6 +56,11 @@ struct FwdArgs {
   float* lpart;
   unsigned* status;
   int* sched;  // work-item counter (zero at launch): blocks take items in order as they get free
+  // this pass: the items [*item_lo, *item_hi) (NULL: 0, the list's total) of the tokens
+  // [pass_t0, pass_t0 + pass_tokens), whose partials are indexed from pass_t0
+  const int* item_lo;
+  const int* item_hi;
+  int pass_t0, pass_tokens;
 };
 
 struct FwdShared {
@@ -106,8 +111,9 @@ __global__ void __launch_bounds__(448, 1)
 
   const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
   const float sl2 = d.scale * kLog2e;
-  long long total = *A.n_items;
+  long long total = A.item_hi ? *A.item_hi : *A.n_items;  // items of this pass end here
   if (total > A.max_items) total = A.max_items;
+  const int item0 = A.item_lo ? *A.item_lo : 0;
 
   if (tid == 0) {
     for (int x = 0; x < kRing; ++x) {
@@ -175,7 +181,7 @@ __global__ void __launch_bounds__(448, 1)
         }
         int v = 0;
         if (lane == 0) {
-          v = atomicAdd(A.sched, 1);
+          v = item0 + atomicAdd(A.sched, 1);
           sh->it_ring[x] = v;
           mbar_arrive(&sh->it_full[x]);
         }
@@ -475,7 +481,8 @@ __global__ void __launch_bounds__(448, 1)
           l = lac.x + lac.y;
         }
         const bool valid = t >= 0;
-        const long long dst = valid ? (((long long)b * d.S + t) * d.Hq + a * G + r % G) * d.top_k + slot : -1;
+        const long long dst =
+            valid ? (((long long)b * A.pass_tokens + (t - A.pass_t0)) * d.Hq + a * G + r % G) * d.top_k + slot : -1;
         const float sc = valid ? __fdividef(1.f, l) : 0.f;
         const float lse = valid ? (m2 + __log2f(l)) * kLn2 : 0.f;
         tmem_wait_st();
@@ -557,7 +564,8 @@ int fwd_item_tiles() { return kFwdItemTiles; }
 
 bool launch_attn_fwd(const Dims& d, const void* q, const void* k, const void* v,
                      const int* seg_offset, const int* entries, const Item* items,
-                     const int* n_items, long long max_items, void* opart, float* lpart,
+                     const int* n_items, long long max_items, const int* item_lo,
+                     const int* item_hi, int pass_t0, int pass_tokens, void* opart, float* lpart,
                      unsigned* status, cudaStream_t st) {
   CUtensorMap mk, mv;
   const uint64_t kvd[3] = {128, (uint64_t)d.Hkv, (uint64_t)d.B * d.S};
@@ -577,6 +585,10 @@ bool launch_attn_fwd(const Dims& d, const void* q, const void* k, const void* v,
   a.lpart = lpart;
   a.status = status;
   a.sched = reinterpret_cast<int*>(status + kSchedAttnFwd);
+  a.item_lo = item_lo;
+  a.item_hi = item_hi;
+  a.pass_t0 = pass_t0;
+  a.pass_tokens = pass_tokens;
   cudaMemsetAsync(a.sched, 0, sizeof(int), st);
   switch (d.G) {
     case 1: attn_fwd_g<1, false>(mk, mv, a, st); break;
@@ -613,6 +625,10 @@ bool launch_proxy_lse_sparse(const Dims& d, const void* qp, const void* kp, cons
   a.lpart = lpx_part;
   a.status = status;
   a.sched = reinterpret_cast<int*>(status + kSchedProxyLse);
+  a.item_lo = nullptr;  // one pass over every item and token
+  a.item_hi = nullptr;
+  a.pass_t0 = 0;
+  a.pass_tokens = d.S;
   cudaMemsetAsync(a.sched, 0, sizeof(int), st);
   attn_fwd_g<1, true>(mk, mk, a, st);
   return true;

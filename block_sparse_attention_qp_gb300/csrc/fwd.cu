@@ -17,15 +17,22 @@ namespace msa {
 // its valid slots,  O = sum_s w_s O_s / sum_s w_s,  w_s = exp(lse_s - max),  LSE = max + log sum.
 // A slot is valid iff its partial log-sum-exp was written: the workspace holds NaN (all-ones
 // bytes) elsewhere.  Half-warps take alternate slots with 16-byte loads (8 columns per lane).
+// One pass covers the tokens [t0, t0 + tn) of every sequence, its partials indexed
+// ((b tp + t - t0) Hq + h) top_k + slot.
 __global__ void __launch_bounds__(256, 3) combine_kernel(Dims d, const bf16* __restrict__ opart,
                                                       const float* __restrict__ lpart,
-                                                      bf16* __restrict__ o, float* __restrict__ lse) {
-  const long long rows = (long long)d.B * d.S * d.Hq;
+                                                      bf16* __restrict__ o, float* __restrict__ lse,
+                                                      int t0, int tn, int tp) {
+  const long long rows = (long long)d.B * tn * d.Hq;
   const int lane = threadIdx.x % 32, half = lane >> 4, l16 = lane & 15;
   const uint64_t pol = l2_policy_evict_first();  // each partial is read exactly once
   for (long long r = (blockIdx.x * (long long)blockDim.x + threadIdx.x) / 32; r < rows;
        r += (long long)gridDim.x * blockDim.x / 32) {
-    const size_t base = (size_t)r * d.top_k;
+    const int h = (int)(r % d.Hq);
+    const long long bt = r / d.Hq;
+    const int tr = (int)(bt % tn), b = (int)(bt / tn);  // token t0 + tr of sequence b
+    const size_t base = (((size_t)b * tp + tr) * d.Hq + h) * d.top_k;
+    const size_t orow = ((size_t)b * d.S + t0 + tr) * d.Hq + h;
     float l0 = lane < d.top_k ? lpart[base + lane] : NAN;
     float l1 = lane + 32 < d.top_k ? lpart[base + lane + 32] : NAN;
     // the first 16 slots' partials are requested together with the log-sum-exps, before the
@@ -83,15 +90,10 @@ __global__ void __launch_bounds__(256, 3) combine_kernel(Dims d, const bf16* __r
     for (int e = 0; e < 8; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], 16);
     const float inv = sum > 0.f ? 1.f / sum : 0.f;
     if (half == 0)
-      *reinterpret_cast<uint4*>(o + (size_t)r * kD + l16 * 8) =
+      *reinterpret_cast<uint4*>(o + orow * kD + l16 * 8) =
           make_uint4(pack_bf16(acc[0] * inv, acc[1] * inv), pack_bf16(acc[2] * inv, acc[3] * inv),
                      pack_bf16(acc[4] * inv, acc[5] * inv), pack_bf16(acc[6] * inv, acc[7] * inv));
-    if (lane == 0) {
-      const int h = (int)(r % d.Hq);
-      const long long bt = r / d.Hq;
-      const int t = (int)(bt % d.S), b = (int)(bt / d.S);
-      lse[((size_t)b * d.Hq + h) * d.S + t] = sum > 0.f ? mx + logf(sum) : -INFINITY;
-    }
+    if (lane == 0) lse[((size_t)b * d.Hq + h) * d.S + t0 + tr] = sum > 0.f ? mx + logf(sum) : -INFINITY;
   }
 }
 
@@ -125,11 +127,11 @@ __global__ void proxy_lse_combine_kernel(Dims d, const float* __restrict__ lpx_p
 // ------------------------------------------------------------------------------------------
 
 void launch_combine(const Dims& d, const void* opart, const float* lpart, void* o, float* lse,
-                    cudaStream_t st) {
-  const long long rows = (long long)d.B * d.S * d.Hq;
+                    int t0, int tn, int tp, cudaStream_t st) {
+  const long long rows = (long long)d.B * tn * d.Hq;
   long long grid = (rows * 32 + 255) / 256;
   if (grid > (long long)num_sms() * 8) grid = (long long)num_sms() * 8;
-  combine_kernel<<<(int)grid, 256, 0, st>>>(d, (const bf16*)opart, lpart, (bf16*)o, lse);
+  combine_kernel<<<(int)grid, 256, 0, st>>>(d, (const bf16*)opart, lpart, (bf16*)o, lse, t0, tn, tp);
 }
 
 

@@ -74,15 +74,20 @@ bool launch_proxy_lse_dense(const Dims& d, const void* qp, const void* kp, float
 // of the group, the block's normalised output (bf16, opart[(t, h, slot)][128]) and its natural
 // log-sum-exp (lpart).  Returns false for an unsupported group size or if the TMA tensor maps
 // cannot be created.
+// One pass takes the items [*item_lo, *item_hi) (NULL: 0 / all) -- the lists of a range of
+// sequence chunks -- and indexes its partials from token pass_t0 ((b pass_tokens + t - pass_t0)
+// Hq + h) top_k + slot.
 bool launch_attn_fwd(const Dims& d, const void* q, const void* k, const void* v,
                      const int* seg_offset, const int* entries, const Item* items,
-                     const int* n_items, long long max_items, void* opart, float* lpart,
+                     const int* n_items, long long max_items, const int* item_lo,
+                     const int* item_hi, int pass_t0, int pass_tokens, void* opart, float* lpart,
                      unsigned* status, cudaStream_t st);
 int fwd_item_tiles();  // 128-row tiles per sparse-forward work item
-// Merges the partials of every (b, t, h); a partial is valid iff its log-sum-exp is not NaN
-// (the caller fills lpart with NaN bytes before the partial pass).
+// Merges the partials of every (b, t, h) with t in [t0, t0 + tn) (partials indexed as the pass
+// with pass_tokens = tp wrote them); a partial is valid iff its log-sum-exp is not NaN (the
+// caller fills lpart with NaN bytes before the partial pass).
 void launch_combine(const Dims& d, const void* opart, const float* lpart, void* o, float* lse,
-                    cudaStream_t st);
+                    int t0, int tn, int tp, cudaStream_t st);
 // Dense causal forward of the warmup mode (dense_fwd.cu).  Returns false for an unsupported group
 // size or if the TMA tensor maps cannot be created.
 bool launch_dense_fwd(const Dims& d, const void* q, const void* k, const void* v, void* o,

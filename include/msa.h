@@ -108,6 +108,10 @@ MSA_API size_t msa_workspace_size(const msa_shape_t* shape, int op);
  *      block_idx (blog "Main attention"; forum summary "Architecture") -> o, lse.
  * indices_given != 0: block_idx is an input (for instance the cached indices of an earlier
  * call); invalid entries are skipped and flagged with MSA_DEVICE_BAD_INDEX.
+ * Workspace: the per-(token, head, slot) partial outputs of step 2 are produced and merged in
+ * passes over consecutive sequence chunks.  msa_workspace_size sizes them for passes of at most
+ * 8 GiB of partials; a larger workspace_bytes gives fewer passes, a smaller one more (down to one
+ * chunk per pass; below that MSA_ERR_WORKSPACE).  The results do not depend on the passes.
  */
 MSA_API int msa_forward(const msa_shape_t* shape, const void* q, const void* k, const void* v,
                 const void* qp, const void* kp, int32_t* block_idx, int indices_given, void* o,

@@ -375,3 +375,25 @@ def test_training_step_replays_from_a_cuda_graph():
     assert torch.equal(captured[0], eager[0]) and torch.equal(captured[1], eager[1])  # O, LSE
     for name, a, b in zip(("dq", "dk", "dv", "dqp", "dkp"), captured[3:], eager[3:]):
         close(name, a, b.float(), rel=1e-3, atol=1e-4, ulps=1.0)  # fp32 reduction order only
+
+
+def test_forward_in_passes_equals_one_pass():
+    """A workspace smaller than msa_workspace_size makes the forward produce and merge its partial
+    outputs in passes over the sequence chunks (here four chunks of 8192 tokens: passes of 3 + 1
+    and 1 + 1 + 1 + 1 chunks); every result equals the one-pass result bit for bit."""
+    w = Workload("passes", B=2, S=32768, Hq=16, Hkv=2, Hp=2, top_k=8)  # chunks of 8192 tokens
+    g = to_dev(make_inputs(w, 41))
+    shape = msa.make_shape(g["q"], g["k"], g["qp"], w.top_k, w.scale)
+    full = msa.msa_workspace_size(shape, msa.OP_FORWARD)
+    chunk_bytes = w.B * 8192 * w.Hq * w.top_k * (128 * 2 + 4)  # partials of one chunk
+    ref = msa.msa_forward(g["q"], g["k"], g["v"], g["qp"], g["kp"], w.top_k, w.scale,
+                          ws=torch.empty(full, dtype=torch.uint8, device=DEV))
+    for fewer in (1, 3):
+        ws = torch.empty(full - fewer * chunk_bytes, dtype=torch.uint8, device=DEV)
+        got = msa.msa_forward(g["q"], g["k"], g["v"], g["qp"], g["kp"], w.top_k, w.scale, ws=ws)
+        assert msa.msa_device_status(ws) == 0
+        for name, a, b in zip(("O", "LSE", "block_idx"), got, ref):
+            assert torch.equal(a, b), (fewer, name)
+    with pytest.raises(msa.MSAError, match="workspace"):
+        msa.msa_forward(g["q"], g["k"], g["v"], g["qp"], g["kp"], w.top_k, w.scale,
+                        ws=torch.empty(full - 4 * chunk_bytes, dtype=torch.uint8, device=DEV))
