@@ -7,6 +7,7 @@
 
 #include <atomic>
 #include <map>
+#include <memory>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -145,7 +146,8 @@ struct Plan {
   size_t bytes = 0;
   long long max0 = 0, max1 = 0;
   ItemSpec spec0{1, 1}, spec1{1, 1};
-  int pass_chunks = 1;  // forward: sequence chunks per pass of the partial outputs
+  int pass_chunks = 1;  // forward: sequence chunks per pass of the partial outputs; backward:
+                        // per pass of the teacher rows
 };
 
 struct Carver {
@@ -215,6 +217,42 @@ int default_pass_chunks(const Dims& d) {
   return (int)(fit < 1 ? 1 : fit > d.nchunk ? d.nchunk : fit);
 }
 
+// The backward's teacher rows (fp16, one per list entry) likewise live for one pass of
+// consecutive sequence chunks: attn_bwd writes them and proxy_bwd reads them, pass by pass.  A
+// pass holds at most kBwdTeacherBudget bytes of them (one chunk at least).
+constexpr size_t kBwdTeacherBudget = 8ull << 30;
+
+// List entries of the chunks [c0, c1): exact for dense lists (every token t >= 128 n of the chunk
+// in the list of block n), the most there can be for sparse ones (top_k per token and proxy head).
+long long pass_entries(const Dims& d, bool dense, int c0, int c1) {
+  const long long lo = (long long)c0 * d.chunk;
+  const long long hi = (long long)c1 * d.chunk < d.S ? (long long)c1 * d.chunk : d.S;
+  if (!dense) return (long long)d.B * d.Hp * (hi - lo) * d.top_k;
+  long long e = 0;
+  for (int c = c0; c < c1; ++c) {
+    const long long a = (long long)c * d.chunk;
+    const long long z = a + d.chunk < d.S ? a + d.chunk : d.S;
+    for (long long n = 0; n < d.nblk && n * kBlock < z; ++n) e += z - (n * kBlock > a ? n * kBlock : a);
+  }
+  return e * d.B * d.Hp;
+}
+
+// The largest entry count of any pass of `pc` chunks.
+long long max_pass_entries(const Dims& d, bool dense, int pc) {
+  long long m = 0;
+  for (int c0 = 0; c0 < d.nchunk; c0 += pc) {
+    const long long e = pass_entries(d, dense, c0, c0 + pc < d.nchunk ? c0 + pc : d.nchunk);
+    if (e > m) m = e;
+  }
+  return m;
+}
+
+int bwd_pass_chunks(const Dims& d, bool dense) {
+  int pc = d.nchunk;
+  while (pc > 1 && (size_t)max_pass_entries(d, dense, pc) * kBlock * 2 > kBwdTeacherBudget) --pc;
+  return pc;
+}
+
 Plan make_plan(const Dims& d, int op, int pass_chunks = 0) {
   Plan p;
   Carver c;
@@ -269,7 +307,9 @@ Plan make_plan(const Dims& d, int op, int pass_chunks = 0) {
     }
     p.lse_px = c.take((size_t)rows_p * sizeof(float));
     p.rowm = c.take((size_t)rows_q * sizeof(float2));  // {LSE log2 e, D} per query row
-    p.pbar = c.take((size_t)ent * kBlock * sizeof(uint16_t));  // teacher rows (fp16), one per entry
+    p.pass_chunks = pass_chunks > 0 ? pass_chunks : bwd_pass_chunks(d, dense);
+    const long long ent_pass = max_pass_entries(d, dense, p.pass_chunks);
+    p.pbar = c.take((size_t)ent_pass * kBlock * sizeof(uint16_t));  // teacher rows (fp16) of a pass
     p.lpxe = c.take((size_t)ent * sizeof(float));            // proxy log-normaliser per entry
     p.emeta = c.take((size_t)ent * d.Gp() * sizeof(float2));  // rowm per entry and query head
     p.dq = c.take((size_t)rows_q * kD * sizeof(float));
@@ -281,6 +321,19 @@ Plan make_plan(const Dims& d, int op, int pass_chunks = 0) {
   if (op == MSA_OP_DECODE) p.scores = c.take((size_t)d.B * d.Hp * d.nblk * sizeof(float));
   p.bytes = c.off;
   return p;
+}
+
+// The plan for a call with `bytes` of workspace: passes of the default size, or of as many
+// sequence chunks as the workspace holds (more or fewer).  The caller checks that it fits.
+Plan plan_for(const Dims& d, int op, size_t bytes) {
+  Plan p = make_plan(d, op);
+  int pc = p.pass_chunks;
+  if (bytes >= p.bytes) {
+    while (pc < d.nchunk && make_plan(d, op, pc + 1).bytes <= bytes) ++pc;
+  } else {
+    while (pc > 1 && make_plan(d, op, pc).bytes > bytes) --pc;
+  }
+  return pc != p.pass_chunks ? make_plan(d, op, pc) : p;
 }
 
 // Shape checks shared by every op.  Returns MSA_OK or an error code (message set).
@@ -483,17 +536,7 @@ int msa_forward(const msa_shape_t* shape, const void* q, const void* k, const vo
   if (rc) return rc;
   if ((rc = check_ptrs({q, k, v, block_idx, o, lse}))) return rc;
   if (!indices_given && (rc = check_ptrs({qp, kp}))) return rc;
-  // chunks per pass: the default, or as many as the given workspace holds (more or fewer)
-  Plan p = make_plan(d, MSA_OP_FORWARD);
-  {
-    int pc = p.pass_chunks;
-    if (workspace_bytes >= p.bytes) {
-      while (pc < d.nchunk && make_plan(d, MSA_OP_FORWARD, pc + 1).bytes <= workspace_bytes) ++pc;
-    } else {
-      while (pc > 1 && make_plan(d, MSA_OP_FORWARD, pc).bytes > workspace_bytes) --pc;
-    }
-    if (pc != p.pass_chunks) p = make_plan(d, MSA_OP_FORWARD, pc);
-  }
+  const Plan p = plan_for(d, MSA_OP_FORWARD, workspace_bytes);  // chunks per pass
   if ((rc = check_ws(p, workspace, workspace_bytes))) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaGetLastError();
@@ -551,7 +594,7 @@ int msa_backward(const msa_shape_t* shape, const void* q, const void* k, const v
   if ((rc = check_ptrs({q, k, v, qp, kp, o, lse, dout, block_idx, dq, dk, dv, dqp, dkp}))) return rc;
   if (kl_out && (rc = check_kl(kl_out, "kl_out must be 4-byte aligned"))) return rc;
   if (kl_grad_dev && (rc = check_kl(kl_grad_dev, "kl_grad_dev must be 4-byte aligned"))) return rc;
-  const Plan p = make_plan(d, MSA_OP_BACKWARD);
+  const Plan p = plan_for(d, MSA_OP_BACKWARD, workspace_bytes);  // chunks per teacher pass
   if ((rc = check_ws(p, workspace, workspace_bytes))) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaGetLastError();
@@ -589,38 +632,52 @@ int msa_backward(const msa_shape_t* shape, const void* q, const void* k, const v
                       at<float2>(workspace, p.rowm), at<float>(workspace, p.lpxe),
                       at<float2>(workspace, p.emeta), st);
   });
-  if (d.R > 1)  // teacher rows accumulated over the proxy head's attention groups
-    cudaMemsetAsync(at<char>(workspace, p.pbar), 0, (size_t)d.B * d.S * d.Hp * d.top_k * kBlock * 2, st);
+  // passes over consecutive sequence chunks: attn_bwd writes the teacher rows of a pass and
+  // proxy_bwd reads them (the items of chunks [c0, c1) are a contiguous slice of the list)
   bool ok = true;
-  timed("attn_bwd", st, [&] {
-    ok = launch_attn_bwd(d, false, q, k, v, dout, at<float2>(workspace, p.emeta),
-                         at<int>(workspace, p.seg_offset), at<int>(workspace, p.entries),
-                         at<Item>(workspace, p.items1), at<int>(workspace, p.totals) + 2, p.max1,
-                         at<float>(workspace, p.dq), at<float>(workspace, p.dk),
-                         at<float>(workspace, p.dv), at<void>(workspace, p.pbar),
-                         at<unsigned>(workspace, p.status), st);
-  });
-  // dQ, dK, dV are final: their conversion runs beside the proxy backward
-  Branch post(st);
-  if (ok) emit_main_grads(d, p, workspace, dq, dk, dv, post.aux());
   double* kl_acc = kl_out ? kl_accumulator(workspace, p, st) : nullptr;
-  if (ok)
-    timed("proxy_bwd", st, [&] {
-      ok = launch_proxy_bwd(d, false, qp, kp, at<float>(workspace, p.lpxe),
-                            at<void>(workspace, p.pbar), kl_grad, kl_grad_dev,
-                            at<int>(workspace, p.seg_offset),
-                            at<int>(workspace, p.entries), at<Item>(workspace, p.items1),
-                            at<int>(workspace, p.totals) + 2, p.max1, at<float>(workspace, p.dqp),
-                            at<float>(workspace, p.dkp), kl_acc, at<unsigned>(workspace, p.status),
-                            st);
+  std::unique_ptr<Branch> post;
+  const int* io1 = at<int>(workspace, p.io1);
+  const int* so = at<int>(workspace, p.seg_offset);
+  for (int c0 = 0; c0 < d.nchunk && ok; c0 += p.pass_chunks) {
+    const int c1 = c0 + p.pass_chunks < d.nchunk ? c0 + p.pass_chunks : d.nchunk;
+    const int* lo = c0 > 0 ? io1 + (long long)c0 * d.nseg() : nullptr;
+    const int* hi = c1 < d.nchunk ? io1 + (long long)c1 * d.nseg() : nullptr;
+    const int* elo = c0 > 0 ? so + (long long)c0 * d.nseg() : nullptr;
+    if (d.R > 1)  // teacher rows accumulated over the proxy head's attention groups
+      cudaMemsetAsync(at<char>(workspace, p.pbar), 0,
+                      (size_t)max_pass_entries(d, false, p.pass_chunks) * kBlock * 2, st);
+    timed("attn_bwd", st, [&] {
+      ok = launch_attn_bwd(d, false, q, k, v, dout, at<float2>(workspace, p.emeta),
+                           at<int>(workspace, p.seg_offset), at<int>(workspace, p.entries),
+                           at<Item>(workspace, p.items1), at<int>(workspace, p.totals) + 2, p.max1,
+                           lo, hi, elo, at<float>(workspace, p.dq), at<float>(workspace, p.dk),
+                           at<float>(workspace, p.dv), at<void>(workspace, p.pbar),
+                           at<unsigned>(workspace, p.status), st);
     });
+    if (ok && c1 == d.nchunk) {
+      // dQ, dK, dV are final: their conversion runs beside the last proxy backward
+      post.reset(new Branch(st));
+      emit_main_grads(d, p, workspace, dq, dk, dv, post->aux());
+    }
+    if (ok)
+      timed("proxy_bwd", st, [&] {
+        ok = launch_proxy_bwd(d, false, qp, kp, at<float>(workspace, p.lpxe),
+                              at<void>(workspace, p.pbar), kl_grad, kl_grad_dev,
+                              at<int>(workspace, p.seg_offset),
+                              at<int>(workspace, p.entries), at<Item>(workspace, p.items1),
+                              at<int>(workspace, p.totals) + 2, p.max1, lo, hi, elo,
+                              at<float>(workspace, p.dqp), at<float>(workspace, p.dkp), kl_acc,
+                              at<unsigned>(workspace, p.status), st);
+      });
+  }
   if (!ok) {
     set_err("msa_backward: could not create TMA tensor maps (cuTensorMapEncodeTiled)");
     return MSA_ERR_CUDA;
   }
   if (kl_out) timed("kl_finalize", st, [&] { launch_kl_finalize(d, kl_acc, kl_out, st); });
   emit_proxy_grads(d, p, workspace, dqp, dkp, st);
-  post.join();
+  if (post) post->join();
   return cuda_fail("msa_backward");
 }
 
@@ -658,7 +715,7 @@ int msa_warmup_backward(const msa_shape_t* shape, const void* q, const void* k, 
   if ((rc = check_ptrs({q, k, v, qp, kp, o, lse, dout, dq, dk, dv, dqp, dkp}))) return rc;
   if (kl_out && (rc = check_kl(kl_out, "kl_out must be 4-byte aligned"))) return rc;
   if (kl_grad_dev && (rc = check_kl(kl_grad_dev, "kl_grad_dev must be 4-byte aligned"))) return rc;
-  const Plan p = make_plan(d, MSA_OP_WARMUP_BACKWARD);
+  const Plan p = plan_for(d, MSA_OP_WARMUP_BACKWARD, workspace_bytes);  // chunks per teacher pass
   if ((rc = check_ws(p, workspace, workspace_bytes))) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaGetLastError();
@@ -693,35 +750,47 @@ int msa_warmup_backward(const msa_shape_t* shape, const void* q, const void* k, 
                       at<float>(workspace, p.lse_px), at<float2>(workspace, p.rowm),
                       at<float>(workspace, p.lpxe), at<float2>(workspace, p.emeta), st);
   });
-  if (d.R > 1)  // teacher rows accumulated over the proxy head's attention groups
-    cudaMemsetAsync(at<char>(workspace, p.pbar), 0, (size_t)dense_entries(d) * kBlock * 2, st);
-  bool ok = true;
-  timed("attn_bwd_dense", st, [&] {
-    ok = launch_attn_bwd(d, true, q, k, v, dout, at<float2>(workspace, p.emeta),
-                         at<int>(workspace, p.seg_offset), nullptr, at<Item>(workspace, p.items0),
-                         at<int>(workspace, p.totals) + 1, p.max0, at<float>(workspace, p.dq),
-                         at<float>(workspace, p.dk), at<float>(workspace, p.dv),
-                         at<void>(workspace, p.pbar), status, st);
-  });
-  Branch post(st);
-  if (ok) emit_main_grads(d, p, workspace, dq, dk, dv, post.aux());
+  bool ok = true;  // passes as in msa_backward
   double* kl_acc = kl_out ? kl_accumulator(workspace, p, st) : nullptr;
-  if (ok)
-    timed("proxy_bwd_dense", st, [&] {
-      ok = launch_proxy_bwd(d, true, qp, kp, at<float>(workspace, p.lpxe),
-                            at<void>(workspace, p.pbar), kl_grad, kl_grad_dev,
-                            at<int>(workspace, p.seg_offset),
-                            nullptr, at<Item>(workspace, p.items0), at<int>(workspace, p.totals) + 1,
-                            p.max0, at<float>(workspace, p.dqp), at<float>(workspace, p.dkp),
-                            kl_acc, status, st);
+  std::unique_ptr<Branch> post;
+  const int* io0 = at<int>(workspace, p.io0);
+  const int* so = at<int>(workspace, p.seg_offset);
+  for (int c0 = 0; c0 < d.nchunk && ok; c0 += p.pass_chunks) {
+    const int c1 = c0 + p.pass_chunks < d.nchunk ? c0 + p.pass_chunks : d.nchunk;
+    const int* lo = c0 > 0 ? io0 + (long long)c0 * d.nseg() : nullptr;
+    const int* hi = c1 < d.nchunk ? io0 + (long long)c1 * d.nseg() : nullptr;
+    const int* elo = c0 > 0 ? so + (long long)c0 * d.nseg() : nullptr;
+    if (d.R > 1)  // teacher rows accumulated over the proxy head's attention groups
+      cudaMemsetAsync(at<char>(workspace, p.pbar), 0,
+                      (size_t)max_pass_entries(d, true, p.pass_chunks) * kBlock * 2, st);
+    timed("attn_bwd_dense", st, [&] {
+      ok = launch_attn_bwd(d, true, q, k, v, dout, at<float2>(workspace, p.emeta),
+                           at<int>(workspace, p.seg_offset), nullptr, at<Item>(workspace, p.items0),
+                           at<int>(workspace, p.totals) + 1, p.max0, lo, hi, elo,
+                           at<float>(workspace, p.dq), at<float>(workspace, p.dk),
+                           at<float>(workspace, p.dv), at<void>(workspace, p.pbar), status, st);
     });
+    if (ok && c1 == d.nchunk) {
+      post.reset(new Branch(st));
+      emit_main_grads(d, p, workspace, dq, dk, dv, post->aux());
+    }
+    if (ok)
+      timed("proxy_bwd_dense", st, [&] {
+        ok = launch_proxy_bwd(d, true, qp, kp, at<float>(workspace, p.lpxe),
+                              at<void>(workspace, p.pbar), kl_grad, kl_grad_dev,
+                              at<int>(workspace, p.seg_offset),
+                              nullptr, at<Item>(workspace, p.items0), at<int>(workspace, p.totals) + 1,
+                              p.max0, lo, hi, elo, at<float>(workspace, p.dqp),
+                              at<float>(workspace, p.dkp), kl_acc, status, st);
+      });
+  }
   if (!ok) {
     set_err("msa_warmup_backward: could not create TMA tensor maps (cuTensorMapEncodeTiled)");
     return MSA_ERR_CUDA;
   }
   if (kl_out) timed("kl_finalize", st, [&] { launch_kl_finalize(d, kl_acc, kl_out, st); });
   emit_proxy_grads(d, p, workspace, dqp, dkp, st);
-  post.join();
+  if (post) post->join();
   return cuda_fail("msa_warmup_backward");
 }
 

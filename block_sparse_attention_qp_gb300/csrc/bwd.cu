@@ -109,9 +109,12 @@ struct MainArgs {
   const int* n_items;
   long long max_items;
   float *dq, *dk, *dv;
-  __half* pbar;  // teacher rows [list entry][128 keys]: probabilities in [0, 1], fp16
+  __half* pbar;  // teacher rows [list entry - pass base][128 keys]: probabilities in [0, 1], fp16
   unsigned* status;
   int* sched;  // work-item counter (zero at launch): blocks take items in order as they get free
+  // this pass: the items [*item_lo, *item_hi) (NULL: 0, the list's total); its teacher rows are
+  // indexed from list entry *entry_lo (NULL: 0)
+  const int *item_lo, *item_hi, *entry_lo;
 };
 
 struct MainShared {
@@ -140,6 +143,7 @@ struct ProxyArgs {
   double* kl_acc;  // kKL: sum of pbar (ln pbar - ln p_student) over the visited pairs
   unsigned* status;
   int* sched;  // work-item counter (zero at launch)
+  const int *item_lo, *item_hi, *entry_lo;  // this pass, as in MainArgs
 };
 
 constexpr int kQPB = 3;  // proxy query row buffers
@@ -244,8 +248,10 @@ __global__ void __launch_bounds__(352, 1)
 
   const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
   const float sl2 = d.scale * kLog2e;
-  long long total = *A.n_items;
+  long long total = A.item_hi ? *A.item_hi : *A.n_items;  // items of this pass end here
   if (total > A.max_items) total = A.max_items;
+  const int item0 = A.item_lo ? *A.item_lo : 0;
+  const long long ent0 = A.entry_lo ? *A.entry_lo : 0;  // list entry of teacher row 0
 
   if (tid == 0) {
     mbar_init(&sh->kv_full, 1);
@@ -310,7 +316,7 @@ __global__ void __launch_bounds__(352, 1)
         while (!last && pub < ni + 2) {
           const int x = (int)(pub % kIR);
           if (pub >= kIR && !mbar_wait(&sh->it_empty[x], par(pub / kIR - 1), A.status)) break;
-          const int v = atomicAdd(A.sched, 1);
+          const int v = item0 + atomicAdd(A.sched, 1);
           sh->it_ring[x] = v;
           mbar_arrive(&sh->it_full[x]);
           last = v >= total;
@@ -656,12 +662,12 @@ __global__ void __launch_bounds__(352, 1)
 #pragma unroll
           for (int x = 0; x < TT; ++x)
             if (tv[x] >= 0)
-              st_global_h_hint(A.pbar + (size_t)(eb + tl * TT + x) * kBlock + kr, pb[x] * (1.f / G), stream);
+              st_global_h_hint(A.pbar + (size_t)(eb - ent0 + tl * TT + x) * kBlock + kr, pb[x] * (1.f / G), stream);
         } else {
 #pragma unroll
           for (int x = 0; x < TT; ++x)
             if (tv[x] >= 0)
-              red_add_h(A.pbar + (size_t)(eb + tl * TT + x) * kBlock + kr, pb[x] * (1.f / (G * d.R)));
+              red_add_h(A.pbar + (size_t)(eb - ent0 + tl * TT + x) * kBlock + kr, pb[x] * (1.f / (G * d.R)));
         }
         // ---- epilogue of the previous tile
         if (tl > 0 && !epilogue(i - 1)) { ok = false; break; }
@@ -755,8 +761,10 @@ __global__ void __launch_bounds__(kWideThreads, 1)
   WideShared* sh = reinterpret_cast<WideShared*>(sdS + kSTW);
   const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aSl = smem_u32(sSl), adS = smem_u32(sdS);
   const float sl2 = d.scale * kLog2e;
-  long long total = *A.n_items;
+  long long total = A.item_hi ? *A.item_hi : *A.n_items;  // items of this pass end here
   if (total > A.max_items) total = A.max_items;
+  const int item0 = A.item_lo ? *A.item_lo : 0;
+  const long long ent0 = A.entry_lo ? *A.entry_lo : 0;  // list entry of teacher row 0
 
   if (tid == 0) {
     mbar_init(&sh->kv_full, 1);
@@ -827,7 +835,7 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         while (!last && pub < ni + 2) {  // item numbers up to two items ahead of the loads
           const int x = (int)(pub % kIR);
           if (pub >= kIR && !wait1(3, &sh->it_empty[x], par(pub / kIR - 1))) break;
-          const int v = atomicAdd(A.sched, 1);
+          const int v = item0 + atomicAdd(A.sched, 1);
           sh->it_ring[x] = v;
           mbar_arrive(&sh->it_full[x]);
           last = v >= total;
@@ -1105,13 +1113,13 @@ __global__ void __launch_bounds__(kWideThreads, 1)
 #pragma unroll
             for (int w = 0; w < WT; ++w)
               if (sh->tok[sl][c * WT + w] >= 0)
-                st_global_h_hint(A.pbar + (size_t)(eb + tl * TT + c * WT + w) * kBlock + kr,
+                st_global_h_hint(A.pbar + (size_t)(eb - ent0 + tl * TT + c * WT + w) * kBlock + kr,
                                  pc[w] * (1.f / G), stream);
           } else {
 #pragma unroll
             for (int w = 0; w < WT; ++w)
               if (sh->tok[sl][c * WT + w] >= 0)
-                red_add_h(A.pbar + (size_t)(eb + tl * TT + c * WT + w) * kBlock + kr,
+                red_add_h(A.pbar + (size_t)(eb - ent0 + tl * TT + c * WT + w) * kBlock + kr,
                           pc[w] * (1.f / (G * d.R)));
           }
         }
@@ -1205,8 +1213,10 @@ __global__ void __launch_bounds__(384, 1)
   const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
   const float sl2 = d.scale * kLog2e;
   const float cz = A.czp ? A.cz * __ldg(A.czp) : A.cz;
-  long long total = *A.n_items;
+  long long total = A.item_hi ? *A.item_hi : *A.n_items;  // items of this pass end here
   if (total > A.max_items) total = A.max_items;
+  const int item0 = A.item_lo ? *A.item_lo : 0;
+  const long long ent0 = A.entry_lo ? *A.entry_lo : 0;  // list entry of teacher row 0
   if (tid == 0) {
     mbar_init(&sh->kp_full, 1);
     mbar_init(&sh->kp_empty, 1);
@@ -1272,8 +1282,8 @@ __global__ void __launch_bounds__(384, 1)
           if (pub >= kIR && !mbar_wait(&sh->it_empty[x], par(pub / kIR - 1), A.status)) break;
           // the work items repeat each run of tokens for the proxy head's R attention groups;
           // the proxy gradients need each run once
-          int v = atomicAdd(A.sched, 1);
-          while (v < total && A.items[v].sub != 0) v = atomicAdd(A.sched, 1);
+          int v = item0 + atomicAdd(A.sched, 1);
+          while (v < total && A.items[v].sub != 0) v = item0 + atomicAdd(A.sched, 1);
           sh->it_ring[x] = v;
           mbar_arrive(&sh->it_full[x]);
           last = v >= total;
@@ -1392,7 +1402,7 @@ __global__ void __launch_bounds__(384, 1)
         if (w == 0 && lane == 0) {  // gcount entries x 128 keys, one bulk copy
           const uint32_t bytes = (uint32_t)gcount * kBlock * 2;
           mbar_expect_tx(&sh->pb_full[pb], bytes);  // also this lane's arrival
-          bulk_load(sPb + pb * kPG * kBlock, A.pbar + (size_t)(cur.base + gi * kPG) * kBlock, bytes,
+          bulk_load(sPb + pb * kPG * kBlock, A.pbar + (size_t)(cur.base - ent0 + gi * kPG) * kBlock, bytes,
                     &sh->pb_full[pb]);
         } else {
           mbar_arrive(&sh->pb_full[pb]);  // publishes tok / lpx2
@@ -1675,6 +1685,7 @@ void launch_bwd_rowdot(const Dims& d, const void* o, const void* dout, const flo
 bool launch_attn_bwd(const Dims& d, bool dense, const void* q, const void* k, const void* v,
                      const void* dout, const float2* emeta, const int* seg_offset,
                      const int* entries, const Item* items, const int* n_items, long long max_items,
+                     const int* item_lo, const int* item_hi, const int* entry_lo,
                      float* dq_acc, float* dk_acc, float* dv_acc, void* pbar, unsigned* status,
                      cudaStream_t st) {
   CUtensorMap mk, mv;
@@ -1699,6 +1710,9 @@ bool launch_attn_bwd(const Dims& d, bool dense, const void* q, const void* k, co
   a.pbar = static_cast<__half*>(pbar);
   a.status = status;
   a.sched = reinterpret_cast<int*>(status + kSchedAttnBwd);
+  a.item_lo = item_lo;
+  a.item_hi = item_hi;
+  a.entry_lo = entry_lo;
   cudaMemsetAsync(a.sched, 0, sizeof(int), st);
   // 128-row tiles for 4 and 8 heads per group; 16 heads keep 64-row tiles (there P and dS go to
   // the products as a bf16 value plus its bf16 residual, which needs the spare tensor memory).
@@ -1724,7 +1738,8 @@ bool launch_proxy_bwd(const Dims& d, bool dense, const void* qp, const void* kp,
                       const float* lpxe, const void* pbar, float kl_grad,
                       const float* kl_grad_dev, const int* seg_offset,
                       const int* entries, const Item* items, const int* n_items,
-                      long long max_items, float* dqp_acc, float* dkp_acc, double* kl_acc,
+                      long long max_items, const int* item_lo, const int* item_hi,
+                      const int* entry_lo, float* dqp_acc, float* dkp_acc, double* kl_acc,
                       unsigned* status, cudaStream_t st) {
   CUtensorMap mkp;
   const uint64_t kpd[2] = {128, (uint64_t)d.B * d.S};
@@ -1760,6 +1775,9 @@ bool launch_proxy_bwd(const Dims& d, bool dense, const void* qp, const void* kp,
   a.kl_acc = kl_acc;
   a.status = status;
   a.sched = reinterpret_cast<int*>(status + kSchedProxyBwd);
+  a.item_lo = item_lo;
+  a.item_hi = item_hi;
+  a.entry_lo = entry_lo;
   cudaMemsetAsync(a.sched, 0, sizeof(int), st);
   if (dense)
     kl_acc ? proxy_bwd_g<true, true>(mkp, mqp, mdqp, a, st) : proxy_bwd_g<true, false>(mkp, mqp, mdqp, a, st);

@@ -108,11 +108,13 @@ bool launch_proxy_lse_sparse(const Dims& d, const void* qp, const void* kp, cons
 void launch_proxy_lse_combine(const Dims& d, const float* lpx_part, float* lse_px, cudaStream_t st);
 
 // Main-attention backward (dQ, dK, dV into fp32 accumulators) and the teacher pbar
-// ([list entry][128 keys] fp16).  Returns false for an unsupported group size or if the TMA
-// tensor maps cannot be created.
+// ([list entry - *entry_lo][128 keys] fp16) of one pass: the items [*item_lo, *item_hi) (NULL:
+// 0 / all; entry_lo NULL: 0).  Returns false for an unsupported group size or if the TMA tensor
+// maps cannot be created.
 bool launch_attn_bwd(const Dims& d, bool dense, const void* q, const void* k, const void* v,
                      const void* dout, const float2* emeta, const int* seg_offset,
                      const int* entries, const Item* items, const int* n_items, long long max_items,
+                     const int* item_lo, const int* item_hi, const int* entry_lo,
                      float* dq_acc, float* dk_acc, float* dv_acc, void* pbar, unsigned* status,
                      cudaStream_t st);
 // Proxy gradients (dQp, dKp into fp32 accumulators) of the KL term from pbar, scaled by kl_grad,
@@ -123,8 +125,9 @@ bool launch_proxy_bwd(const Dims& d, bool dense, const void* qp, const void* kp,
                       const float* lpxe, const void* pbar, float kl_grad,
                       const float* kl_grad_dev, const int* seg_offset,
                       const int* entries, const Item* items, const int* n_items,
-                      long long max_items, float* dqp_acc, float* dkp_acc, double* kl_acc,
-                      unsigned* status, cudaStream_t st);
+                      long long max_items, const int* item_lo, const int* item_hi,
+                      const int* entry_lo, float* dqp_acc, float* dkp_acc, double* kl_acc,
+                      unsigned* status, cudaStream_t st);  // one pass, as launch_attn_bwd
 // kl_out[0] = kl_acc[0] / (B S Hp)  (one thread)
 void launch_kl_finalize(const Dims& d, const double* kl_acc, float* kl_out, cudaStream_t st);
 int bwd_item_tokens();   // tokens per fused-backward work item

@@ -129,6 +129,10 @@ MSA_API int msa_forward(const msa_shape_t* shape, const void* q, const void* k, 
  *               kl_grad / (B*S*Hp) * (p_student - p_teacher)  (blog, "KL Divergence Loss").
  * o and lse are the outputs of msa_forward for the same inputs.  kl_grad is the incoming
  * gradient of the (zero) KL placeholder the forward returns (package usage note), usually 1.
+ * Workspace: the teacher rows (one fp16 row of 128 keys per list entry) live for one pass of
+ * consecutive sequence chunks at a time (attn_bwd writes them, the proxy gradients read them);
+ * msa_workspace_size sizes a pass for at most 8 GiB of them, a larger workspace_bytes gives fewer
+ * passes and a smaller one more (down to one chunk per pass; below that MSA_ERR_WORKSPACE).
  * kl_grad_dev: NULL, or a device pointer to one float that is used instead of kl_grad, read by
  * the kernel (an autograd backward can pass the placeholder's incoming gradient tensor without a
  * host synchronisation).
@@ -156,7 +160,8 @@ MSA_API int msa_warmup_forward(const msa_shape_t* shape, const void* q, const vo
 /*
  * Warmup backward (blog, "Warmup kernels"): the proxy normaliser over the full causal prefix,
  * then the fused main + proxy backward with every visible key in the key set.  Same outputs
- * (kl_grad_dev and kl_out included) and KL definition as msa_backward.  top_k is ignored.
+ * (kl_grad_dev and kl_out included), KL definition and workspace passes as msa_backward.  top_k
+ * is ignored.
  */
 MSA_API int msa_warmup_backward(const msa_shape_t* shape, const void* q, const void* k, const void* v,
                         const void* qp, const void* kp, const void* o, const float* lse,
