@@ -219,7 +219,8 @@ def run_reference(args, w, wi):
 
 # ------------------------------------------------------------------------------ our arm
 KERNEL_WORK = {
-    # kernel name -> (bound, function(workload) -> algorithmic FLOPs per launch)
+    # kernel name -> (bound, function(workload) -> algorithmic FLOPs per step; a kernel that runs
+    # in passes over sequence chunks divides them over its launches)
     "proxy_topk": ("tensor", lambda w: 2 * w.D * flops.n_px(w.S) * w.Hp * w.B),
     "attn_fwd": ("tensor", lambda w: 4 * w.D * flops.n_sel(w.S, w.top_k) * w.Hq * w.B),
     # main-attention backward: S, dP (2d each), dV, dK, dQ (2d each) per selected pair and head
@@ -317,14 +318,15 @@ def run_ours(args, w, wi):
     dom = max(prof.items(), key=lambda kv: kv[1][1])
     dname, (dn, dms) = dom
     per_launch_s = dms / dn / 1e3
+    lps = dn / args.steps  # launches per step: the kernel may run in passes over sequence chunks
     bound, work = KERNEL_WORK.get(dname, ("tensor", None))
     roof = None
     if work is not None:
-        achieved = work(w) / per_launch_s / 1e12
+        achieved = work(w) / lps / per_launch_s / 1e12  # a step's work spread over its launches
         peak = peaks["bf16_tflops_sustained"]
         roof = {"kernel": dname, "bound": bound, "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic_record(dname, w),
-                "ms_per_launch": per_launch_s * 1e3,
+                "ms_per_launch": per_launch_s * 1e3, "launches_per_step": lps,
                 "peak_note": f"dense bf16 sustained {peak_src} (kernel timed inside a long step)"}
 
     e2e = None
