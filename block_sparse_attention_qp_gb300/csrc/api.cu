@@ -148,6 +148,10 @@ struct Plan {
   ItemSpec spec0{1, 1}, spec1{1, 1};
   int pass_chunks = 1;  // forward: sequence chunks per pass of the partial outputs; backward:
                         // per pass of the teacher rows
+  // warmup backward: its teacher passes as list boundaries (cuts[i] .. cuts[i+1], chunk-major
+  // list numbers) and the most entries any of them holds
+  std::vector<long long> cuts;
+  long long pass_ent = 0;
 };
 
 struct Carver {
@@ -217,43 +221,71 @@ int default_pass_chunks(const Dims& d) {
   return (int)(fit < 1 ? 1 : fit > d.nchunk ? d.nchunk : fit);
 }
 
-// The backward's teacher rows (fp16, one per list entry) likewise live for one pass of
-// consecutive sequence chunks: attn_bwd writes them and proxy_bwd reads them, pass by pass.  A
-// pass holds at most kBwdTeacherBudget bytes of them (one chunk at least).
+// The backward's teacher rows (fp16, one per list entry) likewise live for one pass at a time:
+// attn_bwd writes them and proxy_bwd reads them, pass by pass.  A pass holds at most
+// kBwdTeacherBudget bytes of them: consecutive sequence chunks of the sparse lists (one chunk at
+// least), a run of consecutive dense lists in the warmup backward (one list at least).
 constexpr size_t kBwdTeacherBudget = 8ull << 30;
 
-// List entries of the chunks [c0, c1): exact for dense lists (every token t >= 128 n of the chunk
-// in the list of block n), the most there can be for sparse ones (top_k per token and proxy head).
-long long pass_entries(const Dims& d, bool dense, int c0, int c1) {
+// List entries of the chunks [c0, c1) of the sparse lists: the most there can be (top_k per token
+// and proxy head).
+long long pass_entries(const Dims& d, int c0, int c1) {
   const long long lo = (long long)c0 * d.chunk;
   const long long hi = (long long)c1 * d.chunk < d.S ? (long long)c1 * d.chunk : d.S;
-  if (!dense) return (long long)d.B * d.Hp * (hi - lo) * d.top_k;
-  long long e = 0;
-  for (int c = c0; c < c1; ++c) {
-    const long long a = (long long)c * d.chunk;
-    const long long z = a + d.chunk < d.S ? a + d.chunk : d.S;
-    for (long long n = 0; n < d.nblk && n * kBlock < z; ++n) e += z - (n * kBlock > a ? n * kBlock : a);
-  }
-  return e * d.B * d.Hp;
+  return (long long)d.B * d.Hp * (hi - lo) * d.top_k;
 }
 
 // The largest entry count of any pass of `pc` chunks.
-long long max_pass_entries(const Dims& d, bool dense, int pc) {
+long long max_pass_entries(const Dims& d, int pc) {
   long long m = 0;
   for (int c0 = 0; c0 < d.nchunk; c0 += pc) {
-    const long long e = pass_entries(d, dense, c0, c0 + pc < d.nchunk ? c0 + pc : d.nchunk);
+    const long long e = pass_entries(d, c0, c0 + pc < d.nchunk ? c0 + pc : d.nchunk);
     if (e > m) m = e;
   }
   return m;
 }
 
-int bwd_pass_chunks(const Dims& d, bool dense) {
+// Entries of dense list `seg` (chunk-major number): the chunk's tokens t >= 128 n.
+long long dense_list_len(const Dims& d, long long seg) {
+  const long long c = seg / d.nseg(), n = seg % d.nblk;
+  const long long a = c * d.chunk, z = a + d.chunk < d.S ? a + d.chunk : d.S;
+  const long long lo = n * kBlock > a ? n * kBlock : a;
+  return z > lo ? z - lo : 0;
+}
+
+// The warmup backward's teacher passes: runs of consecutive dense lists (a pass may end inside a
+// sequence chunk) of about equal size, each holding at most `budget` entries unless one list
+// alone holds more (then that list is a pass).  Returns the boundaries; *most = the largest pass.
+std::vector<long long> dense_cuts(const Dims& d, long long budget, long long* most) {
+  const long long total = dense_entries(d);
+  if (budget < 1) budget = 1;
+  const long long np = (total + budget - 1) / budget;
+  const long long target = np > 1 ? (total + np - 1) / np : total;
+  std::vector<long long> cuts{0};
+  long long acc = 0, mx = 0;
+  for (long long seg = 0; seg < d.nlist(); ++seg) {
+    const long long len = dense_list_len(d, seg);
+    if (acc > 0 && acc + len > target) {
+      cuts.push_back(seg);
+      mx = acc > mx ? acc : mx;
+      acc = 0;
+    }
+    acc += len;
+  }
+  cuts.push_back(d.nlist());
+  *most = acc > mx ? acc : mx;
+  return cuts;
+}
+
+int bwd_pass_chunks(const Dims& d) {
   int pc = d.nchunk;
-  while (pc > 1 && (size_t)max_pass_entries(d, dense, pc) * kBlock * 2 > kBwdTeacherBudget) --pc;
+  while (pc > 1 && (size_t)max_pass_entries(d, pc) * kBlock * 2 > kBwdTeacherBudget) --pc;
   return pc;
 }
 
-Plan make_plan(const Dims& d, int op, int pass_chunks = 0) {
+// pass_chunks: chunks per pass (0: the default); dense_budget: entries per warmup-backward teacher
+// pass (0: the default)
+Plan make_plan(const Dims& d, int op, int pass_chunks = 0, long long dense_budget = 0) {
   Plan p;
   Carver c;
   const long long nseg = d.nlist();
@@ -307,11 +339,18 @@ Plan make_plan(const Dims& d, int op, int pass_chunks = 0) {
     }
     p.lse_px = c.take((size_t)rows_p * sizeof(float));
     p.rowm = c.take((size_t)rows_q * sizeof(float2));  // {LSE log2 e, D} per query row
-    p.pass_chunks = pass_chunks > 0 ? pass_chunks : bwd_pass_chunks(d, dense);
-    const long long ent_pass = max_pass_entries(d, dense, p.pass_chunks);
-    p.pbar = c.take((size_t)ent_pass * kBlock * sizeof(uint16_t));  // teacher rows (fp16) of a pass
-    p.lpxe = c.take((size_t)ent * sizeof(float));            // proxy log-normaliser per entry
-    p.emeta = c.take((size_t)ent * d.Gp() * sizeof(float2));  // rowm per entry and query head
+    if (dense) {
+      p.cuts = dense_cuts(d, dense_budget > 0 ? dense_budget : (long long)(kBwdTeacherBudget / (kBlock * 2)),
+                          &p.pass_ent);
+    } else {
+      p.pass_chunks = pass_chunks > 0 ? pass_chunks : bwd_pass_chunks(d);
+      p.pass_ent = max_pass_entries(d, p.pass_chunks);
+    }
+    p.pbar = c.take((size_t)p.pass_ent * kBlock * sizeof(uint16_t));  // teacher rows (fp16) of a pass
+    if (!dense) {  // dense lists' tokens are consecutive: their row data is read by token
+      p.lpxe = c.take((size_t)ent * sizeof(float));            // proxy log-normaliser per entry
+      p.emeta = c.take((size_t)ent * d.Gp() * sizeof(float2));  // rowm per entry and query head
+    }
     p.dq = c.take((size_t)rows_q * kD * sizeof(float));
     p.dk = c.take((size_t)rows_kv * kD * sizeof(float));
     p.dv = c.take((size_t)rows_kv * kD * sizeof(float));
@@ -327,6 +366,14 @@ Plan make_plan(const Dims& d, int op, int pass_chunks = 0) {
 // sequence chunks as the workspace holds (more or fewer).  The caller checks that it fits.
 Plan plan_for(const Dims& d, int op, size_t bytes) {
   Plan p = make_plan(d, op);
+  if (op == MSA_OP_WARMUP_BACKWARD) {  // teacher passes sized by entries: all the room left
+    const size_t fixed = p.bytes - up((size_t)p.pass_ent * kBlock * 2);
+    if (bytes == p.bytes || bytes <= fixed) return p;  // (too small: the caller reports it)
+    long long budget = (long long)((bytes - fixed) / (kBlock * 2));
+    if (budget > dense_entries(d)) budget = dense_entries(d);
+    const Plan q = make_plan(d, op, 0, budget);
+    return q.bytes <= bytes ? q : p;
+  }
   int pc = p.pass_chunks;
   if (bytes >= p.bytes) {
     while (pc < d.nchunk && make_plan(d, op, pc + 1).bytes <= bytes) ++pc;
@@ -627,7 +674,7 @@ int msa_backward(const msa_shape_t* shape, const void* q, const void* k, const v
   });
   pre.join();
   timed("entry_meta", st, [&] {
-    launch_entry_meta(d, false, at<int>(workspace, p.seg_count), at<int>(workspace, p.seg_offset),
+    launch_entry_meta(d, at<int>(workspace, p.seg_count), at<int>(workspace, p.seg_offset),
                       at<int>(workspace, p.entries), at<float>(workspace, p.lse_px),
                       at<float2>(workspace, p.rowm), at<float>(workspace, p.lpxe),
                       at<float2>(workspace, p.emeta), st);
@@ -645,8 +692,7 @@ int msa_backward(const msa_shape_t* shape, const void* q, const void* k, const v
     const int* hi = c1 < d.nchunk ? io1 + (long long)c1 * d.nseg() : nullptr;
     const int* elo = c0 > 0 ? so + (long long)c0 * d.nseg() : nullptr;
     if (d.R > 1)  // teacher rows accumulated over the proxy head's attention groups
-      cudaMemsetAsync(at<char>(workspace, p.pbar), 0,
-                      (size_t)max_pass_entries(d, false, p.pass_chunks) * kBlock * 2, st);
+      cudaMemsetAsync(at<char>(workspace, p.pbar), 0, (size_t)p.pass_ent * kBlock * 2, st);
     timed("attn_bwd", st, [&] {
       ok = launch_attn_bwd(d, false, q, k, v, dout, at<float2>(workspace, p.emeta),
                            at<int>(workspace, p.seg_offset), at<int>(workspace, p.entries),
@@ -715,7 +761,7 @@ int msa_warmup_backward(const msa_shape_t* shape, const void* q, const void* k, 
   if ((rc = check_ptrs({q, k, v, qp, kp, o, lse, dout, dq, dk, dv, dqp, dkp}))) return rc;
   if (kl_out && (rc = check_kl(kl_out, "kl_out must be 4-byte aligned"))) return rc;
   if (kl_grad_dev && (rc = check_kl(kl_grad_dev, "kl_grad_dev must be 4-byte aligned"))) return rc;
-  const Plan p = plan_for(d, MSA_OP_WARMUP_BACKWARD, workspace_bytes);  // chunks per teacher pass
+  const Plan p = plan_for(d, MSA_OP_WARMUP_BACKWARD, workspace_bytes);  // lists per teacher pass
   if ((rc = check_ws(p, workspace, workspace_bytes))) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaGetLastError();
@@ -745,38 +791,34 @@ int msa_warmup_backward(const msa_shape_t* shape, const void* q, const void* k, 
     return MSA_ERR_CUDA;
   }
   pre.join();
-  timed("entry_meta", st, [&] {
-    launch_entry_meta(d, true, nullptr, at<int>(workspace, p.seg_offset), nullptr,
-                      at<float>(workspace, p.lse_px), at<float2>(workspace, p.rowm),
-                      at<float>(workspace, p.lpxe), at<float2>(workspace, p.emeta), st);
-  });
-  bool ok = true;  // passes as in msa_backward
+  // passes as in msa_backward, over runs of consecutive lists [s0, s1) (the row data D and the
+  // proxy normaliser are read by token, so no per-entry copy is made)
+  bool ok = true;
   double* kl_acc = kl_out ? kl_accumulator(workspace, p, st) : nullptr;
   std::unique_ptr<Branch> post;
   const int* io0 = at<int>(workspace, p.io0);
   const int* so = at<int>(workspace, p.seg_offset);
-  for (int c0 = 0; c0 < d.nchunk && ok; c0 += p.pass_chunks) {
-    const int c1 = c0 + p.pass_chunks < d.nchunk ? c0 + p.pass_chunks : d.nchunk;
-    const int* lo = c0 > 0 ? io0 + (long long)c0 * d.nseg() : nullptr;
-    const int* hi = c1 < d.nchunk ? io0 + (long long)c1 * d.nseg() : nullptr;
-    const int* elo = c0 > 0 ? so + (long long)c0 * d.nseg() : nullptr;
+  for (size_t pi = 0; pi + 1 < p.cuts.size() && ok; ++pi) {
+    const long long s0 = p.cuts[pi], s1 = p.cuts[pi + 1];
+    const int* lo = s0 > 0 ? io0 + s0 : nullptr;
+    const int* hi = s1 < d.nlist() ? io0 + s1 : nullptr;
+    const int* elo = s0 > 0 ? so + s0 : nullptr;
     if (d.R > 1)  // teacher rows accumulated over the proxy head's attention groups
-      cudaMemsetAsync(at<char>(workspace, p.pbar), 0,
-                      (size_t)max_pass_entries(d, true, p.pass_chunks) * kBlock * 2, st);
+      cudaMemsetAsync(at<char>(workspace, p.pbar), 0, (size_t)p.pass_ent * kBlock * 2, st);
     timed("attn_bwd_dense", st, [&] {
-      ok = launch_attn_bwd(d, true, q, k, v, dout, at<float2>(workspace, p.emeta),
+      ok = launch_attn_bwd(d, true, q, k, v, dout, at<float2>(workspace, p.rowm),
                            at<int>(workspace, p.seg_offset), nullptr, at<Item>(workspace, p.items0),
                            at<int>(workspace, p.totals) + 1, p.max0, lo, hi, elo,
                            at<float>(workspace, p.dq), at<float>(workspace, p.dk),
                            at<float>(workspace, p.dv), at<void>(workspace, p.pbar), status, st);
     });
-    if (ok && c1 == d.nchunk) {
+    if (ok && s1 == d.nlist()) {
       post.reset(new Branch(st));
       emit_main_grads(d, p, workspace, dq, dk, dv, post->aux());
     }
     if (ok)
       timed("proxy_bwd_dense", st, [&] {
-        ok = launch_proxy_bwd(d, true, qp, kp, at<float>(workspace, p.lpxe),
+        ok = launch_proxy_bwd(d, true, qp, kp, at<float>(workspace, p.lse_px),
                               at<void>(workspace, p.pbar), kl_grad, kl_grad_dev,
                               at<int>(workspace, p.seg_offset),
                               nullptr, at<Item>(workspace, p.items0), at<int>(workspace, p.totals) + 1,

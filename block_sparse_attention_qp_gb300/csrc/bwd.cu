@@ -102,7 +102,9 @@ constexpr int kIR = 4;                 // work-item ring: item numbers handed ou
 struct MainArgs {
   Dims d;
   const bf16 *q, *dout;
-  const float2* emeta;  // per list entry and head: {LSE log2 e, D}
+  const float2* emeta;  // sparse: per list entry and head, {LSE log2 e, D}
+  const float2* rowm;   // dense: the same per query row [B, S, Hq] (a dense item's tokens are
+                        // consecutive, so they need no per-entry copy)
   const int* seg_offset;
   const int* entries;
   const Item* items;
@@ -130,7 +132,8 @@ struct MainShared {
 struct ProxyArgs {
   Dims d;
   const bf16* qp;
-  const float* lpxe;   // per list entry: LSE_px x log2 e
+  const float* lpxe;    // sparse: per list entry, LSE_px x log2 e
+  const float* lse_px;  // dense: LSE_px per proxy row [B, Hp, S]
   const __half* pbar;  // per list entry: teacher row [128 keys] (fp16)
   float cz;          // kl_grad / (B * S * Hp), or 1 / (B * S * Hp) when czp is set
   const float* czp;  // NULL, or the device-resident kl_grad that multiplies cz
@@ -438,13 +441,15 @@ __global__ void __launch_bounds__(352, 1)
         for (int x = 0; x < TT; ++x)
           tv[x] = x < valid ? (kDense ? (int)(tb + pos0 + x) : (__ldg(A.entries + tb + pos0 + x) >> 8)) : -1;
       };
-      // row data of row r0 + (lane & 15) of tile tl_ (lanes 0-15), indexed by the list entry, so
-      // it needs no token first
+      // row data of row r0 + (lane & 15) of tile tl_ (lanes 0-15), indexed by the list entry
+      // (dense: by the token, tb + x), so it needs no token first
       auto load_meta = [&](int tl_) -> float2 {
         const int x = tl_ * TT + (r0 + ch) / G;
+        const int h = item.sub * G + (r0 + ch) % G;  // query head within the proxy head's Gp
         float2 m = make_float2(0.f, 0.f);
         if (hi == 0 && x < item.count)
-          m = __ldg(A.emeta + (size_t)(eb + x) * gp + item.sub * G + (r0 + ch) % G);
+          m = kDense ? __ldg(A.rowm + ((size_t)b * d.S + tb + x) * d.Hq + (size_t)(bg % d.Hp) * gp + h)
+                     : __ldg(A.emeta + (size_t)(eb + x) * gp + h);
         return m;
       };
       const int ntiles = (item.count + TT - 1) / TT;
@@ -945,11 +950,14 @@ __global__ void __launch_bounds__(kWideThreads, 1)
         if (lane >= TT || x >= item.count) return -1;
         return kDense ? (int)(tb + x) : (__ldg(A.entries + tb + x) >> 8);
       };
-      // row data of row r0 + lane of tile tl_, indexed by the list entry
+      // row data of row r0 + lane of tile tl_, indexed by the list entry (dense: by the token)
       auto load_meta = [&](int tl_) -> float2 {
         const int x = tl_ * TT + (r0 + lane) / G;
+        const int h = item.sub * G + (r0 + lane) % G;  // query head within the proxy head's Gp
         float2 m = make_float2(0.f, 0.f);
-        if (x < item.count) m = __ldg(A.emeta + (size_t)(eb + x) * gp + item.sub * G + (r0 + lane) % G);
+        if (x < item.count)
+          m = kDense ? __ldg(A.rowm + ((size_t)b * d.S + tb + x) * d.Hq + (size_t)(bg % d.Hp) * gp + h)
+                     : __ldg(A.emeta + (size_t)(eb + x) * gp + h);
         return m;
       };
       const int ntiles = (item.count + TT - 1) / TT;
@@ -1377,9 +1385,14 @@ __global__ void __launch_bounds__(384, 1)
         const int pos = grp * kPG + x;
         int t = -1;
         lp = 0.f;
-        if (pos < item.count) {  // two independent loads, both indexed by the entry
-          t = kDense ? (int)(item_base<true>(d, nullptr, item) + pos) : (__ldg(A.entries + item.base + pos) >> 8);
-          lp = __ldg(A.lpxe + item.base + pos);
+        if (pos < item.count) {
+          if (kDense) {  // consecutive tokens: the row's normaliser by token
+            t = (int)(item_base<true>(d, nullptr, item) + pos);
+            lp = __ldg(A.lse_px + (size_t)bg * d.S + t) * kLog2e;
+          } else {  // two independent loads, both indexed by the entry
+            t = __ldg(A.entries + item.base + pos) >> 8;
+            lp = __ldg(A.lpxe + item.base + pos);
+          }
         }
         (void)b;
         (void)g;
@@ -1683,7 +1696,7 @@ void launch_bwd_rowdot(const Dims& d, const void* o, const void* dout, const flo
 }
 
 bool launch_attn_bwd(const Dims& d, bool dense, const void* q, const void* k, const void* v,
-                     const void* dout, const float2* emeta, const int* seg_offset,
+                     const void* dout, const float2* rowdata, const int* seg_offset,
                      const int* entries, const Item* items, const int* n_items, long long max_items,
                      const int* item_lo, const int* item_hi, const int* entry_lo,
                      float* dq_acc, float* dk_acc, float* dv_acc, void* pbar, unsigned* status,
@@ -1698,7 +1711,8 @@ bool launch_attn_bwd(const Dims& d, bool dense, const void* q, const void* k, co
   a.d = d;
   a.q = (const bf16*)q;
   a.dout = (const bf16*)dout;
-  a.emeta = emeta;
+  a.emeta = dense ? nullptr : rowdata;
+  a.rowm = dense ? rowdata : nullptr;
   a.seg_offset = seg_offset;
   a.entries = entries;
   a.items = items;
@@ -1735,7 +1749,7 @@ bool launch_attn_bwd(const Dims& d, bool dense, const void* q, const void* k, co
 }
 
 bool launch_proxy_bwd(const Dims& d, bool dense, const void* qp, const void* kp,
-                      const float* lpxe, const void* pbar, float kl_grad,
+                      const float* lpx, const void* pbar, float kl_grad,
                       const float* kl_grad_dev, const int* seg_offset,
                       const int* entries, const Item* items, const int* n_items,
                       long long max_items, const int* item_lo, const int* item_hi,
@@ -1760,7 +1774,8 @@ bool launch_proxy_bwd(const Dims& d, bool dense, const void* qp, const void* kp,
   ProxyArgs a;
   a.d = d;
   a.qp = (const bf16*)qp;
-  a.lpxe = lpxe;
+  a.lpxe = dense ? nullptr : lpx;
+  a.lse_px = dense ? lpx : nullptr;
   a.pbar = static_cast<const __half*>(pbar);
   const double inv_n = 1.0 / ((double)d.B * d.S * d.Hp);
   a.cz = (float)(kl_grad_dev ? inv_n : (double)kl_grad * inv_n);

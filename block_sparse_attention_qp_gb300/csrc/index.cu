@@ -356,29 +356,28 @@ __global__ void items_kernel(Dims d, int dense, const int* __restrict__ seg_coun
 // instead of through its token: lpxe[e] = LSE_px(b, p, t(e)) * log2 e and, for the Gp = Hq / Hp
 // query heads of proxy head p, emeta[e Gp + h] = {LSE(b, p Gp + h, t(e)) log2 e,
 // D(b, t(e), p Gp + h)}.
-__global__ void entry_meta_kernel(Dims d, int dense, const int* __restrict__ seg_count,
+__global__ void entry_meta_kernel(Dims d, const int* __restrict__ seg_count,
                                   const int* __restrict__ seg_offset, const int* __restrict__ entries,
                                   const float* __restrict__ lse_px, const float2* __restrict__ rowm,
                                   float* __restrict__ lpxe, float2* __restrict__ emeta) {
   // one block per list: the lists' lengths vary by orders of magnitude (a block every token
   // selects against a rarely chosen one), which the block scheduler balances
   const long long seg = blockIdx.x;
-  const int len = (int)list_len(d, dense, seg_count, seg);
+  const int len = (int)list_len(d, false, seg_count, seg);
   if (len == 0) return;
   const long long base = seg_offset[seg];
   const long long bg = (seg % d.nseg()) / d.nblk;  // b * Hp + g
   const long long b = bg / d.Hp, g = bg % d.Hp;
   const float* row = lse_px + bg * d.S;
-  const long long t0 = dense ? dense_first(d, seg) : 0;
   for (int k = threadIdx.x; k < len; k += blockDim.x) {
-    const long long t = dense ? t0 + k : (long long)(entries[base + k] >> 8);
+    const long long t = entries[base + k] >> 8;
     lpxe[base + k] = row[t] * kLog2e;
   }
   const int gp = d.Gp();
   const int n = len * gp;  // < 2^31: 32-bit index arithmetic
   for (int x = threadIdx.x; x < n; x += blockDim.x) {
     const int k = x / gp, h = x - k * gp;
-    const long long t = dense ? t0 + k : (long long)(entries[base + k] >> 8);
+    const long long t = entries[base + k] >> 8;
     emeta[base * gp + x] = rowm[((b * d.S + t) * d.Hq + g * gp + h)];
   }
 }
@@ -459,11 +458,11 @@ void launch_items(const Dims& d, bool dense, const int* seg_count, const int* se
                                                        spec, item_offset, items, max_items, status);
 }
 
-void launch_entry_meta(const Dims& d, bool dense, const int* seg_count, const int* seg_offset,
+void launch_entry_meta(const Dims& d, const int* seg_count, const int* seg_offset,
                        const int* entries, const float* lse_px, const float2* rowm, float* lpxe,
                        float2* emeta, cudaStream_t st) {
-  entry_meta_kernel<<<(unsigned)d.nlist(), 256, 0, st>>>(d, dense ? 1 : 0, seg_count, seg_offset,
-                                                          entries, lse_px, rowm, lpxe, emeta);
+  entry_meta_kernel<<<(unsigned)d.nlist(), 256, 0, st>>>(d, seg_count, seg_offset, entries, lse_px,
+                                                          rowm, lpxe, emeta);
 }
 
 void launch_convert(const float* src, void* dst, long long n, cudaStream_t st) {

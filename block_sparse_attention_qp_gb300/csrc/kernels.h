@@ -55,9 +55,10 @@ void launch_items(const Dims& d, bool dense, const int* seg_count, const int* se
                   const ItemSpec& spec, const int* item_offset, Item* items, long long max_items,
                   unsigned* status, cudaStream_t st);
 
-// Row data of every list entry e (dense: the lists' implicit tokens), in entry order:
-// lpxe[e] = LSE_px of e's token x log2(e); emeta[e G + h] = rowm of e's token and head g G + h.
-void launch_entry_meta(const Dims& d, bool dense, const int* seg_count, const int* seg_offset,
+// Row data of every entry e of the sparse lists, in entry order: lpxe[e] = LSE_px of e's token
+// x log2(e); emeta[e Gp + h] = rowm of e's token and head g Gp + h.  (Dense lists need no copy:
+// their tokens are consecutive, and the dense kernels read rowm and LSE_px by token.)
+void launch_entry_meta(const Dims& d, const int* seg_count, const int* seg_offset,
                        const int* entries, const float* lse_px, const float2* rowm, float* lpxe,
                        float2* emeta, cudaStream_t st);
 
@@ -109,10 +110,11 @@ void launch_proxy_lse_combine(const Dims& d, const float* lpx_part, float* lse_p
 
 // Main-attention backward (dQ, dK, dV into fp32 accumulators) and the teacher pbar
 // ([list entry - *entry_lo][128 keys] fp16) of one pass: the items [*item_lo, *item_hi) (NULL:
-// 0 / all; entry_lo NULL: 0).  Returns false for an unsupported group size or if the TMA tensor
-// maps cannot be created.
+// 0 / all; entry_lo NULL: 0).  rowdata: {LSE log2 e, D} per list entry and head (emeta, sparse)
+// or per query row (rowm [B, S, Hq], dense).  Returns false for an unsupported group size or if
+// the TMA tensor maps cannot be created.
 bool launch_attn_bwd(const Dims& d, bool dense, const void* q, const void* k, const void* v,
-                     const void* dout, const float2* emeta, const int* seg_offset,
+                     const void* dout, const float2* rowdata, const int* seg_offset,
                      const int* entries, const Item* items, const int* n_items, long long max_items,
                      const int* item_lo, const int* item_hi, const int* entry_lo,
                      float* dq_acc, float* dk_acc, float* dv_acc, void* pbar, unsigned* status,
@@ -121,8 +123,10 @@ bool launch_attn_bwd(const Dims& d, bool dense, const void* q, const void* k, co
 // or by *kl_grad_dev (read on the device) when that is not NULL.  kl_acc: NULL, or
 // a zeroed double that receives sum over the visited (token, key) pairs of
 // pbar (ln pbar - ln p_student), i.e. B S Hp times the KL value.
+// lpx: LSE_px x log2 e per list entry (lpxe, sparse) or LSE_px per proxy row (lse_px
+// [B, Hp, S], dense).
 bool launch_proxy_bwd(const Dims& d, bool dense, const void* qp, const void* kp,
-                      const float* lpxe, const void* pbar, float kl_grad,
+                      const float* lpx, const void* pbar, float kl_grad,
                       const float* kl_grad_dev, const int* seg_offset,
                       const int* entries, const Item* items, const int* n_items,
                       long long max_items, const int* item_lo, const int* item_hi,

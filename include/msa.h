@@ -160,8 +160,13 @@ MSA_API int msa_warmup_forward(const msa_shape_t* shape, const void* q, const vo
 /*
  * Warmup backward (blog, "Warmup kernels"): the proxy normaliser over the full causal prefix,
  * then the fused main + proxy backward with every visible key in the key set.  Same outputs
- * (kl_grad_dev and kl_out included), KL definition and workspace passes as msa_backward.  top_k
- * is ignored.
+ * (kl_grad_dev and kl_out included) and KL definition as msa_backward.  top_k is ignored.
+ * Workspace: the teacher rows live for one pass of consecutive dense lists at a time (a pass may
+ * end inside a sequence chunk), so the workspace does not grow with the square of S beyond them:
+ * msa_workspace_size sizes a pass for at most 8 GiB of teacher rows, a larger workspace_bytes
+ * gives fewer passes and a smaller one more (down to one list -- at most one chunk of tokens --
+ * per pass; below that MSA_ERR_WORKSPACE).  The results do not depend on the passes beyond the
+ * order of the fp32 gradient reductions.
  */
 MSA_API int msa_warmup_backward(const msa_shape_t* shape, const void* q, const void* k, const void* v,
                         const void* qp, const void* kp, const void* o, const float* lse,

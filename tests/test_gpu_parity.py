@@ -402,7 +402,7 @@ def test_forward_in_passes_equals_one_pass():
 def test_backward_in_passes_equals_one_pass():
     """A smaller workspace makes the backward keep the teacher rows for fewer sequence chunks at a
     time (attn_bwd then proxy_bwd, pass by pass): 3 + 1 and 4 x 1 passes of chunks of 8192 tokens
-    here, and 1 + 1 chunks of 16384 tokens in the dense warmup backward.  The gradients and the KL
+    here, and runs of consecutive lists in the dense warmup backward.  The gradients and the KL
     value equal the one-pass results up to the order of the fp32 reductions."""
     w = Workload("bpasses", B=2, S=32768, Hq=16, Hkv=2, Hp=2, top_k=8)
     g = to_dev(make_inputs(w, 43))
@@ -426,18 +426,29 @@ def test_backward_in_passes_equals_one_pass():
         assert abs(float(got[5]) - float(ref[5])) <= 1e-6 * abs(float(ref[5]))
     with pytest.raises(msa.MSAError, match="workspace"):
         run(full - 4 * teacher_chunk)
-    # dense warmup backward, two chunks of 16384 tokens
+    # dense warmup backward (two chunks of 16384 tokens): its passes are runs of consecutive
+    # lists, so with less room they end inside a chunk -- 2, 3 and about 10 passes here
     wd = Workload("wpasses", B=1, S=32768, Hq=8, Hkv=2, Hp=2, top_k=0)
     gd = to_dev(make_inputs(wd, 44))
     od, ld = msa.msa_warmup_forward(gd["q"], gd["k"], gd["v"], wd.scale)
     shd = msa.make_shape(gd["q"], gd["k"], gd["qp"], 0, wd.scale)
     fulld = msa.msa_workspace_size(shd, msa.OP_WARMUP_BACKWARD)
-    outs = []
-    for nbytes in (fulld, fulld - 1):
+    nblk = wd.S // 128
+    teacher = wd.B * wd.Hp * (wd.S * nblk - 128 * nblk * (nblk - 1) // 2) * 128 * 2  # all rows
+
+    def run_dense(nbytes):
         ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
-        outs.append(msa.msa_warmup_backward(gd["q"], gd["k"], gd["v"], gd["qp"], gd["kp"], od, ld,
-                                            gd["dout"], wd.scale, ws=ws, return_kl=True))
+        out = msa.msa_warmup_backward(gd["q"], gd["k"], gd["v"], gd["qp"], gd["kp"], od, ld,
+                                      gd["dout"], wd.scale, ws=ws, return_kl=True)
         assert msa.msa_device_status(ws) == 0
-    for name, a, b in zip(("dq", "dk", "dv", "dqp", "dkp"), outs[1][:5], outs[0][:5]):
-        close("warmup " + name, a, b.float(), rel=1e-3, atol=1e-4, ulps=1.0)
-    assert abs(float(outs[1][5]) - float(outs[0][5])) <= 1e-6 * abs(float(outs[0][5]))
+        return out
+
+    refd = run_dense(fulld)
+    for nbytes in (fulld - 1, fulld - teacher * 2 // 3, fulld - teacher * 9 // 10):
+        got = run_dense(nbytes)
+        for name, a, b in zip(("dq", "dk", "dv", "dqp", "dkp"), got[:5], refd[:5]):
+            close("warmup " + name, a, b.float(), rel=1e-3, atol=1e-4, ulps=1.0)
+        assert abs(float(got[5]) - float(refd[5])) <= 1e-6 * abs(float(refd[5]))
+    for nbytes in (fulld - teacher, fulld - teacher + 10000 * 256):  # no room / less than a list
+        with pytest.raises(msa.MSAError, match="workspace"):
+            run_dense(nbytes)
