@@ -55,6 +55,32 @@ def test_workspace_size_is_host_only(lib):
     assert lib.msa_workspace_size(ctypes.byref(binding.Shape(1, 256, 8, 2, 2, 128, 65, 0.1)), 0) == 0
 
 
+def test_workspace_is_bounded_by_passes(lib):
+    """The forward's partial outputs and the backwards' teacher rows are held one pass at a time
+    (8 GiB of each by default), so beyond them the workspace grows linearly with S: in the warmup
+    backward as well, whose lists grow with S^2 (B Hp S^2 / 256 entries)."""
+    gib = 2 ** 30
+    budget = 8 * gib
+
+    def linear_bwd(B, S, Hq, Hkv, Hp):  # fp32 accumulators and per-row data, bytes
+        return B * S * (Hq * 512 + 2 * Hkv * 512 + Hp * 512 + 512 + Hq * 8 + Hp * 8)
+
+    for S in (32768, 65536, 131072):
+        s = binding.Shape(1, S, 32, 8, 8, 128, 0, 128 ** -0.5)
+        ws = binding.msa_workspace_size(s, binding.OP_WARMUP_BACKWARD)
+        entries = 8 * S * S // 256
+        assert entries * 256 > ws or S == 32768  # all the teacher rows would not fit
+        # teacher pass + linear part + work items and list offsets (a few bytes per 64 entries)
+        assert ws <= budget + linear_bwd(1, S, 32, 8, 8) + entries // 8 + (64 << 20), (S, ws)
+    for S in (1 << 20, 1 << 21):
+        s = binding.Shape(1, S, 16, 4, 4, 128, 16, 128 ** -0.5)
+        fwd = binding.msa_workspace_size(s, binding.OP_FORWARD)
+        assert fwd <= budget + S * 4 * 16 * 12 + (256 << 20), (S, fwd)  # partials + lists
+        bwd = binding.msa_workspace_size(s, binding.OP_BACKWARD)
+        per_entry = 4 + 4 + 4 * 8 + 4  # entry, proxy normaliser, row data copy, partial normaliser
+        assert bwd <= budget + linear_bwd(1, S, 16, 4, 4) + S * 4 * 16 * per_entry + (256 << 20), (S, bwd)
+
+
 def test_argument_errors_before_any_launch(lib):
     s = binding.Shape(1, 256, 8, 2, 2, 128, 2, 0.1)
     P = ctypes.c_void_p
