@@ -102,17 +102,27 @@ def test_sparse_proxy_kv_head_mappings(name, B, S, Hq, Hkv, Hp, k):
 
 @pytest.mark.parametrize("B,S,Hq,Hkv,Hp", [(1, 768, 16, 4, 2), (1, 640, 16, 2, 4)])
 def test_warmup_proxy_kv_head_mappings(B, S, Hq, Hkv, Hp):
+    """Dense warmup backward with a proxy head over two attention groups (its teacher rows summed
+    from both) and with two proxy heads over one, in one pass and in about three teacher passes
+    over runs of lists (ending inside the 512-token chunks), each against the oracle."""
     w = Workload("wmap", B=B, S=S, Hq=Hq, Hkv=Hkv, Hp=Hp, top_k=0)
     x = make_inputs(w, 800 + S + Hp)
     g = to_dev(x)
     o, lse = msa.msa_warmup_forward(g["q"], g["k"], g["v"], w.scale)
-    *grads, kl = msa.msa_warmup_backward(g["q"], g["k"], g["v"], g["qp"], g["kp"], o, lse,
-                                         g["dout"], w.scale, return_kl=True)
-    torch.cuda.synchronize()
     ref = oracle.backward(x["q"], x["k"], x["v"], x["qp"], x["kp"], x["dout"], None, 1, w.scale)
-    for name_, gt in zip(("dq", "dk", "dv", "dqp", "dkp"), grads):
-        close(name_, gt, ref[name_])
-    check_kl(kl, ref["kl"])
+    shape = msa.make_shape(g["q"], g["k"], g["qp"], 0, w.scale)
+    full = msa.msa_workspace_size(shape, msa.OP_WARMUP_BACKWARD)
+    nblk = S // 128
+    teacher = B * Hp * (S * nblk - 128 * nblk * (nblk - 1) // 2) * 128 * 2  # all teacher rows
+    for nbytes in (full, full - teacher * 2 // 3):
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+        *grads, kl = msa.msa_warmup_backward(g["q"], g["k"], g["v"], g["qp"], g["kp"], o, lse,
+                                             g["dout"], w.scale, ws=ws, return_kl=True)
+        torch.cuda.synchronize()
+        assert msa.msa_device_status(ws) == 0
+        for name_, gt in zip(("dq", "dk", "dv", "dqp", "dkp"), grads):
+            close(name_, gt, ref[name_])
+        check_kl(kl, ref["kl"])
 
 
 def test_sparse_kl_grad_scales_proxy_only():
