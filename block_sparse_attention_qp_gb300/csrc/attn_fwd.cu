@@ -14,10 +14,13 @@
 //
 // Roles (448 threads): warp 0 TMA loads of K/V (a three-slot ring), the block's work-item numbers
 // and tensor-memory ownership, warp 1 the MMA issuer, warps 2, 3, 12, 13 gather the tile's Q rows
-// (cp.async, three buffers), warps 4-7 and 8-11 two softmax + epilogue groups that take alternate
-// tiles.  (TMA issues about one request per 70 cycles per SM, so 1 KB row boxes cannot feed a
-// 128-row tile in time; four cp.async warps can.)  Tensor memory (512 columns): S0, S1 (S, then P
-// in place), O0, O1.
+// (three buffers), warps 4-7 and 8-11 two softmax + epilogue groups that take alternate tiles.
+// Tensor memory (512 columns): S0, S1 (S, then P in place), O0, O1.
+// The gather: TMA issues about one request per 70 cycles per SM whatever its size, so with 8 heads
+// per group each token's rows come as one 2 KB box (its 8 heads x both 64-column panels, through a
+// 4D view of Q whose panel stride is below its head stride): 16 requests per tile.  Other group
+// sizes would need 32 or more boxes per tile, and there four cp.async warps (2,048 16-byte copies
+// per tile) keep up better.
 // The MMA issuer runs S of tile i before O of tile i-1, so the tensor pipe works on one tile while
 // the softmax warps work on the next.  Every wait is bounded (see sm100::mbar_wait).
 //
@@ -79,6 +82,23 @@ __device__ __forceinline__ float ex2f(float x) {
 }
 __device__ __forceinline__ uint32_t par(long long k) { return (uint32_t)(k & 1); }
 
+// Q tile loaded one token (8 query heads) per TMA box: per token 2 KB = [panel][8 rows][128 B],
+// both panels of a token's rows together, so consecutive 8-row groups of a panel are 2 KB apart.
+constexpr int kTokBox = 2 * 8 * 128;
+__device__ __forceinline__ uint64_t desc_kmajor_tok(uint32_t tile_saddr, int ks) {
+  const uint32_t a = tile_saddr + (uint32_t)((ks >> 2) * (kTokBox / 2) + (ks & 3) * 32);
+  return sm100::make_desc(a, 16, kTokBox);
+}
+__device__ __forceinline__ void tma_load_4d(void* dst, const void* tmap, int c0, int c1, int c2,
+                                            int c3, uint64_t* mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3, %4, %5}], [%6];\n" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "r"(static_cast<uint32_t>(__cvta_generic_to_shared(mbar)))
+      : "memory");
+}
+
 // The K/V ring: loads alternate K, V, K, V, ... (load L = 2 * item + {0: K, 1: V}) over kRing
 // slots, so the next item's V can land as soon as the current item's K is no longer needed.
 struct RingPos {
@@ -95,9 +115,10 @@ __device__ __forceinline__ RingPos ring_pos(long long load) {
 template <int G, bool kProxy>
 __global__ void __launch_bounds__(448, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                    FwdArgs A) {
+                    const __grid_constant__ CUtensorMap tm_q, FwdArgs A) {
   using namespace sm100;
   constexpr int TT = kFwdRows / G;  // tokens per tile
+  constexpr bool kTmaQ = G == 8 && !kProxy;  // Q rows by one TMA box per token (else cp.async)
   constexpr int kLoads = kProxy ? 1 : 2;  // ring loads per item: K (or Kp) and V
   const Dims& d = A.d;
 
@@ -275,14 +296,16 @@ __global__ void __launch_bounds__(448, 1)
         if (i >= 2 && !mbar_wait_warp(kProxy ? &sh->p_full[b] : &sh->o_full[b], par((i - 2) >> 1),
                                       A.status)) { ok = false; break; }
         // the Q rows were written by other threads' cp.async (generic proxy) and only tracked by
-        // the barrier: order them before the tensor core's (async proxy) reads
+        // the barrier: order them before the tensor core's (async proxy) reads (TMA-written rows
+        // need no fence; it is harmless there)
         fence_async_smem();
         fence_after_sync();
         if (lane == 0) {
           const uint32_t aQb = aQ + qb * kFwdTile;
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            mma_ss(S0 + 128 * b, desc_kmajor(aQb, 128, ks), desc_kmajor(aK, 128, ks), id_s, ks > 0);
+            mma_ss(S0 + 128 * b, kTmaQ ? desc_kmajor_tok(aQb, ks) : desc_kmajor(aQb, 128, ks),
+                   desc_kmajor(aK, 128, ks), id_s, ks > 0);
           mma_commit(&sh->s_full[b]);
           mma_commit(&sh->q_empty[qb]);
           if (tl == ntiles - 1) mma_commit(&sh->kv_empty[kp.slot]);
@@ -337,16 +360,29 @@ __global__ void __launch_bounds__(448, 1)
         const int bg = (int)((cur.seg % d.nseg()) / d.nblk);
         const int b = bg / d.Hp, a = (bg % d.Hp) * d.R + cur.sub;  // attention group
         uint8_t* dQb = sQ + qb * kFwdTile;
+        if constexpr (kTmaQ) {
+          // lane x < XT: token x0 + x, one box of its 8 heads' rows (a missing token loads token
+          // 0's rows: finite values in a row no result reads)
+          if (lane < XT) {
+            const int t = sh->tok[qb][x0 + lane];
+            mbar_expect_tx(&sh->q_full[qb], kTokBox);  // also this lane's first arrival
+            tma_load_4d(dQb + (x0 + lane) * kTokBox, &tm_q, 0, a * G, 0, b * d.S + (t < 0 ? 0 : t),
+                        &sh->q_full[qb]);
+          } else {
+            mbar_arrive(&sh->q_full[qb]);
+          }
+        } else {
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const int c = lane + 32 * k;                // 16-byte chunk of this warp's 32 rows
-          const int r = 32 * gw + (c >> 4), ch = c & 15;
-          const int t = sh->tok[qb][r / G];
-          const uint32_t off = (ch >> 3) * (kFwdRows * 128) + sm100::sw128_chunk(r, ch & 7);
-          const size_t grow = (((size_t)b * d.S + (t < 0 ? 0 : t)) * d.Hq + a * G + r % G) * kD + ch * 8;
-          cp_async16_hint(dQb + off, A.q + grow, t >= 0, pol_q);
+          for (int k = 0; k < 16; ++k) {
+            const int c = lane + 32 * k;                // 16-byte chunk of this warp's 32 rows
+            const int r = 32 * gw + (c >> 4), ch = c & 15;
+            const int t = sh->tok[qb][r / G];
+            const uint32_t off = (ch >> 3) * (kFwdRows * 128) + sm100::sw128_chunk(r, ch & 7);
+            const size_t grow = (((size_t)b * d.S + (t < 0 ? 0 : t)) * d.Hq + a * G + r % G) * kD + ch * 8;
+            cp_async16_hint(dQb + off, A.q + grow, t >= 0, pol_q);
+          }
+          cp_async_arrive(&sh->q_full[qb]);
         }
-        cp_async_arrive(&sh->q_full[qb]);
         mbar_arrive(&sh->q_full[qb]);  // publishes tok / slot
         ++i;
         // advance: next tile of this item, or the first tile of the next item
@@ -363,6 +399,10 @@ __global__ void __launch_bounds__(448, 1)
         }
       }
       cp_async_wait_all();  // nothing may land after the block exits
+      if constexpr (kTmaQ) {  // nor any TMA box (the waits are bounded)
+        for (long long x = (i >= kQBuf ? i - kQBuf : 0); x < i; ++x)
+          mbar_wait_warp(&sh->q_full[x % kQBuf], par(x / kQBuf), A.status);
+      }
     }
   } else {
     // ---------------------------------------------------------------- softmax + epilogue
@@ -552,15 +592,29 @@ __global__ void __launch_bounds__(448, 1)
 }
 
 template <int G, bool kProxy>
-static void attn_fwd_g(const CUtensorMap& mk, const CUtensorMap& mv, const FwdArgs& a,
-                       cudaStream_t st) {
+static void attn_fwd_g(const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mq,
+                       const FwdArgs& a, cudaStream_t st) {
   const size_t smem = sizeof(FwdShared) + 1024 + (kRing + kQBuf) * kFwdTile + 8 * kStageWarp;
   cudaFuncSetAttribute(attn_fwd_kernel<G, kProxy>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                        (int)smem);
-  attn_fwd_kernel<G, kProxy><<<num_sms(), 448, smem, st>>>(mk, mv, a);
+  attn_fwd_kernel<G, kProxy><<<num_sms(), 448, smem, st>>>(mk, mv, mq, a);
 }
 
 int fwd_item_tiles() { return kFwdItemTiles; }
+
+// Rank-4 bf16 tensor map, 128-byte swizzle (the Q view of the 8-heads-per-group forward).
+static bool make_tmap_q4(CUtensorMap* m, const void* base, const uint64_t* dims,
+                         const uint64_t* strides_bytes, const uint32_t* box) {
+  auto enc = tmap_encoder();
+  if (!enc) return false;
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base),
+                         (const cuuint64_t*)dims, (const cuuint64_t*)strides_bytes,
+                         (const cuuint32_t*)box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
 
 bool launch_attn_fwd(const Dims& d, const void* q, const void* k, const void* v,
                      const int* seg_offset, const int* entries, const Item* items,
@@ -589,13 +643,22 @@ bool launch_attn_fwd(const Dims& d, const void* q, const void* k, const void* v,
   a.item_hi = item_hi;
   a.pass_t0 = pass_t0;
   a.pass_tokens = pass_tokens;
+  // 8 heads per group: Q as a 4D tensor (64 columns, head, 64-column panel, token) so that one box
+  // {64, 8, 2, 1} brings a token's group rows, both panels, as 2 KB of SW128 rows
+  CUtensorMap mq = mk;  // (unused by the other group sizes)
+  if (d.G == 8) {
+    const uint64_t qd[4] = {64, (uint64_t)d.Hq, 2, (uint64_t)d.B * d.S};
+    const uint64_t qs[3] = {128 * 2, 64 * 2, (uint64_t)d.Hq * 128 * 2};
+    const uint32_t qb[4] = {64, 8, 2, 1};
+    if (!make_tmap_q4(&mq, q, qd, qs, qb)) return false;
+  }
   cudaMemsetAsync(a.sched, 0, sizeof(int), st);
   switch (d.G) {
-    case 1: attn_fwd_g<1, false>(mk, mv, a, st); break;
-    case 2: attn_fwd_g<2, false>(mk, mv, a, st); break;
-    case 4: attn_fwd_g<4, false>(mk, mv, a, st); break;
-    case 8: attn_fwd_g<8, false>(mk, mv, a, st); break;
-    case 16: attn_fwd_g<16, false>(mk, mv, a, st); break;
+    case 1: attn_fwd_g<1, false>(mk, mv, mq, a, st); break;
+    case 2: attn_fwd_g<2, false>(mk, mv, mq, a, st); break;
+    case 4: attn_fwd_g<4, false>(mk, mv, mq, a, st); break;
+    case 8: attn_fwd_g<8, false>(mk, mv, mq, a, st); break;
+    case 16: attn_fwd_g<16, false>(mk, mv, mq, a, st); break;
     default: return false;
   }
   return true;
@@ -630,7 +693,7 @@ bool launch_proxy_lse_sparse(const Dims& d, const void* qp, const void* kp, cons
   a.pass_t0 = 0;
   a.pass_tokens = d.S;
   cudaMemsetAsync(a.sched, 0, sizeof(int), st);
-  attn_fwd_g<1, true>(mk, mk, a, st);
+  attn_fwd_g<1, true>(mk, mk, mk, a, st);
   return true;
 }
 
